@@ -1,0 +1,305 @@
+/*
+ * qgemm_oracle.c -- the CPU oracle for blockwise low-bit dequantize + GEMM
+ * and for the fused QMoE decode.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * statement of what the GPU library computes.  Only the test-suite, the
+ * package smoke check and the benchmark's CPU-baseline leg may load it.  It
+ * shares no source, header, table or helper with the CUDA library, and the
+ * library never calls it.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [P1] hip-ep pull request #1318, "2-bit MatMulNBits for phi4-14B on
+ *        gfx1151" -- sections Summary, Why, What (Commit 1, kernels),
+ *        Performance (Model), Notes for reviewers (Follow-ups).
+ *   [P2] hip-ep pull request #1328, "fused QMoE decode picks its tiling
+ *        before computing" -- sections Summary, Why, What, Test plan,
+ *        Notes for reviewers.
+ *   [P3] bitsandbytes pull request #1979, "[ROCm] Fused 4-bit SIMT GEMM" --
+ *        sections Summary, Technical details, Testing plan.
+ *
+ * Readings of points the pages leave open (each one is also listed in the
+ * design notes):
+ *   - codes are packed along K, LSB-first: element k of a row sits in byte
+ *     (k*bits)/8 at bit offset (k*bits)%8; a row occupies K*bits/8 bytes;
+ *   - scales / zero points / absmax are row-major [N][K/bs];
+ *   - an absent zero-point tensor means the midpoint 2^(bits-1);
+ *   - dequantization is two fp32 round-to-nearest operations,
+ *     w = (q - zp) * s, with no fused multiply-add;
+ *   - SwiGLU is silu(gate) * up with gate the first half of fc1's output
+ *     (or the even elements when the interleaved layout is asked for);
+ *   - every matmul is accumulated in fp64, ascending k, and returned
+ *     unrounded, so that a GPU result can be compared against the exact
+ *     product of the dequantized operands.
+ *
+ * Parity pins: every function here is pinned by CPU tests against values
+ * written by hand from the pages' statement of the problem, closed forms,
+ * library routines (numpy/torch fp16 and bf16 conversions, fp64 matmul) and
+ * brute-force integer arithmetic.  No function here is "parity unpinned".
+ *
+ * Build: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (fp32 operations
+ * must stay single-rounded, hence no contraction).
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+/* a_dtype / element type codes.  The first three match the library's enum by
+ * value (they name the same IEEE formats); F64 exists only here, so that a
+ * chain of oracle calls can feed an fp64 intermediate forward. */
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_F64 = 3 };
+
+/* zero-point modes */
+enum { OR_ZP_NONE = 0, OR_ZP_TENSOR = 1, OR_ZP_UNIFORM = 2 };
+
+/* ------------------------------------------------------------------------ */
+/* Scalar formats.                                                          */
+/* ------------------------------------------------------------------------ */
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction
+ * bits.  Exponent 0 encodes subnormals f * 2^-24; exponent 31 encodes inf
+ * (f == 0) and NaN.  Every binary16 value is exact in a double. */
+double oracle_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 31;
+    int f = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f + 1024), e - 25);
+    return sign ? -v : v;
+}
+
+/* bfloat16 is the upper half of an IEEE binary32. */
+double oracle_bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double load_elem(const void *base, int dtype, size_t i)
+{
+    switch (dtype) {
+    case OR_F32: return (double)((const float *)base)[i];
+    case OR_F16: return oracle_half_to_double(((const uint16_t *)base)[i]);
+    case OR_BF16: return oracle_bf16_to_double(((const uint16_t *)base)[i]);
+    default: return ((const double *)base)[i];
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Unpack.  [P1] Summary / What (Commit 1): MatMulNBits with bits=2 (and the  */
+/* bits=4 instantiations it leaves unchanged); [P3] Summary: 4-bit codes     */
+/* decoded inside the GEMM.  Packing order: LSB-first along K (reading).    */
+/* ------------------------------------------------------------------------ */
+int oracle_code(const uint8_t *W, int64_t K, int64_t n, int64_t k, int bits)
+{
+    int64_t row_bytes = K * bits / 8;
+    int64_t bit = k * bits;
+    uint8_t byte = W[n * row_bytes + bit / 8];
+    return (byte >> (bit % 8)) & ((1 << bits) - 1);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dequantize one weight.                                                    */
+/* nbits ([P1] What, Commit 1; Performance, Model: block 64, fp16 scales,    */
+/* fp16 zero points, all 1.5 on phi4, collapsed to a scalar when uniform):   */
+/*     w = fl32( fl32(q - zp) * s )                                          */
+/* codebook ([P3] Summary; Technical details, LDS centroid lookup; Testing   */
+/* plan, absmax):                                                            */
+/*     w = fl32( C[q] * absmax )                                             */
+/* ------------------------------------------------------------------------ */
+float oracle_weight_nbits(const uint8_t *W, const uint16_t *scales, const uint16_t *zp, int zp_mode,
+                          float uniform_zp, int64_t N, int64_t K, int bits, int bs, int64_t n, int64_t k)
+{
+    (void)N;
+    int64_t nb = K / bs;
+    int64_t b = k / bs;
+    int q = oracle_code(W, K, n, k, bits);
+    float zpv;
+    if (zp_mode == OR_ZP_TENSOR)
+        zpv = (float)oracle_half_to_double(zp[n * nb + b]);
+    else if (zp_mode == OR_ZP_UNIFORM)
+        zpv = uniform_zp;
+    else
+        zpv = (float)(1 << (bits - 1));
+    float s = (float)oracle_half_to_double(scales[n * nb + b]);
+    float d = (float)q - zpv;
+    float w = d * s;
+    return w;
+}
+
+float oracle_weight_codebook4(const uint8_t *W, const float *codebook, const float *absmax, int64_t K,
+                              int bs, int64_t n, int64_t k)
+{
+    int64_t nb = K / bs;
+    int q = oracle_code(W, K, n, k, 4);
+    float w = codebook[q] * absmax[n * nb + k / bs];
+    return w;
+}
+
+/* Dequantized matrices, fp32 [N][K].  The library's dequant-export entry
+ * points must reproduce these bit for bit. */
+void oracle_dequant_nbits(const uint8_t *W, const uint16_t *scales, const uint16_t *zp, int zp_mode,
+                          float uniform_zp, int64_t N, int64_t K, int bits, int bs, float *out)
+{
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            out[n * K + k] = oracle_weight_nbits(W, scales, zp, zp_mode, uniform_zp, N, K, bits, bs, n, k);
+}
+
+void oracle_dequant_codebook4(const uint8_t *W, const float *codebook, const float *absmax, int64_t N,
+                              int64_t K, int bs, float *out)
+{
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            out[n * K + k] = oracle_weight_codebook4(W, codebook, absmax, K, bs, n, k);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Matmul  Y[m, n] = sum_k A[m, k] * w[n, k]   (fp64, ascending k).          */
+/* [P1] What (Commit 1): GEMV reads fp32 A and writes fp32 C directly;       */
+/* [P3] Summary: decoded values reused across the M rows of a small batch.   */
+/* `rows` selects which weight rows n to evaluate (NULL: all N); the result  */
+/* is Y[m][j] for n = rows[j], as a dense [M][n_rows] fp64 array.           */
+/* ------------------------------------------------------------------------ */
+void oracle_qgemm_nbits(const void *A, int a_dtype, const uint8_t *W, const uint16_t *scales,
+                        const uint16_t *zp, int zp_mode, float uniform_zp, int64_t M, int64_t N, int64_t K,
+                        int bits, int bs, const int64_t *rows, int64_t n_rows, double *Y)
+{
+    if (!rows) n_rows = N;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t j = 0; j < n_rows; ++j) {
+        int64_t n = rows ? rows[j] : j;
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double a = load_elem(A, a_dtype, (size_t)(m * K + k));
+                double w = (double)oracle_weight_nbits(W, scales, zp, zp_mode, uniform_zp, N, K, bits, bs, n, k);
+                acc += a * w;
+            }
+            Y[m * n_rows + j] = acc;
+        }
+    }
+}
+
+void oracle_qgemm_codebook4(const void *A, int a_dtype, const uint8_t *W, const float *codebook,
+                            const float *absmax, int64_t M, int64_t N, int64_t K, int bs, const int64_t *rows,
+                            int64_t n_rows, double *Y)
+{
+    if (!rows) n_rows = N;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t j = 0; j < n_rows; ++j) {
+        int64_t n = rows ? rows[j] : j;
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double a = load_elem(A, a_dtype, (size_t)(m * K + k));
+                double w = (double)oracle_weight_codebook4(W, codebook, absmax, K, bs, n, k);
+                acc += a * w;
+            }
+            Y[m * n_rows + j] = acc;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Uniform zero point.  [P1] What (Commit 1): an all-equal fp16 zero-point    */
+/* tensor is detected once per buffer and then passed as a scalar.           */
+/* Equality is on bit patterns: +0 and -0 differ, and a NaN pattern is never */
+/* treated as a usable scalar (reading).  Returns 1 and writes the value     */
+/* when uniform, else 0.  An empty tensor is not uniform.                    */
+/* ------------------------------------------------------------------------ */
+int oracle_fp16_uniform_value(const uint16_t *t, int64_t n, float *value)
+{
+    if (n <= 0) return 0;
+    for (int64_t i = 1; i < n; ++i)
+        if (t[i] != t[0]) return 0;
+    double v = oracle_half_to_double(t[0]);
+    if (isnan(v)) return 0;
+    *value = (float)v;
+    return 1;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Fused QMoE decode, one token.                                             */
+/* [P2] Summary / What: fc1 GEMV -> SwiGLU -> fc2 GEMV over the top-k        */
+/* experts of one token, with u4 weights, block 32/64/128, optional zero     */
+/* points and optional bias ([P2] Test plan); num_experts bounds the ids.    */
+/* [P1] Why: the quantized SwiGLU chain is gate -> sigmoid -> two multiplies */
+/* -> up, i.e. h = gate * sigmoid(gate) * up.                                */
+/* For slot j (ascending): e = ids[j]; g = W1[e] x + b1[e];                  */
+/*   gate/up halves of g; h = silu(gate) * up; o = W2[e] h + b2[e];          */
+/*   y += weights[j] * o.                                                    */
+/* Everything after the fp32 dequantized weights is fp64.  An expert id      */
+/* outside [0, num_experts) contributes nothing and is reported through the  */
+/* return value (the number of such slots).                                  */
+/* Weight layouts: fc1 codes [E][2I][H*bits/8], scales/zp [E][2I][H/bs],     */
+/* bias [E][2I]; fc2 codes [E][H][I*bits/8], scales/zp [E][H][I/bs],         */
+/* bias [E][H].  Scratch: g [2I], h [I] doubles supplied by the caller.      */
+/* ------------------------------------------------------------------------ */
+static double silu(double v) { return v / (1.0 + exp(-v)); }
+
+int oracle_qmoe_decode(const uint16_t *x_f16, const int32_t *ids, const float *weights, int k,
+                       int num_experts, const uint8_t *fc1_w, const uint16_t *fc1_scales,
+                       const uint16_t *fc1_zp, const uint16_t *fc1_bias, const uint8_t *fc2_w,
+                       const uint16_t *fc2_scales, const uint16_t *fc2_zp, const uint16_t *fc2_bias,
+                       int64_t hidden, int64_t inter, int bits, int bs, int swiglu_interleaved, double *g,
+                       double *h, double *y)
+{
+    const int64_t H = hidden, I = inter, I2 = 2 * inter;
+    const int64_t fc1_row_bytes = H * bits / 8, fc2_row_bytes = I * bits / 8;
+    const int64_t fc1_nb = H / bs, fc2_nb = I / bs;
+    int bad = 0;
+    for (int64_t i = 0; i < H; ++i) y[i] = 0.0;
+
+    for (int j = 0; j < k; ++j) {
+        int e = ids[j];
+        if (e < 0 || e >= num_experts) {
+            ++bad;
+            continue;
+        }
+        const uint8_t *w1 = fc1_w + (int64_t)e * I2 * fc1_row_bytes;
+        const uint16_t *s1 = fc1_scales + (int64_t)e * I2 * fc1_nb;
+        const uint16_t *z1 = fc1_zp ? fc1_zp + (int64_t)e * I2 * fc1_nb : NULL;
+        const uint8_t *w2 = fc2_w + (int64_t)e * H * fc2_row_bytes;
+        const uint16_t *s2 = fc2_scales + (int64_t)e * H * fc2_nb;
+        const uint16_t *z2 = fc2_zp ? fc2_zp + (int64_t)e * H * fc2_nb : NULL;
+        int zm1 = z1 ? OR_ZP_TENSOR : OR_ZP_NONE;
+        int zm2 = z2 ? OR_ZP_TENSOR : OR_ZP_NONE;
+
+        /* fc1: g[r] = sum_c x[c] * W1[r][c] + b1[r] */
+        for (int64_t r = 0; r < I2; ++r) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < H; ++c)
+                acc += oracle_half_to_double(x_f16[c]) *
+                       (double)oracle_weight_nbits(w1, s1, z1, zm1, 0.0f, I2, H, bits, bs, r, c);
+            if (fc1_bias) acc += oracle_half_to_double(fc1_bias[(int64_t)e * I2 + r]);
+            g[r] = acc;
+        }
+        /* SwiGLU */
+        for (int64_t i = 0; i < I; ++i) {
+            double gate = swiglu_interleaved ? g[2 * i] : g[i];
+            double up = swiglu_interleaved ? g[2 * i + 1] : g[I + i];
+            h[i] = silu(gate) * up;
+        }
+        /* fc2 and the weighted sum over slots, in slot order */
+        for (int64_t r = 0; r < H; ++r) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < I; ++c)
+                acc += h[c] * (double)oracle_weight_nbits(w2, s2, z2, zm2, 0.0f, H, I, bits, bs, r, c);
+            if (fc2_bias) acc += oracle_half_to_double(fc2_bias[(int64_t)e * H + r]);
+            y[r] += (double)weights[j] * acc;
+        }
+        (void)fc1_row_bytes;
+        (void)fc2_row_bytes;
+    }
+    return bad;
+}

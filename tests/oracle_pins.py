@@ -1,0 +1,338 @@
+"""Pins for the CPU oracle: checks against facts that do not come from the oracle.
+
+Each ``check_*`` function takes a loaded oracle library (so that the same
+checks can be run against deliberately broken copies of the oracle in
+``test_oracle_mutants.py``) and raises ``AssertionError`` on a mismatch.
+
+What pins what:
+  * fp16 / bf16 decoding     -- numpy's float16 and torch's bfloat16
+                                conversions on all 65536 bit patterns;
+  * unpacking / bit order    -- hand-worked fixtures in tests/golden and
+                                numpy.unpackbits(bitorder="little");
+  * dequantization           -- hand-worked fixtures; closed forms computed
+                                with exact rational arithmetic;
+  * matmul index arithmetic  -- one-hot activations; brute-force int64
+                                products with an integer codebook; numpy's
+                                fp64 matmul on the oracle's dequantized matrix;
+  * uniform zero point       -- scalar path vs a full tensor of the value;
+  * QMoE composition         -- hand-worked fixture; the fused decode vs the
+                                unfused chain (oracle GEMMs + numpy bias,
+                                SwiGLU and weighted sum); one-hot slot weights.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _codes_via_unpackbits(W: np.ndarray, bits: int) -> np.ndarray:
+    """Codes from packed bytes using numpy.unpackbits (LSB-first per byte)."""
+    b = np.unpackbits(W, axis=-1, bitorder="little").reshape(W.shape[0], -1, bits)
+    weights = (1 << np.arange(bits)).astype(np.int64)
+    return (b.astype(np.int64) * weights).sum(axis=-1)
+
+
+def _h2f(bits: np.ndarray) -> np.ndarray:
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def _bf2f(bits: np.ndarray) -> np.ndarray:
+    import torch
+
+    t = torch.from_numpy(np.asarray(bits, dtype=np.uint16).view(np.int16).copy()).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+# ---------------------------------------------------------------------------
+def check_half_decode(lib):
+    allp = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = allp.view(np.float16).astype(np.float64)
+    got = np.array([lib.oracle_half_to_double(int(p)) for p in allp])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # signed zeros keep their sign
+    assert math.copysign(1.0, got[0x8000]) == -1.0
+
+
+def check_bf16_decode(lib):
+    allp = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = _bf2f(allp)
+    got = np.array([lib.oracle_bf16_to_double(int(p)) for p in allp])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def check_unpack_vs_unpackbits(lib):
+    g = np.random.default_rng(11)
+    for bits in (2, 4):
+        N, K = 5, 96
+        W = g.integers(0, 256, size=(N, K * bits // 8), dtype=np.uint8)
+        # scale 1, zero point 0 makes the dequantized value the code itself
+        ones = np.full((N, K // 32), np.float16(1.0).view(np.uint16), dtype=np.uint16)
+        deq = O.dequant_nbits(W, ones, None, N=N, K=K, bits=bits, block_size=32, uniform_zp=0.0, lib=lib)
+        assert np.array_equal(deq.astype(np.int64), _codes_via_unpackbits(W, bits))
+        for (n, k) in [(0, 0), (1, 5), (4, K - 1), (3, 17)]:
+            assert lib.oracle_code(W.ctypes.data, K, n, k, bits) == _codes_via_unpackbits(W, bits)[n, k]
+
+
+def check_golden_u2(lib):
+    d = _golden("u2_handworked.json")
+    W = np.array(d["W"], dtype=np.uint8)
+    S = np.array(d["scales_f16"], dtype=np.uint16)
+    Z = np.array(d["zero_points_f16"], dtype=np.uint16)
+    A = np.array(d["A"], dtype=np.float32)
+    kw = dict(N=d["N"], K=d["K"], bits=d["bits"], block_size=d["block_size"], lib=lib)
+    for deq in (O.dequant_nbits(W, S, Z, **kw), O.dequant_nbits(W, S, None, uniform_zp=d["uniform_zp"], **kw)):
+        assert np.array_equal(deq, np.array(d["dequant"], dtype=np.float32))
+    Y = O.qgemm_nbits(A, W, S, None, M=A.shape[0], uniform_zp=d["uniform_zp"], **kw)
+    assert np.array_equal(Y, np.array(d["Y"]))
+    Y = O.qgemm_nbits(A, W, S, Z, M=A.shape[0], **kw)
+    assert np.array_equal(Y, np.array(d["Y"]))
+
+
+def check_golden_u4(lib):
+    d = _golden("u4_handworked.json")
+    W = np.array(d["W"], dtype=np.uint8)
+    S = np.array(d["scales_f16"], dtype=np.uint16)
+    Z = np.array(d["zero_points_f16"], dtype=np.uint16)
+    A = np.array(d["A"], dtype=np.float32)
+    kw = dict(N=d["N"], K=d["K"], bits=d["bits"], block_size=d["block_size"], lib=lib)
+    assert np.array_equal(O.dequant_nbits(W, S, Z, **kw), np.array(d["dequant"], dtype=np.float32))
+    assert np.array_equal(O.dequant_nbits(W, S, None, **kw), np.array(d["dequant_no_zp"], dtype=np.float32))
+    assert np.array_equal(O.qgemm_nbits(A, W, S, Z, M=2, **kw), np.array(d["Y"]))
+    assert np.array_equal(O.qgemm_nbits(A, W, S, None, M=2, **kw), np.array(d["Y_no_zp"]))
+
+
+def check_golden_codebook(lib):
+    d = _golden("codebook4_handworked.json")
+    W = np.array(d["W"], dtype=np.uint8)
+    C = np.array(d["codebook"], dtype=np.float32)
+    AM = np.array(d["absmax"], dtype=np.float32)
+    A = np.array(d["A"], dtype=np.float32)
+    kw = dict(N=d["N"], K=d["K"], block_size=d["block_size"], lib=lib)
+    assert np.array_equal(O.dequant_codebook4(W, C, AM, **kw), np.array(d["dequant"], dtype=np.float32))
+    assert np.array_equal(O.qgemm_codebook4(A, W, C, AM, M=2, **kw), np.array(d["Y"]))
+
+
+def _pack_codes(codes: np.ndarray, bits: int) -> np.ndarray:
+    """Pack integer codes LSB-first along the last axis (numpy.packbits)."""
+    c = np.asarray(codes, dtype=np.uint8)
+    b = ((c[..., None] >> np.arange(bits)) & 1).astype(np.uint8)
+    b = b.reshape(*c.shape[:-1], c.shape[-1] * bits)
+    pad = (-b.shape[-1]) % 8
+    if pad:
+        b = np.concatenate([b, np.zeros((*b.shape[:-1], pad), np.uint8)], axis=-1)
+    return np.packbits(b, axis=-1, bitorder="little")
+
+
+def check_golden_qmoe(lib):
+    d = _golden("qmoe_handworked.json")
+    bits = d["bits"]
+    fc1_w = _pack_codes(np.array(d["fc1_codes"]), bits)
+    fc2_w = _pack_codes(np.array(d["fc2_codes"]), bits)
+    kw = dict(num_experts=d["num_experts"], fc1_w=fc1_w, fc1_scales=np.array(d["fc1_scales_f16"], np.uint16),
+              fc1_zp=None, fc1_bias=np.array(d["fc1_bias_f16"], np.uint16), fc2_w=fc2_w,
+              fc2_scales=np.array(d["fc2_scales_f16"], np.uint16), fc2_zp=None,
+              fc2_bias=np.array(d["fc2_bias_f16"], np.uint16), hidden=d["hidden"], inter=d["inter"],
+              bits=bits, block_size=d["block_size"], lib=lib)
+    x = np.array(d["x_f16"], np.uint16)
+    w = np.array(d["weights"], np.float32)
+    y, bad = O.qmoe_decode(x, np.array(d["ids"], np.int32), w, **kw)
+    assert bad == 0
+    np.testing.assert_allclose(y, d["y"], rtol=1e-14, atol=0)
+    y, bad = O.qmoe_decode(x, np.array(d["ids_bad"], np.int32), w, **kw)
+    assert bad == d["bad_slots"]
+    np.testing.assert_allclose(y, d["y_bad"], rtol=1e-14, atol=0)
+
+
+def check_onehot(lib):
+    """A = e_k recovers column k of the dequantized matrix exactly."""
+    g = np.random.default_rng(5)
+    for bits in (2, 4):
+        N, K, bs = 7, 128, 32
+        W = g.integers(0, 256, size=(N, K * bits // 8), dtype=np.uint8)
+        S = g.uniform(0.01, 0.05, size=(N, K // bs)).astype(np.float16).view(np.uint16)
+        Z = g.integers(0, 2 ** bits, size=(N, K // bs)).astype(np.float16).view(np.uint16)
+        deq = O.dequant_nbits(W, S, Z, N=N, K=K, bits=bits, block_size=bs, lib=lib)
+        A = np.eye(K, dtype=np.float32)[[0, 1, 37, K - 1]]
+        Y = O.qgemm_nbits(A, W, S, Z, M=4, N=N, K=K, bits=bits, block_size=bs, lib=lib)
+        assert np.array_equal(Y, deq[:, [0, 1, 37, K - 1]].T.astype(np.float64))
+        # and the dequantized value is exact: (q - zp) * s needs at most 17 significant bits
+        codes = _codes_via_unpackbits(W, bits)
+        exact = (codes - _h2f(Z).repeat(bs, axis=1)) * _h2f(S).repeat(bs, axis=1)
+        assert np.array_equal(deq.astype(np.float64), exact)
+
+
+def check_uniform_vs_tensor(lib):
+    g = np.random.default_rng(6)
+    for bits, zpv in ((2, 1.5), (4, 7.0), (4, 8.5)):
+        N, K, bs = 9, 256, 64
+        W = g.integers(0, 256, size=(N, K * bits // 8), dtype=np.uint8)
+        S = g.uniform(0.01, 0.05, size=(N, K // bs)).astype(np.float16).view(np.uint16)
+        Z = np.full((N, K // bs), np.float16(zpv).view(np.uint16), dtype=np.uint16)
+        A = g.standard_normal((3, K)).astype(np.float32)
+        kw = dict(M=3, N=N, K=K, bits=bits, block_size=bs, lib=lib)
+        assert np.array_equal(O.qgemm_nbits(A, W, S, Z, **kw), O.qgemm_nbits(A, W, S, None, uniform_zp=zpv, **kw))
+
+
+def check_closed_form(lib):
+    """All codes equal c and A = 1:  y_n = sum_b bs * (c - zp_nb) * s_nb  (exact rationals)."""
+    g = np.random.default_rng(7)
+    for bits, byte_for_code in ((2, {1: 0x55, 2: 0xAA, 3: 0xFF}), (4, {5: 0x55, 10: 0xAA, 15: 0xFF})):
+        N, K, bs = 4, 256, 64
+        S = g.uniform(0.01, 0.05, size=(N, K // bs)).astype(np.float16).view(np.uint16)
+        Z = g.integers(0, 2 ** bits, size=(N, K // bs)).astype(np.float16).view(np.uint16)
+        A = np.ones((1, K), np.float32)
+        for c, byte in byte_for_code.items():
+            W = np.full((N, K * bits // 8), byte, np.uint8)
+            Y = O.qgemm_nbits(A, W, S, Z, M=1, N=N, K=K, bits=bits, block_size=bs, lib=lib)
+            for n in range(N):
+                exact = sum(Fraction(bs) * (c - Fraction(float(_h2f(Z[n, b])))) * Fraction(float(_h2f(S[n, b])))
+                            for b in range(K // bs))
+                assert Fraction(Y[0, n]) == exact, (bits, c, n)
+
+
+def check_integer_codebook(lib):
+    """Codebook [0..15], absmax 1, integer A: an int64 matmul of the codes."""
+    g = np.random.default_rng(8)
+    N, K, bs, M = 6, 192, 64, 3
+    W = g.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    C = np.arange(16, dtype=np.float32)
+    AM = np.ones((N, K // bs), np.float32)
+    Ai = g.integers(-3, 4, size=(M, K)).astype(np.int64)
+    Y = O.qgemm_codebook4(Ai.astype(np.float32), W, C, AM, M=M, N=N, K=K, block_size=bs, lib=lib)
+    exact = Ai @ _codes_via_unpackbits(W, 4).T
+    assert np.array_equal(Y, exact.astype(np.float64))
+
+
+def check_library_matmul(lib):
+    """The oracle's fp64 loop equals numpy's fp64 matmul of A and its dequantized W."""
+    import torch
+
+    g = np.random.default_rng(9)
+    M, N, K, bs = 3, 37, 320, 64
+    A32 = g.standard_normal((M, K)).astype(np.float32)
+    A16 = A32.astype(np.float16).view(np.uint16)
+    Abf = torch.from_numpy(A32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    for bits in (2, 4):
+        W = g.integers(0, 256, size=(N, K * bits // 8), dtype=np.uint8)
+        S = g.uniform(0.005, 0.05, size=(N, K // bs)).astype(np.float16).view(np.uint16)
+        Z = g.integers(0, 2 ** bits, size=(N, K // bs)).astype(np.float16).view(np.uint16)
+        for zp, uz in ((Z, None), (None, None), (None, 1.5)):
+            deq = O.dequant_nbits(W, S, zp, N=N, K=K, bits=bits, block_size=bs, uniform_zp=uz, lib=lib).astype(np.float64)
+            for A, ad, A64 in ((A32, O.F32, A32.astype(np.float64)), (A16, O.F16, _h2f(A16)), (Abf, O.BF16, _bf2f(Abf))):
+                Y = O.qgemm_nbits(A, W, S, zp, M=M, N=N, K=K, bits=bits, block_size=bs, uniform_zp=uz, a_dtype=ad, lib=lib)
+                np.testing.assert_allclose(Y, A64 @ deq.T, rtol=1e-12, atol=1e-12)
+    W = g.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    C = np.sort(g.uniform(-1, 1, 16)).astype(np.float32)
+    AM = g.uniform(0.02, 0.1, size=(N, K // bs)).astype(np.float32)
+    deq = O.dequant_codebook4(W, C, AM, N=N, K=K, block_size=bs, lib=lib).astype(np.float64)
+    Y = O.qgemm_codebook4(A16, W, C, AM, M=M, N=N, K=K, block_size=bs, a_dtype=O.F16, lib=lib)
+    np.testing.assert_allclose(Y, _h2f(A16) @ deq.T, rtol=1e-12, atol=1e-12)
+    # the codebook dequant is C[q] * absmax in fp32 (library: numpy float32 multiply)
+    codes = _codes_via_unpackbits(W, 4)
+    assert np.array_equal(O.dequant_codebook4(W, C, AM, N=N, K=K, block_size=bs, lib=lib),
+                          C[codes] * AM.repeat(bs, axis=1))
+
+
+def check_rows_subset(lib):
+    g = np.random.default_rng(10)
+    M, N, K, bs, bits = 2, 50, 128, 32, 4
+    W = g.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    S = g.uniform(0.01, 0.05, size=(N, K // bs)).astype(np.float16).view(np.uint16)
+    A = g.standard_normal((M, K)).astype(np.float32)
+    full = O.qgemm_nbits(A, W, S, None, M=M, N=N, K=K, bits=bits, block_size=bs, lib=lib)
+    rows = np.array([49, 0, 17, 17, 3])
+    sub = O.qgemm_nbits(A, W, S, None, M=M, N=N, K=K, bits=bits, block_size=bs, rows=rows, lib=lib)
+    assert np.array_equal(sub, full[:, rows])
+
+
+def _qmoe_case(seed, E=5, k=3, H=64, I=96, bs=32, with_zp=True, with_bias=True):
+    g = np.random.default_rng(seed)
+    d = dict(num_experts=E, hidden=H, inter=I, bits=4, block_size=bs)
+    d["fc1_w"] = g.integers(0, 256, size=(E, 2 * I, H // 2), dtype=np.uint8)
+    d["fc2_w"] = g.integers(0, 256, size=(E, H, I // 2), dtype=np.uint8)
+    d["fc1_scales"] = g.uniform(0.005, 0.02, (E, 2 * I, H // bs)).astype(np.float16).view(np.uint16)
+    d["fc2_scales"] = g.uniform(0.005, 0.02, (E, H, I // bs)).astype(np.float16).view(np.uint16)
+    d["fc1_zp"] = g.integers(0, 16, (E, 2 * I, H // bs)).astype(np.float16).view(np.uint16) if with_zp else None
+    d["fc2_zp"] = g.integers(0, 16, (E, H, I // bs)).astype(np.float16).view(np.uint16) if with_zp else None
+    d["fc1_bias"] = (g.standard_normal((E, 2 * I)) * 0.01).astype(np.float16).view(np.uint16) if with_bias else None
+    d["fc2_bias"] = (g.standard_normal((E, H)) * 0.01).astype(np.float16).view(np.uint16) if with_bias else None
+    x = g.standard_normal(H).astype(np.float16).view(np.uint16)
+    ids = g.choice(E, size=k, replace=False).astype(np.int32)
+    w = g.uniform(0.1, 1.0, size=k).astype(np.float32)
+    return d, x, ids, w
+
+
+def _unfused_chain(lib, d, x, ids, w, interleaved):
+    """The unfused chain: oracle GEMMs for fc1 and fc2, numpy for the rest."""
+    H, I, bs = d["hidden"], d["inter"], d["block_size"]
+    y = np.zeros(H)
+    for j, e in enumerate(ids):
+        z1 = None if d["fc1_zp"] is None else d["fc1_zp"][e]
+        z2 = None if d["fc2_zp"] is None else d["fc2_zp"][e]
+        gvec = O.qgemm_nbits(x.reshape(1, H), d["fc1_w"][e], d["fc1_scales"][e], z1, M=1, N=2 * I, K=H, bits=4,
+                             block_size=bs, a_dtype=O.F16, lib=lib)[0]
+        if d["fc1_bias"] is not None:
+            gvec = gvec + _h2f(d["fc1_bias"][e])
+        gate, up = (gvec[0::2], gvec[1::2]) if interleaved else (gvec[:I], gvec[I:])
+        h = gate / (1.0 + np.exp(-gate)) * up
+        o = O.qgemm_nbits(h.reshape(1, I), d["fc2_w"][e], d["fc2_scales"][e], z2, M=1, N=H, K=I, bits=4,
+                          block_size=bs, a_dtype=O.F64, lib=lib)[0]
+        if d["fc2_bias"] is not None:
+            o = o + _h2f(d["fc2_bias"][e])
+        y = y + float(w[j]) * o
+    return y
+
+
+def check_qmoe_chain(lib):
+    for seed, zp, bias in ((1, True, True), (2, False, True), (3, True, False)):
+        d, x, ids, w = _qmoe_case(seed, with_zp=zp, with_bias=bias)
+        for inter_flag in (0, 1):
+            y, bad = O.qmoe_decode(x, ids, w, swiglu_interleaved=inter_flag, lib=lib, **d)
+            assert bad == 0
+            np.testing.assert_allclose(y, _unfused_chain(lib, d, x, ids, w, inter_flag), rtol=1e-12, atol=1e-13)
+    # one-hot slot weights reproduce one expert's chain alone
+    d, x, ids, w = _qmoe_case(4)
+    for j in range(len(ids)):
+        onehot = np.zeros(len(ids), np.float32)
+        onehot[j] = 1.0
+        y, _ = O.qmoe_decode(x, ids, onehot, lib=lib, **d)
+        np.testing.assert_allclose(y, _unfused_chain(lib, d, x, ids[j:j + 1], onehot[j:j + 1], 0),
+                                   rtol=1e-12, atol=1e-13)
+
+
+def check_uniform_detection(lib):
+    h = lambda v: int(np.float16(v).view(np.uint16))
+    assert O.fp16_uniform_value(np.full(1000, h(1.5), np.uint16), lib=lib) == (True, 1.5)
+    t = np.full(1000, h(1.5), np.uint16)
+    t[999] = h(2.5)
+    assert O.fp16_uniform_value(t, lib=lib) == (False, None)
+    t = np.full(10, 0, np.uint16)
+    t[3] = 0x8000  # -0 next to +0: different bit patterns
+    assert O.fp16_uniform_value(t, lib=lib) == (False, None)
+    assert O.fp16_uniform_value(np.full(10, 0x7E00, np.uint16), lib=lib) == (False, None)  # NaN
+    assert O.fp16_uniform_value(np.zeros(0, np.uint16), lib=lib) == (False, None)
+    assert O.fp16_uniform_value(np.array([h(-3.0)], np.uint16), lib=lib) == (True, -3.0)
+
+
+ALL_CHECKS = [
+    check_half_decode, check_bf16_decode, check_unpack_vs_unpackbits, check_golden_u2, check_golden_u4,
+    check_golden_codebook, check_golden_qmoe, check_onehot, check_uniform_vs_tensor, check_closed_form,
+    check_integer_codebook, check_library_matmul, check_rows_subset, check_qmoe_chain, check_uniform_detection,
+]

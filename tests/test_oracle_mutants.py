@@ -1,0 +1,65 @@
+"""Planted mistakes in the oracle must be caught by its pins (CPU only).
+
+Each case copies the oracle's C source, plants one plausible mistake by a
+textual substitution, compiles the copy into a temporary library and runs
+every pin check against it.  At least one pin must fail for every mutant;
+the unmodified source must pass them all (tests/test_oracle_pins.py).
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins as P
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "qgemm_oracle.c")
+
+MUTANTS = {
+    "msb_first_bit_order": ("return (byte >> (bit % 8)) & ((1 << bits) - 1);",
+                            "return (byte >> (8 - bits - bit % 8)) & ((1 << bits) - 1);"),
+    "scales_transposed": ("float s = (float)oracle_half_to_double(scales[n * nb + b]);",
+                          "float s = (float)oracle_half_to_double(scales[b * N + n]);"),
+    "zero_point_sign": ("float d = (float)q - zpv;", "float d = zpv - (float)q;"),
+    "midpoint_wrong": ("zpv = (float)(1 << (bits - 1));", "zpv = (float)((1 << bits) - 1);"),
+    "block_index_mod": ("int64_t b = k / bs;", "int64_t b = k % nb;"),
+    "codebook_reversed": ("float w = codebook[q] * absmax[n * nb + k / bs];",
+                          "float w = codebook[15 - q] * absmax[n * nb + k / bs];"),
+    "absmax_row_dropped": ("float w = codebook[q] * absmax[n * nb + k / bs];",
+                           "float w = codebook[q] * absmax[k / bs];"),
+    "half_exponent_bias": ("v = ldexp((double)(f + 1024), e - 25);", "v = ldexp((double)(f + 1024), e - 24);"),
+    "half_subnormal_scale": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
+    "bf16_shift": ("uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
+    "activation_transposed": ("double a = load_elem(A, a_dtype, (size_t)(m * K + k));\n                double w = (double)oracle_weight_nbits",
+                              "double a = load_elem(A, a_dtype, (size_t)(k * M + m));\n                double w = (double)oracle_weight_nbits"),
+    "gate_up_swapped": ("double gate = swiglu_interleaved ? g[2 * i] : g[i];\n            double up = swiglu_interleaved ? g[2 * i + 1] : g[I + i];",
+                        "double gate = swiglu_interleaved ? g[2 * i] : g[I + i];\n            double up = swiglu_interleaved ? g[2 * i + 1] : g[i];"),
+    "silu_sign": ("return v / (1.0 + exp(-v));", "return v / (1.0 + exp(v));"),
+    "fc2_bias_dropped": ("if (fc2_bias) acc += oracle_half_to_double(fc2_bias[(int64_t)e * H + r]);", ""),
+    "fc1_bias_wrong_expert": ("if (fc1_bias) acc += oracle_half_to_double(fc1_bias[(int64_t)e * I2 + r]);",
+                              "if (fc1_bias) acc += oracle_half_to_double(fc1_bias[r]);"),
+    "slot_weight_dropped": ("y[r] += (double)weights[j] * acc;", "y[r] += acc;"),
+    "expert_offset_by_slot": ("const uint8_t *w1 = fc1_w + (int64_t)e * I2 * fc1_row_bytes;",
+                              "const uint8_t *w1 = fc1_w + (int64_t)j * I2 * fc1_row_bytes;"),
+    "bad_id_not_reported": ("if (e < 0 || e >= num_experts) {\n            ++bad;\n            continue;\n        }",
+                            "if (e < 0 || e >= num_experts) {\n            continue;\n        }"),
+    "uniform_by_value": ("if (t[i] != t[0]) return 0;",
+                         "if (oracle_half_to_double(t[i]) != oracle_half_to_double(t[0])) return 0;"),
+    "uniform_accepts_nan": ("if (isnan(v)) return 0;", ""),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, "mutation anchor not found exactly once: %s" % name
+    msrc = tmp_path / "mutant.c"
+    msrc.write_text(src.replace(old, new))
+    lib = oracle.load(oracle.build(force=True, src=str(msrc), out=str(tmp_path / "libmutant.so")))
+    failed = []
+    for check in P.ALL_CHECKS:
+        try:
+            check(lib)
+        except (AssertionError, IndexError, ValueError):
+            failed.append(check.__name__)
+    assert failed, "no pin catches the planted mistake %r" % name
