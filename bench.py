@@ -1,0 +1,384 @@
+#!/usr/bin/env python3
+"""Benchmark: M=1 quantized GEMV weight GB/s (and us/call) on GB300.
+
+Workload (one "step"): the phi4-14B-shaped 2-bit MatMulNBits decode GEMVs
+(bits=2, block 64, fp16 scales, uniform zero point 1.5 passed as a scalar,
+fp32 activations and output, M=1) for the five linear shapes qkv (7680x5120),
+o (5120x5120), gate_up (35840x5120), down (5120x17920) and lm_head
+(100352x5120), one call each.  Inputs are seeded synthetic tensors of those
+shapes (the pages measured a real phi4 export that is not available here).
+
+value    = weight bytes (packed codes + fp16 scales) read per step x steps /
+           device time, in GB/s, summed over ranks (replicas: every rank runs
+           the same step on its own GPU).
+Cold weights: every step reads a different replica of all five weight sets;
+the replicas total more than three times the 129 MB L2, so no step finds its
+weights in L2 (the rotation the pages use for cold timing).
+
+--impl reference times the CPU oracle (the reference arm of this build) on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "M=1 quantized GEMV weight GB/s (% of GB300 HBM peak) and µs/call"
+SHAPES = ["qkv", "o", "gate_up", "down", "lm_head"]
+BITS, BS, ZP = 2, 64, 1.5
+L2_BYTES = 129 * 1024 * 1024
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemv_u2_m1_traffic.json")
+
+
+def weight_bytes(N, K):
+    return N * K * BITS // 8 + N * (K // BS) * 2
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("qg_simt.cu", "qg_device.cuh"):
+        with open(os.path.join(ROOT, "gemm_blockwise_dequant_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------- distributed
+def dist_setup(want_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    """Max of a float over ranks (timing only; not on the data path)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------- clocks
+class Clocks:
+    """nvidia-smi samples during the timed region (SM clock, throttle reasons)."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % gpu_index) \
+            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp/qg_clocks_%d.csv" % os.getpid()
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- CPU baseline
+def cpu_baseline(budget_s=12.0):
+    """Time the oracle (as it stands) on a bounded row sample of the workload."""
+    import oracle as O
+    import workloads as WL
+
+    O.load()
+    cores = os.cpu_count() or 1
+    # calibrate on a few rows of one shape, then size the sample to the budget
+    d = WL.phi4_u2("o", M=1)
+    t0 = time.perf_counter()
+    O.qgemm_nbits(d["A"], d["W"], d["scales"], None, M=1, N=d["N"], K=d["K"], bits=BITS, block_size=BS,
+                  uniform_zp=ZP, rows=np.arange(64))
+    per_row_k = (time.perf_counter() - t0) / (64 * d["K"])
+    total_k = sum(WL.PHI4_SHAPES[s][1] for s in SHAPES)
+    rows = max(16, int(budget_s / (per_row_k * total_k)))
+    done_bytes, secs = 0, 0.0
+    for s in SHAPES:
+        d = WL.phi4_u2(s, M=1)
+        r = np.linspace(0, d["N"] - 1, min(rows, d["N"])).astype(np.int64)
+        t0 = time.perf_counter()
+        O.qgemm_nbits(d["A"], d["W"], d["scales"], None, M=1, N=d["N"], K=d["K"], bits=BITS, block_size=BS,
+                      uniform_zp=ZP, rows=r)
+        secs += time.perf_counter() - t0
+        done_bytes += weight_bytes(len(r), d["K"])
+    return {"value": done_bytes / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "%d rows of each of the 5 phi4 shapes, M=1 (%.1f MB of weights, %.1f s)" % (
+                rows, done_bytes / 1e6, secs)}, secs
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    steps = []
+    for _ in range(args.warmup):
+        cpu_baseline(budget_s=2.0)
+    for _ in range(args.steps):
+        cb, secs = cpu_baseline(budget_s=max(2.0, 60.0 / max(1, args.steps)))
+        steps.append(cb)
+    v = statistics.median(s["value"] for s in steps)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "phi4-14B u2 decode GEMVs (qkv, o, gate_up, down, lm_head), M=1, bits=2, "
+                                   "block 64, uniform zp 1.5, fp32 A/Y; CPU oracle on a row sample"},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": steps[0]["cores"], "kind": "oracle",
+                             "sample": steps[0]["sample"]},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args, world, rank, local):
+    import torch
+
+    import gemm_blockwise_dequant_gb300 as qg
+    import workloads as WL
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    qg.lib()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+
+    # weights: one seeded set per shape, replicated so the rotation exceeds 3x L2
+    per_step = sum(weight_bytes(*WL.PHI4_SHAPES[s]) for s in SHAPES)
+    reps = max(2, -(-3 * L2_BYTES // per_step))
+    data = {}
+    for s in SHAPES:
+        d = WL.phi4_u2(s, M=1, seed=0)
+        W = torch.from_numpy(d["W"]).to(dev)
+        S = torch.from_numpy(d["scales"].view(np.int16)).to(dev).view(torch.float16)
+        A = torch.from_numpy(d["A"]).to(dev)
+        data[s] = dict(N=d["N"], K=d["K"], W=[W] + [W.clone() for _ in range(reps - 1)],
+                       S=[S] + [S.clone() for _ in range(reps - 1)], A=A,
+                       Y=torch.empty(1, d["N"], device=dev), A_host=torch.from_numpy(d["A"]).pin_memory(),
+                       Y_host=torch.empty(1, d["N"]).pin_memory())
+    ws_need = max(qg.qgemm_workspace_bytes(0, 1, data[s]["N"], data[s]["K"], BITS, BS) for s in SHAPES)
+    ws = torch.empty(max(ws_need, 16), dtype=torch.uint8, device=dev)
+
+    def call(s, r):
+        e = data[s]
+        qg.qgemm_nbits_uniform_zp(e["A"], e["W"][r], e["S"][r], ZP, e["Y"], bits=BITS, block_size=BS,
+                                  workspace=ws, stream=stream)
+
+    def step(r):
+        for s in SHAPES:
+            call(s, r)
+
+    # CUDA graphs: one per replica set (the library is capture-safe: no sync, no allocation)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for r in range(reps):
+            step(r)
+        stream.synchronize()
+        for r in range(reps):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(r)
+            graphs.append(g)
+    torch.cuda.synchronize()
+
+    # ---- timed region: K graph replays (5 GEMV launches each)
+    for i in range(args.warmup):
+        graphs[i % reps].replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for i in range(args.steps):
+                graphs[(i + args.warmup) % reps].replay()
+            end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    step_ms = start.elapsed_time(end) / args.steps
+    step_ms = max_over_ranks(step_ms, world)
+    clocks = clk.summary()
+
+    # ---- per-launch durations of each kernel (events around every launch, same stream)
+    per_shape_us = {}
+    dom_bytes, dom_time = 0, 0.0
+    launches = 0
+    for s in SHAPES:
+        evs = []
+        with torch.cuda.stream(stream):
+            for i in range(max(args.steps, 8)):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                call(s, i % reps)
+                b.record(stream)
+                evs.append((a, b))
+        torch.cuda.synchronize()
+        us = [a.elapsed_time(b) * 1e3 for a, b in evs]
+        per_shape_us[s] = statistics.median(us)
+        launches += 1
+        if WL.PHI4_SHAPES[s][1] == 5120:  # the K=5120 launches share one kernel instantiation
+            dom_bytes += weight_bytes(*WL.PHI4_SHAPES[s])
+            dom_time += statistics.mean(us)
+
+    # ---- end to end through the API with host buffers: H2D of A, 5 GEMVs, D2H of Y every step
+    h2d = sum(data[s]["A_host"].numel() * 4 for s in SHAPES)
+    d2h = sum(data[s]["Y_host"].numel() * 4 for s in SHAPES)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i % reps)
+        stream.synchronize()
+        e0.record(stream)
+        for i in range(args.steps):
+            r = i % reps
+            for s in SHAPES:
+                e = data[s]
+                e["A"].copy_(e["A_host"], non_blocking=True)
+                call(s, r)
+                e["Y_host"].copy_(e["Y"], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+
+    peak, peak_kind = peaks()
+    value = world * per_step / (step_ms * 1e-3) / 1e9
+    achieved = dom_bytes / (dom_time * 1e-6) / 1e9
+    traffic = None
+    if os.path.exists(TRAFFIC_FILE):
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        if tr.get("kernel_source_hash") == kernel_source_hash():
+            traffic = tr.get("bytes_per_launch")
+    cb = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb, _ = cpu_baseline()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "phi4-14B u2 decode GEMVs (qkv 7680x5120, o 5120x5120, gate_up 35840x5120, "
+                               "down 5120x17920, lm_head 100352x5120), M=1, bits=2, block 64, fp16 scales, "
+                               "uniform zp 1.5, fp32 A/Y",
+                   "weight_bytes_per_step": per_step, "l2": "weights rotate over %d replicas (%.0f MB > 3x L2)" % (
+                       reps, reps * per_step / 1e6),
+                   "step": "one CUDA-graph replay of the 5 GEMV launches", "pct_of_hbm_peak": round(
+                       100 * value / world / peak, 1), "us_per_call": {s: round(v, 2) for s, v in per_shape_us.items()},
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "gemv_kernel u2 M=1 (K=5120 launches: qkv, o, gate_up, lm_head)",
+                     "peak_kind": peak_kind},
+        "e2e": {"value": round(world * per_step / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": len(SHAPES) * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cb,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

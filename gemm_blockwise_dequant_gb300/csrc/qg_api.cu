@@ -1,0 +1,382 @@
+// qg_api.cu -- the C ABI (include/qgemm.h): argument checks, error-state
+// hygiene and dispatch to the kernels.
+//
+// Argument refusal before any launch and clearing the stale CUDA error on
+// entry follow hip-ep #1328 ("What": clear the error state before the fused
+// decode launches; "Test plan": the arguments the launchers must refuse).
+#include <atomic>
+#include <climits>
+#include <cstring>
+
+#include "../../include/qgemm.h"
+#include "qg_internal.h"
+
+namespace qg {
+
+__device__ unsigned g_fault_word;
+
+namespace {
+constexpr int kMaxDevices = 64;
+DeviceInfo g_info[kMaxDevices];
+std::atomic<int> g_info_ready[kMaxDevices];
+unsigned *g_fault_ptr[kMaxDevices];
+std::atomic<int> g_fault_ready[kMaxDevices];
+
+int current_device() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return dev < 0 || dev >= kMaxDevices ? 0 : dev;
+}
+}  // namespace
+
+const DeviceInfo &device_info() {
+    const int dev = current_device();
+    if (!g_info_ready[dev].load(std::memory_order_acquire)) {
+        DeviceInfo d{};
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (d.sm_count <= 0) d.sm_count = 1;
+        if (d.max_smem_optin <= 0) d.max_smem_optin = 48 * 1024;
+        g_info[dev] = d;
+        g_info_ready[dev].store(1, std::memory_order_release);
+    }
+    return g_info[dev];
+}
+
+unsigned *fault_word() {
+    const int dev = current_device();
+    if (!g_fault_ready[dev].load(std::memory_order_acquire)) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fault_word) != cudaSuccess) return nullptr;
+        g_fault_ptr[dev] = static_cast<unsigned *>(p);
+        g_fault_ready[dev].store(1, std::memory_order_release);
+    }
+    return g_fault_ptr[dev];
+}
+
+}  // namespace qg
+
+namespace {
+
+using qg::GemmProblem;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool valid_dtype(int d) { return d == QG_F32 || d == QG_F16 || d == QG_BF16; }
+bool valid_bs(int bs) { return bs == 32 || bs == 64 || bs == 128 || bs == 256; }
+
+// Sizes beyond these are valid in principle but not implemented (32-bit
+// index arithmetic inside the kernels).
+constexpr long long kMaxK = 1 << 24;
+constexpr long long kMaxN = 1 << 28;
+constexpr long long kMaxM = 1 << 20;
+
+size_t gemm_workspace(int a_dtype, int M, int N, int K, int bits, int bs) {
+    (void)a_dtype;
+    if (M <= 0 || N <= 0 || K <= 0 || (bits != 2 && bits != 4) || !valid_bs(bs) || K % bs) return 0;
+    return qg::simt_workspace_bytes(M, N, K, bits, bs);
+}
+
+// Common checks of the three GEMM entry points.  `params` is the scales or
+// absmax pointer.
+int check_gemm(const void *A, int a_dtype, const uint8_t *W, const void *params, const void *zp, const void *Y,
+               int y_dtype, int M, int N, int K, int bits, int bs, const void *ws, size_t ws_bytes) {
+    if (!valid_dtype(a_dtype) || !valid_dtype(y_dtype)) return QG_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0) return QG_ERR_INVALID_ARG;
+    if (bits != 2 && bits != 4) return QG_ERR_UNSUPPORTED;
+    if (!valid_bs(bs)) return QG_ERR_UNSUPPORTED;
+    if (K % bs) return QG_ERR_INVALID_ARG;
+    if (M > kMaxM || N > kMaxN || K > kMaxK) return QG_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return QG_OK;
+    if (!Y) return QG_ERR_INVALID_ARG;
+    if (K > 0) {
+        if (!A || !W || !params) return QG_ERR_INVALID_ARG;
+        if (!aligned16(A) || !aligned16(W) || !aligned16(params)) return QG_ERR_INVALID_ARG;
+        if (zp && !aligned16(zp)) return QG_ERR_INVALID_ARG;
+    }
+    const size_t need = gemm_workspace(a_dtype, M, N, K, bits, bs);
+    if (need > 0) {
+        if (!ws || ws_bytes < need) return QG_ERR_WORKSPACE_TOO_SMALL;
+        if (!aligned16(ws)) return QG_ERR_INVALID_ARG;
+    }
+    return QG_OK;
+}
+
+size_t elem_size(int dtype) { return dtype == QG_F32 ? 4 : 2; }
+
+int run_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s) {
+    if (p.M == 0 || p.N == 0) return QG_OK;
+    if (p.K == 0) {
+        if (cudaMemsetAsync(p.Y, 0, static_cast<size_t>(p.M) * p.N * elem_size(p.y_dtype), s) != cudaSuccess)
+            return QG_ERR_CUDA;
+        return QG_OK;
+    }
+    const cudaError_t e = qg::simt_gemm(p, ws, ws_bytes, s);
+    if (e == cudaErrorNotSupported) return QG_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+int nbits_common(const void *A, int a_dtype, const uint8_t *W, const uint16_t *scales, const uint16_t *zp,
+                 int zp_mode, float uniform_zp, void *Y, int y_dtype, int M, int N, int K, int bits, int bs,
+                 void *ws, size_t ws_bytes, qg_stream_t stream) {
+    (void)cudaGetLastError();  // do not report an earlier, unrelated failure as ours
+    const int st = check_gemm(A, a_dtype, W, scales, zp, Y, y_dtype, M, N, K, bits, bs, ws, ws_bytes);
+    if (st != QG_OK) return st;
+    GemmProblem p{};
+    p.A = A;
+    p.a_dtype = a_dtype;
+    p.W = W;
+    p.kind = qg::WK_NBITS;
+    p.scales = scales;
+    p.zp = zp;
+    p.zp_mode = zp_mode;
+    p.uniform_zp = zp_mode == qg::ZP_NONE ? static_cast<float>(1 << (bits - 1)) : uniform_zp;
+    p.Y = Y;
+    p.y_dtype = y_dtype;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.bits = bits;
+    p.bs = bs;
+    return run_gemm(p, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int qgemm_nbits(const void *A, int a_dtype, const uint8_t *W, const uint16_t *scales_f16,
+                const uint16_t *zero_points_f16, void *Y, int y_dtype, int M, int N, int K, int bits, int block_size,
+                void *workspace, size_t workspace_bytes, qg_stream_t stream) {
+    return nbits_common(A, a_dtype, W, scales_f16, zero_points_f16,
+                        zero_points_f16 ? qg::ZP_TENSOR : qg::ZP_NONE, 0.f, Y, y_dtype, M, N, K, bits, block_size,
+                        workspace, workspace_bytes, stream);
+}
+
+int qgemm_nbits_uniform_zp(const void *A, int a_dtype, const uint8_t *W, const uint16_t *scales_f16,
+                           float uniform_zp, void *Y, int y_dtype, int M, int N, int K, int bits, int block_size,
+                           void *workspace, size_t workspace_bytes, qg_stream_t stream) {
+    if (!(uniform_zp == uniform_zp) || uniform_zp > 65504.f || uniform_zp < -65504.f) {
+        (void)cudaGetLastError();
+        return QG_ERR_INVALID_ARG;  // not a finite fp16 value
+    }
+    return nbits_common(A, a_dtype, W, scales_f16, nullptr, qg::ZP_UNIFORM, uniform_zp, Y, y_dtype, M, N, K, bits,
+                        block_size, workspace, workspace_bytes, stream);
+}
+
+int qgemm_codebook4(const void *A, int a_dtype, const uint8_t *W, const float *codebook16, const float *absmax,
+                    void *Y, int y_dtype, int M, int N, int K, int block_size, void *workspace,
+                    size_t workspace_bytes, qg_stream_t stream) {
+    (void)cudaGetLastError();
+    int st = check_gemm(A, a_dtype, W, absmax, nullptr, Y, y_dtype, M, N, K, 4, block_size, workspace,
+                        workspace_bytes);
+    if (st != QG_OK) return st;
+    if (M > 0 && N > 0 && K > 0 && !codebook16) return QG_ERR_INVALID_ARG;
+    GemmProblem p{};
+    p.A = A;
+    p.a_dtype = a_dtype;
+    p.W = W;
+    p.kind = qg::WK_CODEBOOK;
+    p.codebook = codebook16;
+    p.absmax = absmax;
+    p.Y = Y;
+    p.y_dtype = y_dtype;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.bits = 4;
+    p.bs = block_size;
+    return run_gemm(p, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t qgemm_workspace_bytes(int a_dtype, int M, int N, int K, int bits, int block_size) {
+    return gemm_workspace(a_dtype, M, N, K, bits, block_size);
+}
+
+int qmoe_decode_fused(const uint16_t *x_f16, const int32_t *expert_ids, const float *expert_weights, int k,
+                      int num_experts, const uint8_t *fc1_w, const uint16_t *fc1_scales, const uint16_t *fc1_zp,
+                      const uint16_t *fc1_bias, const uint8_t *fc2_w, const uint16_t *fc2_scales,
+                      const uint16_t *fc2_zp, const uint16_t *fc2_bias, int hidden, int inter, int bits,
+                      int block_size, int swiglu_interleaved, uint16_t *y_f16, int *status_dev, void *workspace,
+                      size_t workspace_bytes, qg_stream_t stream) {
+    (void)cudaGetLastError();  // do not report an earlier, unrelated failure as ours
+    if (k < 0 || num_experts < 0 || hidden <= 0 || inter <= 0) return QG_ERR_INVALID_ARG;
+    if (swiglu_interleaved != 0 && swiglu_interleaved != 1) return QG_ERR_INVALID_ARG;
+    if (bits != 2 && bits != 4) return QG_ERR_UNSUPPORTED;
+    if (!valid_bs(block_size)) return QG_ERR_UNSUPPORTED;
+    if (hidden % block_size || inter % block_size) return QG_ERR_INVALID_ARG;
+    if (hidden > kMaxK || inter > kMaxK / 2 || k > 4096) return QG_ERR_UNSUPPORTED;
+    if (!x_f16 || !y_f16) return QG_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (k == 0) {
+        if (cudaMemsetAsync(y_f16, 0, static_cast<size_t>(hidden) * 2, s) != cudaSuccess) return QG_ERR_CUDA;
+        if (status_dev && cudaMemsetAsync(status_dev, 0, sizeof(int), s) != cudaSuccess) return QG_ERR_CUDA;
+        return QG_OK;
+    }
+    if (num_experts < 1 || !expert_ids || !expert_weights || !fc1_w || !fc1_scales || !fc2_w || !fc2_scales)
+        return QG_ERR_INVALID_ARG;
+    const void *al16[] = {fc1_w, fc1_scales, fc2_w, fc2_scales};
+    for (const void *q : al16)
+        if (!aligned16(q)) return QG_ERR_INVALID_ARG;
+    if ((fc1_zp && !aligned16(fc1_zp)) || (fc2_zp && !aligned16(fc2_zp))) return QG_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(expert_ids) | reinterpret_cast<uintptr_t>(expert_weights)) & 3u)
+        return QG_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x_f16) | reinterpret_cast<uintptr_t>(y_f16) |
+         reinterpret_cast<uintptr_t>(fc1_bias) | reinterpret_cast<uintptr_t>(fc2_bias)) & 1u)
+        return QG_ERR_INVALID_ARG;
+    if (status_dev && (reinterpret_cast<uintptr_t>(status_dev) & 3u)) return QG_ERR_INVALID_ARG;
+    const size_t need = qg::qmoe_workspace_bytes(k, hidden, inter);
+    if (!workspace || workspace_bytes < need) return QG_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(workspace)) return QG_ERR_INVALID_ARG;
+    qg::QmoeProblem q{};
+    q.x = x_f16;
+    q.ids = expert_ids;
+    q.weights = expert_weights;
+    q.k = k;
+    q.num_experts = num_experts;
+    q.fc1_w = fc1_w;
+    q.fc1_scales = fc1_scales;
+    q.fc1_zp = fc1_zp;
+    q.fc1_bias = fc1_bias;
+    q.fc2_w = fc2_w;
+    q.fc2_scales = fc2_scales;
+    q.fc2_zp = fc2_zp;
+    q.fc2_bias = fc2_bias;
+    q.hidden = hidden;
+    q.inter = inter;
+    q.bits = bits;
+    q.bs = block_size;
+    q.swiglu_interleaved = swiglu_interleaved;
+    q.y = y_f16;
+    q.status = status_dev;
+    const cudaError_t e = qg::qmoe_decode(q, workspace, s);
+    if (e == cudaErrorNotSupported) return QG_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+size_t qmoe_decode_workspace_bytes(int k, int hidden, int inter) {
+    return qg::qmoe_workspace_bytes(k, hidden, inter);
+}
+
+int qg_fp16_uniform_value(const uint16_t *t, size_t n, int *is_uniform, float *value, void *workspace,
+                          size_t workspace_bytes, qg_stream_t stream) {
+    (void)cudaGetLastError();
+    if (!is_uniform || !value) return QG_ERR_INVALID_ARG;
+    if (n == 0) {
+        *is_uniform = 0;
+        return QG_OK;
+    }
+    if (!t || !aligned16(t)) return QG_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace)) return QG_ERR_INVALID_ARG;
+    if (workspace_bytes < 16) return QG_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned *ws = static_cast<unsigned *>(workspace);
+    if (qg::launch_uniform_check(t, n, ws, s) != cudaSuccess) return QG_ERR_CUDA;
+    unsigned diff = 0;
+    uint16_t first = 0;
+    if (cudaMemcpyAsync(&diff, ws, sizeof diff, cudaMemcpyDeviceToHost, s) != cudaSuccess) return QG_ERR_CUDA;
+    if (cudaMemcpyAsync(&first, t, sizeof first, cudaMemcpyDeviceToHost, s) != cudaSuccess) return QG_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return QG_ERR_CUDA;
+    const bool nan = (first & 0x7C00u) == 0x7C00u && (first & 0x03FFu) != 0u;
+    if (diff || nan) {
+        *is_uniform = 0;
+        return QG_OK;
+    }
+    // binary16 -> float (exact)
+    const uint32_t sign = (first >> 15) & 1u, ex = (first >> 10) & 31u, fr = first & 1023u;
+    float v;
+    if (ex == 0)
+        v = static_cast<float>(fr) * (1.0f / 16777216.0f);
+    else if (ex == 31)
+        v = INFINITY;
+    else {
+        uint32_t bits = ((ex - 15 + 127) << 23) | (fr << 13);
+        std::memcpy(&v, &bits, sizeof v);
+    }
+    *value = sign ? -v : v;
+    *is_uniform = 1;
+    return QG_OK;
+}
+
+static int dequant_common(GemmProblem &p, float *out, qg_stream_t stream) {
+    (void)cudaGetLastError();
+    if (p.N < 0 || p.K < 0) return QG_ERR_INVALID_ARG;
+    if (p.bits != 2 && p.bits != 4) return QG_ERR_UNSUPPORTED;
+    if (!valid_bs(p.bs)) return QG_ERR_UNSUPPORTED;
+    if (p.K % p.bs) return QG_ERR_INVALID_ARG;
+    if (p.N > kMaxN || p.K > kMaxK) return QG_ERR_UNSUPPORTED;
+    if (p.N == 0 || p.K == 0) return QG_OK;
+    const void *params = p.kind == qg::WK_CODEBOOK ? static_cast<const void *>(p.absmax) : p.scales;
+    if (!p.W || !params || !out) return QG_ERR_INVALID_ARG;
+    if (p.kind == qg::WK_CODEBOOK && !p.codebook) return QG_ERR_INVALID_ARG;
+    if (!aligned16(p.W) || !aligned16(params) || !aligned16(out) || (p.zp && !aligned16(p.zp)))
+        return QG_ERR_INVALID_ARG;
+    return qg::launch_dequant(p, out, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+int qg_dequant_nbits(const uint8_t *W, const uint16_t *scales_f16, const uint16_t *zero_points_f16, float *out,
+                     int N, int K, int bits, int block_size, qg_stream_t stream) {
+    GemmProblem p{};
+    p.W = W;
+    p.kind = qg::WK_NBITS;
+    p.scales = scales_f16;
+    p.zp = zero_points_f16;
+    p.zp_mode = zero_points_f16 ? qg::ZP_TENSOR : qg::ZP_NONE;
+    p.uniform_zp = (bits == 2 || bits == 4) ? static_cast<float>(1 << (bits - 1)) : 0.f;
+    p.N = N;
+    p.K = K;
+    p.bits = bits;
+    p.bs = block_size;
+    return dequant_common(p, out, stream);
+}
+
+int qg_dequant_nbits_uniform_zp(const uint8_t *W, const uint16_t *scales_f16, float uniform_zp, float *out, int N,
+                                int K, int bits, int block_size, qg_stream_t stream) {
+    GemmProblem p{};
+    p.W = W;
+    p.kind = qg::WK_NBITS;
+    p.scales = scales_f16;
+    p.zp_mode = qg::ZP_UNIFORM;
+    p.uniform_zp = uniform_zp;
+    p.N = N;
+    p.K = K;
+    p.bits = bits;
+    p.bs = block_size;
+    return dequant_common(p, out, stream);
+}
+
+int qg_dequant_codebook4(const uint8_t *W, const float *codebook16, const float *absmax, float *out, int N, int K,
+                         int block_size, qg_stream_t stream) {
+    GemmProblem p{};
+    p.W = W;
+    p.kind = qg::WK_CODEBOOK;
+    p.codebook = codebook16;
+    p.absmax = absmax;
+    p.N = N;
+    p.K = K;
+    p.bits = 4;
+    p.bs = block_size;
+    return dequant_common(p, out, stream);
+}
+
+int qg_read_device_fault(unsigned int *flags) {
+    if (!flags) return QG_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return QG_ERR_CUDA;
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, qg::g_fault_word, sizeof v) != cudaSuccess) return QG_ERR_CUDA;
+    if (cudaMemcpyToSymbol(qg::g_fault_word, &zero, sizeof zero) != cudaSuccess) return QG_ERR_CUDA;
+    *flags = v;
+    return QG_OK;
+}
+
+const char *qg_status_string(int status) {
+    switch (status) {
+    case QG_OK: return "QG_OK";
+    case QG_ERR_INVALID_ARG: return "QG_ERR_INVALID_ARG";
+    case QG_ERR_UNSUPPORTED: return "QG_ERR_UNSUPPORTED";
+    case QG_ERR_CUDA: return "QG_ERR_CUDA";
+    case QG_ERR_WORKSPACE_TOO_SMALL: return "QG_ERR_WORKSPACE_TOO_SMALL";
+    default: return "QG_ERR_UNKNOWN";
+    }
+}
+
+}  // extern "C"

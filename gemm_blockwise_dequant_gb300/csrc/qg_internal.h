@@ -1,0 +1,67 @@
+// qg_internal.h -- host-side declarations shared by the library's translation
+// units (not part of the public ABI; see include/qgemm.h for that).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qg {
+
+enum ZpMode { ZP_NONE = 0, ZP_TENSOR = 1, ZP_UNIFORM = 2 };
+enum WeightKind { WK_NBITS = 0, WK_CODEBOOK = 1 };
+
+// Per-device facts cached on first use.
+struct DeviceInfo {
+    int sm_count;
+    int max_smem_optin;
+};
+const DeviceInfo &device_info();
+
+// Address of the device fault word of the current device (see
+// qg_read_device_fault).
+unsigned *fault_word();
+
+// One blockwise-dequant GEMM/GEMV request, already validated.
+struct GemmProblem {
+    const void *A;
+    int a_dtype;
+    const uint8_t *W;
+    int kind;                 // WeightKind
+    const uint16_t *scales;   // nbits
+    const uint16_t *zp;       // nbits, ZP_TENSOR
+    int zp_mode;
+    float uniform_zp;         // ZP_UNIFORM (ZP_NONE: midpoint filled in by the caller)
+    const float *codebook;    // codebook
+    const float *absmax;      // codebook
+    void *Y;
+    int y_dtype;
+    int M, N, K, bits, bs;
+};
+
+// SIMT decode path (small M).
+size_t simt_workspace_bytes(int M, int N, int K, int bits, int bs);
+cudaError_t simt_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s);
+
+// Fused single-token QMoE decode (fc1 -> SwiGLU -> fc2 -> weighted sum).
+struct QmoeProblem {
+    const uint16_t *x;
+    const int32_t *ids;
+    const float *weights;
+    int k, num_experts;
+    const uint8_t *fc1_w;
+    const uint16_t *fc1_scales, *fc1_zp, *fc1_bias;
+    const uint8_t *fc2_w;
+    const uint16_t *fc2_scales, *fc2_zp, *fc2_bias;
+    int hidden, inter, bits, bs, swiglu_interleaved;
+    uint16_t *y;
+    int *status;
+};
+size_t qmoe_workspace_bytes(int k, int hidden, int inter);
+cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s);
+
+// Utility kernels.
+cudaError_t launch_dequant(const GemmProblem &p, float *out, cudaStream_t s);
+cudaError_t launch_uniform_check(const uint16_t *t, size_t n, unsigned *ws, cudaStream_t s);
+
+}  // namespace qg

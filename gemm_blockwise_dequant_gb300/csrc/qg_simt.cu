@@ -1,0 +1,725 @@
+// qg_simt.cu -- SIMT blockwise-dequant GEMV / small-M GEMM for sm_103a.
+//
+// Computes Y[m][n] = sum_k A[m][k] * w[n][k] for small M, with w the
+// blockwise dequantized weight:
+//   nbits:    w = (q - zp) * s      (MatMulNBits; hip-ep #1318, "What",
+//                                     Commit 1: u2 GEMV reading fp32 A and
+//                                     writing fp32 C directly)
+//   codebook: w = C[q] * absmax     (NF4/FP4; bitsandbytes #1979, "Summary":
+//                                     codes decoded inside the GEMM, decoded
+//                                     values reused across the M rows)
+//
+// Design (GB300-first; the pages' RDNA design -- dot2, DPP, LDS centroids --
+// is prior art only):
+//  * Weights stream through shared memory.  One producer warp per CTA moves
+//    tiles of SR whole rows (codes + per-block parameters) with 1-D bulk
+//    copies (TMA engine) into an NST-deep ring guarded by mbarriers, so the
+//    consumer warps never wait on HBM latency and hold no load registers.
+//  * Each consumer warp owns one K-slice (32 lanes x KPL consecutive k) and
+//    keeps the activations of that slice in registers for the whole kernel;
+//    it walks the rows of every stage.  Reading a lane's codes from shared
+//    memory is one conflict-free vector load.
+//  * Unpacking costs one LOP per code: a code masked in place inside its
+//    32-bit word IS an fp32 subnormal equal to q * 2^(pos - 149).  The
+//    activations are pre-scaled by 2^(126 - pos) (and by a per-lane power of
+//    two that normalises their magnitude), so one packed fp32x2 FMA per two
+//    codes accumulates a * q exactly as an ordinary FMA would.  The zero
+//    point and the scale are applied once per block per row:
+//        sum_k a_k (q_k - zp) s = s * (sum_k a_k q_k - zp * sum_k a_k).
+//  * Reductions run in a fixed order: a transposed butterfly over the 32
+//    lanes, then the K-slices of a row summed in slice order in shared
+//    memory, then (for very long K) split-K partials summed in split order by
+//    a second kernel.  No atomics, no dependence on timing: every call on the
+//    same inputs is bit-identical (hip-ep #1328, "Why").
+//  * Every wait is bounded (see qg_device.cuh): a stuck pipeline records a
+//    fault bit and the kernel returns instead of hanging.
+#include <algorithm>
+#include <atomic>
+
+#include "qg_device.cuh"
+#include "qg_internal.h"
+
+namespace qg {
+namespace {
+
+constexpr int kMaxConsumerWarps = 12;
+constexpr int kRedV = 8;  // values per warp per stage entering the cross-lane reduction
+constexpr int kMaxStages = 8;
+constexpr int kLutOff = 256;
+
+struct GemvArgs {
+    const void *A;
+    int a_dtype;
+    const uint8_t *W;
+    const unsigned char *params;  // fp16 scales (nbits) or fp32 absmax (codebook), [N][nb]
+    const uint16_t *zp;           // fp16 zero points [N][nb] (ZP_TENSOR)
+    int zp_mode;
+    float zpv;  // zero point for ZP_UNIFORM / ZP_NONE
+    const float *codebook;
+    void *Y;
+    int y_dtype;
+    float *partial;  // split-K partials [splits][M][N], or nullptr
+    int M, N, K, bs, nb, row_bytes, m0;
+    int S_total, S_cta, G, SR, NST;
+    int w_pitch, stage_bytes, s_off, z_off, red_off, stage_off, ntiles;
+    unsigned *fault;
+    // Slots (the experts of a QMoE decode): tile t covers rows of slot
+    // t / tiles_per_slot; slot j reads the weights of expert ids[j].  Plain
+    // GEMMs have one slot and ids == nullptr.
+    int tiles_per_slot;
+    const int32_t *ids;
+    int num_experts;
+    size_t w_slot_stride, p_slot_stride, z_slot_stride;  // bytes per expert
+    int a_mode;               // A_ROWS, or A_SWIGLU: slot j's activation is silu(gate) * up of g[j]
+    const float *gbuf;        // A_SWIGLU: fc1 output [slots][2 * K]
+    int swiglu_interleaved;
+    float *out_f32;           // slot outputs [slots][N] (QMoE), with bias added
+    const uint16_t *bias;     // fp16 [experts][N], or nullptr
+};
+
+enum { A_ROWS = 0, A_SWIGLU = 1 };
+
+template <int BITS>
+__host__ __device__ constexpr int pos_exp(int i) {
+    // bit position of code i of a 32-bit word after the single split shift:
+    // u2: codes 0..10 in place (bits 2i), codes 11..15 from word >> 22;
+    // u4: codes 0..4 in place (bits 4i), codes 5..7 from word >> 20.
+    return BITS == 2 ? (i < 11 ? 2 * i : 2 * (i - 11)) : (i < 5 ? 4 * i : 4 * (i - 5));
+}
+
+template <int VEC>
+__device__ __forceinline__ void load_words(const unsigned char *p, uint32_t (&x)[VEC / 4]) {
+    if constexpr (VEC == 16) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(p);
+        x[0] = v.x;
+        x[1] = v.y;
+        x[2] = v.z;
+        x[3] = v.w;
+    } else if constexpr (VEC == 8) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        x[0] = v.x;
+        x[1] = v.y;
+    } else {
+        x[0] = *reinterpret_cast<const uint32_t *>(p);
+    }
+}
+
+// acc[m] += sum over the codes of word x of ap[m][.] * (code as subnormal)
+template <int BITS, int MT, int KPL>
+__device__ __forceinline__ void dot_word_nbits(uint32_t x, const float (&ap)[MT][KPL], int j, float2 (&acc)[MT]) {
+    constexpr int CPW = 32 / BITS;
+    constexpr int LO = BITS == 2 ? 11 : 5;
+    constexpr int SH = BITS == 2 ? 22 : 20;
+    constexpr uint32_t MASK = (1u << BITS) - 1u;
+    const uint32_t xh = x >> SH;
+#pragma unroll
+    for (int i = 0; i < CPW; i += 2) {
+        const float f0 = __uint_as_float((i < LO ? x : xh) & (MASK << pos_exp<BITS>(i)));
+        const float f1 = __uint_as_float((i + 1 < LO ? x : xh) & (MASK << pos_exp<BITS>(i + 1)));
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+            acc[m] = ffma2(make_float2(ap[m][j * CPW + i], ap[m][j * CPW + i + 1]), make_float2(f0, f1), acc[m]);
+    }
+}
+
+// acc[m] += sum over the 8 codes of word x of ap[m][.] * C[code]; the
+// codebook sits in shared memory replicated per lane (entry q of lane l at
+// word q*32 + l), so the 32 lanes' lookups never share a bank.
+template <int MT, int KPL>
+__device__ __forceinline__ void dot_word_codebook(uint32_t x, const float (&ap)[MT][KPL], int j, float2 (&acc)[MT],
+                                                  const float *lut_lane) {
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+        const float c0 = lut_lane[((x >> (4 * i)) & 15u) * 32];
+        const float c1 = lut_lane[((x >> (4 * i + 4)) & 15u) * 32];
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+            acc[m] = ffma2(make_float2(ap[m][j * 8 + i], ap[m][j * 8 + i + 1]), make_float2(c0, c1), acc[m]);
+    }
+}
+
+// Fixed-order transposed reduction of V values held by each of the 32 lanes:
+// returns, on lane l, the 32-lane sum of value index l / (32 / V).
+template <int V>
+__device__ __forceinline__ float transpose_reduce(float (&v)[V], int lane) {
+#pragma unroll
+    for (int cnt = V, off = 16; cnt > 1; cnt >>= 1, off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int j = 0; j < cnt / 2; ++j) {
+            const float send = upper ? v[j] : v[j + cnt / 2];
+            const float keep = upper ? v[j + cnt / 2] : v[j];
+            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int off = 16 / V; off >= 1; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+    return r;
+}
+
+// Load (or reload, when the slot changes) this lane's activations.
+//  A_ROWS:   rows m0 .. m0+MT-1 of A[M][K] (fp32 / fp16 / bf16).
+//  A_SWIGLU: one row, h = silu(gate) * up of the fc1 output of slot `sl`
+//            (gate = g[0:K], up = g[K:2K], or the even / odd elements).
+// For MatMulNBits the values are then normalised by a power of two 2^E per
+// (lane, row) and pre-multiplied by 2^(126 - pos) for the subnormal-code
+// product; ahat holds the block sums of the normalised values.
+template <int BITS, int MT, int KPL, int BPL, int WK>
+__device__ __forceinline__ void load_activations(const GemvArgs &p, int sl, bool lane_active, int k0,
+                                                 float (&ap)[MT][KPL], float (&e2)[MT], float (&ahat)[MT][BPL]) {
+    constexpr int CPW = 32 / BITS;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        const int am = p.m0 + m;
+        const bool row_ok = lane_active && am < p.M;
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < KPL; ++i) {
+            float a = 0.f;
+            if (row_ok) {
+                if (p.a_mode == A_SWIGLU) {
+                    const float *gs = p.gbuf + static_cast<size_t>(sl) * 2 * p.K;
+                    const int c = k0 + i;
+                    const float gate = p.swiglu_interleaved ? gs[2 * c] : gs[c];
+                    const float up = p.swiglu_interleaved ? gs[2 * c + 1] : gs[p.K + c];
+                    a = gate / (1.f + expf(-gate)) * up;
+                } else {
+                    a = load_a_elem(p.A, p.a_dtype, static_cast<size_t>(am) * p.K + k0 + i);
+                }
+            }
+            ap[m][i] = a;
+            amax = fmaxf(amax, fabsf(a));
+        }
+        e2[m] = 1.f;
+#pragma unroll
+        for (int b = 0; b < BPL; ++b) ahat[m][b] = 0.f;
+        if constexpr (WK == WK_NBITS) {
+            const uint32_t ex = (__float_as_uint(amax) >> 23) & 0xFFu;
+            int E = ex == 0u ? -126 : (ex == 255u ? 0 : static_cast<int>(ex) - 127);
+            if (amax == 0.f) E = 0;
+            const float inv = exp2i(-E);
+            e2[m] = exp2i(E);
+#pragma unroll
+            for (int i = 0; i < KPL; ++i) {
+                const float ah = ap[m][i] * inv;
+                ahat[m][i / (KPL / BPL)] += ah;
+                ap[m][i] = ah * exp2i(126 - pos_exp<BITS>(i % CPW));
+            }
+        }
+    }
+}
+
+template <int BITS, int VEC, int MT, int BPL, int WK>
+__global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) gemv_kernel(const GemvArgs p) {
+    constexpr int CPW = 32 / BITS;
+    constexpr int WPL = VEC / 4;
+    constexpr int KPL = WPL * CPW;
+    constexpr int RPW = kRedV / MT;
+    constexpr int PB = WK == WK_CODEBOOK ? 4 : 2;  // bytes per block parameter
+    extern __shared__ __align__(1024) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + kMaxStages;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 2 * kMaxStages * 8);
+    float *lut = reinterpret_cast<float *>(smem + kLutOff);
+    float *red = reinterpret_cast<float *>(smem + p.red_off);
+    unsigned char *stages = smem + p.stage_off;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NWC = p.S_cta * p.G;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NWC);
+        }
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if constexpr (WK == WK_CODEBOOK) {
+        for (int i = threadIdx.x; i < 16 * 32; i += blockDim.x) lut[i] = __ldg(p.codebook + (i >> 5));
+    }
+    __syncthreads();
+
+    const bool split = gridDim.y > 1;
+    const int s_begin = blockIdx.y * p.S_cta;
+    const int s_count = min(p.S_cta, p.S_total - s_begin);
+    const int kc0 = split ? s_begin * 32 * KPL : 0;  // first k held in a stage row
+
+    // ------------------------------------------------------------ producer
+    if (warp == NWC) {
+        const int prow = p.nb * PB;
+        const int kb0 = kc0 * BITS / 8;
+        const int kb1 = split ? min(p.row_bytes, (s_begin + s_count) * 32 * VEC) : p.row_bytes;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++it) {
+            const int slot = it % p.NST;
+            const uint32_t par = ((it / p.NST) & 1) ^ 1;
+            if (!mbar_wait(&empty[slot], par, abort_flag, p.fault, FAULT_WAIT_EMPTY)) break;
+            const int sl = tile / p.tiles_per_slot;
+            const int r0 = (tile - sl * p.tiles_per_slot) * p.SR;
+            const int e = p.ids ? __ldg(p.ids + sl) : 0;
+            const bool valid = e >= 0 && e < p.num_experts;
+            const int rows = valid ? min(p.SR, p.N - r0) : 0;  // an invalid expert id copies nothing
+            const int es = valid ? e : 0;
+            const unsigned char *Wb = p.W + es * p.w_slot_stride;
+            const unsigned char *Pb = p.params + es * p.p_slot_stride;
+            const unsigned char *Zb = reinterpret_cast<const unsigned char *>(p.zp) + es * p.z_slot_stride;
+            unsigned char *st = stages + static_cast<size_t>(slot) * p.stage_bytes;
+            uint32_t tx = 0;
+            // codes
+            if (!split) {
+                const unsigned char *src = Wb + static_cast<size_t>(r0) * p.row_bytes;
+                const uint32_t bytes = static_cast<uint32_t>(rows) * p.row_bytes;
+                const CopyPlan cp = copy_plan(st, src, bytes);
+                copy_tail_lanes(st, src, bytes, cp, lane);
+                tx += cp.bulk_bytes;
+            } else {
+                for (int r = 0; r < rows; ++r) {
+                    const unsigned char *src = Wb + static_cast<size_t>(r0 + r) * p.row_bytes + kb0;
+                    unsigned char *dst = st + r * p.w_pitch;
+                    const CopyPlan cp = copy_plan(dst, src, kb1 - kb0);
+                    copy_tail_lanes(dst, src, kb1 - kb0, cp, lane);
+                    tx += cp.bulk_bytes;
+                }
+            }
+            // block parameters (scales or absmax), then zero points
+            {
+                const unsigned char *src = Pb + static_cast<size_t>(r0) * prow;
+                const CopyPlan cp = copy_plan(st + p.s_off, src, rows * prow);
+                copy_tail_lanes(st + p.s_off, src, rows * prow, cp, lane);
+                tx += cp.bulk_bytes;
+            }
+            if (p.zp_mode == ZP_TENSOR) {
+                const unsigned char *src = Zb + static_cast<size_t>(r0) * p.nb * 2;
+                const CopyPlan cp = copy_plan(st + p.z_off, src, rows * p.nb * 2);
+                copy_tail_lanes(st + p.z_off, src, rows * p.nb * 2, cp, lane);
+                tx += cp.bulk_bytes;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], tx);
+            __syncwarp();
+            // issue the bulk parts (after the expected byte count is registered)
+            if (!split) {
+                if (lane == 0) {
+                    const unsigned char *src = Wb + static_cast<size_t>(r0) * p.row_bytes;
+                    const CopyPlan cp = copy_plan(st, src, static_cast<uint32_t>(rows) * p.row_bytes);
+                    if (cp.bulk_bytes) bulk_g2s(st, src, cp.bulk_bytes, &full[slot]);
+                }
+            } else {
+                for (int r = lane; r < rows; r += 32) {
+                    const unsigned char *src = Wb + static_cast<size_t>(r0 + r) * p.row_bytes + kb0;
+                    unsigned char *dst = st + r * p.w_pitch;
+                    const CopyPlan cp = copy_plan(dst, src, kb1 - kb0);
+                    if (cp.bulk_bytes) bulk_g2s(dst, src, cp.bulk_bytes, &full[slot]);
+                }
+            }
+            if (lane == 1) {
+                const unsigned char *src = Pb + static_cast<size_t>(r0) * prow;
+                const CopyPlan cp = copy_plan(st + p.s_off, src, rows * prow);
+                if (cp.bulk_bytes) bulk_g2s(st + p.s_off, src, cp.bulk_bytes, &full[slot]);
+            }
+            if (lane == 2 && p.zp_mode == ZP_TENSOR) {
+                const unsigned char *src = Zb + static_cast<size_t>(r0) * p.nb * 2;
+                const CopyPlan cp = copy_plan(st + p.z_off, src, rows * p.nb * 2);
+                if (cp.bulk_bytes) bulk_g2s(st + p.z_off, src, cp.bulk_bytes, &full[slot]);
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ consumers
+    const int sigma = warp % p.S_cta, g = warp / p.S_cta;
+    const bool warp_active = sigma < s_count;
+    const int k0 = (s_begin + sigma) * 32 * KPL + lane * KPL;
+    const bool lane_active = warp_active && k0 < p.K;
+    const int lane_boff = (k0 - kc0) * BITS / 8;
+    const int blk0 = lane_active ? k0 / p.bs : 0;
+    const float *lut_lane = lut + lane;
+
+    // Activations of this lane's slice, for MT rows, kept in registers.
+    float ap[MT][KPL];
+    float e2[MT];
+    float ahat[MT][BPL];
+    int cur_slot = -1;
+
+    int it = 0;
+    for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++it) {
+        const int sl = tile / p.tiles_per_slot;
+        const int rbase = (tile - sl * p.tiles_per_slot) * p.SR;
+        const int e = p.ids ? __ldg(p.ids + sl) : 0;
+        const bool valid = e >= 0 && e < p.num_experts;
+        if (sl != cur_slot && (cur_slot < 0 || p.a_mode == A_SWIGLU)) {
+            load_activations<BITS, MT, KPL, BPL, WK>(p, sl, lane_active, k0, ap, e2, ahat);
+            cur_slot = sl;
+        }
+        const int slot = it % p.NST;
+        const uint32_t par = (it / p.NST) & 1;
+        const bool ok = mbar_wait(&full[slot], par, abort_flag, p.fault, FAULT_WAIT_FULL);
+        const unsigned char *st = stages + static_cast<size_t>(slot) * p.stage_bytes;
+        float racc[kRedV];
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+            const int rt = g * RPW + i;
+            const int row = rbase + rt;
+            float rv[MT];
+#pragma unroll
+            for (int m = 0; m < MT; ++m) rv[m] = 0.f;
+            if (ok && valid && lane_active && row < p.N) {
+                uint32_t x[WPL];
+                load_words<VEC>(st + rt * p.w_pitch + lane_boff, x);
+#pragma unroll
+                for (int b = 0; b < BPL; ++b) {
+                    float2 acc0[MT], acc1[MT];
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) acc0[m] = acc1[m] = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int j = b * (WPL / BPL); j < (b + 1) * (WPL / BPL); ++j) {
+                        if constexpr (WK == WK_NBITS) {
+                            if (j & 1) dot_word_nbits<BITS, MT, KPL>(x[j], ap, j, acc1);
+                            else dot_word_nbits<BITS, MT, KPL>(x[j], ap, j, acc0);
+                        } else {
+                            if (j & 1) dot_word_codebook<MT, KPL>(x[j], ap, j, acc1, lut_lane);
+                            else dot_word_codebook<MT, KPL>(x[j], ap, j, acc0, lut_lane);
+                        }
+                    }
+                    const int pidx = rt * p.nb + blk0 + b;
+                    if constexpr (WK == WK_NBITS) {
+                        const float s = h2f(*reinterpret_cast<const uint16_t *>(st + p.s_off + pidx * 2));
+                        const float z = p.zp_mode == ZP_TENSOR
+                                            ? h2f(*reinterpret_cast<const uint16_t *>(st + p.z_off + pidx * 2))
+                                            : p.zpv;
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            const float P = (acc0[m].x + acc0[m].y) + (acc1[m].x + acc1[m].y);
+                            const float t = fmaf(P, 8388608.f, -(z * ahat[m][b]));
+                            rv[m] = fmaf(s, t, rv[m]);
+                        }
+                    } else {
+                        const float am = *reinterpret_cast<const float *>(st + p.s_off + pidx * 4);
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            const float P = (acc0[m].x + acc0[m].y) + (acc1[m].x + acc1[m].y);
+                            rv[m] = fmaf(am, P, rv[m]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < MT; ++m) racc[i * MT + m] = rv[m] * e2[m];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+
+        const float tot = transpose_reduce<kRedV>(racc, lane);
+        float *redb = red + (it & 1) * (NWC * kRedV);
+        if ((lane & (32 / kRedV - 1)) == 0) redb[warp * kRedV + lane / (32 / kRedV)] = tot;
+        named_bar_sync(1, NWC * 32);
+        if (sigma == 0 && lane < kRedV) {
+            float sum = 0.f;
+            for (int s = 0; s < s_count; ++s) sum += redb[(g * p.S_cta + s) * kRedV + lane];
+            const int i = lane / MT, m = lane % MT;
+            const int row = rbase + g * RPW + i;
+            const int am = p.m0 + m;
+            if (row < p.N && am < p.M) {
+                if (p.out_f32) {
+                    float v = 0.f;
+                    if (valid) v = sum + (p.bias ? h2f(__ldg(reinterpret_cast<const unsigned short *>(p.bias) +
+                                                            static_cast<size_t>(e) * p.N + row))
+                                                 : 0.f);
+                    p.out_f32[static_cast<size_t>(sl) * p.N + row] = v;
+                } else if (p.partial) {
+                    p.partial[(static_cast<size_t>(blockIdx.y) * p.M + am) * p.N + row] = sum;
+                } else {
+                    store_y_elem(p.Y, p.y_dtype, static_cast<size_t>(am) * p.N + row, sum);
+                }
+            }
+        }
+    }
+}
+
+// Y = sum over splits of the partials, in split order.
+__global__ void splitk_reduce_kernel(const float *__restrict__ partial, int splits, size_t MN, void *Y, int y_dtype) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < MN;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        float s = 0.f;
+        for (int sp = 0; sp < splits; ++sp) s += partial[sp * MN + i];
+        store_y_elem(Y, y_dtype, i, s);
+    }
+}
+
+// QMoE: y[r] = fp16( sum_j w_j * o_j[r] ), slots summed in slot order; a slot
+// whose expert id is out of range adds nothing and sets *status to 1.
+__global__ void qmoe_combine_kernel(const float *__restrict__ o, const int32_t *__restrict__ ids,
+                                    const float *__restrict__ w, int k, int num_experts, int H, uint16_t *y,
+                                    int *status) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    int bad = 0;
+    float acc = 0.f;
+    for (int j = 0; j < k; ++j) {
+        const int e = __ldg(ids + j);
+        if (e < 0 || e >= num_experts) {
+            bad = 1;
+            continue;
+        }
+        if (r < H) acc = fmaf(__ldg(w + j), o[static_cast<size_t>(j) * H + r], acc);
+    }
+    if (r < H) y[r] = f2h(acc);
+    if (status && r == 0) *status = bad;
+}
+
+// ---------------------------------------------------------------- host side
+struct Cfg {
+    int vec, mt, bpl;
+    int S_total, S_cta, splits, G, SR, NST;
+    int w_pitch, stage_bytes, s_off, z_off, red_off, stage_off, smem, ntiles, grid_x;
+};
+
+inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
+
+// Static launch table: a pure function of the shape (no timing, no tuning).
+bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, Cfg &c) {
+    const DeviceInfo &di = device_info();
+    c.mt = M <= 1 ? 1 : (M <= 2 ? 2 : 4);
+    const int row_bytes = K * bits / 8;
+    const int pb = kind == WK_CODEBOOK ? 4 : 2;
+    const int nb = K / bs;
+    int cands[2];
+    int ncand = 0;
+    if (bits == 2) {
+        if (c.mt == 1) { cands[ncand++] = 16; cands[ncand++] = 8; }
+        else if (c.mt == 2) { cands[ncand++] = 8; cands[ncand++] = 4; }
+        else cands[ncand++] = 4;
+    } else {
+        if (c.mt <= 2) { cands[ncand++] = 16; cands[ncand++] = 8; }
+        else { cands[ncand++] = 8; cands[ncand++] = 4; }
+    }
+    // pick the vector width whose K-slices waste the fewest lanes
+    c.vec = 0;
+    long best_waste = -1;
+    for (int i = 0; i < ncand; ++i) {
+        const int v = cands[i];
+        if (row_bytes % v) continue;
+        const int sw = 32 * v * 8 / bits;
+        const long waste = static_cast<long>((K + sw - 1) / sw) * sw - K;
+        if (best_waste < 0 || waste < best_waste) {
+            best_waste = waste;
+            c.vec = v;
+        }
+    }
+    if (!c.vec) return false;
+    const int kpl = c.vec * 8 / bits;
+    c.bpl = kpl > bs ? kpl / bs : 1;
+    c.S_total = (K + 32 * kpl - 1) / (32 * kpl);
+    c.splits = (c.S_total + kMaxConsumerWarps - 1) / kMaxConsumerWarps;
+    c.S_cta = (c.S_total + c.splits - 1) / c.splits;
+    const int rpw = kRedV / c.mt;
+    c.G = std::max(1, kMaxConsumerWarps / c.S_cta);
+    // prefer stage heights that are multiples of 8 rows (16-byte aligned parameter tiles)
+    while (c.G > 1 && (c.G * rpw) % 8) --c.G;
+    c.w_pitch = c.splits > 1 ? round_up(c.S_cta * 32 * c.vec, 16) : row_bytes;
+    const int nwc = c.S_cta * c.G;
+    c.red_off = kLutOff + (kind == WK_CODEBOOK ? 16 * 32 * 4 : 0);
+    c.stage_off = round_up(c.red_off + 2 * nwc * kRedV * 4, 1024);
+    const int budget = di.max_smem_optin - c.stage_off;
+    for (;;) {
+        c.SR = c.G * rpw;
+        c.s_off = round_up(c.SR * c.w_pitch, 128);
+        c.z_off = c.s_off + round_up(c.SR * nb * pb, 128);
+        c.stage_bytes = c.z_off + (zp_tensor ? round_up(c.SR * nb * 2, 128) : 0);
+        c.NST = std::min(kMaxStages, budget / c.stage_bytes);
+        if (c.NST >= 3 || c.G == 1) break;
+        c.G = std::max(1, c.G / 2);
+    }
+    if (c.NST < 2) return false;
+    c.smem = c.stage_off + c.NST * c.stage_bytes;
+    c.ntiles = (N + c.SR - 1) / c.SR;
+    c.grid_x = std::min(c.ntiles, di.sm_count);
+    (void)M;
+    return true;
+}
+
+template <int BITS, int VEC, int MT, int BPL, int WK>
+cudaError_t launch_one(const GemvArgs &a, const Cfg &c, cudaStream_t s) {
+    auto kern = gemv_kernel<BITS, VEC, MT, BPL, WK>;
+    static std::atomic<unsigned> configured{0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const unsigned bit = 1u << (dev & 31);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             device_info().max_smem_optin);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    dim3 grid(c.grid_x, c.splits);
+    dim3 block((c.S_cta * c.G + 1) * 32);
+    kern<<<grid, block, c.smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t dispatch(const GemvArgs &a, const Cfg &c, int bits, int kind, cudaStream_t s) {
+#define QG_CASE(B, V, MT_, BPL_, WK_)                                                           \
+    if (bits == B && c.vec == V && c.mt == MT_ && c.bpl == BPL_ && kind == WK_) \
+        return launch_one<B, V, MT_, BPL_, WK_>(a, c, s);
+    QG_CASE(2, 16, 1, 1, WK_NBITS)
+    QG_CASE(2, 16, 1, 2, WK_NBITS)
+    QG_CASE(2, 8, 1, 1, WK_NBITS)
+    QG_CASE(2, 8, 2, 1, WK_NBITS)
+    QG_CASE(2, 4, 2, 1, WK_NBITS)
+    QG_CASE(2, 4, 4, 1, WK_NBITS)
+    QG_CASE(4, 16, 1, 1, WK_NBITS)
+    QG_CASE(4, 8, 1, 1, WK_NBITS)
+    QG_CASE(4, 16, 2, 1, WK_NBITS)
+    QG_CASE(4, 8, 2, 1, WK_NBITS)
+    QG_CASE(4, 8, 4, 1, WK_NBITS)
+    QG_CASE(4, 4, 4, 1, WK_NBITS)
+    QG_CASE(4, 16, 1, 1, WK_CODEBOOK)
+    QG_CASE(4, 8, 1, 1, WK_CODEBOOK)
+    QG_CASE(4, 16, 2, 1, WK_CODEBOOK)
+    QG_CASE(4, 8, 2, 1, WK_CODEBOOK)
+    QG_CASE(4, 8, 4, 1, WK_CODEBOOK)
+    QG_CASE(4, 4, 4, 1, WK_CODEBOOK)
+#undef QG_CASE
+    return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+size_t simt_workspace_bytes(int M, int N, int K, int bits, int bs) {
+    Cfg c;
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    // the zero-point mode does not change the split count
+    if (!choose_cfg(M, N, K, bits, bs, WK_NBITS, 1, c)) return 0;
+    return c.splits > 1 ? static_cast<size_t>(c.splits) * M * N * sizeof(float) : 0;
+}
+
+cudaError_t simt_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s) {
+    Cfg c;
+    if (!choose_cfg(p.M, p.N, p.K, p.bits, p.bs, p.kind, p.zp_mode == ZP_TENSOR, c)) return cudaErrorNotSupported;
+    GemvArgs a{};
+    a.A = p.A;
+    a.a_dtype = p.a_dtype;
+    a.W = p.W;
+    a.params = p.kind == WK_CODEBOOK ? reinterpret_cast<const unsigned char *>(p.absmax)
+                                     : reinterpret_cast<const unsigned char *>(p.scales);
+    a.zp = p.zp;
+    a.zp_mode = p.zp_mode;
+    a.zpv = p.uniform_zp;
+    a.codebook = p.codebook;
+    a.Y = p.Y;
+    a.y_dtype = p.y_dtype;
+    a.M = p.M;
+    a.N = p.N;
+    a.K = p.K;
+    a.bs = p.bs;
+    a.nb = p.K / p.bs;
+    a.row_bytes = p.K * p.bits / 8;
+    a.S_total = c.S_total;
+    a.S_cta = c.S_cta;
+    a.G = c.G;
+    a.SR = c.SR;
+    a.NST = c.NST;
+    a.w_pitch = c.w_pitch;
+    a.stage_bytes = c.stage_bytes;
+    a.s_off = c.s_off;
+    a.z_off = c.z_off;
+    a.red_off = c.red_off;
+    a.stage_off = c.stage_off;
+    a.ntiles = c.ntiles;
+    a.fault = fault_word();
+    a.tiles_per_slot = c.ntiles;
+    a.ids = nullptr;
+    a.num_experts = 1;
+    a.a_mode = A_ROWS;
+    if (c.splits > 1) {
+        const size_t need = static_cast<size_t>(c.splits) * p.M * p.N * sizeof(float);
+        if (!ws || ws_bytes < need) return cudaErrorInvalidValue;  // checked by the caller first
+        a.partial = static_cast<float *>(ws);
+    }
+    for (int m0 = 0; m0 < p.M; m0 += c.mt) {
+        a.m0 = m0;
+        cudaError_t e = dispatch(a, c, p.bits, p.kind, s);
+        if (e != cudaSuccess) return e;
+    }
+    if (c.splits > 1) {
+        const size_t MN = static_cast<size_t>(p.M) * p.N;
+        const int threads = 256;
+        const int blocks = static_cast<int>(std::min<size_t>((MN + threads - 1) / threads, 4096));
+        splitk_reduce_kernel<<<blocks, threads, 0, s>>>(a.partial, c.splits, MN, p.Y, p.y_dtype);
+        return cudaGetLastError();
+    }
+    return cudaSuccess;
+}
+
+size_t qmoe_workspace_bytes(int k, int hidden, int inter) {
+    if (k <= 0 || hidden <= 0 || inter <= 0) return 0;
+    const size_t g = (static_cast<size_t>(k) * 2 * inter * sizeof(float) + 255) / 256 * 256;
+    const size_t o = (static_cast<size_t>(k) * hidden * sizeof(float) + 255) / 256 * 256;
+    return g + o;
+}
+
+cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s) {
+    const DeviceInfo &di = device_info();
+    float *g = static_cast<float *>(ws);
+    float *o = reinterpret_cast<float *>(static_cast<char *>(ws) +
+                                         (static_cast<size_t>(q.k) * 2 * q.inter * sizeof(float) + 255) / 256 * 256);
+    const int mid = 1 << (q.bits - 1);
+    for (int stage = 0; stage < 2; ++stage) {
+        const bool fc1 = stage == 0;
+        const int N = fc1 ? 2 * q.inter : q.hidden;
+        const int K = fc1 ? q.hidden : q.inter;
+        const uint16_t *zp = fc1 ? q.fc1_zp : q.fc2_zp;
+        Cfg c;
+        if (!choose_cfg(1, N, K, q.bits, q.bs, WK_NBITS, zp != nullptr, c) || c.splits != 1)
+            return cudaErrorNotSupported;
+        GemvArgs a{};
+        a.A = q.x;
+        a.a_dtype = 1;  // fp16 token
+        a.W = fc1 ? q.fc1_w : q.fc2_w;
+        a.params = reinterpret_cast<const unsigned char *>(fc1 ? q.fc1_scales : q.fc2_scales);
+        a.zp = zp;
+        a.zp_mode = zp ? ZP_TENSOR : ZP_NONE;
+        a.zpv = static_cast<float>(mid);
+        a.M = 1;
+        a.N = N;
+        a.K = K;
+        a.bs = q.bs;
+        a.nb = K / q.bs;
+        a.row_bytes = K * q.bits / 8;
+        a.m0 = 0;
+        a.S_total = c.S_total;
+        a.S_cta = c.S_cta;
+        a.G = c.G;
+        a.SR = c.SR;
+        a.NST = c.NST;
+        a.w_pitch = c.w_pitch;
+        a.stage_bytes = c.stage_bytes;
+        a.s_off = c.s_off;
+        a.z_off = c.z_off;
+        a.red_off = c.red_off;
+        a.stage_off = c.stage_off;
+        a.tiles_per_slot = c.ntiles;
+        a.ntiles = c.ntiles * q.k;
+        a.fault = fault_word();
+        a.ids = q.ids;
+        a.num_experts = q.num_experts;
+        a.w_slot_stride = static_cast<size_t>(N) * a.row_bytes;
+        a.p_slot_stride = static_cast<size_t>(N) * a.nb * 2;
+        a.z_slot_stride = static_cast<size_t>(N) * a.nb * 2;
+        a.a_mode = fc1 ? A_ROWS : A_SWIGLU;
+        a.gbuf = g;
+        a.swiglu_interleaved = q.swiglu_interleaved;
+        a.out_f32 = fc1 ? g : o;
+        a.bias = fc1 ? q.fc1_bias : q.fc2_bias;
+        c.grid_x = std::min(a.ntiles, di.sm_count);
+        cudaError_t e = dispatch(a, c, q.bits, WK_NBITS, s);
+        if (e != cudaSuccess) return e;
+    }
+    const int threads = 256;
+    qmoe_combine_kernel<<<(q.hidden + threads - 1) / threads, threads, 0, s>>>(o, q.ids, q.weights, q.k,
+                                                                               q.num_experts, q.hidden, q.y,
+                                                                               q.status);
+    return cudaGetLastError();
+}
+
+}  // namespace qg

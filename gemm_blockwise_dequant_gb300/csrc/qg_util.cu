@@ -1,0 +1,99 @@
+// qg_util.cu -- dequantize-to-fp32 export and the fp16 uniform-value check.
+//
+// The export writes w[n][k] exactly as the GEMM kernels define it (two fp32
+// round-to-nearest operations for MatMulNBits, one for the codebook), so the
+// unpacking and dequantization can be checked bit for bit in isolation.
+// The uniform check backs the scalar zero-point path of hip-ep #1318
+// ("What", Commit 1: an all-equal fp16 zero-point tensor is detected once
+// per buffer and then passed as a scalar).
+#include "qg_device.cuh"
+#include "qg_internal.h"
+
+namespace qg {
+namespace {
+
+// One thread per 32-bit word of codes (16 u2 or 8 u4 codes).
+template <int BITS, int WK>
+__global__ void dequant_kernel(const uint8_t *__restrict__ W, const unsigned char *__restrict__ params,
+                               const uint16_t *__restrict__ zp, int zp_mode, float zpv,
+                               const float *__restrict__ codebook, float *__restrict__ out, int N, int K, int bs) {
+    constexpr int CPW = 32 / BITS;
+    constexpr uint32_t MASK = (1u << BITS) - 1u;
+    const int wpr = K / CPW;  // words per row
+    const int nb = K / bs;
+    const size_t total = static_cast<size_t>(N) * wpr;
+    for (size_t t = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; t < total;
+         t += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const int n = static_cast<int>(t / wpr);
+        const int wi = static_cast<int>(t % wpr);
+        const uint32_t x = __ldg(reinterpret_cast<const uint32_t *>(W + static_cast<size_t>(n) * (K * BITS / 8)) + wi);
+        const int kbase = wi * CPW;
+        const int b = kbase / bs;  // a word never straddles a block (bs >= 32 >= codes per word)
+        float *o = out + static_cast<size_t>(n) * K + kbase;
+        if constexpr (WK == WK_NBITS) {
+            const float s = h2f(__ldg(reinterpret_cast<const unsigned short *>(params) + static_cast<size_t>(n) * nb + b));
+            const float z = zp_mode == ZP_TENSOR ? h2f(__ldg(reinterpret_cast<const unsigned short *>(zp) + static_cast<size_t>(n) * nb + b)) : zpv;
+#pragma unroll
+            for (int i = 0; i < CPW; ++i) {
+                const float d = __fsub_rn(static_cast<float>((x >> (BITS * i)) & MASK), z);
+                o[i] = __fmul_rn(d, s);
+            }
+        } else {
+            const float am = __ldg(reinterpret_cast<const float *>(params) + static_cast<size_t>(n) * nb + b);
+#pragma unroll
+            for (int i = 0; i < CPW; ++i) o[i] = __fmul_rn(__ldg(codebook + ((x >> (4 * i)) & 15u)), am);
+        }
+    }
+}
+
+// ws[0] <- 1 if some element's bit pattern differs from t[0].  Every writer
+// stores the same value, so the result does not depend on the order.
+__global__ void uniform_kernel(const uint16_t *__restrict__ t, size_t n, unsigned *ws) {
+    const uint16_t v0 = __ldg(reinterpret_cast<const unsigned short *>(t));
+    bool diff = false;
+    const size_t n8 = n / 8;
+    const uint4 *t4 = reinterpret_cast<const uint4 *>(t);
+    const uint32_t pair = static_cast<uint32_t>(v0) | (static_cast<uint32_t>(v0) << 16);
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const uint4 v = __ldg(t4 + i);
+        diff |= (v.x != pair) | (v.y != pair) | (v.z != pair) | (v.w != pair);
+    }
+    for (size_t i = n8 * 8 + blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x)
+        diff |= __ldg(reinterpret_cast<const unsigned short *>(t) + i) != v0;
+    if (__syncthreads_or(diff) && threadIdx.x == 0) ws[0] = 1u;
+}
+
+}  // namespace
+
+cudaError_t launch_dequant(const GemmProblem &p, float *out, cudaStream_t s) {
+    const int cpw = 32 / p.bits;
+    const size_t total = static_cast<size_t>(p.N) * (p.K / cpw);
+    const int threads = 256;
+    const int blocks = static_cast<int>(std::min<size_t>((total + threads - 1) / threads, 65536));
+    if (total == 0) return cudaSuccess;
+    if (p.kind == WK_CODEBOOK)
+        dequant_kernel<4, WK_CODEBOOK><<<blocks, threads, 0, s>>>(
+            p.W, reinterpret_cast<const unsigned char *>(p.absmax), nullptr, 0, 0.f, p.codebook, out, p.N, p.K, p.bs);
+    else if (p.bits == 2)
+        dequant_kernel<2, WK_NBITS><<<blocks, threads, 0, s>>>(p.W, reinterpret_cast<const unsigned char *>(p.scales),
+                                                                p.zp, p.zp_mode, p.uniform_zp, nullptr, out, p.N,
+                                                                p.K, p.bs);
+    else
+        dequant_kernel<4, WK_NBITS><<<blocks, threads, 0, s>>>(p.W, reinterpret_cast<const unsigned char *>(p.scales),
+                                                                p.zp, p.zp_mode, p.uniform_zp, nullptr, out, p.N,
+                                                                p.K, p.bs);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_uniform_check(const uint16_t *t, size_t n, unsigned *ws, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(unsigned), s);
+    if (e != cudaSuccess) return e;
+    const int threads = 256;
+    const int blocks = static_cast<int>(std::min<size_t>((n / 8 + threads - 1) / threads + 1, 1024));
+    uniform_kernel<<<blocks, threads, 0, s>>>(t, n, ws);
+    return cudaGetLastError();
+}
+
+}  // namespace qg

@@ -1,0 +1,220 @@
+/*
+ * qgemm.h -- C ABI of the GB300 (sm_103a) blockwise low-bit dequantize +
+ * GEMV / small-M GEMM library, and of the fused single-token QMoE decode.
+ *
+ *     Y[M, N] = A[M, K] . dequant(W)[N, K]^T
+ *
+ * Sources (web pages, cited by title and section):
+ *   [hip-ep #1318]  hip-ep pull request #1318: 2-bit MatMulNBits kernels for
+ *                   phi4-14B on gfx1151.
+ *   [hip-ep #1328]  hip-ep pull request #1328: fused QMoE decode that picks
+ *                   its tiling before computing.
+ *   [bnb #1979]     bitsandbytes pull request #1979: "[ROCm] Fused 4-bit SIMT
+ *                   GEMM" (NF4/FP4 codebook weights).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every data pointer is a DEVICE pointer owned by the caller.  The library
+ *    never allocates, frees or synchronises (except qg_fp16_uniform_value and
+ *    qg_read_device_fault, which return a value to the host), and enqueues
+ *    work on `stream` only.  It keeps no per-call state between calls, so
+ *    concurrent calls on different streams with disjoint outputs and
+ *    workspaces are independent.
+ *  - Weight codes are packed along K, least significant bits first: element
+ *    k of row n is bits [(k*bits)%8, (k*bits)%8 + bits) of byte
+ *    n*(K*bits/8) + (k*bits)/8.  W is row-major [N][K*bits/8] bytes.
+ *  - Per-block parameters (fp16 scales, fp16 zero points, fp32 absmax) are
+ *    row-major [N][K/block_size].  fp16/bf16 tensors are passed as their
+ *    16-bit patterns (uint16_t).
+ *  - A is row-major and contiguous, [M][K] (the raw-pointer contract of
+ *    [bnb #1979], "Technical details", raw-pointer safety).  Y is row-major
+ *    [M][N] and is fully overwritten.
+ *  - Alignment: A, W, scales, zero points, absmax and the workspace must be
+ *    16-byte aligned; otherwise the call returns QG_ERR_INVALID_ARG.
+ *  - Block sizes 32, 64, 128 and 256 are supported, with K % block_size == 0.
+ *    Other block sizes (16 in particular, which [hip-ep #1328] "Notes for
+ *    reviewers" reports computing every output wrongly) are refused with
+ *    QG_ERR_UNSUPPORTED, never computed.
+ *  - Arguments are checked on the host before anything is enqueued; a refused
+ *    call launches nothing ([hip-ep #1328], "Test plan": arguments the
+ *    launchers must refuse).
+ *  - On entry the calling thread's pending, non-sticky CUDA error is cleared,
+ *    so an earlier unrelated failure is not reported as this call's failure;
+ *    after each launch the launch status is checked and returned as
+ *    QG_ERR_CUDA ([hip-ep #1328], "What": clear the error state before the
+ *    fused decode launches).
+ *  - Results are deterministic: every reduction runs in a fixed order that
+ *    depends only on the shape, never on timing, so repeated calls on the
+ *    same inputs are bit-identical ([hip-ep #1328], "Why" and "Test plan":
+ *    129 calls bit-identical).  Nothing is tuned or timed on live calls.
+ *  - M == 0 or N == 0 is a no-op.  K == 0 writes zeros.
+ */
+#ifndef QGEMM_H
+#define QGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st *qg_stream_t;
+
+/* Status codes returned by every entry point. */
+enum {
+    QG_OK = 0,
+    QG_ERR_INVALID_ARG = 1,          /* null/misaligned pointer, bad size, K % block_size != 0 */
+    QG_ERR_UNSUPPORTED = 2,          /* valid request this library does not implement (bits, block size, dtype combination) */
+    QG_ERR_CUDA = 3,                 /* a CUDA launch or copy failed; the CUDA error stays readable via cudaGetLastError */
+    QG_ERR_WORKSPACE_TOO_SMALL = 4   /* workspace_bytes below what *_workspace_bytes() returned for this shape */
+};
+
+/* Element types of A and Y. */
+enum { QG_F32 = 0, QG_F16 = 1, QG_BF16 = 2 };
+
+/*
+ * qgemm_nbits -- MatMulNBits: per-block fp16 scale and fp16 zero point.
+ *   [hip-ep #1318] "What", Commit 1 (u2 GEMV and WMMA kernels templated on
+ *   the A/C element types, reading fp32 A and writing fp32 C directly) and
+ *   "Performance", Model (block 64, fp16 scales and zero points).
+ *
+ *   w[n][k] = (q[n][k] - zp[n][k/bs]) * s[n][k/bs], computed exactly in fp32;
+ *   Y[m][n] = sum_k A[m][k] * w[n][k], accumulated in fp32 (tensor-core path:
+ *   the weight is rounded to A's 16-bit type before the product) and rounded
+ *   once to y_dtype.
+ *
+ *   A            [M][K], a_dtype (QG_F32, QG_F16 or QG_BF16)
+ *   W            [N][K*bits/8] packed codes, bits = 2 or 4
+ *   scales_f16   [N][K/block_size] fp16 patterns
+ *   zero_points_f16  [N][K/block_size] fp16 patterns, or NULL for the
+ *                midpoint 2^(bits-1)
+ *   Y            [M][N], y_dtype
+ *   workspace    device scratch of at least
+ *                qgemm_workspace_bytes(a_dtype, M, N, K, bits, block_size)
+ *                bytes (NULL allowed when that is 0); its contents on entry
+ *                do not matter and are garbage on return.
+ *   Returns a QG_* status.
+ */
+int qgemm_nbits(const void *A, int a_dtype, const uint8_t *W, const uint16_t *scales_f16,
+                const uint16_t *zero_points_f16, void *Y, int y_dtype, int M, int N, int K, int bits,
+                int block_size, void *workspace, size_t workspace_bytes, qg_stream_t stream);
+
+/*
+ * qgemm_nbits_uniform_zp -- as qgemm_nbits, with every zero point equal to
+ * the scalar `uniform_zp` ([hip-ep #1318] "What", Commit 1:
+ * hip_matmul_nbits_ex(..., float uniform_zp); "Why": fp16 zero points that
+ * are all 1.5 cost as many bytes per token as the scales).  The zero-point
+ * tensor is never read.  Bit-identical to qgemm_nbits with a full zero-point
+ * tensor holding the fp16 value uniform_zp.
+ */
+int qgemm_nbits_uniform_zp(const void *A, int a_dtype, const uint8_t *W, const uint16_t *scales_f16,
+                           float uniform_zp, void *Y, int y_dtype, int M, int N, int K, int bits,
+                           int block_size, void *workspace, size_t workspace_bytes, qg_stream_t stream);
+
+/*
+ * qgemm_codebook4 -- NF4/FP4-style weights: a 4-bit code selects one of 16
+ * fp32 codebook entries, multiplied by the block's fp32 absmax.
+ *   [bnb #1979] "Summary" (NF4/FP4 weights decoded inside the GEMM, decoded
+ *   values reused across the M rows) and "Technical details" (centroid
+ *   lookup).
+ *
+ *   w[n][k] = codebook16[q[n][k]] * absmax[n][k/bs]   (fp32)
+ *   codebook16  16 fp32 entries (device)
+ *   absmax      [N][K/block_size] fp32
+ *   Other arguments as qgemm_nbits (bits is 4).
+ */
+int qgemm_codebook4(const void *A, int a_dtype, const uint8_t *W, const float *codebook16, const float *absmax,
+                    void *Y, int y_dtype, int M, int N, int K, int block_size, void *workspace,
+                    size_t workspace_bytes, qg_stream_t stream);
+
+/* Workspace bytes the two GEMM entry points need for this shape (same value
+ * for qgemm_nbits, qgemm_nbits_uniform_zp and, with bits = 4,
+ * qgemm_codebook4).  0 means no workspace is needed. */
+size_t qgemm_workspace_bytes(int a_dtype, int M, int N, int K, int bits, int block_size);
+
+/*
+ * qmoe_decode_fused -- one token through the top-k experts of a quantized
+ * MoE layer: fc1 GEMV, SwiGLU, fc2 GEMV, weighted sum over the k slots.
+ *   [hip-ep #1328] "Summary" and "What" (hip_qmoe_decode_fused with
+ *   num_experts; u4 weights; block 32/64/128; zero points and bias
+ *   optional, "Test plan"); [hip-ep #1318] "Why" (the SwiGLU chain gate ->
+ *   sigmoid -> multiplies -> up).
+ *
+ *   For slot j = 0..k-1 in order, e = expert_ids[j]:
+ *     g = dequant(fc1[e]) . x + fc1_bias[e]                 (2*inter values)
+ *     gate, up = g[0:inter], g[inter:2*inter]  (swiglu_interleaved = 0)
+ *              = g[0::2],    g[1::2]           (swiglu_interleaved = 1)
+ *     h = silu(gate) * up                                    (kept in fp32)
+ *     o = dequant(fc2[e]) . h + fc2_bias[e]                  (hidden values)
+ *   y = round_to_fp16( sum_j expert_weights[j] * o_j ), summed in slot order.
+ *
+ *   x_f16        [hidden] fp16
+ *   expert_ids   [k] int32 (device); an id outside [0, num_experts) adds
+ *                nothing and sets *status_dev to 1 (status_dev may be NULL)
+ *   expert_weights [k] fp32 (device)
+ *   fc1_w        [num_experts][2*inter][hidden*bits/8]
+ *   fc1_scales   [num_experts][2*inter][hidden/block_size] fp16
+ *   fc1_zp       same shape as fc1_scales, or NULL (midpoint 2^(bits-1))
+ *   fc1_bias     [num_experts][2*inter] fp16, or NULL
+ *   fc2_w        [num_experts][hidden][inter*bits/8]
+ *   fc2_scales   [num_experts][hidden][inter/block_size] fp16
+ *   fc2_zp       same shape as fc2_scales, or NULL
+ *   fc2_bias     [num_experts][hidden] fp16, or NULL
+ *   bits         4 (2 is accepted too)
+ *   block_size   32, 64, 128 or 256; hidden and inter multiples of it
+ *   y_f16        [hidden] fp16 output
+ *   status_dev   device int written with 0 (all ids valid) or 1, or NULL
+ *   workspace    at least qmoe_decode_workspace_bytes(k, hidden, inter)
+ */
+int qmoe_decode_fused(const uint16_t *x_f16, const int32_t *expert_ids, const float *expert_weights, int k,
+                      int num_experts, const uint8_t *fc1_w, const uint16_t *fc1_scales, const uint16_t *fc1_zp,
+                      const uint16_t *fc1_bias, const uint8_t *fc2_w, const uint16_t *fc2_scales,
+                      const uint16_t *fc2_zp, const uint16_t *fc2_bias, int hidden, int inter, int bits,
+                      int block_size, int swiglu_interleaved, uint16_t *y_f16, int *status_dev, void *workspace,
+                      size_t workspace_bytes, qg_stream_t stream);
+
+size_t qmoe_decode_workspace_bytes(int k, int hidden, int inter);
+
+/*
+ * qg_fp16_uniform_value -- detect an fp16 tensor whose elements all have the
+ * same bit pattern ([hip-ep #1318] "What", Commit 1: the runtime detects an
+ * all-equal fp16 zero-point tensor once per buffer and then passes it as a
+ * scalar).  +0 and -0 differ; a NaN pattern is reported as not uniform; an
+ * empty tensor is not uniform.  Enqueues one kernel on `stream`, then
+ * synchronises the stream and writes *is_uniform (0/1) and, when uniform,
+ * *value (host pointers).  workspace: at least 16 bytes of device memory.
+ */
+int qg_fp16_uniform_value(const uint16_t *t, size_t n, int *is_uniform, float *value, void *workspace,
+                          size_t workspace_bytes, qg_stream_t stream);
+
+/*
+ * Dequantize to fp32 [N][K] (device), bit-exact with the definitions above.
+ * Used to check unpacking and dequantization in isolation, and as the
+ * "dequantize then dense GEMM" building block.
+ *   qg_dequant_nbits: zero_points_f16 may be NULL (midpoint).
+ */
+int qg_dequant_nbits(const uint8_t *W, const uint16_t *scales_f16, const uint16_t *zero_points_f16, float *out,
+                     int N, int K, int bits, int block_size, qg_stream_t stream);
+int qg_dequant_nbits_uniform_zp(const uint8_t *W, const uint16_t *scales_f16, float uniform_zp, float *out, int N,
+                                int K, int bits, int block_size, qg_stream_t stream);
+int qg_dequant_codebook4(const uint8_t *W, const float *codebook16, const float *absmax, float *out, int N, int K,
+                         int block_size, qg_stream_t stream);
+
+/*
+ * qg_read_device_fault -- every wait inside the library's kernels is
+ * bounded; a wait that gives up records a bit in a device-side fault word
+ * instead of hanging.  This call synchronises the current device, returns
+ * the word in *flags (0: no fault since the last read) and clears it.
+ */
+int qg_read_device_fault(unsigned int *flags);
+
+/* Human-readable name of a QG_* status. */
+const char *qg_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMM_H */
