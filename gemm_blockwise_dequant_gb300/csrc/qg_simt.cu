@@ -15,10 +15,11 @@
 //    tiles of SR whole rows (codes + per-block parameters) with 1-D bulk
 //    copies (TMA engine) into an NST-deep ring guarded by mbarriers, so the
 //    consumer warps never wait on HBM latency and hold no load registers.
-//  * Each consumer warp owns one K-slice (32 lanes x KPL consecutive k) and
-//    keeps the activations of that slice in registers for the whole kernel;
-//    it walks the rows of every stage.  Reading a lane's codes from shared
-//    memory is one conflict-free vector load.
+//  * Each consumer warp owns one K-slice and keeps the activations of that
+//    slice in registers for the whole kernel.  A slice is LPR lanes x KPL
+//    consecutive k; with LPR = 16 a warp works on two rows at once (one per
+//    half-warp), which lets 64 codes per lane tile K = 5120 without idle
+//    lanes.  A lane's codes of one row are one 16-byte shared-memory load.
 //  * Unpacking costs one LOP per code: a code masked in place inside its
 //    32-bit word IS an fp32 subnormal equal to q * 2^(pos - 149).  The
 //    activations are pre-scaled by 2^(126 - pos) (and by a per-lane power of
@@ -26,11 +27,14 @@
 //    codes accumulates a * q exactly as an ordinary FMA would.  The zero
 //    point and the scale are applied once per block per row:
 //        sum_k a_k (q_k - zp) s = s * (sum_k a_k q_k - zp * sum_k a_k).
-//  * Reductions run in a fixed order: a transposed butterfly over the 32
-//    lanes, then the K-slices of a row summed in slice order in shared
-//    memory, then (for very long K) split-K partials summed in split order by
-//    a second kernel.  No atomics, no dependence on timing: every call on the
-//    same inputs is bit-identical (hip-ep #1328, "Why").
+//  * The row loop has no data-dependent branches: lanes past the end of K
+//    read an in-bounds clamped address and are masked once per tile.
+//  * Reductions run in a fixed order: a transposed butterfly over the lanes
+//    of a row, then the K-slices of a row summed in slice order in shared
+//    memory (one named barrier per row group), then (for very long K)
+//    split-K partials summed in split order by a second kernel.  No atomics,
+//    no dependence on timing: every call on the same inputs is
+//    bit-identical (hip-ep #1328, "Why").
 //  * Every wait is bounded (see qg_device.cuh): a stuck pipeline records a
 //    fault bit and the kernel returns instead of hanging.
 #include <algorithm>
@@ -42,10 +46,15 @@
 namespace qg {
 namespace {
 
-constexpr int kMaxConsumerWarps = 12;
-constexpr int kRedV = 8;  // values per warp per stage entering the cross-lane reduction
 constexpr int kMaxStages = 8;
 constexpr int kLutOff = 256;
+
+// Most consumer warps a CTA may have (launch bound), by activation rows held.
+__host__ __device__ constexpr int max_consumer_warps(int mt) { return mt == 1 ? 15 : 11; }
+// Values each lane feeds into the per-tile transposed reduction.
+constexpr int kRedV = 8;
+
+enum { A_ROWS = 0, A_SWIGLU = 1 };
 
 struct GemvArgs {
     const void *A;
@@ -76,8 +85,6 @@ struct GemvArgs {
     float *out_f32;           // slot outputs [slots][N] (QMoE), with bias added
     const uint16_t *bias;     // fp16 [experts][N], or nullptr
 };
-
-enum { A_ROWS = 0, A_SWIGLU = 1 };
 
 template <int BITS>
 __host__ __device__ constexpr int pos_exp(int i) {
@@ -138,12 +145,14 @@ __device__ __forceinline__ void dot_word_codebook(uint32_t x, const float (&ap)[
     }
 }
 
-// Fixed-order transposed reduction of V values held by each of the 32 lanes:
-// returns, on lane l, the 32-lane sum of value index l / (32 / V).
-template <int V>
+// Fixed-order transposed reduction of V values held by each lane of an
+// LPR-lane group: returns, on lane l, the group sum of value index
+// (l % LPR) / (LPR / V).
+template <int V, int LPR>
 __device__ __forceinline__ float transpose_reduce(float (&v)[V], int lane) {
+    static_assert(V <= LPR, "one value per lane at most");
 #pragma unroll
-    for (int cnt = V, off = 16; cnt > 1; cnt >>= 1, off >>= 1) {
+    for (int cnt = V, off = LPR / 2; cnt > 1; cnt >>= 1, off >>= 1) {
         const bool upper = (lane & off) != 0;
 #pragma unroll
         for (int j = 0; j < cnt / 2; ++j) {
@@ -154,7 +163,7 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[V], int lane) {
     }
     float r = v[0];
 #pragma unroll
-    for (int off = 16 / V; off >= 1; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+    for (int off = LPR / V / 2; off >= 1; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
     return r;
 }
 
@@ -165,36 +174,86 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[V], int lane) {
 // For MatMulNBits the values are then normalised by a power of two 2^E per
 // (lane, row) and pre-multiplied by 2^(126 - pos) for the subnormal-code
 // product; ahat holds the block sums of the normalised values.
-template <int BITS, int MT, int KPL, int BPL, int WK>
+template <int BITS, int MT, int KPL, int BPL, int WK, int AM>
 __device__ __forceinline__ void load_activations(const GemvArgs &p, int sl, bool lane_active, int k0,
                                                  float (&ap)[MT][KPL], float (&e2)[MT], float (&ahat)[MT][BPL]) {
     constexpr int CPW = 32 / BITS;
+    static_assert(KPL % 8 == 0, "activation vectors are 8 elements");
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
         const int am = p.m0 + m;
         const bool row_ok = lane_active && am < p.M;
-        float amax = 0.f;
 #pragma unroll
-        for (int i = 0; i < KPL; ++i) {
-            float a = 0.f;
-            if (row_ok) {
-                if (p.a_mode == A_SWIGLU) {
-                    const float *gs = p.gbuf + static_cast<size_t>(sl) * 2 * p.K;
-                    const int c = k0 + i;
-                    const float gate = p.swiglu_interleaved ? gs[2 * c] : gs[c];
-                    const float up = p.swiglu_interleaved ? gs[2 * c + 1] : gs[p.K + c];
-                    a = gate / (1.f + expf(-gate)) * up;
-                } else {
-                    a = load_a_elem(p.A, p.a_dtype, static_cast<size_t>(am) * p.K + k0 + i);
+        for (int i = 0; i < KPL; ++i) ap[m][i] = 0.f;
+        if (row_ok) {
+            // every load of the lane's slice is issued before any is used (16-byte vectors)
+            if constexpr (AM == A_SWIGLU) {
+                // runs only when the slot changes; 8 values at a time to keep registers low
+                const float *gs = p.gbuf + static_cast<size_t>(sl) * 2 * p.K;
+#pragma unroll
+                for (int c = 0; c < KPL; c += 8) {
+                    float gate[8], up[8];
+                    if (p.swiglu_interleaved) {
+                        const float4 *q = reinterpret_cast<const float4 *>(gs + 2 * (k0 + c));
+                        const float4 v0 = q[0], v1 = q[1], v2 = q[2], v3 = q[3];
+                        gate[0] = v0.x; up[0] = v0.y; gate[1] = v0.z; up[1] = v0.w;
+                        gate[2] = v1.x; up[2] = v1.y; gate[3] = v1.z; up[3] = v1.w;
+                        gate[4] = v2.x; up[4] = v2.y; gate[5] = v2.z; up[5] = v2.w;
+                        gate[6] = v3.x; up[6] = v3.y; gate[7] = v3.z; up[7] = v3.w;
+                    } else {
+                        const float4 *qg = reinterpret_cast<const float4 *>(gs + k0 + c);
+                        const float4 *qu = reinterpret_cast<const float4 *>(gs + p.K + k0 + c);
+                        const float4 g0 = qg[0], g1 = qg[1], u0 = qu[0], u1 = qu[1];
+                        gate[0] = g0.x; gate[1] = g0.y; gate[2] = g0.z; gate[3] = g0.w;
+                        gate[4] = g1.x; gate[5] = g1.y; gate[6] = g1.z; gate[7] = g1.w;
+                        up[0] = u0.x; up[1] = u0.y; up[2] = u0.z; up[3] = u0.w;
+                        up[4] = u1.x; up[5] = u1.y; up[6] = u1.z; up[7] = u1.w;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) ap[m][c + i] = gate[i] / (1.f + expf(-gate[i])) * up[i];
+                }
+            } else if (p.a_dtype == 0) {
+                const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(p.A) +
+                                                                     static_cast<size_t>(am) * p.K + k0);
+                float4 v[KPL / 4];
+#pragma unroll
+                for (int j = 0; j < KPL / 4; ++j) v[j] = __ldg(src + j);
+#pragma unroll
+                for (int j = 0; j < KPL / 4; ++j) {
+                    ap[m][4 * j] = v[j].x;
+                    ap[m][4 * j + 1] = v[j].y;
+                    ap[m][4 * j + 2] = v[j].z;
+                    ap[m][4 * j + 3] = v[j].w;
+                }
+            } else {
+                const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.A) +
+                                                                   static_cast<size_t>(am) * p.K + k0);
+                uint4 v[KPL / 8];
+#pragma unroll
+                for (int j = 0; j < KPL / 8; ++j) v[j] = __ldg(src + j);
+                const bool f16 = p.a_dtype == 1;
+#pragma unroll
+                for (int j = 0; j < KPL / 8; ++j) {
+                    const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint16_t lo = static_cast<uint16_t>(w4[q] & 0xFFFFu), hi = static_cast<uint16_t>(w4[q] >> 16);
+                        ap[m][8 * j + 2 * q] = f16 ? h2f(lo) : bf2f(lo);
+                        ap[m][8 * j + 2 * q + 1] = f16 ? h2f(hi) : bf2f(hi);
+                    }
                 }
             }
-            ap[m][i] = a;
-            amax = fmaxf(amax, fabsf(a));
         }
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < KPL; ++i) amax = fmaxf(amax, fabsf(ap[m][i]));
         e2[m] = 1.f;
 #pragma unroll
         for (int b = 0; b < BPL; ++b) ahat[m][b] = 0.f;
         if constexpr (WK == WK_NBITS) {
+            // Normalise by a power of two so |a_hat| < 2, then fold in the
+            // code position: a' = a_hat * 2^(126 - pos); a' * subnormal(q at
+            // pos) = a_hat * q * 2^-23, exactly as with ordinary operands.
             const uint32_t ex = (__float_as_uint(amax) >> 23) & 0xFFu;
             int E = ex == 0u ? -126 : (ex == 255u ? 0 : static_cast<int>(ex) - 127);
             if (amax == 0.f) E = 0;
@@ -210,12 +269,13 @@ __device__ __forceinline__ void load_activations(const GemvArgs &p, int sl, bool
     }
 }
 
-template <int BITS, int VEC, int MT, int BPL, int WK>
-__global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) gemv_kernel(const GemvArgs p) {
+template <int BITS, int VEC, int MT, int BPL, int WK, int LPR, int AM>
+__global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_kernel(const GemvArgs p) {
     constexpr int CPW = 32 / BITS;
     constexpr int WPL = VEC / 4;
     constexpr int KPL = WPL * CPW;
-    constexpr int RPW = kRedV / MT;
+    constexpr int H = 32 / LPR;         // rows a warp works on at once
+    constexpr int ITER = kRedV / MT;    // row iterations per tile
     constexpr int PB = WK == WK_CODEBOOK ? 4 : 2;  // bytes per block parameter
     extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
@@ -230,7 +290,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) gemv_kernel(c
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.NST; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], NWC);
+            mbar_init(&empty[i], p.S_cta);  // released by the warps of the group that consumed it
         }
         *abort_flag = 0;
         mbar_fence_init();
@@ -243,13 +303,13 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) gemv_kernel(c
     const bool split = gridDim.y > 1;
     const int s_begin = blockIdx.y * p.S_cta;
     const int s_count = min(p.S_cta, p.S_total - s_begin);
-    const int kc0 = split ? s_begin * 32 * KPL : 0;  // first k held in a stage row
+    const int kc0 = split ? s_begin * LPR * KPL : 0;  // first k held in a stage row
 
     // ------------------------------------------------------------ producer
     if (warp == NWC) {
         const int prow = p.nb * PB;
         const int kb0 = kc0 * BITS / 8;
-        const int kb1 = split ? min(p.row_bytes, (s_begin + s_count) * 32 * VEC) : p.row_bytes;
+        const int kb1 = split ? min(p.row_bytes, (s_begin + s_count) * LPR * VEC) : p.row_bytes;
         int it = 0;
         for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++it) {
             const int slot = it % p.NST;
@@ -329,27 +389,39 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) gemv_kernel(c
 
     // ------------------------------------------------------------ consumers
     const int sigma = warp % p.S_cta, g = warp / p.S_cta;
+    const int half = lane / LPR, gl = lane % LPR;  // row within the warp's pair, lane within the row
     const bool warp_active = sigma < s_count;
-    const int k0 = (s_begin + sigma) * 32 * KPL + lane * KPL;
+    const int k0 = (s_begin + sigma) * LPR * KPL + gl * KPL;
     const bool lane_active = warp_active && k0 < p.K;
-    const int lane_boff = (k0 - kc0) * BITS / 8;
+    // lanes past the end of K read (in bounds) the start of the row and are masked per tile
+    const int lane_boff = lane_active ? (k0 - kc0) * BITS / 8 : 0;
     const int blk0 = lane_active ? k0 / p.bs : 0;
     const float *lut_lane = lut + lane;
+    const int row_stride = H * p.w_pitch;           // stage bytes between a lane's successive rows
+    const int prow_stride = H * p.nb * PB;          // same for the block parameters
+    const int zrow_stride = H * p.nb * 2;
 
     // Activations of this lane's slice, for MT rows, kept in registers.
     float ap[MT][KPL];
     float e2[MT];
     float ahat[MT][BPL];
+    float zah[MT][BPL];  // zp * ahat for a zero point that is the same for every row
     int cur_slot = -1;
 
-    int it = 0;
-    for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++it) {
+    // group g consumes the CTA's tiles g, g + G, g + 2G, ... (stage `it` holds tile it)
+    for (int it = g;; it += p.G) {
+        const int tile = blockIdx.x + it * gridDim.x;
+        if (tile >= p.ntiles) break;
         const int sl = tile / p.tiles_per_slot;
         const int rbase = (tile - sl * p.tiles_per_slot) * p.SR;
         const int e = p.ids ? __ldg(p.ids + sl) : 0;
         const bool valid = e >= 0 && e < p.num_experts;
-        if (sl != cur_slot && (cur_slot < 0 || p.a_mode == A_SWIGLU)) {
-            load_activations<BITS, MT, KPL, BPL, WK>(p, sl, lane_active, k0, ap, e2, ahat);
+        if (sl != cur_slot && (cur_slot < 0 || AM == A_SWIGLU)) {
+            load_activations<BITS, MT, KPL, BPL, WK, AM>(p, sl, lane_active, k0, ap, e2, ahat);
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int b = 0; b < BPL; ++b) zah[m][b] = p.zpv * ahat[m][b];
             cur_slot = sl;
         }
         const int slot = it % p.NST;
@@ -358,15 +430,19 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) gemv_kernel(c
         const unsigned char *st = stages + static_cast<size_t>(slot) * p.stage_bytes;
         float racc[kRedV];
 #pragma unroll
-        for (int i = 0; i < RPW; ++i) {
-            const int rt = g * RPW + i;
-            const int row = rbase + rt;
-            float rv[MT];
+        for (int v = 0; v < kRedV; ++v) racc[v] = 0.f;
+        if (ok && valid) {  // warp-uniform
+            const int rt0 = half;  // this lane's first row in the tile
+            const unsigned char *wp = st + rt0 * p.w_pitch + lane_boff;
+            const unsigned char *sp = st + p.s_off + (rt0 * p.nb + blk0) * PB;
+            const unsigned char *zpp = st + p.z_off + (rt0 * p.nb + blk0) * 2;
 #pragma unroll
-            for (int m = 0; m < MT; ++m) rv[m] = 0.f;
-            if (ok && valid && lane_active && row < p.N) {
+            for (int i = 0; i < ITER; ++i) {
                 uint32_t x[WPL];
-                load_words<VEC>(st + rt * p.w_pitch + lane_boff, x);
+                load_words<VEC>(wp, x);
+                float rv[MT];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) rv[m] = 0.f;
 #pragma unroll
                 for (int b = 0; b < BPL; ++b) {
                     float2 acc0[MT], acc1[MT];
@@ -382,20 +458,24 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) gemv_kernel(c
                             else dot_word_codebook<MT, KPL>(x[j], ap, j, acc0, lut_lane);
                         }
                     }
-                    const int pidx = rt * p.nb + blk0 + b;
                     if constexpr (WK == WK_NBITS) {
-                        const float s = h2f(*reinterpret_cast<const uint16_t *>(st + p.s_off + pidx * 2));
-                        const float z = p.zp_mode == ZP_TENSOR
-                                            ? h2f(*reinterpret_cast<const uint16_t *>(st + p.z_off + pidx * 2))
-                                            : p.zpv;
+                        const float s = h2f(*reinterpret_cast<const uint16_t *>(sp + b * 2));
+                        if (p.zp_mode == ZP_TENSOR) {
+                            const float z = h2f(*reinterpret_cast<const uint16_t *>(zpp + b * 2));
 #pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            const float P = (acc0[m].x + acc0[m].y) + (acc1[m].x + acc1[m].y);
-                            const float t = fmaf(P, 8388608.f, -(z * ahat[m][b]));
-                            rv[m] = fmaf(s, t, rv[m]);
+                            for (int m = 0; m < MT; ++m) {
+                                const float P = (acc0[m].x + acc0[m].y) + (acc1[m].x + acc1[m].y);
+                                rv[m] = fmaf(s, fmaf(P, 8388608.f, -(z * ahat[m][b])), rv[m]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int m = 0; m < MT; ++m) {
+                                const float P = (acc0[m].x + acc0[m].y) + (acc1[m].x + acc1[m].y);
+                                rv[m] = fmaf(s, fmaf(P, 8388608.f, -zah[m][b]), rv[m]);
+                            }
                         }
                     } else {
-                        const float am = *reinterpret_cast<const float *>(st + p.s_off + pidx * 4);
+                        const float am = *reinterpret_cast<const float *>(sp + b * 4);
 #pragma unroll
                         for (int m = 0; m < MT; ++m) {
                             const float P = (acc0[m].x + acc0[m].y) + (acc1[m].x + acc1[m].y);
@@ -403,30 +483,39 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) gemv_kernel(c
                         }
                     }
                 }
+#pragma unroll
+                for (int m = 0; m < MT; ++m) racc[i * MT + m] = rv[m] * e2[m];
+                wp += row_stride;
+                sp += prow_stride;
+                zpp += zrow_stride;
             }
 #pragma unroll
-            for (int m = 0; m < MT; ++m) racc[i * MT + m] = rv[m] * e2[m];
+            for (int v = 0; v < kRedV; ++v) racc[v] = lane_active ? racc[v] : 0.f;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
 
-        const float tot = transpose_reduce<kRedV>(racc, lane);
-        float *redb = red + (it & 1) * (NWC * kRedV);
-        if ((lane & (32 / kRedV - 1)) == 0) redb[warp * kRedV + lane / (32 / kRedV)] = tot;
-        named_bar_sync(1, NWC * 32);
-        if (sigma == 0 && lane < kRedV) {
+        // lane l now holds, for row half `half`, the slice sum of value (l % LPR) / (LPR / kRedV)
+        const float tot = transpose_reduce<kRedV, LPR>(racc, lane);
+        constexpr int VPW = kRedV * H;  // values per warp
+        // per group, double-buffered: [g][(it / G) & 1][slice][value]
+        float *redb = red + (g * 2 + ((it / p.G) & 1)) * (p.S_cta * VPW);
+        if ((gl & (LPR / kRedV - 1)) == 0) redb[sigma * VPW + half * kRedV + gl / (LPR / kRedV)] = tot;
+        named_bar_sync(1 + g, p.S_cta * 32);
+        if (sigma == 0 && lane < VPW) {
             float sum = 0.f;
-            for (int s = 0; s < s_count; ++s) sum += redb[(g * p.S_cta + s) * kRedV + lane];
-            const int i = lane / MT, m = lane % MT;
-            const int row = rbase + g * RPW + i;
+            for (int s = 0; s < s_count; ++s) sum += redb[s * VPW + lane];
+            const int hh = lane / kRedV, v = lane % kRedV;
+            const int i = v / MT, m = v % MT;
+            const int row = rbase + i * H + hh;
             const int am = p.m0 + m;
             if (row < p.N && am < p.M) {
                 if (p.out_f32) {
-                    float v = 0.f;
-                    if (valid) v = sum + (p.bias ? h2f(__ldg(reinterpret_cast<const unsigned short *>(p.bias) +
+                    float o = 0.f;
+                    if (valid) o = sum + (p.bias ? h2f(__ldg(reinterpret_cast<const unsigned short *>(p.bias) +
                                                             static_cast<size_t>(e) * p.N + row))
                                                  : 0.f);
-                    p.out_f32[static_cast<size_t>(sl) * p.N + row] = v;
+                    p.out_f32[static_cast<size_t>(sl) * p.N + row] = o;
                 } else if (p.partial) {
                     p.partial[(static_cast<size_t>(blockIdx.y) * p.M + am) * p.N + row] = sum;
                 } else {
@@ -469,7 +558,7 @@ __global__ void qmoe_combine_kernel(const float *__restrict__ o, const int32_t *
 
 // ---------------------------------------------------------------- host side
 struct Cfg {
-    int vec, mt, bpl;
+    int vec, lpr, mt, bpl;
     int S_total, S_cta, splits, G, SR, NST;
     int w_pitch, stage_bytes, s_off, z_off, red_off, stage_off, smem, ntiles, grid_x;
 };
@@ -477,59 +566,65 @@ struct Cfg {
 inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
 // Static launch table: a pure function of the shape (no timing, no tuning).
+// Per vector width / row-lane layout the cost is estimated as the issue work
+// per useful code: idle lanes of the last K-slice, the per-row bookkeeping
+// (about 12 instructions per lane and row) and, for layouts needing more
+// slices than fit in one CTA, a split-K penalty.
 bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, Cfg &c) {
     const DeviceInfo &di = device_info();
     c.mt = M <= 1 ? 1 : (M <= 2 ? 2 : 4);
+    const int maxw = max_consumer_warps(c.mt);
     const int row_bytes = K * bits / 8;
     const int pb = kind == WK_CODEBOOK ? 4 : 2;
     const int nb = K / bs;
-    int cands[2];
+    struct Cand { int vec, lpr; };
+    Cand cands[4];
     int ncand = 0;
     if (bits == 2) {
-        if (c.mt == 1) { cands[ncand++] = 16; cands[ncand++] = 8; }
-        else if (c.mt == 2) { cands[ncand++] = 8; cands[ncand++] = 4; }
-        else cands[ncand++] = 4;
+        if (c.mt == 1) { cands[ncand++] = {16, 32}; cands[ncand++] = {16, 16}; cands[ncand++] = {8, 32}; }
+        else if (c.mt == 2) { cands[ncand++] = {8, 32}; cands[ncand++] = {8, 16}; cands[ncand++] = {4, 32}; }
+        else { cands[ncand++] = {4, 32}; }
     } else {
-        if (c.mt <= 2) { cands[ncand++] = 16; cands[ncand++] = 8; }
-        else { cands[ncand++] = 8; cands[ncand++] = 4; }
+        if (c.mt <= 2) { cands[ncand++] = {16, 32}; cands[ncand++] = {16, 16}; cands[ncand++] = {8, 32}; }
+        else { cands[ncand++] = {8, 32}; cands[ncand++] = {4, 32}; }
     }
-    // pick the vector width whose K-slices waste the fewest lanes
+    double best = -1.0;
     c.vec = 0;
-    long best_waste = -1;
     for (int i = 0; i < ncand; ++i) {
-        const int v = cands[i];
+        const int v = cands[i].vec, l = cands[i].lpr;
         if (row_bytes % v) continue;
-        const int sw = 32 * v * 8 / bits;
-        const long waste = static_cast<long>((K + sw - 1) / sw) * sw - K;
-        if (best_waste < 0 || waste < best_waste) {
-            best_waste = waste;
+        const int kpl = v * 8 / bits;
+        const int sw = l * kpl;
+        const int st = (K + sw - 1) / sw;
+        const double lane_eff = static_cast<double>(K) / (static_cast<double>(st) * sw);
+        const double row_eff = static_cast<double>(kpl) / (kpl + 12.0);
+        const double split_pen = st > maxw ? 0.8 : 1.0;
+        const double score = lane_eff * row_eff * split_pen;
+        if (score > best + 1e-9) {
+            best = score;
             c.vec = v;
+            c.lpr = l;
         }
     }
     if (!c.vec) return false;
     const int kpl = c.vec * 8 / bits;
     c.bpl = kpl > bs ? kpl / bs : 1;
-    c.S_total = (K + 32 * kpl - 1) / (32 * kpl);
-    c.splits = (c.S_total + kMaxConsumerWarps - 1) / kMaxConsumerWarps;
+    c.S_total = (K + c.lpr * kpl - 1) / (c.lpr * kpl);
+    c.splits = (c.S_total + maxw - 1) / maxw;
     c.S_cta = (c.S_total + c.splits - 1) / c.splits;
-    const int rpw = kRedV / c.mt;
-    c.G = std::max(1, kMaxConsumerWarps / c.S_cta);
-    // prefer stage heights that are multiples of 8 rows (16-byte aligned parameter tiles)
-    while (c.G > 1 && (c.G * rpw) % 8) --c.G;
-    c.w_pitch = c.splits > 1 ? round_up(c.S_cta * 32 * c.vec, 16) : row_bytes;
+    // a stage holds one tile of SR rows; the G row groups of consumer warps take
+    // stages in turn, so the stage size does not grow with the number of warps
+    c.SR = (kRedV / c.mt) * (32 / c.lpr);
+    c.G = std::max(1, maxw / c.S_cta);
+    c.w_pitch = c.splits > 1 ? round_up(c.S_cta * c.lpr * c.vec, 16) : row_bytes;
     const int nwc = c.S_cta * c.G;
     c.red_off = kLutOff + (kind == WK_CODEBOOK ? 16 * 32 * 4 : 0);
-    c.stage_off = round_up(c.red_off + 2 * nwc * kRedV * 4, 1024);
+    c.stage_off = round_up(c.red_off + 2 * nwc * 32 * 4, 1024);
     const int budget = di.max_smem_optin - c.stage_off;
-    for (;;) {
-        c.SR = c.G * rpw;
-        c.s_off = round_up(c.SR * c.w_pitch, 128);
-        c.z_off = c.s_off + round_up(c.SR * nb * pb, 128);
-        c.stage_bytes = c.z_off + (zp_tensor ? round_up(c.SR * nb * 2, 128) : 0);
-        c.NST = std::min(kMaxStages, budget / c.stage_bytes);
-        if (c.NST >= 3 || c.G == 1) break;
-        c.G = std::max(1, c.G / 2);
-    }
+    c.s_off = round_up(c.SR * c.w_pitch, 128);
+    c.z_off = c.s_off + round_up(c.SR * nb * pb, 128);
+    c.stage_bytes = c.z_off + (zp_tensor ? round_up(c.SR * nb * 2, 128) : 0);
+    c.NST = std::min(kMaxStages, budget / c.stage_bytes);
     if (c.NST < 2) return false;
     c.smem = c.stage_off + c.NST * c.stage_bytes;
     c.ntiles = (N + c.SR - 1) / c.SR;
@@ -538,9 +633,9 @@ bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, 
     return true;
 }
 
-template <int BITS, int VEC, int MT, int BPL, int WK>
+template <int BITS, int VEC, int MT, int BPL, int WK, int LPR, int AM>
 cudaError_t launch_one(const GemvArgs &a, const Cfg &c, cudaStream_t s) {
-    auto kern = gemv_kernel<BITS, VEC, MT, BPL, WK>;
+    auto kern = gemv_kernel<BITS, VEC, MT, BPL, WK, LPR, AM>;
     static std::atomic<unsigned> configured{0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -558,29 +653,68 @@ cudaError_t launch_one(const GemvArgs &a, const Cfg &c, cudaStream_t s) {
 }
 
 cudaError_t dispatch(const GemvArgs &a, const Cfg &c, int bits, int kind, cudaStream_t s) {
-#define QG_CASE(B, V, MT_, BPL_, WK_)                                                           \
-    if (bits == B && c.vec == V && c.mt == MT_ && c.bpl == BPL_ && kind == WK_) \
-        return launch_one<B, V, MT_, BPL_, WK_>(a, c, s);
-    QG_CASE(2, 16, 1, 1, WK_NBITS)
-    QG_CASE(2, 16, 1, 2, WK_NBITS)
-    QG_CASE(2, 8, 1, 1, WK_NBITS)
-    QG_CASE(2, 8, 2, 1, WK_NBITS)
-    QG_CASE(2, 4, 2, 1, WK_NBITS)
-    QG_CASE(2, 4, 4, 1, WK_NBITS)
-    QG_CASE(4, 16, 1, 1, WK_NBITS)
-    QG_CASE(4, 8, 1, 1, WK_NBITS)
-    QG_CASE(4, 16, 2, 1, WK_NBITS)
-    QG_CASE(4, 8, 2, 1, WK_NBITS)
-    QG_CASE(4, 8, 4, 1, WK_NBITS)
-    QG_CASE(4, 4, 4, 1, WK_NBITS)
-    QG_CASE(4, 16, 1, 1, WK_CODEBOOK)
-    QG_CASE(4, 8, 1, 1, WK_CODEBOOK)
-    QG_CASE(4, 16, 2, 1, WK_CODEBOOK)
-    QG_CASE(4, 8, 2, 1, WK_CODEBOOK)
-    QG_CASE(4, 8, 4, 1, WK_CODEBOOK)
-    QG_CASE(4, 4, 4, 1, WK_CODEBOOK)
+#define QG_CASE(B, V, MT_, BPL_, WK_, L_)                                                                 \
+    if (bits == B && c.vec == V && c.mt == MT_ && c.bpl == BPL_ && kind == WK_ && c.lpr == L_) \
+        return a.a_mode == A_ROWS ? launch_one<B, V, MT_, BPL_, WK_, L_, A_ROWS>(a, c, s) : cudaErrorNotSupported;
+#define QG_CASE_SW(B, V, BPL_, L_)                                                                    \
+    if (bits == B && c.vec == V && c.mt == 1 && c.bpl == BPL_ && kind == WK_NBITS && c.lpr == L_ && \
+        a.a_mode == A_SWIGLU)                                                                      \
+        return launch_one<B, V, 1, BPL_, WK_NBITS, L_, A_SWIGLU>(a, c, s);
+    // fused QMoE fc2 (activations = SwiGLU of fc1's output)
+    QG_CASE_SW(4, 16, 1, 32)
+    QG_CASE_SW(4, 16, 1, 16)
+    QG_CASE_SW(4, 8, 1, 32)
+    QG_CASE_SW(2, 16, 1, 32)
+    QG_CASE_SW(2, 16, 1, 16)
+    QG_CASE_SW(2, 16, 2, 32)
+    QG_CASE_SW(2, 16, 2, 16)
+    QG_CASE_SW(2, 8, 1, 32)
+    // MatMulNBits u2
+    QG_CASE(2, 16, 1, 1, WK_NBITS, 32)
+    QG_CASE(2, 16, 1, 1, WK_NBITS, 16)
+    QG_CASE(2, 16, 1, 2, WK_NBITS, 32)
+    QG_CASE(2, 16, 1, 2, WK_NBITS, 16)
+    QG_CASE(2, 8, 1, 1, WK_NBITS, 32)
+    QG_CASE(2, 8, 2, 1, WK_NBITS, 32)
+    QG_CASE(2, 8, 2, 1, WK_NBITS, 16)
+    QG_CASE(2, 4, 2, 1, WK_NBITS, 32)
+    QG_CASE(2, 4, 4, 1, WK_NBITS, 32)
+    // MatMulNBits u4
+    QG_CASE(4, 16, 1, 1, WK_NBITS, 32)
+    QG_CASE(4, 16, 1, 1, WK_NBITS, 16)
+    QG_CASE(4, 8, 1, 1, WK_NBITS, 32)
+    QG_CASE(4, 16, 2, 1, WK_NBITS, 32)
+    QG_CASE(4, 16, 2, 1, WK_NBITS, 16)
+    QG_CASE(4, 8, 2, 1, WK_NBITS, 32)
+    QG_CASE(4, 8, 4, 1, WK_NBITS, 32)
+    QG_CASE(4, 4, 4, 1, WK_NBITS, 32)
+    // codebook (NF4 / FP4)
+    QG_CASE(4, 16, 1, 1, WK_CODEBOOK, 32)
+    QG_CASE(4, 16, 1, 1, WK_CODEBOOK, 16)
+    QG_CASE(4, 8, 1, 1, WK_CODEBOOK, 32)
+    QG_CASE(4, 16, 2, 1, WK_CODEBOOK, 32)
+    QG_CASE(4, 16, 2, 1, WK_CODEBOOK, 16)
+    QG_CASE(4, 8, 2, 1, WK_CODEBOOK, 32)
+    QG_CASE(4, 8, 4, 1, WK_CODEBOOK, 32)
+    QG_CASE(4, 4, 4, 1, WK_CODEBOOK, 32)
 #undef QG_CASE
+#undef QG_CASE_SW
     return cudaErrorNotSupported;
+}
+
+void fill_args(GemvArgs &a, const Cfg &c) {
+    a.S_total = c.S_total;
+    a.S_cta = c.S_cta;
+    a.G = c.G;
+    a.SR = c.SR;
+    a.NST = c.NST;
+    a.w_pitch = c.w_pitch;
+    a.stage_bytes = c.stage_bytes;
+    a.s_off = c.s_off;
+    a.z_off = c.z_off;
+    a.red_off = c.red_off;
+    a.stage_off = c.stage_off;
+    a.fault = fault_word();
 }
 
 }  // namespace
@@ -588,7 +722,7 @@ cudaError_t dispatch(const GemvArgs &a, const Cfg &c, int bits, int kind, cudaSt
 size_t simt_workspace_bytes(int M, int N, int K, int bits, int bs) {
     Cfg c;
     if (M <= 0 || N <= 0 || K <= 0) return 0;
-    // the zero-point mode does not change the split count
+    // the zero-point mode and the weight kind do not change the split count
     if (!choose_cfg(M, N, K, bits, bs, WK_NBITS, 1, c)) return 0;
     return c.splits > 1 ? static_cast<size_t>(c.splits) * M * N * sizeof(float) : 0;
 }
@@ -614,19 +748,8 @@ cudaError_t simt_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStrea
     a.bs = p.bs;
     a.nb = p.K / p.bs;
     a.row_bytes = p.K * p.bits / 8;
-    a.S_total = c.S_total;
-    a.S_cta = c.S_cta;
-    a.G = c.G;
-    a.SR = c.SR;
-    a.NST = c.NST;
-    a.w_pitch = c.w_pitch;
-    a.stage_bytes = c.stage_bytes;
-    a.s_off = c.s_off;
-    a.z_off = c.z_off;
-    a.red_off = c.red_off;
-    a.stage_off = c.stage_off;
+    fill_args(a, c);
     a.ntiles = c.ntiles;
-    a.fault = fault_word();
     a.tiles_per_slot = c.ntiles;
     a.ids = nullptr;
     a.num_experts = 1;
@@ -687,20 +810,9 @@ cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s) {
         a.nb = K / q.bs;
         a.row_bytes = K * q.bits / 8;
         a.m0 = 0;
-        a.S_total = c.S_total;
-        a.S_cta = c.S_cta;
-        a.G = c.G;
-        a.SR = c.SR;
-        a.NST = c.NST;
-        a.w_pitch = c.w_pitch;
-        a.stage_bytes = c.stage_bytes;
-        a.s_off = c.s_off;
-        a.z_off = c.z_off;
-        a.red_off = c.red_off;
-        a.stage_off = c.stage_off;
+        fill_args(a, c);
         a.tiles_per_slot = c.ntiles;
         a.ntiles = c.ntiles * q.k;
-        a.fault = fault_word();
         a.ids = q.ids;
         a.num_experts = q.num_experts;
         a.w_slot_stride = static_cast<size_t>(N) * a.row_bytes;
