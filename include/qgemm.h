@@ -178,6 +178,34 @@ int qmoe_decode_fused(const uint16_t *x_f16, const int32_t *expert_ids, const fl
 size_t qmoe_decode_workspace_bytes(int k, int hidden, int inter);
 
 /*
+ * qmoe_decode_fused_noalloc -- qmoe_decode_fused for callers that cannot
+ * allocate device memory (a decode loop inside a runtime that forbids
+ * allocation on its hot path, an embedded host that must not allocate after
+ * start-up, a C caller without an allocator).  The source pages have no
+ * counterpart: this is an addition of this library.
+ *
+ * Same arguments and results as qmoe_decode_fused, minus the workspace: the
+ * scratch is a fixed device array of QG_QMOE_NOALLOC_SCRATCH_BYTES inside the
+ * library, held by every GPU that loads it until the process exits.  Shapes
+ * needing more, i.e. qmoe_decode_workspace_bytes(k, hidden, inter) >
+ * QG_QMOE_NOALLOC_SCRATCH_BYTES, are refused with QG_ERR_UNSUPPORTED before
+ * anything is enqueued.  Calls no cudaMalloc, cudaFree or other allocator.
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before any
+ *    stream capture.
+ *  - All calls on a device share the one array: calls that can overlap on
+ *    the GPU (unordered streams) race.  The array keeps the last call's
+ *    contents; no call depends on them.
+ */
+#define QG_QMOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+int qmoe_decode_fused_noalloc(const uint16_t *x_f16, const int32_t *expert_ids, const float *expert_weights, int k,
+                              int num_experts, const uint8_t *fc1_w, const uint16_t *fc1_scales,
+                              const uint16_t *fc1_zp, const uint16_t *fc1_bias, const uint8_t *fc2_w,
+                              const uint16_t *fc2_scales, const uint16_t *fc2_zp, const uint16_t *fc2_bias,
+                              int hidden, int inter, int bits, int block_size, int swiglu_interleaved,
+                              uint16_t *y_f16, int *status_dev, qg_stream_t stream);
+
+/*
  * qg_fp16_uniform_value -- detect an fp16 tensor whose elements all have the
  * same bit pattern ([hip-ep #1318] "What", Commit 1: the runtime detects an
  * all-equal fp16 zero-point tensor once per buffer and then passes it as a
