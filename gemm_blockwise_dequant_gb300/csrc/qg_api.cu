@@ -72,7 +72,7 @@ constexpr long long kMaxM = 1 << 20;
 
 size_t gemm_workspace(int a_dtype, int M, int N, int K, int bits, int bs) {
     if (M <= 0 || N <= 0 || K <= 0 || (bits != 2 && bits != 4) || !valid_bs(bs) || K % bs) return 0;
-    if (qg::tc_eligible(M, K, bits, a_dtype)) return qg::tc_workspace_bytes(M, N, K, bits);
+    if (qg::tc_eligible(M, K, bits, a_dtype, bs)) return qg::tc_workspace_bytes(M, N, K, bits);
     return qg::simt_workspace_bytes(M, N, K, bits, bs);
 }
 
@@ -110,7 +110,7 @@ int run_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s) {
             return QG_ERR_CUDA;
         return QG_OK;
     }
-    const cudaError_t e = qg::tc_eligible(p.M, p.K, p.bits, p.a_dtype) ? qg::tc_gemm(p, ws, ws_bytes, s)
+    const cudaError_t e = qg::tc_eligible(p.M, p.K, p.bits, p.a_dtype, p.bs) ? qg::tc_gemm(p, ws, ws_bytes, s)
                                                                        : qg::simt_gemm(p, ws, ws_bytes, s);
     if (e == cudaErrorNotSupported) return QG_ERR_UNSUPPORTED;
     return e == cudaSuccess ? QG_OK : QG_ERR_CUDA;

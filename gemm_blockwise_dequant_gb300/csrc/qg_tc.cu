@@ -46,9 +46,11 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
-constexpr int kThreads = 192;
-constexpr int kDequantThreads = 128;
+// pipeline depth: 4 stages, 3 for the widest tile (shared-memory budget)
+__host__ __device__ constexpr int stages_for(int bn) { return bn >= 256 ? 3 : 4; }
+constexpr int kThreads = 320;         // warp 0 TMA, warp 1 MMA, warps 2-9 dequant + epilogue
+constexpr int kDequantThreads = 256;
+constexpr int kParamBox = 16;         // bytes of block parameters per weight row per stage (one TMA box column)
 
 struct TcArgs {
     const uint16_t *scales;  // nbits, [N][nb] fp16
@@ -203,11 +205,16 @@ __device__ __forceinline__ uint4 dequant8_codebook(uint32_t codes, float am, con
 template <int WK, int BITS, bool BF16, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constant__ CUtensorMap code_map,
+                   const __grid_constant__ CUtensorMap par_map, const __grid_constant__ CUtensorMap zp_map,
                    const TcArgs p) {
+    constexpr int kStages = stages_for(BN);
     constexpr int CB = kBK * BITS / 8;           // code bytes per row per stage
     constexpr int ACT_BYTES = kBM * kBK * 2;     // 16 KB
     constexpr int WDQ_BYTES = BN * kBK * 2;
     constexpr int CODE_BYTES = BN * CB;
+    constexpr int PAR_BYTES = BN * kParamBox;
+    constexpr int PE = WK == WK_CODEBOOK ? 4 : 2;  // bytes per block parameter
+    constexpr int PPB = kParamBox / PE;            // parameters per box row
     constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte alignment for the swizzled tiles
@@ -215,7 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char *act_s = smem;
     unsigned char *wdq_s = act_s + kStages * ACT_BYTES;
     unsigned char *code_s = wdq_s + kStages * WDQ_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(code_s + kStages * CODE_BYTES);
+    unsigned char *par_s = code_s + kStages * CODE_BYTES;
+    unsigned char *zp_s = par_s + kStages * PAR_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(zp_s + kStages * PAR_BYTES);
     uint64_t *full = bars;                 // TMA landed (count 1 + tx)
     uint64_t *wfull = bars + kStages;      // dequantized weights written (count 4 warps)
     uint64_t *empty = bars + 2 * kStages;  // MMAs of the stage finished (commit)
@@ -233,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&wfull[s], 4);
+            mbar_init(&wfull[s], kDequantThreads / 32);
             mbar_init(&empty[s], 1);
         }
         mbar_init(accf, 1);
@@ -255,10 +264,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < nks; ++i) {
                 const int s = i % kStages;
                 if (!mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1, abort_flag, p.fault, FAULT_WAIT_TC)) break;
-                mbar_arrive_expect_tx(&full[s], ACT_BYTES + CODE_BYTES);
+                const bool zt = WK == WK_NBITS && p.zp_mode == ZP_TENSOR;
+                mbar_arrive_expect_tx(&full[s], ACT_BYTES + CODE_BYTES + PAR_BYTES * (zt ? 2 : 1));
                 const int ks = ks0 + i;
+                const int pcol = (ks * kBK / p.bs) / PPB * PPB;  // first parameter column of the box
                 tma_load_2d(act_s + s * ACT_BYTES, &act_map, ks * kBK, m0, &full[s]);
                 tma_load_2d(code_s + s * CODE_BYTES, &code_map, ks * CB, n0, &full[s]);
+                tma_load_2d(par_s + s * PAR_BYTES, &par_map, pcol, n0, &full[s]);
+                if (zt) tma_load_2d(zp_s + s * PAR_BYTES, &zp_map, pcol, n0, &full[s]);
             }
         }
     } else if (warp == 1) {
@@ -284,13 +297,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ dequant warps
-        const int t = threadIdx.x - 64;  // 0 .. 127
+        const int t = threadIdx.x - 64;  // 0 .. kDequantThreads-1
         const float *lut_lane = lut + lane;
         for (int i = 0; i < nks; ++i) {
             const int s = i % kStages;
             if (!mbar_wait(&full[s], (i / kStages) & 1, abort_flag, p.fault, FAULT_WAIT_TC)) break;
             const int kb = (ks0 + i) * kBK;
+            const int pcol = (kb / p.bs) / PPB * PPB;
             const unsigned char *cs = code_s + s * CODE_BYTES;
+            const unsigned char *ps = par_s + s * PAR_BYTES;
+            const unsigned char *zs = zp_s + s * PAR_BYTES;
             unsigned char *ws = wdq_s + s * WDQ_BYTES;
 #pragma unroll 4
             for (int u = t; u < BN * 8; u += kDequantThreads) {
@@ -298,20 +314,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n = n0 + r, k = kb + 8 * c;
                 uint4 w = make_uint4(0u, 0u, 0u, 0u);
                 if (n < p.N && k < p.K) {
-                    const int b = k / p.bs;
-                    const size_t pi = static_cast<size_t>(n) * p.nb + b;
+                    const int pc = k / p.bs - pcol;  // column inside the stage's parameter box
                     if constexpr (WK == WK_NBITS) {
                         const uint32_t codes = BITS == 2
                                                    ? static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(cs + r * CB + c * 2))
                                                    : *reinterpret_cast<const uint32_t *>(cs + r * CB + c * 4);
-                        const __half s1 = __ushort_as_half(__ldg(reinterpret_cast<const unsigned short *>(p.scales) + pi));
+                        const __half s1 = __ushort_as_half(*reinterpret_cast<const unsigned short *>(ps + r * kParamBox + pc * 2));
                         const __half z1 = p.zp_mode == ZP_TENSOR
-                                              ? __ushort_as_half(__ldg(reinterpret_cast<const unsigned short *>(p.zp) + pi))
+                                              ? __ushort_as_half(*reinterpret_cast<const unsigned short *>(zs + r * kParamBox + pc * 2))
                                               : __float2half_rn(p.zpv);
                         w = dequant8_nbits<BITS, BF16>(codes, __halves2half2(z1, z1), __halves2half2(s1, s1));
                     } else {
                         const uint32_t codes = *reinterpret_cast<const uint32_t *>(cs + r * CB + c * 4);
-                        w = dequant8_codebook<BF16>(codes, __ldg(p.absmax + pi), lut_lane);
+                        w = dequant8_codebook<BF16>(codes, *reinterpret_cast<const float *>(ps + r * kParamBox + pc * 4),
+                                                    lut_lane);
                     }
                 }
                 *reinterpret_cast<uint4 *>(ws + swz128(r, c)) = w;
@@ -324,10 +340,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool ok = mbar_wait(accf, 0, abort_flag, p.fault, FAULT_WAIT_TC);
         tc_fence_after();
         const int sub = warp & 3;  // tensor-memory sub-partition this warp may read
+        const int chalf = (warp - 2) >> 2;  // two warps share a sub-partition: each takes half the columns
         const int m = m0 + sub * 32 + lane;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(sub * 32) << 16);
+        constexpr int CW = BN >= 64 ? BN / 2 : BN;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = chalf * CW; c0 < (chalf + 1) * CW && c0 < BN; c0 += 32) {
             uint32_t r[32];
             tmem_ld32(lane_addr + c0, r);
             if (!ok || m >= p.M || nks == 0) continue;
@@ -391,7 +409,8 @@ struct TcCfg {
 
 int smem_bytes(int bn, int bits) {
     const int cb = kBK * bits / 8;
-    return 1024 + kStages * (kBM * kBK * 2 + bn * kBK * 2 + bn * cb) + 4 * kStages * 8 + 64 + 16 * 32 * 4;
+    const int st = stages_for(bn);
+    return 1024 + st * (kBM * kBK * 2 + bn * kBK * 2 + bn * cb + 2 * bn * kParamBox) + 4 * st * 8 + 64 + 16 * 32 * 4;
 }
 
 // Static tile choice: the weight-tile width BN and the split of K that
@@ -424,7 +443,8 @@ TcCfg choose_tc(int M, int N, int K, int bits) {
 }
 
 template <int WK, int BITS, bool BF16, int BN>
-cudaError_t launch_tc(const CUtensorMap &am, const CUtensorMap &cm, const TcArgs &a, const TcCfg &c, cudaStream_t s) {
+cudaError_t launch_tc(const CUtensorMap &am, const CUtensorMap &cm, const CUtensorMap &pm, const CUtensorMap &zm,
+                      const TcArgs &a, const TcCfg &c, cudaStream_t s) {
     auto kern = tc_gemm_kernel<WK, BITS, BF16, BN>;
     static std::atomic<unsigned> configured{0};
     int dev = 0;
@@ -437,7 +457,7 @@ cudaError_t launch_tc(const CUtensorMap &am, const CUtensorMap &cm, const TcArgs
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     dim3 grid(c.n_tiles, c.m_tiles, c.splits);
-    kern<<<grid, kThreads, smem, s>>>(am, cm, a);
+    kern<<<grid, kThreads, smem, s>>>(am, cm, pm, zm, a);
     return cudaGetLastError();
 }
 
@@ -445,11 +465,12 @@ cudaError_t launch_tc(const CUtensorMap &am, const CUtensorMap &cm, const TcArgs
 
 // M >= 9 with fp16 / bf16 activations runs on the tensor cores; fp32
 // activations stay on the SIMT path (rounding them to 16 bits would break the
-// 1e-4 bar), and so do shapes whose packed rows are not a multiple of 16 bytes
-// (the TMA row stride).
-bool tc_eligible(int M, int K, int bits, int a_dtype) {
+// 1e-4 bar), and so do shapes whose packed rows or parameter rows are not a
+// multiple of 16 bytes (the TMA row stride).
+bool tc_eligible(int M, int K, int bits, int a_dtype, int bs) {
     if (M < 9 || a_dtype == 0) return false;
     if ((K * bits / 8) % 16 != 0) return false;
+    if ((K / bs) % 8 != 0) return false;  // parameter rows (fp16 scales / zero points, fp32 absmax) in 16-byte units
     return encode_fn() != nullptr;
 }
 
@@ -486,6 +507,30 @@ cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    // block parameters (and zero points): [N][nb] matrices read as boxes of 16
+    // bytes x BN rows, one box per stage
+    CUtensorMap pm, zm;
+    {
+        const bool cbk = p.kind == WK_CODEBOOK;
+        const int pe = cbk ? 4 : 2;
+        const int nb = p.K / p.bs;
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nb), static_cast<cuuint64_t>(p.N)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nb) * pe};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kParamBox / pe), static_cast<cuuint32_t>(c.bn)};
+        const cuuint32_t es[2] = {1, 1};
+        const CUtensorMapDataType dt = cbk ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+        const void *pp = cbk ? static_cast<const void *>(p.absmax) : static_cast<const void *>(p.scales);
+        if (enc(&pm, dt, 2, const_cast<void *>(pp), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        zm = pm;
+        if (!cbk && p.zp_mode == ZP_TENSOR &&
+            enc(&zm, dt, 2, const_cast<uint16_t *>(p.zp), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     TcArgs a{};
     a.scales = p.scales;
     a.zp = p.zp;
@@ -512,7 +557,7 @@ cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_
     cudaError_t e = cudaErrorNotSupported;
 #define QG_TC(WK_, B_, BF_, BN_)                                                                     \
     if (p.kind == WK_ && (WK_ == WK_CODEBOOK || p.bits == B_) && bf16 == BF_ && c.bn == BN_) \
-        e = launch_tc<WK_, B_, BF_, BN_>(am, cm, a, c, s);                                        \
+        e = launch_tc<WK_, B_, BF_, BN_>(am, cm, pm, zm, a, c, s);                                \
     else
     QG_TC(WK_NBITS, 2, false, 256) QG_TC(WK_NBITS, 2, false, 128) QG_TC(WK_NBITS, 2, false, 64)
     QG_TC(WK_NBITS, 2, true, 256) QG_TC(WK_NBITS, 2, true, 128) QG_TC(WK_NBITS, 2, true, 64)

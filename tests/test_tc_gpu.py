@@ -55,11 +55,11 @@ TC_CASES = [
     # (M, N, K, bits, bs, a_dtype, zp_mode, y_dtype)
     (16, 256, 1024, 2, 64, F16, "uniform", F32),
     (9, 200, 1024, 2, 64, F16, "uniform", F32),
-    (130, 333, 1088, 2, 64, F16, "tensor", F32),
+    (130, 333, 1536, 2, 64, F16, "tensor", F32),
     (300, 520, 2048, 2, 128, BF16, "uniform", F32),
     (64, 1000, 4096, 4, 64, F16, "tensor", F32),
     (33, 77, 512, 4, 32, BF16, "none", BF16),
-    (128, 384, 3072, 4, 256, F16, "none", F16),
+    (128, 384, 4096, 4, 256, F16, "none", F16),
     (16, 96, 8192, 2, 64, F16, "uniform", F32),     # few tiles, long K: split-K
     (260, 1024, 1536, 2, 64, BF16, "tensor", F32),
 ]
