@@ -62,7 +62,7 @@ struct TcArgs {
     void *Y;
     int y_dtype;
     float *partial;          // split-K partials [splits][M][N] or nullptr
-    int M, N, K, bs, nb, nk, ks_per_split;
+    int M, N, K, bs, lbs, nb, nk, ks_per_split;  // lbs = log2(bs)
     unsigned *fault;
 };
 
@@ -155,9 +155,10 @@ __device__ __forceinline__ uint32_t to_operand(__half2 h) {
 }
 
 // 8 weights (k = 8c .. 8c+7 of one row) from their packed codes, as four
-// operand pairs.  nbits: w = (q - zp) * s in fp16.
+// operand pairs.  nbits: w = (q - zp) * s in fp16 (zp2, s2: fp16 pairs).
 template <int BITS, bool BF16>
-__device__ __forceinline__ uint4 dequant8_nbits(uint32_t codes, __half2 zp2, __half2 s2) {
+__device__ __forceinline__ uint4 dequant8_nbits(uint32_t codes, uint32_t zp2u, uint32_t s2u) {
+    const __half2 zp2 = u32_as_h2(zp2u), s2 = u32_as_h2(s2u);
     uint32_t out[4];
     if constexpr (BITS == 2) {
         // codes: 16 bits, 8 codes; byte j holds codes 4j .. 4j+3
@@ -217,8 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int PPB = kParamBox / PE;            // parameters per box row
     constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    // 1024-byte alignment for the swizzled tiles
-    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte alignment for the swizzled tiles (pointer arithmetic on the
+    // shared array keeps the accesses in the shared address space)
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char *act_s = smem;
     unsigned char *wdq_s = act_s + kStages * ACT_BYTES;
     unsigned char *code_s = wdq_s + kStages * WDQ_BYTES;
@@ -297,40 +299,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ dequant warps
+        // Thread t owns units u = t + j*kDequantThreads (j < UPT); unit u is 8
+        // weights: row u/8 of the tile, 16-byte chunk u%8 of the 64-wide stage.
+        // Offsets are fixed for the whole K loop; per stage every load of the
+        // thread is issued before any conversion, so its UPT chains overlap.
+        constexpr int UPT = BN * 8 / kDequantThreads;
         const int t = threadIdx.x - 64;  // 0 .. kDequantThreads-1
         const float *lut_lane = lut + lane;
+        // Rows past N and k past K need no test: the TMA boxes zero-fill them,
+        // so their codes, scales and absmax are 0 and the weight comes out 0.
+        uint32_t code_off[UPT], wdq_off[UPT], par_off[UPT];
+#pragma unroll
+        for (int j = 0; j < UPT; ++j) {
+            const int u = t + j * kDequantThreads;
+            const int r = u >> 3, c = u & 7;
+            code_off[j] = r * CB + c * (CB / 8);
+            wdq_off[j] = swz128(r, c);
+            par_off[j] = r * kParamBox + ((8 * c) >> p.lbs) * PE;  // block of this chunk within the stage
+        }
+        const uint32_t zpu = __half_as_ushort(__float2half_rn(p.zpv)) * 0x10001u;
+        const bool zt = WK == WK_NBITS && p.zp_mode == ZP_TENSOR;
         for (int i = 0; i < nks; ++i) {
             const int s = i % kStages;
             if (!mbar_wait(&full[s], (i / kStages) & 1, abort_flag, p.fault, FAULT_WAIT_TC)) break;
             const int kb = (ks0 + i) * kBK;
-            const int pcol = (kb / p.bs) / PPB * PPB;
-            const unsigned char *cs = code_s + s * CODE_BYTES;
-            const unsigned char *ps = par_s + s * PAR_BYTES;
-            const unsigned char *zs = zp_s + s * PAR_BYTES;
-            unsigned char *ws = wdq_s + s * WDQ_BYTES;
-#pragma unroll 4
-            for (int u = t; u < BN * 8; u += kDequantThreads) {
-                const int r = u >> 3, c = u & 7;
-                const int n = n0 + r, k = kb + 8 * c;
-                uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                if (n < p.N && k < p.K) {
-                    const int pc = k / p.bs - pcol;  // column inside the stage's parameter box
-                    if constexpr (WK == WK_NBITS) {
-                        const uint32_t codes = BITS == 2
-                                                   ? static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(cs + r * CB + c * 2))
-                                                   : *reinterpret_cast<const uint32_t *>(cs + r * CB + c * 4);
-                        const __half s1 = __ushort_as_half(*reinterpret_cast<const unsigned short *>(ps + r * kParamBox + pc * 2));
-                        const __half z1 = p.zp_mode == ZP_TENSOR
-                                              ? __ushort_as_half(*reinterpret_cast<const unsigned short *>(zs + r * kParamBox + pc * 2))
-                                              : __float2half_rn(p.zpv);
-                        w = dequant8_nbits<BITS, BF16>(codes, __halves2half2(z1, z1), __halves2half2(s1, s1));
-                    } else {
-                        const uint32_t codes = *reinterpret_cast<const uint32_t *>(cs + r * CB + c * 4);
-                        w = dequant8_codebook<BF16>(codes, *reinterpret_cast<const float *>(ps + r * kParamBox + pc * 4),
-                                                    lut_lane);
-                    }
+            const int pc0 = ((kb >> p.lbs) % PPB) * PE;  // first block of the stage inside its parameter box
+            const unsigned char *__restrict__ cs = code_s + s * CODE_BYTES;
+            const unsigned char *__restrict__ ps = par_s + s * PAR_BYTES + pc0;
+            const unsigned char *__restrict__ zs = zp_s + s * PAR_BYTES + pc0;
+            unsigned char *__restrict__ ws = wdq_s + s * WDQ_BYTES;
+            uint32_t codes[UPT], pv[UPT], zv[UPT];
+#pragma unroll
+            for (int j = 0; j < UPT; ++j) {
+                if constexpr (WK == WK_NBITS) {
+                    codes[j] = BITS == 2 ? static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(cs + code_off[j]))
+                                         : *reinterpret_cast<const uint32_t *>(cs + code_off[j]);
+                    pv[j] = *reinterpret_cast<const uint16_t *>(ps + par_off[j]);
+                    zv[j] = zt ? *reinterpret_cast<const uint16_t *>(zs + par_off[j]) : 0u;
+                } else {
+                    codes[j] = *reinterpret_cast<const uint32_t *>(cs + code_off[j]);
+                    pv[j] = *reinterpret_cast<const uint32_t *>(ps + par_off[j]);
                 }
-                *reinterpret_cast<uint4 *>(ws + swz128(r, c)) = w;
+            }
+#pragma unroll
+            for (int j = 0; j < UPT; ++j) {
+                uint4 w;
+                if constexpr (WK == WK_NBITS) {
+                    w = dequant8_nbits<BITS, BF16>(codes[j], zt ? zv[j] * 0x10001u : zpu, pv[j] * 0x10001u);
+                } else {
+                    w = dequant8_codebook<BF16>(codes[j], __uint_as_float(pv[j]), lut_lane);
+                }
+                *reinterpret_cast<uint4 *>(ws + wdq_off[j]) = w;
             }
             fence_async_smem();  // make the generic-proxy stores visible to the tensor core
             __syncwarp();
@@ -429,6 +448,7 @@ TcCfg choose_tc(int M, int N, int K, int bits) {
             if (kps < 4 && sp > 1) break;
             const int splits = (nk + kps - 1) / kps;
             const long ctas = static_cast<long>(mt) * nt * splits;
+            if (splits > 1 && static_cast<long>(mt) * nt >= di.sm_count) break;  // split K only to fill the GPU
             const long waves = (ctas + di.sm_count - 1) / di.sm_count;
             // per-CTA time ~ k-steps x max(MMA time ~ bn, fixed dequant+issue cost) + fixed epilogue/fill
             const double per_cta = kps * std::max(bn, 96) + 600.0 + (splits > 1 ? 200.0 : 0.0);
@@ -544,6 +564,7 @@ cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_
     a.N = p.N;
     a.K = p.K;
     a.bs = p.bs;
+    a.lbs = 31 - __builtin_clz(static_cast<unsigned>(p.bs));
     a.nb = p.K / p.bs;
     a.nk = c.nk;
     a.ks_per_split = c.ks_per_split;
