@@ -116,6 +116,13 @@ __device__ __forceinline__ void copy_tail_lanes(void *dst, const void *src, uint
     for (uint32_t i = p.bulk_bytes / 2 + lane; i < bytes / 2; i += 32) d[i] = __ldg(s + i);
 }
 
+// Programmatic dependent launch.  pdl_wait(): block until the preceding
+// kernel on the stream has completed and its writes are visible (a no-op when
+// the kernel was not launched as a dependent).  pdl_launch_dependents(): let
+// the next kernel on the stream begin launching as this one's CTAs retire.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

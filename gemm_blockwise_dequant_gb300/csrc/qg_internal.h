@@ -6,7 +6,27 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 namespace qg {
+
+// Launch `kern` as a programmatic dependent of the preceding work on `s`: it
+// may begin before the preceding kernel ends, and must itself call
+// pdl_wait() before touching anything that kernel may have written.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 enum ZpMode { ZP_NONE = 0, ZP_TENSOR = 1, ZP_UNIFORM = 2 };
 enum WeightKind { WK_NBITS = 0, WK_CODEBOOK = 1 };

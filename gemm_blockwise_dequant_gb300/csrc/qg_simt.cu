@@ -299,6 +299,11 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
         for (int i = threadIdx.x; i < 16 * 32; i += blockDim.x) lut[i] = __ldg(p.codebook + (i >> 5));
     }
     __syncthreads();
+    // Launched as a programmatic dependent: the next kernel may start launching
+    // as these CTAs retire.  Weights (codes, block parameters, codebook) are
+    // streamed before waiting for the preceding kernel; activations, expert ids
+    // and outputs are touched only after pdl_wait().
+    pdl_launch_dependents();
 
     const bool split = gridDim.y > 1;
     const int s_begin = blockIdx.y * p.S_cta;
@@ -307,6 +312,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
 
     // ------------------------------------------------------------ producer
     if (warp == NWC) {
+        if (p.ids) pdl_wait();  // expert ids may come from the preceding kernel
         const int prow = p.nb * PB;
         const int kb0 = kc0 * BITS / 8;
         const int kb1 = split ? min(p.row_bytes, (s_begin + s_count) * LPR * VEC) : p.row_bytes;
@@ -407,6 +413,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     float ahat[MT][BPL];
     float zah[MT][BPL];  // zp * ahat for a zero point that is the same for every row
     int cur_slot = -1;
+    pdl_wait();  // activations, the fc1 output and Y belong to the preceding kernel's world
 
     // group g consumes the CTA's tiles g, g + G, g + 2G, ... (stage `it` holds tile it)
     for (int it = g;; it += p.G) {
@@ -528,6 +535,8 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
 
 // Y = sum over splits of the partials, in split order.
 __global__ void splitk_reduce_kernel(const float *__restrict__ partial, int splits, size_t MN, void *Y, int y_dtype) {
+    pdl_wait();
+    pdl_launch_dependents();
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < MN;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
         float s = 0.f;
@@ -541,6 +550,8 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ partial, int spli
 __global__ void qmoe_combine_kernel(const float *__restrict__ o, const int32_t *__restrict__ ids,
                                     const float *__restrict__ w, int k, int num_experts, int H, uint16_t *y,
                                     int *status) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     int bad = 0;
     float acc = 0.f;
@@ -648,8 +659,8 @@ cudaError_t launch_one(const GemvArgs &a, const Cfg &c, cudaStream_t s) {
     }
     dim3 grid(c.grid_x, c.splits);
     dim3 block((c.S_cta * c.G + 1) * 32);
-    kern<<<grid, block, c.smem, s>>>(a);
-    return cudaGetLastError();
+    const cudaError_t e = launch_pdl(kern, grid, block, c.smem, s, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t dispatch(const GemvArgs &a, const Cfg &c, int bits, int kind, cudaStream_t s) {
@@ -768,8 +779,9 @@ cudaError_t simt_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStrea
         const size_t MN = static_cast<size_t>(p.M) * p.N;
         const int threads = 256;
         const int blocks = static_cast<int>(std::min<size_t>((MN + threads - 1) / threads, 4096));
-        splitk_reduce_kernel<<<blocks, threads, 0, s>>>(a.partial, c.splits, MN, p.Y, p.y_dtype);
-        return cudaGetLastError();
+        const cudaError_t e = launch_pdl(splitk_reduce_kernel, dim3(blocks), dim3(threads), 0, s,
+                                         static_cast<const float *>(a.partial), c.splits, MN, p.Y, p.y_dtype);
+        return e != cudaSuccess ? e : cudaGetLastError();
     }
     return cudaSuccess;
 }
@@ -828,10 +840,10 @@ cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     const int threads = 256;
-    qmoe_combine_kernel<<<(q.hidden + threads - 1) / threads, threads, 0, s>>>(o, q.ids, q.weights, q.k,
-                                                                               q.num_experts, q.hidden, q.y,
-                                                                               q.status);
-    return cudaGetLastError();
+    const cudaError_t e = launch_pdl(qmoe_combine_kernel, dim3((q.hidden + threads - 1) / threads), dim3(threads), 0, s,
+                                     static_cast<const float *>(o), q.ids, q.weights, q.k, q.num_experts, q.hidden,
+                                     q.y, q.status);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace qg

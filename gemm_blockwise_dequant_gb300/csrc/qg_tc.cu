@@ -259,10 +259,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();  // the next kernel may start launching as these CTAs retire
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            pdl_wait();  // activations may come from the preceding kernel; everything else follows this producer
             for (int i = 0; i < nks; ++i) {
                 const int s = i % kStages;
                 if (!mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1, abort_flag, p.fault, FAULT_WAIT_TC)) break;
@@ -398,6 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 __global__ void tc_splitk_reduce_kernel(const float *__restrict__ partial, int splits, size_t MN, void *Y,
                                         int y_dtype) {
+    pdl_wait();
+    pdl_launch_dependents();
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < MN;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
         float s = 0.f;
@@ -413,7 +417,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     if (!f) {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) != cudaSuccess ||
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
             q != cudaDriverEntryPointSuccess)
             return nullptr;
         f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
@@ -477,8 +481,8 @@ cudaError_t launch_tc(const CUtensorMap &am, const CUtensorMap &cm, const CUtens
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     dim3 grid(c.n_tiles, c.m_tiles, c.splits);
-    kern<<<grid, kThreads, smem, s>>>(am, cm, pm, zm, a);
-    return cudaGetLastError();
+    const cudaError_t e = launch_pdl(kern, grid, dim3(kThreads), smem, s, am, cm, pm, zm, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -592,8 +596,9 @@ cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_
         const size_t MN = static_cast<size_t>(p.M) * p.N;
         const int threads = 256;
         const int blocks = static_cast<int>(std::min<size_t>((MN + threads - 1) / threads, 8192));
-        tc_splitk_reduce_kernel<<<blocks, threads, 0, s>>>(a.partial, c.splits, MN, p.Y, p.y_dtype);
-        return cudaGetLastError();
+        const cudaError_t e2 = launch_pdl(tc_splitk_reduce_kernel, dim3(blocks), dim3(threads), 0, s,
+                                          static_cast<const float *>(a.partial), c.splits, MN, p.Y, p.y_dtype);
+        return e2 != cudaSuccess ? e2 : cudaGetLastError();
     }
     return cudaSuccess;
 }

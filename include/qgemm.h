@@ -48,6 +48,13 @@
  *    same inputs are bit-identical ([hip-ep #1328], "Why" and "Test plan":
  *    129 calls bit-identical).  Nothing is tuned or timed on live calls.
  *  - M == 0 or N == 0 is a no-op.  K == 0 writes zeros.
+ *  - Kernels are launched as programmatic dependents of the preceding kernel
+ *    on `stream`: they may start streaming the WEIGHT buffers (W, scales,
+ *    zero points, codebook, absmax, expert weights' codes) before that kernel
+ *    has finished; activations, expert ids/weights, biases and outputs are
+ *    touched only after it has finished.  So weight buffers must not be
+ *    written by the kernel that immediately precedes a call on the same
+ *    stream (copies and events order as usual).
  */
 #ifndef QGEMM_H
 #define QGEMM_H
