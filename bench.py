@@ -156,61 +156,84 @@ class Clocks:
 
 
 # ------------------------------------------------------------- CPU baseline
-def cpu_baseline(budget_s=12.0):
-    """Time the oracle (as it stands) on a bounded sample of the workload.
+class OracleSample:
+    """The oracle (as it stands) on a bounded row sample of the workload.
 
-    The sample is every row of the five shapes at M=1 when that fits the time
-    budget (repeated until the budget is used), else an evenly spaced row
-    subset of each shape."""
-    import oracle as O
-    import workloads as WL
+    The five M=1 weight sets are generated once; `run(budget_s)` evaluates an
+    evenly spaced row subset of every shape sized from a calibration so that
+    one pass takes about `budget_s` seconds (every row when that fits)."""
 
-    O.load()
-    cores = os.cpu_count() or 1
-    data = [WL.phi4_u2(s, M=1) for s in SHAPES]
-    # calibrate on 512 rows of the first shape
-    d = data[0]
-    O.qgemm_nbits(d["A"], d["W"], d["scales"], None, M=1, N=d["N"], K=d["K"], bits=BITS, block_size=BS,
-                  uniform_zp=ZP, rows=np.arange(64))
-    t0 = time.perf_counter()
-    O.qgemm_nbits(d["A"], d["W"], d["scales"], None, M=1, N=d["N"], K=d["K"], bits=BITS, block_size=BS,
-                  uniform_zp=ZP, rows=np.arange(512))
-    per_row_k = (time.perf_counter() - t0) / (512 * d["K"])
-    full = sum(d["N"] * d["K"] for d in data)
-    frac = min(1.0, budget_s / (per_row_k * full))
-    done_bytes, secs, passes = 0, 0.0, 0
-    while secs < 0.8 * budget_s or passes == 0:
-        for d in data:
+    def __init__(self):
+        import oracle as O
+        import workloads as WL
+
+        O.load()
+        self.O = O
+        self.cores = os.cpu_count() or 1
+        self.data = [WL.phi4_u2(s, M=1) for s in SHAPES]
+        d = self.data[0]
+        self._rows(d, np.arange(64))
+        t0 = time.perf_counter()
+        self._rows(d, np.arange(512))
+        self.per_row_k = (time.perf_counter() - t0) / (512 * d["K"])
+        self.full = sum(d["N"] * d["K"] for d in self.data)
+
+    def _rows(self, d, r):
+        self.O.qgemm_nbits(d["A"], d["W"], d["scales"], None, M=1, N=d["N"], K=d["K"], bits=BITS, block_size=BS,
+                           uniform_zp=ZP, rows=r)
+
+    def run(self, budget_s):
+        frac = min(1.0, budget_s / (self.per_row_k * self.full))
+        done, secs = 0, 0.0
+        for d in self.data:
             r = np.linspace(0, d["N"] - 1, max(16, int(frac * d["N"]))).astype(np.int64)
             t0 = time.perf_counter()
-            O.qgemm_nbits(d["A"], d["W"], d["scales"], None, M=1, N=d["N"], K=d["K"], bits=BITS, block_size=BS,
-                          uniform_zp=ZP, rows=r)
+            self._rows(d, r)
             secs += time.perf_counter() - t0
-            done_bytes += weight_bytes(len(r), d["K"])
-        passes += 1
-    return {"value": done_bytes / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            done += weight_bytes(len(r), d["K"])
+        return done, secs, frac
+
+
+def cpu_baseline(budget_s=12.0, sample=None):
+    """Time the oracle on a bounded sample of the workload (about budget_s of CPU work)."""
+    S = sample or OracleSample()
+    done, secs, passes, frac = 0, 0.0, 0, 0.0
+    while secs < 0.8 * budget_s or passes == 0:
+        b, t, frac = S.run(min(budget_s, 4.0))
+        done, secs, passes = done + b, secs + t, passes + 1
+    return {"value": done / secs / 1e9, "unit": "GB/s", "cores": S.cores, "kind": "oracle",
             "sample": "%d pass(es) over %.1f%% of the rows of the 5 phi4 shapes, M=1 (%.1f MB of weights, %.1f s, "
-                      "OpenMP over rows)" % (passes, 100 * frac, done_bytes / 1e6, secs)}, secs
+                      "OpenMP over rows)" % (passes, 100 * frac, done / 1e6, secs)}, secs
 
 
 def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle, as it stands, on this host's cores.
+
+    Each step is one pass of the oracle over a row sample of the five shapes,
+    sized so that the whole run stays near a minute of CPU work.  Under
+    torchrun only rank 0 runs it."""
     if rank != 0:
         return 0
-    steps = []
+    S = OracleSample()
+    per_step = max(0.05, 60.0 / max(1, args.steps))
     for _ in range(args.warmup):
-        cpu_baseline(budget_s=2.0)
+        S.run(min(per_step, 0.5))
+    done, secs, frac = 0, 0.0, 0.0
     for _ in range(args.steps):
-        cb, secs = cpu_baseline(budget_s=max(2.0, 60.0 / max(1, args.steps)))
-        steps.append(cb)
-    v = statistics.median(s["value"] for s in steps)
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": "phi4-14B u2 decode GEMVs (qkv, o, gate_up, down, lm_head), M=1, bits=2, "
-                                   "block 64, uniform zp 1.5, fp32 A/Y; CPU oracle on a row sample"},
-            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": steps[0]["cores"], "kind": "oracle",
-                             "sample": steps[0]["sample"]},
-            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        b, t, frac = S.run(per_step)
+        done, secs = done + b, secs + t
+    v = done / secs / 1e9
+    sample = ("%d steps, each one pass over %.2f%% of the rows of the 5 phi4 shapes, M=1 (%.1f MB of weights in "
+              "%.1f s, OpenMP over rows)" % (args.steps, 100 * frac, done / 1e6, secs))
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "phi4-14B u2 decode GEMVs (qkv 7680x5120, o 5120x5120, gate_up 35840x5120, "
+                                   "down 5120x17920, lm_head 100352x5120), M=1, bits=2, block 64, fp16 scales, "
+                                   "uniform zp 1.5, fp32 A/Y; CPU oracle on a row sample"},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": S.cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -366,6 +389,66 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+# ------------------------------------------------------------- ncu probes
+def run_probe(name):
+    """Small fixed workloads for profiler captures (no timing, no JSON line).
+
+    gemv_k5120   3 warm-up calls, then one call, of each K=5120 phi4 u2 M=1 shape
+                 (qkv, o, gate_up, lm_head): the launches of the dominant kernel
+    gemv_lm_head 4 calls of the lm_head shape (100352 x 5120, u2, M=1)
+    tc_prefill   4 calls of a prefill-sized u2 GEMM on the tensor cores
+                 (M=2048, N=K=5120, fp16 activations, fp32 out)
+    qmoe         4 calls of the 128-expert top-8 2880/2880 block-32 QMoE decode
+    """
+    import torch
+
+    import gemm_blockwise_dequant_gb300 as qg
+    import workloads as WL
+
+    def nbits(d):
+        ad = d["a_dtype"]
+        A = torch.from_numpy(d["A"] if ad == 0 else d["A"].view(np.int16)).cuda()
+        if ad == 1:
+            A = A.view(torch.float16)
+        W = torch.from_numpy(d["W"]).cuda()
+        S = torch.from_numpy(d["scales"].view(np.int16)).cuda().view(torch.float16)
+        Y = torch.empty(d["M"], d["N"], device="cuda")
+        ws = torch.empty(max(16, qg.qgemm_workspace_bytes(ad, d["M"], d["N"], d["K"], 2, 64)), dtype=torch.uint8,
+                         device="cuda")
+        return lambda: qg.qgemm_nbits_uniform_zp(A, W, S, ZP, Y, bits=2, block_size=64, workspace=ws)
+
+    if name == "gemv_k5120":
+        calls = [nbits(WL.phi4_u2(s, M=1)) for s in ("qkv", "o", "gate_up", "lm_head")]
+        for c in calls:
+            for _ in range(3):
+                c()
+        for c in calls:
+            c()
+    elif name == "gemv_lm_head":
+        c = nbits(WL.phi4_u2("lm_head", M=1))
+        for _ in range(4):
+            c()
+    elif name == "tc_prefill":
+        c = nbits(WL.prefill_u2((5120, 5120), M=2048))
+        for _ in range(4):
+            c()
+    elif name == "qmoe":
+        d = WL.qmoe()
+        h = lambda a: None if a is None else torch.from_numpy(a.view(np.int16)).cuda().view(torch.float16)
+        y = torch.empty(d["hidden"], dtype=torch.float16, device="cuda")
+        kw = dict(num_experts=d["num_experts"], fc1_w=torch.from_numpy(d["fc1_w"]).cuda(), fc1_scales=h(d["fc1_scales"]),
+                  fc1_zp=None, fc1_bias=h(d["fc1_bias"]), fc2_w=torch.from_numpy(d["fc2_w"]).cuda(),
+                  fc2_scales=h(d["fc2_scales"]), fc2_zp=None, fc2_bias=h(d["fc2_bias"]), bits=4, block_size=32, y=y)
+        x, ids, w = h(d["x"]), torch.from_numpy(d["ids"]).cuda(), torch.from_numpy(d["weights"]).cuda()
+        for _ in range(4):
+            qg.qmoe_decode_fused(x, ids, w, **kw)
+    else:
+        raise SystemExit("unknown probe %r" % name)
+    torch.cuda.synchronize()
+    print("probe %s done" % name)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -373,7 +456,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--probe", choices=["gemv_k5120", "gemv_lm_head", "tc_prefill", "qmoe"],
+                    help="run a small fixed workload for a profiler capture instead of the benchmark")
     args = ap.parse_args()
+    if args.probe:
+        return run_probe(args.probe)
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_setup(args.gpus)
