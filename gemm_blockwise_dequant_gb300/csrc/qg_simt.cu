@@ -46,8 +46,9 @@
 namespace qg {
 namespace {
 
-constexpr int kMaxStages = 8;
-constexpr int kLutOff = 256;
+constexpr int kMaxStages = 16;
+constexpr int kLutOff = 512;  // after the 2 x kMaxStages mbarriers and the abort flag
+static_assert(2 * kMaxStages * 8 + 4 <= kLutOff, "shared-memory header overlaps the codebook table");
 
 // Most consumer warps a CTA may have (launch bound), by activation rows held.
 __host__ __device__ constexpr int max_consumer_warps(int mt) { return mt == 1 ? 15 : 11; }
@@ -269,6 +270,37 @@ __device__ __forceinline__ void load_activations(const GemvArgs &p, int sl, bool
     }
 }
 
+// Producer side of a tile: add the S slice sums of each of the tile's rows in
+// slice order and write the outputs (Y, split-K partials, or the QMoE slot
+// outputs with the expert's bias).  `rs` holds [slice][kRedV * H] values.
+template <int MT, int LPR>
+__device__ __forceinline__ void finish_tile(const GemvArgs &p, const float *rs, int s_count, int tile, int lane) {
+    constexpr int H = 32 / LPR;
+    constexpr int VPW = kRedV * H;
+    if (lane >= VPW) return;
+    float sum = 0.f;
+    for (int s = 0; s < s_count; ++s) sum += rs[s * VPW + lane];
+    const int sl = tile / p.tiles_per_slot;
+    const int rbase = (tile - sl * p.tiles_per_slot) * p.SR;
+    const int hh = lane / kRedV, v = lane % kRedV;
+    const int i = v / MT, m = v % MT;
+    const int row = rbase + i * H + hh;
+    const int am = p.m0 + m;
+    if (row >= p.N || am >= p.M) return;
+    if (p.out_f32) {
+        const int e = p.ids ? __ldg(p.ids + sl) : 0;
+        float o = 0.f;
+        if (e >= 0 && e < p.num_experts)
+            o = sum + (p.bias ? h2f(__ldg(reinterpret_cast<const unsigned short *>(p.bias) + static_cast<size_t>(e) * p.N + row))
+                              : 0.f);
+        p.out_f32[static_cast<size_t>(sl) * p.N + row] = o;
+    } else if (p.partial) {
+        p.partial[(static_cast<size_t>(blockIdx.y) * p.M + am) * p.N + row] = sum;
+    } else {
+        store_y_elem(p.Y, p.y_dtype, static_cast<size_t>(am) * p.N + row, sum);
+    }
+}
+
 template <int BITS, int VEC, int MT, int BPL, int WK, int LPR, int AM>
 __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_kernel(const GemvArgs p) {
     constexpr int CPW = 32 / BITS;
@@ -311,16 +343,32 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     const int kc0 = split ? s_begin * LPR * KPL : 0;  // first k held in a stage row
 
     // ------------------------------------------------------------ producer
+    // The producer warp also finishes every tile: when a stage comes back
+    // empty, the consumer warps of its group have left their slice sums of
+    // that tile in the stage's reduction slot; the producer adds them in
+    // slice order and writes the outputs before it refills the stage.  The
+    // consumer warps therefore never wait on one another.
     if (warp == NWC) {
         if (p.ids) pdl_wait();  // expert ids may come from the preceding kernel
+        bool waited = p.ids != nullptr;
         const int prow = p.nb * PB;
         const int kb0 = kc0 * BITS / 8;
         const int kb1 = split ? min(p.row_bytes, (s_begin + s_count) * LPR * VEC) : p.row_bytes;
-        int it = 0;
+        int it = 0, slot = 0;
+        uint32_t par = 1;  // parity of the empty phase that must complete before filling (it / NST)
+        bool alive = true;
         for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++it) {
-            const int slot = it % p.NST;
-            const uint32_t par = ((it / p.NST) & 1) ^ 1;
-            if (!mbar_wait(&empty[slot], par, abort_flag, p.fault, FAULT_WAIT_EMPTY)) break;
+            if (!mbar_wait(&empty[slot], par, abort_flag, p.fault, FAULT_WAIT_EMPTY)) {
+                alive = false;
+                break;
+            }
+            if (it >= p.NST) {
+                if (!waited) {
+                    pdl_wait();  // outputs may be read by the preceding kernel until it completes
+                    waited = true;
+                }
+                finish_tile<MT, LPR>(p, red + slot * (p.S_cta * kRedV * H), s_count, tile - p.NST * gridDim.x, lane);
+            }
             const int sl = tile / p.tiles_per_slot;
             const int r0 = (tile - sl * p.tiles_per_slot) * p.SR;
             const int e = p.ids ? __ldg(p.ids + sl) : 0;
@@ -389,6 +437,19 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
                 const CopyPlan cp = copy_plan(st + p.z_off, src, rows * p.nb * 2);
                 if (cp.bulk_bytes) bulk_g2s(st + p.z_off, src, cp.bulk_bytes, &full[slot]);
             }
+            if (++slot == p.NST) {
+                slot = 0;
+                par ^= 1u;
+            }
+        }
+        // finish the last (up to NST) tiles once their stages come back
+        if (alive) {
+            if (!waited) pdl_wait();
+            for (int j = max(0, it - p.NST); j < it; ++j) {
+                const int sj = j % p.NST;
+                if (!mbar_wait(&empty[sj], (j / p.NST) & 1, abort_flag, p.fault, FAULT_WAIT_EMPTY)) break;
+                finish_tile<MT, LPR>(p, red + sj * (p.S_cta * kRedV * H), s_count, blockIdx.x + j * gridDim.x, lane);
+            }
         }
         return;
     }
@@ -406,6 +467,9 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     const int row_stride = H * p.w_pitch;           // stage bytes between a lane's successive rows
     const int prow_stride = H * p.nb * PB;          // same for the block parameters
     const int zrow_stride = H * p.nb * 2;
+    constexpr int VPW = kRedV * H;  // reduced values per warp and tile
+    const bool writer = (gl & (LPR / kRedV - 1)) == 0;
+    const int red_idx = sigma * VPW + half * kRedV + gl / (LPR / kRedV);
 
     // Activations of this lane's slice, for MT rows, kept in registers.
     float ap[MT][KPL];
@@ -415,24 +479,39 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     int cur_slot = -1;
     pdl_wait();  // activations, the fc1 output and Y belong to the preceding kernel's world
 
-    // group g consumes the CTA's tiles g, g + G, g + 2G, ... (stage `it` holds tile it)
-    for (int it = g;; it += p.G) {
-        const int tile = blockIdx.x + it * gridDim.x;
-        if (tile >= p.ntiles) break;
-        const int sl = tile / p.tiles_per_slot;
-        const int rbase = (tile - sl * p.tiles_per_slot) * p.SR;
-        const int e = p.ids ? __ldg(p.ids + sl) : 0;
-        const bool valid = e >= 0 && e < p.num_experts;
-        if (sl != cur_slot && (cur_slot < 0 || AM == A_SWIGLU)) {
-            load_activations<BITS, MT, KPL, BPL, WK, AM>(p, sl, lane_active, k0, ap, e2, ahat);
+    // group g consumes the CTA's tiles g, g + G, g + 2G, ... (stage `it` holds
+    // tile it); ring slot, phase parity, expert slot and tile are advanced
+    // incrementally (no division in the loop)
+    int slot = g, sl = 0;
+    uint32_t par = 0;
+    while (slot >= p.NST) {
+        slot -= p.NST;
+        par ^= 1u;
+    }
+    const int tstep = p.G * gridDim.x;
+    int tile = blockIdx.x + g * gridDim.x;
+    int ltile = tile;  // tile index within the expert slot
+    while (ltile >= p.tiles_per_slot) {
+        ltile -= p.tiles_per_slot;
+        ++sl;
+    }
+    int e = 0;
+    bool valid = true;
+    for (; tile < p.ntiles; tile += tstep) {
+        if (sl != cur_slot) {
+            if (p.ids) {
+                e = __ldg(p.ids + sl);
+                valid = e >= 0 && e < p.num_experts;
+            }
+            if (cur_slot < 0 || AM == A_SWIGLU) {
+                load_activations<BITS, MT, KPL, BPL, WK, AM>(p, sl, lane_active, k0, ap, e2, ahat);
 #pragma unroll
-            for (int m = 0; m < MT; ++m)
+                for (int m = 0; m < MT; ++m)
 #pragma unroll
-                for (int b = 0; b < BPL; ++b) zah[m][b] = p.zpv * ahat[m][b];
+                    for (int b = 0; b < BPL; ++b) zah[m][b] = p.zpv * ahat[m][b];
+            }
             cur_slot = sl;
         }
-        const int slot = it % p.NST;
-        const uint32_t par = (it / p.NST) & 1;
         const bool ok = mbar_wait(&full[slot], par, abort_flag, p.fault, FAULT_WAIT_FULL);
         const unsigned char *st = stages + static_cast<size_t>(slot) * p.stage_bytes;
         float racc[kRedV];
@@ -499,36 +578,21 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
 #pragma unroll
             for (int v = 0; v < kRedV; ++v) racc[v] = lane_active ? racc[v] : 0.f;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-
         // lane l now holds, for row half `half`, the slice sum of value (l % LPR) / (LPR / kRedV)
         const float tot = transpose_reduce<kRedV, LPR>(racc, lane);
-        constexpr int VPW = kRedV * H;  // values per warp
-        // per group, double-buffered: [g][(it / G) & 1][slice][value]
-        float *redb = red + (g * 2 + ((it / p.G) & 1)) * (p.S_cta * VPW);
-        if ((gl & (LPR / kRedV - 1)) == 0) redb[sigma * VPW + half * kRedV + gl / (LPR / kRedV)] = tot;
-        named_bar_sync(1 + g, p.S_cta * 32);
-        if (sigma == 0 && lane < VPW) {
-            float sum = 0.f;
-            for (int s = 0; s < s_count; ++s) sum += redb[s * VPW + lane];
-            const int hh = lane / kRedV, v = lane % kRedV;
-            const int i = v / MT, m = v % MT;
-            const int row = rbase + i * H + hh;
-            const int am = p.m0 + m;
-            if (row < p.N && am < p.M) {
-                if (p.out_f32) {
-                    float o = 0.f;
-                    if (valid) o = sum + (p.bias ? h2f(__ldg(reinterpret_cast<const unsigned short *>(p.bias) +
-                                                            static_cast<size_t>(e) * p.N + row))
-                                                 : 0.f);
-                    p.out_f32[static_cast<size_t>(sl) * p.N + row] = o;
-                } else if (p.partial) {
-                    p.partial[(static_cast<size_t>(blockIdx.y) * p.M + am) * p.N + row] = sum;
-                } else {
-                    store_y_elem(p.Y, p.y_dtype, static_cast<size_t>(am) * p.N + row, sum);
-                }
-            }
+        if (writer) red[slot * (p.S_cta * VPW) + red_idx] = tot;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);  // releases the stage and this warp's slice sums
+
+        slot += p.G;
+        while (slot >= p.NST) {
+            slot -= p.NST;
+            par ^= 1u;
+        }
+        ltile += tstep;
+        while (ltile >= p.tiles_per_slot) {
+            ltile -= p.tiles_per_slot;
+            ++sl;
         }
     }
 }
@@ -628,16 +692,25 @@ bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, 
     c.SR = (kRedV / c.mt) * (32 / c.lpr);
     c.G = std::max(1, maxw / c.S_cta);
     c.w_pitch = c.splits > 1 ? round_up(c.S_cta * c.lpr * c.vec, 16) : row_bytes;
-    const int nwc = c.S_cta * c.G;
-    c.red_off = kLutOff + (kind == WK_CODEBOOK ? 16 * 32 * 4 : 0);
-    c.stage_off = round_up(c.red_off + 2 * nwc * 32 * 4, 1024);
+    c.stage_off = round_up(kLutOff + (kind == WK_CODEBOOK ? 16 * 32 * 4 : 0), 1024);
     const int budget = di.max_smem_optin - c.stage_off;
     c.s_off = round_up(c.SR * c.w_pitch, 128);
     c.z_off = c.s_off + round_up(c.SR * nb * pb, 128);
     c.stage_bytes = c.z_off + (zp_tensor ? round_up(c.SR * nb * 2, 128) : 0);
-    c.NST = std::min(kMaxStages, budget / c.stage_bytes);
-    if (c.NST < 2) return false;
-    c.smem = c.stage_off + c.NST * c.stage_bytes;
+    // each stage also has a reduction slot: S_cta slices x kRedV x H sums
+    const int red_slot = c.S_cta * kRedV * (32 / c.lpr) * 4;
+    const int nfit = std::min(kMaxStages, budget / (c.stage_bytes + red_slot));
+    if (nfit < 2) return false;
+    // Ring slots are owned by row groups: slot s serves group s % G only, so
+    // NST is a multiple of G.  A group then waits on a slot's phase k only
+    // after it has itself consumed phase k - 1 of that slot.  (If slots were
+    // shared, stage fills that land out of order could let a group wait on
+    // phase k while phase k - 1 is still pending, whose parity the barrier
+    // reports as complete.)  At least two stages per group when possible.
+    c.G = std::max(1, std::min(c.G, nfit / 2));
+    c.NST = nfit - nfit % c.G;
+    c.red_off = c.stage_off + c.NST * c.stage_bytes;
+    c.smem = c.red_off + c.NST * red_slot;
     c.ntiles = (N + c.SR - 1) / c.SR;
     c.grid_x = std::min(c.ntiles, di.sm_count);
     (void)M;

@@ -108,6 +108,8 @@ NBITS_CASES = [
     (4, 70, 8192, 2, 64, F32, "uniform", F32),     # long K: split across CTAs
     (4, 33, 17920, 2, 64, F32, "tensor", F32),     # long K, split-K with a ragged last split
     (12, 50, 1536, 2, 64, F32, "uniform", F32),    # fp32 activations beyond 8 rows
+    (1, 40000, 512, 2, 64, F32, "uniform", F32),   # short K, many rows: more row groups than ring stages
+    (1, 30000, 256, 4, 64, F32, "tensor", F32),
 ]
 
 
