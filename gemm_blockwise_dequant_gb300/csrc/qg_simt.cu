@@ -71,6 +71,8 @@ struct GemvArgs {
     float *partial;  // split-K partials [splits][M][N], or nullptr
     int M, N, K, bs, nb, row_bytes, m0;
     int S_total, S_cta, G, SR, NST;
+    int fast_tx;  // bytes of a whole aligned stage (codes + parameters [+ zero points]); 0: no fast path
+    int a_off, a_rstride;  // shared-memory staging of the activations: offset, floats per staged row
     int w_pitch, stage_bytes, s_off, z_off, red_off, stage_off, ntiles;
     unsigned *fault;
     // Slots (the experts of a QMoE decode): tile t covers rows of slot
@@ -168,83 +170,57 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[V], int lane) {
     return r;
 }
 
-// Load (or reload, when the slot changes) this lane's activations.
-//  A_ROWS:   rows m0 .. m0+MT-1 of A[M][K] (fp32 / fp16 / bf16).
-//  A_SWIGLU: one row, h = silu(gate) * up of the fc1 output of slot `sl`
-//            (gate = g[0:K], up = g[K:2K], or the even / odd elements).
-// For MatMulNBits the values are then normalised by a power of two 2^E per
-// (lane, row) and pre-multiplied by 2^(126 - pos) for the subnormal-code
-// product; ahat holds the block sums of the normalised values.
-template <int BITS, int MT, int KPL, int BPL, int WK, int AM>
-__device__ __forceinline__ void load_activations(const GemvArgs &p, int sl, bool lane_active, int k0,
-                                                 float (&ap)[MT][KPL], float (&e2)[MT], float (&ahat)[MT][BPL]) {
+// Stage this CTA's slice of the activation rows m0 .. m0+MT-1 in shared
+// memory as fp32, with coalesced 16-byte loads by all consumer threads.  The
+// staged row keeps each lane's KPL values contiguous with a 16-byte pad after
+// them, so that the lanes' later 16-byte reads of their own values fall in
+// distinct bank groups.  Values past K or past M are zero.
+template <int MT, int KPL>
+__device__ __forceinline__ void stage_activations(const GemvArgs &p, float *as, int kc0, int nslots, int tid, int nthr) {
+    constexpr int PITCH = KPL + 4;  // floats per lane slot
+    if (p.a_dtype == 0) {
+        const int nv = nslots * (KPL / 4);  // float4 per staged row
+        for (int i = tid; i < MT * nv; i += nthr) {
+            const int m = i / nv, v = i - m * nv;
+            const int k = kc0 + 4 * v, am = p.m0 + m;
+            float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (am < p.M && k < p.K)
+                val = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(p.A) + static_cast<size_t>(am) * p.K + k));
+            *reinterpret_cast<float4 *>(as + m * p.a_rstride + (v / (KPL / 4)) * PITCH + (v % (KPL / 4)) * 4) = val;
+        }
+    } else {
+        const bool f16 = p.a_dtype == 1;
+        const int nv = nslots * (KPL / 8);  // 8-element groups per staged row
+        for (int i = tid; i < MT * nv; i += nthr) {
+            const int m = i / nv, v = i - m * nv;
+            const int k = kc0 + 8 * v, am = p.m0 + m;
+            uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+            if (am < p.M && k < p.K)
+                raw = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.A) + static_cast<size_t>(am) * p.K + k));
+            const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+            float f[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint16_t lo = static_cast<uint16_t>(w4[q] & 0xFFFFu), hi = static_cast<uint16_t>(w4[q] >> 16);
+                f[2 * q] = f16 ? h2f(lo) : bf2f(lo);
+                f[2 * q + 1] = f16 ? h2f(hi) : bf2f(hi);
+            }
+            float *d = as + m * p.a_rstride + (v / (KPL / 8)) * PITCH + (v % (KPL / 8)) * 8;
+            *reinterpret_cast<float4 *>(d) = make_float4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<float4 *>(d + 4) = make_float4(f[4], f[5], f[6], f[7]);
+        }
+    }
+}
+
+// Normalise a lane's activations by a power of two per row and fold in the
+// code positions (MatMulNBits), computing the block sums on the way.  a_hat
+// = a * 2^-E with |a_hat| < 2; a' = a_hat * 2^(126 - pos), so that a' times
+// the subnormal code at pos equals a_hat * q * 2^-23 exactly.
+template <int BITS, int MT, int KPL, int BPL, int WK>
+__device__ __forceinline__ void prepare_activations(float (&ap)[MT][KPL], float (&e2)[MT], float (&ahat)[MT][BPL]) {
     constexpr int CPW = 32 / BITS;
-    static_assert(KPL % 8 == 0, "activation vectors are 8 elements");
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-        const int am = p.m0 + m;
-        const bool row_ok = lane_active && am < p.M;
-#pragma unroll
-        for (int i = 0; i < KPL; ++i) ap[m][i] = 0.f;
-        if (row_ok) {
-            // every load of the lane's slice is issued before any is used (16-byte vectors)
-            if constexpr (AM == A_SWIGLU) {
-                // runs only when the slot changes; 8 values at a time to keep registers low
-                const float *gs = p.gbuf + static_cast<size_t>(sl) * 2 * p.K;
-#pragma unroll
-                for (int c = 0; c < KPL; c += 8) {
-                    float gate[8], up[8];
-                    if (p.swiglu_interleaved) {
-                        const float4 *q = reinterpret_cast<const float4 *>(gs + 2 * (k0 + c));
-                        const float4 v0 = q[0], v1 = q[1], v2 = q[2], v3 = q[3];
-                        gate[0] = v0.x; up[0] = v0.y; gate[1] = v0.z; up[1] = v0.w;
-                        gate[2] = v1.x; up[2] = v1.y; gate[3] = v1.z; up[3] = v1.w;
-                        gate[4] = v2.x; up[4] = v2.y; gate[5] = v2.z; up[5] = v2.w;
-                        gate[6] = v3.x; up[6] = v3.y; gate[7] = v3.z; up[7] = v3.w;
-                    } else {
-                        const float4 *qg = reinterpret_cast<const float4 *>(gs + k0 + c);
-                        const float4 *qu = reinterpret_cast<const float4 *>(gs + p.K + k0 + c);
-                        const float4 g0 = qg[0], g1 = qg[1], u0 = qu[0], u1 = qu[1];
-                        gate[0] = g0.x; gate[1] = g0.y; gate[2] = g0.z; gate[3] = g0.w;
-                        gate[4] = g1.x; gate[5] = g1.y; gate[6] = g1.z; gate[7] = g1.w;
-                        up[0] = u0.x; up[1] = u0.y; up[2] = u0.z; up[3] = u0.w;
-                        up[4] = u1.x; up[5] = u1.y; up[6] = u1.z; up[7] = u1.w;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) ap[m][c + i] = gate[i] / (1.f + expf(-gate[i])) * up[i];
-                }
-            } else if (p.a_dtype == 0) {
-                const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(p.A) +
-                                                                     static_cast<size_t>(am) * p.K + k0);
-                float4 v[KPL / 4];
-#pragma unroll
-                for (int j = 0; j < KPL / 4; ++j) v[j] = __ldg(src + j);
-#pragma unroll
-                for (int j = 0; j < KPL / 4; ++j) {
-                    ap[m][4 * j] = v[j].x;
-                    ap[m][4 * j + 1] = v[j].y;
-                    ap[m][4 * j + 2] = v[j].z;
-                    ap[m][4 * j + 3] = v[j].w;
-                }
-            } else {
-                const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.A) +
-                                                                   static_cast<size_t>(am) * p.K + k0);
-                uint4 v[KPL / 8];
-#pragma unroll
-                for (int j = 0; j < KPL / 8; ++j) v[j] = __ldg(src + j);
-                const bool f16 = p.a_dtype == 1;
-#pragma unroll
-                for (int j = 0; j < KPL / 8; ++j) {
-                    const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint16_t lo = static_cast<uint16_t>(w4[q] & 0xFFFFu), hi = static_cast<uint16_t>(w4[q] >> 16);
-                        ap[m][8 * j + 2 * q] = f16 ? h2f(lo) : bf2f(lo);
-                        ap[m][8 * j + 2 * q + 1] = f16 ? h2f(hi) : bf2f(hi);
-                    }
-                }
-            }
-        }
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < KPL; ++i) amax = fmaxf(amax, fabsf(ap[m][i]));
@@ -252,9 +228,6 @@ __device__ __forceinline__ void load_activations(const GemvArgs &p, int sl, bool
 #pragma unroll
         for (int b = 0; b < BPL; ++b) ahat[m][b] = 0.f;
         if constexpr (WK == WK_NBITS) {
-            // Normalise by a power of two so |a_hat| < 2, then fold in the
-            // code position: a' = a_hat * 2^(126 - pos); a' * subnormal(q at
-            // pos) = a_hat * q * 2^-23, exactly as with ordinary operands.
             const uint32_t ex = (__float_as_uint(amax) >> 23) & 0xFFu;
             int E = ex == 0u ? -126 : (ex == 255u ? 0 : static_cast<int>(ex) - 127);
             if (amax == 0.f) E = 0;
@@ -270,6 +243,45 @@ __device__ __forceinline__ void load_activations(const GemvArgs &p, int sl, bool
     }
 }
 
+// Load this lane's activations for expert slot `sl` of a fused QMoE fc2: one
+// row h = silu(gate) * up of that slot's fc1 output (gate = g[0:K], up =
+// g[K:2K], or the even / odd elements), then normalise them.
+template <int BITS, int MT, int KPL, int BPL, int WK>
+__device__ __forceinline__ void load_swiglu_activations(const GemvArgs &p, int sl, bool lane_active, int k0,
+                                                        float (&ap)[MT][KPL], float (&e2)[MT], float (&ahat)[MT][BPL]) {
+    static_assert(KPL % 8 == 0, "activation vectors are 8 elements");
+    static_assert(MT == 1, "one activation row");
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) ap[0][i] = 0.f;
+    if (lane_active) {
+        // 8 values at a time to keep registers low
+        const float *gs = p.gbuf + static_cast<size_t>(sl) * 2 * p.K;
+#pragma unroll
+        for (int c = 0; c < KPL; c += 8) {
+            float gate[8], up[8];
+            if (p.swiglu_interleaved) {
+                const float4 *q = reinterpret_cast<const float4 *>(gs + 2 * (k0 + c));
+                const float4 v0 = q[0], v1 = q[1], v2 = q[2], v3 = q[3];
+                gate[0] = v0.x; up[0] = v0.y; gate[1] = v0.z; up[1] = v0.w;
+                gate[2] = v1.x; up[2] = v1.y; gate[3] = v1.z; up[3] = v1.w;
+                gate[4] = v2.x; up[4] = v2.y; gate[5] = v2.z; up[5] = v2.w;
+                gate[6] = v3.x; up[6] = v3.y; gate[7] = v3.z; up[7] = v3.w;
+            } else {
+                const float4 *qg = reinterpret_cast<const float4 *>(gs + k0 + c);
+                const float4 *qu = reinterpret_cast<const float4 *>(gs + p.K + k0 + c);
+                const float4 g0 = qg[0], g1 = qg[1], u0 = qu[0], u1 = qu[1];
+                gate[0] = g0.x; gate[1] = g0.y; gate[2] = g0.z; gate[3] = g0.w;
+                gate[4] = g1.x; gate[5] = g1.y; gate[6] = g1.z; gate[7] = g1.w;
+                up[0] = u0.x; up[1] = u0.y; up[2] = u0.z; up[3] = u0.w;
+                up[4] = u1.x; up[5] = u1.y; up[6] = u1.z; up[7] = u1.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ap[0][c + i] = gate[i] / (1.f + expf(-gate[i])) * up[i];
+        }
+    }
+    prepare_activations<BITS, MT, KPL, BPL, WK>(ap, e2, ahat);
+}
+
 // Producer side of a tile: add the S slice sums of each of the tile's rows in
 // slice order and write the outputs (Y, split-K partials, or the QMoE slot
 // outputs with the expert's bias).  `rs` holds [slice][kRedV * H] values.
@@ -280,7 +292,7 @@ __device__ __forceinline__ void finish_tile(const GemvArgs &p, const float *rs, 
     if (lane >= VPW) return;
     float sum = 0.f;
     for (int s = 0; s < s_count; ++s) sum += rs[s * VPW + lane];
-    const int sl = tile / p.tiles_per_slot;
+    const int sl = p.ids ? tile / p.tiles_per_slot : 0;
     const int rbase = (tile - sl * p.tiles_per_slot) * p.SR;
     const int hh = lane / kRedV, v = lane % kRedV;
     const int i = v / MT, m = v % MT;
@@ -369,7 +381,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
                 }
                 finish_tile<MT, LPR>(p, red + slot * (p.S_cta * kRedV * H), s_count, tile - p.NST * gridDim.x, lane);
             }
-            const int sl = tile / p.tiles_per_slot;
+            const int sl = p.ids ? tile / p.tiles_per_slot : 0;
             const int r0 = (tile - sl * p.tiles_per_slot) * p.SR;
             const int e = p.ids ? __ldg(p.ids + sl) : 0;
             const bool valid = e >= 0 && e < p.num_experts;
@@ -379,6 +391,20 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
             const unsigned char *Pb = p.params + es * p.p_slot_stride;
             const unsigned char *Zb = reinterpret_cast<const unsigned char *>(p.zp) + es * p.z_slot_stride;
             unsigned char *st = stages + static_cast<size_t>(slot) * p.stage_bytes;
+            if (p.fast_tx && rows == p.SR && !split) {  // warp-uniform: a whole stage, every copy 16-byte aligned
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[slot], p.fast_tx);
+                    bulk_g2s(st, Wb + static_cast<size_t>(r0) * p.row_bytes, p.SR * p.row_bytes, &full[slot]);
+                    bulk_g2s(st + p.s_off, Pb + static_cast<size_t>(r0) * prow, p.SR * prow, &full[slot]);
+                    if (p.zp_mode == ZP_TENSOR)
+                        bulk_g2s(st + p.z_off, Zb + static_cast<size_t>(r0) * p.nb * 2, p.SR * p.nb * 2, &full[slot]);
+                }
+                if (++slot == p.NST) {
+                    slot = 0;
+                    par ^= 1u;
+                }
+                continue;
+            }
             uint32_t tx = 0;
             // codes
             if (!split) {
@@ -478,6 +504,28 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     float zah[MT][BPL];  // zp * ahat for a zero point that is the same for every row
     int cur_slot = -1;
     pdl_wait();  // activations, the fc1 output and Y belong to the preceding kernel's world
+    if constexpr (AM == A_ROWS) {
+        // the same activations serve every tile (and every expert slot): load them once
+        float *as = reinterpret_cast<float *>(smem + p.a_off);
+        stage_activations<MT, KPL>(p, as, kc0, p.S_cta * LPR, threadIdx.x, NWC * 32);
+        named_bar_sync(1, NWC * 32);
+        const float *mine = as + (sigma * LPR + gl) * (KPL + 4);
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int j = 0; j < KPL / 4; ++j) {
+                const float4 v = *reinterpret_cast<const float4 *>(mine + m * p.a_rstride + 4 * j);
+                ap[m][4 * j] = v.x;
+                ap[m][4 * j + 1] = v.y;
+                ap[m][4 * j + 2] = v.z;
+                ap[m][4 * j + 3] = v.w;
+            }
+        prepare_activations<BITS, MT, KPL, BPL, WK>(ap, e2, ahat);
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int b = 0; b < BPL; ++b) zah[m][b] = p.zpv * ahat[m][b];
+    }
 
     // group g consumes the CTA's tiles g, g + G, g + 2G, ... (stage `it` holds
     // tile it); ring slot, phase parity, expert slot and tile are advanced
@@ -503,8 +551,8 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
                 e = __ldg(p.ids + sl);
                 valid = e >= 0 && e < p.num_experts;
             }
-            if (cur_slot < 0 || AM == A_SWIGLU) {
-                load_activations<BITS, MT, KPL, BPL, WK, AM>(p, sl, lane_active, k0, ap, e2, ahat);
+            if constexpr (AM == A_SWIGLU) {
+                load_swiglu_activations<BITS, MT, KPL, BPL, WK>(p, sl, lane_active, k0, ap, e2, ahat);
 #pragma unroll
                 for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -636,6 +684,7 @@ struct Cfg {
     int vec, lpr, mt, bpl;
     int S_total, S_cta, splits, G, SR, NST;
     int w_pitch, stage_bytes, s_off, z_off, red_off, stage_off, smem, ntiles, grid_x;
+    int a_off, a_rstride;
 };
 
 inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -692,7 +741,10 @@ bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, 
     c.SR = (kRedV / c.mt) * (32 / c.lpr);
     c.G = std::max(1, maxw / c.S_cta);
     c.w_pitch = c.splits > 1 ? round_up(c.S_cta * c.lpr * c.vec, 16) : row_bytes;
-    c.stage_off = round_up(kLutOff + (kind == WK_CODEBOOK ? 16 * 32 * 4 : 0), 1024);
+    // activation staging: MT rows x S_cta slices x LPR lanes x (KPL + 4) floats
+    c.a_off = round_up(kLutOff + (kind == WK_CODEBOOK ? 16 * 32 * 4 : 0), 128);
+    c.a_rstride = c.S_cta * c.lpr * (kpl + 4);
+    c.stage_off = round_up(c.a_off + c.mt * c.a_rstride * 4, 1024);
     const int budget = di.max_smem_optin - c.stage_off;
     c.s_off = round_up(c.SR * c.w_pitch, 128);
     c.z_off = c.s_off + round_up(c.SR * nb * pb, 128);
@@ -786,6 +838,19 @@ cudaError_t dispatch(const GemvArgs &a, const Cfg &c, int bits, int kind, cudaSt
     return cudaErrorNotSupported;
 }
 
+// Whole-stage byte count for the producer's fast path, or 0 when a whole
+// stage's copies are not all multiples of 16 bytes (then every stage takes the
+// general path).  Base pointers and expert strides must be 16-byte multiples.
+int fast_stage_tx(const GemvArgs &a, const Cfg &c, int pb) {
+    if (c.splits > 1) return 0;
+    const long long code = static_cast<long long>(c.SR) * a.row_bytes;
+    const long long par = static_cast<long long>(c.SR) * a.nb * pb;
+    const long long zp = a.zp_mode == ZP_TENSOR ? static_cast<long long>(c.SR) * a.nb * 2 : 0;
+    if (code % 16 || par % 16 || zp % 16) return 0;
+    if (a.ids && (a.w_slot_stride % 16 || a.p_slot_stride % 16 || a.z_slot_stride % 16)) return 0;
+    return static_cast<int>(code + par + zp);
+}
+
 void fill_args(GemvArgs &a, const Cfg &c) {
     a.S_total = c.S_total;
     a.S_cta = c.S_cta;
@@ -797,6 +862,8 @@ void fill_args(GemvArgs &a, const Cfg &c) {
     a.s_off = c.s_off;
     a.z_off = c.z_off;
     a.red_off = c.red_off;
+    a.a_off = c.a_off;
+    a.a_rstride = c.a_rstride;
     a.stage_off = c.stage_off;
     a.fault = fault_word();
 }
@@ -843,6 +910,7 @@ cudaError_t simt_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStrea
         if (!ws || ws_bytes < need) return cudaErrorInvalidValue;  // checked by the caller first
         a.partial = static_cast<float *>(ws);
     }
+    a.fast_tx = fast_stage_tx(a, c, p.kind == WK_CODEBOOK ? 4 : 2);
     for (int m0 = 0; m0 < p.M; m0 += c.mt) {
         a.m0 = m0;
         cudaError_t e = dispatch(a, c, p.bits, p.kind, s);
@@ -909,6 +977,7 @@ cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s) {
         a.out_f32 = fc1 ? g : o;
         a.bias = fc1 ? q.fc1_bias : q.fc2_bias;
         c.grid_x = std::min(a.ntiles, di.sm_count);
+        a.fast_tx = fast_stage_tx(a, c, 2);
         cudaError_t e = dispatch(a, c, q.bits, WK_NBITS, s);
         if (e != cudaSuccess) return e;
     }
