@@ -148,6 +148,71 @@ __device__ __forceinline__ void dot_word_codebook(uint32_t x, const float (&ap)[
     }
 }
 
+// One tile's dot products for one lane: ITER rows (stride `row_stride` in the
+// stage) times this lane's KPL codes, scaled per block; racc[i * MT + m] gets
+// row i, activation row m.  ZPT: a zero point per block and row (else the
+// scalar zero point folded into zah).
+template <bool ZPT, int BITS, int VEC, int MT, int BPL, int WK, int ITER, int KPL = VEC / 4 * (32 / BITS)>
+__device__ __forceinline__ void tile_dot(const unsigned char *wp, const unsigned char *sp, const unsigned char *zpp,
+                                         int row_stride, int prow_stride, int zrow_stride, const float (&ap)[MT][KPL],
+                                         const float (&e2)[MT], const float (&ahat)[MT][BPL],
+                                         const float (&zah)[MT][BPL], const float *lut_lane, float (&racc)[kRedV]) {
+    constexpr int WPL = VEC / 4;
+#pragma unroll
+    for (int i = 0; i < ITER; ++i) {
+        uint32_t x[WPL];
+        load_words<VEC>(wp, x);
+        float rv[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) rv[m] = 0.f;
+#pragma unroll
+        for (int b = 0; b < BPL; ++b) {
+            float2 acc0[MT], acc1[MT];
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc0[m] = acc1[m] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = b * (WPL / BPL); j < (b + 1) * (WPL / BPL); ++j) {
+                if constexpr (WK == WK_NBITS) {
+                    if (j & 1) dot_word_nbits<BITS, MT, KPL>(x[j], ap, j, acc1);
+                    else dot_word_nbits<BITS, MT, KPL>(x[j], ap, j, acc0);
+                } else {
+                    if (j & 1) dot_word_codebook<MT, KPL>(x[j], ap, j, acc1, lut_lane);
+                    else dot_word_codebook<MT, KPL>(x[j], ap, j, acc0, lut_lane);
+                }
+            }
+            if constexpr (WK == WK_NBITS) {
+                const float s = h2f(*reinterpret_cast<const uint16_t *>(sp + b * 2));
+                if constexpr (ZPT) {
+                    const float z = h2f(*reinterpret_cast<const uint16_t *>(zpp + b * 2));
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        const float P = (acc0[m].x + acc0[m].y) + (acc1[m].x + acc1[m].y);
+                        rv[m] = fmaf(s, fmaf(P, 8388608.f, -(z * ahat[m][b])), rv[m]);
+                    }
+                } else {
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        const float P = (acc0[m].x + acc0[m].y) + (acc1[m].x + acc1[m].y);
+                        rv[m] = fmaf(s, fmaf(P, 8388608.f, -zah[m][b]), rv[m]);
+                    }
+                }
+            } else {
+                const float am = *reinterpret_cast<const float *>(sp + b * 4);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const float P = (acc0[m].x + acc0[m].y) + (acc1[m].x + acc1[m].y);
+                    rv[m] = fmaf(am, P, rv[m]);
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) racc[i * MT + m] = rv[m] * e2[m];
+        wp += row_stride;
+        sp += prow_stride;
+        zpp += zrow_stride;
+    }
+}
+
 // Fixed-order transposed reduction of V values held by each lane of an
 // LPR-lane group: returns, on lane l, the group sum of value index
 // (l % LPR) / (LPR / V).
@@ -282,6 +347,72 @@ __device__ __forceinline__ void load_swiglu_activations(const GemvArgs &p, int s
     prepare_activations<BITS, MT, KPL, BPL, WK>(ap, e2, ahat);
 }
 
+// General stage fill (ragged last tile, split K, unaligned sizes, invalid
+// expert): lane parts first, then the expected byte count, then the bulk parts.
+template <int LPR, int VEC, int BITS>
+__device__ __forceinline__ void fill_stage_general(const GemvArgs &p, unsigned char *st, const unsigned char *Wb,
+                                                   const unsigned char *Pb, const unsigned char *Zb, int r0, int rows,
+                                                   bool split, int kb0, int kb1, int prow, uint64_t *fullb, int lane) {
+    uint32_t tx = 0;
+    // codes
+    if (!split) {
+        const unsigned char *src = Wb + static_cast<size_t>(r0) * p.row_bytes;
+        const uint32_t bytes = static_cast<uint32_t>(rows) * p.row_bytes;
+        const CopyPlan cp = copy_plan(st, src, bytes);
+        copy_tail_lanes(st, src, bytes, cp, lane);
+        tx += cp.bulk_bytes;
+    } else {
+        for (int r = 0; r < rows; ++r) {
+            const unsigned char *src = Wb + static_cast<size_t>(r0 + r) * p.row_bytes + kb0;
+            unsigned char *dst = st + r * p.w_pitch;
+            const CopyPlan cp = copy_plan(dst, src, kb1 - kb0);
+            copy_tail_lanes(dst, src, kb1 - kb0, cp, lane);
+            tx += cp.bulk_bytes;
+        }
+    }
+    // block parameters (scales or absmax), then zero points
+    {
+        const unsigned char *src = Pb + static_cast<size_t>(r0) * prow;
+        const CopyPlan cp = copy_plan(st + p.s_off, src, rows * prow);
+        copy_tail_lanes(st + p.s_off, src, rows * prow, cp, lane);
+        tx += cp.bulk_bytes;
+    }
+    if (p.zp_mode == ZP_TENSOR) {
+        const unsigned char *src = Zb + static_cast<size_t>(r0) * p.nb * 2;
+        const CopyPlan cp = copy_plan(st + p.z_off, src, rows * p.nb * 2);
+        copy_tail_lanes(st + p.z_off, src, rows * p.nb * 2, cp, lane);
+        tx += cp.bulk_bytes;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(fullb, tx);
+    __syncwarp();
+    // issue the bulk parts (after the expected byte count is registered)
+    if (!split) {
+        if (lane == 0) {
+            const unsigned char *src = Wb + static_cast<size_t>(r0) * p.row_bytes;
+            const CopyPlan cp = copy_plan(st, src, static_cast<uint32_t>(rows) * p.row_bytes);
+            if (cp.bulk_bytes) bulk_g2s(st, src, cp.bulk_bytes, fullb);
+        }
+    } else {
+        for (int r = lane; r < rows; r += 32) {
+            const unsigned char *src = Wb + static_cast<size_t>(r0 + r) * p.row_bytes + kb0;
+            unsigned char *dst = st + r * p.w_pitch;
+            const CopyPlan cp = copy_plan(dst, src, kb1 - kb0);
+            if (cp.bulk_bytes) bulk_g2s(dst, src, cp.bulk_bytes, fullb);
+        }
+    }
+    if (lane == 1) {
+        const unsigned char *src = Pb + static_cast<size_t>(r0) * prow;
+        const CopyPlan cp = copy_plan(st + p.s_off, src, rows * prow);
+        if (cp.bulk_bytes) bulk_g2s(st + p.s_off, src, cp.bulk_bytes, fullb);
+    }
+    if (lane == 2 && p.zp_mode == ZP_TENSOR) {
+        const unsigned char *src = Zb + static_cast<size_t>(r0) * p.nb * 2;
+        const CopyPlan cp = copy_plan(st + p.z_off, src, rows * p.nb * 2);
+        if (cp.bulk_bytes) bulk_g2s(st + p.z_off, src, cp.bulk_bytes, fullb);
+    }
+}
+
 // Producer side of a tile: add the S slice sums of each of the tile's rows in
 // slice order and write the outputs (Y, split-K partials, or the QMoE slot
 // outputs with the expert's bias).  `rs` holds [slice][kRedV * H] values.
@@ -374,13 +505,6 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
                 alive = false;
                 break;
             }
-            if (it >= p.NST) {
-                if (!waited) {
-                    pdl_wait();  // outputs may be read by the preceding kernel until it completes
-                    waited = true;
-                }
-                finish_tile<MT, LPR>(p, red + slot * (p.S_cta * kRedV * H), s_count, tile - p.NST * gridDim.x, lane);
-            }
             const int sl = p.ids ? tile / p.tiles_per_slot : 0;
             const int r0 = (tile - sl * p.tiles_per_slot) * p.SR;
             const int e = p.ids ? __ldg(p.ids + sl) : 0;
@@ -399,69 +523,18 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
                     if (p.zp_mode == ZP_TENSOR)
                         bulk_g2s(st + p.z_off, Zb + static_cast<size_t>(r0) * p.nb * 2, p.SR * p.nb * 2, &full[slot]);
                 }
-                if (++slot == p.NST) {
-                    slot = 0;
-                    par ^= 1u;
-                }
-                continue;
-            }
-            uint32_t tx = 0;
-            // codes
-            if (!split) {
-                const unsigned char *src = Wb + static_cast<size_t>(r0) * p.row_bytes;
-                const uint32_t bytes = static_cast<uint32_t>(rows) * p.row_bytes;
-                const CopyPlan cp = copy_plan(st, src, bytes);
-                copy_tail_lanes(st, src, bytes, cp, lane);
-                tx += cp.bulk_bytes;
             } else {
-                for (int r = 0; r < rows; ++r) {
-                    const unsigned char *src = Wb + static_cast<size_t>(r0 + r) * p.row_bytes + kb0;
-                    unsigned char *dst = st + r * p.w_pitch;
-                    const CopyPlan cp = copy_plan(dst, src, kb1 - kb0);
-                    copy_tail_lanes(dst, src, kb1 - kb0, cp, lane);
-                    tx += cp.bulk_bytes;
+                fill_stage_general<LPR, VEC, BITS>(p, st, Wb, Pb, Zb, r0, rows, split, kb0, kb1, prow, &full[slot], lane);
+            }
+            // finish the tile this slot held before the refill (its sums sit in
+            // the reduction slot of the previous fill's parity)
+            if (it >= p.NST) {
+                if (!waited) {
+                    pdl_wait();  // outputs may be read by the preceding kernel until it completes
+                    waited = true;
                 }
-            }
-            // block parameters (scales or absmax), then zero points
-            {
-                const unsigned char *src = Pb + static_cast<size_t>(r0) * prow;
-                const CopyPlan cp = copy_plan(st + p.s_off, src, rows * prow);
-                copy_tail_lanes(st + p.s_off, src, rows * prow, cp, lane);
-                tx += cp.bulk_bytes;
-            }
-            if (p.zp_mode == ZP_TENSOR) {
-                const unsigned char *src = Zb + static_cast<size_t>(r0) * p.nb * 2;
-                const CopyPlan cp = copy_plan(st + p.z_off, src, rows * p.nb * 2);
-                copy_tail_lanes(st + p.z_off, src, rows * p.nb * 2, cp, lane);
-                tx += cp.bulk_bytes;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(&full[slot], tx);
-            __syncwarp();
-            // issue the bulk parts (after the expected byte count is registered)
-            if (!split) {
-                if (lane == 0) {
-                    const unsigned char *src = Wb + static_cast<size_t>(r0) * p.row_bytes;
-                    const CopyPlan cp = copy_plan(st, src, static_cast<uint32_t>(rows) * p.row_bytes);
-                    if (cp.bulk_bytes) bulk_g2s(st, src, cp.bulk_bytes, &full[slot]);
-                }
-            } else {
-                for (int r = lane; r < rows; r += 32) {
-                    const unsigned char *src = Wb + static_cast<size_t>(r0 + r) * p.row_bytes + kb0;
-                    unsigned char *dst = st + r * p.w_pitch;
-                    const CopyPlan cp = copy_plan(dst, src, kb1 - kb0);
-                    if (cp.bulk_bytes) bulk_g2s(dst, src, cp.bulk_bytes, &full[slot]);
-                }
-            }
-            if (lane == 1) {
-                const unsigned char *src = Pb + static_cast<size_t>(r0) * prow;
-                const CopyPlan cp = copy_plan(st + p.s_off, src, rows * prow);
-                if (cp.bulk_bytes) bulk_g2s(st + p.s_off, src, cp.bulk_bytes, &full[slot]);
-            }
-            if (lane == 2 && p.zp_mode == ZP_TENSOR) {
-                const unsigned char *src = Zb + static_cast<size_t>(r0) * p.nb * 2;
-                const CopyPlan cp = copy_plan(st + p.z_off, src, rows * p.nb * 2);
-                if (cp.bulk_bytes) bulk_g2s(st + p.z_off, src, cp.bulk_bytes, &full[slot]);
+                finish_tile<MT, LPR>(p, red + (slot * 2 + par) * (p.S_cta * kRedV * H), s_count,
+                                     tile - p.NST * gridDim.x, lane);
             }
             if (++slot == p.NST) {
                 slot = 0;
@@ -474,7 +547,8 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
             for (int j = max(0, it - p.NST); j < it; ++j) {
                 const int sj = j % p.NST;
                 if (!mbar_wait(&empty[sj], (j / p.NST) & 1, abort_flag, p.fault, FAULT_WAIT_EMPTY)) break;
-                finish_tile<MT, LPR>(p, red + sj * (p.S_cta * kRedV * H), s_count, blockIdx.x + j * gridDim.x, lane);
+                finish_tile<MT, LPR>(p, red + (sj * 2 + ((j / p.NST) & 1)) * (p.S_cta * kRedV * H), s_count,
+                                     blockIdx.x + j * gridDim.x, lane);
             }
         }
         return;
@@ -566,69 +640,21 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
 #pragma unroll
         for (int v = 0; v < kRedV; ++v) racc[v] = 0.f;
         if (ok && valid) {  // warp-uniform
-            const int rt0 = half;  // this lane's first row in the tile
-            const unsigned char *wp = st + rt0 * p.w_pitch + lane_boff;
-            const unsigned char *sp = st + p.s_off + (rt0 * p.nb + blk0) * PB;
-            const unsigned char *zpp = st + p.z_off + (rt0 * p.nb + blk0) * 2;
-#pragma unroll
-            for (int i = 0; i < ITER; ++i) {
-                uint32_t x[WPL];
-                load_words<VEC>(wp, x);
-                float rv[MT];
-#pragma unroll
-                for (int m = 0; m < MT; ++m) rv[m] = 0.f;
-#pragma unroll
-                for (int b = 0; b < BPL; ++b) {
-                    float2 acc0[MT], acc1[MT];
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) acc0[m] = acc1[m] = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int j = b * (WPL / BPL); j < (b + 1) * (WPL / BPL); ++j) {
-                        if constexpr (WK == WK_NBITS) {
-                            if (j & 1) dot_word_nbits<BITS, MT, KPL>(x[j], ap, j, acc1);
-                            else dot_word_nbits<BITS, MT, KPL>(x[j], ap, j, acc0);
-                        } else {
-                            if (j & 1) dot_word_codebook<MT, KPL>(x[j], ap, j, acc1, lut_lane);
-                            else dot_word_codebook<MT, KPL>(x[j], ap, j, acc0, lut_lane);
-                        }
-                    }
-                    if constexpr (WK == WK_NBITS) {
-                        const float s = h2f(*reinterpret_cast<const uint16_t *>(sp + b * 2));
-                        if (p.zp_mode == ZP_TENSOR) {
-                            const float z = h2f(*reinterpret_cast<const uint16_t *>(zpp + b * 2));
-#pragma unroll
-                            for (int m = 0; m < MT; ++m) {
-                                const float P = (acc0[m].x + acc0[m].y) + (acc1[m].x + acc1[m].y);
-                                rv[m] = fmaf(s, fmaf(P, 8388608.f, -(z * ahat[m][b])), rv[m]);
-                            }
-                        } else {
-#pragma unroll
-                            for (int m = 0; m < MT; ++m) {
-                                const float P = (acc0[m].x + acc0[m].y) + (acc1[m].x + acc1[m].y);
-                                rv[m] = fmaf(s, fmaf(P, 8388608.f, -zah[m][b]), rv[m]);
-                            }
-                        }
-                    } else {
-                        const float am = *reinterpret_cast<const float *>(sp + b * 4);
-#pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            const float P = (acc0[m].x + acc0[m].y) + (acc1[m].x + acc1[m].y);
-                            rv[m] = fmaf(am, P, rv[m]);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int m = 0; m < MT; ++m) racc[i * MT + m] = rv[m] * e2[m];
-                wp += row_stride;
-                sp += prow_stride;
-                zpp += zrow_stride;
-            }
+            const unsigned char *wp = st + half * p.w_pitch + lane_boff;  // this lane's first row is `half`
+            const unsigned char *sp = st + p.s_off + (half * p.nb + blk0) * PB;
+            const unsigned char *zpp = st + p.z_off + (half * p.nb + blk0) * 2;
+            if (WK == WK_NBITS && p.zp_mode == ZP_TENSOR)
+                tile_dot<true, BITS, VEC, MT, BPL, WK, ITER>(wp, sp, zpp, row_stride, prow_stride, zrow_stride, ap, e2,
+                                                            ahat, zah, lut_lane, racc);
+            else
+                tile_dot<false, BITS, VEC, MT, BPL, WK, ITER>(wp, sp, zpp, row_stride, prow_stride, zrow_stride, ap, e2,
+                                                             ahat, zah, lut_lane, racc);
 #pragma unroll
             for (int v = 0; v < kRedV; ++v) racc[v] = lane_active ? racc[v] : 0.f;
         }
         // lane l now holds, for row half `half`, the slice sum of value (l % LPR) / (LPR / kRedV)
         const float tot = transpose_reduce<kRedV, LPR>(racc, lane);
-        if (writer) red[slot * (p.S_cta * VPW) + red_idx] = tot;
+        if (writer) red[(slot * 2 + par) * (p.S_cta * VPW) + red_idx] = tot;
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);  // releases the stage and this warp's slice sums
 
@@ -751,7 +777,7 @@ bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, 
     c.stage_bytes = c.z_off + (zp_tensor ? round_up(c.SR * nb * 2, 128) : 0);
     // each stage also has a reduction slot: S_cta slices x kRedV x H sums
     const int red_slot = c.S_cta * kRedV * (32 / c.lpr) * 4;
-    const int nfit = std::min(kMaxStages, budget / (c.stage_bytes + red_slot));
+    const int nfit = std::min(kMaxStages, budget / (c.stage_bytes + 2 * red_slot));
     if (nfit < 2) return false;
     // Ring slots are owned by row groups: slot s serves group s % G only, so
     // NST is a multiple of G.  A group then waits on a slot's phase k only
@@ -762,7 +788,7 @@ bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, 
     c.G = std::max(1, std::min(c.G, nfit / 2));
     c.NST = nfit - nfit % c.G;
     c.red_off = c.stage_off + c.NST * c.stage_bytes;
-    c.smem = c.red_off + c.NST * red_slot;
+    c.smem = c.red_off + 2 * c.NST * red_slot;  // reduction slots double-buffered by fill parity
     c.ntiles = (N + c.SR - 1) / c.SR;
     c.grid_x = std::min(c.ntiles, di.sm_count);
     (void)M;
