@@ -44,13 +44,31 @@
 namespace qg {
 namespace {
 
-constexpr int kBM = 128;
+constexpr int kBM = 256;  // activation rows per CTA tile: two MMA halves of kMH rows sharing the weight tile
+constexpr int kMH = 128;
 constexpr int kBK = 64;
-// pipeline depth: 4 stages, 3 for the widest tile (shared-memory budget)
-__host__ __device__ constexpr int stages_for(int bn) { return bn >= 256 ? 3 : 4; }
-constexpr int kThreads = 320;         // warp 0 TMA, warp 1 MMA, warps 2-9 dequant + epilogue
-constexpr int kDequantThreads = 256;
-constexpr int kParamBox = 16;         // bytes of block parameters per weight row per stage (one TMA box column)
+constexpr int kDequantThreads = 512;  // 16 dequant + epilogue warps
+constexpr int kThreads = 64 + kDequantThreads;  // warp 0 TMA, warp 1 MMA, warps 2-17 dequant + epilogue
+constexpr int kParamBox = 16;         // bytes of block parameters per weight row per super-stage (one TMA box column)
+constexpr int kCodeBox = 64;          // bytes of packed codes per weight row per super-stage
+constexpr int kCodeSlots = 2;         // super-stages of codes / parameters in flight
+constexpr int kSmemBudget = 227 * 1024;
+constexpr int kSmemFixed = 1024 + 4096;  // alignment slack + barriers, tensor-memory slot, codebook table
+// Three buffers:
+//  * the activation ring: NA K steps of 128 x 64 activations (one TMA tile each),
+//    released when the step's MMAs finish;
+//  * the code ring: kCodeSlots super-stages of CS = kCodeBox / (64 * bits / 8)
+//    K steps, holding the packed codes (kCodeBox bytes per weight row) and one
+//    box of block parameters (and zero points) per weight row, released by the
+//    dequant warps -- far fewer and larger TMA rows than one small box per step;
+//  * two buffers of dequantized weights (the MMA's B operand).
+__host__ __device__ constexpr int code_slot_bytes(int bn) { return bn * (kCodeBox + 2 * kParamBox); }
+__host__ __device__ constexpr int wdq_bytes(int bn) { return bn * kBK * 2; }
+__host__ __device__ constexpr int act_slots(int bn) {
+    return (kSmemBudget - kSmemFixed - 2 * wdq_bytes(bn) - kCodeSlots * code_slot_bytes(bn)) / (kBM * kBK * 2) > 8
+               ? 8
+               : (kSmemBudget - kSmemFixed - 2 * wdq_bytes(bn) - kCodeSlots * code_slot_bytes(bn)) / (kBM * kBK * 2);
+}
 
 struct TcArgs {
     const uint16_t *scales;  // nbits, [N][nb] fp16
@@ -208,30 +226,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constant__ CUtensorMap code_map,
                    const __grid_constant__ CUtensorMap par_map, const __grid_constant__ CUtensorMap zp_map,
                    const TcArgs p) {
-    constexpr int kStages = stages_for(BN);
-    constexpr int CB = kBK * BITS / 8;           // code bytes per row per stage
-    constexpr int ACT_BYTES = kBM * kBK * 2;     // 16 KB
-    constexpr int WDQ_BYTES = BN * kBK * 2;
-    constexpr int CODE_BYTES = BN * CB;
+    constexpr int NS = act_slots(BN);
+    static_assert(NS >= 3, "shared memory too small for the activation ring");
+    constexpr int CB = kBK * BITS / 8;           // code bytes per row per K step
+    constexpr int CS = kCodeBox / CB;            // K steps per super-stage
+    constexpr int ACT_BYTES = kBM * kBK * 2;     // 32 KB: two 128-row halves, 16 KB apart
+    constexpr int WDQ_BYTES = wdq_bytes(BN);
+    constexpr int CODE_BYTES = BN * kCodeBox;
     constexpr int PAR_BYTES = BN * kParamBox;
     constexpr int PE = WK == WK_CODEBOOK ? 4 : 2;  // bytes per block parameter
     constexpr int PPB = kParamBox / PE;            // parameters per box row
-    constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+    constexpr uint32_t TMEM_COLS = 2 * BN;       // one BN-column accumulator per 128-row half
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte alignment for the swizzled tiles (pointer arithmetic on the
     // shared array keeps the accesses in the shared address space)
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char *act_s = smem;
-    unsigned char *wdq_s = act_s + kStages * ACT_BYTES;
-    unsigned char *code_s = wdq_s + kStages * WDQ_BYTES;
-    unsigned char *par_s = code_s + kStages * CODE_BYTES;
-    unsigned char *zp_s = par_s + kStages * PAR_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(zp_s + kStages * PAR_BYTES);
-    uint64_t *full = bars;                 // TMA landed (count 1 + tx)
-    uint64_t *wfull = bars + kStages;      // dequantized weights written (count 4 warps)
-    uint64_t *empty = bars + 2 * kStages;  // MMAs of the stage finished (commit)
-    uint64_t *accf = bars + 3 * kStages;   // all MMAs finished
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * kStages + 1);
+    unsigned char *wdq_s = act_s + NS * ACT_BYTES;
+    unsigned char *code_s = wdq_s + 2 * WDQ_BYTES;
+    unsigned char *par_s = code_s + kCodeSlots * CODE_BYTES;
+    unsigned char *zp_s = par_s + kCodeSlots * PAR_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(zp_s + kCodeSlots * PAR_BYTES);
+    uint64_t *full = bars;                 // activation tile of a K step landed (count 1 + tx)
+    uint64_t *empty = bars + NS;           // the step's MMAs finished: activation slot free (commit)
+    uint64_t *wfull = bars + 2 * NS;       // dequantized weights written (count: dequant warps)
+    uint64_t *wempty = bars + 2 * NS + 2;  // MMAs reading a dequant buffer finished (commit)
+    uint64_t *accf = bars + 2 * NS + 4;    // all MMAs finished
+    uint64_t *cfull = bars + 2 * NS + 5;   // codes + parameters of a super-stage landed (count 1 + tx)
+    uint64_t *cempty = cfull + kCodeSlots; // the dequant warps are done with a code slot (count: dequant warps)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cempty + kCodeSlots);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *lut = reinterpret_cast<float *>(tmem_slot + 4);  // 16 x 32 floats (codebook)
 
@@ -242,10 +265,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nks = max(0, ks1 - ks0);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&wfull[s], kDequantThreads / 32);
             mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&wfull[b], kDequantThreads / 32);
+            mbar_init(&wempty[b], 1);
+        }
+        for (int c = 0; c < kCodeSlots; ++c) {
+            mbar_init(&cfull[c], 1);
+            mbar_init(&cempty[c], kDequantThreads / 32);
         }
         mbar_init(accf, 1);
         *abort_flag = 0;
@@ -265,37 +295,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             pdl_wait();  // activations may come from the preceding kernel; everything else follows this producer
+            const bool zt = WK == WK_NBITS && p.zp_mode == ZP_TENSOR;
             for (int i = 0; i < nks; ++i) {
-                const int s = i % kStages;
-                if (!mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1, abort_flag, p.fault, FAULT_WAIT_TC)) break;
-                const bool zt = WK == WK_NBITS && p.zp_mode == ZP_TENSOR;
-                mbar_arrive_expect_tx(&full[s], ACT_BYTES + CODE_BYTES + PAR_BYTES * (zt ? 2 : 1));
                 const int ks = ks0 + i;
-                const int pcol = (ks * kBK / p.bs) / PPB * PPB;  // first parameter column of the box
+                if (i % CS == 0) {  // codes and block parameters of the next CS steps
+                    const int j = i / CS, c = j % kCodeSlots;
+                    if (!mbar_wait(&cempty[c], ((j / kCodeSlots) & 1) ^ 1, abort_flag, p.fault, FAULT_WAIT_TC)) break;
+                    mbar_arrive_expect_tx(&cfull[c], CODE_BYTES + PAR_BYTES * (zt ? 2 : 1));
+                    const int pcol = (ks * kBK / p.bs) / PPB * PPB;  // first parameter column of the box
+                    tma_load_2d(code_s + c * CODE_BYTES, &code_map, ks * CB, n0, &cfull[c]);
+                    tma_load_2d(par_s + c * PAR_BYTES, &par_map, pcol, n0, &cfull[c]);
+                    if (zt) tma_load_2d(zp_s + c * PAR_BYTES, &zp_map, pcol, n0, &cfull[c]);
+                }
+                const int s = i % NS;
+                if (!mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, abort_flag, p.fault, FAULT_WAIT_TC)) break;
+                mbar_arrive_expect_tx(&full[s], ACT_BYTES);
                 tma_load_2d(act_s + s * ACT_BYTES, &act_map, ks * kBK, m0, &full[s]);
-                tma_load_2d(code_s + s * CODE_BYTES, &code_map, ks * CB, n0, &full[s]);
-                tma_load_2d(par_s + s * PAR_BYTES, &par_map, pcol, n0, &full[s]);
-                if (zt) tma_load_2d(zp_s + s * PAR_BYTES, &zp_map, pcol, n0, &full[s]);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(kBM, BN, BF16);
+            constexpr uint32_t idesc = idesc_f16(kMH, BN, BF16);
+            const bool two = m0 + kMH < p.M;  // the second half holds rows below M
             bool ok = true;
             for (int i = 0; i < nks && ok; ++i) {
-                const int s = i % kStages;
-                const uint32_t par = (i / kStages) & 1;
-                ok = mbar_wait(&full[s], par, abort_flag, p.fault, FAULT_WAIT_TC) &&
-                     mbar_wait(&wfull[s], par, abort_flag, p.fault, FAULT_WAIT_TC);
+                const int s = i % NS, b = i & 1;
+                ok = mbar_wait(&full[s], (i / NS) & 1, abort_flag, p.fault, FAULT_WAIT_TC) &&
+                     mbar_wait(&wfull[b], (i >> 1) & 1, abort_flag, p.fault, FAULT_WAIT_TC);
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t ad = sdesc_k128(smem_u32(act_s + s * ACT_BYTES));
-                const uint64_t bd = sdesc_k128(smem_u32(wdq_s + s * WDQ_BYTES));
+                const uint64_t ad1 = sdesc_k128(smem_u32(act_s + s * ACT_BYTES + kMH * kBK * 2));
+                const uint64_t bd = sdesc_k128(smem_u32(wdq_s + b * WDQ_BYTES));
 #pragma unroll
-                for (int k = 0; k < kBK / 16; ++k)  // +32 bytes per K=16 step inside the swizzle row
+                for (int k = 0; k < kBK / 16; ++k) {  // +32 bytes per K=16 step inside the swizzle row
                     umma_f16(tmem, ad + 2 * k, bd + 2 * k, idesc, (i > 0 || k > 0) ? 1u : 0u);
-                umma_commit(&empty[s]);
+                    if (two) umma_f16(tmem + BN, ad1 + 2 * k, bd + 2 * k, idesc, (i > 0 || k > 0) ? 1u : 0u);
+                }
+                umma_commit(&empty[s]);   // ring slot (activations, codes) free for the next TMA fill
+                umma_commit(&wempty[b]);  // dequant buffer free
             }
             umma_commit(accf);  // arrives when every MMA issued above has finished
         }
@@ -315,21 +354,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < UPT; ++j) {
             const int u = t + j * kDequantThreads;
             const int r = u >> 3, c = u & 7;
-            code_off[j] = r * CB + c * (CB / 8);
+            code_off[j] = r * kCodeBox + c * (CB / 8);
             wdq_off[j] = swz128(r, c);
             par_off[j] = r * kParamBox + ((8 * c) >> p.lbs) * PE;  // block of this chunk within the stage
         }
         const uint32_t zpu = __half_as_ushort(__float2half_rn(p.zpv)) * 0x10001u;
         const bool zt = WK == WK_NBITS && p.zp_mode == ZP_TENSOR;
         for (int i = 0; i < nks; ++i) {
-            const int s = i % kStages;
-            if (!mbar_wait(&full[s], (i / kStages) & 1, abort_flag, p.fault, FAULT_WAIT_TC)) break;
+            const int b = i & 1, j = i / CS, cslot = j % kCodeSlots;
+            if (i % CS == 0 && !mbar_wait(&cfull[cslot], (j / kCodeSlots) & 1, abort_flag, p.fault, FAULT_WAIT_TC)) break;
+            if (!mbar_wait(&wempty[b], ((i >> 1) & 1) ^ 1, abort_flag, p.fault, FAULT_WAIT_TC)) break;
             const int kb = (ks0 + i) * kBK;
             const int pc0 = ((kb >> p.lbs) % PPB) * PE;  // first block of the stage inside its parameter box
-            const unsigned char *__restrict__ cs = code_s + s * CODE_BYTES;
-            const unsigned char *__restrict__ ps = par_s + s * PAR_BYTES + pc0;
-            const unsigned char *__restrict__ zs = zp_s + s * PAR_BYTES + pc0;
-            unsigned char *__restrict__ ws = wdq_s + s * WDQ_BYTES;
+            const unsigned char *__restrict__ cs = code_s + cslot * CODE_BYTES + (i % CS) * CB;
+            const unsigned char *__restrict__ ps = par_s + cslot * PAR_BYTES + pc0;
+            const unsigned char *__restrict__ zs = zp_s + cslot * PAR_BYTES + pc0;
+            unsigned char *__restrict__ ws = wdq_s + b * WDQ_BYTES;
             uint32_t codes[UPT], pv[UPT], zv[UPT];
 #pragma unroll
             for (int j = 0; j < UPT; ++j) {
@@ -355,20 +395,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_async_smem();  // make the generic-proxy stores visible to the tensor core
             __syncwarp();
-            if (lane == 0) mbar_arrive(&wfull[s]);
+            if (lane == 0) {
+                mbar_arrive(&wfull[b]);
+                if (i % CS == CS - 1 || i == nks - 1) mbar_arrive(&cempty[cslot]);  // codes of this slot consumed
+            }
         }
         // ------------------------------------------------------------ epilogue
         const bool ok = mbar_wait(accf, 0, abort_flag, p.fault, FAULT_WAIT_TC);
         tc_fence_after();
         const int sub = warp & 3;  // tensor-memory sub-partition this warp may read
-        const int chalf = (warp - 2) >> 2;  // two warps share a sub-partition: each takes half the columns
-        const int m = m0 + sub * 32 + lane;
+        constexpr int NQ = kDequantThreads / 128;  // warps sharing a sub-partition split its columns
+        const int cq = (warp - 2) >> 2;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(sub * 32) << 16);
-        constexpr int CW = BN >= 64 ? BN / 2 : BN;
+        // columns [0, BN) hold rows m0 .. m0+127, [BN, 2 BN) rows m0+128 .. m0+255
+        constexpr int CW = 2 * BN / NQ >= 32 ? 2 * BN / NQ : 32;
 #pragma unroll 1
-        for (int c0 = chalf * CW; c0 < (chalf + 1) * CW && c0 < BN; c0 += 32) {
+        for (int cc = cq * CW; cc < (cq + 1) * CW && cc < 2 * BN; cc += 32) {
             uint32_t r[32];
-            tmem_ld32(lane_addr + c0, r);
+            tmem_ld32(lane_addr + cc, r);
+            const int h = cc / BN, c0 = cc - h * BN;
+            const int m = m0 + h * kMH + sub * 32 + lane;
             if (!ok || m >= p.M || nks == 0) continue;
             const int nb0 = n0 + c0;
             if (p.partial) {
@@ -431,9 +477,8 @@ struct TcCfg {
 };
 
 int smem_bytes(int bn, int bits) {
-    const int cb = kBK * bits / 8;
-    const int st = stages_for(bn);
-    return 1024 + st * (kBM * kBK * 2 + bn * kBK * 2 + bn * cb + 2 * bn * kParamBox) + 4 * st * 8 + 64 + 16 * 32 * 4;
+    (void)bits;
+    return kSmemFixed + act_slots(bn) * kBM * kBK * 2 + 2 * wdq_bytes(bn) + kCodeSlots * code_slot_bytes(bn);
 }
 
 // Static tile choice: the weight-tile width BN and the split of K that
@@ -448,15 +493,21 @@ TcCfg choose_tc(int M, int N, int K, int bits) {
         if (smem_bytes(bn, bits) > di.max_smem_optin) continue;
         const int nt = (N + bn - 1) / bn;
         for (int sp = 1; sp <= 16; sp *= 2) {
-            const int kps = (nk + sp - 1) / sp;
+            const int kps = ((nk + sp - 1) / sp + 3) / 4 * 4;  // whole code super-stages per split
             if (kps < 4 && sp > 1) break;
             const int splits = (nk + kps - 1) / kps;
             const long ctas = static_cast<long>(mt) * nt * splits;
-            if (splits > 1 && static_cast<long>(mt) * nt >= di.sm_count) break;  // split K only to fill the GPU
+            if (splits > 1 && static_cast<long>(mt) * nt >= 2L * di.sm_count) break;  // split K only to fill waves
             const long waves = (ctas + di.sm_count - 1) / di.sm_count;
-            // per-CTA time ~ k-steps x max(MMA time ~ bn, fixed dequant+issue cost) + fixed epilogue/fill
-            const double per_cta = kps * std::max(bn, 96) + 600.0 + (splits > 1 ? 200.0 : 0.0);
-            const double t = waves * per_cta;
+            // Per K step (units of about 1.4 ns): the MMAs, ~halves x bn (N=256 MMAs run at full rate,
+            // narrower ones lose about a third to shared-memory bandwidth), or the dequant, ~1.4 bn + a
+            // fixed cost, whichever is larger.  Plus the pipeline fill / epilogue per CTA, and for a
+            // split K the reduce: (splits + 1) x M x N fp32 through HBM.
+            const int halves = M > kMH ? 2 : 1;
+            const double mma = halves * bn * (bn >= 256 ? 1.0 : 1.45);
+            const double per_cta = kps * std::max(mma, 1.4 * bn + 100.0) + 800.0;
+            const double reduce = splits > 1 ? (splits + 1.0) * M * N * 4.0 / 9520.0 : 0.0;  // ~6.8 TB/s in these units
+            const double t = waves * per_cta + reduce;
             if (t < best_t * 0.97) {
                 best_t = t;
                 best = TcCfg{bn, splits, kps, nk, mt, nt};
@@ -524,7 +575,7 @@ cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_
         const int row_bytes = p.K * p.bits / 8;
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(p.N)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK * p.bits / 8), static_cast<cuuint32_t>(c.bn)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kCodeBox), static_cast<cuuint32_t>(c.bn)};
         const cuuint32_t es[2] = {1, 1};
         if (enc(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(p.W), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

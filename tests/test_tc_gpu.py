@@ -62,6 +62,8 @@ TC_CASES = [
     (128, 384, 4096, 4, 256, F16, "none", F16),
     (16, 96, 8192, 2, 64, F16, "uniform", F32),     # few tiles, long K: split-K
     (260, 1024, 1536, 2, 64, BF16, "tensor", F32),
+    (16, 256, 512, 2, 64, F16, "tensor", F32),      # 8 parameter columns: narrower than one parameter box
+    (40, 300, 2560, 4, 32, F16, "tensor", F32),     # 40 K steps: code super-stages of 2 steps for 4-bit codes
 ]
 
 
