@@ -79,8 +79,12 @@ struct TcArgs {
     const float *absmax;     // codebook, [N][nb]
     void *Y;
     int y_dtype;
-    float *partial;          // split-K partials [splits][M][N] or nullptr
-    int M, N, K, bs, lbs, nb, nk, ks_per_split;  // lbs = log2(bs)
+    float *partial;          // tail partials [tail tile x split][kBM][BN] (fp32)
+    int M, N, K, bs, lbs, nb, nk;  // lbs = log2(bs)
+    // Schedule: CTAs 0 .. full_tiles-1 compute whole tiles (whole K); the
+    // remaining tiles are split along K into tail_splits pieces of tail_kps
+    // steps each, one CTA per piece, summed afterwards in split order.
+    int nt, full_tiles, tail_splits, tail_kps;
     unsigned *fault;
 };
 
@@ -259,10 +263,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *lut = reinterpret_cast<float *>(tmem_slot + 4);  // 16 x 32 floats (codebook)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * BN;
-    const int ks0 = blockIdx.z * p.ks_per_split;
-    const int ks1 = min(p.nk, ks0 + p.ks_per_split);
-    const int nks = max(0, ks1 - ks0);
+    int tile = blockIdx.x, ks0 = 0, nks = p.nk, pslot = -1;
+    if (tile >= p.full_tiles) {
+        const int q = tile - p.full_tiles, r = q / p.tail_splits, z = q - r * p.tail_splits;
+        tile = p.full_tiles + r;
+        ks0 = z * p.tail_kps;
+        nks = max(0, min(p.nk, ks0 + p.tail_kps) - ks0);
+        pslot = p.tail_splits > 1 ? q : -1;  // an unsplit tail tile writes Y directly
+    }
+    const int m0 = (tile / p.nt) * kBM, n0 = (tile % p.nt) * BN;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -414,14 +423,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t r[32];
             tmem_ld32(lane_addr + cc, r);
             const int h = cc / BN, c0 = cc - h * BN;
-            const int m = m0 + h * kMH + sub * 32 + lane;
-            if (!ok || m >= p.M || nks == 0) continue;
+            const int row = h * kMH + sub * 32 + lane, m = m0 + row;
+            if (!ok || nks == 0 || m >= p.M) continue;  // rows past M are never read back
             const int nb0 = n0 + c0;
-            if (p.partial) {
-                float *dst = p.partial + (static_cast<size_t>(blockIdx.z) * p.M + m) * p.N + nb0;
+            if (pslot >= 0) {  // a tail piece: the whole 32-column row segment (columns past N are ignored)
+                float4 *dst = reinterpret_cast<float4 *>(p.partial + (static_cast<size_t>(pslot) * kBM + row) * BN + c0);
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (nb0 + j < p.N) dst[j] = __uint_as_float(r[j]);
+                for (int j = 0; j < 8; ++j)
+                    dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                         __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
             } else if (p.y_dtype == 0 && (p.N & 3) == 0 && nb0 + 32 <= p.N) {
                 float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.Y) + static_cast<size_t>(m) * p.N + nb0);
 #pragma unroll
@@ -444,15 +454,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-__global__ void tc_splitk_reduce_kernel(const float *__restrict__ partial, int splits, size_t MN, void *Y,
-                                        int y_dtype) {
+// Y for the tail tiles: the sum of each tile's K pieces in split order.
+__global__ void tc_tail_reduce_kernel(const float *__restrict__ partial, int tail_tiles, int splits, int bn,
+                                      int full_tiles, int nt, int M, int N, void *Y, int y_dtype) {
     pdl_wait();
     pdl_launch_dependents();
-    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < MN;
+    const size_t per_tile = static_cast<size_t>(kBM) * bn;
+    const size_t total = static_cast<size_t>(tail_tiles) * per_tile;
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const int r = static_cast<int>(i / per_tile);
+        const int e = static_cast<int>(i - r * per_tile), row = e / bn, col = e - row * bn;
+        const int tile = full_tiles + r;
+        const int m = (tile / nt) * kBM + row, n = (tile % nt) * bn + col;
+        if (m >= M || n >= N) continue;
         float s = 0.f;
-        for (int sp = 0; sp < splits; ++sp) s += partial[sp * MN + i];
-        store_y_elem(Y, y_dtype, i, s);
+        for (int z = 0; z < splits; ++z) s += partial[(static_cast<size_t>(r) * splits + z) * per_tile + e];
+        store_y_elem(Y, y_dtype, static_cast<size_t>(m) * N + n, s);
     }
 }
 
@@ -473,7 +491,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 struct TcCfg {
-    int bn, splits, ks_per_split, nk, m_tiles, n_tiles;
+    int bn, nk, mt, nt, full_tiles, tail_tiles, tail_splits, tail_kps;
+    int grid() const { return full_tiles + tail_tiles * tail_splits; }
+    size_t partial_bytes() const {
+        return tail_splits > 1 ? static_cast<size_t>(tail_tiles) * tail_splits * kBM * bn * sizeof(float) : 0;
+    }
 };
 
 int smem_bytes(int bn, int bits) {
@@ -481,37 +503,47 @@ int smem_bytes(int bn, int bits) {
     return kSmemFixed + act_slots(bn) * kBM * kBK * 2 + 2 * wdq_bytes(bn) + kCodeSlots * code_slot_bytes(bn);
 }
 
-// Static tile choice: the weight-tile width BN and the split of K that
-// minimise (waves of CTAs) x (work per CTA), preferring wide tiles.
+// Static tile choice (no timing, no tuning): the weight-tile width BN, and the
+// schedule -- whole tiles fill complete waves of CTAs, the tiles left over are
+// split along K over the SMs (their pieces summed afterwards) -- that minimise
+// a cost model in units of about 1.4 ns:
+//  * per K step, the MMAs (~halves x BN; N=256 MMAs run at full rate, narrower
+//    ones lose about a third to shared-memory bandwidth) or the dequant
+//    (~1.4 BN + a fixed cost), whichever is larger;
+//  * per CTA, the pipeline fill and the epilogue;
+//  * for split tail tiles, writing and reducing their fp32 pieces through HBM.
 TcCfg choose_tc(int M, int N, int K, int bits) {
     const DeviceInfo &di = device_info();
+    const int sms = di.sm_count;
     TcCfg best{};
     double best_t = 1e300;
     const int nk = (K + kBK - 1) / kBK;
     const int mt = (M + kBM - 1) / kBM;
+    const int halves = M > kMH ? 2 : 1;
     for (int bn : {256, 128, 64}) {
         if (smem_bytes(bn, bits) > di.max_smem_optin) continue;
         const int nt = (N + bn - 1) / bn;
-        for (int sp = 1; sp <= 16; sp *= 2) {
-            const int kps = ((nk + sp - 1) / sp + 3) / 4 * 4;  // whole code super-stages per split
-            if (kps < 4 && sp > 1) break;
-            const int splits = (nk + kps - 1) / kps;
-            const long ctas = static_cast<long>(mt) * nt * splits;
-            if (splits > 1 && static_cast<long>(mt) * nt >= 2L * di.sm_count) break;  // split K only to fill waves
-            const long waves = (ctas + di.sm_count - 1) / di.sm_count;
-            // Per K step (units of about 1.4 ns): the MMAs, ~halves x bn (N=256 MMAs run at full rate,
-            // narrower ones lose about a third to shared-memory bandwidth), or the dequant, ~1.4 bn + a
-            // fixed cost, whichever is larger.  Plus the pipeline fill / epilogue per CTA, and for a
-            // split K the reduce: (splits + 1) x M x N fp32 through HBM.
-            const int halves = M > kMH ? 2 : 1;
-            const double mma = halves * bn * (bn >= 256 ? 1.0 : 1.45);
-            const double per_cta = kps * std::max(mma, 1.4 * bn + 100.0) + 800.0;
-            const double reduce = splits > 1 ? (splits + 1.0) * M * N * 4.0 / 9520.0 : 0.0;  // ~6.8 TB/s in these units
-            const double t = waves * per_cta + reduce;
-            if (t < best_t * 0.97) {
-                best_t = t;
-                best = TcCfg{bn, splits, kps, nk, mt, nt};
+        const long tiles = static_cast<long>(mt) * nt;
+        const double step = std::max(halves * bn * (bn >= 256 ? 1.0 : 1.45), 1.4 * bn + 100.0);
+        const long full_waves = tiles / sms;
+        TcCfg c{bn, nk, mt, nt, static_cast<int>(full_waves * sms), static_cast<int>(tiles - full_waves * sms), 1, nk};
+        double t = full_waves * (nk * step + 800.0);
+        if (c.tail_tiles > 0) {
+            // split the tail over the SMs, in whole 4-step code super-stages
+            int sp = std::max(1, std::min(sms / c.tail_tiles, nk / 4));
+            int kps = ((nk + sp - 1) / sp + 3) / 4 * 4;
+            sp = (nk + kps - 1) / kps;
+            if (sp > 1) {
+                c.tail_splits = sp;
+                c.tail_kps = kps;
+                t += kps * step + 800.0 + (sp + 1.0) * c.tail_tiles * kBM * bn * 4.0 / 9520.0;
+            } else {
+                t += nk * step + 800.0;
             }
+        }
+        if (t < best_t * 0.97) {
+            best_t = t;
+            best = c;
         }
     }
     return best;
@@ -531,7 +563,7 @@ cudaError_t launch_tc(const CUtensorMap &am, const CUtensorMap &cm, const CUtens
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    dim3 grid(c.n_tiles, c.m_tiles, c.splits);
+    dim3 grid(c.grid());
     const cudaError_t e = launch_pdl(kern, grid, dim3(kThreads), smem, s, am, cm, pm, zm, a);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -551,7 +583,7 @@ bool tc_eligible(int M, int K, int bits, int a_dtype, int bs) {
 
 size_t tc_workspace_bytes(int M, int N, int K, int bits) {
     const TcCfg c = choose_tc(M, N, K, bits);
-    return c.splits > 1 ? static_cast<size_t>(c.splits) * M * N * sizeof(float) : 0;
+    return c.partial_bytes();
 }
 
 cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s) {
@@ -622,11 +654,13 @@ cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_
     a.lbs = 31 - __builtin_clz(static_cast<unsigned>(p.bs));
     a.nb = p.K / p.bs;
     a.nk = c.nk;
-    a.ks_per_split = c.ks_per_split;
+    a.nt = c.nt;
+    a.full_tiles = c.full_tiles;
+    a.tail_splits = c.tail_splits;
+    a.tail_kps = c.tail_kps;
     a.fault = fault_word();
-    if (c.splits > 1) {
-        const size_t need = static_cast<size_t>(c.splits) * p.M * p.N * sizeof(float);
-        if (!ws || ws_bytes < need) return cudaErrorInvalidValue;
+    if (c.partial_bytes()) {
+        if (!ws || ws_bytes < c.partial_bytes()) return cudaErrorInvalidValue;
         a.partial = static_cast<float *>(ws);
     }
     const bool bf16 = p.a_dtype == 2;
@@ -643,12 +677,13 @@ cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_
     QG_TC(WK_CODEBOOK, 4, true, 256) QG_TC(WK_CODEBOOK, 4, true, 128) QG_TC(WK_CODEBOOK, 4, true, 64) {}
 #undef QG_TC
     if (e != cudaSuccess) return e;
-    if (c.splits > 1) {
-        const size_t MN = static_cast<size_t>(p.M) * p.N;
+    if (c.partial_bytes()) {
+        const size_t total = static_cast<size_t>(c.tail_tiles) * kBM * c.bn;
         const int threads = 256;
-        const int blocks = static_cast<int>(std::min<size_t>((MN + threads - 1) / threads, 8192));
-        const cudaError_t e2 = launch_pdl(tc_splitk_reduce_kernel, dim3(blocks), dim3(threads), 0, s,
-                                          static_cast<const float *>(a.partial), c.splits, MN, p.Y, p.y_dtype);
+        const int blocks = static_cast<int>(std::min<size_t>((total + threads - 1) / threads, 8192));
+        const cudaError_t e2 = launch_pdl(tc_tail_reduce_kernel, dim3(blocks), dim3(threads), 0, s,
+                                          static_cast<const float *>(a.partial), c.tail_tiles, c.tail_splits, c.bn,
+                                          c.full_tiles, c.nt, p.M, p.N, p.Y, p.y_dtype);
         return e2 != cudaSuccess ? e2 : cudaGetLastError();
     }
     return cudaSuccess;

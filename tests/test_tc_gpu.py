@@ -10,7 +10,7 @@ import pytest
 
 import oracle as O
 import workloads as WL
-from gpu_util import BF16, F16, F32, act_tensor, dev, nbits_case, oracle_nbits, to64, torch, y_tensor
+from gpu_util import BF16, F16, F32, act_tensor, dev, nbits_case, oracle_nbits, sample_rows, to64, torch, y_tensor
 
 pytestmark = pytest.mark.gpu
 
@@ -73,6 +73,22 @@ def test_tc_nbits_parity(qg, case):
     d = _rand(31, M, N, K, bits, bs, ad, zpm)
     Y = _run(qg, d, yd)
     assert O.max_rel_l2(to64(Y), oracle_nbits(d)) <= 5e-3
+
+
+@pytest.mark.parametrize("case", [
+    (300, 19968, 1024, 2, 64, F16, "uniform", F32),   # 156 tiles of 256 x 256: a full wave plus a K-split tail
+    (512, 9984, 2048, 4, 128, BF16, "tensor", F32),   # 78 tiles of 256 x 256 (or 156 of 256 x 128)
+])
+def test_tc_split_tail_sampled(qg, case):
+    """Shapes whose tiles do not fill whole waves: the tiles left over run split
+    along K and are summed afterwards; checked on sampled weight rows."""
+    M, N, K, bits, bs, ad, zpm, yd = case
+    d = _rand(43, M, N, K, bits, bs, ad, zpm)
+    Y = _run(qg, d, yd)
+    rows = sample_rows(N, 48, seed=3)
+    rows = np.unique(np.concatenate([rows, np.arange(N - 300, N, 37)]))  # the last tiles are the split ones
+    got = to64(Y)[:, rows]
+    assert O.max_rel_l2(got, oracle_nbits(d, rows=rows)) <= 5e-3
 
 
 @pytest.mark.parametrize("bits", [2, 4])
