@@ -53,8 +53,11 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+
+
 def peaks():
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    p = PEAKS_FILE
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
@@ -389,6 +392,142 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+# ------------------------------------------------------------- config suite
+def run_suite():
+    """Time every configuration of the hot path through the public API (one
+    JSON line each): tiny u4 GEMV; the phi4 u2 decode shapes at M=1 and M=4;
+    the NF4 codebook shapes at M=1, 4, 16, 64 (bf16 activations); the QMoE
+    decode (128 experts, top-8, 2880/2880, u4 block 32) with and without zero
+    points; the two M=2048 prefill GEMMs.  Each figure is the mean over a CUDA
+    graph of R back-to-back calls whose weights rotate over copies (or expert
+    sets) totalling more than three times the L2, so every call reads cold
+    weights; prefill is compute-bound and reuses one weight set."""
+    import torch
+
+    import gemm_blockwise_dequant_gb300 as qg
+    import workloads as WL
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py --suite: no CUDA device (the library has no CPU path)")
+    qg.lib()
+    peak_gbs, _ = peaks()
+    tf_peak = None
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            tf_peak = json.load(f).get("bf16_tflops")
+    st = torch.cuda.Stream()
+    dev = torch.device("cuda")
+
+    def t16(a, dt):
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(dt)
+
+    def timed(call, n):
+        with torch.cuda.stream(st):
+            for i in range(min(n, 4)):
+                call(i)
+            st.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                for i in range(n):
+                    call(i)
+            g.replay()
+            st.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            for _ in range(5):
+                g.replay()
+            b.record(st)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / (5 * n)
+
+    def emit(name, us, nbytes=None, flops=None, **extra):
+        line = {"config": name, "us_per_call": round(us, 2)}
+        if nbytes:
+            gbs = nbytes / (us * 1e-6) / 1e9
+            line.update(weight_bytes=int(nbytes), gbs=round(gbs, 1), hbm_frac=round(gbs / peak_gbs, 4))
+        if flops:
+            tfs = flops / (us * 1e-6) / 1e12
+            line.update(tflops=round(tfs, 1))
+            if tf_peak:
+                line.update(tensor_frac=round(tfs / tf_peak, 4))
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+
+    def reps_for(nbytes):
+        return max(2, -(-3 * L2_BYTES // max(1, nbytes)))
+
+    # tiny u4 (M=1, 128 x 256, block 64, zero-point tensor)
+    d = WL.tiny_u4()
+    A, W, S, Z = torch.from_numpy(d["A"]).to(dev), torch.from_numpy(d["W"]).to(dev), t16(d["scales"], torch.float16), \
+        t16(d["zero_points"], torch.float16)
+    Y = torch.empty(1, 128, device=dev)
+    emit("tiny_u4_m1", timed(lambda i: qg.qgemm_nbits(A, W, S, Z, Y, bits=4, block_size=64, stream=st), 50))
+
+    # phi4 u2 decode, M = 1 and 4
+    for M in (1, 4):
+        for shape in SHAPES:
+            d = WL.phi4_u2(shape, M=M)
+            wb = d["W"].nbytes + d["scales"].nbytes
+            r = reps_for(wb)
+            Ws = [torch.from_numpy(d["W"]).to(dev) for _ in range(r)]
+            Ss = [t16(d["scales"], torch.float16) for _ in range(r)]
+            A = torch.from_numpy(d["A"]).to(dev)
+            Y = torch.empty(M, d["N"], device=dev)
+            ws = torch.empty(max(16, qg.qgemm_workspace_bytes(0, M, d["N"], d["K"], 2, 64)), dtype=torch.uint8, device=dev)
+            us = timed(lambda i: qg.qgemm_nbits_uniform_zp(A, Ws[i % r], Ss[i % r], ZP, Y, bits=2, block_size=64,
+                                                           workspace=ws, stream=st), 2 * r)
+            emit("phi4_u2_%s_m%d" % (shape, M), us, nbytes=wb)
+            del Ws, Ss
+
+    # NF4 codebook, bf16 activations
+    for shape in ("square", "gqa_kv", "up", "down"):
+        for M in (1, 4, 16, 64):
+            d = WL.nf4(shape, M=M, a_dtype=2)
+            wb = d["W"].nbytes + d["absmax"].nbytes
+            r = reps_for(wb)
+            Ws = [torch.from_numpy(d["W"]).to(dev) for _ in range(r)]
+            am = torch.from_numpy(d["absmax"]).to(dev)
+            cb = torch.from_numpy(d["codebook"]).to(dev)
+            A = t16(d["A"], torch.bfloat16)
+            Y = torch.empty(M, d["N"], device=dev, dtype=torch.bfloat16)
+            ws = torch.empty(max(16, qg.qgemm_workspace_bytes(2, M, d["N"], d["K"], 4, 64)), dtype=torch.uint8, device=dev)
+            us = timed(lambda i: qg.qgemm_codebook4(A, Ws[i % r], cb, am, Y, block_size=64, workspace=ws, stream=st), 2 * r)
+            emit("nf4_%s_%dx%d_m%d" % (shape, d["N"], d["K"], M), us, nbytes=wb,
+                 flops=2.0 * M * d["N"] * d["K"])
+            del Ws
+
+    # QMoE decode: rotate over disjoint expert sets (128 experts, top-8)
+    for with_zp in (False, True):
+        d = WL.qmoe(with_zp=with_zp)
+        h = lambda a: None if a is None else t16(a, torch.float16)
+        kw = dict(num_experts=d["num_experts"], fc1_w=torch.from_numpy(d["fc1_w"]).to(dev), fc1_scales=h(d["fc1_scales"]),
+                  fc1_zp=h(d["fc1_zp"]), fc1_bias=h(d["fc1_bias"]), fc2_w=torch.from_numpy(d["fc2_w"]).to(dev),
+                  fc2_scales=h(d["fc2_scales"]), fc2_zp=h(d["fc2_zp"]), fc2_bias=h(d["fc2_bias"]), bits=4, block_size=32)
+        k, E = d["k"], d["num_experts"]
+        sets = [torch.arange(j * k, (j + 1) * k, dtype=torch.int32, device=dev) for j in range(E // k)]
+        wts = torch.from_numpy(d["weights"]).to(dev)
+        x = h(d["x"])
+        y = torch.empty(d["hidden"], dtype=torch.float16, device=dev)
+        ws = torch.empty(qg.qmoe_decode_workspace_bytes(k, d["hidden"], d["inter"]), dtype=torch.uint8, device=dev)
+        per_expert = (d["fc1_w"][0].nbytes + d["fc1_scales"][0].nbytes + d["fc2_w"][0].nbytes + d["fc2_scales"][0].nbytes
+                      + (d["fc1_zp"][0].nbytes + d["fc2_zp"][0].nbytes if with_zp else 0))
+        us = timed(lambda i: qg.qmoe_decode_fused(x, sets[i % len(sets)], wts, y=y, workspace=ws, stream=st, **kw),
+                   len(sets))
+        emit("qmoe_top8_2880_u4_bs32_%s" % ("zp" if with_zp else "nozp"), us, nbytes=k * per_expert)
+        del kw
+
+    # prefill u2, M = 2048, fp16 activations, fp32 out
+    for shape in ("gate_up", "down"):
+        d = WL.prefill_u2(shape, M=2048)
+        A, W, S = t16(d["A"], torch.float16), torch.from_numpy(d["W"]).to(dev), t16(d["scales"], torch.float16)
+        Y = torch.empty(d["M"], d["N"], device=dev)
+        ws = torch.empty(max(16, qg.qgemm_workspace_bytes(1, d["M"], d["N"], d["K"], 2, 64)), dtype=torch.uint8, device=dev)
+        us = timed(lambda i: qg.qgemm_nbits_uniform_zp(A, W, S, ZP, Y, bits=2, block_size=64, workspace=ws, stream=st), 4)
+        emit("prefill_u2_%s_m2048" % shape, us, flops=2.0 * d["M"] * d["N"] * d["K"])
+        del A, W, S, Y
+    return 0
+
+
 # ------------------------------------------------------------- ncu probes
 def run_probe(name):
     """Small fixed workloads for profiler captures (no timing, no JSON line).
@@ -458,9 +597,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--probe", choices=["gemv_k5120", "gemv_lm_head", "tc_prefill", "qmoe"],
                     help="run a small fixed workload for a profiler capture instead of the benchmark")
+    ap.add_argument("--suite", action="store_true",
+                    help="time every configuration (one JSON line each) instead of the benchmark")
     args = ap.parse_args()
     if args.probe:
         return run_probe(args.probe)
+    if args.suite:
+        return run_suite()
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_setup(args.gpus)

@@ -79,6 +79,7 @@ struct GemvArgs {
     // t / tiles_per_slot; slot j reads the weights of expert ids[j].  Plain
     // GEMMs have one slot and ids == nullptr.
     int tiles_per_slot;
+    int cps;  // CTAs per expert slot (slot mode), or 0: tiles dealt round-robin over the grid
     const int32_t *ids;
     int num_experts;
     size_t w_slot_stride, p_slot_stride, z_slot_stride;  // bytes per expert
@@ -308,43 +309,37 @@ __device__ __forceinline__ void prepare_activations(float (&ap)[MT][KPL], float 
     }
 }
 
-// Load this lane's activations for expert slot `sl` of a fused QMoE fc2: one
-// row h = silu(gate) * up of that slot's fc1 output (gate = g[0:K], up =
-// g[K:2K], or the even / odd elements), then normalise them.
-template <int BITS, int MT, int KPL, int BPL, int WK>
-__device__ __forceinline__ void load_swiglu_activations(const GemvArgs &p, int sl, bool lane_active, int k0,
-                                                        float (&ap)[MT][KPL], float (&e2)[MT], float (&ahat)[MT][BPL]) {
-    static_assert(KPL % 8 == 0, "activation vectors are 8 elements");
-    static_assert(MT == 1, "one activation row");
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) ap[0][i] = 0.f;
-    if (lane_active) {
-        // 8 values at a time to keep registers low
-        const float *gs = p.gbuf + static_cast<size_t>(sl) * 2 * p.K;
-#pragma unroll
-        for (int c = 0; c < KPL; c += 8) {
-            float gate[8], up[8];
+// Stage the fused QMoE fc2 activation row h = silu(gate) * up of expert
+// slot `sl` (gate = g[0:K], up = g[K:2K] of that slot's fc1 output, or the
+// even / odd elements), in the same padded layout as stage_activations; all
+// consumer threads, coalesced 16-byte loads.  Values past K are zero.
+template <int KPL>
+__device__ __forceinline__ void stage_swiglu_activations(const GemvArgs &p, float *as, int sl, int kc0, int nslots,
+                                                         int tid, int nthr) {
+    constexpr int PITCH = KPL + 4;
+    const float *gs = p.gbuf + static_cast<size_t>(sl) * 2 * p.K;
+    const int nv = nslots * (KPL / 4);
+    for (int v = tid; v < nv; v += nthr) {
+        const int k = kc0 + 4 * v;
+        float h[4] = {0.f, 0.f, 0.f, 0.f};
+        if (k < p.K) {
+            float gate[4], up[4];
             if (p.swiglu_interleaved) {
-                const float4 *q = reinterpret_cast<const float4 *>(gs + 2 * (k0 + c));
-                const float4 v0 = q[0], v1 = q[1], v2 = q[2], v3 = q[3];
-                gate[0] = v0.x; up[0] = v0.y; gate[1] = v0.z; up[1] = v0.w;
-                gate[2] = v1.x; up[2] = v1.y; gate[3] = v1.z; up[3] = v1.w;
-                gate[4] = v2.x; up[4] = v2.y; gate[5] = v2.z; up[5] = v2.w;
-                gate[6] = v3.x; up[6] = v3.y; gate[7] = v3.z; up[7] = v3.w;
+                const float4 a = *reinterpret_cast<const float4 *>(gs + 2 * k);
+                const float4 b = *reinterpret_cast<const float4 *>(gs + 2 * k + 4);
+                gate[0] = a.x; up[0] = a.y; gate[1] = a.z; up[1] = a.w;
+                gate[2] = b.x; up[2] = b.y; gate[3] = b.z; up[3] = b.w;
             } else {
-                const float4 *qg = reinterpret_cast<const float4 *>(gs + k0 + c);
-                const float4 *qu = reinterpret_cast<const float4 *>(gs + p.K + k0 + c);
-                const float4 g0 = qg[0], g1 = qg[1], u0 = qu[0], u1 = qu[1];
-                gate[0] = g0.x; gate[1] = g0.y; gate[2] = g0.z; gate[3] = g0.w;
-                gate[4] = g1.x; gate[5] = g1.y; gate[6] = g1.z; gate[7] = g1.w;
-                up[0] = u0.x; up[1] = u0.y; up[2] = u0.z; up[3] = u0.w;
-                up[4] = u1.x; up[5] = u1.y; up[6] = u1.z; up[7] = u1.w;
+                const float4 a = *reinterpret_cast<const float4 *>(gs + k);
+                const float4 b = *reinterpret_cast<const float4 *>(gs + p.K + k);
+                gate[0] = a.x; gate[1] = a.y; gate[2] = a.z; gate[3] = a.w;
+                up[0] = b.x; up[1] = b.y; up[2] = b.z; up[3] = b.w;
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) ap[0][c + i] = gate[i] / (1.f + expf(-gate[i])) * up[i];
+            for (int i = 0; i < 4; ++i) h[i] = gate[i] / (1.f + expf(-gate[i])) * up[i];
         }
+        *reinterpret_cast<float4 *>(as + (v / (KPL / 4)) * PITCH + (v % (KPL / 4)) * 4) = make_float4(h[0], h[1], h[2], h[3]);
     }
-    prepare_activations<BITS, MT, KPL, BPL, WK>(ap, e2, ahat);
 }
 
 // General stage fill (ragged last tile, split K, unaligned sizes, invalid
@@ -417,13 +412,12 @@ __device__ __forceinline__ void fill_stage_general(const GemvArgs &p, unsigned c
 // slice order and write the outputs (Y, split-K partials, or the QMoE slot
 // outputs with the expert's bias).  `rs` holds [slice][kRedV * H] values.
 template <int MT, int LPR>
-__device__ __forceinline__ void finish_tile(const GemvArgs &p, const float *rs, int s_count, int tile, int lane) {
+__device__ __forceinline__ void finish_tile(const GemvArgs &p, const float *rs, int s_count, int tile, int sl, int lane) {
     constexpr int H = 32 / LPR;
     constexpr int VPW = kRedV * H;
     if (lane >= VPW) return;
     float sum = 0.f;
     for (int s = 0; s < s_count; ++s) sum += rs[s * VPW + lane];
-    const int sl = p.ids ? tile / p.tiles_per_slot : 0;
     const int rbase = (tile - sl * p.tiles_per_slot) * p.SR;
     const int hh = lane / kRedV, v = lane % kRedV;
     const int i = v / MT, m = v % MT;
@@ -484,6 +478,17 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     const int s_begin = blockIdx.y * p.S_cta;
     const int s_count = min(p.S_cta, p.S_total - s_begin);
     const int kc0 = split ? s_begin * LPR * KPL : 0;  // first k held in a stage row
+    // This CTA's tiles: t_begin, t_begin + t_stride, ... below t_end.  Plain
+    // GEMMs deal tiles round-robin over the grid; with expert slots each slot
+    // owns p.cps consecutive CTAs that take its tiles round-robin, so a CTA
+    // works for one expert (one activation row) from start to end.
+    int cta_slot = 0, t_begin = blockIdx.x, t_stride = gridDim.x, t_end = p.ntiles;
+    if (p.cps > 0) {
+        cta_slot = blockIdx.x / p.cps;
+        t_begin = cta_slot * p.tiles_per_slot + (blockIdx.x - cta_slot * p.cps);
+        t_stride = p.cps;
+        t_end = min(p.ntiles, (cta_slot + 1) * p.tiles_per_slot);
+    }
 
     // ------------------------------------------------------------ producer
     // The producer warp also finishes every tile: when a stage comes back
@@ -500,15 +505,15 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
         int it = 0, slot = 0;
         uint32_t par = 1;  // parity of the empty phase that must complete before filling (it / NST)
         bool alive = true;
-        for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++it) {
+        const int e = p.ids ? __ldg(p.ids + cta_slot) : 0;  // after pdl_wait() above
+        const bool valid = e >= 0 && e < p.num_experts;
+        const int sl = cta_slot;
+        for (int tile = t_begin; tile < t_end; tile += t_stride, ++it) {
             if (!mbar_wait(&empty[slot], par, abort_flag, p.fault, FAULT_WAIT_EMPTY)) {
                 alive = false;
                 break;
             }
-            const int sl = p.ids ? tile / p.tiles_per_slot : 0;
             const int r0 = (tile - sl * p.tiles_per_slot) * p.SR;
-            const int e = p.ids ? __ldg(p.ids + sl) : 0;
-            const bool valid = e >= 0 && e < p.num_experts;
             const int rows = valid ? min(p.SR, p.N - r0) : 0;  // an invalid expert id copies nothing
             const int es = valid ? e : 0;
             const unsigned char *Wb = p.W + es * p.w_slot_stride;
@@ -534,7 +539,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
                     waited = true;
                 }
                 finish_tile<MT, LPR>(p, red + (slot * 2 + par) * (p.S_cta * kRedV * H), s_count,
-                                     tile - p.NST * gridDim.x, lane);
+                                     tile - p.NST * t_stride, sl, lane);
             }
             if (++slot == p.NST) {
                 slot = 0;
@@ -548,7 +553,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
                 const int sj = j % p.NST;
                 if (!mbar_wait(&empty[sj], (j / p.NST) & 1, abort_flag, p.fault, FAULT_WAIT_EMPTY)) break;
                 finish_tile<MT, LPR>(p, red + (sj * 2 + ((j / p.NST) & 1)) * (p.S_cta * kRedV * H), s_count,
-                                     blockIdx.x + j * gridDim.x, lane);
+                                     t_begin + j * t_stride, sl, lane);
             }
         }
         return;
@@ -576,12 +581,15 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     float e2[MT];
     float ahat[MT][BPL];
     float zah[MT][BPL];  // zp * ahat for a zero point that is the same for every row
-    int cur_slot = -1;
-    pdl_wait();  // activations, the fc1 output and Y belong to the preceding kernel's world
-    if constexpr (AM == A_ROWS) {
-        // the same activations serve every tile (and every expert slot): load them once
+    pdl_wait();  // activations, the fc1 output, expert ids and Y belong to the preceding kernel's world
+    // This CTA's activation row (the same for every tile it computes): staged
+    // in shared memory with coalesced loads, then each lane takes its slice.
+    {
         float *as = reinterpret_cast<float *>(smem + p.a_off);
-        stage_activations<MT, KPL>(p, as, kc0, p.S_cta * LPR, threadIdx.x, NWC * 32);
+        if constexpr (AM == A_ROWS)
+            stage_activations<MT, KPL>(p, as, kc0, p.S_cta * LPR, threadIdx.x, NWC * 32);
+        else
+            stage_swiglu_activations<KPL>(p, as, cta_slot, kc0, p.S_cta * LPR, threadIdx.x, NWC * 32);
         named_bar_sync(1, NWC * 32);
         const float *mine = as + (sigma * LPR + gl) * (KPL + 4);
 #pragma unroll
@@ -600,40 +608,18 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
 #pragma unroll
             for (int b = 0; b < BPL; ++b) zah[m][b] = p.zpv * ahat[m][b];
     }
+    const int e = p.ids ? __ldg(p.ids + cta_slot) : 0;
+    const bool valid = e >= 0 && e < p.num_experts;
 
     // group g consumes the CTA's tiles g, g + G, g + 2G, ... (stage `it` holds
-    // tile it); ring slot, phase parity, expert slot and tile are advanced
-    // incrementally (no division in the loop)
-    int slot = g, sl = 0;
+    // tile it); ring slot and phase parity are advanced incrementally
+    int slot = g;
     uint32_t par = 0;
     while (slot >= p.NST) {
         slot -= p.NST;
         par ^= 1u;
     }
-    const int tstep = p.G * gridDim.x;
-    int tile = blockIdx.x + g * gridDim.x;
-    int ltile = tile;  // tile index within the expert slot
-    while (ltile >= p.tiles_per_slot) {
-        ltile -= p.tiles_per_slot;
-        ++sl;
-    }
-    int e = 0;
-    bool valid = true;
-    for (; tile < p.ntiles; tile += tstep) {
-        if (sl != cur_slot) {
-            if (p.ids) {
-                e = __ldg(p.ids + sl);
-                valid = e >= 0 && e < p.num_experts;
-            }
-            if constexpr (AM == A_SWIGLU) {
-                load_swiglu_activations<BITS, MT, KPL, BPL, WK>(p, sl, lane_active, k0, ap, e2, ahat);
-#pragma unroll
-                for (int m = 0; m < MT; ++m)
-#pragma unroll
-                    for (int b = 0; b < BPL; ++b) zah[m][b] = p.zpv * ahat[m][b];
-            }
-            cur_slot = sl;
-        }
+    for (int tile = t_begin + g * t_stride; tile < t_end; tile += p.G * t_stride) {
         const bool ok = mbar_wait(&full[slot], par, abort_flag, p.fault, FAULT_WAIT_FULL);
         const unsigned char *st = stages + static_cast<size_t>(slot) * p.stage_bytes;
         float racc[kRedV];
@@ -662,11 +648,6 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
         while (slot >= p.NST) {
             slot -= p.NST;
             par ^= 1u;
-        }
-        ltile += tstep;
-        while (ltile >= p.tiles_per_slot) {
-            ltile -= p.tiles_per_slot;
-            ++sl;
         }
     }
 }
@@ -1002,7 +983,9 @@ cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s) {
         a.swiglu_interleaved = q.swiglu_interleaved;
         a.out_f32 = fc1 ? g : o;
         a.bias = fc1 ? q.fc1_bias : q.fc2_bias;
-        c.grid_x = std::min(a.ntiles, di.sm_count);
+        // each expert slot owns an equal share of the SMs (its activation row is staged once per CTA)
+        a.cps = std::max(1, di.sm_count / q.k);
+        c.grid_x = q.k * a.cps;
         a.fast_tx = fast_stage_tx(a, c, 2);
         cudaError_t e = dispatch(a, c, q.bits, WK_NBITS, s);
         if (e != cudaSuccess) return e;
