@@ -52,8 +52,10 @@ static_assert(2 * kMaxStages * 8 + 4 <= kLutOff, "shared-memory header overlaps 
 
 // Most consumer warps a CTA may have (launch bound), by activation rows held.
 __host__ __device__ constexpr int max_consumer_warps(int mt) { return mt == 1 ? 15 : 11; }
-// Values each lane feeds into the per-tile transposed reduction.
-constexpr int kRedV = 8;
+// Rows each lane group computes per tile; a lane feeds 8 x MT values into the
+// per-tile transposed reduction (at most its group's LPR lanes).
+constexpr int kTileIter = 8;
+__host__ __device__ constexpr int red_v(int mt) { return kTileIter * mt; }
 
 enum { A_ROWS = 0, A_SWIGLU = 1 };
 
@@ -157,7 +159,7 @@ template <bool ZPT, int BITS, int VEC, int MT, int BPL, int WK, int ITER, int KP
 __device__ __forceinline__ void tile_dot(const unsigned char *wp, const unsigned char *sp, const unsigned char *zpp,
                                          int row_stride, int prow_stride, int zrow_stride, const float (&ap)[MT][KPL],
                                          const float (&e2)[MT], const float (&ahat)[MT][BPL],
-                                         const float (&zah)[MT][BPL], const float *lut_lane, float (&racc)[kRedV]) {
+                                         const float (&zah)[MT][BPL], const float *lut_lane, float (&racc)[red_v(MT)]) {
     constexpr int WPL = VEC / 4;
 #pragma unroll
     for (int i = 0; i < ITER; ++i) {
@@ -410,16 +412,17 @@ __device__ __forceinline__ void fill_stage_general(const GemvArgs &p, unsigned c
 
 // Producer side of a tile: add the S slice sums of each of the tile's rows in
 // slice order and write the outputs (Y, split-K partials, or the QMoE slot
-// outputs with the expert's bias).  `rs` holds [slice][kRedV * H] values.
+// outputs with the expert's bias).  `rs` holds [slice][red_v(MT) * H] values.
 template <int MT, int LPR>
 __device__ __forceinline__ void finish_tile(const GemvArgs &p, const float *rs, int s_count, int tile, int sl, int lane) {
     constexpr int H = 32 / LPR;
-    constexpr int VPW = kRedV * H;
+    constexpr int RV = red_v(MT);
+    constexpr int VPW = RV * H;
     if (lane >= VPW) return;
     float sum = 0.f;
     for (int s = 0; s < s_count; ++s) sum += rs[s * VPW + lane];
     const int rbase = (tile - sl * p.tiles_per_slot) * p.SR;
-    const int hh = lane / kRedV, v = lane % kRedV;
+    const int hh = lane / RV, v = lane % RV;
     const int i = v / MT, m = v % MT;
     const int row = rbase + i * H + hh;
     const int am = p.m0 + m;
@@ -444,7 +447,9 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     constexpr int WPL = VEC / 4;
     constexpr int KPL = WPL * CPW;
     constexpr int H = 32 / LPR;         // rows a warp works on at once
-    constexpr int ITER = kRedV / MT;    // row iterations per tile
+    constexpr int ITER = kTileIter;     // row iterations per tile
+    constexpr int RV = red_v(MT);       // values per lane in the tile's transposed reduction
+    static_assert(RV <= LPR, "a lane group reduces at most one value per lane");
     constexpr int PB = WK == WK_CODEBOOK ? 4 : 2;  // bytes per block parameter
     extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
@@ -538,7 +543,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
                     pdl_wait();  // outputs may be read by the preceding kernel until it completes
                     waited = true;
                 }
-                finish_tile<MT, LPR>(p, red + (slot * 2 + par) * (p.S_cta * kRedV * H), s_count,
+                finish_tile<MT, LPR>(p, red + (slot * 2 + par) * (p.S_cta * RV * H), s_count,
                                      tile - p.NST * t_stride, sl, lane);
             }
             if (++slot == p.NST) {
@@ -552,7 +557,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
             for (int j = max(0, it - p.NST); j < it; ++j) {
                 const int sj = j % p.NST;
                 if (!mbar_wait(&empty[sj], (j / p.NST) & 1, abort_flag, p.fault, FAULT_WAIT_EMPTY)) break;
-                finish_tile<MT, LPR>(p, red + (sj * 2 + ((j / p.NST) & 1)) * (p.S_cta * kRedV * H), s_count,
+                finish_tile<MT, LPR>(p, red + (sj * 2 + ((j / p.NST) & 1)) * (p.S_cta * RV * H), s_count,
                                      t_begin + j * t_stride, sl, lane);
             }
         }
@@ -572,9 +577,9 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     const int row_stride = H * p.w_pitch;           // stage bytes between a lane's successive rows
     const int prow_stride = H * p.nb * PB;          // same for the block parameters
     const int zrow_stride = H * p.nb * 2;
-    constexpr int VPW = kRedV * H;  // reduced values per warp and tile
-    const bool writer = (gl & (LPR / kRedV - 1)) == 0;
-    const int red_idx = sigma * VPW + half * kRedV + gl / (LPR / kRedV);
+    constexpr int VPW = RV * H;  // reduced values per warp and tile
+    const bool writer = (gl & (LPR / RV - 1)) == 0;
+    const int red_idx = sigma * VPW + half * RV + gl / (LPR / RV);
 
     // Activations of this lane's slice, for MT rows, kept in registers.
     float ap[MT][KPL];
@@ -622,9 +627,9 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     for (int tile = t_begin + g * t_stride; tile < t_end; tile += p.G * t_stride) {
         const bool ok = mbar_wait(&full[slot], par, abort_flag, p.fault, FAULT_WAIT_FULL);
         const unsigned char *st = stages + static_cast<size_t>(slot) * p.stage_bytes;
-        float racc[kRedV];
+        float racc[RV];
 #pragma unroll
-        for (int v = 0; v < kRedV; ++v) racc[v] = 0.f;
+        for (int v = 0; v < RV; ++v) racc[v] = 0.f;
         if (ok && valid) {  // warp-uniform
             const unsigned char *wp = st + half * p.w_pitch + lane_boff;  // this lane's first row is `half`
             const unsigned char *sp = st + p.s_off + (half * p.nb + blk0) * PB;
@@ -636,10 +641,10 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
                 tile_dot<false, BITS, VEC, MT, BPL, WK, ITER>(wp, sp, zpp, row_stride, prow_stride, zrow_stride, ap, e2,
                                                              ahat, zah, lut_lane, racc);
 #pragma unroll
-            for (int v = 0; v < kRedV; ++v) racc[v] = lane_active ? racc[v] : 0.f;
+            for (int v = 0; v < RV; ++v) racc[v] = lane_active ? racc[v] : 0.f;
         }
-        // lane l now holds, for row half `half`, the slice sum of value (l % LPR) / (LPR / kRedV)
-        const float tot = transpose_reduce<kRedV, LPR>(racc, lane);
+        // lane l now holds, for row half `half`, the slice sum of value (l % LPR) / (LPR / RV)
+        const float tot = transpose_reduce<RV, LPR>(racc, lane);
         if (writer) red[(slot * 2 + par) * (p.S_cta * VPW) + red_idx] = tot;
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);  // releases the stage and this warp's slice sums
@@ -745,7 +750,7 @@ bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, 
     c.S_cta = (c.S_total + c.splits - 1) / c.splits;
     // a stage holds one tile of SR rows; the G row groups of consumer warps take
     // stages in turn, so the stage size does not grow with the number of warps
-    c.SR = (kRedV / c.mt) * (32 / c.lpr);
+    c.SR = kTileIter * (32 / c.lpr);
     c.G = std::max(1, maxw / c.S_cta);
     c.w_pitch = c.splits > 1 ? round_up(c.S_cta * c.lpr * c.vec, 16) : row_bytes;
     // activation staging: MT rows x S_cta slices x LPR lanes x (KPL + 4) floats
@@ -756,8 +761,8 @@ bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, 
     c.s_off = round_up(c.SR * c.w_pitch, 128);
     c.z_off = c.s_off + round_up(c.SR * nb * pb, 128);
     c.stage_bytes = c.z_off + (zp_tensor ? round_up(c.SR * nb * 2, 128) : 0);
-    // each stage also has a reduction slot: S_cta slices x kRedV x H sums
-    const int red_slot = c.S_cta * kRedV * (32 / c.lpr) * 4;
+    // each stage also has a reduction slot: S_cta slices x red_v(MT) x H sums
+    const int red_slot = c.S_cta * red_v(c.mt) * (32 / c.lpr) * 4;
     const int nfit = std::min(kMaxStages, budget / (c.stage_bytes + 2 * red_slot));
     if (nfit < 2) return false;
     // Ring slots are owned by row groups: slot s serves group s % G only, so
