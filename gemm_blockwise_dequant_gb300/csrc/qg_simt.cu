@@ -75,6 +75,7 @@ struct GemvArgs {
     int S_total, S_cta, G, SR, NST;
     int fast_tx;  // bytes of a whole aligned stage (codes + parameters [+ zero points]); 0: no fast path
     int a_off, a_rstride;  // shared-memory staging of the activations: offset, floats per staged row
+    int bias_off;          // shared-memory copy of the CTA's expert bias row (QMoE), or 0: read from global
     int w_pitch, stage_bytes, s_off, z_off, red_off, stage_off, ntiles;
     unsigned *fault;
     // Slots (the experts of a QMoE decode): tile t covers rows of slot
@@ -414,7 +415,8 @@ __device__ __forceinline__ void fill_stage_general(const GemvArgs &p, unsigned c
 // slice order and write the outputs (Y, split-K partials, or the QMoE slot
 // outputs with the expert's bias).  `rs` holds [slice][red_v(MT) * H] values.
 template <int MT, int LPR>
-__device__ __forceinline__ void finish_tile(const GemvArgs &p, const float *rs, int s_count, int tile, int sl, int lane) {
+__device__ __forceinline__ void finish_tile(const GemvArgs &p, const float *rs, int s_count, int tile, int sl, int lane,
+                                            const uint16_t *bias_s) {
     constexpr int H = 32 / LPR;
     constexpr int RV = red_v(MT);
     constexpr int VPW = RV * H;
@@ -430,9 +432,14 @@ __device__ __forceinline__ void finish_tile(const GemvArgs &p, const float *rs, 
     if (p.out_f32) {
         const int e = p.ids ? __ldg(p.ids + sl) : 0;
         float o = 0.f;
-        if (e >= 0 && e < p.num_experts)
-            o = sum + (p.bias ? h2f(__ldg(reinterpret_cast<const unsigned short *>(p.bias) + static_cast<size_t>(e) * p.N + row))
-                              : 0.f);
+        if (e >= 0 && e < p.num_experts) {
+            float b = 0.f;
+            if (bias_s)  // the expert's bias row, staged in shared memory by the consumer warps
+                b = h2f(bias_s[row]);
+            else if (p.bias)
+                b = h2f(__ldg(reinterpret_cast<const unsigned short *>(p.bias) + static_cast<size_t>(e) * p.N + row));
+            o = sum + b;
+        }
         p.out_f32[static_cast<size_t>(sl) * p.N + row] = o;
     } else if (p.partial) {
         p.partial[(static_cast<size_t>(blockIdx.y) * p.M + am) * p.N + row] = sum;
@@ -458,6 +465,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     float *lut = reinterpret_cast<float *>(smem + kLutOff);
     float *red = reinterpret_cast<float *>(smem + p.red_off);
     unsigned char *stages = smem + p.stage_off;
+    const uint16_t *bias_s = p.bias_off ? reinterpret_cast<const uint16_t *>(smem + p.bias_off) : nullptr;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NWC = p.S_cta * p.G;
@@ -544,7 +552,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
                     waited = true;
                 }
                 finish_tile<MT, LPR>(p, red + (slot * 2 + par) * (p.S_cta * RV * H), s_count,
-                                     tile - p.NST * t_stride, sl, lane);
+                                     tile - p.NST * t_stride, sl, lane, bias_s);
             }
             if (++slot == p.NST) {
                 slot = 0;
@@ -558,7 +566,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
                 const int sj = j % p.NST;
                 if (!mbar_wait(&empty[sj], (j / p.NST) & 1, abort_flag, p.fault, FAULT_WAIT_EMPTY)) break;
                 finish_tile<MT, LPR>(p, red + (sj * 2 + ((j / p.NST) & 1)) * (p.S_cta * RV * H), s_count,
-                                     t_begin + j * t_stride, sl, lane);
+                                     t_begin + j * t_stride, sl, lane, bias_s);
             }
         }
         return;
@@ -595,6 +603,13 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
             stage_activations<MT, KPL>(p, as, kc0, p.S_cta * LPR, threadIdx.x, NWC * 32);
         else
             stage_swiglu_activations<KPL>(p, as, cta_slot, kc0, p.S_cta * LPR, threadIdx.x, NWC * 32);
+        if (p.bias_off) {  // this CTA's expert bias row, for the producer's finish_tile
+            uint16_t *bs = reinterpret_cast<uint16_t *>(smem + p.bias_off);
+            const int be = p.ids ? __ldg(p.ids + cta_slot) : 0;
+            const bool bvalid = be >= 0 && be < p.num_experts;
+            for (int i = threadIdx.x; i < p.N; i += NWC * 32)
+                bs[i] = bvalid ? __ldg(p.bias + static_cast<size_t>(be) * p.N + i) : static_cast<uint16_t>(0);
+        }
         named_bar_sync(1, NWC * 32);
         const float *mine = as + (sigma * LPR + gl) * (KPL + 4);
 #pragma unroll
@@ -696,7 +711,7 @@ struct Cfg {
     int vec, lpr, mt, bpl;
     int S_total, S_cta, splits, G, SR, NST;
     int w_pitch, stage_bytes, s_off, z_off, red_off, stage_off, smem, ntiles, grid_x;
-    int a_off, a_rstride;
+    int a_off, a_rstride, bias_off;
 };
 
 inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -706,7 +721,7 @@ inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
 // per useful code: idle lanes of the last K-slice, the per-row bookkeeping
 // (about 12 instructions per lane and row) and, for layouts needing more
 // slices than fit in one CTA, a split-K penalty.
-bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, Cfg &c) {
+bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, Cfg &c, int bias_bytes = 0) {
     const DeviceInfo &di = device_info();
     c.mt = M <= 1 ? 1 : (M <= 2 ? 2 : 4);
     const int maxw = max_consumer_warps(c.mt);
@@ -756,7 +771,8 @@ bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, 
     // activation staging: MT rows x S_cta slices x LPR lanes x (KPL + 4) floats
     c.a_off = round_up(kLutOff + (kind == WK_CODEBOOK ? 16 * 32 * 4 : 0), 128);
     c.a_rstride = c.S_cta * c.lpr * (kpl + 4);
-    c.stage_off = round_up(c.a_off + c.mt * c.a_rstride * 4, 1024);
+    c.bias_off = bias_bytes ? round_up(c.a_off + c.mt * c.a_rstride * 4, 128) : 0;
+    c.stage_off = round_up(c.a_off + c.mt * c.a_rstride * 4 + (bias_bytes ? 128 + bias_bytes : 0), 1024);
     const int budget = di.max_smem_optin - c.stage_off;
     c.s_off = round_up(c.SR * c.w_pitch, 128);
     c.z_off = c.s_off + round_up(c.SR * nb * pb, 128);
@@ -876,6 +892,7 @@ void fill_args(GemvArgs &a, const Cfg &c) {
     a.red_off = c.red_off;
     a.a_off = c.a_off;
     a.a_rstride = c.a_rstride;
+    a.bias_off = c.bias_off;
     a.stage_off = c.stage_off;
     a.fault = fault_word();
 }
@@ -958,7 +975,10 @@ cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s) {
         const int K = fc1 ? q.hidden : q.inter;
         const uint16_t *zp = fc1 ? q.fc1_zp : q.fc2_zp;
         Cfg c;
-        if (!choose_cfg(1, N, K, q.bits, q.bs, WK_NBITS, zp != nullptr, c) || c.splits != 1)
+        // the expert's bias row is staged in shared memory when it is small enough
+        const uint16_t *bias = fc1 ? q.fc1_bias : q.fc2_bias;
+        const int bias_bytes = bias && N <= 16384 ? (N * 2 + 15) / 16 * 16 : 0;
+        if (!choose_cfg(1, N, K, q.bits, q.bs, WK_NBITS, zp != nullptr, c, bias_bytes) || c.splits != 1)
             return cudaErrorNotSupported;
         GemvArgs a{};
         a.A = q.x;
