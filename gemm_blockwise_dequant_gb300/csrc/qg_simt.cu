@@ -607,8 +607,17 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
             uint16_t *bs = reinterpret_cast<uint16_t *>(smem + p.bias_off);
             const int be = p.ids ? __ldg(p.ids + cta_slot) : 0;
             const bool bvalid = be >= 0 && be < p.num_experts;
-            for (int i = threadIdx.x; i < p.N; i += NWC * 32)
-                bs[i] = bvalid ? __ldg(p.bias + static_cast<size_t>(be) * p.N + i) : static_cast<uint16_t>(0);
+            const uint16_t *src = p.bias + static_cast<size_t>(bvalid ? be : 0) * p.N;
+            if ((p.N & 7) == 0 && (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0) {  // 16-byte aligned rows
+                const int nv = p.N / 8;
+#pragma unroll 4
+                for (int i = threadIdx.x; i < nv; i += NWC * 32)
+                    reinterpret_cast<uint4 *>(bs)[i] =
+                        bvalid ? __ldg(reinterpret_cast<const uint4 *>(src) + i) : make_uint4(0u, 0u, 0u, 0u);
+            } else {
+#pragma unroll 4
+                for (int i = threadIdx.x; i < p.N; i += NWC * 32) bs[i] = bvalid ? __ldg(src + i) : uint16_t(0);
+            }
         }
         named_bar_sync(1, NWC * 32);
         const float *mine = as + (sigma * LPR + gl) * (KPL + 4);

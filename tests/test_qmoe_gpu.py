@@ -87,6 +87,25 @@ def test_qmoe_128_experts_top8_2880(qg, with_zp):
     assert qg.qg_read_device_fault() == 0
 
 
+def test_qmoe_bias_not_16_byte_aligned(qg):
+    """Biases that start 2 bytes past a 16-byte boundary take the scalar copy
+    into shared memory."""
+    t = torch()
+    d = WL.qmoe(num_experts=8, k=3, hidden=512, inter=768, block_size=32, with_bias=True, seed=11)
+    T = _dev_case(d)
+    for key in ("fc1_bias", "fc2_bias"):
+        b = T[key]
+        buf = t.empty(b.numel() + 8, dtype=t.float16, device="cuda")
+        view = buf[1:1 + b.numel()].view(b.shape)
+        view.copy_(b)
+        assert view.data_ptr() % 16 != 0
+        T[key] = view
+    y = _run(qg, d, T)
+    ref, bad = _oracle(d)
+    assert bad == 0
+    assert _relerr(y, ref) <= 5e-3
+
+
 def test_qmoe_interleaved_swiglu(qg):
     d = WL.qmoe(num_experts=8, k=3, hidden=256, inter=384, block_size=32, seed=4)
     y = _run(qg, d, _dev_case(d), interleaved=1)
