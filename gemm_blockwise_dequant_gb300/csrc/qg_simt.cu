@@ -416,7 +416,7 @@ __device__ __forceinline__ void fill_stage_general(const GemvArgs &p, unsigned c
 // outputs with the expert's bias).  `rs` holds [slice][red_v(MT) * H] values.
 template <int MT, int LPR>
 __device__ __forceinline__ void finish_tile(const GemvArgs &p, const float *rs, int s_count, int tile, int sl, int lane,
-                                            const uint16_t *bias_s) {
+                                            const uint16_t *bias_s, int e) {
     constexpr int H = 32 / LPR;
     constexpr int RV = red_v(MT);
     constexpr int VPW = RV * H;
@@ -429,8 +429,7 @@ __device__ __forceinline__ void finish_tile(const GemvArgs &p, const float *rs, 
     const int row = rbase + i * H + hh;
     const int am = p.m0 + m;
     if (row >= p.N || am >= p.M) return;
-    if (p.out_f32) {
-        const int e = p.ids ? __ldg(p.ids + sl) : 0;
+    if (p.out_f32) {  // e: the slot's expert id, as the producer read it
         float o = 0.f;
         if (e >= 0 && e < p.num_experts) {
             float b = 0.f;
@@ -552,7 +551,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
                     waited = true;
                 }
                 finish_tile<MT, LPR>(p, red + (slot * 2 + par) * (p.S_cta * RV * H), s_count,
-                                     tile - p.NST * t_stride, sl, lane, bias_s);
+                                     tile - p.NST * t_stride, sl, lane, bias_s, e);
             }
             if (++slot == p.NST) {
                 slot = 0;
@@ -566,7 +565,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
                 const int sj = j % p.NST;
                 if (!mbar_wait(&empty[sj], (j / p.NST) & 1, abort_flag, p.fault, FAULT_WAIT_EMPTY)) break;
                 finish_tile<MT, LPR>(p, red + (sj * 2 + ((j / p.NST) & 1)) * (p.S_cta * RV * H), s_count,
-                                     t_begin + j * t_stride, sl, lane, bias_s);
+                                     t_begin + j * t_stride, sl, lane, bias_s, e);
             }
         }
         return;
