@@ -52,10 +52,11 @@ static_assert(2 * kMaxStages * 8 + 4 <= kLutOff, "shared-memory header overlaps 
 
 // Most consumer warps a CTA may have (launch bound), by activation rows held.
 __host__ __device__ constexpr int max_consumer_warps(int mt) { return mt == 1 ? 15 : 11; }
-// Rows each lane group computes per tile; a lane feeds 8 x MT values into the
-// per-tile transposed reduction (at most its group's LPR lanes).
-constexpr int kTileIter = 8;
-__host__ __device__ constexpr int red_v(int mt) { return kTileIter * mt; }
+// IT, the rows each lane group computes per tile, is 8, or 16 for full-warp
+// lane groups whose stages stay small (fewer, larger stages for the producer
+// warp, which competes for issue slots with the consumer warps).  A lane feeds
+// IT x MT values into the per-tile transposed reduction (at most one per lane
+// of its group).
 
 enum { A_ROWS = 0, A_SWIGLU = 1 };
 
@@ -160,7 +161,7 @@ template <bool ZPT, int BITS, int VEC, int MT, int BPL, int WK, int ITER, int KP
 __device__ __forceinline__ void tile_dot(const unsigned char *wp, const unsigned char *sp, const unsigned char *zpp,
                                          int row_stride, int prow_stride, int zrow_stride, const float (&ap)[MT][KPL],
                                          const float (&e2)[MT], const float (&ahat)[MT][BPL],
-                                         const float (&zah)[MT][BPL], const float *lut_lane, float (&racc)[red_v(MT)]) {
+                                         const float (&zah)[MT][BPL], const float *lut_lane, float (&racc)[ITER * MT]) {
     constexpr int WPL = VEC / 4;
 #pragma unroll
     for (int i = 0; i < ITER; ++i) {
@@ -413,12 +414,12 @@ __device__ __forceinline__ void fill_stage_general(const GemvArgs &p, unsigned c
 
 // Producer side of a tile: add the S slice sums of each of the tile's rows in
 // slice order and write the outputs (Y, split-K partials, or the QMoE slot
-// outputs with the expert's bias).  `rs` holds [slice][red_v(MT) * H] values.
-template <int MT, int LPR>
+// outputs with the expert's bias).  `rs` holds [slice][IT * MT * H] values.
+template <int MT, int LPR, int IT>
 __device__ __forceinline__ void finish_tile(const GemvArgs &p, const float *rs, int s_count, int tile, int sl, int lane,
                                             const uint16_t *bias_s, int e) {
     constexpr int H = 32 / LPR;
-    constexpr int RV = red_v(MT);
+    constexpr int RV = IT * MT;
     constexpr int VPW = RV * H;
     if (lane >= VPW) return;
     float sum = 0.f;
@@ -447,14 +448,14 @@ __device__ __forceinline__ void finish_tile(const GemvArgs &p, const float *rs, 
     }
 }
 
-template <int BITS, int VEC, int MT, int BPL, int WK, int LPR, int AM>
+template <int BITS, int VEC, int MT, int BPL, int WK, int LPR, int AM, int IT>
 __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_kernel(const GemvArgs p) {
     constexpr int CPW = 32 / BITS;
     constexpr int WPL = VEC / 4;
     constexpr int KPL = WPL * CPW;
     constexpr int H = 32 / LPR;         // rows a warp works on at once
-    constexpr int ITER = kTileIter;     // row iterations per tile
-    constexpr int RV = red_v(MT);       // values per lane in the tile's transposed reduction
+    constexpr int ITER = IT;            // row iterations per tile
+    constexpr int RV = IT * MT;         // values per lane in the tile's transposed reduction
     static_assert(RV <= LPR, "a lane group reduces at most one value per lane");
     constexpr int PB = WK == WK_CODEBOOK ? 4 : 2;  // bytes per block parameter
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -550,7 +551,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
                     pdl_wait();  // outputs may be read by the preceding kernel until it completes
                     waited = true;
                 }
-                finish_tile<MT, LPR>(p, red + (slot * 2 + par) * (p.S_cta * RV * H), s_count,
+                finish_tile<MT, LPR, IT>(p, red + (slot * 2 + par) * (p.S_cta * RV * H), s_count,
                                      tile - p.NST * t_stride, sl, lane, bias_s, e);
             }
             if (++slot == p.NST) {
@@ -564,7 +565,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
             for (int j = max(0, it - p.NST); j < it; ++j) {
                 const int sj = j % p.NST;
                 if (!mbar_wait(&empty[sj], (j / p.NST) & 1, abort_flag, p.fault, FAULT_WAIT_EMPTY)) break;
-                finish_tile<MT, LPR>(p, red + (sj * 2 + ((j / p.NST) & 1)) * (p.S_cta * RV * H), s_count,
+                finish_tile<MT, LPR, IT>(p, red + (sj * 2 + ((j / p.NST) & 1)) * (p.S_cta * RV * H), s_count,
                                      t_begin + j * t_stride, sl, lane, bias_s, e);
             }
         }
@@ -719,7 +720,7 @@ struct Cfg {
     int vec, lpr, mt, bpl;
     int S_total, S_cta, splits, G, SR, NST;
     int w_pitch, stage_bytes, s_off, z_off, red_off, stage_off, smem, ntiles, grid_x;
-    int a_off, a_rstride, bias_off;
+    int a_off, a_rstride, bias_off, iter;
 };
 
 inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -773,7 +774,14 @@ bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, 
     c.S_cta = (c.S_total + c.splits - 1) / c.splits;
     // a stage holds one tile of SR rows; the G row groups of consumer warps take
     // stages in turn, so the stage size does not grow with the number of warps
-    c.SR = kTileIter * (32 / c.lpr);
+    // 16 rows per lane group for MatMulNBits when a lane holds 32 activations and
+    // the 16-row stage stays small (the codebook kernel is slower with them); the
+    // kernels instantiated with 16 are listed in dispatch()
+    c.iter = (kind == WK_NBITS && c.lpr == 32 && c.mt == 1 && row_bytes <= 4096 &&
+              ((bits == 4 && c.vec == 16) || (bits == 2 && c.vec == 8)))
+                 ? 16
+                 : 8;
+    c.SR = c.iter * (32 / c.lpr);
     c.G = std::max(1, maxw / c.S_cta);
     c.w_pitch = c.splits > 1 ? round_up(c.S_cta * c.lpr * c.vec, 16) : row_bytes;
     // activation staging: MT rows x S_cta slices x LPR lanes x (KPL + 4) floats
@@ -785,8 +793,8 @@ bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, 
     c.s_off = round_up(c.SR * c.w_pitch, 128);
     c.z_off = c.s_off + round_up(c.SR * nb * pb, 128);
     c.stage_bytes = c.z_off + (zp_tensor ? round_up(c.SR * nb * 2, 128) : 0);
-    // each stage also has a reduction slot: S_cta slices x red_v(MT) x H sums
-    const int red_slot = c.S_cta * red_v(c.mt) * (32 / c.lpr) * 4;
+    // each stage also has a reduction slot: S_cta slices x iter x MT x H sums
+    const int red_slot = c.S_cta * c.iter * c.mt * (32 / c.lpr) * 4;
     const int nfit = std::min(kMaxStages, budget / (c.stage_bytes + 2 * red_slot));
     if (nfit < 2) return false;
     // Ring slots are owned by row groups: slot s serves group s % G only, so
@@ -805,9 +813,9 @@ bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, 
     return true;
 }
 
-template <int BITS, int VEC, int MT, int BPL, int WK, int LPR, int AM>
+template <int BITS, int VEC, int MT, int BPL, int WK, int LPR, int AM, int IT = 8>
 cudaError_t launch_one(const GemvArgs &a, const Cfg &c, cudaStream_t s) {
-    auto kern = gemv_kernel<BITS, VEC, MT, BPL, WK, LPR, AM>;
+    auto kern = gemv_kernel<BITS, VEC, MT, BPL, WK, LPR, AM, IT>;
     static std::atomic<unsigned> configured{0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -832,6 +840,18 @@ cudaError_t dispatch(const GemvArgs &a, const Cfg &c, int bits, int kind, cudaSt
     if (bits == B && c.vec == V && c.mt == 1 && c.bpl == BPL_ && kind == WK_NBITS && c.lpr == L_ && \
         a.a_mode == A_SWIGLU)                                                                      \
         return launch_one<B, V, 1, BPL_, WK_NBITS, L_, A_SWIGLU>(a, c, s);
+    // 16 rows per tile (see choose_cfg): full-warp lane groups holding 32 activations
+    if (c.iter == 16) {
+        if (c.mt == 1 && c.lpr == 32 && c.bpl == 1) {
+            if (bits == 4 && c.vec == 16 && kind == WK_NBITS)
+                return a.a_mode == A_ROWS ? launch_one<4, 16, 1, 1, WK_NBITS, 32, A_ROWS, 16>(a, c, s)
+                                          : launch_one<4, 16, 1, 1, WK_NBITS, 32, A_SWIGLU, 16>(a, c, s);
+            if (bits == 2 && c.vec == 8 && kind == WK_NBITS)
+                return a.a_mode == A_ROWS ? launch_one<2, 8, 1, 1, WK_NBITS, 32, A_ROWS, 16>(a, c, s)
+                                          : launch_one<2, 8, 1, 1, WK_NBITS, 32, A_SWIGLU, 16>(a, c, s);
+        }
+        return cudaErrorNotSupported;
+    }
     // fused QMoE fc2 (activations = SwiGLU of fc1's output)
     QG_CASE_SW(4, 16, 1, 32)
     QG_CASE_SW(4, 16, 1, 16)
