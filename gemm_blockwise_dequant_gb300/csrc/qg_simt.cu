@@ -156,12 +156,18 @@ __device__ __forceinline__ void dot_word_codebook(uint32_t x, const float (&ap)[
 // One tile's dot products for one lane: ITER rows (stride `row_stride` in the
 // stage) times this lane's KPL codes, scaled per block; racc[i * MT + m] gets
 // row i, activation row m.  ZPT: a zero point per block and row (else the
-// scalar zero point folded into zah).
+// scalar zero point folded into zah).  The lane's power-of-two activation
+// scale e2 is folded into the constants: c23 = 2^23 e2c, ahat and zah are
+// pre-multiplied by e2c = min(e2, 2^104) (exact scalings, and 2^23 e2c stays
+// finite), so no multiply per row remains; in the rare case that a lane of
+// the warp has e2 > 2^104 (activations of 2^105 or more) the remaining power
+// of two `post` is applied to the row sums once per tile.
 template <bool ZPT, int BITS, int VEC, int MT, int BPL, int WK, int ITER, int KPL = VEC / 4 * (32 / BITS)>
 __device__ __forceinline__ void tile_dot(const unsigned char *wp, const unsigned char *sp, const unsigned char *zpp,
                                          int row_stride, int prow_stride, int zrow_stride, const float (&ap)[MT][KPL],
-                                         const float (&e2)[MT], const float (&ahat)[MT][BPL],
-                                         const float (&zah)[MT][BPL], const float *lut_lane, float (&racc)[ITER * MT]) {
+                                         const float (&c23)[MT], const float (&ahat)[MT][BPL],
+                                         const float (&zah)[MT][BPL], const float *lut_lane, float (&racc)[ITER * MT],
+                                         const float (&post)[MT], bool need_post) {
     constexpr int WPL = VEC / 4;
 #pragma unroll
     for (int i = 0; i < ITER; ++i) {
@@ -192,13 +198,13 @@ __device__ __forceinline__ void tile_dot(const unsigned char *wp, const unsigned
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
                         const float P = (acc0[m].x + acc0[m].y) + (acc1[m].x + acc1[m].y);
-                        rv[m] = fmaf(s, fmaf(P, 8388608.f, -(z * ahat[m][b])), rv[m]);
+                        rv[m] = fmaf(s, fmaf(P, c23[m], -(z * ahat[m][b])), rv[m]);
                     }
                 } else {
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
                         const float P = (acc0[m].x + acc0[m].y) + (acc1[m].x + acc1[m].y);
-                        rv[m] = fmaf(s, fmaf(P, 8388608.f, -zah[m][b]), rv[m]);
+                        rv[m] = fmaf(s, fmaf(P, c23[m], -zah[m][b]), rv[m]);
                     }
                 }
             } else {
@@ -211,10 +217,16 @@ __device__ __forceinline__ void tile_dot(const unsigned char *wp, const unsigned
             }
         }
 #pragma unroll
-        for (int m = 0; m < MT; ++m) racc[i * MT + m] = rv[m] * e2[m];
+        for (int m = 0; m < MT; ++m) racc[i * MT + m] = rv[m];  // e2 already folded in (codebook: e2 = 1)
         wp += row_stride;
         sp += prow_stride;
         zpp += zrow_stride;
+    }
+    if (need_post) {  // warp-uniform
+#pragma unroll
+        for (int i = 0; i < ITER; ++i)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) racc[i * MT + m] *= post[m];
     }
 }
 
@@ -594,6 +606,9 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     float e2[MT];
     float ahat[MT][BPL];
     float zah[MT][BPL];  // zp * ahat for a zero point that is the same for every row
+    float c23[MT];       // 2^23 e2c (see tile_dot)
+    float post[MT];
+    bool need_post = false;
     pdl_wait();  // activations, the fc1 output, expert ids and Y belong to the preceding kernel's world
     // This CTA's activation row (the same for every tile it computes): staged
     // in shared memory with coalesced loads, then each lane takes its slice.
@@ -632,10 +647,20 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
                 ap[m][4 * j + 3] = v.w;
             }
         prepare_activations<BITS, MT, KPL, BPL, WK>(ap, e2, ahat);
+        bool big = false;
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
+        for (int m = 0; m < MT; ++m) {
+            const float e2c = fminf(e2[m], __uint_as_float((104u + 127u) << 23));  // min(e2, 2^104)
+            post[m] = e2[m] / e2c;                                    // 1, or the power of two left over
+            big |= post[m] != 1.f;
+            c23[m] = 8388608.f * e2c;  // 2^23 e2c: exact, finite
 #pragma unroll
-            for (int b = 0; b < BPL; ++b) zah[m][b] = p.zpv * ahat[m][b];
+            for (int b = 0; b < BPL; ++b) {
+                zah[m][b] = (p.zpv * ahat[m][b]) * e2c;
+                ahat[m][b] *= e2c;
+            }
+        }
+        need_post = __any_sync(0xffffffffu, big);
     }
     const int e = p.ids ? __ldg(p.ids + cta_slot) : 0;
     const bool valid = e >= 0 && e < p.num_experts;
@@ -659,11 +684,11 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
             const unsigned char *sp = st + p.s_off + (half * p.nb + blk0) * PB;
             const unsigned char *zpp = st + p.z_off + (half * p.nb + blk0) * 2;
             if (WK == WK_NBITS && p.zp_mode == ZP_TENSOR)
-                tile_dot<true, BITS, VEC, MT, BPL, WK, ITER>(wp, sp, zpp, row_stride, prow_stride, zrow_stride, ap, e2,
-                                                            ahat, zah, lut_lane, racc);
+                tile_dot<true, BITS, VEC, MT, BPL, WK, ITER>(wp, sp, zpp, row_stride, prow_stride, zrow_stride, ap, c23,
+                                                            ahat, zah, lut_lane, racc, post, need_post);
             else
-                tile_dot<false, BITS, VEC, MT, BPL, WK, ITER>(wp, sp, zpp, row_stride, prow_stride, zrow_stride, ap, e2,
-                                                             ahat, zah, lut_lane, racc);
+                tile_dot<false, BITS, VEC, MT, BPL, WK, ITER>(wp, sp, zpp, row_stride, prow_stride, zrow_stride, ap, c23,
+                                                             ahat, zah, lut_lane, racc, post, need_post);
 #pragma unroll
             for (int v = 0; v < RV; ++v) racc[v] = lane_active ? racc[v] : 0.f;
         }

@@ -123,6 +123,21 @@ def test_qgemm_nbits_parity(qg, case):
     assert err <= tol_for(ad, yd), err
 
 
+@pytest.mark.parametrize("scale_exp", [110, -110])
+def test_extreme_activation_magnitudes(qg, scale_exp):
+    """Activations near the ends of the fp32 range in part of K (the kernel
+    normalises each lane's slice by a power of two; slices past 2^104 take the
+    rare post-scaling path) against the oracle."""
+    M, N, K, bits, bs = 1, 301, 5120, 2, 64
+    d = _rand_nbits(13, M, N, K, bits, bs, F32, "uniform")
+    A = d["A"].astype(np.float64)
+    A[:, 1024:2048] *= 2.0 ** scale_exp
+    d["A"] = A.astype(np.float32)
+    Y = _run_nbits(qg, d, F32)
+    assert np.all(np.isfinite(Y.cpu().numpy()))
+    assert O.max_rel_l2(to64(Y), oracle_nbits(d)) <= 1e-4
+
+
 @pytest.mark.parametrize("bits", [2, 4])
 def test_onehot_recovers_dequantized_column_exactly(qg, bits):
     N, K, bs = 96, 1024, 64
