@@ -396,6 +396,7 @@ def run_ours(args, world, rank, local):
 def run_suite():
     """Time every configuration of the hot path through the public API (one
     JSON line each): tiny u4 GEMV; the phi4 u2 decode shapes at M=1 and M=4;
+    8-bit codes on two of those shapes;
     the NF4 codebook shapes at M=1, 4, 16, 64 (bf16 activations); the QMoE
     decode (128 experts, top-8, 2880/2880, u4 block 32) with and without zero
     points; the two M=2048 prefill GEMMs.  Each figure is the mean over a CUDA
@@ -478,6 +479,21 @@ def run_suite():
                                                            workspace=ws, stream=st), 2 * r)
             emit("phi4_u2_%s_m%d" % (shape, M), us, nbytes=wb)
             del Ws, Ss
+
+    # 8-bit MatMulNBits codes on two of the phi4 shapes, M = 1
+    for shape in ("qkv", "lm_head"):
+        d = WL.phi4_u8(shape, M=1)
+        wb = d["W"].nbytes + d["scales"].nbytes
+        r = reps_for(wb)
+        Ws = [torch.from_numpy(d["W"]).to(dev) for _ in range(r)]
+        S = t16(d["scales"], torch.float16)
+        A = torch.from_numpy(d["A"]).to(dev)
+        Y = torch.empty(1, d["N"], device=dev)
+        ws = torch.empty(max(16, qg.qgemm_workspace_bytes(0, 1, d["N"], d["K"], 8, 64)), dtype=torch.uint8, device=dev)
+        us = timed(lambda i: qg.qgemm_nbits_uniform_zp(A, Ws[i % r], S, 128.0, Y, bits=8, block_size=64,
+                                                       workspace=ws, stream=st), 2 * r)
+        emit("phi4_u8_%s_m1" % shape, us, nbytes=wb)
+        del Ws
 
     # NF4 codebook, bf16 activations
     for shape in ("square", "gqa_kv", "up", "down"):

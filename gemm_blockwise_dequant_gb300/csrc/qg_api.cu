@@ -70,8 +70,11 @@ constexpr long long kMaxK = 1 << 24;
 constexpr long long kMaxN = 1 << 28;
 constexpr long long kMaxM = 1 << 20;
 
+// Code widths of the GEMM entry points: MatMulNBits u2 / u4 / u8 (the codebook is 4-bit).
+bool valid_bits(int bits) { return bits == 2 || bits == 4 || bits == 8; }
+
 size_t gemm_workspace(int a_dtype, int M, int N, int K, int bits, int bs) {
-    if (M <= 0 || N <= 0 || K <= 0 || (bits != 2 && bits != 4) || !valid_bs(bs) || K % bs) return 0;
+    if (M <= 0 || N <= 0 || K <= 0 || !valid_bits(bits) || !valid_bs(bs) || K % bs) return 0;
     if (qg::tc_eligible(M, K, bits, a_dtype, bs)) return qg::tc_workspace_bytes(M, N, K, bits);
     return qg::simt_workspace_bytes(M, N, K, bits, bs);
 }
@@ -82,7 +85,7 @@ int check_gemm(const void *A, int a_dtype, const uint8_t *W, const void *params,
                int y_dtype, int M, int N, int K, int bits, int bs, const void *ws, size_t ws_bytes) {
     if (!valid_dtype(a_dtype) || !valid_dtype(y_dtype)) return QG_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0) return QG_ERR_INVALID_ARG;
-    if (bits != 2 && bits != 4) return QG_ERR_UNSUPPORTED;
+    if (!valid_bits(bits)) return QG_ERR_UNSUPPORTED;
     if (!valid_bs(bs)) return QG_ERR_UNSUPPORTED;
     if (K % bs) return QG_ERR_INVALID_ARG;
     if (M > kMaxM || N > kMaxN || K > kMaxK) return QG_ERR_UNSUPPORTED;
@@ -301,7 +304,7 @@ int qg_fp16_uniform_value(const uint16_t *t, size_t n, int *is_uniform, float *v
 static int dequant_common(GemmProblem &p, float *out, qg_stream_t stream) {
     (void)cudaGetLastError();
     if (p.N < 0 || p.K < 0) return QG_ERR_INVALID_ARG;
-    if (p.bits != 2 && p.bits != 4) return QG_ERR_UNSUPPORTED;
+    if (!valid_bits(p.bits)) return QG_ERR_UNSUPPORTED;
     if (!valid_bs(p.bs)) return QG_ERR_UNSUPPORTED;
     if (p.K % p.bs) return QG_ERR_INVALID_ARG;
     if (p.N > kMaxN || p.K > kMaxK) return QG_ERR_UNSUPPORTED;
@@ -322,7 +325,7 @@ int qg_dequant_nbits(const uint8_t *W, const uint16_t *scales_f16, const uint16_
     p.scales = scales_f16;
     p.zp = zero_points_f16;
     p.zp_mode = zero_points_f16 ? qg::ZP_TENSOR : qg::ZP_NONE;
-    p.uniform_zp = (bits == 2 || bits == 4) ? static_cast<float>(1 << (bits - 1)) : 0.f;
+    p.uniform_zp = valid_bits(bits) ? static_cast<float>(1 << (bits - 1)) : 0.f;
     p.N = N;
     p.K = K;
     p.bits = bits;

@@ -96,11 +96,18 @@ struct GemvArgs {
 
 template <int BITS>
 __host__ __device__ constexpr int pos_exp(int i) {
-    // bit position of code i of a 32-bit word after the single split shift:
+    // bit position of code i of a 32-bit word after the single split shift
+    // (a masked code must sit below bit 23, the exponent's lowest bit):
     // u2: codes 0..10 in place (bits 2i), codes 11..15 from word >> 22;
-    // u4: codes 0..4 in place (bits 4i), codes 5..7 from word >> 20.
-    return BITS == 2 ? (i < 11 ? 2 * i : 2 * (i - 11)) : (i < 5 ? 4 * i : 4 * (i - 5));
+    // u4: codes 0..4 in place (bits 4i), codes 5..7 from word >> 20;
+    // u8: codes 0, 1 in place (bits 8i), codes 2, 3 from word >> 16.
+    return BITS == 2 ? (i < 11 ? 2 * i : 2 * (i - 11))
+                     : (BITS == 4 ? (i < 5 ? 4 * i : 4 * (i - 5)) : (i < 2 ? 8 * i : 8 * (i - 2)));
 }
+template <int BITS>
+__host__ __device__ constexpr int split_lo() { return BITS == 2 ? 11 : (BITS == 4 ? 5 : 2); }
+template <int BITS>
+__host__ __device__ constexpr int split_shift() { return BITS == 2 ? 22 : (BITS == 4 ? 20 : 16); }
 
 template <int VEC>
 __device__ __forceinline__ void load_words(const unsigned char *p, uint32_t (&x)[VEC / 4]) {
@@ -123,8 +130,8 @@ __device__ __forceinline__ void load_words(const unsigned char *p, uint32_t (&x)
 template <int BITS, int MT, int KPL>
 __device__ __forceinline__ void dot_word_nbits(uint32_t x, const float (&ap)[MT][KPL], int j, float2 (&acc)[MT]) {
     constexpr int CPW = 32 / BITS;
-    constexpr int LO = BITS == 2 ? 11 : 5;
-    constexpr int SH = BITS == 2 ? 22 : 20;
+    constexpr int LO = split_lo<BITS>();
+    constexpr int SH = split_shift<BITS>();
     constexpr uint32_t MASK = (1u << BITS) - 1u;
     const uint32_t xh = x >> SH;
 #pragma unroll
@@ -769,6 +776,9 @@ bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, 
         if (c.mt == 1) { cands[ncand++] = {16, 32}; cands[ncand++] = {16, 16}; cands[ncand++] = {8, 32}; }
         else if (c.mt == 2) { cands[ncand++] = {8, 32}; cands[ncand++] = {8, 16}; cands[ncand++] = {4, 32}; }
         else { cands[ncand++] = {4, 32}; }
+    } else if (bits == 8) {  // 16 codes per 16-byte load
+        if (c.mt <= 2) { cands[ncand++] = {16, 32}; cands[ncand++] = {16, 16}; }
+        else { cands[ncand++] = {16, 32}; }
     } else {
         if (c.mt <= 2) { cands[ncand++] = {16, 32}; cands[ncand++] = {16, 16}; cands[ncand++] = {8, 32}; }
         else { cands[ncand++] = {8, 32}; cands[ncand++] = {4, 32}; }
@@ -896,6 +906,12 @@ cudaError_t dispatch(const GemvArgs &a, const Cfg &c, int bits, int kind, cudaSt
     QG_CASE(2, 8, 2, 1, WK_NBITS, 16)
     QG_CASE(2, 4, 2, 1, WK_NBITS, 32)
     QG_CASE(2, 4, 4, 1, WK_NBITS, 32)
+    // MatMulNBits u8
+    QG_CASE(8, 16, 1, 1, WK_NBITS, 32)
+    QG_CASE(8, 16, 1, 1, WK_NBITS, 16)
+    QG_CASE(8, 16, 2, 1, WK_NBITS, 32)
+    QG_CASE(8, 16, 2, 1, WK_NBITS, 16)
+    QG_CASE(8, 16, 4, 1, WK_NBITS, 32)
     // MatMulNBits u4
     QG_CASE(4, 16, 1, 1, WK_NBITS, 32)
     QG_CASE(4, 16, 1, 1, WK_NBITS, 16)

@@ -179,10 +179,20 @@ __device__ __forceinline__ uint32_t to_operand(__half2 h) {
 // 8 weights (k = 8c .. 8c+7 of one row) from their packed codes, as four
 // operand pairs.  nbits: w = (q - zp) * s in fp16 (zp2, s2: fp16 pairs).
 template <int BITS, bool BF16>
-__device__ __forceinline__ uint4 dequant8_nbits(uint32_t codes, uint32_t zp2u, uint32_t s2u) {
+__device__ __forceinline__ uint4 dequant8_nbits(uint32_t codes, uint32_t codes_hi, uint32_t zp2u, uint32_t s2u) {
     const __half2 zp2 = u32_as_h2(zp2u), s2 = u32_as_h2(s2u);
     uint32_t out[4];
-    if constexpr (BITS == 2) {
+    if constexpr (BITS == 8) {
+        // codes: 8 bytes, one code each; a byte permute puts two codes under the
+        // fp16 exponent of 1024 (0x64): (1024 + q0, 1024 + q1), exact for q < 1024
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t wsrc = j < 2 ? codes : codes_hi;
+            const uint32_t h = __byte_perm(wsrc, 0x64646464u, (j & 1) ? 0x4342u : 0x4140u);
+            const __half2 q = __hsub2(u32_as_h2(h), __floats2half2_rn(1024.f, 1024.f));
+            out[j] = to_operand<BF16>(__hmul2(__hsub2(q, zp2), s2));
+        }
+    } else if constexpr (BITS == 2) {
         // codes: 16 bits, 8 codes; byte j holds codes 4j .. 4j+3
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -379,12 +389,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const unsigned char *__restrict__ ps = par_s + cslot * PAR_BYTES + pc0;
             const unsigned char *__restrict__ zs = zp_s + cslot * PAR_BYTES + pc0;
             unsigned char *__restrict__ ws = wdq_s + b * WDQ_BYTES;
-            uint32_t codes[UPT], pv[UPT], zv[UPT];
+            uint32_t codes[UPT], codes_hi[UPT], pv[UPT], zv[UPT];
 #pragma unroll
             for (int j = 0; j < UPT; ++j) {
+                codes_hi[j] = 0u;
                 if constexpr (WK == WK_NBITS) {
-                    codes[j] = BITS == 2 ? static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(cs + code_off[j]))
-                                         : *reinterpret_cast<const uint32_t *>(cs + code_off[j]);
+                    if constexpr (BITS == 8) {  // 8 weights = 8 bytes
+                        const uint2 v = *reinterpret_cast<const uint2 *>(cs + code_off[j]);
+                        codes[j] = v.x;
+                        codes_hi[j] = v.y;
+                    } else {
+                        codes[j] = BITS == 2 ? static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(cs + code_off[j]))
+                                             : *reinterpret_cast<const uint32_t *>(cs + code_off[j]);
+                    }
                     pv[j] = *reinterpret_cast<const uint16_t *>(ps + par_off[j]);
                     zv[j] = zt ? *reinterpret_cast<const uint16_t *>(zs + par_off[j]) : 0u;
                 } else {
@@ -396,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < UPT; ++j) {
                 uint4 w;
                 if constexpr (WK == WK_NBITS) {
-                    w = dequant8_nbits<BITS, BF16>(codes[j], zt ? zv[j] * 0x10001u : zpu, pv[j] * 0x10001u);
+                    w = dequant8_nbits<BITS, BF16>(codes[j], codes_hi[j], zt ? zv[j] * 0x10001u : zpu, pv[j] * 0x10001u);
                 } else {
                     w = dequant8_codebook<BF16>(codes[j], __uint_as_float(pv[j]), lut_lane);
                 }
@@ -673,6 +690,8 @@ cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_
     QG_TC(WK_NBITS, 2, true, 256) QG_TC(WK_NBITS, 2, true, 128) QG_TC(WK_NBITS, 2, true, 64)
     QG_TC(WK_NBITS, 4, false, 256) QG_TC(WK_NBITS, 4, false, 128) QG_TC(WK_NBITS, 4, false, 64)
     QG_TC(WK_NBITS, 4, true, 256) QG_TC(WK_NBITS, 4, true, 128) QG_TC(WK_NBITS, 4, true, 64)
+    QG_TC(WK_NBITS, 8, false, 256) QG_TC(WK_NBITS, 8, false, 128) QG_TC(WK_NBITS, 8, false, 64)
+    QG_TC(WK_NBITS, 8, true, 256) QG_TC(WK_NBITS, 8, true, 128) QG_TC(WK_NBITS, 8, true, 64)
     QG_TC(WK_CODEBOOK, 4, false, 256) QG_TC(WK_CODEBOOK, 4, false, 128) QG_TC(WK_CODEBOOK, 4, false, 64)
     QG_TC(WK_CODEBOOK, 4, true, 256) QG_TC(WK_CODEBOOK, 4, true, 128) QG_TC(WK_CODEBOOK, 4, true, 64) {}
 #undef QG_TC

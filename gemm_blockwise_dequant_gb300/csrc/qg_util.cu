@@ -12,7 +12,7 @@
 namespace qg {
 namespace {
 
-// One thread per 32-bit word of codes (16 u2 or 8 u4 codes).
+// One thread per 32-bit word of codes (16 u2, 8 u4 or 4 u8 codes).
 template <int BITS, int WK>
 __global__ void dequant_kernel(const uint8_t *__restrict__ W, const unsigned char *__restrict__ params,
                                const uint16_t *__restrict__ zp, int zp_mode, float zpv,
@@ -78,6 +78,10 @@ cudaError_t launch_dequant(const GemmProblem &p, float *out, cudaStream_t s) {
             p.W, reinterpret_cast<const unsigned char *>(p.absmax), nullptr, 0, 0.f, p.codebook, out, p.N, p.K, p.bs);
     else if (p.bits == 2)
         dequant_kernel<2, WK_NBITS><<<blocks, threads, 0, s>>>(p.W, reinterpret_cast<const unsigned char *>(p.scales),
+                                                                p.zp, p.zp_mode, p.uniform_zp, nullptr, out, p.N,
+                                                                p.K, p.bs);
+    else if (p.bits == 8)
+        dequant_kernel<8, WK_NBITS><<<blocks, threads, 0, s>>>(p.W, reinterpret_cast<const unsigned char *>(p.scales),
                                                                 p.zp, p.zp_mode, p.uniform_zp, nullptr, out, p.N,
                                                                 p.K, p.bs);
     else

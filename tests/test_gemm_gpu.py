@@ -53,7 +53,7 @@ def _run_nbits(qg, d, y_dtype=F32, use_uniform=True):
 
 
 # --------------------------------------------------------------- dequant export
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 @pytest.mark.parametrize("bs", [32, 64, 128, 256])
 @pytest.mark.parametrize("zp_mode", ["tensor", "none", "uniform"])
 def test_dequant_nbits_bit_exact(qg, bits, bs, zp_mode):
@@ -109,6 +109,13 @@ NBITS_CASES = [
     (4, 33, 17920, 2, 64, F32, "tensor", F32),     # long K, split-K with a ragged last split
     (12, 50, 1536, 2, 64, F32, "uniform", F32),    # fp32 activations beyond 8 rows
     (1, 40000, 512, 2, 64, F32, "uniform", F32),   # short K, many rows: more row groups than ring stages
+    (1, 301, 1536, 8, 64, F32, "tensor", F32),     # 8-bit codes (hip-ep #1318 kernel test table, Wi8 leaves)
+    (1, 257, 2048, 8, 32, F32, "uniform", F32),
+    (1, 200, 4096, 8, 128, F32, "none", F32),
+    (2, 150, 1024, 8, 256, F32, "uniform", F32),
+    (4, 301, 1536, 8, 64, F32, "tensor", F32),
+    (1, 301, 1536, 8, 64, F16, "uniform", F32),
+    (3, 97, 5120, 8, 64, BF16, "tensor", BF16),
     (1, 30000, 256, 4, 64, F32, "tensor", F32),
 ]
 
@@ -138,7 +145,7 @@ def test_extreme_activation_magnitudes(qg, scale_exp):
     assert O.max_rel_l2(to64(Y), oracle_nbits(d)) <= 1e-4
 
 
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 def test_onehot_recovers_dequantized_column_exactly(qg, bits):
     N, K, bs = 96, 1024, 64
     d = _rand_nbits(9, 1, N, K, bits, bs, F32, "tensor")
@@ -150,7 +157,7 @@ def test_onehot_recovers_dequantized_column_exactly(qg, bits):
         assert np.array_equal(Y.cpu().numpy()[0], deq[:, k]), k
 
 
-@pytest.mark.parametrize("bits,zpv", [(2, 1.5), (4, 7.0)])
+@pytest.mark.parametrize("bits,zpv", [(2, 1.5), (4, 7.0), (8, 127.5)])
 def test_uniform_zp_matches_full_tensor_bitwise(qg, bits, zpv):
     d = _rand_nbits(11, 4, 333, 2048, bits, 64, F32, "uniform")
     d["uniform_zp"] = zpv

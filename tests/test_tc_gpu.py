@@ -64,6 +64,9 @@ TC_CASES = [
     (260, 1024, 1536, 2, 64, BF16, "tensor", F32),
     (16, 256, 512, 2, 64, F16, "tensor", F32),      # 8 parameter columns: narrower than one parameter box
     (40, 300, 2560, 4, 32, F16, "tensor", F32),     # 40 K steps: code super-stages of 2 steps for 4-bit codes
+    (64, 300, 2048, 8, 64, F16, "tensor", F32),     # 8-bit codes: one K step per code super-stage
+    (130, 256, 1024, 8, 128, BF16, "uniform", F32),
+    (300, 520, 4096, 8, 256, F16, "none", F16),
 ]
 
 
@@ -91,7 +94,7 @@ def test_tc_split_tail_sampled(qg, case):
     assert O.max_rel_l2(got, oracle_nbits(d, rows=rows)) <= 5e-3
 
 
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 def test_tc_onehot_layout_exact(qg, bits):
     """A = e_k for 16 rows: Y[i, n] = fp16(w[n, k_i]) exactly (zero point 1.5 and
     power-of-two-free fp16 scales make (q - zp) exact, so the only rounding is

@@ -140,6 +140,20 @@ def tiny_u4(seed: int = 0) -> dict:
                 a_dtype=F32)
 
 
+def phi4_u8(shape: str, M: int = 1, seed: int = 0) -> dict:
+    """The phi4-14B decode shapes with 8-bit codes: block 64, fp16 scales
+    U(0.0005, 0.002) (|w| of the same order as the u2 workload), zero points
+    all 128 (the midpoint, passed as a scalar), fp32 A ~ N(0,1), fp32 out."""
+    N, K = PHI4_SHAPES[shape]
+    g = rng(seed)
+    bits, bs = 8, 64
+    W = packed_codes(g, N, K, bits)
+    scales = fp16_uniform(g, (N, K // bs), 0.0005, 0.002)
+    A = activations(g, M, K, F32)
+    return dict(M=M, N=N, K=K, bits=bits, block_size=bs, W=W, scales=scales, zero_points=None,
+                uniform_zp=128.0, A=A, a_dtype=F32)
+
+
 def phi4_u2(shape: str, M: int = 1, seed: int = 0, full_zp_tensor: bool = False) -> dict:
     """phi4-14B-shaped 2-bit decode: u2 block 64, fp16 scales U(0.01, 0.05),
     zero points all exactly 1.5 (scalar path; optionally also as a full fp16
