@@ -96,15 +96,21 @@ static double load_elem(const void *base, int dtype, size_t i)
 
 /* ------------------------------------------------------------------------ */
 /* Unpack.  [P1] Summary / What (Commit 1): MatMulNBits with bits=2 (and the  */
-/* bits=4 instantiations it leaves unchanged); [P3] Summary: 4-bit codes     */
-/* decoded inside the GEMM.  Packing order: LSB-first along K (reading).    */
+/* bits=4 instantiations it leaves unchanged); [P1] Kernel Unit Test Results: */
+/* u2 / u3 / u4 / 8-bit leaves; [P3] Summary: 4-bit codes decoded inside the */
+/* GEMM.  Packing order: LSB-first along K (reading): code k of a row is the */
+/* `bits` bits starting at bit k*bits of the row's bit string, so a 3-bit    */
+/* code may continue into the next byte.                                     */
 /* ------------------------------------------------------------------------ */
 int oracle_code(const uint8_t *W, int64_t K, int64_t n, int64_t k, int bits)
 {
     int64_t row_bytes = K * bits / 8;
     int64_t bit = k * bits;
-    uint8_t byte = W[n * row_bytes + bit / 8];
-    return (byte >> (bit % 8)) & ((1 << bits) - 1);
+    const uint8_t *row = W + n * row_bytes;
+    unsigned v = row[bit / 8];
+    if (bit % 8 + bits > 8) /* the code continues into the next byte */
+        v |= (unsigned)row[bit / 8 + 1] << 8;
+    return (int)((v >> (bit % 8)) & ((1u << bits) - 1u));
 }
 
 /* ------------------------------------------------------------------------ */

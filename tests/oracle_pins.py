@@ -79,7 +79,7 @@ def check_bf16_decode(lib):
 
 def check_unpack_vs_unpackbits(lib):
     g = np.random.default_rng(11)
-    for bits in (2, 4, 8):
+    for bits in (2, 3, 4, 8):
         N, K = 5, 96
         W = g.integers(0, 256, size=(N, K * bits // 8), dtype=np.uint8)
         # scale 1, zero point 0 makes the dequantized value the code itself
@@ -128,6 +128,22 @@ def check_golden_u8(lib):
     for n in range(d["N"]):
         for k in range(d["K"]):
             assert O.code(W, d["K"], n, k, 8, lib=lib) == d["codes"][n][k]
+    assert np.array_equal(O.dequant_nbits(W, S, Z, **kw), np.array(d["dequant"], dtype=np.float32))
+    assert np.array_equal(O.dequant_nbits(W, S, None, **kw), np.array(d["dequant_no_zp"], dtype=np.float32))
+    assert np.array_equal(O.qgemm_nbits(A, W, S, Z, M=2, **kw), np.array(d["Y"]))
+    assert np.array_equal(O.qgemm_nbits(A, W, S, None, M=2, **kw), np.array(d["Y_no_zp"]))
+
+
+def check_golden_u3(lib):
+    d = _golden("u3_handworked.json")
+    W = np.array(d["W"], dtype=np.uint8)
+    S = np.array(d["scales_f16"], dtype=np.uint16)
+    Z = np.array(d["zero_points_f16"], dtype=np.uint16)
+    A = np.array(d["A"], dtype=np.float32)
+    kw = dict(N=d["N"], K=d["K"], bits=d["bits"], block_size=d["block_size"], lib=lib)
+    for n in range(d["N"]):
+        for k in range(d["K"]):
+            assert O.code(W, d["K"], n, k, 3, lib=lib) == d["codes"][n][k]
     assert np.array_equal(O.dequant_nbits(W, S, Z, **kw), np.array(d["dequant"], dtype=np.float32))
     assert np.array_equal(O.dequant_nbits(W, S, None, **kw), np.array(d["dequant_no_zp"], dtype=np.float32))
     assert np.array_equal(O.qgemm_nbits(A, W, S, Z, M=2, **kw), np.array(d["Y"]))
@@ -348,7 +364,7 @@ def check_uniform_detection(lib):
 
 
 ALL_CHECKS = [
-    check_half_decode, check_bf16_decode, check_unpack_vs_unpackbits, check_golden_u2, check_golden_u4, check_golden_u8,
+    check_half_decode, check_bf16_decode, check_unpack_vs_unpackbits, check_golden_u2, check_golden_u3, check_golden_u4, check_golden_u8,
     check_golden_codebook, check_golden_qmoe, check_onehot, check_uniform_vs_tensor, check_closed_form,
     check_integer_codebook, check_library_matmul, check_rows_subset, check_qmoe_chain, check_uniform_detection,
 ]

@@ -15,8 +15,10 @@ import oracle_pins as P
 SRC = os.path.join(os.path.dirname(oracle.__file__), "qgemm_oracle.c")
 
 MUTANTS = {
-    "msb_first_bit_order": ("return (byte >> (bit % 8)) & ((1 << bits) - 1);",
-                            "return (byte >> (8 - bits - bit % 8)) & ((1 << bits) - 1);"),
+    "msb_first_bit_order": ("return (int)((v >> (bit % 8)) & ((1u << bits) - 1u));",
+                            "return (int)((v >> (8 - bits - bit % 8)) & ((1u << bits) - 1u));"),
+    "straddling_code_truncated": ("if (bit % 8 + bits > 8) /* the code continues into the next byte */\n"
+                                  "        v |= (unsigned)row[bit / 8 + 1] << 8;", ""),
     "scales_transposed": ("float s = (float)oracle_half_to_double(scales[n * nb + b]);",
                           "float s = (float)oracle_half_to_double(scales[b * N + n]);"),
     "zero_point_sign": ("float d = (float)q - zpv;", "float d = zpv - (float)q;"),
