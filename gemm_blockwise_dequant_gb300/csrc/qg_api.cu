@@ -70,8 +70,8 @@ constexpr long long kMaxK = 1 << 24;
 constexpr long long kMaxN = 1 << 28;
 constexpr long long kMaxM = 1 << 20;
 
-// Code widths of the GEMM entry points: MatMulNBits u2 / u4 / u8 (the codebook is 4-bit).
-bool valid_bits(int bits) { return bits == 2 || bits == 4 || bits == 8; }
+// Code widths of the GEMM entry points: MatMulNBits u2 / u3 / u4 / u8 (the codebook is 4-bit).
+bool valid_bits(int bits) { return bits == 2 || bits == 3 || bits == 4 || bits == 8; }
 
 size_t gemm_workspace(int a_dtype, int M, int N, int K, int bits, int bs) {
     if (M <= 0 || N <= 0 || K <= 0 || !valid_bits(bits) || !valid_bs(bs) || K % bs) return 0;

@@ -94,16 +94,32 @@ struct GemvArgs {
     const uint16_t *bias;     // fp16 [experts][N], or nullptr
 };
 
+// u3: 32 codes in 3 words; bit position of code i of the group after its
+// shift (see dot_group_u3), always below 21 so that the 3-bit field stays
+// below the exponent.
+__host__ __device__ constexpr int pos_u3(int i) {
+    return i < 7 ? 3 * i
+                 : (i < 10 ? 3 * i - 21
+                           : (i == 10 ? 0
+                                      : (i < 18 ? 3 * i - 32
+                                                : (i < 21 ? 3 * i - 54
+                                                          : (i == 21 ? 0 : (i < 29 ? 3 * i - 64 : 3 * i - 87))))));
+}
 template <int BITS>
 __host__ __device__ constexpr int pos_exp(int i) {
     // bit position of code i of a 32-bit word after the single split shift
     // (a masked code must sit below bit 23, the exponent's lowest bit):
     // u2: codes 0..10 in place (bits 2i), codes 11..15 from word >> 22;
     // u4: codes 0..4 in place (bits 4i), codes 5..7 from word >> 20;
-    // u8: codes 0, 1 in place (bits 8i), codes 2, 3 from word >> 16.
-    return BITS == 2 ? (i < 11 ? 2 * i : 2 * (i - 11))
-                     : (BITS == 4 ? (i < 5 ? 4 * i : 4 * (i - 5)) : (i < 2 ? 8 * i : 8 * (i - 2)));
+    // u8: codes 0, 1 in place (bits 8i), codes 2, 3 from word >> 16;
+    // u3: position inside a 32-code group of 3 words (pos_u3).
+    return BITS == 3 ? pos_u3(i)
+                     : (BITS == 2 ? (i < 11 ? 2 * i : 2 * (i - 11))
+                                  : (BITS == 4 ? (i < 5 ? 4 * i : 4 * (i - 5)) : (i < 2 ? 8 * i : 8 * (i - 2))));
 }
+// Codes per unpack unit: one 32-bit word, or a 3-word group for u3.
+__host__ __device__ constexpr int unit_codes(int bits) { return bits == 3 ? 32 : 32 / bits; }
+__host__ __device__ constexpr int kpl_of(int vec, int bits) { return vec * 8 / bits; }
 template <int BITS>
 __host__ __device__ constexpr int split_lo() { return BITS == 2 ? 11 : (BITS == 4 ? 5 : 2); }
 template <int BITS>
@@ -111,7 +127,14 @@ __host__ __device__ constexpr int split_shift() { return BITS == 2 ? 22 : (BITS 
 
 template <int VEC>
 __device__ __forceinline__ void load_words(const unsigned char *p, uint32_t (&x)[VEC / 4]) {
-    if constexpr (VEC == 16) {
+    if constexpr (VEC == 24) {  // u3: two 3-word groups, 8-byte aligned
+        const uint2 a = *reinterpret_cast<const uint2 *>(p), b = *reinterpret_cast<const uint2 *>(p + 8),
+                    c = *reinterpret_cast<const uint2 *>(p + 16);
+        x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y; x[4] = c.x; x[5] = c.y;
+    } else if constexpr (VEC == 12) {  // u3: one 3-word group, 4-byte aligned
+        const uint32_t *q = reinterpret_cast<const uint32_t *>(p);
+        x[0] = q[0]; x[1] = q[1]; x[2] = q[2];
+    } else if constexpr (VEC == 16) {
         const uint4 v = *reinterpret_cast<const uint4 *>(p);
         x[0] = v.x;
         x[1] = v.y;
@@ -144,6 +167,29 @@ __device__ __forceinline__ void dot_word_nbits(uint32_t x, const float (&ap)[MT]
     }
 }
 
+// u3: acc[m] += sum over the 32 codes of the 3-word group (w0, w1, w2) of
+// ap[m][g * 32 + .] * (code as subnormal).  Code i sits at bit 3i of the
+// group's 96-bit string: codes 0-6, 11-17 and 22-28 are masked in place,
+// codes 7-9, 18-20 and 29-31 after one shift of their word, and codes 10 and
+// 21, which cross a word boundary, after a funnel shift of two words.
+template <int MT, int KPL>
+__device__ __forceinline__ void dot_group_u3(uint32_t w0, uint32_t w1, uint32_t w2, const float (&ap)[MT][KPL], int g,
+                                             float2 (&acc)[MT]) {
+    const uint32_t a = w0 >> 21, b = w1 >> 22, c = w2 >> 23;
+    const uint32_t f10 = __funnelshift_r(w0, w1, 30), f21 = __funnelshift_r(w1, w2, 31);
+    float f[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t src = i < 7 ? w0 : (i < 10 ? a : (i == 10 ? f10 : (i < 18 ? w1 : (i < 21 ? b : (i == 21 ? f21 : (i < 29 ? w2 : c))))));
+        f[i] = __uint_as_float(src & (7u << pos_u3(i)));
+    }
+#pragma unroll
+    for (int i = 0; i < 32; i += 2)
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+            acc[m] = ffma2(make_float2(ap[m][g * 32 + i], ap[m][g * 32 + i + 1]), make_float2(f[i], f[i + 1]), acc[m]);
+}
+
 // acc[m] += sum over the 8 codes of word x of ap[m][.] * C[code]; the
 // codebook sits in shared memory replicated per lane (entry q of lane l at
 // word q*32 + l), so the 32 lanes' lookups never share a bank.
@@ -169,7 +215,7 @@ __device__ __forceinline__ void dot_word_codebook(uint32_t x, const float (&ap)[
 // finite), so no multiply per row remains; in the rare case that a lane of
 // the warp has e2 > 2^104 (activations of 2^105 or more) the remaining power
 // of two `post` is applied to the row sums once per tile.
-template <bool ZPT, int BITS, int VEC, int MT, int BPL, int WK, int ITER, int KPL = VEC / 4 * (32 / BITS)>
+template <bool ZPT, int BITS, int VEC, int MT, int BPL, int WK, int ITER, int KPL = kpl_of(VEC, BITS)>
 __device__ __forceinline__ void tile_dot(const unsigned char *wp, const unsigned char *sp, const unsigned char *zpp,
                                          int row_stride, int prow_stride, int zrow_stride, const float (&ap)[MT][KPL],
                                          const float (&c23)[MT], const float (&ahat)[MT][BPL],
@@ -188,6 +234,14 @@ __device__ __forceinline__ void tile_dot(const unsigned char *wp, const unsigned
             float2 acc0[MT], acc1[MT];
 #pragma unroll
             for (int m = 0; m < MT; ++m) acc0[m] = acc1[m] = make_float2(0.f, 0.f);
+            if constexpr (BITS == 3) {  // 3-word groups of 32 codes; a block holds whole groups
+                constexpr int NG = WPL / 3;
+#pragma unroll
+                for (int gi = b * (NG / BPL); gi < (b + 1) * (NG / BPL); ++gi) {
+                    if (gi & 1) dot_group_u3<MT, KPL>(x[3 * gi], x[3 * gi + 1], x[3 * gi + 2], ap, gi, acc1);
+                    else dot_group_u3<MT, KPL>(x[3 * gi], x[3 * gi + 1], x[3 * gi + 2], ap, gi, acc0);
+                }
+            } else
 #pragma unroll
             for (int j = b * (WPL / BPL); j < (b + 1) * (WPL / BPL); ++j) {
                 if constexpr (WK == WK_NBITS) {
@@ -307,7 +361,7 @@ __device__ __forceinline__ void stage_activations(const GemvArgs &p, float *as, 
 // the subnormal code at pos equals a_hat * q * 2^-23 exactly.
 template <int BITS, int MT, int KPL, int BPL, int WK>
 __device__ __forceinline__ void prepare_activations(float (&ap)[MT][KPL], float (&e2)[MT], float (&ahat)[MT][BPL]) {
-    constexpr int CPW = 32 / BITS;
+    constexpr int CPW = unit_codes(BITS);
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
         float amax = 0.f;
@@ -469,9 +523,8 @@ __device__ __forceinline__ void finish_tile(const GemvArgs &p, const float *rs, 
 
 template <int BITS, int VEC, int MT, int BPL, int WK, int LPR, int AM, int IT>
 __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_kernel(const GemvArgs p) {
-    constexpr int CPW = 32 / BITS;
     constexpr int WPL = VEC / 4;
-    constexpr int KPL = WPL * CPW;
+    constexpr int KPL = kpl_of(VEC, BITS);
     constexpr int H = 32 / LPR;         // rows a warp works on at once
     constexpr int ITER = IT;            // row iterations per tile
     constexpr int RV = IT * MT;         // values per lane in the tile's transposed reduction
@@ -765,6 +818,7 @@ inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
 bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, Cfg &c, int bias_bytes = 0) {
     const DeviceInfo &di = device_info();
     c.mt = M <= 1 ? 1 : (M <= 2 ? 2 : 4);
+    if (bits == 3) c.mt = std::min(c.mt, 2);  // u3 groups of 32 codes: at most 2 activation rows in registers
     const int maxw = max_consumer_warps(c.mt);
     const int row_bytes = K * bits / 8;
     const int pb = kind == WK_CODEBOOK ? 4 : 2;
@@ -776,6 +830,9 @@ bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, 
         if (c.mt == 1) { cands[ncand++] = {16, 32}; cands[ncand++] = {16, 16}; cands[ncand++] = {8, 32}; }
         else if (c.mt == 2) { cands[ncand++] = {8, 32}; cands[ncand++] = {8, 16}; cands[ncand++] = {4, 32}; }
         else { cands[ncand++] = {4, 32}; }
+    } else if (bits == 3) {  // 3-word groups of 32 codes: 24 bytes (64 codes) or 12 bytes per lane
+        if (c.mt == 1) { cands[ncand++] = {24, 32}; cands[ncand++] = {24, 16}; cands[ncand++] = {12, 32}; }
+        else { cands[ncand++] = {12, 32}; cands[ncand++] = {12, 16}; }
     } else if (bits == 8) {  // 16 codes per 16-byte load
         if (c.mt <= 2) { cands[ncand++] = {16, 32}; cands[ncand++] = {16, 16}; }
         else { cands[ncand++] = {16, 32}; }
@@ -906,6 +963,14 @@ cudaError_t dispatch(const GemvArgs &a, const Cfg &c, int bits, int kind, cudaSt
     QG_CASE(2, 8, 2, 1, WK_NBITS, 16)
     QG_CASE(2, 4, 2, 1, WK_NBITS, 32)
     QG_CASE(2, 4, 4, 1, WK_NBITS, 32)
+    // MatMulNBits u3
+    QG_CASE(3, 24, 1, 1, WK_NBITS, 32)
+    QG_CASE(3, 24, 1, 1, WK_NBITS, 16)
+    QG_CASE(3, 24, 1, 2, WK_NBITS, 32)
+    QG_CASE(3, 24, 1, 2, WK_NBITS, 16)
+    QG_CASE(3, 12, 1, 1, WK_NBITS, 32)
+    QG_CASE(3, 12, 2, 1, WK_NBITS, 32)
+    QG_CASE(3, 12, 2, 1, WK_NBITS, 16)
     // MatMulNBits u8
     QG_CASE(8, 16, 1, 1, WK_NBITS, 32)
     QG_CASE(8, 16, 1, 1, WK_NBITS, 16)

@@ -593,6 +593,7 @@ cudaError_t launch_tc(const CUtensorMap &am, const CUtensorMap &cm, const CUtens
 // multiple of 16 bytes (the TMA row stride).
 bool tc_eligible(int M, int K, int bits, int a_dtype, int bs) {
     if (M < 9 || a_dtype == 0) return false;
+    if (bits == 3) return false;  // 3-bit codes (8 per 3 bytes) run on the SIMT path
     if ((K * bits / 8) % 16 != 0) return false;
     if ((K / bs) % 8 != 0) return false;  // parameter rows (fp16 scales / zero points, fp32 absmax) in 16-byte units
     return encode_fn() != nullptr;

@@ -46,6 +46,28 @@ __global__ void dequant_kernel(const uint8_t *__restrict__ W, const unsigned cha
     }
 }
 
+// u3: one thread per weight; code k is the 3 bits at bit 3k of the row,
+// which may continue into the next byte.
+__global__ void dequant_u3_kernel(const uint8_t *__restrict__ W, const uint16_t *__restrict__ scales,
+                                  const uint16_t *__restrict__ zp, int zp_mode, float zpv, float *__restrict__ out, int N,
+                                  int K, int bs) {
+    const int nb = K / bs, row_bytes = K * 3 / 8;
+    const size_t total = static_cast<size_t>(N) * K;
+    for (size_t t = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; t < total;
+         t += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const int n = static_cast<int>(t / K), k = static_cast<int>(t % K);
+        const uint8_t *row = W + static_cast<size_t>(n) * row_bytes;
+        const int bit = 3 * k;
+        uint32_t v = __ldg(row + bit / 8);
+        if (bit % 8 > 5) v |= static_cast<uint32_t>(__ldg(row + bit / 8 + 1)) << 8;
+        const float q = static_cast<float>((v >> (bit % 8)) & 7u);
+        const int b = k / bs;
+        const float s = h2f(__ldg(scales + static_cast<size_t>(n) * nb + b));
+        const float z = zp_mode == ZP_TENSOR ? h2f(__ldg(zp + static_cast<size_t>(n) * nb + b)) : zpv;
+        out[t] = __fmul_rn(__fsub_rn(q, z), s);
+    }
+}
+
 // ws[0] <- 1 if some element's bit pattern differs from t[0].  Every writer
 // stores the same value, so the result does not depend on the order.
 __global__ void uniform_kernel(const uint16_t *__restrict__ t, size_t n, unsigned *ws) {
@@ -68,6 +90,14 @@ __global__ void uniform_kernel(const uint16_t *__restrict__ t, size_t n, unsigne
 }  // namespace
 
 cudaError_t launch_dequant(const GemmProblem &p, float *out, cudaStream_t s) {
+    if (p.kind == WK_NBITS && p.bits == 3) {
+        const size_t total = static_cast<size_t>(p.N) * p.K;
+        if (total == 0) return cudaSuccess;
+        const int threads = 256;
+        const int blocks = static_cast<int>(std::min<size_t>((total + threads - 1) / threads, 65536));
+        dequant_u3_kernel<<<blocks, threads, 0, s>>>(p.W, p.scales, p.zp, p.zp_mode, p.uniform_zp, out, p.N, p.K, p.bs);
+        return cudaGetLastError();
+    }
     const int cpw = 32 / p.bits;
     const size_t total = static_cast<size_t>(p.N) * (p.K / cpw);
     const int threads = 256;

@@ -93,10 +93,11 @@ enum { QG_F32 = 0, QG_F16 = 1, QG_BF16 = 2 };
  *   once to y_dtype.
  *
  *   A            [M][K], a_dtype (QG_F32, QG_F16 or QG_BF16)
- *   W            [N][K*bits/8] packed codes, bits = 2, 4 or 8 (8-bit: one code per
- *                byte, the "Wi8" MatMulNBits leaves of the hip-ep #1318 kernel test
- *                table, read as w = (q - zp) * s with the midpoint 128 by default);
- *                other widths are refused with QG_ERR_UNSUPPORTED
+ *   W            [N][K*bits/8] packed codes, bits = 2, 3, 4 or 8 (the u2 / u3 / u4 /
+ *                "Wi8" MatMulNBits leaves of the hip-ep #1318 kernel test table;
+ *                3-bit codes run on the SIMT path for every M, a code may continue
+ *                into the next byte; 8-bit: one code per byte, midpoint 128 by
+ *                default); other widths are refused with QG_ERR_UNSUPPORTED
  *   scales_f16   [N][K/block_size] fp16 patterns
  *   zero_points_f16  [N][K/block_size] fp16 patterns, or NULL for the
  *                midpoint 2^(bits-1)

@@ -57,7 +57,7 @@ def test_refused_arguments_launch_nothing(qg):
     cases = {
         "block 16": (dict(bs=16), qg.QG_ERR_UNSUPPORTED),
         "block 48": (dict(bs=48), qg.QG_ERR_UNSUPPORTED),
-        "bits 3": (dict(bits=3), qg.QG_ERR_UNSUPPORTED),
+        "bits 5": (dict(bits=5), qg.QG_ERR_UNSUPPORTED),
         "bits 16": (dict(bits=16), qg.QG_ERR_UNSUPPORTED),
         "K not a multiple of the block": (dict(K=500, bs=32), qg.QG_ERR_INVALID_ARG),
         "negative M": (dict(M=-1), qg.QG_ERR_INVALID_ARG),

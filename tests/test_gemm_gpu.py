@@ -53,7 +53,7 @@ def _run_nbits(qg, d, y_dtype=F32, use_uniform=True):
 
 
 # --------------------------------------------------------------- dequant export
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 @pytest.mark.parametrize("bs", [32, 64, 128, 256])
 @pytest.mark.parametrize("zp_mode", ["tensor", "none", "uniform"])
 def test_dequant_nbits_bit_exact(qg, bits, bs, zp_mode):
@@ -109,6 +109,15 @@ NBITS_CASES = [
     (4, 33, 17920, 2, 64, F32, "tensor", F32),     # long K, split-K with a ragged last split
     (12, 50, 1536, 2, 64, F32, "uniform", F32),    # fp32 activations beyond 8 rows
     (1, 40000, 512, 2, 64, F32, "uniform", F32),   # short K, many rows: more row groups than ring stages
+    (1, 301, 1536, 3, 64, F32, "tensor", F32),     # 3-bit codes (hip-ep #1318 kernel test table, Wu3 leaves)
+    (1, 257, 2048, 3, 32, F32, "uniform", F32),    # 64 codes per lane span two 32-blocks
+    (1, 200, 4096, 3, 128, F32, "none", F32),
+    (1, 130, 1056, 3, 32, F32, "tensor", F32),     # K % 64 != 0: 12-byte lane groups
+    (2, 150, 1024, 3, 256, F32, "uniform", F32),
+    (4, 301, 1536, 3, 64, F32, "tensor", F32),     # two 2-row launches
+    (5, 33, 17920, 3, 64, F32, "tensor", F32),     # long K: split across CTAs
+    (1, 301, 1536, 3, 64, F16, "uniform", F32),
+    (16, 300, 2048, 3, 64, F16, "tensor", F32),    # M >= 9 with 16-bit activations stays on SIMT for u3
     (1, 301, 1536, 8, 64, F32, "tensor", F32),     # 8-bit codes (hip-ep #1318 kernel test table, Wi8 leaves)
     (1, 257, 2048, 8, 32, F32, "uniform", F32),
     (1, 200, 4096, 8, 128, F32, "none", F32),
@@ -145,7 +154,7 @@ def test_extreme_activation_magnitudes(qg, scale_exp):
     assert O.max_rel_l2(to64(Y), oracle_nbits(d)) <= 1e-4
 
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 def test_onehot_recovers_dequantized_column_exactly(qg, bits):
     N, K, bs = 96, 1024, 64
     d = _rand_nbits(9, 1, N, K, bits, bs, F32, "tensor")
@@ -157,7 +166,7 @@ def test_onehot_recovers_dequantized_column_exactly(qg, bits):
         assert np.array_equal(Y.cpu().numpy()[0], deq[:, k]), k
 
 
-@pytest.mark.parametrize("bits,zpv", [(2, 1.5), (4, 7.0), (8, 127.5)])
+@pytest.mark.parametrize("bits,zpv", [(2, 1.5), (3, 3.5), (4, 7.0), (8, 127.5)])
 def test_uniform_zp_matches_full_tensor_bitwise(qg, bits, zpv):
     d = _rand_nbits(11, 4, 333, 2048, bits, 64, F32, "uniform")
     d["uniform_zp"] = zpv
