@@ -9,7 +9,7 @@ fp64 accumulation); this module compiles it with gcc and wraps it with ctypes.
 Every function is pinned by ``tests/test_oracle_pins.py``.
 
 Sources: hip-ep pull requests #1318 (2-bit MatMulNBits, section "What",
-Commit 1) and #1328 (fused QMoE decode, sections "Summary" and "What"), and
+Commit 1; the kernel test table's gather_block_quantized leaves) and #1328 (fused QMoE decode, sections "Summary" and "What"), and
 bitsandbytes pull request #1979 ("[ROCm] Fused 4-bit SIMT GEMM", section
 "Summary").
 """
@@ -30,6 +30,9 @@ _lib = None
 
 F32, F16, BF16, F64 = 0, 1, 2, 3
 ZP_NONE, ZP_TENSOR, ZP_UNIFORM = 0, 1, 2
+# table formats of the embedding gather
+W_U2, W_U4, W_U8, W_E4M3 = 0, 1, 2, 3
+W_BITS = {W_U2: 2, W_U4: 4, W_U8: 8, W_E4M3: 8}
 
 
 def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
@@ -71,6 +74,10 @@ def load(path: str | None = None):
         lib.oracle_fp16_uniform_value.restype = I
         lib.oracle_qmoe_decode.argtypes = [P, P, P, I, I, P, P, P, P, P, P, P, P, I64, I64, I, I, I, P, P, P]
         lib.oracle_qmoe_decode.restype = I
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_double.restype = D
+        lib.oracle_gather_block_quantized.argtypes = [P, I64, P, I, P, P, I64, I64, I, P]
+        lib.oracle_gather_block_quantized.restype = I64
         if path is None:
             _lib = lib
         return lib
@@ -193,6 +200,30 @@ def qmoe_decode(x_f16, ids, weights, *, num_experts, fc1_w, fc1_scales, fc1_zp, 
         _ptr(fc1_zp), _ptr(fc1_bias), _ptr(fc2_w), _ptr(fc2_scales), _ptr(fc2_zp), _ptr(fc2_bias),
         hidden, inter, bits, block_size, int(swiglu_interleaved), _ptr(g), _ptr(h), _ptr(y))
     return y, bad
+
+
+def e4m3_to_double(bits: int, lib=None) -> float:
+    return (lib or load()).oracle_e4m3_to_double(bits)
+
+
+def gather_block_quantized(indices, W, scales, zero_points=None, *, V, D, fmt, block_size, lib=None):
+    """Gather rows of a block-quantized [V][D] table (kernel test table, gather_block_quantized).
+
+    Returns (out fp32 [n][D] exact dequantized values, number of indices outside [-V, V)).
+    Rounding to an output type is the caller's step (numpy float16 / torch bfloat16, RN-even).
+    """
+    lib = lib or load()
+    idx = _c(np.asarray(indices, dtype=np.int64).reshape(-1), np.int64)
+    W = _c(W, np.uint8)
+    scales = _c(scales, np.uint16)
+    zero_points = _c(zero_points, np.uint16)
+    if fmt == W_E4M3 and zero_points is not None:
+        raise ValueError("E4M3 tables have no zero points")
+    n = idx.shape[0]
+    out = np.empty((n, D), dtype=np.float32)
+    bad = lib.oracle_gather_block_quantized(_ptr(idx), n, _ptr(W), fmt, _ptr(scales), _ptr(zero_points), V, D,
+                                            block_size, _ptr(out))
+    return out, int(bad)
 
 
 def max_rel_l2(Y, Yref) -> float:

@@ -309,3 +309,71 @@ int oracle_qmoe_decode(const uint16_t *x_f16, const int32_t *ids, const float *w
     }
     return bad;
 }
+
+/* ------------------------------------------------------------------------ */
+/* 8-bit floating point, E4M3 ([P1] Notes for reviewers, kernel test table: */
+/* gather_block_quantized leaf Xi64_Wfp8_Yfp16; the format is read as the   */
+/* OCP E4M3 encoding without infinities): 1 sign bit, 4 exponent bits (bias */
+/* 7), 3 fraction bits.  Exponent 0 encodes subnormals f * 2^-9; the two    */
+/* patterns with every exponent and fraction bit set are NaN.               */
+/* ------------------------------------------------------------------------ */
+double oracle_e4m3_to_double(uint8_t b)
+{
+    int s = b >> 7, e = (b >> 3) & 15, f = b & 7;
+    double v;
+    if (e == 15 && f == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)f, -9);
+    else
+        v = ldexp((double)(f + 8), e - 10);
+    return s ? -v : v;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Block-quantized embedding gather ([P1] Notes for reviewers, kernel test  */
+/* table: gather_block_quantized leaves Xi64_Wu4_Yfp16, Xi64_Wu8_Yfp16,     */
+/* Xi64_Wfp8_Yfp16; [P1] Summary, Commit 3: embedding lookups through       */
+/* hip.gather).  Reading: the table is [V][D], quantized along D in blocks  */
+/* of bs with the MatMulNBits layout (codes LSB-first, scales and zero      */
+/* points [V][D/bs]); integer codes dequantize as in oracle_weight_nbits,   */
+/* E4M3 bytes as w = fl32(e4m3(q) * s).  out[i][d] = w(row, d) for          */
+/* row = idx[i], a negative index counting from the end (row = idx[i] + V). */
+/* An index outside [-V, V) yields a zero row and is counted in the return  */
+/* value.  out is fp32 [n][D]: the exact dequantized values, before any     */
+/* rounding to an output type.                                              */
+/* ------------------------------------------------------------------------ */
+enum { OR_W_U2 = 0, OR_W_U4 = 1, OR_W_U8 = 2, OR_W_E4M3 = 3 };
+
+int64_t oracle_gather_block_quantized(const int64_t *idx, int64_t n, const uint8_t *W, int wfmt,
+                                      const uint16_t *scales, const uint16_t *zp, int64_t V, int64_t D,
+                                      int bs, float *out)
+{
+    int64_t bad = 0;
+    int64_t nb = D / bs;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t row = idx[i];
+        if (row < 0)
+            row += V;
+        if (row < 0 || row >= V) {
+            ++bad;
+            for (int64_t d = 0; d < D; ++d)
+                out[i * D + d] = 0.0f;
+            continue;
+        }
+        for (int64_t d = 0; d < D; ++d) {
+            float w;
+            if (wfmt == OR_W_E4M3) {
+                float s = (float)oracle_half_to_double(scales[row * nb + d / bs]);
+                float q = (float)oracle_e4m3_to_double(W[row * D + d]);
+                w = q * s;
+            } else {
+                int bits = wfmt == OR_W_U2 ? 2 : (wfmt == OR_W_U4 ? 4 : 8);
+                w = oracle_weight_nbits(W, scales, zp, zp ? OR_ZP_TENSOR : OR_ZP_NONE, 0.0f, V, D, bits, bs,
+                                        row, d);
+            }
+            out[i * D + d] = w;
+        }
+    }
+    return bad;
+}

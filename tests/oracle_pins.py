@@ -17,7 +17,13 @@ What pins what:
   * uniform zero point       -- scalar path vs a full tensor of the value;
   * QMoE composition         -- hand-worked fixture; the fused decode vs the
                                 unfused chain (oracle GEMMs + numpy bias,
-                                SwiGLU and weighted sum); one-hot slot weights.
+                                SwiGLU and weighted sum); one-hot slot weights;
+  * E4M3 decoding            -- torch's float8_e4m3fn conversion on all 256
+                                bit patterns;
+  * embedding gather         -- hand-worked fixture (u4 with and without zero
+                                points, E4M3); numpy row selection of the
+                                dequantized table; torch's float8 decode times
+                                the scale.
 """
 from __future__ import annotations
 
@@ -363,8 +369,86 @@ def check_uniform_detection(lib):
     assert O.fp16_uniform_value(np.array([h(-3.0)], np.uint16), lib=lib) == (True, -3.0)
 
 
+# ---------------------------------------------------------------------------
+def _e4m3_via_torch(b: np.ndarray) -> np.ndarray:
+    import torch
+
+    t = torch.from_numpy(np.asarray(b, dtype=np.uint8).copy()).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def check_e4m3_decode(lib):
+    """All 256 E4M3 patterns against torch's float8_e4m3fn conversion."""
+    got = np.array([O.e4m3_to_double(b, lib) for b in range(256)])
+    ref = _e4m3_via_torch(np.arange(256))
+    assert np.array_equal(got, ref, equal_nan=True)
+    assert np.array_equal(np.signbit(got[~np.isnan(got)]), np.signbit(ref[~np.isnan(ref)]))
+
+
+def _exact(got, want):
+    want = np.asarray(want, dtype=np.float64)
+    got = np.asarray(got, dtype=np.float64)
+    assert got.shape == want.shape, (got.shape, want.shape)
+    assert np.array_equal(got, want), (got, want)
+    assert np.array_equal(np.signbit(got), np.signbit(want))
+
+
+def check_golden_gather(lib):
+    g = _golden("gather_handworked.json")
+    u = g["u4"]
+    W = np.array(u["W"], dtype=np.uint8)
+    sc = np.array(u["scales_f16"], dtype=np.uint16)
+    zp = np.array(u["zero_points_f16"], dtype=np.uint16)
+    out, bad = O.gather_block_quantized(u["indices"], W, sc, zp, V=u["V"], D=u["D"], fmt=O.W_U4,
+                                        block_size=u["block_size"], lib=lib)
+    _exact(out, u["out"])
+    assert bad == u["bad"]
+    out, bad = O.gather_block_quantized(u["indices"], W, sc, None, V=u["V"], D=u["D"], fmt=O.W_U4,
+                                        block_size=u["block_size"], lib=lib)
+    _exact(out, u["out_no_zp"])
+    assert bad == u["bad"]
+    e = g["e4m3"]
+    out, bad = O.gather_block_quantized(e["indices"], np.array(e["W"], dtype=np.uint8),
+                                        np.array(e["scales_f16"], dtype=np.uint16), None, V=e["V"], D=e["D"],
+                                        fmt=O.W_E4M3, block_size=e["block_size"], lib=lib)
+    _exact(out, e["out"])
+    assert bad == e["bad"]
+
+
+def check_gather_rows(lib):
+    """The gather equals row selection (numpy fancy indexing, negative indices
+    wrapped by numpy) of the dequantized table; E4M3 tables equal torch's
+    float8 decode times the fp16 scale in fp32 (numpy)."""
+    rng = np.random.default_rng(11)
+    V, D, bs = 37, 96, 32
+    idx = np.array([0, 36, -1, -37, 5, 5, 12, -20, 30], dtype=np.int64)
+    for fmt, bits in ((O.W_U2, 2), (O.W_U4, 4), (O.W_U8, 8)):
+        W = rng.integers(0, 256, size=(V, D * bits // 8), dtype=np.uint8)
+        sc = rng.uniform(-0.1, 0.1, size=(V, D // bs)).astype(np.float16).view(np.uint16)
+        zp = rng.integers(0, 1 << bits, size=(V, D // bs)).astype(np.float16).view(np.uint16)
+        for z, zmode in ((zp, O.ZP_TENSOR), (None, O.ZP_NONE)):
+            table = O.dequant_nbits(W, sc, z, N=V, K=D, bits=bits, block_size=bs, lib=lib)
+            out, bad = O.gather_block_quantized(idx, W, sc, z, V=V, D=D, fmt=fmt, block_size=bs, lib=lib)
+            assert bad == 0
+            _exact(out, table[idx])
+    W = rng.integers(0, 256, size=(V, D), dtype=np.uint8)
+    W[W & 0x7F == 0x7F] = 0x3F  # no NaN patterns, so that exact equality applies
+    sc = rng.uniform(-4, 4, size=(V, D // bs)).astype(np.float16)
+    table = (_e4m3_via_torch(W).astype(np.float32) * np.repeat(sc.astype(np.float32), bs, axis=1)).astype(np.float32)
+    out, bad = O.gather_block_quantized(idx, W, sc.view(np.uint16), None, V=V, D=D, fmt=O.W_E4M3, block_size=bs,
+                                        lib=lib)
+    assert bad == 0
+    _exact(out, table[idx])
+    out, bad = O.gather_block_quantized(np.array([V, -V - 1, 0]), W, sc.view(np.uint16), None, V=V, D=D,
+                                        fmt=O.W_E4M3, block_size=bs, lib=lib)
+    assert bad == 2
+    _exact(out[:2], np.zeros((2, D)))
+    _exact(out[2], table[0])
+
+
 ALL_CHECKS = [
     check_half_decode, check_bf16_decode, check_unpack_vs_unpackbits, check_golden_u2, check_golden_u3, check_golden_u4, check_golden_u8,
     check_golden_codebook, check_golden_qmoe, check_onehot, check_uniform_vs_tensor, check_closed_form,
     check_integer_codebook, check_library_matmul, check_rows_subset, check_qmoe_chain, check_uniform_detection,
+    check_e4m3_decode, check_golden_gather, check_gather_rows,
 ]

@@ -47,6 +47,13 @@ MUTANTS = {
     "uniform_by_value": ("if (t[i] != t[0]) return 0;",
                          "if (oracle_half_to_double(t[i]) != oracle_half_to_double(t[0])) return 0;"),
     "uniform_accepts_nan": ("if (isnan(v)) return 0;", ""),
+    "e4m3_exponent_bias": ("v = ldexp((double)(f + 8), e - 10);", "v = ldexp((double)(f + 8), e - 9);"),
+    "e4m3_subnormal_scale": ("v = ldexp((double)f, -9);", "v = ldexp((double)f, -10);"),
+    "e4m3_nan_missing": ("if (e == 15 && f == 7)\n        return NAN;", ""),
+    "gather_negative_not_wrapped": ("if (row < 0)\n            row += V;", ""),
+    "gather_bad_index_not_counted": ("++bad;\n            for (int64_t d = 0; d < D; ++d)",
+                                     "for (int64_t d = 0; d < D; ++d)"),
+    "gather_scale_by_position": ("scales[row * nb + d / bs]", "scales[i * nb + d / bs]"),
 }
 
 
