@@ -393,13 +393,14 @@ def run_ours(args, world, rank, local):
 
 
 # ------------------------------------------------------------- config suite
-def run_suite():
+def run_suite(only=None):
     """Time every configuration of the hot path through the public API (one
     JSON line each): tiny u4 GEMV; the phi4 u2 decode shapes at M=1 and M=4;
     8-bit codes on two of those shapes;
     the NF4 codebook shapes at M=1, 4, 16, 64 (bf16 activations); the QMoE
     decode (128 experts, top-8, 2880/2880, u4 block 32) with and without zero
-    points; the two M=2048 prefill GEMMs.  Each figure is the mean over a CUDA
+    points; the two M=2048 prefill GEMMs; the block-quantized embedding gather
+    (u4, u8, E4M3 tables).  Each figure is the mean over a CUDA
     graph of R back-to-back calls whose weights rotate over copies (or expert
     sets) totalling more than three times the L2, so every call reads cold
     weights; prefill is compute-bound and reuses one weight set."""
@@ -457,90 +458,120 @@ def run_suite():
     def reps_for(nbytes):
         return max(2, -(-3 * L2_BYTES // max(1, nbytes)))
 
+    def want(group):
+        return only is None or only in group
+
     # tiny u4 (M=1, 128 x 256, block 64, zero-point tensor)
-    d = WL.tiny_u4()
-    A, W, S, Z = torch.from_numpy(d["A"]).to(dev), torch.from_numpy(d["W"]).to(dev), t16(d["scales"], torch.float16), \
-        t16(d["zero_points"], torch.float16)
-    Y = torch.empty(1, 128, device=dev)
-    emit("tiny_u4_m1", timed(lambda i: qg.qgemm_nbits(A, W, S, Z, Y, bits=4, block_size=64, stream=st), 50))
+    if want("tiny_u4"):
+        d = WL.tiny_u4()
+        A, W, S, Z = torch.from_numpy(d["A"]).to(dev), torch.from_numpy(d["W"]).to(dev), t16(d["scales"], torch.float16), \
+            t16(d["zero_points"], torch.float16)
+        Y = torch.empty(1, 128, device=dev)
+        emit("tiny_u4_m1", timed(lambda i: qg.qgemm_nbits(A, W, S, Z, Y, bits=4, block_size=64, stream=st), 50))
 
     # phi4 u2 decode, M = 1 and 4
-    for M in (1, 4):
-        for shape in SHAPES:
-            d = WL.phi4_u2(shape, M=M)
+    if want("phi4_u2"):
+        for M in (1, 4):
+            for shape in SHAPES:
+                d = WL.phi4_u2(shape, M=M)
+                wb = d["W"].nbytes + d["scales"].nbytes
+                r = reps_for(wb)
+                Ws = [torch.from_numpy(d["W"]).to(dev) for _ in range(r)]
+                Ss = [t16(d["scales"], torch.float16) for _ in range(r)]
+                A = torch.from_numpy(d["A"]).to(dev)
+                Y = torch.empty(M, d["N"], device=dev)
+                ws = torch.empty(max(16, qg.qgemm_workspace_bytes(0, M, d["N"], d["K"], 2, 64)), dtype=torch.uint8, device=dev)
+                us = timed(lambda i: qg.qgemm_nbits_uniform_zp(A, Ws[i % r], Ss[i % r], ZP, Y, bits=2, block_size=64,
+                                                               workspace=ws, stream=st), 2 * r)
+                emit("phi4_u2_%s_m%d" % (shape, M), us, nbytes=wb)
+                del Ws, Ss
+
+    # 8-bit MatMulNBits codes on two of the phi4 shapes, M = 1
+    if want("phi4_u8"):
+        for shape in ("qkv", "lm_head"):
+            d = WL.phi4_u8(shape, M=1)
             wb = d["W"].nbytes + d["scales"].nbytes
             r = reps_for(wb)
             Ws = [torch.from_numpy(d["W"]).to(dev) for _ in range(r)]
-            Ss = [t16(d["scales"], torch.float16) for _ in range(r)]
+            S = t16(d["scales"], torch.float16)
             A = torch.from_numpy(d["A"]).to(dev)
-            Y = torch.empty(M, d["N"], device=dev)
-            ws = torch.empty(max(16, qg.qgemm_workspace_bytes(0, M, d["N"], d["K"], 2, 64)), dtype=torch.uint8, device=dev)
-            us = timed(lambda i: qg.qgemm_nbits_uniform_zp(A, Ws[i % r], Ss[i % r], ZP, Y, bits=2, block_size=64,
+            Y = torch.empty(1, d["N"], device=dev)
+            ws = torch.empty(max(16, qg.qgemm_workspace_bytes(0, 1, d["N"], d["K"], 8, 64)), dtype=torch.uint8, device=dev)
+            us = timed(lambda i: qg.qgemm_nbits_uniform_zp(A, Ws[i % r], S, 128.0, Y, bits=8, block_size=64,
                                                            workspace=ws, stream=st), 2 * r)
-            emit("phi4_u2_%s_m%d" % (shape, M), us, nbytes=wb)
-            del Ws, Ss
-
-    # 8-bit MatMulNBits codes on two of the phi4 shapes, M = 1
-    for shape in ("qkv", "lm_head"):
-        d = WL.phi4_u8(shape, M=1)
-        wb = d["W"].nbytes + d["scales"].nbytes
-        r = reps_for(wb)
-        Ws = [torch.from_numpy(d["W"]).to(dev) for _ in range(r)]
-        S = t16(d["scales"], torch.float16)
-        A = torch.from_numpy(d["A"]).to(dev)
-        Y = torch.empty(1, d["N"], device=dev)
-        ws = torch.empty(max(16, qg.qgemm_workspace_bytes(0, 1, d["N"], d["K"], 8, 64)), dtype=torch.uint8, device=dev)
-        us = timed(lambda i: qg.qgemm_nbits_uniform_zp(A, Ws[i % r], S, 128.0, Y, bits=8, block_size=64,
-                                                       workspace=ws, stream=st), 2 * r)
-        emit("phi4_u8_%s_m1" % shape, us, nbytes=wb)
-        del Ws
-
-    # NF4 codebook, bf16 activations
-    for shape in ("square", "gqa_kv", "up", "down"):
-        for M in (1, 4, 16, 64):
-            d = WL.nf4(shape, M=M, a_dtype=2)
-            wb = d["W"].nbytes + d["absmax"].nbytes
-            r = reps_for(wb)
-            Ws = [torch.from_numpy(d["W"]).to(dev) for _ in range(r)]
-            am = torch.from_numpy(d["absmax"]).to(dev)
-            cb = torch.from_numpy(d["codebook"]).to(dev)
-            A = t16(d["A"], torch.bfloat16)
-            Y = torch.empty(M, d["N"], device=dev, dtype=torch.bfloat16)
-            ws = torch.empty(max(16, qg.qgemm_workspace_bytes(2, M, d["N"], d["K"], 4, 64)), dtype=torch.uint8, device=dev)
-            us = timed(lambda i: qg.qgemm_codebook4(A, Ws[i % r], cb, am, Y, block_size=64, workspace=ws, stream=st), 2 * r)
-            emit("nf4_%s_%dx%d_m%d" % (shape, d["N"], d["K"], M), us, nbytes=wb,
-                 flops=2.0 * M * d["N"] * d["K"])
+            emit("phi4_u8_%s_m1" % shape, us, nbytes=wb)
             del Ws
 
+    # NF4 codebook, bf16 activations
+    if want("nf4"):
+        for shape in ("square", "gqa_kv", "up", "down"):
+            for M in (1, 4, 16, 64):
+                d = WL.nf4(shape, M=M, a_dtype=2)
+                wb = d["W"].nbytes + d["absmax"].nbytes
+                r = reps_for(wb)
+                Ws = [torch.from_numpy(d["W"]).to(dev) for _ in range(r)]
+                am = torch.from_numpy(d["absmax"]).to(dev)
+                cb = torch.from_numpy(d["codebook"]).to(dev)
+                A = t16(d["A"], torch.bfloat16)
+                Y = torch.empty(M, d["N"], device=dev, dtype=torch.bfloat16)
+                ws = torch.empty(max(16, qg.qgemm_workspace_bytes(2, M, d["N"], d["K"], 4, 64)), dtype=torch.uint8, device=dev)
+                us = timed(lambda i: qg.qgemm_codebook4(A, Ws[i % r], cb, am, Y, block_size=64, workspace=ws, stream=st), 2 * r)
+                emit("nf4_%s_%dx%d_m%d" % (shape, d["N"], d["K"], M), us, nbytes=wb,
+                     flops=2.0 * M * d["N"] * d["K"])
+                del Ws
+
     # QMoE decode: rotate over disjoint expert sets (128 experts, top-8)
-    for with_zp in (False, True):
-        d = WL.qmoe(with_zp=with_zp)
-        h = lambda a: None if a is None else t16(a, torch.float16)
-        kw = dict(num_experts=d["num_experts"], fc1_w=torch.from_numpy(d["fc1_w"]).to(dev), fc1_scales=h(d["fc1_scales"]),
-                  fc1_zp=h(d["fc1_zp"]), fc1_bias=h(d["fc1_bias"]), fc2_w=torch.from_numpy(d["fc2_w"]).to(dev),
-                  fc2_scales=h(d["fc2_scales"]), fc2_zp=h(d["fc2_zp"]), fc2_bias=h(d["fc2_bias"]), bits=4, block_size=32)
-        k, E = d["k"], d["num_experts"]
-        sets = [torch.arange(j * k, (j + 1) * k, dtype=torch.int32, device=dev) for j in range(E // k)]
-        wts = torch.from_numpy(d["weights"]).to(dev)
-        x = h(d["x"])
-        y = torch.empty(d["hidden"], dtype=torch.float16, device=dev)
-        ws = torch.empty(qg.qmoe_decode_workspace_bytes(k, d["hidden"], d["inter"]), dtype=torch.uint8, device=dev)
-        per_expert = (d["fc1_w"][0].nbytes + d["fc1_scales"][0].nbytes + d["fc2_w"][0].nbytes + d["fc2_scales"][0].nbytes
-                      + (d["fc1_zp"][0].nbytes + d["fc2_zp"][0].nbytes if with_zp else 0))
-        us = timed(lambda i: qg.qmoe_decode_fused(x, sets[i % len(sets)], wts, y=y, workspace=ws, stream=st, **kw),
-                   len(sets))
-        emit("qmoe_top8_2880_u4_bs32_%s" % ("zp" if with_zp else "nozp"), us, nbytes=k * per_expert)
-        del kw
+    if want("qmoe"):
+        for with_zp in (False, True):
+            d = WL.qmoe(with_zp=with_zp)
+            h = lambda a: None if a is None else t16(a, torch.float16)
+            kw = dict(num_experts=d["num_experts"], fc1_w=torch.from_numpy(d["fc1_w"]).to(dev), fc1_scales=h(d["fc1_scales"]),
+                      fc1_zp=h(d["fc1_zp"]), fc1_bias=h(d["fc1_bias"]), fc2_w=torch.from_numpy(d["fc2_w"]).to(dev),
+                      fc2_scales=h(d["fc2_scales"]), fc2_zp=h(d["fc2_zp"]), fc2_bias=h(d["fc2_bias"]), bits=4, block_size=32)
+            k, E = d["k"], d["num_experts"]
+            sets = [torch.arange(j * k, (j + 1) * k, dtype=torch.int32, device=dev) for j in range(E // k)]
+            wts = torch.from_numpy(d["weights"]).to(dev)
+            x = h(d["x"])
+            y = torch.empty(d["hidden"], dtype=torch.float16, device=dev)
+            ws = torch.empty(qg.qmoe_decode_workspace_bytes(k, d["hidden"], d["inter"]), dtype=torch.uint8, device=dev)
+            per_expert = (d["fc1_w"][0].nbytes + d["fc1_scales"][0].nbytes + d["fc2_w"][0].nbytes + d["fc2_scales"][0].nbytes
+                          + (d["fc1_zp"][0].nbytes + d["fc2_zp"][0].nbytes if with_zp else 0))
+            us = timed(lambda i: qg.qmoe_decode_fused(x, sets[i % len(sets)], wts, y=y, workspace=ws, stream=st, **kw),
+                       len(sets))
+            emit("qmoe_top8_2880_u4_bs32_%s" % ("zp" if with_zp else "nozp"), us, nbytes=k * per_expert)
+            del kw
 
     # prefill u2, M = 2048, fp16 activations, fp32 out
-    for shape in ("gate_up", "down"):
-        d = WL.prefill_u2(shape, M=2048)
-        A, W, S = t16(d["A"], torch.float16), torch.from_numpy(d["W"]).to(dev), t16(d["scales"], torch.float16)
-        Y = torch.empty(d["M"], d["N"], device=dev)
-        ws = torch.empty(max(16, qg.qgemm_workspace_bytes(1, d["M"], d["N"], d["K"], 2, 64)), dtype=torch.uint8, device=dev)
-        us = timed(lambda i: qg.qgemm_nbits_uniform_zp(A, W, S, ZP, Y, bits=2, block_size=64, workspace=ws, stream=st), 4)
-        emit("prefill_u2_%s_m2048" % shape, us, flops=2.0 * d["M"] * d["N"] * d["K"])
-        del A, W, S, Y
+    if want("prefill"):
+        for shape in ("gate_up", "down"):
+            d = WL.prefill_u2(shape, M=2048)
+            A, W, S = t16(d["A"], torch.float16), torch.from_numpy(d["W"]).to(dev), t16(d["scales"], torch.float16)
+            Y = torch.empty(d["M"], d["N"], device=dev)
+            ws = torch.empty(max(16, qg.qgemm_workspace_bytes(1, d["M"], d["N"], d["K"], 2, 64)), dtype=torch.uint8, device=dev)
+            us = timed(lambda i: qg.qgemm_nbits_uniform_zp(A, W, S, ZP, Y, bits=2, block_size=64, workspace=ws, stream=st), 4)
+            emit("prefill_u2_%s_m2048" % shape, us, flops=2.0 * d["M"] * d["N"] * d["K"])
+            del A, W, S, Y
+
+    # block-quantized embedding gather: phi4 table 100352 x 5120, block 32, 2048 token ids, fp16 out.
+    # 16 index sets, each drawn from its own sixteenth of the vocabulary, so a row read by one call
+    # is not read again for 15 calls (over 3x the L2 of traffic in between).
+    if want("gather"):
+        for fmt, name in ((1, "u4"), (2, "u8"), (3, "e4m3")):
+            d = WL.embedding(fmt)
+            n, D, V, bs = d["n"], d["D"], d["V"], d["block_size"]
+            W = torch.from_numpy(d["W"]).to(dev)
+            S = t16(d["scales"], torch.float16)
+            Z = None if d["zero_points"] is None else t16(d["zero_points"], torch.float16)
+            g = np.random.Generator(np.random.PCG64(1))
+            sets = [torch.from_numpy(g.integers(j * (V // 16), (j + 1) * (V // 16), size=n, dtype=np.int64)).to(dev)
+                    for j in range(16)]
+            Y = torch.empty(n, D, dtype=torch.float16, device=dev)
+            nbytes = n * (8 + D * WL.EMBED_BITS[fmt] // 8 + (D // bs) * 2 * (1 if Z is None else 2) + D * 2)
+            us = timed(lambda i: qg.qg_gather_block_quantized(sets[i % 16], W, S, Z, Y, w_format=fmt, block_size=bs,
+                                                              stream=st), 32)
+            emit("gather_%s_phi4_embed_n2048_bs32_f16" % name, us, nbytes=nbytes, bytes_include="indices, codes, "
+                 "scales, zero points, fp16 output")
+            del W, S, Z, Y
     return 0
 
 
@@ -554,6 +585,8 @@ def run_probe(name):
     tc_prefill   4 calls of a prefill-sized u2 GEMM on the tensor cores
                  (M=2048, N=K=5120, fp16 activations, fp32 out)
     qmoe         4 calls of the 128-expert top-8 2880/2880 block-32 QMoE decode
+    gather       4 calls of the u4 embedding gather (100352 x 5120 table, block 32,
+                 2048 token ids, fp16 out)
     """
     import torch
 
@@ -597,6 +630,15 @@ def run_probe(name):
         x, ids, w = h(d["x"]), torch.from_numpy(d["ids"]).cuda(), torch.from_numpy(d["weights"]).cuda()
         for _ in range(4):
             qg.qmoe_decode_fused(x, ids, w, **kw)
+    elif name == "gather":
+        d = WL.embedding(1)
+        W = torch.from_numpy(d["W"]).cuda()
+        S = torch.from_numpy(d["scales"].view(np.int16)).cuda().view(torch.float16)
+        Z = torch.from_numpy(d["zero_points"].view(np.int16)).cuda().view(torch.float16)
+        idx = torch.from_numpy(d["indices"]).cuda()
+        Y = torch.empty(d["n"], d["D"], dtype=torch.float16, device="cuda")
+        for _ in range(4):
+            qg.qg_gather_block_quantized(idx, W, S, Z, Y, w_format=1, block_size=d["block_size"])
     else:
         raise SystemExit("unknown probe %r" % name)
     torch.cuda.synchronize()
@@ -611,15 +653,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--probe", choices=["gemv_k5120", "gemv_lm_head", "tc_prefill", "qmoe"],
+    ap.add_argument("--probe", choices=["gemv_k5120", "gemv_lm_head", "tc_prefill", "qmoe", "gather"],
                     help="run a small fixed workload for a profiler capture instead of the benchmark")
     ap.add_argument("--suite", action="store_true",
                     help="time every configuration (one JSON line each) instead of the benchmark")
+    ap.add_argument("--only", choices=["tiny_u4", "phi4_u2", "phi4_u8", "nf4", "qmoe", "prefill", "gather"],
+                    help="with --suite: time one group of configurations only")
     args = ap.parse_args()
     if args.probe:
         return run_probe(args.probe)
-    if args.suite:
-        return run_suite()
+    if args.suite or args.only:
+        return run_suite(args.only)
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_setup(args.gpus)

@@ -23,11 +23,13 @@ __all__ = [
     "qmoe_decode_fused", "qmoe_decode_fused_noalloc", "qmoe_decode_workspace_bytes", "QG_QMOE_NOALLOC_SCRATCH_BYTES",
     "qg_fp16_uniform_value", "qg_dequant_nbits",
     "qg_dequant_nbits_uniform_zp", "qg_dequant_codebook4", "qg_read_device_fault", "qg_status_string",
+    "qg_gather_block_quantized", "QG_WF_U2", "QG_WF_U4", "QG_WF_U8", "QG_WF_E4M3",
 ]
 
 QG_OK, QG_ERR_INVALID_ARG, QG_ERR_UNSUPPORTED, QG_ERR_CUDA, QG_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3, 4
 QG_F32, QG_F16, QG_BF16 = 0, 1, 2
 QG_QMOE_NOALLOC_SCRATCH_BYTES = 1 << 20
+QG_WF_U2, QG_WF_U4, QG_WF_U8, QG_WF_E4M3 = 0, 1, 2, 3
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libqgemm.so")
@@ -65,6 +67,7 @@ _SIGS = {
     "qg_dequant_nbits": ([_P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "qg_dequant_nbits_uniform_zp": ([_P, _P, _F, _P, _I, _I, _I, _I, _P], _I),
     "qg_dequant_codebook4": ([_P, _P, _P, _P, _I, _I, _I, _P], _I),
+    "qg_gather_block_quantized": ([_P, ctypes.c_int64, _P, _I, _P, _P, ctypes.c_int64, _I, _I, _P, _I, _P, _P], _I),
     "qg_read_device_fault": ([_P], _I),
     "qg_status_string": ([_I], ctypes.c_char_p),
 }
@@ -228,6 +231,21 @@ def qg_dequant_codebook4(W, codebook, absmax, out, *, block_size, stream=None, r
     s = lib().qg_dequant_codebook4(_ptr(W), _ptr(codebook), _ptr(absmax), _ptr(out), N, K, block_size,
                                    _stream(stream))
     return s if raw else _check(s, "qg_dequant_codebook4")
+
+
+def qg_gather_block_quantized(indices, W, scales, zero_points, Y, *, w_format, block_size, status=None, stream=None,
+                              raw=False):
+    """Y[i] = dequant(table row indices[i]) for a block-quantized [vocab, D] table.
+
+    indices: int64 (any shape; Y is [indices.numel(), D]); W: [vocab, D*bits/8] uint8 codes or
+    [vocab, D] E4M3 bytes; scales / zero_points: [vocab, D/block_size] float16 (zero_points None
+    for the midpoint, and for E4M3); Y: float32/float16/bfloat16; status: a device int32 or None.
+    """
+    n, D = Y.shape
+    s = lib().qg_gather_block_quantized(_ptr(indices), n, _ptr(W), int(w_format), _ptr(scales), _ptr(zero_points),
+                                        W.shape[0], D, block_size, _ptr(Y), _dtype_code(Y), _ptr(status),
+                                        _stream(stream))
+    return s if raw else _check(s, "qg_gather_block_quantized")
 
 
 def qg_read_device_fault() -> int:

@@ -362,6 +362,42 @@ int qg_dequant_codebook4(const uint8_t *W, const float *codebook16, const float 
     return dequant_common(p, out, stream);
 }
 
+int qg_gather_block_quantized(const int64_t *indices, int64_t n_indices, const uint8_t *W, int w_format,
+                              const uint16_t *scales_f16, const uint16_t *zero_points_f16, int64_t vocab, int D,
+                              int block_size, void *Y, int y_dtype, int *status_dev, qg_stream_t stream) {
+    (void)cudaGetLastError();
+    if (n_indices < 0 || vocab < 0 || D < 0) return QG_ERR_INVALID_ARG;
+    if (w_format < QG_WF_U2 || w_format > QG_WF_E4M3) return QG_ERR_UNSUPPORTED;
+    if (y_dtype != QG_F32 && y_dtype != QG_F16 && y_dtype != QG_BF16) return QG_ERR_UNSUPPORTED;
+    if (!valid_bs(block_size)) return QG_ERR_UNSUPPORTED;
+    if (D % block_size) return QG_ERR_INVALID_ARG;
+    if (w_format == QG_WF_E4M3 && zero_points_f16) return QG_ERR_INVALID_ARG;
+    if (D > kMaxK) return QG_ERR_UNSUPPORTED;
+    if (status_dev && (reinterpret_cast<uintptr_t>(status_dev) & 3u)) return QG_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (status_dev && cudaMemsetAsync(status_dev, 0, sizeof(int), s) != cudaSuccess) return QG_ERR_CUDA;
+    if (n_indices == 0 || D == 0) return QG_OK;
+    if (!indices || !Y) return QG_ERR_INVALID_ARG;
+    if (vocab > 0 && (!W || !scales_f16)) return QG_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(indices) & 7u) return QG_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(scales_f16) || !aligned16(Y) || (zero_points_f16 && !aligned16(zero_points_f16)))
+        return QG_ERR_INVALID_ARG;
+    qg::GatherProblem g{};
+    g.idx = indices;
+    g.n = n_indices;
+    g.W = W;
+    g.fmt = w_format;
+    g.scales = scales_f16;
+    g.zp = zero_points_f16;
+    g.V = vocab;
+    g.D = D;
+    g.bs = block_size;
+    g.Y = Y;
+    g.y_dtype = y_dtype;
+    g.status = status_dev;
+    return qg::launch_gather(g, s) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
 int qg_read_device_fault(unsigned int *flags) {
     if (!flags) return QG_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return QG_ERR_CUDA;

@@ -85,6 +85,22 @@ struct QmoeProblem {
 size_t qmoe_workspace_bytes(int k, int hidden, int inter);
 cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s);
 
+// Block-quantized embedding gather (validated request).
+struct GatherProblem {
+    const int64_t *idx;
+    long long n;              // number of indices
+    const uint8_t *W;         // [V][D * bits / 8]
+    int fmt;                  // 0 u2, 1 u4, 2 u8, 3 E4M3 (QG_WF_*)
+    const uint16_t *scales;   // [V][D / bs] fp16
+    const uint16_t *zp;       // [V][D / bs] fp16 or null (integer formats only)
+    long long V;
+    int D, bs;
+    void *Y;                  // [n][D]
+    int y_dtype;
+    int *status;              // set to 1 when an index is out of range, or null
+};
+cudaError_t launch_gather(const GatherProblem &g, cudaStream_t s);
+
 // Utility kernels.
 cudaError_t launch_dequant(const GemmProblem &p, float *out, cudaStream_t s);
 cudaError_t launch_uniform_check(const uint16_t *t, size_t n, unsigned *ws, cudaStream_t s);

@@ -242,6 +242,39 @@ int qg_dequant_codebook4(const uint8_t *W, const float *codebook16, const float 
                          int block_size, qg_stream_t stream);
 
 /*
+ * qg_gather_block_quantized -- embedding lookup in a block-quantized table.
+ * [hip-ep #1318] kernel test table, gather_block_quantized leaves
+ * Xi64_Wu4_Yfp16, Xi64_Wu8_Yfp16 and Xi64_Wfp8_Yfp16 ("Summary", Commit 3:
+ * embedding lookups through a gather).  The pages name the op and its types;
+ * the layout and rule below are this library's reading of them.
+ *
+ *   Y[i][d] = round_to(y_dtype, w(row_i, d)),  row_i = indices[i], or
+ *             indices[i] + vocab when indices[i] < 0
+ *   integer formats: w = fl32( fl32(q - zp) * s )  (as qgemm_nbits; zp the
+ *                    midpoint 2^(bits-1) when zero_points_f16 is NULL)
+ *   QG_WF_E4M3:      w = fl32( e4m3(q) * s )  (OCP E4M3 without infinities;
+ *                    no zero point)
+ *   with s = scales_f16[row_i][d / block_size], and rounding to nearest-even.
+ *
+ *   indices      [n_indices] int64 (device, 8-byte aligned).  An index outside
+ *                [-vocab, vocab) gives a zero row and sets *status_dev to 1.
+ *   W            [vocab][D*bits/8] codes packed LSB-first along D (bits 2, 4
+ *                or 8 for QG_WF_U2 / U4 / U8), or [vocab][D] E4M3 bytes
+ *   scales_f16   [vocab][D/block_size] fp16
+ *   zero_points_f16  same shape, fp16, or NULL; must be NULL for E4M3
+ *   block_size   32, 64, 128 or 256; D a multiple of it
+ *   Y            [n_indices][D] of y_dtype (QG_F32, QG_F16 or QG_BF16)
+ *   status_dev   device int, written with 0 (every index valid) or 1, or NULL
+ * W, scales, zero points and Y must be 16-byte aligned.  Results are exact
+ * (bit-identical to the definition) whenever w is exact in fp32, e.g. for
+ * integer or half-integer zero points and for every E4M3 table.
+ */
+enum { QG_WF_U2 = 0, QG_WF_U4 = 1, QG_WF_U8 = 2, QG_WF_E4M3 = 3 };
+int qg_gather_block_quantized(const int64_t *indices, int64_t n_indices, const uint8_t *W, int w_format,
+                              const uint16_t *scales_f16, const uint16_t *zero_points_f16, int64_t vocab, int D,
+                              int block_size, void *Y, int y_dtype, int *status_dev, qg_stream_t stream);
+
+/*
  * qg_read_device_fault -- every wait inside the library's kernels is
  * bounded; a wait that gives up records a bit in a device-side fault word
  * instead of hanging.  This call synchronises the current device, returns

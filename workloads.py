@@ -226,3 +226,26 @@ def prefill_u2(shape: str, M: int = 2048, seed: int = 0) -> dict:
     A = activations(g, M, K, F16)
     return dict(M=M, N=N, K=K, bits=bits, block_size=bs, W=W, scales=scales, zero_points=None,
                 uniform_zp=1.5, A=A, a_dtype=F16)
+
+
+# Embedding tables: the kernel test table's gather_block_quantized leaves
+# (int64 indices, u4 / u8 / fp8 table, fp16 output), on phi4-14B's
+# embedding shape (vocab 100352, hidden 5120) looked up for a 2048-token
+# prompt.  Table formats: 0 u2, 1 u4, 2 u8, 3 E4M3.
+EMBED_BITS = {0: 2, 1: 4, 2: 8, 3: 8}
+
+
+def embedding(fmt: int, V: int = 100352, D: int = 5120, n: int = 2048, block_size: int = 32,
+              zero_points: bool = True, seed: int = 0) -> dict:
+    """Table codes (uniform bytes; E4M3 tables without the two NaN patterns),
+    fp16 scales U(0.005, 0.02), fp16 integer zero points (integer formats) and
+    n token ids uniform in [0, V)."""
+    g = rng(seed)
+    bits = EMBED_BITS[fmt]
+    W = packed_codes(g, V, D, bits)
+    if fmt == 3:
+        W[(W & 0x7F) == 0x7F] ^= 1  # 0x7F / 0xFF (NaN) -> 0x7E / 0xFE
+    scales = fp16_uniform(g, (V, D // block_size), 0.005, 0.02)
+    zp = fp16_uniform_int(g, (V, D // block_size), 0, (1 << bits) - 1) if (zero_points and fmt != 3) else None
+    idx = g.integers(0, V, size=n, dtype=np.int64)
+    return dict(fmt=fmt, V=V, D=D, n=n, block_size=block_size, W=W, scales=scales, zero_points=zp, indices=idx)
