@@ -78,6 +78,11 @@ def load(path: str | None = None):
         lib.oracle_e4m3_to_double.restype = D
         lib.oracle_gather_block_quantized.argtypes = [P, I64, P, I, P, P, I64, I64, I, P]
         lib.oracle_gather_block_quantized.restype = I64
+        lib.oracle_quantize_i8_blocks.argtypes = [P, I64, I, P, P]
+        lib.oracle_quantize_i8_blocks.restype = None
+        lib.oracle_qmoe_decode_dp4a.argtypes = [P, P, P, I, I, P, P, P, P, P, P, P, P, I64, I64, I, I, I, P, P, P,
+                                                P, P]
+        lib.oracle_qmoe_decode_dp4a.restype = I
         if path is None:
             _lib = lib
         return lib
@@ -199,6 +204,42 @@ def qmoe_decode(x_f16, ids, weights, *, num_experts, fc1_w, fc1_scales, fc1_zp, 
         _ptr(x_f16), _ptr(ids), _ptr(weights), ids.size, num_experts, _ptr(fc1_w), _ptr(fc1_scales),
         _ptr(fc1_zp), _ptr(fc1_bias), _ptr(fc2_w), _ptr(fc2_scales), _ptr(fc2_zp), _ptr(fc2_bias),
         hidden, inter, bits, block_size, int(swiglu_interleaved), _ptr(g), _ptr(h), _ptr(y))
+    return y, bad
+
+
+def quantize_i8_blocks(v, block_size, lib=None):
+    """Per-block symmetric int8 quantization of an fp32 vector (dp4a QMoE activations).
+
+    Returns (q8 int8 [n], sx float32 [n / block_size]).
+    """
+    v = _c(np.asarray(v, dtype=np.float32).reshape(-1), np.float32)
+    q8 = np.empty(v.size, dtype=np.int8)
+    sx = np.empty(v.size // block_size, dtype=np.float32)
+    (lib or load()).oracle_quantize_i8_blocks(_ptr(v), v.size, block_size, _ptr(q8), _ptr(sx))
+    return q8, sx
+
+
+def qmoe_decode_dp4a(x_f16, ids, weights, *, num_experts, fc1_w, fc1_scales, fc1_zp, fc1_bias, fc2_w,
+                     fc2_scales, fc2_zp, fc2_bias, hidden, inter, bits, block_size, swiglu_interleaved=0,
+                     lib=None):
+    """The int8-activation decode: unrounded fp64 y[hidden] and the number of out-of-range slots."""
+    x_f16 = _c(x_f16, np.uint16)
+    ids = _c(ids, np.int32)
+    weights = _c(weights, np.float32)
+    fc1_w, fc2_w = _c(fc1_w, np.uint8), _c(fc2_w, np.uint8)
+    fc1_scales, fc2_scales = _c(fc1_scales, np.uint16), _c(fc2_scales, np.uint16)
+    fc1_zp, fc2_zp = _c(fc1_zp, np.uint16), _c(fc2_zp, np.uint16)
+    fc1_bias, fc2_bias = _c(fc1_bias, np.uint16), _c(fc2_bias, np.uint16)
+    n = max(hidden, inter)
+    g = np.empty(2 * inter, dtype=np.float64)
+    h = np.empty(n, dtype=np.float32)
+    q8 = np.empty(n, dtype=np.int8)
+    sx = np.empty(n // block_size, dtype=np.float32)
+    y = np.empty(hidden, dtype=np.float64)
+    bad = (lib or load()).oracle_qmoe_decode_dp4a(
+        _ptr(x_f16), _ptr(ids), _ptr(weights), ids.size, num_experts, _ptr(fc1_w), _ptr(fc1_scales),
+        _ptr(fc1_zp), _ptr(fc1_bias), _ptr(fc2_w), _ptr(fc2_scales), _ptr(fc2_zp), _ptr(fc2_bias),
+        hidden, inter, bits, block_size, int(swiglu_interleaved), _ptr(g), _ptr(h), _ptr(q8), _ptr(sx), _ptr(y))
     return y, bad
 
 

@@ -377,3 +377,120 @@ int64_t oracle_gather_block_quantized(const int64_t *idx, int64_t n, const uint8
     }
     return bad;
 }
+
+/* ------------------------------------------------------------------------ */
+/* int8-activation QMoE decode ([P2] Summary: the fused decode "and its dp4a */
+/* variant"; Test plan: fp and dp4a x block size x zero points x bias, a CPU */
+/* reference that quantizes where the kernels do; Why: int8 activations).    */
+/* The pages do not give the activation quantization; reading: per block of  */
+/* bs consecutive values along the contraction, symmetric int8 with the      */
+/* block's largest magnitude mapped to 127, every step in fp32:              */
+/*     a = max |v|;  sx = fl32(a / 127);                                     */
+/*     q8 = clamp(rint(fl32(v / sx)), -127, 127)   (ties to even)            */
+/* and a block of zeros has sx = 0 and q8 = 0.  The decision (q8) is taken   */
+/* in fp32 on both sides of any comparison.                                  */
+/* ------------------------------------------------------------------------ */
+void oracle_quantize_i8_blocks(const float *v, int64_t n, int bs, int8_t *q8, float *sx)
+{
+    for (int64_t b = 0; b < n / bs; ++b) {
+        float a = 0.0f;
+        for (int64_t k = b * bs; k < (b + 1) * bs; ++k) {
+            float m = fabsf(v[k]);
+            if (m > a)
+                a = m;
+        }
+        if (a == 0.0f) {
+            sx[b] = 0.0f;
+            for (int64_t k = b * bs; k < (b + 1) * bs; ++k)
+                q8[k] = 0;
+            continue;
+        }
+        float s = a / 127.0f;
+        sx[b] = s;
+        for (int64_t k = b * bs; k < (b + 1) * bs; ++k) {
+            float r = rintf(v[k] / s);
+            if (r > 127.0f)
+                r = 127.0f;
+            if (r < -127.0f)
+                r = -127.0f;
+            q8[k] = (int8_t)r;
+        }
+    }
+}
+
+/* One output of a dp4a GEMV: sum over blocks b of
+ *     s[r,b] * sx[b] * ( sum_{k in b} q8[k] * q[r,k]  -  zp[r,b] * sum_{k in b} q8[k] )
+ * with the integer sums exact and the rest in fp64 (zp: the fp16 zero point,
+ * or the midpoint 2^(bits-1) when the tensor is absent). */
+static double dp4a_row(const int8_t *q8, const float *sx, const uint8_t *W, const uint16_t *scales,
+                       const uint16_t *zp, int64_t K, int bits, int bs, int64_t r)
+{
+    int64_t nb = K / bs;
+    double acc = 0.0;
+    for (int64_t b = 0; b < nb; ++b) {
+        int64_t dot = 0, sum = 0;
+        for (int64_t k = b * bs; k < (b + 1) * bs; ++k) {
+            dot += (int64_t)q8[k] * oracle_code(W, K, r, k, bits);
+            sum += q8[k];
+        }
+        double z = zp ? oracle_half_to_double(zp[r * nb + b]) : (double)(1 << (bits - 1));
+        double s = oracle_half_to_double(scales[r * nb + b]);
+        acc += s * (double)sx[b] * ((double)dot - z * (double)sum);
+    }
+    return acc;
+}
+
+/* The decode: for slot j (ascending) with e = ids[j] in range,
+ *   x8 = quantize(x);  g[r] = dp4a_row(x8, fc1[e], r) + b1[e][r];
+ *   h = silu(gate) * up, rounded to fp32;  h8 = quantize(h);
+ *   o[r] = dp4a_row(h8, fc2[e], r) + b2[e][r];  y += w_j * o.
+ * Returns the number of out-of-range ids (their slots add nothing).
+ * Scratch from the caller: g [2I] doubles, h [I] floats, q8 [max(H, I)]
+ * bytes, sx [max(H, I)/bs] floats. */
+int oracle_qmoe_decode_dp4a(const uint16_t *x_f16, const int32_t *ids, const float *weights, int k,
+                            int num_experts, const uint8_t *fc1_w, const uint16_t *fc1_scales,
+                            const uint16_t *fc1_zp, const uint16_t *fc1_bias, const uint8_t *fc2_w,
+                            const uint16_t *fc2_scales, const uint16_t *fc2_zp, const uint16_t *fc2_bias,
+                            int64_t hidden, int64_t inter, int bits, int bs, int swiglu_interleaved, double *g,
+                            float *h, int8_t *q8, float *sx, double *y)
+{
+    const int64_t H = hidden, I = inter, I2 = 2 * inter;
+    const int64_t fc1_row_bytes = H * bits / 8, fc2_row_bytes = I * bits / 8;
+    const int64_t fc1_nb = H / bs, fc2_nb = I / bs;
+    int bad = 0;
+    for (int64_t i = 0; i < H; ++i) y[i] = 0.0;
+    for (int j = 0; j < k; ++j) {
+        int e = ids[j];
+        if (e < 0 || e >= num_experts) {
+            ++bad;
+            continue;
+        }
+        const uint8_t *w1 = fc1_w + (int64_t)e * I2 * fc1_row_bytes;
+        const uint16_t *s1 = fc1_scales + (int64_t)e * I2 * fc1_nb;
+        const uint16_t *z1 = fc1_zp ? fc1_zp + (int64_t)e * I2 * fc1_nb : NULL;
+        const uint8_t *w2 = fc2_w + (int64_t)e * H * fc2_row_bytes;
+        const uint16_t *s2 = fc2_scales + (int64_t)e * H * fc2_nb;
+        const uint16_t *z2 = fc2_zp ? fc2_zp + (int64_t)e * H * fc2_nb : NULL;
+
+        for (int64_t c = 0; c < H; ++c)
+            h[c] = (float)oracle_half_to_double(x_f16[c]); /* x, exactly, as the quantizer's input */
+        oracle_quantize_i8_blocks(h, H, bs, q8, sx);
+        for (int64_t r = 0; r < I2; ++r) {
+            double acc = dp4a_row(q8, sx, w1, s1, z1, H, bits, bs, r);
+            if (fc1_bias) acc += oracle_half_to_double(fc1_bias[(int64_t)e * I2 + r]);
+            g[r] = acc;
+        }
+        for (int64_t i = 0; i < I; ++i) {
+            double gate = swiglu_interleaved ? g[2 * i] : g[i];
+            double up = swiglu_interleaved ? g[2 * i + 1] : g[I + i];
+            h[i] = (float)(silu(gate) * up);
+        }
+        oracle_quantize_i8_blocks(h, I, bs, q8, sx);
+        for (int64_t r = 0; r < H; ++r) {
+            double acc = dp4a_row(q8, sx, w2, s2, z2, I, bits, bs, r);
+            if (fc2_bias) acc += oracle_half_to_double(fc2_bias[(int64_t)e * H + r]);
+            y[r] += (double)weights[j] * acc;
+        }
+    }
+    return bad;
+}

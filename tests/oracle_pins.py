@@ -20,6 +20,12 @@ What pins what:
                                 SwiGLU and weighted sum); one-hot slot weights;
   * E4M3 decoding            -- torch's float8_e4m3fn conversion on all 256
                                 bit patterns;
+  * int8 activations (dp4a)  -- hand-worked quantizer fixture (exact steps,
+                                ties to even, zero block); bound, range and
+                                oddness properties on random blocks; the fused
+                                int8 decode vs the chain quantizer -> oracle
+                                fp64 GEMM on q8*sx -> numpy bias / SwiGLU /
+                                weighted sum;
   * embedding gather         -- hand-worked fixture (u4 with and without zero
                                 points, E4M3); numpy row selection of the
                                 dequantized table; torch's float8 decode times
@@ -446,9 +452,88 @@ def check_gather_rows(lib):
     _exact(out[2], table[0])
 
 
+# ---------------------------------------------------------------------------
+def check_golden_i8_quant(lib):
+    g = _golden("i8_quant_handworked.json")
+    q8, sx = O.quantize_i8_blocks(np.array(g["v"], dtype=np.float32), g["block_size"], lib=lib)
+    assert q8.tolist() == g["q8"], q8.tolist()
+    assert sx.tolist() == g["sx"], sx.tolist()
+
+
+def check_i8_quant_properties(lib):
+    """Random blocks over a wide range of magnitudes: |q| <= 127, the block's
+    largest magnitude maps to +-127, the rounding error is at most half a step,
+    and the quantizer is odd (q(-v) = -q(v))."""
+    rng = np.random.default_rng(21)
+    bs = 32
+    mags = np.repeat(10.0 ** rng.uniform(-30, 30, size=64), bs)
+    v = (rng.standard_normal(64 * bs) * mags).astype(np.float32)
+    v[5 * bs:6 * bs] = 0.0
+    q8, sx = O.quantize_i8_blocks(v, bs, lib=lib)
+    qn, sxn = O.quantize_i8_blocks(-v, bs, lib=lib)
+    assert np.array_equal(qn, -q8) and np.array_equal(sxn, sx)
+    assert np.abs(q8.astype(np.int64)).max() <= 127
+    for b in range(64):
+        blk = slice(b * bs, (b + 1) * bs)
+        vb, qb = v[blk].astype(np.float64), q8[blk].astype(np.float64)
+        if not np.any(vb):
+            assert sx[b] == 0 and not np.any(qb)
+            continue
+        i = int(np.argmax(np.abs(vb)))
+        assert abs(qb[i]) == 127 and np.sign(qb[i]) == np.sign(vb[i])
+        assert np.all(np.abs(qb * float(sx[b]) - vb) <= 0.5001 * float(sx[b]))
+
+
+def _dp4a_chain(lib, d, x, ids, w, interleaved):
+    """The int8-activation decode as a chain of pinned pieces: the quantizer,
+    the oracle's fp64 GEMM on the dequantized activations q8 * sx (exact in
+    fp64), numpy for bias, SwiGLU (rounded to fp32, as the quantizer's input)
+    and the weighted sum."""
+    H, I, bs = d["hidden"], d["inter"], d["block_size"]
+
+    def deq(v):
+        q8, sx = O.quantize_i8_blocks(v, bs, lib=lib)
+        return q8.astype(np.float64) * np.repeat(sx.astype(np.float64), bs)
+
+    y = np.zeros(H)
+    xa = deq(_h2f(x).astype(np.float32))
+    for j, e in enumerate(ids):
+        z1 = None if d["fc1_zp"] is None else d["fc1_zp"][e]
+        z2 = None if d["fc2_zp"] is None else d["fc2_zp"][e]
+        gvec = O.qgemm_nbits(xa.reshape(1, H), d["fc1_w"][e], d["fc1_scales"][e], z1, M=1, N=2 * I, K=H, bits=4,
+                             block_size=bs, a_dtype=O.F64, lib=lib)[0]
+        if d["fc1_bias"] is not None:
+            gvec = gvec + _h2f(d["fc1_bias"][e])
+        gate, up = (gvec[0::2], gvec[1::2]) if interleaved else (gvec[:I], gvec[I:])
+        h = (gate / (1.0 + np.exp(-gate)) * up).astype(np.float32)
+        o = O.qgemm_nbits(deq(h).reshape(1, I), d["fc2_w"][e], d["fc2_scales"][e], z2, M=1, N=H, K=I, bits=4,
+                          block_size=bs, a_dtype=O.F64, lib=lib)[0]
+        if d["fc2_bias"] is not None:
+            o = o + _h2f(d["fc2_bias"][e])
+        y = y + float(w[j]) * o
+    return y
+
+
+def check_qmoe_dp4a_chain(lib):
+    for seed, zp, bias in ((1, True, True), (2, False, True), (3, True, False)):
+        d, x, ids, w = _qmoe_case(seed, with_zp=zp, with_bias=bias)
+        for inter_flag in (0, 1):
+            y, bad = O.qmoe_decode_dp4a(x, ids, w, swiglu_interleaved=inter_flag, lib=lib, **d)
+            assert bad == 0
+            np.testing.assert_allclose(y, _dp4a_chain(lib, d, x, ids, w, inter_flag), rtol=1e-10, atol=1e-12)
+    d, x, ids, w = _qmoe_case(5)
+    bad_ids = ids.copy()
+    bad_ids[1] = d["num_experts"]
+    y, bad = O.qmoe_decode_dp4a(x, bad_ids, w, lib=lib, **d)
+    assert bad == 1
+    keep = np.array([0, 2])
+    np.testing.assert_allclose(y, _dp4a_chain(lib, d, x, ids[keep], w[keep], 0), rtol=1e-10, atol=1e-12)
+
+
 ALL_CHECKS = [
     check_half_decode, check_bf16_decode, check_unpack_vs_unpackbits, check_golden_u2, check_golden_u3, check_golden_u4, check_golden_u8,
     check_golden_codebook, check_golden_qmoe, check_onehot, check_uniform_vs_tensor, check_closed_form,
     check_integer_codebook, check_library_matmul, check_rows_subset, check_qmoe_chain, check_uniform_detection,
     check_e4m3_decode, check_golden_gather, check_gather_rows,
+    check_golden_i8_quant, check_i8_quant_properties, check_qmoe_dp4a_chain,
 ]

@@ -1,7 +1,7 @@
 """Planted mistakes in the oracle must be caught by its pins (CPU only).
 
 Each case copies the oracle's C source, plants one plausible mistake by a
-textual substitution, compiles the copy into a temporary library and runs
+textual substitution (at every place the anchor text occurs), compiles the copy into a temporary library and runs
 every pin check against it.  At least one pin must fail for every mutant;
 the unmodified source must pass them all (tests/test_oracle_pins.py).
 """
@@ -54,6 +54,12 @@ MUTANTS = {
     "gather_bad_index_not_counted": ("++bad;\n            for (int64_t d = 0; d < D; ++d)",
                                      "for (int64_t d = 0; d < D; ++d)"),
     "gather_scale_by_position": ("scales[row * nb + d / bs]", "scales[i * nb + d / bs]"),
+    "i8_truncates": ("float r = rintf(v[k] / s);", "float r = truncf(v[k] / s);"),
+    "i8_rounds_half_up": ("float r = rintf(v[k] / s);", "float r = floorf(v[k] / s + 0.5f);"),
+    "i8_scale_128": ("float s = a / 127.0f;", "float s = a / 128.0f;"),
+    "dp4a_zero_point_sum_dropped": ("((double)dot - z * (double)sum)", "((double)dot)"),
+    "dp4a_first_block_scale": ("acc += s * (double)sx[b] *", "acc += s * (double)sx[0] *"),
+    "dp4a_h_not_requantized": ("oracle_quantize_i8_blocks(h, I, bs, q8, sx);", ""),
 }
 
 
@@ -61,7 +67,9 @@ MUTANTS = {
 def test_planted_mistake_is_caught(name, tmp_path):
     old, new = MUTANTS[name]
     src = open(SRC).read()
-    assert src.count(old) == 1, "mutation anchor not found exactly once: %s" % name
+    # the same mistake is planted at every occurrence (the fp and int8 QMoE
+    # decodes share their slot loop's text)
+    assert src.count(old) >= 1, "mutation anchor not found: %s" % name
     msrc = tmp_path / "mutant.c"
     msrc.write_text(src.replace(old, new))
     lib = oracle.load(oracle.build(force=True, src=str(msrc), out=str(tmp_path / "libmutant.so")))
