@@ -399,7 +399,8 @@ def run_suite(only=None):
     8-bit codes on two of those shapes;
     the NF4 codebook shapes at M=1, 4, 16, 64 (bf16 activations); the QMoE
     decode (128 experts, top-8, 2880/2880, u4 block 32) with and without zero
-    points; the two M=2048 prefill GEMMs; the block-quantized embedding gather
+    points, with fp16 and with int8 activations; the two M=2048 prefill GEMMs;
+    the block-quantized embedding gather
     (u4, u8, E4M3 tables).  Each figure is the mean over a CUDA
     graph of R back-to-back calls whose weights rotate over copies (or expert
     sets) totalling more than three times the L2, so every call reads cold
@@ -539,6 +540,9 @@ def run_suite(only=None):
             us = timed(lambda i: qg.qmoe_decode_fused(x, sets[i % len(sets)], wts, y=y, workspace=ws, stream=st, **kw),
                        len(sets))
             emit("qmoe_top8_2880_u4_bs32_%s" % ("zp" if with_zp else "nozp"), us, nbytes=k * per_expert)
+            us = timed(lambda i: qg.qmoe_decode_fused_dp4a(x, sets[i % len(sets)], wts, y=y, workspace=ws, stream=st,
+                                                           **kw), len(sets))
+            emit("qmoe_dp4a_top8_2880_u4_bs32_%s" % ("zp" if with_zp else "nozp"), us, nbytes=k * per_expert)
             del kw
 
     # prefill u2, M = 2048, fp16 activations, fp32 out
@@ -585,6 +589,7 @@ def run_probe(name):
     tc_prefill   4 calls of a prefill-sized u2 GEMM on the tensor cores
                  (M=2048, N=K=5120, fp16 activations, fp32 out)
     qmoe         4 calls of the 128-expert top-8 2880/2880 block-32 QMoE decode
+    qmoe_dp4a    the same with int8 activations
     gather       4 calls of the u4 embedding gather (100352 x 5120 table, block 32,
                  2048 token ids, fp16 out)
     """
@@ -620,7 +625,7 @@ def run_probe(name):
         c = nbits(WL.prefill_u2((5120, 5120), M=2048))
         for _ in range(4):
             c()
-    elif name == "qmoe":
+    elif name in ("qmoe", "qmoe_dp4a"):
         d = WL.qmoe()
         h = lambda a: None if a is None else torch.from_numpy(a.view(np.int16)).cuda().view(torch.float16)
         y = torch.empty(d["hidden"], dtype=torch.float16, device="cuda")
@@ -629,7 +634,7 @@ def run_probe(name):
                   fc2_scales=h(d["fc2_scales"]), fc2_zp=None, fc2_bias=h(d["fc2_bias"]), bits=4, block_size=32, y=y)
         x, ids, w = h(d["x"]), torch.from_numpy(d["ids"]).cuda(), torch.from_numpy(d["weights"]).cuda()
         for _ in range(4):
-            qg.qmoe_decode_fused(x, ids, w, **kw)
+            (qg.qmoe_decode_fused_dp4a if name == "qmoe_dp4a" else qg.qmoe_decode_fused)(x, ids, w, **kw)
     elif name == "gather":
         d = WL.embedding(1)
         W = torch.from_numpy(d["W"]).cuda()
@@ -653,7 +658,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--probe", choices=["gemv_k5120", "gemv_lm_head", "tc_prefill", "qmoe", "gather"],
+    ap.add_argument("--probe", choices=["gemv_k5120", "gemv_lm_head", "tc_prefill", "qmoe", "qmoe_dp4a", "gather"],
                     help="run a small fixed workload for a profiler capture instead of the benchmark")
     ap.add_argument("--suite", action="store_true",
                     help="time every configuration (one JSON line each) instead of the benchmark")

@@ -20,7 +20,7 @@ __all__ = [
     "QG_OK", "QG_ERR_INVALID_ARG", "QG_ERR_UNSUPPORTED", "QG_ERR_CUDA", "QG_ERR_WORKSPACE_TOO_SMALL",
     "QG_F32", "QG_F16", "QG_BF16", "QGError", "QGLibraryMissing", "lib", "library_path",
     "qgemm_nbits", "qgemm_nbits_uniform_zp", "qgemm_codebook4", "qgemm_workspace_bytes",
-    "qmoe_decode_fused", "qmoe_decode_fused_noalloc", "qmoe_decode_workspace_bytes", "QG_QMOE_NOALLOC_SCRATCH_BYTES",
+    "qmoe_decode_fused", "qmoe_decode_fused_dp4a", "qmoe_decode_fused_noalloc", "qmoe_decode_workspace_bytes", "QG_QMOE_NOALLOC_SCRATCH_BYTES",
     "qg_fp16_uniform_value", "qg_dequant_nbits",
     "qg_dequant_nbits_uniform_zp", "qg_dequant_codebook4", "qg_read_device_fault", "qg_status_string",
     "qg_gather_block_quantized", "QG_WF_U2", "QG_WF_U4", "QG_WF_U8", "QG_WF_E4M3",
@@ -60,6 +60,8 @@ _SIGS = {
     "qgemm_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _SZ),
     "qmoe_decode_fused": ([_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ,
                            _P], _I),
+    "qmoe_decode_fused_dp4a": ([_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P,
+                                _SZ, _P], _I),
     "qmoe_decode_workspace_bytes": ([_I, _I, _I], _SZ),
     "qmoe_decode_fused_noalloc": ([_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
                                    _P], _I),
@@ -183,6 +185,21 @@ def qmoe_decode_fused(x, expert_ids, expert_weights, *, num_experts, fc1_w, fc1_
                                 _ptr(fc2_zp), _ptr(fc2_bias), hidden, inter, bits, block_size,
                                 int(swiglu_interleaved), _ptr(y), _ptr(status), _ptr(ws), wsb, _stream(stream))
     return s if raw else _check(s, "qmoe_decode_fused")
+
+
+def qmoe_decode_fused_dp4a(x, expert_ids, expert_weights, *, num_experts, fc1_w, fc1_scales, fc1_zp, fc1_bias,
+                           fc2_w, fc2_scales, fc2_zp, fc2_bias, bits, block_size, y, swiglu_interleaved=0,
+                           status=None, workspace=None, stream=None, raw=False):
+    """qmoe_decode_fused with int8 activations (per-block symmetric quantization, dp4a dot products)."""
+    hidden = x.shape[-1]
+    inter = fc2_w.shape[-1] * 8 // bits
+    k = expert_ids.numel()
+    ws, wsb = _workspace(qmoe_decode_workspace_bytes(k, hidden, inter), workspace, x.device)
+    s = lib().qmoe_decode_fused_dp4a(_ptr(x), _ptr(expert_ids), _ptr(expert_weights), k, num_experts, _ptr(fc1_w),
+                                     _ptr(fc1_scales), _ptr(fc1_zp), _ptr(fc1_bias), _ptr(fc2_w), _ptr(fc2_scales),
+                                     _ptr(fc2_zp), _ptr(fc2_bias), hidden, inter, bits, block_size,
+                                     int(swiglu_interleaved), _ptr(y), _ptr(status), _ptr(ws), wsb, _stream(stream))
+    return s if raw else _check(s, "qmoe_decode_fused_dp4a")
 
 
 def qmoe_decode_fused_noalloc(x, expert_ids, expert_weights, *, num_experts, fc1_w, fc1_scales, fc1_zp, fc1_bias,

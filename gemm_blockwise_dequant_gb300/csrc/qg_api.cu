@@ -144,6 +144,67 @@ int nbits_common(const void *A, int a_dtype, const uint8_t *W, const uint16_t *s
     return run_gemm(p, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int qmoe_common(bool dp4a, const uint16_t *x_f16, const int32_t *expert_ids, const float *expert_weights, int k,
+                int num_experts, const uint8_t *fc1_w, const uint16_t *fc1_scales, const uint16_t *fc1_zp,
+                const uint16_t *fc1_bias, const uint8_t *fc2_w, const uint16_t *fc2_scales, const uint16_t *fc2_zp,
+                const uint16_t *fc2_bias, int hidden, int inter, int bits, int block_size, int swiglu_interleaved,
+                uint16_t *y_f16, int *status_dev, void *workspace, size_t workspace_bytes, qg_stream_t stream) {
+    (void)cudaGetLastError();  // do not report an earlier, unrelated failure as ours
+    if (k < 0 || num_experts < 0 || hidden <= 0 || inter <= 0) return QG_ERR_INVALID_ARG;
+    if (swiglu_interleaved != 0 && swiglu_interleaved != 1) return QG_ERR_INVALID_ARG;
+    if (bits != 2 && bits != 4) return QG_ERR_UNSUPPORTED;
+    if (!valid_bs(block_size)) return QG_ERR_UNSUPPORTED;
+    if (hidden % block_size || inter % block_size) return QG_ERR_INVALID_ARG;
+    if (hidden > kMaxK || inter > kMaxK / 2 || k > 4096) return QG_ERR_UNSUPPORTED;
+    if (dp4a && (hidden > 65536 || inter > 65536)) return QG_ERR_UNSUPPORTED;  // quantized vector in shared memory
+    if (!x_f16 || !y_f16) return QG_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (k == 0) {
+        if (cudaMemsetAsync(y_f16, 0, static_cast<size_t>(hidden) * 2, s) != cudaSuccess) return QG_ERR_CUDA;
+        if (status_dev && cudaMemsetAsync(status_dev, 0, sizeof(int), s) != cudaSuccess) return QG_ERR_CUDA;
+        return QG_OK;
+    }
+    if (num_experts < 1 || !expert_ids || !expert_weights || !fc1_w || !fc1_scales || !fc2_w || !fc2_scales)
+        return QG_ERR_INVALID_ARG;
+    const void *al16[] = {fc1_w, fc1_scales, fc2_w, fc2_scales};
+    for (const void *q : al16)
+        if (!aligned16(q)) return QG_ERR_INVALID_ARG;
+    if ((fc1_zp && !aligned16(fc1_zp)) || (fc2_zp && !aligned16(fc2_zp))) return QG_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(expert_ids) | reinterpret_cast<uintptr_t>(expert_weights)) & 3u)
+        return QG_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x_f16) | reinterpret_cast<uintptr_t>(y_f16) |
+         reinterpret_cast<uintptr_t>(fc1_bias) | reinterpret_cast<uintptr_t>(fc2_bias)) & 1u)
+        return QG_ERR_INVALID_ARG;
+    if (status_dev && (reinterpret_cast<uintptr_t>(status_dev) & 3u)) return QG_ERR_INVALID_ARG;
+    const size_t need = qg::qmoe_workspace_bytes(k, hidden, inter);
+    if (!workspace || workspace_bytes < need) return QG_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(workspace)) return QG_ERR_INVALID_ARG;
+    qg::QmoeProblem q{};
+    q.x = x_f16;
+    q.ids = expert_ids;
+    q.weights = expert_weights;
+    q.k = k;
+    q.num_experts = num_experts;
+    q.fc1_w = fc1_w;
+    q.fc1_scales = fc1_scales;
+    q.fc1_zp = fc1_zp;
+    q.fc1_bias = fc1_bias;
+    q.fc2_w = fc2_w;
+    q.fc2_scales = fc2_scales;
+    q.fc2_zp = fc2_zp;
+    q.fc2_bias = fc2_bias;
+    q.hidden = hidden;
+    q.inter = inter;
+    q.bits = bits;
+    q.bs = block_size;
+    q.swiglu_interleaved = swiglu_interleaved;
+    q.y = y_f16;
+    q.status = status_dev;
+    const cudaError_t e = dp4a ? qg::qmoe_decode_dp4a(q, workspace, s) : qg::qmoe_decode(q, workspace, s);
+    if (e == cudaErrorNotSupported) return QG_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -202,59 +263,20 @@ int qmoe_decode_fused(const uint16_t *x_f16, const int32_t *expert_ids, const fl
                       const uint16_t *fc2_zp, const uint16_t *fc2_bias, int hidden, int inter, int bits,
                       int block_size, int swiglu_interleaved, uint16_t *y_f16, int *status_dev, void *workspace,
                       size_t workspace_bytes, qg_stream_t stream) {
-    (void)cudaGetLastError();  // do not report an earlier, unrelated failure as ours
-    if (k < 0 || num_experts < 0 || hidden <= 0 || inter <= 0) return QG_ERR_INVALID_ARG;
-    if (swiglu_interleaved != 0 && swiglu_interleaved != 1) return QG_ERR_INVALID_ARG;
-    if (bits != 2 && bits != 4) return QG_ERR_UNSUPPORTED;
-    if (!valid_bs(block_size)) return QG_ERR_UNSUPPORTED;
-    if (hidden % block_size || inter % block_size) return QG_ERR_INVALID_ARG;
-    if (hidden > kMaxK || inter > kMaxK / 2 || k > 4096) return QG_ERR_UNSUPPORTED;
-    if (!x_f16 || !y_f16) return QG_ERR_INVALID_ARG;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (k == 0) {
-        if (cudaMemsetAsync(y_f16, 0, static_cast<size_t>(hidden) * 2, s) != cudaSuccess) return QG_ERR_CUDA;
-        if (status_dev && cudaMemsetAsync(status_dev, 0, sizeof(int), s) != cudaSuccess) return QG_ERR_CUDA;
-        return QG_OK;
-    }
-    if (num_experts < 1 || !expert_ids || !expert_weights || !fc1_w || !fc1_scales || !fc2_w || !fc2_scales)
-        return QG_ERR_INVALID_ARG;
-    const void *al16[] = {fc1_w, fc1_scales, fc2_w, fc2_scales};
-    for (const void *q : al16)
-        if (!aligned16(q)) return QG_ERR_INVALID_ARG;
-    if ((fc1_zp && !aligned16(fc1_zp)) || (fc2_zp && !aligned16(fc2_zp))) return QG_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(expert_ids) | reinterpret_cast<uintptr_t>(expert_weights)) & 3u)
-        return QG_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(x_f16) | reinterpret_cast<uintptr_t>(y_f16) |
-         reinterpret_cast<uintptr_t>(fc1_bias) | reinterpret_cast<uintptr_t>(fc2_bias)) & 1u)
-        return QG_ERR_INVALID_ARG;
-    if (status_dev && (reinterpret_cast<uintptr_t>(status_dev) & 3u)) return QG_ERR_INVALID_ARG;
-    const size_t need = qg::qmoe_workspace_bytes(k, hidden, inter);
-    if (!workspace || workspace_bytes < need) return QG_ERR_WORKSPACE_TOO_SMALL;
-    if (!aligned16(workspace)) return QG_ERR_INVALID_ARG;
-    qg::QmoeProblem q{};
-    q.x = x_f16;
-    q.ids = expert_ids;
-    q.weights = expert_weights;
-    q.k = k;
-    q.num_experts = num_experts;
-    q.fc1_w = fc1_w;
-    q.fc1_scales = fc1_scales;
-    q.fc1_zp = fc1_zp;
-    q.fc1_bias = fc1_bias;
-    q.fc2_w = fc2_w;
-    q.fc2_scales = fc2_scales;
-    q.fc2_zp = fc2_zp;
-    q.fc2_bias = fc2_bias;
-    q.hidden = hidden;
-    q.inter = inter;
-    q.bits = bits;
-    q.bs = block_size;
-    q.swiglu_interleaved = swiglu_interleaved;
-    q.y = y_f16;
-    q.status = status_dev;
-    const cudaError_t e = qg::qmoe_decode(q, workspace, s);
-    if (e == cudaErrorNotSupported) return QG_ERR_UNSUPPORTED;
-    return e == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+    return qmoe_common(false, x_f16, expert_ids, expert_weights, k, num_experts, fc1_w, fc1_scales, fc1_zp, fc1_bias,
+                       fc2_w, fc2_scales, fc2_zp, fc2_bias, hidden, inter, bits, block_size, swiglu_interleaved, y_f16,
+                       status_dev, workspace, workspace_bytes, stream);
+}
+
+int qmoe_decode_fused_dp4a(const uint16_t *x_f16, const int32_t *expert_ids, const float *expert_weights, int k,
+                           int num_experts, const uint8_t *fc1_w, const uint16_t *fc1_scales, const uint16_t *fc1_zp,
+                           const uint16_t *fc1_bias, const uint8_t *fc2_w, const uint16_t *fc2_scales,
+                           const uint16_t *fc2_zp, const uint16_t *fc2_bias, int hidden, int inter, int bits,
+                           int block_size, int swiglu_interleaved, uint16_t *y_f16, int *status_dev, void *workspace,
+                           size_t workspace_bytes, qg_stream_t stream) {
+    return qmoe_common(true, x_f16, expert_ids, expert_weights, k, num_experts, fc1_w, fc1_scales, fc1_zp, fc1_bias,
+                       fc2_w, fc2_scales, fc2_zp, fc2_bias, hidden, inter, bits, block_size, swiglu_interleaved, y_f16,
+                       status_dev, workspace, workspace_bytes, stream);
 }
 
 size_t qmoe_decode_workspace_bytes(int k, int hidden, int inter) {

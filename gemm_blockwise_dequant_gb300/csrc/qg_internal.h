@@ -84,6 +84,8 @@ struct QmoeProblem {
 };
 size_t qmoe_workspace_bytes(int k, int hidden, int inter);
 cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s);
+// Same decode with int8 activations (dp4a); hidden and inter at most 65536.
+cudaError_t qmoe_decode_dp4a(const QmoeProblem &q, void *ws, cudaStream_t s);
 
 // Block-quantized embedding gather (validated request).
 struct GatherProblem {

@@ -189,6 +189,32 @@ int qmoe_decode_fused(const uint16_t *x_f16, const int32_t *expert_ids, const fl
 size_t qmoe_decode_workspace_bytes(int k, int hidden, int inter);
 
 /*
+ * qmoe_decode_fused_dp4a -- the same decode with int8 activations.
+ * [hip-ep #1328] "Summary" (the fused decode and its dp4a variant), "Test
+ * plan" (fp and dp4a x block size x zero points x bias).  The pages do not
+ * give the activation quantization; this library's reading: each activation
+ * vector (x before fc1, h = silu(gate) * up before fc2) is quantized per block
+ * of block_size values along the contraction,
+ *     a = max |v|,  sx = fl32(a / 127),  q8 = clamp(rint(fl32(v / sx)), -127, 127)
+ * (ties to even; an all-zero block gives sx = 0, q8 = 0), and each output is
+ *     sum_b s[r][b] * sx[b] * ( sum_{k in b} q8[k] * q[r][k] - zp[r][b] * sum_{k in b} q8[k] )
+ * with exact integer sums, plus the bias.  Results therefore differ from
+ * qmoe_decode_fused by the activation quantization error (about 1/254 of each
+ * block's largest magnitude per element).
+ *
+ * Arguments, layouts, statuses and the workspace size are those of
+ * qmoe_decode_fused; in addition hidden and inter must be at most 65536
+ * (QG_ERR_UNSUPPORTED otherwise).  Deterministic: repeated calls are
+ * bit-identical.
+ */
+int qmoe_decode_fused_dp4a(const uint16_t *x_f16, const int32_t *expert_ids, const float *expert_weights, int k,
+                           int num_experts, const uint8_t *fc1_w, const uint16_t *fc1_scales, const uint16_t *fc1_zp,
+                           const uint16_t *fc1_bias, const uint8_t *fc2_w, const uint16_t *fc2_scales,
+                           const uint16_t *fc2_zp, const uint16_t *fc2_bias, int hidden, int inter, int bits,
+                           int block_size, int swiglu_interleaved, uint16_t *y_f16, int *status_dev, void *workspace,
+                           size_t workspace_bytes, qg_stream_t stream);
+
+/*
  * qmoe_decode_fused_noalloc -- qmoe_decode_fused for callers that cannot
  * allocate device memory (a decode loop inside a runtime that forbids
  * allocation on its hot path, an embedded host that must not allocate after

@@ -221,8 +221,9 @@ def quantize_i8_blocks(v, block_size, lib=None):
 
 def qmoe_decode_dp4a(x_f16, ids, weights, *, num_experts, fc1_w, fc1_scales, fc1_zp, fc1_bias, fc2_w,
                      fc2_scales, fc2_zp, fc2_bias, hidden, inter, bits, block_size, swiglu_interleaved=0,
-                     lib=None):
-    """The int8-activation decode: unrounded fp64 y[hidden] and the number of out-of-range slots."""
+                     lib=None, return_g=False):
+    """The int8-activation decode: unrounded fp64 y[hidden] and the number of out-of-range slots
+    (and, with return_g, the fc1 output g[2*inter] of the last valid slot)."""
     x_f16 = _c(x_f16, np.uint16)
     ids = _c(ids, np.int32)
     weights = _c(weights, np.float32)
@@ -240,7 +241,7 @@ def qmoe_decode_dp4a(x_f16, ids, weights, *, num_experts, fc1_w, fc1_scales, fc1
         _ptr(x_f16), _ptr(ids), _ptr(weights), ids.size, num_experts, _ptr(fc1_w), _ptr(fc1_scales),
         _ptr(fc1_zp), _ptr(fc1_bias), _ptr(fc2_w), _ptr(fc2_scales), _ptr(fc2_zp), _ptr(fc2_bias),
         hidden, inter, bits, block_size, int(swiglu_interleaved), _ptr(g), _ptr(h), _ptr(q8), _ptr(sx), _ptr(y))
-    return y, bad
+    return (y, bad, g) if return_g else (y, bad)
 
 
 def e4m3_to_double(bits: int, lib=None) -> float:

@@ -184,19 +184,20 @@ def nf4(shape: str, M: int, a_dtype: int, seed: int = 0) -> dict:
 
 
 def qmoe(num_experts: int = 128, k: int = 8, hidden: int = 2880, inter: int = 2880, block_size: int = 32,
-         with_zp: bool = False, with_bias: bool = True, seed: int = 0) -> dict:
-    """One-token QMoE decode: fc1 [E][2I][H] and fc2 [E][H][I] u4 codes, fp16
-    scales U(0.005, 0.02), optional fp16 zero points (integers in [0, 15]),
+         with_zp: bool = False, with_bias: bool = True, seed: int = 0, bits: int = 4) -> dict:
+    """One-token QMoE decode: fc1 [E][2I][H] and fc2 [E][H][I] codes (u4 unless
+    bits says otherwise), fp16 scales U(0.005, 0.02), optional fp16 zero points
+    (integers in [0, 2^bits - 1]),
     fp16 bias ~ N(0, 0.01), fp16 x ~ N(0, 1); k distinct expert ids and
     softmax weights over k N(0, 1) logits (fp64 softmax rounded to fp32)."""
     g = rng(seed)
-    E, H, I, bits, bs = num_experts, hidden, inter, 4, block_size
+    E, H, I, bs = num_experts, hidden, inter, block_size
     fc1_w = packed_codes(g, E * 2 * I, H, bits).reshape(E, 2 * I, H * bits // 8)
     fc2_w = packed_codes(g, E * H, I, bits).reshape(E, H, I * bits // 8)
     fc1_scales = fp16_uniform(g, (E, 2 * I, H // bs), 0.005, 0.02)
     fc2_scales = fp16_uniform(g, (E, H, I // bs), 0.005, 0.02)
-    fc1_zp = fp16_uniform_int(g, (E, 2 * I, H // bs), 0, 15) if with_zp else None
-    fc2_zp = fp16_uniform_int(g, (E, H, I // bs), 0, 15) if with_zp else None
+    fc1_zp = fp16_uniform_int(g, (E, 2 * I, H // bs), 0, (1 << bits) - 1) if with_zp else None
+    fc2_zp = fp16_uniform_int(g, (E, H, I // bs), 0, (1 << bits) - 1) if with_zp else None
     fc1_bias = fp16_normal(g, (E, 2 * I), 0.01) if with_bias else None
     fc2_bias = fp16_normal(g, (E, H), 0.01) if with_bias else None
     x = fp16_normal(g, (H,), 1.0)
