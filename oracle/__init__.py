@@ -83,6 +83,8 @@ def load(path: str | None = None):
         lib.oracle_qmoe_decode_dp4a.argtypes = [P, P, P, I, I, P, P, P, P, P, P, P, P, I64, I64, I, I, I, P, P, P,
                                                 P, P]
         lib.oracle_qmoe_decode_dp4a.restype = I
+        lib.oracle_qmoe_ragged_mm.argtypes = [P, I, P, I, P, P, P, I64, I64, I, I, P]
+        lib.oracle_qmoe_ragged_mm.restype = I
         if path is None:
             _lib = lib
         return lib
@@ -242,6 +244,31 @@ def qmoe_decode_dp4a(x_f16, ids, weights, *, num_experts, fc1_w, fc1_scales, fc1
         _ptr(fc1_zp), _ptr(fc1_bias), _ptr(fc2_w), _ptr(fc2_scales), _ptr(fc2_zp), _ptr(fc2_bias),
         hidden, inter, bits, block_size, int(swiglu_interleaved), _ptr(g), _ptr(h), _ptr(q8), _ptr(sx), _ptr(y))
     return (y, bad, g) if return_g else (y, bad)
+
+
+def qmoe_ragged_mm(X, offsets, W, scales, zero_points=None, *, N, K, bits, block_size, x_dtype=None, lib=None):
+    """Ragged expert GEMM: rows offsets[e] .. offsets[e+1]-1 of X use expert e's weight.
+
+    X: [T, K] float32 / float64, or uint16 fp16 / bf16 bit patterns with x_dtype;
+    W: [E, N, K*bits/8]; scales / zero_points: [E, N, K/block_size] fp16 bits.
+    Returns fp64 Y [T, N] (unrounded).  Raises ValueError for offsets that do not
+    start at 0 or decrease.
+    """
+    lib = lib or load()
+    X = np.ascontiguousarray(X)
+    if x_dtype is None:
+        x_dtype = _a_dtype(X)
+    off = _c(np.asarray(offsets, dtype=np.int64), np.int64)
+    E = off.size - 1
+    W = _c(W, np.uint8)
+    scales = _c(scales, np.uint16)
+    zero_points = _c(zero_points, np.uint16)
+    T = int(off[-1])
+    Y = np.zeros((T, N), dtype=np.float64)
+    if lib.oracle_qmoe_ragged_mm(_ptr(X), x_dtype, _ptr(off), E, _ptr(W), _ptr(scales), _ptr(zero_points), N, K,
+                                 bits, block_size, _ptr(Y)) != 0:
+        raise ValueError("offsets must start at 0 and not decrease")
+    return Y
 
 
 def e4m3_to_double(bits: int, lib=None) -> float:

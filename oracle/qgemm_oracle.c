@@ -494,3 +494,40 @@ int oracle_qmoe_decode_dp4a(const uint16_t *x_f16, const int32_t *ids, const flo
     }
     return bad;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Ragged expert GEMM ([P1] Notes for reviewers, kernel test table:          */
+/* qmoe_ragged_mm leaf Xfp16_Wu4_Yfp16; [P2] Summary: the QMoE op family).   */
+/* Reading: the rows of X are grouped by expert, expert e owning rows        */
+/* [off[e], off[e+1]); each row is multiplied by its expert's dequantized    */
+/* MatMulNBits weight:  Y[r][n] = sum_k X[r][k] * w_e(n, k)  (fp64, ascending */
+/* k, unrounded).  W is [E][N][K*bits/8], scales / zero points [E][N][K/bs]. */
+/* Returns 0, or -1 (nothing written) when off[0] != 0 or the offsets        */
+/* decrease.                                                                 */
+/* ------------------------------------------------------------------------ */
+int oracle_qmoe_ragged_mm(const void *X, int x_dtype, const int64_t *off, int E, const uint8_t *W,
+                          const uint16_t *scales, const uint16_t *zp, int64_t N, int64_t K, int bits, int bs,
+                          double *Y)
+{
+    if (off[0] != 0)
+        return -1;
+    for (int e = 0; e < E; ++e)
+        if (off[e + 1] < off[e])
+            return -1;
+    const int64_t row_bytes = K * bits / 8, nb = K / bs;
+    for (int e = 0; e < E; ++e) {
+        const uint8_t *we = W + (int64_t)e * N * row_bytes;
+        const uint16_t *se = scales + (int64_t)e * N * nb;
+        const uint16_t *ze = zp ? zp + (int64_t)e * N * nb : NULL;
+        for (int64_t r = off[e]; r < off[e + 1]; ++r)
+            for (int64_t n = 0; n < N; ++n) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k)
+                    acc += load_elem(X, x_dtype, (size_t)(r * K + k)) *
+                           (double)oracle_weight_nbits(we, se, ze, ze ? OR_ZP_TENSOR : OR_ZP_NONE, 0.0f, N, K,
+                                                       bits, bs, n, k);
+                Y[r * N + n] = acc;
+            }
+    }
+    return 0;
+}

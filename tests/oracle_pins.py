@@ -26,6 +26,9 @@ What pins what:
                                 int8 decode vs the chain quantizer -> oracle
                                 fp64 GEMM on q8*sx -> numpy bias / SwiGLU /
                                 weighted sum;
+  * ragged expert GEMM       -- hand-worked fixture (an expert with no rows);
+                                segment by segment equal to the MatMulNBits
+                                oracle; bad offsets refused;
   * embedding gather         -- hand-worked fixture (u4 with and without zero
                                 points, E4M3); numpy row selection of the
                                 dequantized table; torch's float8 decode times
@@ -530,10 +533,55 @@ def check_qmoe_dp4a_chain(lib):
     np.testing.assert_allclose(y, _dp4a_chain(lib, d, x, ids[keep], w[keep], 0), rtol=1e-10, atol=1e-12)
 
 
+# ---------------------------------------------------------------------------
+def check_golden_ragged(lib):
+    g = _golden("ragged_handworked.json")
+    Y = O.qmoe_ragged_mm(np.array(g["X"], dtype=np.float32), g["offsets"], np.array(g["W"], dtype=np.uint8),
+                         np.array(g["scales_f16"], dtype=np.uint16), None, N=g["N"], K=g["K"], bits=4,
+                         block_size=g["block_size"], lib=lib)
+    assert Y.tolist() == g["Y"], Y.tolist()
+
+
+def check_ragged_vs_per_expert(lib):
+    """The ragged GEMM equals, segment by segment, the (pinned) MatMulNBits
+    oracle applied to the segment's rows with that expert's weight."""
+    rng = np.random.default_rng(31)
+    E, N, K, bs = 6, 20, 96, 32
+    offsets = np.array([0, 3, 3, 4, 11, 11, 15], dtype=np.int64)  # experts 1 and 4 own no rows
+    T = int(offsets[-1])
+    for bits in (2, 4):
+        W = rng.integers(0, 256, size=(E, N, K * bits // 8), dtype=np.uint8)
+        sc = rng.uniform(0.005, 0.05, size=(E, N, K // bs)).astype(np.float16).view(np.uint16)
+        zp = rng.integers(0, 1 << bits, size=(E, N, K // bs)).astype(np.float16).view(np.uint16)
+        X = rng.standard_normal((T, K)).astype(np.float16)
+        for z in (zp, None):
+            Y = O.qmoe_ragged_mm(X.view(np.uint16), offsets, W, sc, z, N=N, K=K, bits=bits, block_size=bs,
+                                 x_dtype=O.F16, lib=lib)
+            for e in range(E):
+                a, b = int(offsets[e]), int(offsets[e + 1])
+                if a == b:
+                    continue
+                ref = O.qgemm_nbits(X[a:b].view(np.uint16), W[e], sc[e], None if z is None else z[e], M=b - a, N=N,
+                                    K=K, bits=bits, block_size=bs, a_dtype=O.F16, lib=lib)
+                assert np.array_equal(Y[a:b], ref), e
+
+
+def check_ragged_bad_offsets(lib):
+    W = np.zeros((2, 2, 16), dtype=np.uint8)
+    sc = np.zeros((2, 2, 1), dtype=np.uint16)
+    for bad in ([1, 2, 3], [0, 3, 2]):
+        try:
+            O.qmoe_ragged_mm(np.zeros((3, 32), np.float32), bad, W, sc, N=2, K=32, bits=4, block_size=32, lib=lib)
+        except ValueError:
+            continue
+        raise AssertionError("offsets %s accepted" % bad)
+
+
 ALL_CHECKS = [
     check_half_decode, check_bf16_decode, check_unpack_vs_unpackbits, check_golden_u2, check_golden_u3, check_golden_u4, check_golden_u8,
     check_golden_codebook, check_golden_qmoe, check_onehot, check_uniform_vs_tensor, check_closed_form,
     check_integer_codebook, check_library_matmul, check_rows_subset, check_qmoe_chain, check_uniform_detection,
     check_e4m3_decode, check_golden_gather, check_gather_rows,
     check_golden_i8_quant, check_i8_quant_properties, check_qmoe_dp4a_chain,
+    check_golden_ragged, check_ragged_vs_per_expert, check_ragged_bad_offsets,
 ]

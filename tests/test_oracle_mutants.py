@@ -60,6 +60,10 @@ MUTANTS = {
     "dp4a_zero_point_sum_dropped": ("((double)dot - z * (double)sum)", "((double)dot)"),
     "dp4a_first_block_scale": ("acc += s * (double)sx[b] *", "acc += s * (double)sx[0] *"),
     "dp4a_h_not_requantized": ("oracle_quantize_i8_blocks(h, I, bs, q8, sx);", ""),
+    "ragged_scales_not_offset": ("const uint16_t *se = scales + (int64_t)e * N * nb;", "const uint16_t *se = scales;"),
+    "ragged_row_within_segment": ("load_elem(X, x_dtype, (size_t)(r * K + k))",
+                                  "load_elem(X, x_dtype, (size_t)((r - off[e]) * K + k))"),
+    "ragged_first_offset_unchecked": ("if (off[0] != 0)\n        return -1;", ""),
 }
 
 
