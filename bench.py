@@ -399,7 +399,8 @@ def run_suite(only=None):
     8-bit codes on two of those shapes;
     the NF4 codebook shapes at M=1, 4, 16, 64 (bf16 activations); the QMoE
     decode (128 experts, top-8, 2880/2880, u4 block 32) with and without zero
-    points, with fp16 and with int8 activations; the two M=2048 prefill GEMMs;
+    points, with fp16 and with int8 activations; the two M=2048 prefill GEMMs; the
+    ragged expert GEMM of a 128-expert top-8 2048/768 layer over a 2048-token prompt;
     the block-quantized embedding gather
     (u4, u8, E4M3 tables).  Each figure is the mean over a CUDA
     graph of R back-to-back calls whose weights rotate over copies (or expert
@@ -556,6 +557,25 @@ def run_suite(only=None):
             emit("prefill_u2_%s_m2048" % shape, us, flops=2.0 * d["M"] * d["N"] * d["K"])
             del A, W, S, Y
 
+    # ragged expert GEMM: fc1 (1536 x 2048 per expert) of the 128-expert top-8 "2048 / 768" MoE layer over a
+    # 2048-token prompt (16384 rows, ~128 per expert), u4 block 32, fp16 in and out; one weight set
+    # (compute-bound)
+    if want("ragged"):
+        d = WL.ragged()
+        X = t16(d["X"], torch.float16)
+        W = torch.from_numpy(d["W"]).to(dev)
+        S = t16(d["scales"], torch.float16)
+        T = int(d["offsets"][-1])
+        Y = torch.empty(T, d["N"], dtype=torch.float16, device=dev)
+        off = d["offsets"]
+        ws = torch.empty(max(16, qg.qmoe_ragged_mm_workspace_bytes(1, off, d["N"], d["K"], 4, 32)), dtype=torch.uint8,
+                         device=dev)
+        us = timed(lambda i: qg.qmoe_ragged_mm(X, off, W, S, None, Y, bits=4, block_size=32, workspace=ws,
+                                               stream=st), 4)
+        emit("ragged_fc1_128x1536x2048_u4_bs32_tokens2048_top8", us, flops=2.0 * T * d["N"] * d["K"],
+             rows=T, experts_min_rows=int(np.diff(off).min()), experts_max_rows=int(np.diff(off).max()))
+        del X, W, S, Y
+
     # block-quantized embedding gather: phi4 table 100352 x 5120, block 32, 2048 token ids, fp16 out.
     # 16 index sets, each drawn from its own sixteenth of the vocabulary, so a row read by one call
     # is not read again for 15 calls (over 3x the L2 of traffic in between).
@@ -590,6 +610,7 @@ def run_probe(name):
                  (M=2048, N=K=5120, fp16 activations, fp32 out)
     qmoe         4 calls of the 128-expert top-8 2880/2880 block-32 QMoE decode
     qmoe_dp4a    the same with int8 activations
+    ragged       4 calls of the ragged expert GEMM (128 experts, 16384 rows, 1536 x 2048 u4 block 32)
     gather       4 calls of the u4 embedding gather (100352 x 5120 table, block 32,
                  2048 token ids, fp16 out)
     """
@@ -635,6 +656,14 @@ def run_probe(name):
         x, ids, w = h(d["x"]), torch.from_numpy(d["ids"]).cuda(), torch.from_numpy(d["weights"]).cuda()
         for _ in range(4):
             (qg.qmoe_decode_fused_dp4a if name == "qmoe_dp4a" else qg.qmoe_decode_fused)(x, ids, w, **kw)
+    elif name == "ragged":
+        d = WL.ragged()
+        X = torch.from_numpy(d["X"].view(np.int16)).cuda().view(torch.float16)
+        W = torch.from_numpy(d["W"]).cuda()
+        S = torch.from_numpy(d["scales"].view(np.int16)).cuda().view(torch.float16)
+        Y = torch.empty(int(d["offsets"][-1]), d["N"], dtype=torch.float16, device="cuda")
+        for _ in range(4):
+            qg.qmoe_ragged_mm(X, d["offsets"], W, S, None, Y, bits=4, block_size=32)
     elif name == "gather":
         d = WL.embedding(1)
         W = torch.from_numpy(d["W"]).cuda()
@@ -658,11 +687,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--probe", choices=["gemv_k5120", "gemv_lm_head", "tc_prefill", "qmoe", "qmoe_dp4a", "gather"],
+    ap.add_argument("--probe", choices=["gemv_k5120", "gemv_lm_head", "tc_prefill", "qmoe", "qmoe_dp4a", "ragged",
+                                        "gather"],
                     help="run a small fixed workload for a profiler capture instead of the benchmark")
     ap.add_argument("--suite", action="store_true",
                     help="time every configuration (one JSON line each) instead of the benchmark")
-    ap.add_argument("--only", choices=["tiny_u4", "phi4_u2", "phi4_u8", "nf4", "qmoe", "prefill", "gather"],
+    ap.add_argument("--only", choices=["tiny_u4", "phi4_u2", "phi4_u8", "nf4", "qmoe", "prefill", "ragged", "gather"],
                     help="with --suite: time one group of configurations only")
     args = ap.parse_args()
     if args.probe:

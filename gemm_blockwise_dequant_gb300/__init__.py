@@ -23,7 +23,7 @@ __all__ = [
     "qmoe_decode_fused", "qmoe_decode_fused_dp4a", "qmoe_decode_fused_noalloc", "qmoe_decode_workspace_bytes", "QG_QMOE_NOALLOC_SCRATCH_BYTES",
     "qg_fp16_uniform_value", "qg_dequant_nbits",
     "qg_dequant_nbits_uniform_zp", "qg_dequant_codebook4", "qg_read_device_fault", "qg_status_string",
-    "qg_gather_block_quantized", "QG_WF_U2", "QG_WF_U4", "QG_WF_U8", "QG_WF_E4M3",
+    "qmoe_ragged_mm", "qmoe_ragged_mm_workspace_bytes", "qg_gather_block_quantized", "QG_WF_U2", "QG_WF_U4", "QG_WF_U8", "QG_WF_E4M3",
 ]
 
 QG_OK, QG_ERR_INVALID_ARG, QG_ERR_UNSUPPORTED, QG_ERR_CUDA, QG_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3, 4
@@ -70,6 +70,8 @@ _SIGS = {
     "qg_dequant_nbits_uniform_zp": ([_P, _P, _F, _P, _I, _I, _I, _I, _P], _I),
     "qg_dequant_codebook4": ([_P, _P, _P, _P, _I, _I, _I, _P], _I),
     "qg_gather_block_quantized": ([_P, ctypes.c_int64, _P, _I, _P, _P, ctypes.c_int64, _I, _I, _P, _I, _P, _P], _I),
+    "qmoe_ragged_mm": ([_P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P], _I),
+    "qmoe_ragged_mm_workspace_bytes": ([_I, _P, _I, _I, _I, _I, _I], _SZ),
     "qg_read_device_fault": ([_P], _I),
     "qg_status_string": ([_I], ctypes.c_char_p),
 }
@@ -248,6 +250,36 @@ def qg_dequant_codebook4(W, codebook, absmax, out, *, block_size, stream=None, r
     s = lib().qg_dequant_codebook4(_ptr(W), _ptr(codebook), _ptr(absmax), _ptr(out), N, K, block_size,
                                    _stream(stream))
     return s if raw else _check(s, "qg_dequant_codebook4")
+
+
+def _host_offsets(offsets):
+    import numpy as np
+
+    off = np.ascontiguousarray(np.asarray(offsets.cpu() if hasattr(offsets, "cpu") else offsets, dtype=np.int64))
+    return off, off.ctypes.data_as(ctypes.c_void_p)
+
+
+def qmoe_ragged_mm_workspace_bytes(x_dtype: int, offsets, N: int, K: int, bits: int, block_size: int) -> int:
+    off, p = _host_offsets(offsets)
+    return lib().qmoe_ragged_mm_workspace_bytes(x_dtype, p, off.size - 1, N, K, bits, block_size)
+
+
+def qmoe_ragged_mm(X, offsets, W, scales, zero_points, Y, *, bits, block_size, workspace=None, stream=None,
+                   raw=False):
+    """Y[r] = X[r] . dequant(W[e])^T for the rows r of expert e (offsets[e] <= r < offsets[e+1]).
+
+    X: [T, K] float32/float16/bfloat16; offsets: host sequence (or CPU tensor) of E+1 ints;
+    W: [E, N, K*bits/8] uint8; scales / zero_points: [E, N, K/block_size] float16 (zero_points None
+    for the midpoint); Y: [T, N] float32/float16/bfloat16.
+    """
+    off, p = _host_offsets(offsets)
+    E, N = W.shape[0], W.shape[1]
+    K = X.shape[1]
+    ws, wsb = _workspace(lib().qmoe_ragged_mm_workspace_bytes(_dtype_code(X), p, E, N, K, bits, block_size),
+                         workspace, X.device)
+    s = lib().qmoe_ragged_mm(_ptr(X), _dtype_code(X), p, E, _ptr(W), _ptr(scales), _ptr(zero_points), _ptr(Y),
+                             _dtype_code(Y), N, K, bits, block_size, _ptr(ws), wsb, _stream(stream))
+    return s if raw else _check(s, "qmoe_ragged_mm")
 
 
 def qg_gather_block_quantized(indices, W, scales, zero_points, Y, *, w_format, block_size, status=None, stream=None,

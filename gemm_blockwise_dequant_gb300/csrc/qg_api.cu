@@ -4,6 +4,7 @@
 // Argument refusal before any launch and clearing the stale CUDA error on
 // entry follow hip-ep #1328 ("What": clear the error state before the fused
 // decode launches; "Test plan": the arguments the launchers must refuse).
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cstring>
@@ -203,6 +204,59 @@ int qmoe_common(bool dp4a, const uint16_t *x_f16, const int32_t *expert_ids, con
     const cudaError_t e = dp4a ? qg::qmoe_decode_dp4a(q, workspace, s) : qg::qmoe_decode(q, workspace, s);
     if (e == cudaErrorNotSupported) return QG_ERR_UNSUPPORTED;
     return e == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+// Ragged expert GEMM: the checks and the plan.  Experts with at least
+// kRaggedTcRows rows run in one grouped tensor-core launch when the shape is
+// eligible; every other expert with rows is one ordinary GEMM call on its
+// slice (SIMT for few rows or fp32 activations).
+constexpr int kRaggedTcRows = 9;
+
+// Offsets, types and sizes; *T_out = total rows.
+int ragged_check_shape(const int64_t *off, int E, int x_dtype, int y_dtype, int N, int K, int bits, int bs,
+                       long long *T_out) {
+    if (!off || E < 1) return QG_ERR_INVALID_ARG;
+    if (off[0] != 0) return QG_ERR_INVALID_ARG;
+    for (int e = 0; e < E; ++e)
+        if (off[e + 1] < off[e]) return QG_ERR_INVALID_ARG;
+    const long long T = off[E];
+    if (!valid_dtype(x_dtype) || !valid_dtype(y_dtype) || N < 0 || K < 0) return QG_ERR_INVALID_ARG;
+    if (bits != 2 && bits != 4 && bits != 8) return QG_ERR_UNSUPPORTED;
+    if (!valid_bs(bs)) return QG_ERR_UNSUPPORTED;
+    if (K % bs) return QG_ERR_INVALID_ARG;
+    if (T > kMaxM || N > kMaxN || K > kMaxK || E > (1 << 20)) return QG_ERR_UNSUPPORTED;
+    // each expert's slice of the stacked tensors must keep 16-byte alignment
+    if ((static_cast<long long>(N) * K * bits / 8) % 16 || (static_cast<long long>(N) * (K / bs) * 2) % 16)
+        return QG_ERR_UNSUPPORTED;
+    *T_out = T;
+    return QG_OK;
+}
+
+int ragged_check(const void *X, int x_dtype, const int64_t *off, int E, const uint8_t *W, const uint16_t *scales,
+                 const uint16_t *zp, const void *Y, int y_dtype, int N, int K, int bits, int bs, long long *T_out) {
+    const int st = ragged_check_shape(off, E, x_dtype, y_dtype, N, K, bits, bs, T_out);
+    if (st != QG_OK || *T_out == 0 || N == 0) return st;
+    if (!Y) return QG_ERR_INVALID_ARG;
+    if (K > 0) {
+        if (!X || !W || !scales) return QG_ERR_INVALID_ARG;
+        if (!aligned16(X) || !aligned16(W) || !aligned16(scales) || (zp && !aligned16(zp))) return QG_ERR_INVALID_ARG;
+    }
+    return QG_OK;
+}
+
+bool ragged_grouped(int x_dtype, int E, int K, int bits, int bs) {
+    return E <= 256 && qg::tc_eligible(kRaggedTcRows, K, bits, x_dtype, bs);
+}
+
+size_t ragged_workspace(int x_dtype, const int64_t *off, int E, int N, int K, int bits, int bs) {
+    const bool grouped = ragged_grouped(x_dtype, E, K, bits, bs);
+    size_t need = 0;
+    for (int e = 0; e < E; ++e) {
+        const long long c = off[e + 1] - off[e];
+        if (c <= 0 || (grouped && c >= kRaggedTcRows)) continue;
+        need = std::max(need, gemm_workspace(x_dtype, static_cast<int>(c), N, K, bits, bs));
+    }
+    return need;
 }
 
 }  // namespace
@@ -418,6 +472,67 @@ int qg_gather_block_quantized(const int64_t *indices, int64_t n_indices, const u
     g.y_dtype = y_dtype;
     g.status = status_dev;
     return qg::launch_gather(g, s) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+size_t qmoe_ragged_mm_workspace_bytes(int x_dtype, const int64_t *expert_offsets, int num_experts, int N, int K,
+                                      int bits, int block_size) {
+    long long T = 0;
+    if (ragged_check_shape(expert_offsets, num_experts, x_dtype, QG_F32, N, K, bits, block_size, &T) != QG_OK)
+        return 0;
+    return ragged_workspace(x_dtype, expert_offsets, num_experts, N, K, bits, block_size);
+}
+
+int qmoe_ragged_mm(const void *X, int x_dtype, const int64_t *expert_offsets, int num_experts, const uint8_t *W,
+                   const uint16_t *scales_f16, const uint16_t *zero_points_f16, void *Y, int y_dtype, int N, int K,
+                   int bits, int block_size, void *workspace, size_t workspace_bytes, qg_stream_t stream) {
+    (void)cudaGetLastError();
+    long long T = 0;
+    int st = ragged_check(X, x_dtype, expert_offsets, num_experts, W, scales_f16, zero_points_f16, Y, y_dtype, N, K,
+                          bits, block_size, &T);
+    if (st != QG_OK || T == 0 || N == 0) return st;
+    const size_t need = ragged_workspace(x_dtype, expert_offsets, num_experts, N, K, bits, block_size);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return QG_ERR_WORKSPACE_TOO_SMALL;
+        if (!aligned16(workspace)) return QG_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    GemmProblem p{};
+    p.A = X;
+    p.a_dtype = x_dtype;
+    p.W = W;
+    p.kind = qg::WK_NBITS;
+    p.scales = scales_f16;
+    p.zp = zero_points_f16;
+    p.zp_mode = zero_points_f16 ? qg::ZP_TENSOR : qg::ZP_NONE;
+    p.uniform_zp = static_cast<float>(1 << (bits - 1));
+    p.Y = Y;
+    p.y_dtype = y_dtype;
+    p.M = static_cast<int>(T);
+    p.N = N;
+    p.K = K;
+    p.bits = bits;
+    p.bs = block_size;
+    const bool grouped = K > 0 && ragged_grouped(x_dtype, num_experts, K, bits, block_size);
+    if (grouped) {
+        const cudaError_t e = qg::tc_gemm_grouped(p, expert_offsets, num_experts, kRaggedTcRows, s);
+        if (e == cudaErrorNotSupported) return QG_ERR_UNSUPPORTED;
+        if (e != cudaSuccess) return QG_ERR_CUDA;
+    }
+    const size_t w_stride = static_cast<size_t>(N) * K * bits / 8, p_stride = static_cast<size_t>(N) * (K / block_size);
+    for (int e = 0; e < num_experts; ++e) {
+        const long long r0 = expert_offsets[e], c = expert_offsets[e + 1] - r0;
+        if (c == 0 || (grouped && c >= kRaggedTcRows)) continue;
+        GemmProblem q = p;
+        q.A = static_cast<const char *>(X) + static_cast<size_t>(r0) * K * elem_size(x_dtype);
+        q.W = W + e * w_stride;
+        q.scales = scales_f16 + e * p_stride;
+        q.zp = zero_points_f16 ? zero_points_f16 + e * p_stride : nullptr;
+        q.Y = static_cast<char *>(Y) + static_cast<size_t>(r0) * N * elem_size(y_dtype);
+        q.M = static_cast<int>(c);
+        st = run_gemm(q, workspace, workspace_bytes, s);
+        if (st != QG_OK) return st;
+    }
+    return QG_OK;
 }
 
 int qg_read_device_fault(unsigned int *flags) {

@@ -67,6 +67,9 @@ cudaError_t simt_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStrea
 bool tc_eligible(int M, int K, int bits, int a_dtype, int bs);
 size_t tc_workspace_bytes(int M, int N, int K, int bits);
 cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s);
+// Ragged expert GEMM (grouped tensor-core launch over the experts with at least
+// min_rows rows; offsets[0..E] host values).  At most 256 experts.
+cudaError_t tc_gemm_grouped(const GemmProblem &p, const int64_t *offsets, int E, int min_rows, cudaStream_t s);
 
 // Fused single-token QMoE decode (fc1 -> SwiGLU -> fc2 -> weighted sum).
 struct QmoeProblem {

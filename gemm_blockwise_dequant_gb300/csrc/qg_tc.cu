@@ -85,6 +85,7 @@ struct TcArgs {
     // remaining tiles are split along K into tail_splits pieces of tail_kps
     // steps each, one CTA per piece, summed afterwards in split order.
     int nt, full_tiles, tail_splits, tail_kps;
+    int y_vec16;  // 16-bit Y with 16-byte aligned rows (N % 8 == 0, Y 16-byte aligned): packed stores
     unsigned *fault;
 };
 
@@ -235,11 +236,27 @@ __device__ __forceinline__ uint4 dequant8_codebook(uint32_t codes, float am, con
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-template <int WK, int BITS, bool BF16, int BN>
+// Grouped (ragged expert) mode: expert e owns activation rows row_off[e] ..
+// row_off[e+1]-1 and weight rows e*N .. e*N+N-1 of the stacked [E*N] weight
+// tensors; its M tiles are numbered mt_prefix[e] .. mt_prefix[e+1]-1 (an
+// expert the grouped launch leaves out has none).  Passed by value.
+constexpr int kMaxGroups = 256;
+template <bool G>
+struct TcGroups {
+    int unused;
+};
+template <>
+struct TcGroups<true> {
+    int count;
+    int mt_prefix[kMaxGroups + 1];
+    int row_off[kMaxGroups + 1];
+};
+
+template <int WK, int BITS, bool BF16, int BN, bool GROUPED = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constant__ CUtensorMap code_map,
                    const __grid_constant__ CUtensorMap par_map, const __grid_constant__ CUtensorMap zp_map,
-                   const TcArgs p) {
+                   const TcArgs p, const __grid_constant__ TcGroups<GROUPED> grp) {
     constexpr int NS = act_slots(BN);
     static_assert(NS >= 3, "shared memory too small for the activation ring");
     constexpr int CB = kBK * BITS / 8;           // code bytes per row per K step
@@ -274,14 +291,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int tile = blockIdx.x, ks0 = 0, nks = p.nk, pslot = -1;
-    if (tile >= p.full_tiles) {
+    if (!GROUPED && tile >= p.full_tiles) {
         const int q = tile - p.full_tiles, r = q / p.tail_splits, z = q - r * p.tail_splits;
         tile = p.full_tiles + r;
         ks0 = z * p.tail_kps;
         nks = max(0, min(p.nk, ks0 + p.tail_kps) - ks0);
         pslot = p.tail_splits > 1 ? q : -1;  // an unsplit tail tile writes Y directly
     }
-    const int m0 = (tile / p.nt) * kBM, n0 = (tile % p.nt) * BN;
+    int m0 = (tile / p.nt) * kBM, m_end = p.M, wrow = 0;
+    const int n0 = (tile % p.nt) * BN;
+    if constexpr (GROUPED) {
+        // the expert owning M tile mt: the last e with mt_prefix[e] <= mt
+        const int mt = tile / p.nt;
+        int lo = 0, hi = grp.count;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (grp.mt_prefix[mid] <= mt) lo = mid;
+            else hi = mid;
+        }
+        m0 = grp.row_off[lo] + (mt - grp.mt_prefix[lo]) * kBM;
+        m_end = grp.row_off[lo + 1];
+        wrow = lo * p.N;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -322,9 +353,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!mbar_wait(&cempty[c], ((j / kCodeSlots) & 1) ^ 1, abort_flag, p.fault, FAULT_WAIT_TC)) break;
                     mbar_arrive_expect_tx(&cfull[c], CODE_BYTES + PAR_BYTES * (zt ? 2 : 1));
                     const int pcol = (ks * kBK / p.bs) / PPB * PPB;  // first parameter column of the box
-                    tma_load_2d(code_s + c * CODE_BYTES, &code_map, ks * CB, n0, &cfull[c]);
-                    tma_load_2d(par_s + c * PAR_BYTES, &par_map, pcol, n0, &cfull[c]);
-                    if (zt) tma_load_2d(zp_s + c * PAR_BYTES, &zp_map, pcol, n0, &cfull[c]);
+                    tma_load_2d(code_s + c * CODE_BYTES, &code_map, ks * CB, wrow + n0, &cfull[c]);
+                    tma_load_2d(par_s + c * PAR_BYTES, &par_map, pcol, wrow + n0, &cfull[c]);
+                    if (zt) tma_load_2d(zp_s + c * PAR_BYTES, &zp_map, pcol, wrow + n0, &cfull[c]);
                 }
                 const int s = i % NS;
                 if (!mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, abort_flag, p.fault, FAULT_WAIT_TC)) break;
@@ -336,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(kMH, BN, BF16);
-            const bool two = m0 + kMH < p.M;  // the second half holds rows below M
+            const bool two = m0 + kMH < m_end;  // the second half holds rows below M (the expert's end)
             bool ok = true;
             for (int i = 0; i < nks && ok; ++i) {
                 const int s = i % NS, b = i & 1;
@@ -441,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(lane_addr + cc, r);
             const int h = cc / BN, c0 = cc - h * BN;
             const int row = h * kMH + sub * 32 + lane, m = m0 + row;
-            if (!ok || nks == 0 || m >= p.M) continue;  // rows past M are never read back
+            if (!ok || nks == 0 || m >= m_end) continue;  // rows past M (the expert's end) are never read back
             const int nb0 = n0 + c0;
             if (pslot >= 0) {  // a tail piece: the whole 32-column row segment (columns past N are ignored)
                 float4 *dst = reinterpret_cast<float4 *>(p.partial + (static_cast<size_t>(pslot) * kBM + row) * BN + c0);
@@ -455,6 +486,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 8; ++j)
                     dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            } else if (p.y_vec16 && nb0 + 32 <= p.N) {  // 16-bit output: 32 values as four 16-byte stores
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.Y) + static_cast<size_t>(m) * p.N + nb0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t h[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float lo = __uint_as_float(r[8 * j + 2 * q]), hi = __uint_as_float(r[8 * j + 2 * q + 1]);
+                        if (p.y_dtype == 1) {
+                            h[q] = h2_as_u32(__floats2half2_rn(lo, hi));
+                        } else {
+                            const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+                            h[q] = *reinterpret_cast<const uint32_t *>(&b);
+                        }
+                    }
+                    dst[j] = make_uint4(h[0], h[1], h[2], h[3]);
+                }
             } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
@@ -566,10 +614,10 @@ TcCfg choose_tc(int M, int N, int K, int bits) {
     return best;
 }
 
-template <int WK, int BITS, bool BF16, int BN>
+template <int WK, int BITS, bool BF16, int BN, bool GROUPED = false>
 cudaError_t launch_tc(const CUtensorMap &am, const CUtensorMap &cm, const CUtensorMap &pm, const CUtensorMap &zm,
-                      const TcArgs &a, const TcCfg &c, cudaStream_t s) {
-    auto kern = tc_gemm_kernel<WK, BITS, BF16, BN>;
+                      const TcArgs &a, int grid_x, const TcGroups<GROUPED> &grp, cudaStream_t s) {
+    auto kern = tc_gemm_kernel<WK, BITS, BF16, BN, GROUPED>;
     static std::atomic<unsigned> configured{0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -580,9 +628,86 @@ cudaError_t launch_tc(const CUtensorMap &am, const CUtensorMap &cm, const CUtens
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    dim3 grid(c.grid());
-    const cudaError_t e = launch_pdl(kern, grid, dim3(kThreads), smem, s, am, cm, pm, zm, a);
+    const cudaError_t e = launch_pdl(kern, dim3(grid_x), dim3(kThreads), smem, s, am, cm, pm, zm, a, grp);
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Tensor maps of one problem: activations [M][K] (128-byte swizzled boxes of
+// 64 x 256), codes [w_rows][K*bits/8] and block parameters (and zero points)
+// [w_rows][K/bs] in boxes of BN rows.  w_rows is N, or E*N for the stacked
+// experts of a grouped launch.
+cudaError_t build_maps(PFN_cuTensorMapEncodeTiled_v12000 enc, const GemmProblem &p, int bn, long long w_rows,
+                       CUtensorMap &am, CUtensorMap &cm, CUtensorMap &pm, CUtensorMap &zm) {
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.M)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K) * 2};
+        const cuuint32_t box[2] = {kBK, kBM};
+        const cuuint32_t es[2] = {1, 1};
+        if (enc(&am, p.a_dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                const_cast<void *>(p.A), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const int row_bytes = p.K * p.bits / 8;
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(w_rows)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kCodeBox), static_cast<cuuint32_t>(bn)};
+        const cuuint32_t es[2] = {1, 1};
+        if (enc(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(p.W), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    // block parameters (and zero points): [rows][nb] matrices read as boxes of
+    // 16 bytes x BN rows, one box per stage
+    const bool cbk = p.kind == WK_CODEBOOK;
+    const int pe = cbk ? 4 : 2;
+    const int nb = p.K / p.bs;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nb), static_cast<cuuint64_t>(w_rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nb) * pe};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kParamBox / pe), static_cast<cuuint32_t>(bn)};
+    const cuuint32_t es[2] = {1, 1};
+    const CUtensorMapDataType dt = cbk ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    const void *pp = cbk ? static_cast<const void *>(p.absmax) : static_cast<const void *>(p.scales);
+    if (enc(&pm, dt, 2, const_cast<void *>(pp), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    zm = pm;
+    if (!cbk && p.zp_mode == ZP_TENSOR &&
+        enc(&zm, dt, 2, const_cast<uint16_t *>(p.zp), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+TcArgs make_args(const GemmProblem &p, const TcCfg &c) {
+    TcArgs a{};
+    a.scales = p.scales;
+    a.zp = p.zp;
+    a.zp_mode = p.zp_mode;
+    a.zpv = p.uniform_zp;
+    a.codebook = p.codebook;
+    a.absmax = p.absmax;
+    a.Y = p.Y;
+    a.y_dtype = p.y_dtype;
+    a.M = p.M;
+    a.N = p.N;
+    a.K = p.K;
+    a.bs = p.bs;
+    a.lbs = 31 - __builtin_clz(static_cast<unsigned>(p.bs));
+    a.nb = p.K / p.bs;
+    a.nk = c.nk;
+    a.nt = c.nt;
+    a.full_tiles = c.full_tiles;
+    a.tail_splits = c.tail_splits;
+    a.tail_kps = c.tail_kps;
+    a.y_vec16 = p.y_dtype != 0 && (p.N & 7) == 0 && (reinterpret_cast<uintptr_t>(p.Y) & 15u) == 0;
+    a.fault = fault_word();
+    return a;
 }
 
 }  // namespace
@@ -609,74 +734,10 @@ cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_
     if (!enc) return cudaErrorNotSupported;
     const TcCfg c = choose_tc(p.M, p.N, p.K, p.bits);
     if (c.bn == 0) return cudaErrorNotSupported;
-    CUtensorMap am, cm;
-    {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.M)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K) * 2};
-        const cuuint32_t box[2] = {kBK, kBM};
-        const cuuint32_t es[2] = {1, 1};
-        if (enc(&am, p.a_dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                const_cast<void *>(p.A), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    {
-        const int row_bytes = p.K * p.bits / 8;
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(p.N)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kCodeBox), static_cast<cuuint32_t>(c.bn)};
-        const cuuint32_t es[2] = {1, 1};
-        if (enc(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(p.W), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    // block parameters (and zero points): [N][nb] matrices read as boxes of 16
-    // bytes x BN rows, one box per stage
-    CUtensorMap pm, zm;
-    {
-        const bool cbk = p.kind == WK_CODEBOOK;
-        const int pe = cbk ? 4 : 2;
-        const int nb = p.K / p.bs;
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nb), static_cast<cuuint64_t>(p.N)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nb) * pe};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kParamBox / pe), static_cast<cuuint32_t>(c.bn)};
-        const cuuint32_t es[2] = {1, 1};
-        const CUtensorMapDataType dt = cbk ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
-        const void *pp = cbk ? static_cast<const void *>(p.absmax) : static_cast<const void *>(p.scales);
-        if (enc(&pm, dt, 2, const_cast<void *>(pp), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-        zm = pm;
-        if (!cbk && p.zp_mode == ZP_TENSOR &&
-            enc(&zm, dt, 2, const_cast<uint16_t *>(p.zp), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    TcArgs a{};
-    a.scales = p.scales;
-    a.zp = p.zp;
-    a.zp_mode = p.zp_mode;
-    a.zpv = p.uniform_zp;
-    a.codebook = p.codebook;
-    a.absmax = p.absmax;
-    a.Y = p.Y;
-    a.y_dtype = p.y_dtype;
-    a.M = p.M;
-    a.N = p.N;
-    a.K = p.K;
-    a.bs = p.bs;
-    a.lbs = 31 - __builtin_clz(static_cast<unsigned>(p.bs));
-    a.nb = p.K / p.bs;
-    a.nk = c.nk;
-    a.nt = c.nt;
-    a.full_tiles = c.full_tiles;
-    a.tail_splits = c.tail_splits;
-    a.tail_kps = c.tail_kps;
-    a.fault = fault_word();
+    CUtensorMap am, cm, pm, zm;
+    const cudaError_t me = build_maps(enc, p, c.bn, p.N, am, cm, pm, zm);
+    if (me != cudaSuccess) return me;
+    TcArgs a = make_args(p, c);
     if (c.partial_bytes()) {
         if (!ws || ws_bytes < c.partial_bytes()) return cudaErrorInvalidValue;
         a.partial = static_cast<float *>(ws);
@@ -685,7 +746,7 @@ cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_
     cudaError_t e = cudaErrorNotSupported;
 #define QG_TC(WK_, B_, BF_, BN_)                                                                     \
     if (p.kind == WK_ && (WK_ == WK_CODEBOOK || p.bits == B_) && bf16 == BF_ && c.bn == BN_) \
-        e = launch_tc<WK_, B_, BF_, BN_>(am, cm, pm, zm, a, c, s);                                \
+        e = launch_tc<WK_, B_, BF_, BN_>(am, cm, pm, zm, a, c.grid(), TcGroups<false>{}, s);       \
     else
     QG_TC(WK_NBITS, 2, false, 256) QG_TC(WK_NBITS, 2, false, 128) QG_TC(WK_NBITS, 2, false, 64)
     QG_TC(WK_NBITS, 2, true, 256) QG_TC(WK_NBITS, 2, true, 128) QG_TC(WK_NBITS, 2, true, 64)
@@ -707,6 +768,61 @@ cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_
         return e2 != cudaSuccess ? e2 : cudaGetLastError();
     }
     return cudaSuccess;
+}
+
+// Ragged expert GEMM on the tensor cores: one launch over the M tiles of every
+// expert with at least min_rows rows (the others are left to the caller);
+// p.M is the total row count, p.N the rows of one expert, p.W / p.scales /
+// p.zp the stacked [E][N][...] tensors.  No K split.
+cudaError_t tc_gemm_grouped(const GemmProblem &p, const int64_t *offsets, int E, int min_rows, cudaStream_t s) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc || E > kMaxGroups || p.kind != WK_NBITS) return cudaErrorNotSupported;
+    TcGroups<true> g{};
+    g.count = E;
+    int tiles_m = 0, big = 0, rows_big = 0;
+    for (int e = 0; e < E; ++e) {
+        const int64_t c = offsets[e + 1] - offsets[e];
+        g.mt_prefix[e] = tiles_m;
+        g.row_off[e] = static_cast<int>(offsets[e]);
+        if (c >= min_rows) {
+            tiles_m += static_cast<int>((c + kBM - 1) / kBM);
+            ++big;
+            rows_big += static_cast<int>(c);
+        }
+    }
+    g.mt_prefix[E] = tiles_m;
+    g.row_off[E] = static_cast<int>(offsets[E]);
+    if (tiles_m == 0) return cudaSuccess;
+    // tile width from the static model at the experts' mean row count
+    TcCfg c = choose_tc(std::max(min_rows, rows_big / big), p.N, p.K, p.bits);
+    if (c.bn == 0) return cudaErrorNotSupported;
+    // Each M tile is used by one expert only, so a tile's fixed costs (tensor
+    // memory, barriers, pipeline fill, epilogue) are spread over few K steps:
+    // take the widest tile that fits the experts' N (grouped launches are
+    // instantiated for 128- and 256-wide tiles).
+    const int bn = (p.N >= 256 && smem_bytes(256, p.bits) <= device_info().max_smem_optin) ? 256 : 128;
+    if (c.bn != bn) {
+        c.bn = bn;
+        c.nt = (p.N + bn - 1) / bn;
+    }
+    c.mt = tiles_m;
+    c.full_tiles = tiles_m * c.nt;
+    c.tail_tiles = 0;
+    c.tail_splits = 1;
+    c.tail_kps = c.nk;
+    CUtensorMap am, cm, pm, zm;
+    const cudaError_t me = build_maps(enc, p, c.bn, static_cast<long long>(E) * p.N, am, cm, pm, zm);
+    if (me != cudaSuccess) return me;
+    const TcArgs a = make_args(p, c);
+    const bool bf16 = p.a_dtype == 2;
+    const int grid = c.full_tiles;
+#define QG_TCG(B_, BF_, BN_) \
+    if (p.bits == B_ && bf16 == BF_ && c.bn == BN_) return launch_tc<WK_NBITS, B_, BF_, BN_, true>(am, cm, pm, zm, a, grid, g, s);
+    QG_TCG(4, false, 256) QG_TCG(4, false, 128) QG_TCG(4, true, 256) QG_TCG(4, true, 128)
+    QG_TCG(2, false, 256) QG_TCG(2, false, 128) QG_TCG(2, true, 256) QG_TCG(2, true, 128)
+    QG_TCG(8, false, 256) QG_TCG(8, false, 128) QG_TCG(8, true, 256) QG_TCG(8, true, 128)
+#undef QG_TCG
+    return cudaErrorNotSupported;
 }
 
 }  // namespace qg

@@ -268,6 +268,36 @@ int qg_dequant_codebook4(const uint8_t *W, const float *codebook16, const float 
                          int block_size, qg_stream_t stream);
 
 /*
+ * qmoe_ragged_mm -- ragged expert GEMM: the rows of X are grouped by expert
+ * and each group is multiplied by its expert's MatMulNBits weight.
+ * [hip-ep #1318] kernel test table, qmoe_ragged_mm leaf Xfp16_Wu4_Yfp16; the
+ * pages name the op and its types, the layout is this library's reading.
+ *
+ *   for e in 0 .. num_experts-1, r in [offs[e], offs[e+1]):
+ *       Y[r][n] = sum_k X[r][k] * w_e[n][k],  w_e = (q - zp) * s as qgemm_nbits
+ *
+ *   X                [T][K] of x_dtype (QG_F32 / F16 / BF16), T = offs[num_experts]
+ *   expert_offsets   [num_experts + 1] int64, HOST memory: offs[0] = 0, never
+ *                    decreasing (an expert may own no row); read before return
+ *   W                [num_experts][N][K*bits/8] codes, bits 2, 4 or 8
+ *   scales_f16       [num_experts][N][K/block_size] fp16
+ *   zero_points_f16  same shape, fp16, or NULL (midpoint 2^(bits-1))
+ *   Y                [T][N] of y_dtype
+ * X, W, scales and zero points 16-byte aligned; one expert's slice of W and of
+ * the scales must be a multiple of 16 bytes (QG_ERR_UNSUPPORTED otherwise).
+ * With 16-bit activations the experts with 9 or more rows run in one grouped
+ * tensor-core launch (at most 256 experts); the others, and fp32 activations,
+ * run as one GEMM per expert on its rows.  Workspace: at least
+ * qmoe_ragged_mm_workspace_bytes(...) for the same offsets (0 when every expert
+ * takes the grouped launch).
+ */
+int qmoe_ragged_mm(const void *X, int x_dtype, const int64_t *expert_offsets, int num_experts, const uint8_t *W,
+                   const uint16_t *scales_f16, const uint16_t *zero_points_f16, void *Y, int y_dtype, int N, int K,
+                   int bits, int block_size, void *workspace, size_t workspace_bytes, qg_stream_t stream);
+size_t qmoe_ragged_mm_workspace_bytes(int x_dtype, const int64_t *expert_offsets, int num_experts, int N, int K,
+                                      int bits, int block_size);
+
+/*
  * qg_gather_block_quantized -- embedding lookup in a block-quantized table.
  * [hip-ep #1318] kernel test table, gather_block_quantized leaves
  * Xi64_Wu4_Yfp16, Xi64_Wu8_Yfp16 and Xi64_Wfp8_Yfp16 ("Summary", Commit 3:

@@ -250,3 +250,25 @@ def embedding(fmt: int, V: int = 100352, D: int = 5120, n: int = 2048, block_siz
     zp = fp16_uniform_int(g, (V, D // block_size), 0, (1 << bits) - 1) if (zero_points and fmt != 3) else None
     idx = g.integers(0, V, size=n, dtype=np.int64)
     return dict(fmt=fmt, V=V, D=D, n=n, block_size=block_size, W=W, scales=scales, zero_points=zp, indices=idx)
+
+
+def ragged(num_experts: int = 128, tokens: int = 2048, k: int = 8, N: int = 1536, K: int = 2048, bits: int = 4,
+           block_size: int = 32, with_zp: bool = False, seed: int = 0, counts=None) -> dict:
+    """Ragged expert GEMM (the kernel test table's qmoe_ragged_mm leaf, u4 / fp16): by default the fc1 GEMM
+    (2 x 768 outputs, hidden 2048) of the 128-expert top-8 "2048 / 768" MoE layer of hip-ep #1328
+    "Performance", over a 2048-token prompt.  Each token picks k distinct experts
+    uniformly (or `counts` gives the rows per expert); X rows grouped by expert ~ N(0, 1) fp16; codes
+    uniform; fp16 scales U(0.005, 0.02); optional fp16 integer zero points."""
+    g = rng(seed)
+    E = num_experts
+    W = packed_codes(g, E * N, K, bits).reshape(E, N, K * bits // 8)
+    scales = fp16_uniform(g, (E, N, K // block_size), 0.005, 0.02)
+    zp = fp16_uniform_int(g, (E, N, K // block_size), 0, (1 << bits) - 1) if with_zp else None
+    if counts is None:
+        picks = np.concatenate([g.choice(E, size=k, replace=False) for _ in range(tokens)])
+        counts = np.bincount(picks, minlength=E)
+    counts = np.asarray(counts, dtype=np.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    X = fp16_normal(g, (int(offsets[-1]), K), 1.0)
+    return dict(num_experts=E, N=N, K=K, bits=bits, block_size=block_size, W=W, scales=scales, zero_points=zp,
+                offsets=offsets, X=X)
