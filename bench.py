@@ -561,20 +561,21 @@ def run_suite(only=None):
     # 2048-token prompt (16384 rows, ~128 per expert), u4 block 32, fp16 in and out; one weight set
     # (compute-bound)
     if want("ragged"):
-        d = WL.ragged()
-        X = t16(d["X"], torch.float16)
-        W = torch.from_numpy(d["W"]).to(dev)
-        S = t16(d["scales"], torch.float16)
-        T = int(d["offsets"][-1])
-        Y = torch.empty(T, d["N"], dtype=torch.float16, device=dev)
-        off = d["offsets"]
-        ws = torch.empty(max(16, qg.qmoe_ragged_mm_workspace_bytes(1, off, d["N"], d["K"], 4, 32)), dtype=torch.uint8,
-                         device=dev)
-        us = timed(lambda i: qg.qmoe_ragged_mm(X, off, W, S, None, Y, bits=4, block_size=32, workspace=ws,
-                                               stream=st), 4)
-        emit("ragged_fc1_128x1536x2048_u4_bs32_tokens2048_top8", us, flops=2.0 * T * d["N"] * d["K"],
-             rows=T, experts_min_rows=int(np.diff(off).min()), experts_max_rows=int(np.diff(off).max()))
-        del X, W, S, Y
+        for NK in ((1536, 2048), (5760, 2880)):  # the 2048/768 layer; a 2880-wide layer (90 blocks per row)
+            d = WL.ragged(N=NK[0], K=NK[1])
+            X = t16(d["X"], torch.float16)
+            W = torch.from_numpy(d["W"]).to(dev)
+            S = t16(d["scales"], torch.float16)
+            T = int(d["offsets"][-1])
+            Y = torch.empty(T, d["N"], dtype=torch.float16, device=dev)
+            off = d["offsets"]
+            ws = torch.empty(max(16, qg.qmoe_ragged_mm_workspace_bytes(1, off, d["N"], d["K"], 4, 32)),
+                             dtype=torch.uint8, device=dev)
+            us = timed(lambda i: qg.qmoe_ragged_mm(X, off, W, S, None, Y, bits=4, block_size=32, workspace=ws,
+                                                   stream=st), 4)
+            emit("ragged_fc1_128x%dx%d_u4_bs32_tokens2048_top8" % NK, us, flops=2.0 * T * d["N"] * d["K"],
+                 rows=T, experts_min_rows=int(np.diff(off).min()), experts_max_rows=int(np.diff(off).max()))
+            del X, W, S, Y
 
     # block-quantized embedding gather: phi4 table 100352 x 5120, block 32, 2048 token ids, fp16 out.
     # 16 index sets, each drawn from its own sixteenth of the vocabulary, so a row read by one call

@@ -76,8 +76,13 @@ bool valid_bits(int bits) { return bits == 2 || bits == 3 || bits == 4 || bits =
 
 size_t gemm_workspace(int a_dtype, int M, int N, int K, int bits, int bs) {
     if (M <= 0 || N <= 0 || K <= 0 || !valid_bits(bits) || !valid_bs(bs) || K % bs) return 0;
-    if (qg::tc_eligible(M, K, bits, a_dtype, bs)) return qg::tc_workspace_bytes(M, N, K, bits);
-    return qg::simt_workspace_bytes(M, N, K, bits, bs);
+    // the query has no weight kind: the larger need of MatMulNBits and codebook
+    // (their tensor-core eligibility differs when K / bs is not a multiple of 8)
+    size_t need = 0;
+    for (int kind : {qg::WK_NBITS, qg::WK_CODEBOOK})
+        need = std::max(need, qg::tc_eligible(M, K, bits, a_dtype, bs, kind) ? qg::tc_workspace_bytes(M, N, K, bits)
+                                                                              : qg::simt_workspace_bytes(M, N, K, bits, bs));
+    return need;
 }
 
 // Common checks of the three GEMM entry points.  `params` is the scales or
@@ -114,7 +119,7 @@ int run_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s) {
             return QG_ERR_CUDA;
         return QG_OK;
     }
-    const cudaError_t e = qg::tc_eligible(p.M, p.K, p.bits, p.a_dtype, p.bs) ? qg::tc_gemm(p, ws, ws_bytes, s)
+    const cudaError_t e = qg::tc_eligible(p.M, p.K, p.bits, p.a_dtype, p.bs, p.kind) ? qg::tc_gemm(p, ws, ws_bytes, s)
                                                                        : qg::simt_gemm(p, ws, ws_bytes, s);
     if (e == cudaErrorNotSupported) return QG_ERR_UNSUPPORTED;
     return e == cudaSuccess ? QG_OK : QG_ERR_CUDA;
@@ -245,7 +250,7 @@ int ragged_check(const void *X, int x_dtype, const int64_t *off, int E, const ui
 }
 
 bool ragged_grouped(int x_dtype, int E, int K, int bits, int bs) {
-    return E <= 256 && qg::tc_eligible(kRaggedTcRows, K, bits, x_dtype, bs);
+    return E <= 256 && qg::tc_eligible(kRaggedTcRows, K, bits, x_dtype, bs, qg::WK_NBITS);
 }
 
 size_t ragged_workspace(int x_dtype, const int64_t *off, int E, int N, int K, int bits, int bs) {

@@ -64,7 +64,7 @@ size_t simt_workspace_bytes(int M, int N, int K, int bits, int bs);
 cudaError_t simt_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s);
 
 // Tensor-core path (M >= 9 with 16-bit activations).
-bool tc_eligible(int M, int K, int bits, int a_dtype, int bs);
+bool tc_eligible(int M, int K, int bits, int a_dtype, int bs, int kind);
 size_t tc_workspace_bytes(int M, int N, int K, int bits);
 cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s);
 // Ragged expert GEMM (grouped tensor-core launch over the experts with at least

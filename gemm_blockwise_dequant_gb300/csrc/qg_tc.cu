@@ -86,6 +86,10 @@ struct TcArgs {
     // steps each, one CTA per piece, summed afterwards in split order.
     int nt, full_tiles, tail_splits, tail_kps;
     int y_vec16;  // 16-bit Y with 16-byte aligned rows (N % 8 == 0, Y 16-byte aligned): packed stores
+    // fp16 block parameters whose rows (nb * 2 bytes) are not a multiple of 16
+    // bytes cannot be a tensor map: the producer warp copies them with 4-byte
+    // cp.async instead (nb even); w_rows = rows of the weight tensors
+    int par_plain, w_rows;
     unsigned *fault;
 };
 
@@ -96,6 +100,17 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
             smem_u32(dst)),
         "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
+}
+
+// 4 bytes global -> shared, asynchronous; src_bytes 0 writes zeros (nothing is read)
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+// one arrival on `bar` once every cp.async this thread issued before has landed
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
@@ -324,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&wempty[b], 1);
         }
         for (int c = 0; c < kCodeSlots; ++c) {
-            mbar_init(&cfull[c], 1);
+            mbar_init(&cfull[c], p.par_plain ? 33 : 1);  // + one cp.async arrival per producer lane
             mbar_init(&cempty[c], kDequantThreads / 32);
         }
         mbar_init(accf, 1);
@@ -341,7 +356,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     pdl_launch_dependents();  // the next kernel may start launching as these CTAs retire
 
-    if (warp == 0) {
+    if (warp == 0 && p.par_plain) {
+        // ------------------------------------------------------------ producer, parameters by cp.async
+        // Lane 0 waits and issues the tensor copies of codes and activations
+        // as below; every lane copies the parameter boxes of its rows (16
+        // bytes = 8 fp16 per row) in 4-byte pieces, zero past N or past nb.
+        const bool zt = WK == WK_NBITS && p.zp_mode == ZP_TENSOR;
+        if (lane == 0) pdl_wait();
+        __syncwarp();
+        for (int i = 0; i < nks; ++i) {
+            const int ks = ks0 + i;
+            bool ok = true;
+            if (i % CS == 0) {
+                const int j = i / CS, c = j % kCodeSlots;
+                if (lane == 0) ok = mbar_wait(&cempty[c], ((j / kCodeSlots) & 1) ^ 1, abort_flag, p.fault, FAULT_WAIT_TC);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&cfull[c], CODE_BYTES);
+                    tma_load_2d(code_s + c * CODE_BYTES, &code_map, ks * CB, wrow + n0, &cfull[c]);
+                }
+                const int pcol = (ks * kBK / p.bs) / PPB * PPB;
+                for (int r = lane; r < BN; r += 32) {
+                    const int grow = wrow + n0 + r;
+#pragma unroll
+                    for (int q = 0; q < kParamBox / 4; ++q) {
+                        const int col = pcol + 2 * q;  // two fp16 per piece; nb is even
+                        const bool in = grow < p.w_rows && col < p.nb;
+                        const size_t off = in ? (static_cast<size_t>(grow) * p.nb + col) : 0;
+                        cp_async4(par_s + c * PAR_BYTES + r * kParamBox + 4 * q, p.scales + off, in ? 4u : 0u);
+                        if (zt) cp_async4(zp_s + c * PAR_BYTES + r * kParamBox + 4 * q, p.zp + off, in ? 4u : 0u);
+                    }
+                }
+                cp_async_arrive(&cfull[c]);
+            }
+            if (lane == 0) {
+                const int s = i % NS;
+                ok = mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, abort_flag, p.fault, FAULT_WAIT_TC);
+                if (ok) {
+                    mbar_arrive_expect_tx(&full[s], ACT_BYTES);
+                    tma_load_2d(act_s + s * ACT_BYTES, &act_map, ks * kBK, m0, &full[s]);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+        }
+    } else if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             pdl_wait();  // activations may come from the preceding kernel; everything else follows this producer
@@ -661,7 +721,13 @@ cudaError_t build_maps(PFN_cuTensorMapEncodeTiled_v12000 enc, const GemmProblem 
             return cudaErrorInvalidValue;
     }
     // block parameters (and zero points): [rows][nb] matrices read as boxes of
-    // 16 bytes x BN rows, one box per stage
+    // 16 bytes x BN rows, one box per stage -- unless their rows are not a
+    // multiple of 16 bytes (then the kernel copies them without a map)
+    if (p.kind == WK_NBITS && (p.K / p.bs) % 8 != 0) {
+        pm = cm;
+        zm = cm;
+        return cudaSuccess;
+    }
     const bool cbk = p.kind == WK_CODEBOOK;
     const int pe = cbk ? 4 : 2;
     const int nb = p.K / p.bs;
@@ -706,6 +772,8 @@ TcArgs make_args(const GemmProblem &p, const TcCfg &c) {
     a.tail_splits = c.tail_splits;
     a.tail_kps = c.tail_kps;
     a.y_vec16 = p.y_dtype != 0 && (p.N & 7) == 0 && (reinterpret_cast<uintptr_t>(p.Y) & 15u) == 0;
+    a.par_plain = p.kind == WK_NBITS && (p.K / p.bs) % 8 != 0;
+    a.w_rows = p.N;
     a.fault = fault_word();
     return a;
 }
@@ -716,11 +784,14 @@ TcArgs make_args(const GemmProblem &p, const TcCfg &c) {
 // activations stay on the SIMT path (rounding them to 16 bits would break the
 // 1e-4 bar), and so do shapes whose packed rows or parameter rows are not a
 // multiple of 16 bytes (the TMA row stride).
-bool tc_eligible(int M, int K, int bits, int a_dtype, int bs) {
+bool tc_eligible(int M, int K, int bits, int a_dtype, int bs, int kind) {
     if (M < 9 || a_dtype == 0) return false;
     if (bits == 3) return false;  // 3-bit codes (8 per 3 bytes) run on the SIMT path
     if ((K * bits / 8) % 16 != 0) return false;
-    if ((K / bs) % 8 != 0) return false;  // parameter rows (fp16 scales / zero points, fp32 absmax) in 16-byte units
+    // parameter rows: a tensor map needs 16-byte rows (nb % 8 == 0); otherwise
+    // the fp16 scales / zero points of MatMulNBits are copied in 4-byte pieces
+    // (nb even).  The codebook's fp32 absmax always uses the map.
+    if ((K / bs) % 8 != 0 && (kind != WK_NBITS || (K / bs) % 2 != 0)) return false;
     return encode_fn() != nullptr;
 }
 
@@ -813,7 +884,8 @@ cudaError_t tc_gemm_grouped(const GemmProblem &p, const int64_t *offsets, int E,
     CUtensorMap am, cm, pm, zm;
     const cudaError_t me = build_maps(enc, p, c.bn, static_cast<long long>(E) * p.N, am, cm, pm, zm);
     if (me != cudaSuccess) return me;
-    const TcArgs a = make_args(p, c);
+    TcArgs a = make_args(p, c);
+    a.w_rows = E * p.N;
     const bool bf16 = p.a_dtype == 2;
     const int grid = c.full_tiles;
 #define QG_TCG(B_, BF_, BN_) \

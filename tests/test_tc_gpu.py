@@ -67,6 +67,12 @@ TC_CASES = [
     (64, 300, 2048, 8, 64, F16, "tensor", F32),     # 8-bit codes: one K step per code super-stage
     (130, 256, 1024, 8, 128, BF16, "uniform", F32),
     (300, 520, 4096, 8, 256, F16, "none", F16),
+    # K / bs not a multiple of 8: parameter rows of 180 / 40 / 12 bytes, copied in 4-byte pieces
+    (64, 300, 2880, 4, 32, F16, "tensor", F32),
+    (300, 520, 2880, 4, 32, BF16, "none", F16),
+    (16, 96, 640, 2, 32, F16, "tensor", F32),
+    (40, 200, 768, 8, 128, BF16, "uniform", BF16),
+    (16, 100, 2080, 4, 32, F16, "tensor", F32),    # 65 blocks (odd): stays on the SIMT path
 ]
 
 
