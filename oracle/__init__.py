@@ -85,6 +85,8 @@ def load(path: str | None = None):
         lib.oracle_qmoe_decode_dp4a.restype = I
         lib.oracle_qmoe_ragged_mm.argtypes = [P, I, P, I, P, P, P, I64, I64, I, I, P]
         lib.oracle_qmoe_ragged_mm.restype = I
+        lib.oracle_nested_absmax.argtypes = [P, P, P, F, I, I64, P]
+        lib.oracle_nested_absmax.restype = None
         if path is None:
             _lib = lib
         return lib
@@ -178,6 +180,25 @@ def qgemm_codebook4(A, W, codebook, absmax, *, M, N, K, block_size, a_dtype=None
     (lib or load()).oracle_qgemm_codebook4(_ptr(A), a_dtype, _ptr(W), _ptr(codebook), _ptr(absmax),
                                            M, N, K, block_size, _ptr(rows_a), n_rows, _ptr(Y))
     return Y
+
+
+def nested_absmax(qa, table256, absmax2, offset, nested_block, lib=None):
+    """Expand a nested (double-quantized) absmax: fp32 array of qa's shape."""
+    qa = _c(qa, np.uint8)
+    table256 = _c(table256, np.float32)
+    absmax2 = _c(absmax2, np.float32)
+    out = np.empty(qa.shape, dtype=np.float32)
+    (lib or load()).oracle_nested_absmax(_ptr(qa), _ptr(table256), _ptr(absmax2), float(offset), nested_block,
+                                         qa.size, _ptr(out))
+    return out
+
+
+def qgemm_codebook4_nested(A, W, codebook, qa, table256, absmax2, offset, *, M, N, K, block_size, nested_block,
+                           a_dtype=None, rows=None, lib=None):
+    """The codebook GEMM with a nested absmax: the expansion above, then the plain codebook GEMM."""
+    absmax = nested_absmax(qa, table256, absmax2, offset, nested_block, lib=lib)
+    return qgemm_codebook4(A, W, codebook, absmax, M=M, N=N, K=K, block_size=block_size, a_dtype=a_dtype,
+                           rows=rows, lib=lib)
 
 
 def fp16_uniform_value(t, lib=None):

@@ -531,3 +531,23 @@ int oracle_qmoe_ragged_mm(const void *X, int x_dtype, const int64_t *off, int E,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Nested ("double-quantized") absmax of the codebook GEMM ([P3] Testing     */
+/* plan: quantization modes, nested / non-nested absmax).  The pages do not  */
+/* give the format; reading: the per-block absmax values, taken as one flat  */
+/* row-major sequence i = n * nb + b, are stored as 8-bit codes qa[i] into a */
+/* 256-entry fp32 table, with one fp32 second-level scale per group of       */
+/* nested_bs consecutive values and one fp32 offset:                         */
+/*     absmax[i] = fl32( fl32(table[qa[i]] * absmax2[i / nested_bs]) + offset ) */
+/* (two fp32 round-to-nearest operations).  The GEMM then uses absmax as the */
+/* plain codebook GEMM does.                                                 */
+/* ------------------------------------------------------------------------ */
+void oracle_nested_absmax(const uint8_t *qa, const float *table256, const float *absmax2, float offset,
+                          int nested_bs, int64_t n, float *absmax)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        float v = table256[qa[i]] * absmax2[i / nested_bs];
+        absmax[i] = v + offset;
+    }
+}

@@ -26,6 +26,9 @@ What pins what:
                                 int8 decode vs the chain quantizer -> oracle
                                 fp64 GEMM on q8*sx -> numpy bias / SwiGLU /
                                 weighted sum;
+  * nested absmax            -- hand-worked fixture; table[q] = q with an
+                                affine second level reduces to the plain
+                                codebook GEMM;
   * ragged expert GEMM       -- hand-worked fixture (an expert with no rows);
                                 segment by segment equal to the MatMulNBits
                                 oracle; bad offsets refused;
@@ -577,6 +580,39 @@ def check_ragged_bad_offsets(lib):
         raise AssertionError("offsets %s accepted" % bad)
 
 
+# ---------------------------------------------------------------------------
+def check_golden_nested_absmax(lib):
+    g = _golden("nested_absmax_handworked.json")
+    table = ((np.arange(256) - 128) / 128).astype(np.float32)  # the fixture's table rule
+    got = O.nested_absmax(np.array(g["qa"], dtype=np.uint8), table, np.array(g["absmax2"], dtype=np.float32),
+                          g["offset"], g["nested_block"], lib=lib)
+    assert got.tolist() == g["absmax"], got.tolist()
+
+
+def check_nested_reduces_to_plain(lib):
+    """table[q] = q, absmax2 = 2, offset = 0.5: absmax = 2 q + 0.5 exactly, so the
+    nested GEMM equals the (pinned) plain codebook GEMM on that absmax."""
+    rng = np.random.default_rng(41)
+    M, N, K, bs, nbl = 3, 37, 256, 64, 16
+    W = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    cb = rng.standard_normal(16).astype(np.float32)
+    qa = rng.integers(0, 256, size=(N, K // bs), dtype=np.uint8)
+    nblocks = -(-qa.size // nbl)
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    table = np.arange(256, dtype=np.float32)
+    absmax2 = np.full(nblocks, 2.0, dtype=np.float32)
+    y = O.qgemm_codebook4_nested(A, W, cb, qa, table, absmax2, 0.5, M=M, N=N, K=K, block_size=bs, nested_block=nbl,
+                                 lib=lib)
+    ref = O.qgemm_codebook4(A, W, cb, (2.0 * qa.astype(np.float64) + 0.5).astype(np.float32), M=M, N=N, K=K,
+                            block_size=bs, lib=lib)
+    assert np.array_equal(y, ref)
+    # a second-level scale per group of nested_block values in flat order
+    absmax2 = (1.0 + np.arange(nblocks)).astype(np.float32)
+    got = O.nested_absmax(qa, table, absmax2, 0.0, nbl, lib=lib)
+    flat = qa.reshape(-1).astype(np.float64) * np.repeat(absmax2.astype(np.float64), nbl)[: qa.size]
+    assert np.array_equal(got.reshape(-1).astype(np.float64), flat)
+
+
 ALL_CHECKS = [
     check_half_decode, check_bf16_decode, check_unpack_vs_unpackbits, check_golden_u2, check_golden_u3, check_golden_u4, check_golden_u8,
     check_golden_codebook, check_golden_qmoe, check_onehot, check_uniform_vs_tensor, check_closed_form,
@@ -584,4 +620,5 @@ ALL_CHECKS = [
     check_e4m3_decode, check_golden_gather, check_gather_rows,
     check_golden_i8_quant, check_i8_quant_properties, check_qmoe_dp4a_chain,
     check_golden_ragged, check_ragged_vs_per_expert, check_ragged_bad_offsets,
+    check_golden_nested_absmax, check_nested_reduces_to_plain,
 ]

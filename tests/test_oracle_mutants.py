@@ -64,6 +64,9 @@ MUTANTS = {
     "ragged_row_within_segment": ("load_elem(X, x_dtype, (size_t)(r * K + k))",
                                   "load_elem(X, x_dtype, (size_t)((r - off[e]) * K + k))"),
     "ragged_first_offset_unchecked": ("if (off[0] != 0)\n        return -1;", ""),
+    "nested_offset_dropped": ("absmax[i] = v + offset;", "absmax[i] = v;"),
+    "nested_scale_index": ("absmax2[i / nested_bs]", "absmax2[i % nested_bs]"),
+    "nested_table_reversed": ("table256[qa[i]]", "table256[255 - qa[i]]"),
 }
 
 
