@@ -522,6 +522,25 @@ def run_suite(only=None):
                      flops=2.0 * M * d["N"] * d["K"])
                 del Ws
 
+    # NF4 with a nested (double-quantized) absmax, M = 1, bf16: the expansion plus the codebook GEMV;
+    # bytes = codes + 8-bit absmax codes + second-level scales
+    if want("nf4"):
+        d = WL.nf4_nested("square", M=1, a_dtype=2)
+        wb = d["W"].nbytes + d["absmax_q"].nbytes + d["absmax2"].nbytes
+        r = reps_for(wb)
+        Ws = [torch.from_numpy(d["W"]).to(dev) for _ in range(r)]
+        qa = torch.from_numpy(d["absmax_q"]).to(dev)
+        tab, a2 = torch.from_numpy(d["absmax_table"]).to(dev), torch.from_numpy(d["absmax2"]).to(dev)
+        cb = torch.from_numpy(d["codebook"]).to(dev)
+        A = t16(d["A"], torch.bfloat16)
+        Y = torch.empty(1, d["N"], device=dev, dtype=torch.bfloat16)
+        ws = torch.empty(qg.qgemm_codebook4_nested_workspace_bytes(2, 1, d["N"], d["K"], 64), dtype=torch.uint8,
+                         device=dev)
+        us = timed(lambda i: qg.qgemm_codebook4_nested(A, Ws[i % r], cb, qa, tab, a2, d["absmax_offset"], Y,
+                                                       block_size=64, workspace=ws, stream=st), 2 * r)
+        emit("nf4_nested_square_4096x4096_m1", us, nbytes=wb)
+        del Ws
+
     # QMoE decode: rotate over disjoint expert sets (128 experts, top-8)
     if want("qmoe"):
         for with_zp in (False, True):

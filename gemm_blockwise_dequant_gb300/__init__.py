@@ -23,7 +23,8 @@ __all__ = [
     "qmoe_decode_fused", "qmoe_decode_fused_dp4a", "qmoe_decode_fused_noalloc", "qmoe_decode_workspace_bytes", "QG_QMOE_NOALLOC_SCRATCH_BYTES",
     "qg_fp16_uniform_value", "qg_dequant_nbits",
     "qg_dequant_nbits_uniform_zp", "qg_dequant_codebook4", "qg_read_device_fault", "qg_status_string",
-    "qmoe_ragged_mm", "qmoe_ragged_mm_workspace_bytes", "qg_gather_block_quantized", "QG_WF_U2", "QG_WF_U4", "QG_WF_U8", "QG_WF_E4M3",
+    "qgemm_codebook4_nested", "qgemm_codebook4_nested_workspace_bytes", "qmoe_ragged_mm",
+    "qmoe_ragged_mm_workspace_bytes", "qg_gather_block_quantized", "QG_WF_U2", "QG_WF_U4", "QG_WF_U8", "QG_WF_E4M3",
 ]
 
 QG_OK, QG_ERR_INVALID_ARG, QG_ERR_UNSUPPORTED, QG_ERR_CUDA, QG_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3, 4
@@ -70,6 +71,8 @@ _SIGS = {
     "qg_dequant_nbits_uniform_zp": ([_P, _P, _F, _P, _I, _I, _I, _I, _P], _I),
     "qg_dequant_codebook4": ([_P, _P, _P, _P, _I, _I, _I, _P], _I),
     "qg_gather_block_quantized": ([_P, ctypes.c_int64, _P, _I, _P, _P, ctypes.c_int64, _I, _I, _P, _I, _P, _P], _I),
+    "qgemm_codebook4_nested": ([_P, _I, _P, _P, _P, _P, _P, _F, _I, _P, _I, _I, _I, _I, _I, _P, _SZ, _P], _I),
+    "qgemm_codebook4_nested_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
     "qmoe_ragged_mm": ([_P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P], _I),
     "qmoe_ragged_mm_workspace_bytes": ([_I, _P, _I, _I, _I, _I, _I], _SZ),
     "qg_read_device_fault": ([_P], _I),
@@ -250,6 +253,24 @@ def qg_dequant_codebook4(W, codebook, absmax, out, *, block_size, stream=None, r
     s = lib().qg_dequant_codebook4(_ptr(W), _ptr(codebook), _ptr(absmax), _ptr(out), N, K, block_size,
                                    _stream(stream))
     return s if raw else _check(s, "qg_dequant_codebook4")
+
+
+def qgemm_codebook4_nested_workspace_bytes(a_dtype: int, M: int, N: int, K: int, block_size: int) -> int:
+    return lib().qgemm_codebook4_nested_workspace_bytes(a_dtype, M, N, K, block_size)
+
+
+def qgemm_codebook4_nested(A, W, codebook, absmax_q, absmax_table, absmax2, absmax_offset, Y, *, block_size,
+                           nested_block=256, workspace=None, stream=None, raw=False):
+    """qgemm_codebook4 with a nested absmax: absmax = table[absmax_q] * absmax2[i // nested_block] + offset
+    (absmax_q [N, K/block_size] uint8, absmax_table [256] float32, absmax2 float32)."""
+    M, K = A.shape
+    N = W.shape[0]
+    ws, wsb = _workspace(qgemm_codebook4_nested_workspace_bytes(_dtype_code(A), M, N, K, block_size), workspace,
+                         A.device)
+    s = lib().qgemm_codebook4_nested(_ptr(A), _dtype_code(A), _ptr(W), _ptr(codebook), _ptr(absmax_q),
+                                     _ptr(absmax_table), _ptr(absmax2), float(absmax_offset), nested_block, _ptr(Y),
+                                     _dtype_code(Y), M, N, K, block_size, _ptr(ws), wsb, _stream(stream))
+    return s if raw else _check(s, "qgemm_codebook4_nested")
 
 
 def _host_offsets(offsets):

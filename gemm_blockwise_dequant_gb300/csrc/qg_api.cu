@@ -312,6 +312,63 @@ int qgemm_codebook4(const void *A, int a_dtype, const uint8_t *W, const float *c
     return run_gemm(p, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t qgemm_codebook4_nested_workspace_bytes(int a_dtype, int M, int N, int K, int block_size) {
+    if (M <= 0 || N <= 0 || K <= 0 || !valid_bs(block_size) || K % block_size) return 0;
+    const size_t expanded = (static_cast<size_t>(N) * (K / block_size) * sizeof(float) + 255) / 256 * 256;
+    return expanded + gemm_workspace(a_dtype, M, N, K, 4, block_size);
+}
+
+int qgemm_codebook4_nested(const void *A, int a_dtype, const uint8_t *W, const float *codebook16,
+                           const uint8_t *absmax_q, const float *absmax_table256, const float *absmax2,
+                           float absmax_offset, int nested_block, void *Y, int y_dtype, int M, int N, int K,
+                           int block_size, void *workspace, size_t workspace_bytes, qg_stream_t stream) {
+    (void)cudaGetLastError();
+    if (!valid_dtype(a_dtype) || !valid_dtype(y_dtype) || M < 0 || N < 0 || K < 0) return QG_ERR_INVALID_ARG;
+    if (!valid_bs(block_size)) return QG_ERR_UNSUPPORTED;
+    if (K % block_size) return QG_ERR_INVALID_ARG;
+    if (M > kMaxM || N > kMaxN || K > kMaxK) return QG_ERR_UNSUPPORTED;
+    if (nested_block < 1 || !(absmax_offset == absmax_offset)) return QG_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return QG_OK;
+    if (!Y) return QG_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        GemmProblem z{};
+        z.Y = Y;
+        z.y_dtype = y_dtype;
+        z.M = M;
+        z.N = N;
+        return run_gemm(z, nullptr, 0, s);  // an empty sum: zeros
+    }
+    if (!A || !W || !codebook16 || !absmax_q || !absmax_table256 || !absmax2) return QG_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(W)) return QG_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(absmax_table256) | reinterpret_cast<uintptr_t>(absmax2)) & 3u)
+        return QG_ERR_INVALID_ARG;
+    const size_t need = qgemm_codebook4_nested_workspace_bytes(a_dtype, M, N, K, block_size);
+    if (!workspace || workspace_bytes < need) return QG_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(workspace)) return QG_ERR_INVALID_ARG;
+    const size_t n = static_cast<size_t>(N) * (K / block_size);
+    float *absmax = static_cast<float *>(workspace);
+    if (qg::launch_nested_absmax(absmax_q, absmax_table256, absmax2, absmax_offset, nested_block, n, absmax, s) !=
+        cudaSuccess)
+        return QG_ERR_CUDA;
+    const size_t expanded = (n * sizeof(float) + 255) / 256 * 256;
+    GemmProblem p{};
+    p.A = A;
+    p.a_dtype = a_dtype;
+    p.W = W;
+    p.kind = qg::WK_CODEBOOK;
+    p.codebook = codebook16;
+    p.absmax = absmax;
+    p.Y = Y;
+    p.y_dtype = y_dtype;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.bits = 4;
+    p.bs = block_size;
+    return run_gemm(p, static_cast<char *>(workspace) + expanded, workspace_bytes - expanded, s);
+}
+
 size_t qgemm_workspace_bytes(int a_dtype, int M, int N, int K, int bits, int block_size) {
     return gemm_workspace(a_dtype, M, N, K, bits, block_size);
 }

@@ -109,5 +109,7 @@ cudaError_t launch_gather(const GatherProblem &g, cudaStream_t s);
 // Utility kernels.
 cudaError_t launch_dequant(const GemmProblem &p, float *out, cudaStream_t s);
 cudaError_t launch_uniform_check(const uint16_t *t, size_t n, unsigned *ws, cudaStream_t s);
+cudaError_t launch_nested_absmax(const uint8_t *qa, const float *table, const float *absmax2, float offset,
+                                 int nested, size_t n, float *out, cudaStream_t s);
 
 }  // namespace qg

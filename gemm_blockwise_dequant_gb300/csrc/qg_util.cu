@@ -9,6 +9,8 @@
 #include "qg_device.cuh"
 #include "qg_internal.h"
 
+#include <algorithm>
+
 namespace qg {
 namespace {
 
@@ -68,6 +70,17 @@ __global__ void dequant_u3_kernel(const uint8_t *__restrict__ W, const uint16_t 
     }
 }
 
+// Nested absmax: absmax[i] = (table[qa[i]] * absmax2[i / nested]) + offset,
+// two fp32 round-to-nearest operations (bitsandbytes #1979 "Testing plan":
+// nested / non-nested absmax; the layout is this library's reading).
+__global__ void nested_absmax_kernel(const uint8_t *__restrict__ qa, const float *__restrict__ table,
+                                     const float *__restrict__ absmax2, float offset, int nested, size_t n,
+                                     float *__restrict__ out) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x)
+        out[i] = __fadd_rn(__fmul_rn(__ldg(table + __ldg(qa + i)), __ldg(absmax2 + i / nested)), offset);
+}
+
 // ws[0] <- 1 if some element's bit pattern differs from t[0].  Every writer
 // stores the same value, so the result does not depend on the order.
 __global__ void uniform_kernel(const uint16_t *__restrict__ t, size_t n, unsigned *ws) {
@@ -118,6 +131,15 @@ cudaError_t launch_dequant(const GemmProblem &p, float *out, cudaStream_t s) {
         dequant_kernel<4, WK_NBITS><<<blocks, threads, 0, s>>>(p.W, reinterpret_cast<const unsigned char *>(p.scales),
                                                                 p.zp, p.zp_mode, p.uniform_zp, nullptr, out, p.N,
                                                                 p.K, p.bs);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_nested_absmax(const uint8_t *qa, const float *table, const float *absmax2, float offset,
+                                 int nested, size_t n, float *out, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    const int threads = 256;
+    const int blocks = static_cast<int>(std::min<size_t>((n + threads - 1) / threads, 4096));
+    nested_absmax_kernel<<<blocks, threads, 0, s>>>(qa, table, absmax2, offset, nested, n, out);
     return cudaGetLastError();
 }
 

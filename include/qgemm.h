@@ -268,6 +268,27 @@ int qg_dequant_codebook4(const uint8_t *W, const float *codebook16, const float 
                          int block_size, qg_stream_t stream);
 
 /*
+ * qgemm_codebook4_nested -- qgemm_codebook4 with a nested ("double-quantized")
+ * absmax.  [bnb #1979] "Testing plan": nested / non-nested absmax; the pages
+ * do not give the format, this library's reading:
+ *   absmax[i] = fl32( fl32(absmax_table256[absmax_q[i]] * absmax2[i / nested_block]) + absmax_offset )
+ * over the flat row-major index i = n * (K/block_size) + b; then exactly as
+ * qgemm_codebook4 with that absmax.
+ *
+ *   absmax_q         [N][K/block_size] uint8 codes (device)
+ *   absmax_table256  [256] fp32 (device, 4-byte aligned)
+ *   absmax2          [ceil(N*(K/block_size) / nested_block)] fp32 (device, 4-byte aligned)
+ *   absmax_offset    fp32 scalar (not NaN); nested_block >= 1 (bitsandbytes uses 256)
+ *   Other arguments as qgemm_codebook4.  The expanded absmax is written to the
+ *   front of the workspace (at least qgemm_codebook4_nested_workspace_bytes()).
+ */
+int qgemm_codebook4_nested(const void *A, int a_dtype, const uint8_t *W, const float *codebook16,
+                           const uint8_t *absmax_q, const float *absmax_table256, const float *absmax2,
+                           float absmax_offset, int nested_block, void *Y, int y_dtype, int M, int N, int K,
+                           int block_size, void *workspace, size_t workspace_bytes, qg_stream_t stream);
+size_t qgemm_codebook4_nested_workspace_bytes(int a_dtype, int M, int N, int K, int block_size);
+
+/*
  * qmoe_ragged_mm -- ragged expert GEMM: the rows of X are grouped by expert
  * and each group is multiplied by its expert's MatMulNBits weight.
  * [hip-ep #1318] kernel test table, qmoe_ragged_mm leaf Xfp16_Wu4_Yfp16; the

@@ -272,3 +272,20 @@ def ragged(num_experts: int = 128, tokens: int = 2048, k: int = 8, N: int = 1536
     X = fp16_normal(g, (int(offsets[-1]), K), 1.0)
     return dict(num_experts=E, N=N, K=K, bits=bits, block_size=block_size, W=W, scales=scales, zero_points=zp,
                 offsets=offsets, X=X)
+
+
+def nf4_nested(shape, M: int, a_dtype: int, seed: int = 0, nested_block: int = 256) -> dict:
+    """NF4-style codebook GEMM with a nested absmax: the nf4 workload's codes, codebook and activations;
+    absmax stored as uniform 8-bit codes into a 256-entry table evenly spaced over [-1, 1] (fp32), one fp32
+    second-level scale U(0.01, 0.03) per nested_block values and offset 0.06 (so absmax spans about
+    [0.03, 0.09], the plain workload's range)."""
+    d = nf4(shape, M, a_dtype, seed)
+    g = rng(seed + 1000)
+    n = d["N"] * (d["K"] // d["block_size"])
+    d.pop("absmax")
+    d["absmax_q"] = g.integers(0, 256, size=(d["N"], d["K"] // d["block_size"]), dtype=np.uint8)
+    d["absmax_table"] = np.linspace(-1.0, 1.0, 256).astype(np.float32)
+    d["absmax2"] = f32_uniform(g, (-(-n // nested_block),), 0.01, 0.03)
+    d["absmax_offset"] = 0.06
+    d["nested_block"] = nested_block
+    return d
