@@ -523,7 +523,6 @@ __device__ __forceinline__ void finish_tile(const GemvArgs &p, const float *rs, 
 
 template <int BITS, int VEC, int MT, int BPL, int WK, int LPR, int AM, int IT>
 __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_kernel(const GemvArgs p) {
-    constexpr int WPL = VEC / 4;
     constexpr int KPL = kpl_of(VEC, BITS);
     constexpr int H = 32 / LPR;         // rows a warp works on at once
     constexpr int ITER = IT;            // row iterations per tile
