@@ -26,6 +26,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -109,11 +110,12 @@ class Clocks:
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, log_path=None):
         self.proc = None
         self.gpu = gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % gpu_index) \
-            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp/qg_clocks_%d.csv" % os.getpid()
+        # raw samples: the --clocks-log file (one per rank), else a temporary file
+        self.path = (log_path % gpu_index if log_path and "%d" in log_path else log_path) or \
+            os.path.join(tempfile.gettempdir(), "qg_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
 
     def __enter__(self):
         try:
@@ -298,7 +300,7 @@ def run_ours(args, world, rank, local):
         graphs[i % reps].replay()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with Clocks(local) as clk:
+    with Clocks(local, getattr(args, "clocks_log", None)) as clk:
         barrier(world)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
@@ -707,6 +709,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-log", default=None,
+                    help="file for the raw nvidia-smi samples of the timed region (%%d: GPU index); default a temp file")
     ap.add_argument("--probe", choices=["gemv_k5120", "gemv_lm_head", "tc_prefill", "qmoe", "qmoe_dp4a", "ragged",
                                         "gather"],
                     help="run a small fixed workload for a profiler capture instead of the benchmark")
