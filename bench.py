@@ -630,6 +630,7 @@ def run_probe(name):
     gemv_lm_head 4 calls of the lm_head shape (100352 x 5120, u2, M=1)
     tc_prefill   4 calls of a prefill-sized u2 GEMM on the tensor cores
                  (M=2048, N=K=5120, fp16 activations, fp32 out)
+    tc_nf4_m64   4 calls of the NF4 codebook GEMM 14336 x 4096 at M=64 (bf16, tensor cores)
     qmoe         4 calls of the 128-expert top-8 2880/2880 block-32 QMoE decode
     qmoe_dp4a    the same with int8 activations
     ragged       4 calls of the ragged expert GEMM (128 experts, 16384 rows, 1536 x 2048 u4 block 32)
@@ -678,6 +679,16 @@ def run_probe(name):
         x, ids, w = h(d["x"]), torch.from_numpy(d["ids"]).cuda(), torch.from_numpy(d["weights"]).cuda()
         for _ in range(4):
             (qg.qmoe_decode_fused_dp4a if name == "qmoe_dp4a" else qg.qmoe_decode_fused)(x, ids, w, **kw)
+    elif name == "tc_nf4_m64":
+        d = WL.nf4("up", M=64, a_dtype=2)
+        A = torch.from_numpy(d["A"].view(np.int16)).cuda().view(torch.bfloat16)
+        W = torch.from_numpy(d["W"]).cuda()
+        cb, am = torch.from_numpy(d["codebook"]).cuda(), torch.from_numpy(d["absmax"]).cuda()
+        Y = torch.empty(64, d["N"], dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(max(16, qg.qgemm_workspace_bytes(2, 64, d["N"], d["K"], 4, 64)), dtype=torch.uint8,
+                         device="cuda")
+        for _ in range(4):
+            qg.qgemm_codebook4(A, W, cb, am, Y, block_size=64, workspace=ws)
     elif name == "ragged":
         d = WL.ragged()
         X = torch.from_numpy(d["X"].view(np.int16)).cuda().view(torch.float16)
@@ -711,8 +722,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-log", default=None,
                     help="file for the raw nvidia-smi samples of the timed region (%%d: GPU index); default a temp file")
-    ap.add_argument("--probe", choices=["gemv_k5120", "gemv_lm_head", "tc_prefill", "qmoe", "qmoe_dp4a", "ragged",
-                                        "gather"],
+    ap.add_argument("--probe", choices=["gemv_k5120", "gemv_lm_head", "tc_prefill", "tc_nf4_m64", "qmoe",
+                                        "qmoe_dp4a", "ragged", "gather"],
                     help="run a small fixed workload for a profiler capture instead of the benchmark")
     ap.add_argument("--suite", action="store_true",
                     help="time every configuration (one JSON line each) instead of the benchmark")
