@@ -17,6 +17,9 @@
  *        Notes for reviewers.
  *   [P3] bitsandbytes pull request #1979, "[ROCm] Fused 4-bit SIMT GEMM" --
  *        sections Summary, Technical details, Testing plan.
+ *   [P1] also carries the kernel unit-test table (Notes for reviewers) whose
+ *        leaves name the 3-bit and 8-bit MatMulNBits codes, qmoe_ragged_mm and
+ *        gather_block_quantized.
  *
  * Readings of points the pages leave open (each one is also listed in the
  * design notes):
@@ -30,7 +33,17 @@
  *     (or the even elements when the interleaved layout is asked for);
  *   - every matmul is accumulated in fp64, ascending k, and returned
  *     unrounded, so that a GPU result can be compared against the exact
- *     product of the dequantized operands.
+ *     product of the dequantized operands;
+ *   - 3-bit codes continue into the next byte (one bit string per row);
+ *   - the embedding gather wraps negative indices once (ONNX Gather rule)
+ *     and gives a zero row for any other index outside the table; "fp8" is
+ *     OCP E4M3 without infinities;
+ *   - int8 activations (the dp4a decode) are quantized per weight block,
+ *     largest magnitude to 127, every step in fp32, ties to even;
+ *   - the ragged expert GEMM groups the rows of X by expert through
+ *     offsets starting at 0;
+ *   - a nested absmax is table[code] * second-level scale + offset over the
+ *     flat row-major sequence of per-block values.
  *
  * Parity pins: every function here is pinned by CPU tests against values
  * written by hand from the pages' statement of the problem, closed forms,
