@@ -366,6 +366,7 @@ int qgemm_codebook4_nested(const void *A, int a_dtype, const uint8_t *W, const f
     p.K = K;
     p.bits = 4;
     p.bs = block_size;
+    p.params_from_device = 1;  // the expansion above writes them
     return run_gemm(p, static_cast<char *>(workspace) + expanded, workspace_bytes - expanded, s);
 }
 

@@ -57,6 +57,10 @@ struct GemmProblem {
     void *Y;
     int y_dtype;
     int M, N, K, bits, bs;
+    // The block parameters are written by the kernel launched just before on
+    // the stream (the nested absmax expansion): kernels that start copying
+    // weights before the preceding kernel completes wait for it first.
+    int params_from_device;
 };
 
 // SIMT decode path (small M).

@@ -92,6 +92,7 @@ struct GemvArgs {
     int swiglu_interleaved;
     float *out_f32;           // slot outputs [slots][N] (QMoE), with bias added
     const uint16_t *bias;     // fp16 [experts][N], or nullptr
+    int params_wait;          // the block parameters come from the preceding kernel: wait before copying them
 };
 
 // u3: 32 codes in 3 words; bit position of code i of the group after its
@@ -581,8 +582,9 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     // slice order and writes the outputs before it refills the stage.  The
     // consumer warps therefore never wait on one another.
     if (warp == NWC) {
-        if (p.ids) pdl_wait();  // expert ids may come from the preceding kernel
-        bool waited = p.ids != nullptr;
+        // expert ids, or block parameters computed on the device, may come from the preceding kernel
+        if (p.ids || p.params_wait) pdl_wait();
+        bool waited = p.ids != nullptr || p.params_wait;
         const int prow = p.nb * PB;
         const int kb0 = kc0 * BITS / 8;
         const int kb1 = split ? min(p.row_bytes, (s_begin + s_count) * LPR * VEC) : p.row_bytes;
@@ -1051,6 +1053,7 @@ cudaError_t simt_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStrea
                                      : reinterpret_cast<const unsigned char *>(p.scales);
     a.zp = p.zp;
     a.zp_mode = p.zp_mode;
+    a.params_wait = p.params_from_device;
     a.zpv = p.uniform_zp;
     a.codebook = p.codebook;
     a.Y = p.Y;
