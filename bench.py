@@ -402,7 +402,8 @@ def run_suite(only=None):
     the NF4 codebook shapes at M=1, 4, 16, 64 (bf16 activations); the QMoE
     decode (128 experts, top-8, 2880/2880, u4 block 32) with and without zero
     points, with fp16 and with int8 activations; the two M=2048 prefill GEMMs; the
-    ragged expert GEMM of a 128-expert top-8 2048/768 layer over a 2048-token prompt;
+    ragged expert GEMM of a 128-expert top-8 2048/768 layer over a 2048-token prompt; an N sweep
+    around two decode shapes (partition-camping outliers);
     the block-quantized embedding gather
     (u4, u8, E4M3 tables).  Each figure is the mean over a CUDA
     graph of R back-to-back calls whose weights rotate over copies (or expert
@@ -598,6 +599,33 @@ def run_suite(only=None):
                  rows=T, experts_min_rows=int(np.diff(off).min()), experts_max_rows=int(np.diff(off).max()))
             del X, W, S, Y
 
+    # N sweep around the decode shapes (u2 M=1, K = 5120 around qkv's N and K = 17920 around down's N, steps
+    # of 64 rows): a row count that maps badly onto the HBM channels would show as an outlier against its
+    # neighbours (more than 15 % below the median GB/s of the two on each side).
+    if want("nsweep"):
+        for K, centre in ((5120, 7680), (17920, 5120)):
+            pts = []
+            for N in range(centre - 8 * 64, centre + 8 * 64 + 1, 64):
+                g = np.random.Generator(np.random.PCG64(N))
+                W0 = g.integers(0, 256, size=(N, K // 4), dtype=np.uint8)
+                S0 = g.uniform(0.01, 0.05, size=(N, K // 64)).astype(np.float16).view(np.int16)
+                wb = W0.nbytes + S0.nbytes
+                r = reps_for(wb)
+                Ws = [torch.from_numpy(W0).to(dev) for _ in range(r)]
+                S = torch.from_numpy(S0).to(dev).view(torch.float16)
+                A = torch.from_numpy(g.standard_normal((1, K)).astype(np.float32)).to(dev)
+                Y = torch.empty(1, N, device=dev)
+                ws = torch.empty(max(16, qg.qgemm_workspace_bytes(0, 1, N, K, 2, 64)), dtype=torch.uint8, device=dev)
+                us = timed(lambda i: qg.qgemm_nbits_uniform_zp(A, Ws[i % r], S, ZP, Y, bits=2, block_size=64,
+                                                               workspace=ws, stream=st), 2 * r)
+                pts.append((N, us, wb / (us * 1e-6) / 1e9))
+                del Ws
+            for j, (N, us, gbs) in enumerate(pts):
+                nbr = [q[2] for q in pts[max(0, j - 2):j] + pts[j + 1:j + 3]]
+                med = statistics.median(nbr)
+                emit("nsweep_u2_m1_k%d_n%d" % (K, N), us, nbytes=N * K // 4 + N * (K // 64) * 2,
+                     neighbour_median_gbs=round(med, 1), outlier=bool(gbs < 0.85 * med))
+
     # block-quantized embedding gather: phi4 table 100352 x 5120, block 32, 2048 token ids, fp16 out.
     # 16 index sets, each drawn from its own sixteenth of the vocabulary, so a row read by one call
     # is not read again for 15 calls (over 3x the L2 of traffic in between).
@@ -727,7 +755,8 @@ def main():
                     help="run a small fixed workload for a profiler capture instead of the benchmark")
     ap.add_argument("--suite", action="store_true",
                     help="time every configuration (one JSON line each) instead of the benchmark")
-    ap.add_argument("--only", choices=["tiny_u4", "phi4_u2", "phi4_u8", "nf4", "qmoe", "prefill", "ragged", "gather"],
+    ap.add_argument("--only", choices=["tiny_u4", "phi4_u2", "phi4_u8", "nf4", "qmoe", "prefill", "ragged", "gather",
+                                       "nsweep"],
                     help="with --suite: time one group of configurations only")
     args = ap.parse_args()
     if args.probe:
