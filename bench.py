@@ -199,6 +199,21 @@ class OracleSample:
         return done, secs, frac
 
 
+def cpu_model():
+    """The host CPU's model name (from /proc/cpuinfo when it names one), else the machine type."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                if key.strip() in ("model name", "Model", "CPU part") and val.strip():
+                    return val.strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.machine()
+
+
 def cpu_baseline(budget_s=12.0, sample=None):
     """Time the oracle on a bounded sample of the workload (about budget_s of CPU work)."""
     S = sample or OracleSample()
@@ -206,7 +221,7 @@ def cpu_baseline(budget_s=12.0, sample=None):
     while secs < 0.8 * budget_s or passes == 0:
         b, t, frac = S.run(min(budget_s, 4.0))
         done, secs, passes = done + b, secs + t, passes + 1
-    return {"value": done / secs / 1e9, "unit": "GB/s", "cores": S.cores, "kind": "oracle",
+    return {"value": done / secs / 1e9, "unit": "GB/s", "cores": S.cores, "cpu_model": cpu_model(), "kind": "oracle",
             "sample": "%d pass(es) over %.1f%% of the rows of the 5 phi4 shapes, M=1 (%.1f MB of weights, %.1f s, "
                       "OpenMP over rows)" % (passes, 100 * frac, done / 1e6, secs)}, secs
 
@@ -236,8 +251,8 @@ def run_reference(args, world, rank):
             "config": {"workload": "phi4-14B u2 decode GEMVs (qkv 7680x5120, o 5120x5120, gate_up 35840x5120, "
                                    "down 5120x17920, lm_head 100352x5120), M=1, bits=2, block 64, fp16 scales, "
                                    "uniform zp 1.5, fp32 A/Y; CPU oracle on a row sample"},
-            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": S.cores, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": S.cores, "cpu_model": cpu_model(),
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
