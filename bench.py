@@ -199,18 +199,28 @@ class OracleSample:
         return done, secs, frac
 
 
+# Arm CPU part numbers of /proc/cpuinfo (implementer 0x41) that this host type may report
+ARM_PARTS = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1", "0xd0c": "Arm Neoverse N1",
+             "0xd49": "Arm Neoverse N2"}
+
+
 def cpu_model():
-    """The host CPU's model name (from /proc/cpuinfo when it names one), else the machine type."""
-    try:
-        with open("/proc/cpuinfo") as f:
-            for line in f:
-                key, _, val = line.partition(":")
-                if key.strip() in ("model name", "Model", "CPU part") and val.strip():
-                    return val.strip()
-    except OSError:
-        pass
+    """The host CPU's model name from /proc/cpuinfo (an Arm part number is named), else the machine type."""
     import platform
 
+    try:
+        with open("/proc/cpuinfo") as f:
+            fields = {}
+            for line in f:
+                key, _, val = line.partition(":")
+                fields.setdefault(key.strip(), val.strip())
+        if fields.get("model name"):
+            return fields["model name"]
+        part = fields.get("CPU part", "")
+        if part:
+            return ARM_PARTS.get(part.lower(), "Arm CPU part " + part) + " (" + platform.machine() + ")"
+    except OSError:
+        pass
     return platform.machine()
 
 
