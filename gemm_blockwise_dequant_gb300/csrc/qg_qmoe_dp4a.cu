@@ -1,6 +1,6 @@
 // qg_qmoe_dp4a.cu -- fused single-token QMoE decode with int8 activations.
 //
-// hip-ep pull request #1328 ("Summary": the fused decode and its dp4a variant;
+// hip-ep pull request #1328 ("Summary": a dp4a form of the fused decode sits beside the fp one;
 // "Test plan": fp and dp4a x block size x zero points x bias).  The
 // activation vector of each GEMV (x before fc1, h = silu(gate) * up before
 // fc2) is quantized per block of bs values to int8 (largest magnitude -> 127,

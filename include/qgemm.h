@@ -190,7 +190,7 @@ size_t qmoe_decode_workspace_bytes(int k, int hidden, int inter);
 
 /*
  * qmoe_decode_fused_dp4a -- the same decode with int8 activations.
- * [hip-ep #1328] "Summary" (the fused decode and its dp4a variant), "Test
+ * [hip-ep #1328] "Summary" (a dp4a form of the fused decode exists beside the fp one), "Test
  * plan" (fp and dp4a x block size x zero points x bias).  The pages do not
  * give the activation quantization; this library's reading: each activation
  * vector (x before fc1, h = silu(gate) * up before fc2) is quantized per block
