@@ -307,22 +307,41 @@ def run_ours(args, world, rank, local):
         for s in SHAPES:
             call(s, r)
 
-    # CUDA graphs: one per replica set (the library is capture-safe: no sync, no allocation)
-    graphs = []
+    # CUDA graphs of up to --graph-steps consecutive steps (each step on the next
+    # weight replica), like a decode graph that chains the GEMVs of several
+    # layers; the library is capture-safe (no sync, no allocation)
+    chain = max(1, args.graph_steps)
+    graphs = {}
+
+    def graph(n, first):
+        key = (n, first % reps)
+        if key not in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    step((first + i) % reps)
+            graphs[key] = g
+        return graphs[key]
+
+    def run_steps(n, first):
+        done = 0
+        while done < n:
+            c = min(chain, n - done)
+            graph(c, first + done).replay()
+            done += c
+
     with torch.cuda.stream(stream):
         for r in range(reps):
             step(r)
         stream.synchronize()
-        for r in range(reps):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                step(r)
-            graphs.append(g)
+        for first, n in ((0, args.warmup), (args.warmup, args.steps)):
+            for j in range(0, n, chain):
+                graph(min(chain, n - j), first + j)
     torch.cuda.synchronize()
 
-    # ---- timed region: K graph replays (5 GEMV launches each)
-    for i in range(args.warmup):
-        graphs[i % reps].replay()
+    # ---- timed region: K steps (5 GEMV launches each) as graph replays
+    with torch.cuda.stream(stream):
+        run_steps(args.warmup, 0)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with Clocks(local, getattr(args, "clocks_log", None)) as clk:
@@ -330,8 +349,7 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             start.record(stream)
-            for i in range(args.steps):
-                graphs[(i + args.warmup) % reps].replay()
+            run_steps(args.steps, args.warmup)
             end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -339,26 +357,52 @@ def run_ours(args, world, rank, local):
     step_ms = max_over_ranks(step_ms, world)
     clocks = clk.summary()
 
-    # ---- per-launch durations of each kernel (events around every launch, same stream)
-    per_shape_us = {}
+    # ---- per-launch duration of each shape: a graph of back-to-back launches of
+    # that shape, each on its own weight replica (more than 3x L2 per graph, so
+    # every launch reads cold weights), timed with events around the replay
+    per_shape_us, isolated_us = {}, {}
     dom_bytes, dom_time = 0, 0.0
-    launches = 0
     for s in SHAPES:
-        evs = []
+        e = data[s]
+        nb = weight_bytes(*WL.PHI4_SHAPES[s])
+        n = max(reps, -(-3 * L2_BYTES // nb), 8)
+        Ws = e["W"] + [e["W"][0].clone() for _ in range(n - len(e["W"]))]
+        Ss = e["S"] + [e["S"][0].clone() for _ in range(n - len(e["S"]))]
+
+        def one(i):
+            qg.qgemm_nbits_uniform_zp(e["A"], Ws[i], Ss[i], ZP, e["Y"], bits=BITS, block_size=BS,
+                                      workspace=ws, stream=stream)
+
         with torch.cuda.stream(stream):
-            for i in range(max(args.steps, 8)):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                call(s, i % reps)
-                b.record(stream)
-                evs.append((a, b))
+            for i in range(n):
+                one(i)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    one(i)
+            g.replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(3):
+                g.replay()
+            b.record(stream)
+            # the same launches one at a time, events around each (launch latency included)
+            evs = []
+            for i in range(8):
+                a1, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a1.record(stream)
+                one(i % n)
+                b1.record(stream)
+                evs.append((a1, b1))
         torch.cuda.synchronize()
-        us = [a.elapsed_time(b) * 1e3 for a, b in evs]
-        per_shape_us[s] = statistics.median(us)
-        launches += 1
+        us = a.elapsed_time(b) * 1e3 / (3 * n)
+        per_shape_us[s] = us
+        isolated_us[s] = statistics.median(x.elapsed_time(y) * 1e3 for x, y in evs)
+        del Ws, Ss, g
         if WL.PHI4_SHAPES[s][1] == 5120:  # the K=5120 launches share one kernel instantiation
-            dom_bytes += weight_bytes(*WL.PHI4_SHAPES[s])
-            dom_time += statistics.mean(us)
+            dom_bytes += nb
+            dom_time += us
 
     # ---- end to end through the API with host buffers: H2D of A, 5 GEMVs, D2H of Y every step
     h2d = sum(data[s]["A_host"].numel() * 4 for s in SHAPES)
@@ -401,8 +445,12 @@ def run_ours(args, world, rank, local):
                                "uniform zp 1.5, fp32 A/Y",
                    "weight_bytes_per_step": per_step, "l2": "weights rotate over %d replicas (%.0f MB > 3x L2)" % (
                        reps, reps * per_step / 1e6),
-                   "step": "one CUDA-graph replay of the 5 GEMV launches", "pct_of_hbm_peak": round(
-                       100 * value / world / peak, 1), "us_per_call": {s: round(v, 2) for s, v in per_shape_us.items()},
+                   "step": "the 5 GEMV launches; steps replayed as CUDA graphs of up to %d steps" % chain,
+                   "pct_of_hbm_peak": round(100 * value / world / peak, 1),
+                   "us_per_call": {s: round(v, 2) for s, v in per_shape_us.items()},
+                   "us_per_call_isolated": {s: round(v, 2) for s, v in isolated_us.items()},
+                   "per_launch": "us_per_call: graph of back-to-back launches of one shape, cold weights; "
+                                 "us_per_call_isolated: one launch between two events",
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -773,6 +821,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph-steps", type=int, default=8,
+                    help="steps per CUDA graph in the timed region (each step is 5 GEMV launches)")
     ap.add_argument("--clocks-log", default=None,
                     help="file for the raw nvidia-smi samples of the timed region (%%d: GPU index); default a temp file")
     ap.add_argument("--probe", choices=["gemv_k5120", "gemv_lm_head", "tc_prefill", "tc_nf4_m64", "qmoe",
