@@ -177,7 +177,12 @@ size_t qgemm_workspace_bytes(int a_dtype, int M, int N, int K, int bits, int blo
  *   block_size   32, 64, 128 or 256; hidden and inter multiples of it
  *   y_f16        [hidden] fp16 output
  *   status_dev   device int written with 0 (all ids valid) or 1, or NULL
- *   workspace    at least qmoe_decode_workspace_bytes(k, hidden, inter)
+ *   workspace    at least qmoe_decode_workspace_bytes(k, hidden, inter) bytes
+ *                of device memory, 16-byte aligned (QG_ERR_INVALID_ARG
+ *                otherwise): the fc1 output g [k][2*inter] fp32 first, then,
+ *                at the next multiple of 256 bytes, the slot outputs o
+ *                [k][hidden] fp32.  Needs no initial contents; the call
+ *                overwrites it.
  */
 int qmoe_decode_fused(const uint16_t *x_f16, const int32_t *expert_ids, const float *expert_weights, int k,
                       int num_experts, const uint8_t *fc1_w, const uint16_t *fc1_scales, const uint16_t *fc1_zp,

@@ -37,13 +37,14 @@ def _dev_case(d):
                 fc2_bias=h(d["fc2_bias"]))
 
 
-def _run(qg, d, T, interleaved=0, status=None):
+def _run(qg, d, T, interleaved=0, status=None, workspace=None):
     t = torch()
     y = t.full((d["hidden"],), float("nan"), dtype=t.float16, device="cuda")
     qg.qmoe_decode_fused(T["x"], T["ids"], T["weights"], num_experts=d["num_experts"], fc1_w=T["fc1_w"],
                          fc1_scales=T["fc1_scales"], fc1_zp=T["fc1_zp"], fc1_bias=T["fc1_bias"], fc2_w=T["fc2_w"],
                          fc2_scales=T["fc2_scales"], fc2_zp=T["fc2_zp"], fc2_bias=T["fc2_bias"], bits=d["bits"],
-                         block_size=d["block_size"], y=y, swiglu_interleaved=interleaved, status=status)
+                         block_size=d["block_size"], y=y, swiglu_interleaved=interleaved, status=status,
+                         workspace=workspace)
     t.cuda.synchronize()
     return y
 
@@ -153,3 +154,24 @@ def test_qmoe_out_of_range_id_sets_status_and_adds_nothing(qg):
     status.fill_(-1)
     _run(qg, d, _dev_case(d), status=status)
     assert int(status.item()) == 0
+
+
+@pytest.mark.parametrize("k", [1, 5, 8])
+def test_qmoe_dirty_workspace(qg, k):
+    """The workspace needs no initial contents: a workspace full of 0xA5
+    bytes gives the same bits as a zeroed one, call after call, and every
+    call writes the status."""
+    t = torch()
+    d = WL.qmoe(num_experts=16, k=k, hidden=1024, inter=512, block_size=64, with_zp=True, with_bias=True, seed=20 + k)
+    T = _dev_case(d)
+    nbytes = qg.qmoe_decode_workspace_bytes(k, 1024, 512)
+    y0 = _run(qg, d, T, workspace=t.zeros(nbytes, dtype=t.uint8, device="cuda"))
+    ref, _ = _oracle(d)
+    assert _relerr(y0, ref) <= 5e-3
+    ws = t.full((nbytes,), 0xA5, dtype=t.uint8, device="cuda")
+    status = t.full((1,), -1, dtype=t.int32, device="cuda")
+    for i in range(3):
+        status.fill_(-1)
+        y = _run(qg, d, T, status=status, workspace=ws)
+        assert t.equal(y, y0), i
+        assert int(status.item()) == 0
