@@ -105,9 +105,15 @@ def _torch():
     return torch
 
 
+_DTYPE_CODES = None
+
+
 def _dtype_code(t):
-    torch = _torch()
-    return {torch.float32: QG_F32, torch.float16: QG_F16, torch.bfloat16: QG_BF16}[t.dtype]
+    global _DTYPE_CODES
+    if _DTYPE_CODES is None:
+        torch = _torch()
+        _DTYPE_CODES = {torch.float32: QG_F32, torch.float16: QG_F16, torch.bfloat16: QG_BF16}
+    return _DTYPE_CODES[t.dtype]
 
 
 def _ptr(t):
@@ -126,12 +132,15 @@ def _check(status, where):
     return status
 
 
-def _workspace(nbytes, workspace, device):
+def _workspace(need, workspace, device):
+    """(workspace, its size in bytes): the caller's, else a new one of need()
+    bytes (None when the call needs none); the library checks the size."""
+    if workspace is not None:
+        return workspace, workspace.numel() * workspace.element_size()
+    nbytes = need()
     if nbytes == 0:
-        return workspace, (0 if workspace is None else workspace.numel() * workspace.element_size())
-    if workspace is None:
-        workspace = _torch().empty(nbytes, dtype=_torch().uint8, device=device)
-    return workspace, workspace.numel() * workspace.element_size()
+        return None, 0
+    return _torch().empty(nbytes, dtype=_torch().uint8, device=device), nbytes
 
 
 def qgemm_workspace_bytes(a_dtype: int, M: int, N: int, K: int, bits: int, block_size: int) -> int:
@@ -146,7 +155,7 @@ def qgemm_nbits(A, W, scales, zero_points, Y, *, bits, block_size, workspace=Non
     """
     M, K = A.shape
     N = W.shape[0]
-    ws, wsb = _workspace(qgemm_workspace_bytes(_dtype_code(A), M, N, K, bits, block_size), workspace, A.device)
+    ws, wsb = _workspace(lambda: qgemm_workspace_bytes(_dtype_code(A), M, N, K, bits, block_size), workspace, A.device)
     s = lib().qgemm_nbits(_ptr(A), _dtype_code(A), _ptr(W), _ptr(scales), _ptr(zero_points), _ptr(Y),
                           _dtype_code(Y), M, N, K, bits, block_size, _ptr(ws), wsb, _stream(stream))
     return s if raw else _check(s, "qgemm_nbits")
@@ -157,7 +166,7 @@ def qgemm_nbits_uniform_zp(A, W, scales, uniform_zp, Y, *, bits, block_size, wor
     """As qgemm_nbits with every zero point equal to the scalar uniform_zp."""
     M, K = A.shape
     N = W.shape[0]
-    ws, wsb = _workspace(qgemm_workspace_bytes(_dtype_code(A), M, N, K, bits, block_size), workspace, A.device)
+    ws, wsb = _workspace(lambda: qgemm_workspace_bytes(_dtype_code(A), M, N, K, bits, block_size), workspace, A.device)
     s = lib().qgemm_nbits_uniform_zp(_ptr(A), _dtype_code(A), _ptr(W), _ptr(scales), float(uniform_zp), _ptr(Y),
                                      _dtype_code(Y), M, N, K, bits, block_size, _ptr(ws), wsb, _stream(stream))
     return s if raw else _check(s, "qgemm_nbits_uniform_zp")
@@ -167,7 +176,7 @@ def qgemm_codebook4(A, W, codebook, absmax, Y, *, block_size, workspace=None, st
     """Y = A . (codebook[q] * absmax)^T; codebook [16] float32, absmax [N, K/block_size] float32."""
     M, K = A.shape
     N = W.shape[0]
-    ws, wsb = _workspace(qgemm_workspace_bytes(_dtype_code(A), M, N, K, 4, block_size), workspace, A.device)
+    ws, wsb = _workspace(lambda: qgemm_workspace_bytes(_dtype_code(A), M, N, K, 4, block_size), workspace, A.device)
     s = lib().qgemm_codebook4(_ptr(A), _dtype_code(A), _ptr(W), _ptr(codebook), _ptr(absmax), _ptr(Y),
                               _dtype_code(Y), M, N, K, block_size, _ptr(ws), wsb, _stream(stream))
     return s if raw else _check(s, "qgemm_codebook4")
@@ -184,7 +193,7 @@ def qmoe_decode_fused(x, expert_ids, expert_weights, *, num_experts, fc1_w, fc1_
     hidden = x.shape[-1]
     inter = fc2_w.shape[-1] * 8 // bits
     k = expert_ids.numel()
-    ws, wsb = _workspace(qmoe_decode_workspace_bytes(k, hidden, inter), workspace, x.device)
+    ws, wsb = _workspace(lambda: qmoe_decode_workspace_bytes(k, hidden, inter), workspace, x.device)
     s = lib().qmoe_decode_fused(_ptr(x), _ptr(expert_ids), _ptr(expert_weights), k, num_experts, _ptr(fc1_w),
                                 _ptr(fc1_scales), _ptr(fc1_zp), _ptr(fc1_bias), _ptr(fc2_w), _ptr(fc2_scales),
                                 _ptr(fc2_zp), _ptr(fc2_bias), hidden, inter, bits, block_size,
@@ -199,7 +208,7 @@ def qmoe_decode_fused_dp4a(x, expert_ids, expert_weights, *, num_experts, fc1_w,
     hidden = x.shape[-1]
     inter = fc2_w.shape[-1] * 8 // bits
     k = expert_ids.numel()
-    ws, wsb = _workspace(qmoe_decode_workspace_bytes(k, hidden, inter), workspace, x.device)
+    ws, wsb = _workspace(lambda: qmoe_decode_workspace_bytes(k, hidden, inter), workspace, x.device)
     s = lib().qmoe_decode_fused_dp4a(_ptr(x), _ptr(expert_ids), _ptr(expert_weights), k, num_experts, _ptr(fc1_w),
                                      _ptr(fc1_scales), _ptr(fc1_zp), _ptr(fc1_bias), _ptr(fc2_w), _ptr(fc2_scales),
                                      _ptr(fc2_zp), _ptr(fc2_bias), hidden, inter, bits, block_size,
@@ -265,7 +274,7 @@ def qgemm_codebook4_nested(A, W, codebook, absmax_q, absmax_table, absmax2, absm
     (absmax_q [N, K/block_size] uint8, absmax_table [256] float32, absmax2 float32)."""
     M, K = A.shape
     N = W.shape[0]
-    ws, wsb = _workspace(qgemm_codebook4_nested_workspace_bytes(_dtype_code(A), M, N, K, block_size), workspace,
+    ws, wsb = _workspace(lambda: qgemm_codebook4_nested_workspace_bytes(_dtype_code(A), M, N, K, block_size), workspace,
                          A.device)
     s = lib().qgemm_codebook4_nested(_ptr(A), _dtype_code(A), _ptr(W), _ptr(codebook), _ptr(absmax_q),
                                      _ptr(absmax_table), _ptr(absmax2), float(absmax_offset), nested_block, _ptr(Y),
@@ -296,7 +305,7 @@ def qmoe_ragged_mm(X, offsets, W, scales, zero_points, Y, *, bits, block_size, w
     off, p = _host_offsets(offsets)
     E, N = W.shape[0], W.shape[1]
     K = X.shape[1]
-    ws, wsb = _workspace(lib().qmoe_ragged_mm_workspace_bytes(_dtype_code(X), p, E, N, K, bits, block_size),
+    ws, wsb = _workspace(lambda: lib().qmoe_ragged_mm_workspace_bytes(_dtype_code(X), p, E, N, K, bits, block_size),
                          workspace, X.device)
     s = lib().qmoe_ragged_mm(_ptr(X), _dtype_code(X), p, E, _ptr(W), _ptr(scales), _ptr(zero_points), _ptr(Y),
                              _dtype_code(Y), N, K, bits, block_size, _ptr(ws), wsb, _stream(stream))
