@@ -87,6 +87,8 @@ def load(path: str | None = None):
         lib.oracle_qmoe_ragged_mm.restype = I
         lib.oracle_nested_absmax.argtypes = [P, P, P, F, I, I64, P]
         lib.oracle_nested_absmax.restype = None
+        lib.oracle_unpack_zero_points.argtypes = [P, I64, I64, I, P]
+        lib.oracle_unpack_zero_points.restype = None
         if path is None:
             _lib = lib
         return lib
@@ -165,6 +167,30 @@ def qgemm_nbits(A, W, scales, zero_points=None, *, M, N, K, bits, block_size, un
                                        float(uniform_zp or 0.0), M, N, K, bits, block_size,
                                        _ptr(rows_a), n_rows, _ptr(Y))
     return Y
+
+
+def zp_packed_row_bytes(nb: int, bits: int) -> int:
+    """Bytes per row of packed integer zero points (rows padded to whole bytes)."""
+    return (nb * bits + 7) // 8
+
+
+def unpack_zero_points(zp_packed, *, N, nb, bits, lib=None):
+    """int32 [N, nb] zero points from their packed form [N, ceil(nb*bits/8)] uint8."""
+    zp = _c(zp_packed, np.uint8)
+    assert zp.size == N * zp_packed_row_bytes(nb, bits)
+    out = np.empty((N, nb), dtype=np.int32)
+    (lib or load()).oracle_unpack_zero_points(_ptr(zp), N, nb, bits, _ptr(out))
+    return out
+
+
+def qgemm_nbits_packed_zp(A, W, scales, zp_packed, *, M, N, K, bits, block_size, a_dtype=None, rows=None,
+                          lib=None):
+    """qgemm_nbits with packed integer zero points: the unpacked integers (exact
+    in fp16) serve as the zero-point tensor."""
+    z = unpack_zero_points(zp_packed, N=N, nb=K // block_size, bits=bits, lib=lib)
+    z16 = z.astype(np.float16).view(np.uint16)
+    return qgemm_nbits(A, W, scales, z16, M=M, N=N, K=K, bits=bits, block_size=block_size, a_dtype=a_dtype,
+                       rows=rows, lib=lib)
 
 
 def qgemm_codebook4(A, W, codebook, absmax, *, M, N, K, block_size, a_dtype=None, rows=None, lib=None):

@@ -43,7 +43,10 @@
  *   - the ragged expert GEMM groups the rows of X by expert through
  *     offsets starting at 0;
  *   - a nested absmax is table[code] * second-level scale + offset over the
- *     flat row-major sequence of per-block values.
+ *     flat row-major sequence of per-block values;
+ *   - packed unsigned-integer zero points follow the codes' packing rule:
+ *     zero point b of row n is the `bits`-wide field at bit b*bits of the
+ *     row's bit string, a row padding to whole bytes (ceil(nb*bits/8)).
  *
  * Parity pins: every function here is pinned by CPU tests against values
  * written by hand from the pages' statement of the problem, closed forms,
@@ -562,5 +565,30 @@ void oracle_nested_absmax(const uint8_t *qa, const float *table256, const float 
     for (int64_t i = 0; i < n; ++i) {
         float v = table256[qa[i]] * absmax2[i / nested_bs];
         absmax[i] = v + offset;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Packed unsigned-integer zero points.  [P1] Notes for reviewers, kernel    */
+/* unit-test table: MatMulNBits leaves for 2-, 3-, 4- and 8-bit weights; the */
+/* pages' own zero points are fp16 ([P1] What, Commit 1).  Reading: integer  */
+/* zero points may also come packed like the codes -- zero point b of row n  */
+/* is the unsigned `bits`-wide field starting at bit b*bits of row n's bit   */
+/* string (LSB-first, a field may continue into the next byte), each row     */
+/* occupying ceil(nb*bits/8) bytes.  The GEMM is then the zero-point-tensor  */
+/* GEMM with these integers as zero points (exact in fp16 for bits <= 8).    */
+/* ------------------------------------------------------------------------ */
+void oracle_unpack_zero_points(const uint8_t *zp, int64_t N, int64_t nb, int bits, int32_t *out)
+{
+    int64_t row_bytes = (nb * bits + 7) / 8;
+    for (int64_t n = 0; n < N; ++n) {
+        const uint8_t *row = zp + n * row_bytes;
+        for (int64_t b = 0; b < nb; ++b) {
+            int64_t bit = b * bits;
+            unsigned v = row[bit / 8];
+            if (bit % 8 + bits > 8) /* the field continues into the next byte */
+                v |= (unsigned)row[bit / 8 + 1] << 8;
+            out[n * nb + b] = (int32_t)((v >> (bit % 8)) & ((1u << bits) - 1u));
+        }
     }
 }

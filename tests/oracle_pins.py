@@ -613,6 +613,59 @@ def check_nested_reduces_to_plain(lib):
     assert np.array_equal(got.reshape(-1).astype(np.float64), flat)
 
 
+def check_golden_packed_zp(lib):
+    g = _golden("packed_zp_handworked.json")
+    for c in g["unpack"]:
+        got = O.unpack_zero_points(np.array(c["bytes"], dtype=np.uint8), N=c["N"], nb=c["nb"], bits=c["bits"], lib=lib)
+        assert got.reshape(-1).tolist() == c["zero_points"], (c["bits"], got.tolist())
+    e = g["gemm"]
+    y = O.qgemm_nbits_packed_zp(np.array(e["A"], dtype=np.float32).reshape(e["M"], e["K"]),
+                                np.array(e["W"], dtype=np.uint8).reshape(e["N"], -1),
+                                np.array(e["scales_f16"], dtype=np.uint16).reshape(e["N"], -1),
+                                np.array(e["zp_packed"], dtype=np.uint8).reshape(e["N"], -1), M=e["M"], N=e["N"],
+                                K=e["K"], bits=e["bits"], block_size=e["block_size"], lib=lib)
+    assert y.reshape(-1).tolist() == e["Y"], y
+
+
+def _pack_fields(z, bits):
+    """Pack an [N, nb] integer array bit by bit: field b of a row at bits
+    b*bits .. b*bits+bits-1 of the row's bit string, rows padded to bytes."""
+    N, nb = z.shape
+    nbytes = (nb * bits + 7) // 8
+    out = np.zeros((N, nbytes), dtype=np.uint8)
+    for n in range(N):
+        bitlist = []
+        for b in range(nb):
+            bitlist += [(int(z[n, b]) >> t) & 1 for t in range(bits)]
+        bitlist += [0] * (8 * nbytes - len(bitlist))
+        for i in range(nbytes):
+            out[n, i] = sum(bitlist[8 * i + t] << t for t in range(8))
+    return out
+
+
+def check_packed_zp_roundtrip_and_reduction(lib):
+    """Unpacking inverts a bit-by-bit packer (odd field counts, fields that
+    straddle bytes, padded rows), and the packed-zero-point GEMM equals the
+    (pinned) zero-point-tensor GEMM on the same integers."""
+    rng = np.random.default_rng(53)
+    for bits in (2, 3, 4, 8):
+        for nb in (1, 3, 7, 90):
+            z = rng.integers(0, 1 << bits, size=(5, nb))
+            got = O.unpack_zero_points(_pack_fields(z, bits), N=5, nb=nb, bits=bits, lib=lib)
+            assert np.array_equal(got, z), (bits, nb)
+    for bits, bs in ((2, 64), (3, 32), (4, 32), (8, 128)):
+        M, N, K = 3, 29, 256
+        nb = K // bs
+        W = rng.integers(0, 256, size=(N, K * bits // 8), dtype=np.uint8)
+        S = rng.uniform(0.01, 0.05, size=(N, nb)).astype(np.float16).view(np.uint16)
+        z = rng.integers(0, 1 << bits, size=(N, nb))
+        A = rng.standard_normal((M, K)).astype(np.float32)
+        y = O.qgemm_nbits_packed_zp(A, W, S, _pack_fields(z, bits), M=M, N=N, K=K, bits=bits, block_size=bs, lib=lib)
+        ref = O.qgemm_nbits(A, W, S, z.astype(np.float16).view(np.uint16), M=M, N=N, K=K, bits=bits, block_size=bs,
+                            lib=lib)
+        assert np.array_equal(y, ref), bits
+
+
 ALL_CHECKS = [
     check_half_decode, check_bf16_decode, check_unpack_vs_unpackbits, check_golden_u2, check_golden_u3, check_golden_u4, check_golden_u8,
     check_golden_codebook, check_golden_qmoe, check_onehot, check_uniform_vs_tensor, check_closed_form,
@@ -621,4 +674,5 @@ ALL_CHECKS = [
     check_golden_i8_quant, check_i8_quant_properties, check_qmoe_dp4a_chain,
     check_golden_ragged, check_ragged_vs_per_expert, check_ragged_bad_offsets,
     check_golden_nested_absmax, check_nested_reduces_to_plain,
+    check_golden_packed_zp, check_packed_zp_roundtrip_and_reduction,
 ]

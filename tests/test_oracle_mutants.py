@@ -67,6 +67,11 @@ MUTANTS = {
     "nested_offset_dropped": ("absmax[i] = v + offset;", "absmax[i] = v;"),
     "nested_scale_index": ("absmax2[i / nested_bs]", "absmax2[i % nested_bs]"),
     "nested_table_reversed": ("table256[qa[i]]", "table256[255 - qa[i]]"),
+    "packed_zp_rows_unpadded": ("int64_t row_bytes = (nb * bits + 7) / 8;", "int64_t row_bytes = nb * bits / 8;"),
+    "packed_zp_straddle_dropped": ("if (bit % 8 + bits > 8) /* the field continues into the next byte */\n"
+                                   "                v |= (unsigned)row[bit / 8 + 1] << 8;", ""),
+    "packed_zp_msb_first": ("out[n * nb + b] = (int32_t)((v >> (bit % 8))",
+                            "out[n * nb + b] = (int32_t)((v >> ((8 - bits - bit % 8) & 7))"),
 }
 
 
