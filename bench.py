@@ -597,6 +597,34 @@ def run_suite(only=None):
             emit("phi4_u8_%s_m1" % shape, us, nbytes=wb)
             del Ws
 
+    # u4 block 32 with packed integer zero points, and the same GEMV with an fp16 zero-point tensor
+    if want("packed_zp"):
+        for shape in ("qkv", "lm_head"):
+            N, K = WL.PHI4_SHAPES[shape]
+            d = WL.packed_zp(N, K, M=1, bits=4, block_size=32)
+            z16 = WL.fp16_uniform_int(WL.rng(1), (N, K // 32), 0, 15)
+            A = torch.from_numpy(d["A"]).to(dev)
+            Y = torch.empty(1, N, device=dev)
+            for packed in (True, False):
+                zb = d["zp_packed"] if packed else z16
+                wb = d["W"].nbytes + d["scales"].nbytes + zb.nbytes
+                r = reps_for(wb)
+                Ws = [torch.from_numpy(d["W"]).to(dev) for _ in range(r)]
+                Ss = [t16(d["scales"], torch.float16) for _ in range(r)]
+                Zs = [torch.from_numpy(zb).to(dev) if packed else t16(zb, torch.float16) for _ in range(r)]
+                if packed:
+                    ws = torch.empty(max(16, qg.qgemm_nbits_packed_zp_workspace_bytes(0, 1, N, K, 4, 32)),
+                                     dtype=torch.uint8, device=dev)
+                    call = lambda i: qg.qgemm_nbits_packed_zp(A, Ws[i % r], Ss[i % r], Zs[i % r], Y, bits=4,
+                                                              block_size=32, workspace=ws, stream=st)
+                else:
+                    ws = torch.empty(max(16, qg.qgemm_workspace_bytes(0, 1, N, K, 4, 32)), dtype=torch.uint8,
+                                     device=dev)
+                    call = lambda i: qg.qgemm_nbits(A, Ws[i % r], Ss[i % r], Zs[i % r], Y, bits=4, block_size=32,
+                                                    workspace=ws, stream=st)
+                emit("u4_bs32_%s_zp_%s_m1" % ("packed" if packed else "fp16", shape), timed(call, 2 * r), nbytes=wb)
+                del Ws, Ss, Zs
+
     # NF4 codebook, bf16 activations
     if want("nf4"):
         for shape in ("square", "gqa_kv", "up", "down"):
@@ -847,8 +875,8 @@ def main():
                     help="run a small fixed workload for a profiler capture instead of the benchmark")
     ap.add_argument("--suite", action="store_true",
                     help="time every configuration (one JSON line each) instead of the benchmark")
-    ap.add_argument("--only", choices=["tiny_u4", "phi4_u2", "phi4_u8", "nf4", "qmoe", "prefill", "ragged", "gather",
-                                       "nsweep"],
+    ap.add_argument("--only", choices=["tiny_u4", "phi4_u2", "phi4_u8", "packed_zp", "nf4", "qmoe", "prefill", "ragged",
+                                       "gather", "nsweep"],
                     help="with --suite: time one group of configurations only")
     args = ap.parse_args()
     if args.probe:

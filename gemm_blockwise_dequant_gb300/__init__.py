@@ -25,6 +25,7 @@ __all__ = [
     "qg_dequant_nbits_uniform_zp", "qg_dequant_codebook4", "qg_read_device_fault", "qg_status_string",
     "qgemm_codebook4_nested", "qgemm_codebook4_nested_workspace_bytes", "qmoe_ragged_mm",
     "qmoe_ragged_mm_workspace_bytes", "qg_gather_block_quantized", "QG_WF_U2", "QG_WF_U4", "QG_WF_U8", "QG_WF_E4M3",
+    "qgemm_nbits_packed_zp", "qgemm_nbits_packed_zp_workspace_bytes",
 ]
 
 QG_OK, QG_ERR_INVALID_ARG, QG_ERR_UNSUPPORTED, QG_ERR_CUDA, QG_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3, 4
@@ -73,6 +74,8 @@ _SIGS = {
     "qg_gather_block_quantized": ([_P, ctypes.c_int64, _P, _I, _P, _P, ctypes.c_int64, _I, _I, _P, _I, _P, _P], _I),
     "qgemm_codebook4_nested": ([_P, _I, _P, _P, _P, _P, _P, _F, _I, _P, _I, _I, _I, _I, _I, _P, _SZ, _P], _I),
     "qgemm_codebook4_nested_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
+    "qgemm_nbits_packed_zp": ([_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P], _I),
+    "qgemm_nbits_packed_zp_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _SZ),
     "qmoe_ragged_mm": ([_P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P], _I),
     "qmoe_ragged_mm_workspace_bytes": ([_I, _P, _I, _I, _I, _I, _I], _SZ),
     "qg_read_device_fault": ([_P], _I),
@@ -280,6 +283,25 @@ def qgemm_codebook4_nested(A, W, codebook, absmax_q, absmax_table, absmax2, absm
                                      _ptr(absmax_table), _ptr(absmax2), float(absmax_offset), nested_block, _ptr(Y),
                                      _dtype_code(Y), M, N, K, block_size, _ptr(ws), wsb, _stream(stream))
     return s if raw else _check(s, "qgemm_codebook4_nested")
+
+
+def qgemm_nbits_packed_zp_workspace_bytes(a_dtype: int, M: int, N: int, K: int, bits: int, block_size: int) -> int:
+    return lib().qgemm_nbits_packed_zp_workspace_bytes(a_dtype, M, N, K, bits, block_size)
+
+
+def qgemm_nbits_packed_zp(A, W, scales, zero_points_packed, Y, *, bits, block_size, workspace=None, stream=None,
+                          raw=False):
+    """qgemm_nbits with unsigned integer zero points packed like the codes:
+    zero_points_packed [N, ceil((K/block_size)*bits/8)] uint8, field b of a row
+    at bit b*bits, least significant bit first."""
+    M, K = A.shape
+    N = W.shape[0]
+    ws, wsb = _workspace(lambda: qgemm_nbits_packed_zp_workspace_bytes(_dtype_code(A), M, N, K, bits, block_size),
+                         workspace, A.device)
+    s = lib().qgemm_nbits_packed_zp(_ptr(A), _dtype_code(A), _ptr(W), _ptr(scales), _ptr(zero_points_packed),
+                                    _ptr(Y), _dtype_code(Y), M, N, K, bits, block_size, _ptr(ws), wsb,
+                                    _stream(stream))
+    return s if raw else _check(s, "qgemm_nbits_packed_zp")
 
 
 def _host_offsets(offsets):

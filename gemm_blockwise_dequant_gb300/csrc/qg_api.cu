@@ -374,6 +374,63 @@ size_t qgemm_workspace_bytes(int a_dtype, int M, int N, int K, int bits, int blo
     return gemm_workspace(a_dtype, M, N, K, bits, block_size);
 }
 
+size_t qgemm_nbits_packed_zp_workspace_bytes(int a_dtype, int M, int N, int K, int bits, int block_size) {
+    if (M <= 0 || N <= 0 || K <= 0 || !valid_bits(bits) || !valid_bs(block_size) || K % block_size) return 0;
+    const size_t expanded = (static_cast<size_t>(N) * (K / block_size) * sizeof(uint16_t) + 255) / 256 * 256;
+    return expanded + gemm_workspace(a_dtype, M, N, K, bits, block_size);
+}
+
+int qgemm_nbits_packed_zp(const void *A, int a_dtype, const uint8_t *W, const uint16_t *scales_f16,
+                          const uint8_t *zero_points_packed, void *Y, int y_dtype, int M, int N, int K, int bits,
+                          int block_size, void *workspace, size_t workspace_bytes, qg_stream_t stream) {
+    (void)cudaGetLastError();
+    if (!valid_dtype(a_dtype) || !valid_dtype(y_dtype) || M < 0 || N < 0 || K < 0) return QG_ERR_INVALID_ARG;
+    if (!valid_bits(bits) || !valid_bs(block_size)) return QG_ERR_UNSUPPORTED;
+    if (K % block_size) return QG_ERR_INVALID_ARG;
+    if (M > kMaxM || N > kMaxN || K > kMaxK) return QG_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return QG_OK;
+    if (!Y) return QG_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        GemmProblem z{};
+        z.Y = Y;
+        z.y_dtype = y_dtype;
+        z.M = M;
+        z.N = N;
+        return run_gemm(z, nullptr, 0, s);  // an empty sum: zeros
+    }
+    if (!zero_points_packed) return QG_ERR_INVALID_ARG;
+    const size_t need = qgemm_nbits_packed_zp_workspace_bytes(a_dtype, M, N, K, bits, block_size);
+    if (!workspace || workspace_bytes < need) return QG_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(workspace)) return QG_ERR_INVALID_ARG;
+    const int nb = K / block_size;
+    const size_t expanded = (static_cast<size_t>(N) * nb * sizeof(uint16_t) + 255) / 256 * 256;
+    uint16_t *zp16 = static_cast<uint16_t *>(workspace);
+    void *gws = static_cast<char *>(workspace) + expanded;
+    const size_t gws_bytes = workspace_bytes - expanded;
+    // everything qgemm_nbits checks, before anything is enqueued
+    const int st = check_gemm(A, a_dtype, W, scales_f16, zp16, Y, y_dtype, M, N, K, bits, block_size, gws, gws_bytes);
+    if (st != QG_OK) return st;
+    if (qg::launch_unpack_zero_points(zero_points_packed, bits, N, nb, zp16, s) != cudaSuccess) return QG_ERR_CUDA;
+    GemmProblem p{};
+    p.A = A;
+    p.a_dtype = a_dtype;
+    p.W = W;
+    p.kind = qg::WK_NBITS;
+    p.scales = scales_f16;
+    p.zp = zp16;
+    p.zp_mode = qg::ZP_TENSOR;
+    p.Y = Y;
+    p.y_dtype = y_dtype;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.bits = bits;
+    p.bs = block_size;
+    p.params_from_device = 1;  // the zero points are written by the launch above
+    return run_gemm(p, gws, gws_bytes, s);
+}
+
 int qmoe_decode_fused(const uint16_t *x_f16, const int32_t *expert_ids, const float *expert_weights, int k,
                       int num_experts, const uint8_t *fc1_w, const uint16_t *fc1_scales, const uint16_t *fc1_zp,
                       const uint16_t *fc1_bias, const uint8_t *fc2_w, const uint16_t *fc2_scales,

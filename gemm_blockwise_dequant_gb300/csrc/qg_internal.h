@@ -115,5 +115,6 @@ cudaError_t launch_dequant(const GemmProblem &p, float *out, cudaStream_t s);
 cudaError_t launch_uniform_check(const uint16_t *t, size_t n, unsigned *ws, cudaStream_t s);
 cudaError_t launch_nested_absmax(const uint8_t *qa, const float *table, const float *absmax2, float offset,
                                  int nested, size_t n, float *out, cudaStream_t s);
+cudaError_t launch_unpack_zero_points(const uint8_t *zp, int bits, int N, int nb, uint16_t *out, cudaStream_t s);
 
 }  // namespace qg

@@ -70,6 +70,49 @@ __global__ void dequant_u3_kernel(const uint8_t *__restrict__ W, const uint16_t 
     }
 }
 
+// Packed unsigned-integer zero points -> fp16 [N][nb]: zero point b of row n
+// is the `bits`-wide field at bit b*bits of row n's bit string (least
+// significant bit first, the codes' own packing rule; a field may continue
+// into the next byte), rows padded to row_bytes = ceil(nb*bits/8).  The
+// integers (at most 255) are exact in fp16.
+__global__ void unpack_zero_points_kernel(const uint8_t *__restrict__ zp, int bits, int nb, int row_bytes,
+                                          size_t total, uint16_t *__restrict__ out) {
+    for (size_t t = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; t < total;
+         t += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const size_t n = t / nb;
+        const int b = static_cast<int>(t - n * nb);
+        const int bit = b * bits;
+        const uint8_t *row = zp + n * row_bytes;
+        uint32_t v = __ldg(row + bit / 8);
+        if (bit % 8 + bits > 8) v |= static_cast<uint32_t>(__ldg(row + bit / 8 + 1)) << 8;
+        const unsigned q = (v >> (bit % 8)) & ((1u << bits) - 1u);
+        out[t] = __half_as_ushort(__uint2half_rn(q));
+    }
+}
+
+// The same when rows need no padding (nb*bits a multiple of 8) and bits is
+// 2, 4 or 8: the packed bytes form one flat stream, byte i holding zero points
+// i*8/bits onwards; one thread per byte, one store of its 8/bits values.
+template <int BITS>
+__global__ void unpack_zero_points_flat_kernel(const uint8_t *__restrict__ zp, size_t nbytes,
+                                               uint16_t *__restrict__ out) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < nbytes;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const unsigned v = __ldg(zp + i);
+        if constexpr (BITS == 8) {
+            out[i] = __half_as_ushort(__uint2half_rn(v));
+        } else if constexpr (BITS == 4) {
+            const uint32_t lo = __half_as_ushort(__uint2half_rn(v & 15u)), hi = __half_as_ushort(__uint2half_rn(v >> 4));
+            reinterpret_cast<uint32_t *>(out)[i] = lo | (hi << 16);
+        } else {
+            uint32_t h[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) h[j] = __half_as_ushort(__uint2half_rn((v >> (2 * j)) & 3u));
+            reinterpret_cast<uint2 *>(out)[i] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+        }
+    }
+}
+
 // Nested absmax: absmax[i] = (table[qa[i]] * absmax2[i / nested]) + offset,
 // two fp32 round-to-nearest operations (bitsandbytes #1979 "Testing plan":
 // nested / non-nested absmax; the layout is this library's reading).
@@ -140,6 +183,23 @@ cudaError_t launch_nested_absmax(const uint8_t *qa, const float *table, const fl
     const int threads = 256;
     const int blocks = static_cast<int>(std::min<size_t>((n + threads - 1) / threads, 4096));
     nested_absmax_kernel<<<blocks, threads, 0, s>>>(qa, table, absmax2, offset, nested, n, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unpack_zero_points(const uint8_t *zp, int bits, int N, int nb, uint16_t *out, cudaStream_t s) {
+    const size_t total = static_cast<size_t>(N) * nb;
+    if (total == 0) return cudaSuccess;
+    const int threads = 256;
+    if ((static_cast<size_t>(nb) * bits) % 8 == 0 && bits != 3) {  // out is 16-byte aligned (workspace front)
+        const size_t nbytes = total * bits / 8;
+        const int blocks = static_cast<int>(std::min<size_t>((nbytes + threads - 1) / threads, 65536));
+        if (bits == 8) unpack_zero_points_flat_kernel<8><<<blocks, threads, 0, s>>>(zp, nbytes, out);
+        else if (bits == 4) unpack_zero_points_flat_kernel<4><<<blocks, threads, 0, s>>>(zp, nbytes, out);
+        else unpack_zero_points_flat_kernel<2><<<blocks, threads, 0, s>>>(zp, nbytes, out);
+        return cudaGetLastError();
+    }
+    const int blocks = static_cast<int>(std::min<size_t>((total + threads - 1) / threads, 4096));
+    unpack_zero_points_kernel<<<blocks, threads, 0, s>>>(zp, bits, nb, (nb * bits + 7) / 8, total, out);
     return cudaGetLastError();
 }
 

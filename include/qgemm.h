@@ -294,6 +294,31 @@ int qgemm_codebook4_nested(const void *A, int a_dtype, const uint8_t *W, const f
 size_t qgemm_codebook4_nested_workspace_bytes(int a_dtype, int M, int N, int K, int block_size);
 
 /*
+ * qgemm_nbits_packed_zp -- qgemm_nbits with unsigned integer zero points
+ * packed like the codes.  [hip-ep #1318] "Notes for reviewers", kernel test
+ * table (the 2-, 3-, 4- and 8-bit MatMulNBits leaves); the pages' own zero
+ * points are fp16 ("What", Commit 1) and they describe no packed form, so the
+ * layout is this library's reading: zero point b of row n is the unsigned
+ * `bits`-wide field starting at bit b*bits of row n's bit string, least
+ * significant bit first (a field may continue into the next byte), each row
+ * occupying ceil((K/block_size)*bits/8) bytes.
+ *
+ *   zero_points_packed  [N][ceil((K/block_size)*bits/8)] uint8 (device, any
+ *                alignment; NULL: QG_ERR_INVALID_ARG)
+ *   Other arguments as qgemm_nbits.  The zero points are widened to fp16
+ *   [N][K/block_size] at the front of the workspace (at least
+ *   qgemm_nbits_packed_zp_workspace_bytes() bytes, 16-byte aligned) by one
+ *   small kernel, then the call runs exactly as qgemm_nbits with that
+ *   zero-point tensor: the result is bit-identical to qgemm_nbits given the
+ *   same integers as fp16.  Every check of qgemm_nbits happens before
+ *   anything is enqueued.
+ */
+int qgemm_nbits_packed_zp(const void *A, int a_dtype, const uint8_t *W, const uint16_t *scales_f16,
+                          const uint8_t *zero_points_packed, void *Y, int y_dtype, int M, int N, int K, int bits,
+                          int block_size, void *workspace, size_t workspace_bytes, qg_stream_t stream);
+size_t qgemm_nbits_packed_zp_workspace_bytes(int a_dtype, int M, int N, int K, int bits, int block_size);
+
+/*
  * qmoe_ragged_mm -- ragged expert GEMM: the rows of X are grouped by expert
  * and each group is multiplied by its expert's MatMulNBits weight.
  * [hip-ep #1318] kernel test table, qmoe_ragged_mm leaf Xfp16_Wu4_Yfp16; the

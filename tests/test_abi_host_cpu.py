@@ -93,3 +93,19 @@ def test_three_bit_codes_are_accepted_widths(L):
     # bits 5 is refused, 3 passes the width check (and then fails on the zero-sized problem as OK)
     assert L.qgemm_nbits(P16, 0, P16, P16, None, P16, 0, 1, 64, 64, 5, 32, None, 0, None) == qg.QG_ERR_UNSUPPORTED
     assert L.qgemm_nbits(P16, 0, P16, P16, None, P16, 0, 0, 64, 64, 3, 32, None, 0, None) == qg.QG_OK
+
+
+def test_packed_zp_refusals(L):
+    call = lambda zp=P16, M=1, K=256, bits=4, bs=64, a=0, y=0, ws=None, wsb=0: L.qgemm_nbits_packed_zp(
+        P16, a, P16, P16, zp, P16, y, M, 64, K, bits, bs, ws, wsb, None)
+    assert call(a=9) == qg.QG_ERR_INVALID_ARG
+    assert call(y=7) == qg.QG_ERR_INVALID_ARG
+    assert call(M=-1) == qg.QG_ERR_INVALID_ARG
+    assert call(bits=5) == qg.QG_ERR_UNSUPPORTED
+    assert call(bs=48) == qg.QG_ERR_UNSUPPORTED
+    assert call(K=250, bs=32) == qg.QG_ERR_INVALID_ARG  # K % block_size
+    assert call(zp=None) == qg.QG_ERR_INVALID_ARG
+    assert call(ws=None, wsb=0) == qg.QG_ERR_WORKSPACE_TOO_SMALL
+    assert call(M=0) == qg.QG_OK
+    assert L.qgemm_nbits_packed_zp_workspace_bytes(0, 1, 64, 256, 4, 48) == 0
+    assert L.qgemm_nbits_packed_zp_workspace_bytes(0, 1, 64, 256, 5, 64) == 0

@@ -169,6 +169,22 @@ def phi4_u2(shape: str, M: int = 1, seed: int = 0, full_zp_tensor: bool = False)
                 uniform_zp=1.5, A=A, a_dtype=F32)
 
 
+def packed_zp(N: int, K: int, M: int = 1, bits: int = 4, block_size: int = 32, a_dtype: int = F32,
+              seed: int = 0, scale_range=(0.005, 0.02)) -> dict:
+    """MatMulNBits with packed unsigned-integer zero points: codes uniform,
+    fp16 scales U(scale_range), zero points as uniform random bytes
+    [N, ceil(nb*bits/8)] (uniform fields; any pad bits random too), A ~ N(0,1)
+    in a_dtype."""
+    g = rng(seed)
+    nb = K // block_size
+    W = packed_codes(g, N, K, bits)
+    scales = fp16_uniform(g, (N, nb), *scale_range)
+    zp_packed = g.integers(0, 256, size=(N, (nb * bits + 7) // 8), dtype=np.uint8)
+    A = activations(g, M, K, a_dtype)
+    return dict(M=M, N=N, K=K, bits=bits, block_size=block_size, W=W, scales=scales, zp_packed=zp_packed, A=A,
+                a_dtype=a_dtype)
+
+
 def nf4(shape: str, M: int, a_dtype: int, seed: int = 0) -> dict:
     """NF4-style codebook GEMM: 4-bit codes uniform, fp32 absmax per 64-element
     block U(0.02, 0.1), 16-entry normal-quantile codebook, A ~ N(0,1) in bf16
