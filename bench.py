@@ -15,7 +15,7 @@ Cold weights: every step reads a different replica of all five weight sets;
 the replicas total more than three times the 129 MB L2, so no step finds its
 weights in L2 (the rotation the pages use for cold timing).
 
---impl reference times the CPU oracle (the reference arm of this build) on a
+--impl reference times the CPU oracle (the reference arm of the benchmark) on a
 bounded sample of the same workload.
 """
 from __future__ import annotations
