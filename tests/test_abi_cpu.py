@@ -92,3 +92,13 @@ def test_workload_phi4_shapes():
     assert W.PHI4_SHAPES["lm_head"] == (100352, 5120)
     d = W.phi4_u2("o", M=4)
     assert d["W"].shape == (5120, 5120 // 4) and d["scales"].shape == (5120, 80) and d["A"].shape == (4, 5120)
+
+
+def test_workload_packed_zero_points_shapes():
+    import workloads as W
+
+    for bits, nb in ((2, 7), (3, 7), (4, 160), (8, 2)):
+        d = W.packed_zp(5, nb * 32, M=2, bits=bits, block_size=32, seed=1)
+        assert d["zp_packed"].shape == (5, (nb * bits + 7) // 8) and d["zp_packed"].dtype == np.uint8
+        assert d["W"].shape == (5, nb * 32 * bits // 8) and d["scales"].shape == (5, nb) and d["A"].shape == (2, nb * 32)
+    assert np.array_equal(W.packed_zp(4, 64, seed=3)["zp_packed"], W.packed_zp(4, 64, seed=3)["zp_packed"])
