@@ -26,10 +26,12 @@
 //    the four warps cover the four tensor-memory sub-partitions) and write Y.
 //  * Dequantization of u2/u4 codes uses the fp16 magic-number form: one LOP3
 //    turns two codes into an fp16 pair 1024 + c*q, an HFMA2 removes the
-//    offset exactly, then the zero point and the scale are applied with
-//    packed fp16 arithmetic (the weight is rounded to 16 bits, as the MMA
-//    needs).  Codebook weights use a per-lane replicated table in shared
-//    memory and fp32 products rounded to the activation type.
+//    offset exactly.  For fp16 activations the zero point and the scale are
+//    then applied with packed fp16 arithmetic (one rounding to fp16 of the
+//    exact product); for bf16 activations the fp32 weight (q - zp) * s is
+//    formed as the plain definition forms it and rounded once to bf16.
+//    Codebook weights use a per-lane replicated table in shared memory and
+//    fp32 products rounded once to the activation type.
 //  * Every wait is bounded; a stuck pipeline records a fault bit and the CTA
 //    still releases its tensor memory and exits.
 #include <cuda.h>
@@ -180,23 +182,39 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
-// Convert an fp16 pair to the MMA operand type (identity for fp16).
+// Block parameters of one 8-weight unit: fp16 pairs for the fp16 operand,
+// fp32 values for the bf16 operand.
+struct UnitPar {
+    __half2 zp2, s2;  // fp16 operand
+    float zpf, sf;    // bf16 operand
+};
+
+// One operand pair from two exact integer codes q (an fp16 pair).
+//  fp16: (q - zp) * s with packed fp16 arithmetic.  For the integer and
+//        half-integer zero points of the workloads q - zp is exact, so the
+//        pair is the single fp16 rounding of the exact product.
+//  bf16: the fp32 weight fl32(fl32(q - zp) * s) (two fp32 round-to-nearest
+//        operations, no contraction), then one round-to-nearest to bf16.  No
+//        fp16 intermediate, so products beyond fp16's range or below its
+//        normal range keep bf16's.
 template <bool BF16>
-__device__ __forceinline__ uint32_t to_operand(__half2 h) {
+__device__ __forceinline__ uint32_t operand_pair(__half2 q, const UnitPar &u) {
     if constexpr (BF16) {
-        const float2 f = __half22float2(h);
-        const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+        const float2 qf = __half22float2(q);
+        const float w0 = __fmul_rn(__fsub_rn(qf.x, u.zpf), u.sf);
+        const float w1 = __fmul_rn(__fsub_rn(qf.y, u.zpf), u.sf);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(w0, w1);
         return *reinterpret_cast<const uint32_t *>(&b);
     } else {
-        return h2_as_u32(h);
+        return h2_as_u32(__hmul2(__hsub2(q, u.zp2), u.s2));
     }
 }
 
 // 8 weights (k = 8c .. 8c+7 of one row) from their packed codes, as four
-// operand pairs.  nbits: w = (q - zp) * s in fp16 (zp2, s2: fp16 pairs).
+// operand pairs: the codes are first turned into exact fp16 integers, then
+// operand_pair applies the zero point and the scale.
 template <int BITS, bool BF16>
-__device__ __forceinline__ uint4 dequant8_nbits(uint32_t codes, uint32_t codes_hi, uint32_t zp2u, uint32_t s2u) {
-    const __half2 zp2 = u32_as_h2(zp2u), s2 = u32_as_h2(s2u);
+__device__ __forceinline__ uint4 dequant8_nbits(uint32_t codes, uint32_t codes_hi, const UnitPar &u) {
     uint32_t out[4];
     if constexpr (BITS == 8) {
         // codes: 8 bytes, one code each; a byte permute puts two codes under the
@@ -206,7 +224,7 @@ __device__ __forceinline__ uint4 dequant8_nbits(uint32_t codes, uint32_t codes_h
             const uint32_t wsrc = j < 2 ? codes : codes_hi;
             const uint32_t h = __byte_perm(wsrc, 0x64646464u, (j & 1) ? 0x4342u : 0x4140u);
             const __half2 q = __hsub2(u32_as_h2(h), __floats2half2_rn(1024.f, 1024.f));
-            out[j] = to_operand<BF16>(__hmul2(__hsub2(q, zp2), s2));
+            out[j] = operand_pair<BF16>(q, u);
         }
     } else if constexpr (BITS == 2) {
         // codes: 16 bits, 8 codes; byte j holds codes 4j .. 4j+3
@@ -217,8 +235,8 @@ __device__ __forceinline__ uint4 dequant8_nbits(uint32_t codes, uint32_t codes_h
             const uint32_t h23 = (v & 0x00C00030u) | 0x64006400u;  // (1024 + 16 q2, 1024 + 64 q3)
             const __half2 q01 = __hfma2(u32_as_h2(h01), __floats2half2_rn(1.f, 0.25f), __floats2half2_rn(-1024.f, -256.f));
             const __half2 q23 = __hfma2(u32_as_h2(h23), __floats2half2_rn(0.0625f, 0.015625f), __floats2half2_rn(-64.f, -16.f));
-            out[2 * j] = to_operand<BF16>(__hmul2(__hsub2(q01, zp2), s2));
-            out[2 * j + 1] = to_operand<BF16>(__hmul2(__hsub2(q23, zp2), s2));
+            out[2 * j] = operand_pair<BF16>(q01, u);
+            out[2 * j + 1] = operand_pair<BF16>(q23, u);
         }
     } else {
         // codes: 32 bits, 8 codes; byte j holds codes 2j, 2j+1
@@ -227,7 +245,7 @@ __device__ __forceinline__ uint4 dequant8_nbits(uint32_t codes, uint32_t codes_h
             const uint32_t v = __byte_perm(codes, 0u, 0x4040u | (j * 0x0101u));
             const uint32_t h = (v & 0x00F0000Fu) | 0x64006400u;  // (1024 + q0, 1024 + 16 q1)
             const __half2 q = __hfma2(u32_as_h2(h), __floats2half2_rn(1.f, 0.0625f), __floats2half2_rn(-1024.f, -64.f));
-            out[j] = to_operand<BF16>(__hmul2(__hsub2(q, zp2), s2));
+            out[j] = operand_pair<BF16>(q, u);
         }
     }
     return make_uint4(out[0], out[1], out[2], out[3]);
@@ -468,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             wdq_off[j] = swz128(r, c);
             par_off[j] = r * kParamBox + ((8 * c) >> p.lbs) * PE;  // block of this chunk within the stage
         }
-        const uint32_t zpu = __half_as_ushort(__float2half_rn(p.zpv)) * 0x10001u;
+        const uint32_t zpu = __half_as_ushort(__float2half_rn(p.zpv)) * 0x10001u;  // fp16 operand: zp as an fp16 pair
         const bool zt = WK == WK_NBITS && p.zp_mode == ZP_TENSOR;
         for (int i = 0; i < nks; ++i) {
             const int b = i & 1, j = i / CS, cslot = j % kCodeSlots;
@@ -504,7 +522,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < UPT; ++j) {
                 uint4 w;
                 if constexpr (WK == WK_NBITS) {
-                    w = dequant8_nbits<BITS, BF16>(codes[j], codes_hi[j], zt ? zv[j] * 0x10001u : zpu, pv[j] * 0x10001u);
+                    UnitPar u;
+                    if constexpr (BF16) {
+                        u.zpf = zt ? h2f(static_cast<uint16_t>(zv[j])) : p.zpv;
+                        u.sf = h2f(static_cast<uint16_t>(pv[j]));
+                    } else {
+                        u.zp2 = u32_as_h2(zt ? zv[j] * 0x10001u : zpu);
+                        u.s2 = u32_as_h2(pv[j] * 0x10001u);
+                    }
+                    w = dequant8_nbits<BITS, BF16>(codes[j], codes_hi[j], u);
                 } else {
                     w = dequant8_codebook<BF16>(codes[j], __uint_as_float(pv[j]), lut_lane);
                 }

@@ -218,17 +218,33 @@ def test_qgemm_codebook4_parity(qg, case):
 
 
 # ------------------------------------------------------------ determinism
-@pytest.mark.parametrize("which", ["tiny_u4", "phi4_qkv_M1", "split_k_M4"])
-def test_129_calls_bit_identical(qg, which):
+# Every configuration repeats bit-identically: 129 calls on the same inputs,
+# each compared with the first, the output refilled with NaN before every call
+# (hip-ep #1328, "Test plan": 129 calls, a distinct shape per process).
+REPEAT_CASES = ["tiny_u4", "phi4_qkv_M1", "phi4_lm_head_M4", "split_k_M4", "nf4_simt_M1", "nf4_simt_M4",
+                "nf4_tc_M16", "nf4_tc_M64", "prefill_gate_up", "prefill_down"]
+
+
+def _repeat_case(qg, which):
+    """(output shape and dtype, call(out)) for one repeat case."""
+    if which.startswith("nf4"):
+        M = int(which.rsplit("_M", 1)[1])
+        ad = BF16 if M in (1, 16) else F16
+        shape = {1: (14336, 4096), 4: (4096, 14336), 16: (4096, 4096), 64: (14336, 4096)}[M]
+        d = WL.nf4(shape, M, ad, seed=M)
+        A, W, C, AM = act_tensor(d["A"], ad), dev(d["W"]), dev(d["codebook"]), dev(d["absmax"])
+        return (M, d["N"], ad), lambda out: qg.qgemm_codebook4(A, W, C, AM, out, block_size=64)
     if which == "tiny_u4":
         d = WL.tiny_u4()
     elif which == "phi4_qkv_M1":
         d = WL.phi4_u2("qkv", M=1)
-    else:
+    elif which == "phi4_lm_head_M4":
+        d = WL.phi4_u2("lm_head", M=4)
+    elif which == "split_k_M4":
         d = _rand_nbits(17, 4, 70, 8192, 2, 64, F32, "uniform")
+    else:
+        d = WL.prefill_u2(which.split("_", 1)[1])
     t = nbits_case(d)
-    Y0 = y_tensor(d["M"], d["N"], F32)
-    Y = y_tensor(d["M"], d["N"], F32)
 
     def call(out):
         if d.get("uniform_zp") is not None:
@@ -238,11 +254,21 @@ def test_129_calls_bit_identical(qg, which):
             qg.qgemm_nbits(t["A"], t["W"], t["scales"], t["zero_points"], out, bits=d["bits"],
                            block_size=d["block_size"])
 
+    return (d["M"], d["N"], F32), call
+
+
+@pytest.mark.parametrize("which", REPEAT_CASES)
+def test_129_calls_bit_identical(qg, which):
+    (M, N, yd), call = _repeat_case(qg, which)
+    Y0 = y_tensor(M, N, yd)
+    Y = y_tensor(M, N, yd)
     call(Y0)
+    torch().cuda.synchronize()
+    assert not torch().isnan(Y0).any()
     for i in range(128):
+        Y.fill_(float("nan"))
         call(Y)
-        if i % 16 == 15 or i == 127:
-            assert torch().equal(Y, Y0), i
+        assert torch().equal(Y, Y0), "call %d differs from call 0" % (i + 1)
     assert qg.qg_read_device_fault() == 0
 
 

@@ -1,9 +1,10 @@
 """GPU parity of the tensor-core path (M >= 9, fp16 / bf16 activations).
 
 The weight is rounded to the activation's 16-bit type before the MMA, so the
-bar is 5e-3 max relative L2 against the oracle's exact fp64 result.  A
-one-hot test pins the operand layout exactly: with A = e_k every output is
-one dequantized weight rounded to fp16.
+bar is 5e-3 max relative L2 against the oracle's exact fp64 result.  One-hot
+tests pin the operand layout and its rounding exactly: with A = e_k every
+output is one dequantized weight rounded once to fp16 (fp16 activations) or
+to bf16 (bf16 activations).
 """
 import numpy as np
 import pytest
@@ -116,6 +117,63 @@ def test_tc_onehot_layout_exact(qg, bits):
     deq = O.dequant_nbits(d["W"], d["scales"], None, N=N, K=K, bits=bits, block_size=bs, uniform_zp=1.5)
     expect = deq[:, ks].T.astype(np.float16).astype(np.float32)
     assert np.array_equal(Y.cpu().numpy(), expect)
+
+
+def _bf16_rn(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 (round to nearest even, torch's conversion) -> float32."""
+    b = WL.bf16_bits_from_f32(np.asarray(x, np.float32)).astype(np.uint32) << 16
+    return b.view(np.float32)
+
+
+def _onehot_bf16(M, K, ks):
+    A = np.zeros((M, K), np.float32)
+    A[np.arange(M), ks] = 1.0
+    return WL.bf16_bits_from_f32(A)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("zp_mode", ["uniform", "tensor", "none"])
+def test_tc_onehot_layout_exact_bf16(qg, bits, zp_mode):
+    """bf16 activations, A = e_k for 16 rows: Y[i, n] = bf16(w[n, k_i]) exactly,
+    where w is the oracle's fp32 dequantized weight -- the tensor-core operand is
+    one round-to-nearest of that fp32 value to bf16 (no fp16 step in between)."""
+    M, N, K, bs = 16, 300, 2048, 64
+    d = _rand(6, M, N, K, bits, bs, BF16, zp_mode)
+    ks = np.array([0, 1, 7, 8, 63, 64, 65, 127, 511, 777, 1024, 1500, 1999, 2040, 2046, 2047])
+    d["A"] = _onehot_bf16(M, K, ks)
+    Y = _run(qg, d, F32)
+    if zp_mode == "uniform":
+        deq = O.dequant_nbits(d["W"], d["scales"], None, N=N, K=K, bits=bits, block_size=bs, uniform_zp=1.5)
+    else:
+        deq = O.dequant_nbits(d["W"], d["scales"], d["zero_points"], N=N, K=K, bits=bits, block_size=bs)
+    expect = _bf16_rn(deq[:, ks].T)
+    assert np.array_equal(Y.cpu().numpy(), expect)
+
+
+@pytest.mark.parametrize("scale_range", [(30000.0, 65000.0), (1e-7, 5e-6)], ids=["beyond_fp16_max", "fp16_subnormal"])
+def test_tc_bf16_weight_range(qg, scale_range):
+    """bf16 activations with 8-bit codes and scales chosen so that (q - zp) * s
+    lies beyond fp16's largest finite value (up to 127 * 65000) or in fp16's
+    subnormal range: bf16 represents both, and the operand must be the single
+    bf16 rounding of the fp32 weight (one-hot pin), and the GEMM must match the
+    oracle at the 16-bit bar."""
+    M, N, K, bs, bits = 16, 256, 1024, 64, 8
+    g = WL.rng(9)
+    d = dict(M=M, N=N, K=K, bits=bits, block_size=bs, a_dtype=BF16)
+    d["W"] = WL.packed_codes(g, N, K, bits)
+    d["scales"] = WL.fp16_uniform(g, (N, K // bs), *scale_range)
+    d["zero_points"] = None
+    d["uniform_zp"] = None
+    ks = np.linspace(0, K - 1, M).astype(np.int64)
+    d["A"] = _onehot_bf16(M, K, ks)
+    Y = _run(qg, d, F32)
+    deq = O.dequant_nbits(d["W"], d["scales"], None, N=N, K=K, bits=bits, block_size=bs)
+    assert np.isfinite(deq).all() and np.abs(deq).max() > (65504.0 if scale_range[0] > 1 else 0.0)
+    assert np.array_equal(Y.cpu().numpy(), _bf16_rn(deq[:, ks].T))
+    # a dense GEMM on the same weights
+    d["A"] = WL.activations(g, M, K, BF16)
+    Y = _run(qg, d, F32)
+    assert O.max_rel_l2(to64(Y), oracle_nbits(d)) <= 5e-3
 
 
 @pytest.mark.parametrize("case", [(16, 700, 4096, 64, BF16), (64, 500, 2048, 32, F16), (130, 256, 1024, 128, BF16)])
