@@ -108,7 +108,7 @@ class Clocks:
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+         "clocks_event_reasons.sw_power_cap,utilization.gpu")
 
     def __init__(self, gpu_index, log_path=None):
         self.proc = None
@@ -138,10 +138,13 @@ class Clocks:
                 self.proc.kill()
             self.fh.close()
 
-    def summary(self):
+    def summary(self, loaded_only=False):
+        """Median SM clock, maximum clock and the throttle reasons seen.  With
+        loaded_only, only samples whose GPU utilisation is at least 50 % count
+        (a region that also generates inputs on the host idles in between)."""
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons = [], None, set()
+        sm, smax, reasons, total = [], None, set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
@@ -149,15 +152,27 @@ class Clocks:
                 if len(parts) < 9:
                     continue
                 try:
-                    sm.append(float(parts[1]))
+                    mhz = float(parts[1])
                     smax = float(parts[2])
                 except ValueError:
                     continue
+                total += 1
+                if loaded_only:
+                    try:
+                        if float(parts[9]) < 50.0:
+                            continue
+                    except (IndexError, ValueError):
+                        continue
+                sm.append(mhz)
                 for n, v in zip(names, parts[5:9]):
                     if v.lower().startswith("active"):
                         reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if loaded_only:
+            out["samples_total"] = total
+            out["samples_rule"] = "samples with GPU utilisation >= 50 %"
+        return out
 
 
 # ------------------------------------------------------------- CPU baseline
@@ -233,7 +248,42 @@ def cpu_baseline(budget_s=12.0, sample=None):
         done, secs, passes = done + b, secs + t, passes + 1
     return {"value": done / secs / 1e9, "unit": "GB/s", "cores": S.cores, "cpu_model": cpu_model(), "kind": "oracle",
             "sample": "%d pass(es) over %.1f%% of the rows of the 5 phi4 shapes, M=1 (%.1f MB of weights, %.1f s, "
-                      "OpenMP over rows)" % (passes, 100 * frac, done / 1e6, secs)}, secs
+                      "OpenMP over rows, %s thread(s))" % (passes, 100 * frac, done / 1e6, secs,
+                                                          os.environ.get("OMP_NUM_THREADS", S.cores))}, secs
+
+
+def oracle_prefill_sample(nrows=64):
+    """The oracle on the M=2048 prefill GEMMs, restricted to `nrows` evenly
+    spaced activation rows (rows are independent) and every weight row: the
+    rows the GPU parity tests check, timed on the host cores (OpenMP)."""
+    import oracle as O
+    import workloads as WL
+
+    out = {}
+    for shape in ("gate_up", "down"):
+        d = WL.prefill_u2(shape)
+        mrows = np.linspace(0, d["M"] - 1, nrows).astype(np.int64)
+        A = np.ascontiguousarray(d["A"][mrows])
+        t0 = time.perf_counter()
+        O.qgemm_nbits(A, d["W"], d["scales"], None, M=nrows, N=d["N"], K=d["K"], bits=2, block_size=64,
+                      uniform_zp=ZP, a_dtype=WL.F16)
+        dt = time.perf_counter() - t0
+        out["prefill_u2_%s_m2048" % shape] = {"seconds": round(dt, 3), "activation_rows": nrows,
+                                              "tflops": round(2.0 * nrows * d["N"] * d["K"] / dt / 1e12, 6)}
+    return out
+
+
+def oracle_single_thread(budget_s=8.0):
+    """cpu_baseline with one OpenMP thread, in a child process (the thread count
+    is fixed when the oracle library starts its runtime)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-timing", str(budget_s)], env=env,
+                       capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return {"error": (r.stderr or r.stdout).strip().splitlines()[-1:]}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    d["cores"] = 1
+    return d
 
 
 def run_reference(args, world, rank):
@@ -450,9 +500,19 @@ def run_ours(args, world, rank, local):
             tr = json.load(f)
         if tr.get("kernel_source_hash") == kernel_source_hash():
             traffic = tr.get("bytes_per_launch")
+    # ---- every configuration of the hot path (one GPU): the suite's timing of
+    # each, with its own clock record over the loaded samples
+    configs, cclocks = None, None
+    if world == 1 and not args.no_configs:
+        with Clocks(local, None) as clk2:
+            recs = run_suite(groups=CONFIG_GROUPS, echo=False)
+        configs = {r.pop("config"): r for r in recs}
+        cclocks = clk2.summary(loaded_only=True)
     cb = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb, _ = cpu_baseline()
+        cb["single_thread"] = oracle_single_thread()
+        cb["prefill_sample"] = oracle_prefill_sample()
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
@@ -479,13 +539,25 @@ def run_ours(args, world, rank, local):
         "clocks": clocks,
         "cpu_baseline": cb,
     }
+    if configs is not None:
+        line["config"]["configs"] = configs
+        line["config"]["configs_clocks"] = cclocks
+        line["config"]["configs_method"] = (
+            "each configuration through the public API after the timed steps: a CUDA graph of back-to-back calls "
+            "whose weights rotate over copies (QMoE: disjoint expert sets) totalling more than 3x L2, replayed for "
+            "about 60 ms; us_per_call = event time / calls; gbs over weight bytes (codes + block parameters); "
+            "hbm_frac / tensor_frac against the measured copy / bf16 peaks; prefill and ragged reuse one weight set")
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
 
 
 # ------------------------------------------------------------- config suite
-def run_suite(only=None):
+# the groups the benchmark line carries (the N sweep only runs under --suite)
+CONFIG_GROUPS = ("tiny_u4", "phi4_u2", "nf4", "qmoe", "prefill", "phi4_u8", "packed_zp", "ragged", "gather")
+
+
+def run_suite(only=None, groups=None, echo=True):
     """Time every configuration of the hot path through the public API (one
     JSON line each): tiny u4 GEMV; the phi4 u2 decode shapes at M=1 and M=4;
     8-bit codes on two of those shapes;
@@ -498,7 +570,10 @@ def run_suite(only=None):
     (u4, u8, E4M3 tables).  Each figure is the mean over a CUDA
     graph of R back-to-back calls whose weights rotate over copies (or expert
     sets) totalling more than three times the L2, so every call reads cold
-    weights; prefill is compute-bound and reuses one weight set."""
+    weights; prefill is compute-bound and reuses one weight set.
+
+    `groups` restricts the run to those groups; every record is also returned
+    (a list of dicts), and printed as one JSON line when `echo` is set."""
     import torch
 
     import gemm_blockwise_dequant_gb300 as qg
@@ -527,15 +602,19 @@ def run_suite(only=None):
             with torch.cuda.graph(g, stream=st):
                 for i in range(n):
                     call(i)
-            g.replay()
-            st.synchronize()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(st)
-            for _ in range(5):
+            g.replay()
+            b.record(st)
+            st.synchronize()
+            # enough replays for about 60 ms of back-to-back work (at least 5)
+            reps = int(min(2000, max(5, 60.0 / max(1e-3, a.elapsed_time(b)))))
+            a.record(st)
+            for _ in range(reps):
                 g.replay()
             b.record(st)
         torch.cuda.synchronize()
-        return a.elapsed_time(b) * 1e3 / (5 * n)
+        return a.elapsed_time(b) * 1e3 / (reps * n)
 
     def emit(name, us, nbytes=None, flops=None, **extra):
         line = {"config": name, "us_per_call": round(us, 2)}
@@ -548,13 +627,19 @@ def run_suite(only=None):
             if tf_peak:
                 line.update(tensor_frac=round(tfs / tf_peak, 4))
         line.update(extra)
-        print(json.dumps(line), flush=True)
+        records.append(line)
+        if echo:
+            print(json.dumps(line), flush=True)
 
     def reps_for(nbytes):
         return max(2, -(-3 * L2_BYTES // max(1, nbytes)))
 
     def want(group):
+        if groups is not None:
+            return group in groups
         return only is None or only in group
+
+    records = []
 
     # tiny u4 (M=1, 128 x 256, block 64, zero-point tensor)
     if want("tiny_u4"):
@@ -627,21 +712,24 @@ def run_suite(only=None):
 
     # NF4 codebook, bf16 activations
     if want("nf4"):
-        for shape in ("square", "gqa_kv", "up", "down"):
-            for M in (1, 4, 16, 64):
-                d = WL.nf4(shape, M=M, a_dtype=2)
-                wb = d["W"].nbytes + d["absmax"].nbytes
-                r = reps_for(wb)
-                Ws = [torch.from_numpy(d["W"]).to(dev) for _ in range(r)]
-                am = torch.from_numpy(d["absmax"]).to(dev)
-                cb = torch.from_numpy(d["codebook"]).to(dev)
-                A = t16(d["A"], torch.bfloat16)
-                Y = torch.empty(M, d["N"], device=dev, dtype=torch.bfloat16)
-                ws = torch.empty(max(16, qg.qgemm_workspace_bytes(2, M, d["N"], d["K"], 4, 64)), dtype=torch.uint8, device=dev)
-                us = timed(lambda i: qg.qgemm_codebook4(A, Ws[i % r], cb, am, Y, block_size=64, workspace=ws, stream=st), 2 * r)
-                emit("nf4_%s_%dx%d_m%d" % (shape, d["N"], d["K"], M), us, nbytes=wb,
-                     flops=2.0 * M * d["N"] * d["K"])
-                del Ws
+        for ad, tdt, tag in ((2, torch.bfloat16, "bf16"), (1, torch.float16, "f16")):
+            for shape in ("square", "gqa_kv", "up", "down"):
+                for M in (1, 4, 16, 64):
+                    d = WL.nf4(shape, M=M, a_dtype=ad)
+                    wb = d["W"].nbytes + d["absmax"].nbytes
+                    r = reps_for(wb)
+                    Ws = [torch.from_numpy(d["W"]).to(dev) for _ in range(r)]
+                    am = torch.from_numpy(d["absmax"]).to(dev)
+                    cb = torch.from_numpy(d["codebook"]).to(dev)
+                    A = t16(d["A"], tdt)
+                    Y = torch.empty(M, d["N"], device=dev, dtype=tdt)
+                    ws = torch.empty(max(16, qg.qgemm_workspace_bytes(ad, M, d["N"], d["K"], 4, 64)), dtype=torch.uint8,
+                                     device=dev)
+                    us = timed(lambda i: qg.qgemm_codebook4(A, Ws[i % r], cb, am, Y, block_size=64, workspace=ws,
+                                                            stream=st), 2 * r)
+                    emit("nf4_%s_%s_%dx%d_m%d" % (tag, shape, d["N"], d["K"], M), us, nbytes=wb,
+                         flops=2.0 * M * d["N"] * d["K"])
+                    del Ws
 
     # NF4 with a nested (double-quantized) absmax, M = 1, bf16: the expansion plus the codebook GEMV;
     # bytes = codes + 8-bit absmax codes + second-level scales
@@ -764,7 +852,7 @@ def run_suite(only=None):
             emit("gather_%s_phi4_embed_n2048_bs32_f16" % name, us, nbytes=nbytes, bytes_include="indices, codes, "
                  "scales, zero points, fp16 output")
             del W, S, Z, Y
-    return 0
+    return records
 
 
 # ------------------------------------------------------------- ncu probes
@@ -866,6 +954,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration timings that follow the benchmark step")
+    ap.add_argument("--oracle-timing", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--graph-steps", type=int, default=8,
                     help="steps per CUDA graph in the timed region (each step is 5 GEMV launches)")
     ap.add_argument("--clocks-log", default=None,
@@ -879,10 +970,15 @@ def main():
                                        "gather", "nsweep"],
                     help="with --suite: time one group of configurations only")
     args = ap.parse_args()
+    if args.oracle_timing is not None:  # child of oracle_single_thread()
+        cb, _ = cpu_baseline(budget_s=args.oracle_timing)
+        print(json.dumps(cb), flush=True)
+        return 0
     if args.probe:
         return run_probe(args.probe)
     if args.suite or args.only:
-        return run_suite(args.only)
+        run_suite(args.only)
+        return 0
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_setup(args.gpus)

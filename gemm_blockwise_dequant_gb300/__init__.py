@@ -25,7 +25,7 @@ __all__ = [
     "qg_dequant_nbits_uniform_zp", "qg_dequant_codebook4", "qg_read_device_fault", "qg_status_string",
     "qgemm_codebook4_nested", "qgemm_codebook4_nested_workspace_bytes", "qmoe_ragged_mm",
     "qmoe_ragged_mm_workspace_bytes", "qg_gather_block_quantized", "QG_WF_U2", "QG_WF_U4", "QG_WF_U8", "QG_WF_E4M3",
-    "qgemm_nbits_packed_zp", "qgemm_nbits_packed_zp_workspace_bytes",
+    "qgemm_nbits_packed_zp", "qgemm_nbits_packed_zp_workspace_bytes", "qg_test_bounded_wait",
 ]
 
 QG_OK, QG_ERR_INVALID_ARG, QG_ERR_UNSUPPORTED, QG_ERR_CUDA, QG_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3, 4
@@ -79,6 +79,7 @@ _SIGS = {
     "qmoe_ragged_mm": ([_P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P], _I),
     "qmoe_ragged_mm_workspace_bytes": ([_I, _P, _I, _I, _I, _I, _I], _SZ),
     "qg_read_device_fault": ([_P], _I),
+    "qg_test_bounded_wait": ([_I, ctypes.c_uint, _P, _P], _I),
     "qg_status_string": ([_I], ctypes.c_char_p),
 }
 
@@ -353,6 +354,15 @@ def qg_read_device_fault() -> int:
     v = ctypes.c_uint(0)
     _check(lib().qg_read_device_fault(ctypes.byref(v)), "qg_read_device_fault")
     return int(v.value)
+
+
+def qg_test_bounded_wait(fill: bool, limit_us: int, out, stream=None, raw=False):
+    """Test hook (include/qgemm_testing.h): the library's bounded pipeline wait
+    in a one-CTA kernel whose producer fills the stage only if `fill`; out is a
+    device int32 tensor of 3 (1: that consumer warp's wait completed, 0: it
+    gave up)."""
+    s = lib().qg_test_bounded_wait(1 if fill else 0, int(limit_us), _ptr(out), _stream(stream))
+    return s if raw else _check(s, "qg_test_bounded_wait")
 
 
 def qg_status_string(status: int) -> str:

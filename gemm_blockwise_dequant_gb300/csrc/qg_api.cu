@@ -17,42 +17,53 @@ namespace qg {
 __device__ unsigned g_fault_word;
 
 namespace {
-constexpr int kMaxDevices = 64;
 DeviceInfo g_info[kMaxDevices];
 std::atomic<int> g_info_ready[kMaxDevices];
 unsigned *g_fault_ptr[kMaxDevices];
 std::atomic<int> g_fault_ready[kMaxDevices];
 
-int current_device() {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    return dev < 0 || dev >= kMaxDevices ? 0 : dev;
+DeviceInfo query_info(int dev) {
+    DeviceInfo d{};
+    cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (d.sm_count <= 0) d.sm_count = 1;
+    if (d.max_smem_optin <= 0) d.max_smem_optin = 48 * 1024;
+    return d;
 }
 }  // namespace
 
+int device_slot() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev < 0 || dev >= kMaxDevices ? -1 : dev;
+}
+
 const DeviceInfo &device_info() {
-    const int dev = current_device();
-    if (!g_info_ready[dev].load(std::memory_order_acquire)) {
-        DeviceInfo d{};
-        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
-        cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (d.sm_count <= 0) d.sm_count = 1;
-        if (d.max_smem_optin <= 0) d.max_smem_optin = 48 * 1024;
-        g_info[dev] = d;
-        g_info_ready[dev].store(1, std::memory_order_release);
+    const int slot = device_slot();
+    if (slot < 0) {  // not cached: this thread's copy, queried now
+        thread_local DeviceInfo d;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        d = query_info(dev);
+        return d;
     }
-    return g_info[dev];
+    if (!g_info_ready[slot].load(std::memory_order_acquire)) {
+        g_info[slot] = query_info(slot);
+        g_info_ready[slot].store(1, std::memory_order_release);
+    }
+    return g_info[slot];
 }
 
 unsigned *fault_word() {
-    const int dev = current_device();
-    if (!g_fault_ready[dev].load(std::memory_order_acquire)) {
+    const int slot = device_slot();
+    if (slot < 0 || !g_fault_ready[slot].load(std::memory_order_acquire)) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_fault_word) != cudaSuccess) return nullptr;
-        g_fault_ptr[dev] = static_cast<unsigned *>(p);
-        g_fault_ready[dev].store(1, std::memory_order_release);
+        if (slot < 0) return static_cast<unsigned *>(p);
+        g_fault_ptr[slot] = static_cast<unsigned *>(p);
+        g_fault_ready[slot].store(1, std::memory_order_release);
     }
-    return g_fault_ptr[dev];
+    return g_fault_ptr[slot];
 }
 
 }  // namespace qg
@@ -366,7 +377,6 @@ int qgemm_codebook4_nested(const void *A, int a_dtype, const uint8_t *W, const f
     p.K = K;
     p.bits = 4;
     p.bs = block_size;
-    p.params_from_device = 1;  // the expansion above writes them
     return run_gemm(p, static_cast<char *>(workspace) + expanded, workspace_bytes - expanded, s);
 }
 
@@ -427,7 +437,6 @@ int qgemm_nbits_packed_zp(const void *A, int a_dtype, const uint8_t *W, const ui
     p.K = K;
     p.bits = bits;
     p.bs = block_size;
-    p.params_from_device = 1;  // the zero points are written by the launch above
     return run_gemm(p, gws, gws_bytes, s);
 }
 

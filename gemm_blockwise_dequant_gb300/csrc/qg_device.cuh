@@ -59,18 +59,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
-// after kWaitTimeoutNs, or as soon as another warp of the CTA has given up
+// after limit_ns of %globaltimer (kWaitTimeoutNs unless a caller passes a
+// shorter bound), or as soon as another warp of the CTA has given up
 // (*abort != 0); on giving up it records `code` in the device fault word,
 // raises *abort and returns false.  Never hangs.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, unsigned *fault,
-                                          unsigned code) {
+                                          unsigned code, unsigned long long limit_ns = kWaitTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 if (fault) atomicOr(fault, code);
                 *abort = 1;
                 return false;

@@ -31,6 +31,15 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 enum ZpMode { ZP_NONE = 0, ZP_TENSOR = 1, ZP_UNIFORM = 2 };
 enum WeightKind { WK_NBITS = 0, WK_CODEBOOK = 1 };
 
+// The library's per-device caches (device attributes, symbol addresses) hold
+// kMaxDevices entries.  device_slot() is the current device's index into them,
+// or -1 when cudaGetDevice fails or the index is kMaxDevices or more; such a
+// device is served without caching (looked up on every call), never through
+// another device's entry.  Every entry point works on the current device: its
+// stream must belong to that device.
+constexpr int kMaxDevices = 64;
+int device_slot();
+
 // Per-device facts cached on first use.
 struct DeviceInfo {
     int sm_count;
@@ -57,15 +66,15 @@ struct GemmProblem {
     void *Y;
     int y_dtype;
     int M, N, K, bits, bs;
-    // The block parameters are written by the kernel launched just before on
-    // the stream (the nested absmax expansion): kernels that start copying
-    // weights before the preceding kernel completes wait for it first.
-    int params_from_device;
 };
 
 // SIMT decode path (small M).
 size_t simt_workspace_bytes(int M, int N, int K, int bits, int bs);
 cudaError_t simt_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s);
+
+// cuTensorMapEncodeTiled from the driver (a PFN_cuTensorMapEncodeTiled_v12000),
+// or null when the driver does not provide it.
+void *tensor_map_encode_fn();
 
 // Tensor-core path (M >= 9 with 16-bit activations).
 bool tc_eligible(int M, int K, int bits, int a_dtype, int bs, int kind);

@@ -29,21 +29,25 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_qmoe_scratch[QG_QMOE_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-void *g_scratch_ptr[kMaxDevices];
-std::atomic<int> g_scratch_ready[kMaxDevices];
+void *g_scratch_ptr[qg::kMaxDevices];
+std::atomic<int> g_scratch_ready[qg::kMaxDevices];
 
-// Device address of this device's scratch array (set up on first use).
+// Device address of the current device's scratch array: looked up on the
+// first call made on that device and cached per device (the library's common
+// device index: a device beyond the cache is looked up on every call).
 int scratch_address(void **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QG_ERR_CUDA;
-    if (!g_scratch_ready[dev].load(std::memory_order_acquire)) {
+    const int slot = qg::device_slot();
+    if (slot < 0 || !g_scratch_ready[slot].load(std::memory_order_acquire)) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_qmoe_scratch) != cudaSuccess || p == nullptr) return QG_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
-        g_scratch_ready[dev].store(1, std::memory_order_release);
+        if (slot < 0) {
+            *out = p;
+            return QG_OK;
+        }
+        g_scratch_ptr[slot] = p;
+        g_scratch_ready[slot].store(1, std::memory_order_release);
     }
-    *out = g_scratch_ptr[dev];
+    *out = g_scratch_ptr[slot];
     return QG_OK;
 }
 

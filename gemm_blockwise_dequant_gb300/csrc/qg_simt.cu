@@ -92,7 +92,6 @@ struct GemvArgs {
     int swiglu_interleaved;
     float *out_f32;           // slot outputs [slots][N] (QMoE), with bias added
     const uint16_t *bias;     // fp16 [experts][N], or nullptr
-    int params_wait;          // the block parameters come from the preceding kernel: wait before copying them
 };
 
 // u3: 32 codes in 3 words; bit position of code i of the group after its
@@ -549,15 +548,17 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
         *abort_flag = 0;
         mbar_fence_init();
     }
+    // Launched as a programmatic dependent: the set-up above overlaps the
+    // preceding kernel's tail, and the next kernel may start launching as these
+    // CTAs retire.  Nothing the call reads (weights, parameters, codebook,
+    // activations, expert ids) or writes is touched before pdl_wait(): any
+    // buffer may have been written by the preceding kernel.
+    pdl_launch_dependents();
+    pdl_wait();
     if constexpr (WK == WK_CODEBOOK) {
         for (int i = threadIdx.x; i < 16 * 32; i += blockDim.x) lut[i] = __ldg(p.codebook + (i >> 5));
     }
     __syncthreads();
-    // Launched as a programmatic dependent: the next kernel may start launching
-    // as these CTAs retire.  Weights (codes, block parameters, codebook) are
-    // streamed before waiting for the preceding kernel; activations, expert ids
-    // and outputs are touched only after pdl_wait().
-    pdl_launch_dependents();
 
     const bool split = gridDim.y > 1;
     const int s_begin = blockIdx.y * p.S_cta;
@@ -582,16 +583,13 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     // slice order and writes the outputs before it refills the stage.  The
     // consumer warps therefore never wait on one another.
     if (warp == NWC) {
-        // expert ids, or block parameters computed on the device, may come from the preceding kernel
-        if (p.ids || p.params_wait) pdl_wait();
-        bool waited = p.ids != nullptr || p.params_wait;
         const int prow = p.nb * PB;
         const int kb0 = kc0 * BITS / 8;
         const int kb1 = split ? min(p.row_bytes, (s_begin + s_count) * LPR * VEC) : p.row_bytes;
         int it = 0, slot = 0;
         uint32_t par = 1;  // parity of the empty phase that must complete before filling (it / NST)
         bool alive = true;
-        const int e = p.ids ? __ldg(p.ids + cta_slot) : 0;  // after pdl_wait() above
+        const int e = p.ids ? __ldg(p.ids + cta_slot) : 0;
         const bool valid = e >= 0 && e < p.num_experts;
         const int sl = cta_slot;
         for (int tile = t_begin; tile < t_end; tile += t_stride, ++it) {
@@ -620,10 +618,6 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
             // finish the tile this slot held before the refill (its sums sit in
             // the reduction slot of the previous fill's parity)
             if (it >= p.NST) {
-                if (!waited) {
-                    pdl_wait();  // outputs may be read by the preceding kernel until it completes
-                    waited = true;
-                }
                 finish_tile<MT, LPR, IT>(p, red + (slot * 2 + par) * (p.S_cta * RV * H), s_count,
                                      tile - p.NST * t_stride, sl, lane, bias_s, e);
             }
@@ -634,7 +628,6 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
         }
         // finish the last (up to NST) tiles once their stages come back
         if (alive) {
-            if (!waited) pdl_wait();
             for (int j = max(0, it - p.NST); j < it; ++j) {
                 const int sj = j % p.NST;
                 if (!mbar_wait(&empty[sj], (j / p.NST) & 1, abort_flag, p.fault, FAULT_WAIT_EMPTY)) break;
@@ -670,7 +663,6 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     float c23[MT];       // 2^23 e2c (see tile_dot)
     float post[MT];
     bool need_post = false;
-    pdl_wait();  // activations, the fc1 output, expert ids and Y belong to the preceding kernel's world
     // This CTA's activation row (the same for every tile it computes): staged
     // in shared memory with coalesced loads, then each lane takes its slice.
     {
@@ -1053,7 +1045,6 @@ cudaError_t simt_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStrea
                                      : reinterpret_cast<const unsigned char *>(p.scales);
     a.zp = p.zp;
     a.zp_mode = p.zp_mode;
-    a.params_wait = p.params_from_device;
     a.zpv = p.uniform_zp;
     a.codebook = p.codebook;
     a.Y = p.Y;

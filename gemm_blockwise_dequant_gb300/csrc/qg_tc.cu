@@ -364,15 +364,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         mbar_fence_init();
     }
+    if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+    // Launched as a programmatic dependent: the set-up above overlaps the
+    // preceding kernel's tail and the next kernel may start launching as these
+    // CTAs retire; nothing the call reads or writes is touched before
+    // pdl_wait() (any buffer may have been written by the preceding kernel).
+    pdl_launch_dependents();
+    pdl_wait();
     if constexpr (WK == WK_CODEBOOK) {
         for (int i = threadIdx.x; i < 16 * 32; i += kThreads) lut[i] = __ldg(p.codebook + (i >> 5));
     }
-    if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    pdl_launch_dependents();  // the next kernel may start launching as these CTAs retire
 
     if (warp == 0 && p.par_plain) {
         // ------------------------------------------------------------ producer, parameters by cp.async
@@ -380,7 +385,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // as below; every lane copies the parameter boxes of its rows (16
         // bytes = 8 fp16 per row) in 4-byte pieces, zero past N or past nb.
         const bool zt = WK == WK_NBITS && p.zp_mode == ZP_TENSOR;
-        if (lane == 0) pdl_wait();
         __syncwarp();
         for (int i = 0; i < nks; ++i) {
             const int ks = ks0 + i;
@@ -422,7 +426,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            pdl_wait();  // activations may come from the preceding kernel; everything else follows this producer
             const bool zt = WK == WK_NBITS && p.zp_mode == ZP_TENSOR;
             for (int i = 0; i < nks; ++i) {
                 const int ks = ks0 + i;
@@ -810,6 +813,8 @@ TcArgs make_args(const GemmProblem &p, const TcCfg &c) {
 // activations stay on the SIMT path (rounding them to 16 bits would break the
 // 1e-4 bar), and so do shapes whose packed rows or parameter rows are not a
 // multiple of 16 bytes (the TMA row stride).
+void *tensor_map_encode_fn() { return reinterpret_cast<void *>(encode_fn()); }
+
 bool tc_eligible(int M, int K, int bits, int a_dtype, int bs, int kind) {
     if (M < 9 || a_dtype == 0) return false;
     if (bits == 3) return false;  // 3-bit codes (8 per 3 bytes) run on the SIMT path

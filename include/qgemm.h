@@ -17,9 +17,12 @@
  *  - Every data pointer is a DEVICE pointer owned by the caller.  The library
  *    never allocates, frees or synchronises (except qg_fp16_uniform_value and
  *    qg_read_device_fault, which return a value to the host), and enqueues
- *    work on `stream` only.  It keeps no per-call state between calls, so
- *    concurrent calls on different streams with disjoint outputs and
- *    workspaces are independent.
+ *    work on `stream` only, on the current device (`stream` must belong to
+ *    it).  It keeps no per-call state between calls, so concurrent calls on
+ *    different streams with disjoint outputs and workspaces are independent.
+ *    One exception is device-wide: the fault word of qg_read_device_fault
+ *    (below), which every call's kernels may set and which any caller's read
+ *    clears.
  *  - Weight codes are packed along K, least significant bits first: element
  *    k of row n is bits [(k*bits)%8, (k*bits)%8 + bits) of byte
  *    n*(K*bits/8) + (k*bits)/8.  W is row-major [N][K*bits/8] bytes.
@@ -49,12 +52,10 @@
  *    129 calls bit-identical).  Nothing is tuned or timed on live calls.
  *  - M == 0 or N == 0 is a no-op.  K == 0 writes zeros.
  *  - Kernels are launched as programmatic dependents of the preceding kernel
- *    on `stream`: they may start streaming the WEIGHT buffers (W, scales,
- *    zero points, codebook, absmax, expert weights' codes) before that kernel
- *    has finished; activations, expert ids/weights, biases and outputs are
- *    touched only after it has finished.  So weight buffers must not be
- *    written by the kernel that immediately precedes a call on the same
- *    stream (copies and events order as usual).
+ *    on `stream`: their set-up (barriers, tensor memory) overlaps that
+ *    kernel's tail, but no buffer of the call -- weights, block parameters,
+ *    activations, expert ids, outputs -- is read or written before that kernel
+ *    has completed, so stream order holds exactly as for plain launches.
  */
 #ifndef QGEMM_H
 #define QGEMM_H
@@ -234,7 +235,8 @@ int qmoe_decode_fused_dp4a(const uint16_t *x_f16, const int32_t *expert_ids, con
  * anything is enqueued.  Calls no cudaMalloc, cudaFree or other allocator.
  *  - The first call on a device looks up the array's device address (once
  *    per device, with that device current); make that first call before any
- *    stream capture.
+ *    stream capture.  Like every entry point it works on the current device:
+ *    `stream` must belong to it.
  *  - All calls on a device share the one array: calls that can overlap on
  *    the GPU (unordered streams) race.  The array keeps the last call's
  *    contents; no call depends on them.
@@ -386,6 +388,13 @@ int qg_gather_block_quantized(const int64_t *indices, int64_t n_indices, const u
  * bounded; a wait that gives up records a bit in a device-side fault word
  * instead of hanging.  This call synchronises the current device, returns
  * the word in *flags (0: no fault since the last read) and clears it.
+ * The word is one per device, shared by every call of every stream and
+ * thread: a read reports (and clears) the faults of all calls on the device
+ * since the previous read, whoever made them.  A caller that needs to know
+ * which call gave up must read the word between its own calls, with no other
+ * work on the device in between.  (A wait that gives up is a library fault --
+ * a kernel that did not get its data within seconds -- not an argument
+ * error: arguments are checked before anything is enqueued.)
  */
 int qg_read_device_fault(unsigned int *flags);
 

@@ -1,0 +1,39 @@
+/*
+ * qgemm_testing.h -- a test hook of libqgemm.so, not part of the compute API.
+ *
+ * qg_test_bounded_wait -- runs the library's bounded pipeline wait on the GPU
+ * in a kernel shaped like its pipelines (a producer warp and three consumer
+ * warps waiting on one shared-memory stage barrier), so that a test can make
+ * the wait give up without faulting, trapping or hanging the GPU.  The
+ * source pages have no counterpart: every wait in this library's kernels is
+ * bounded, and this is how that bound is exercised.
+ *
+ *   fill      0: the producer never fills the stage, so each consumer warp's
+ *               wait runs out after `limit_us` and gives up: it records
+ *               FAULT_WAIT_FULL (bit 1) in the device fault word (read it with
+ *               qg_read_device_fault) and the warp ends;
+ *             1: the producer fills the stage; every wait completes.
+ *   limit_us  the bound of each wait, 1 .. 2000000 microseconds (the
+ *             library's own kernels use 2 s).
+ *   out_dev   device int[3]: per consumer warp, 1 if its wait completed, 0 if
+ *             it gave up.
+ * Returns QG_OK, QG_ERR_INVALID_ARG (null out_dev, limit out of range) or
+ * QG_ERR_CUDA (launch error).  Enqueued on `stream` of the current device;
+ * nothing is synchronised.
+ */
+#ifndef QGEMM_TESTING_H
+#define QGEMM_TESTING_H
+
+#include "qgemm.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+int qg_test_bounded_wait(int fill, unsigned int limit_us, int *out_dev, qg_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMM_TESTING_H */

@@ -14,12 +14,15 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "qgemm.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 
 
 def _declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    names = []
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
     return sorted(set(n for n in names if n.startswith(("qg", "qmoe"))))
 
 
@@ -36,7 +39,7 @@ def test_header_declares_the_entry_points():
     names = _declared_functions()
     for n in ["qgemm_nbits", "qgemm_nbits_uniform_zp", "qgemm_codebook4", "qmoe_decode_fused",
               "qgemm_workspace_bytes", "qmoe_decode_workspace_bytes", "qg_fp16_uniform_value",
-              "qg_dequant_nbits", "qg_dequant_codebook4", "qg_status_string"]:
+              "qg_dequant_nbits", "qg_dequant_codebook4", "qg_status_string", "qg_test_bounded_wait"]:
         assert n in names
 
 
@@ -102,3 +105,31 @@ def test_workload_packed_zero_points_shapes():
         assert d["zp_packed"].shape == (5, (nb * bits + 7) // 8) and d["zp_packed"].dtype == np.uint8
         assert d["W"].shape == (5, nb * 32 * bits // 8) and d["scales"].shape == (5, nb) and d["A"].shape == (2, nb * 32)
     assert np.array_equal(W.packed_zp(4, 64, seed=3)["zp_packed"], W.packed_zp(4, 64, seed=3)["zp_packed"])
+
+
+def _header_constants():
+    """#define and enum integer constants of the header, evaluated (shifts and literals only)."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for name, expr in re.findall(r"^#define\s+(QG_[A-Z0-9_]+)\s+(.+)$", text, flags=re.M):
+        expr = re.sub(r"(\d+)[uUlL]+", r"\1", expr.strip())
+        if re.fullmatch(r"[\d\s()<>+*]+", expr):
+            out[name] = eval(expr, {"__builtins__": {}})
+    for body in re.findall(r"enum\s*\{([^}]*)\}", text):
+        for name, val in re.findall(r"(QG_[A-Z0-9_]+)\s*=\s*(\d+)", body):
+            out[name] = int(val)
+    return out
+
+
+def test_binding_constants_match_the_header():
+    """The binding's copies of the header's constants (status codes, dtypes,
+    table formats, the no-allocation scratch size) equal the header's values."""
+    import gemm_blockwise_dequant_gb300 as qg
+
+    consts = _header_constants()
+    assert "QG_QMOE_NOALLOC_SCRATCH_BYTES" in consts
+    for name, value in consts.items():
+        if hasattr(qg, name):
+            assert getattr(qg, name) == value, name
+    for name in ("QG_QMOE_NOALLOC_SCRATCH_BYTES", "QG_OK", "QG_ERR_CUDA", "QG_BF16", "QG_WF_E4M3"):
+        assert hasattr(qg, name) and name in consts, name
