@@ -131,7 +131,8 @@ int run_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s) {
         return QG_OK;
     }
     const cudaError_t e = qg::tc_eligible(p.M, p.K, p.bits, p.a_dtype, p.bs, p.kind) ? qg::tc_gemm(p, ws, ws_bytes, s)
-                                                                       : qg::simt_gemm(p, ws, ws_bytes, s);
+                          : qg::mma_gemv_eligible(p)                                   ? qg::mma_gemv(p, s)
+                                                                                       : qg::simt_gemm(p, ws, ws_bytes, s);
     if (e == cudaErrorNotSupported) return QG_ERR_UNSUPPORTED;
     return e == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }

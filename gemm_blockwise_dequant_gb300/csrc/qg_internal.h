@@ -72,9 +72,10 @@ struct GemmProblem {
 size_t simt_workspace_bytes(int M, int N, int K, int bits, int bs);
 cudaError_t simt_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s);
 
-// cuTensorMapEncodeTiled from the driver (a PFN_cuTensorMapEncodeTiled_v12000),
-// or null when the driver does not provide it.
-void *tensor_map_encode_fn();
+// 2-bit MatMulNBits GEMV / small-M GEMM through warp-level MMAs (M <= 4 with
+// fp32 activations, M <= 8 with 16-bit ones; block 64, K a multiple of 512).
+bool mma_gemv_eligible(const GemmProblem &p);
+cudaError_t mma_gemv(const GemmProblem &p, cudaStream_t s);
 
 // Tensor-core path (M >= 9 with 16-bit activations).
 bool tc_eligible(int M, int K, int bits, int a_dtype, int bs, int kind);

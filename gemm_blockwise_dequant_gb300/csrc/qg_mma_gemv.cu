@@ -1,0 +1,614 @@
+// qg_mma_gemv.cu -- 2-bit MatMulNBits GEMV / small-M GEMM on the tensor
+// cores through warp-level MMAs (mma.sync m16n8k16, fp16 operands, fp32
+// accumulation), for sm_103a.
+//
+//   Y[m][n] = sum_k A[m][k] * (q[n][k] - zp[n][b]) * s[n][b],   b = k / 64
+//
+// hip-ep #1318, "What" (Commit 1): the u2 GEMV reads fp32 A and writes fp32 Y
+// directly, with the uniform fp16 zero point passed as a scalar; "Performance":
+// the phi4-14B export (block 64, zero points 1.5) it is measured on.
+//
+// Why the matrix unit for a GEMV: at M = 1 a u2 weight byte carries four
+// codes, and a SIMT kernel that turns each code into a float needs at least
+// one integer operation per code on the half-rate integer pipe -- a ceiling
+// near 5 TB/s of weights on this GPU, below the HBM roofline.  Here:
+//  * A code masked in place inside a 16-bit half IS an fp16 subnormal:
+//    (word & (3 << p)) per half = q * 2^(p - 24), exactly.  One AND of a
+//    32-bit word of 16 codes yields an fp16 pair (codes i and i + 8), so a
+//    word costs one shift and eight ANDs (0.56 integer operations per code)
+//    and the multiply-add runs on the tensor pipe, fed from registers.
+//  * The four code positions p in {0, 2, 4, 6} inside a byte are folded into
+//    the activations: the MMA's B operand holds a' * 2^-p, so every product
+//    is q * a' * 2^-24 whatever p is.  a' = a * 2^(14 - e), e the exponent of
+//    the row's largest |a|, so that a' * 2^-p fits fp16.
+//  * fp32 activations are split into two fp16 terms (hi = fp16(x), lo =
+//    fp16(x - hi)), each its own B column; fp16 / bf16 activations need one.
+//  * The scale and zero point are applied per block of 64 codes in fp32,
+//    outside the MMA: sum a (q - zp) s = s (sum a q - zp sum a).  To keep a
+//    block's sum separate from its neighbours' without reading the
+//    accumulator back after every block, the B columns are block-diagonal:
+//    column (block, row m, term) holds the activations of that block only, so
+//    one accumulator fragment carries up to eight blocks' sums side by side.
+//  * Weights stream through an mbarrier ring of shared-memory stages filled by
+//    TMA 2-D copies (one producer warp; 128-byte swizzled boxes of 16 rows x
+//    128 bytes, which makes the consumers' code loads bank-conflict free and
+//    zero-fills rows past N).  Each consumer warp owns one 512-code span of
+//    each K chunk; the producer adds the warps' span sums of a tile in span
+//    order and writes Y.  Fixed order everywhere: repeated calls are
+//    bit-identical (hip-ep #1328, "Why").
+//  * Every wait is bounded (qg_device.cuh).
+#include <algorithm>
+#include <atomic>
+
+#include "qg_device.cuh"
+#include "qg_internal.h"
+
+namespace qg {
+namespace {
+
+constexpr int kRows = 16;          // weight rows per MMA row tile (the MMA's M) and per fill
+constexpr int kTileRows = 32;      // weight rows per tile: two MMA row tiles
+constexpr int kSpanBytes = 128;    // u2 code bytes of one row in a span: 512 codes, 8 blocks of 64
+constexpr int kSpanCodes = 512;
+constexpr int kMaxStages = 16;
+constexpr int kMaxWarps = 12;      // consumer warps (warp w owns spans w, w + W, ...)
+constexpr int kHeader = 512;       // barriers, abort flag, row exponents
+
+struct MgArgs {
+    const void *A;
+    int a_dtype;
+    const uint8_t *W;
+    const uint16_t *scales, *zp;
+    int row_bytes;    // K / 4
+    float zpv;        // scalar zero point (uniform, or the midpoint when absent)
+    void *Y;
+    int y_dtype;
+    int M, N, K, nb;
+    int spans;        // K / 512
+    int W_;           // consumer warps: warp w owns spans w, w + W_, ...
+    int NST, ntiles;  // ring stages (16-row fills), 32-row tiles
+    int b_off, sp_off, om_off, zero_off, stage_off, stage_bytes, par_off, zp_off, red_off;
+    unsigned *fault;
+};
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---- the column layout, per MNT = (activation rows) x (fp16 terms) columns per block.
+// BPG = 8 / MNT blocks share one accumulator fragment (a "D-group"); a span of
+// 8 blocks has MNT D-groups of 4 * BPG MMAs.  Thread c of a row quad supplies
+// BPG words (16 codes each) per D-group; block_of / word_of give which, and
+// beta_of the block's column slot inside the D-group.  The assignments keep
+// every code load of a quarter-warp on distinct banks of the swizzled box.
+template <int BPG>
+__host__ __device__ constexpr int block_of(int j, int c, int w) {
+    return BPG == 8 ? 2 * c + (w >> 2) : (BPG == 4 ? 2 * c + j : (BPG == 2 ? ((c >> 1) ? j + 4 : j) : j));
+}
+template <int BPG>
+__host__ __device__ constexpr int word_of(int c, int w) {
+    return BPG == 8 ? (w & 3) : (BPG == 4 ? w : (BPG == 2 ? 2 * (c & 1) + w : c));
+}
+template <int BPG>
+__host__ __device__ constexpr int beta_of(int c, int w) {
+    return BPG == 8 ? 2 * c + (w >> 2) : (BPG == 4 ? c : (BPG == 2 ? (c >> 1) : 0));
+}
+// block of column slot beta in D-group j
+template <int BPG>
+__host__ __device__ constexpr int block_of_beta(int j, int beta) {
+    return BPG == 8 ? beta : (BPG == 4 ? 2 * beta + j : (BPG == 2 ? j + 4 * beta : j));
+}
+
+// B-fragment entries: 16 bytes (the b0, b1 registers of two MMAs) per
+// (span, D-group j, word w, half h, slot); slot = (column within block) * 4 + c.
+template <int MNT>
+__host__ __device__ constexpr int b_entry(int sp, int j, int w, int h, int slot) {
+    return (((sp * MNT + j) * (8 / MNT) + w) * 2 + h) * (4 * MNT) + slot;
+}
+
+// (j, c, w) of the thread word that holds code word wd of block blk of a span:
+// the inverse of block_of / word_of.
+template <int BPG>
+__device__ __forceinline__ void owner_of(int blk, int wd, int &j, int &c, int &w) {
+    if constexpr (BPG == 8) {
+        j = 0; c = blk >> 1; w = ((blk & 1) << 2) | wd;
+    } else if constexpr (BPG == 4) {
+        j = blk & 1; c = blk >> 1; w = wd;
+    } else if constexpr (BPG == 2) {
+        j = blk & 3; c = ((blk >> 2) << 1) | (wd >> 1); w = wd & 1;
+    } else {
+        j = blk; c = wd; w = 0;
+    }
+}
+
+// One warp prepares span sp: lane L owns code word L (block L / 4, word L % 4,
+// codes k = 512 sp + 16 L .. + 15).  Per activation row m: the span's largest
+// |a| gives e and a' = a * 2^(14 - e); the lane writes the B entries of its
+// word (fp16 a' * 2^-p, split into hi / lo terms for fp32 activations); the
+// block's four lanes add the sum of a' in a fixed order (2^-24 sum stored in
+// spart); lane 0 stores the span's output multiplier 2^(10 + e).
+template <int MP, int NT>
+__device__ __forceinline__ void build_span(const MgArgs &p, int sp, int lane, unsigned char *bfrag, float *spart,
+                                           float *somul) {
+    constexpr int MNT = MP * NT;
+    constexpr int BPG = 8 / MNT;
+    const int blk = lane >> 2, wd = lane & 3;
+    int j, c, w;
+    owner_of<BPG>(blk, wd, j, c, w);
+    const size_t k0 = static_cast<size_t>(sp) * kSpanCodes + 16 * lane;
+#pragma unroll 1
+    for (int m = 0; m < MP; ++m) {
+        float a[16];
+        if (m < p.M) {
+            if (p.a_dtype == 0) {
+                const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(p.A) + m * static_cast<size_t>(p.K) + k0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 v = __ldg(src + q);
+                    a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
+                }
+            } else {
+                const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.A) + m * static_cast<size_t>(p.K) + k0);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const uint4 v = __ldg(src + q);
+                    const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const uint16_t lo = static_cast<uint16_t>(ww[r] & 0xFFFFu), hi = static_cast<uint16_t>(ww[r] >> 16);
+                        a[8 * q + 2 * r] = p.a_dtype == 1 ? h2f(lo) : bf2f(lo);
+                        a[8 * q + 2 * r + 1] = p.a_dtype == 1 ? h2f(hi) : bf2f(hi);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) a[i] = 0.f;
+        }
+        float mx = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(a[i]));
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        // e clamped to [-110, 117]: both 2^(14 - e) and 2^(10 + e) stay normal
+        const unsigned bits = __float_as_uint(mx);
+        const int ef = static_cast<int>((bits >> 23) & 0xFFu);
+        const int e = (bits == 0u || ef == 255) ? 0 : min(max(ef - 127, -110), 117);
+        const float asc = exp2i(14 - e);
+        float bs = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            a[i] *= asc;
+            bs += a[i];
+        }
+        bs += __shfl_xor_sync(0xffffffffu, bs, 1);
+        bs += __shfl_xor_sync(0xffffffffu, bs, 2);
+        if (wd == 0) spart[(sp * 8 + blk) * MP + m] = bs * 5.9604644775390625e-08f;  // 2^-24
+        if (lane == 0) somul[sp * MP + m] = exp2i(10 + e);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const int slot = (m * NT + t) * 4 + c;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t regs[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int i = 2 * (2 * h + (q >> 1)) + (q & 1);  // codes i and i + 8 of the word
+                    const float pinv = exp2i(-2 * (i & 3));           // 2^-p
+                    const float x0 = a[i] * pinv, x1 = a[i + 8] * pinv;
+                    const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+                    const uint16_t v0 = t == 0 ? __half_as_ushort(h0) : __half_as_ushort(__float2half_rn(x0 - __half2float(h0)));
+                    const uint16_t v1 = t == 0 ? __half_as_ushort(h1) : __half_as_ushort(__float2half_rn(x1 - __half2float(h1)));
+                    regs[q] = static_cast<uint32_t>(v0) | (static_cast<uint32_t>(v1) << 16);
+                }
+                *reinterpret_cast<uint4 *>(bfrag + static_cast<size_t>(b_entry<MNT>(sp, j, w, h, slot)) * 16) =
+                    make_uint4(regs[0], regs[1], regs[2], regs[3]);
+            }
+        }
+    }
+}
+
+template <int MP, int NT, bool ZPT>
+__global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
+    mma_gemv_kernel(const MgArgs p) {
+    constexpr int MNT = MP * NT;
+    constexpr int BPG = 8 / MNT;
+    static_assert(MNT >= 1 && MNT <= 8 && (8 % MNT) == 0, "columns per block");
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + kMaxStages;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 2 * kMaxStages * 8);
+    unsigned char *bfrag_w = smem + p.b_off;                    // B-fragment entries of every span
+    float *spart = reinterpret_cast<float *>(smem + p.sp_off);  // [blocks][MP]: 2^-24 sum of a' per block
+    float *somul = reinterpret_cast<float *>(smem + p.om_off);  // [spans][MP]: each span's output multiplier
+    unsigned char *stages = smem + p.stage_off;
+    float *red = reinterpret_cast<float *>(smem + p.red_off);   // [stage / 2][warp][32 rows][MP][4 lanes]
+
+    const int W = p.W_;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], W);
+        }
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    // the zero slab that lanes without a B column of a word read instead
+    for (int i = threadIdx.x; i < 64 * MNT; i += blockDim.x)
+        reinterpret_cast<uint4 *>(smem + p.zero_off)[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    // A programmatic dependent: the set-up above overlaps the preceding
+    // kernel's tail; no buffer of the call is touched before pdl_wait().
+    pdl_launch_dependents();
+    pdl_wait();
+
+    // A tile is 32 weight rows: two 16-row MMA row tiles.  Fill f of this CTA
+    // holds rows 16 (f % 2) .. + 15 of its tile f / 2 -- whole rows: their
+    // codes are one contiguous run of HBM, copied by ONE bulk copy, and their
+    // block parameters by one more (a copy instruction costs the TMA engine a
+    // fixed time, so few large copies keep HBM busy).
+    const int ntl = (p.ntiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                    static_cast<int>(gridDim.x);  // tiles of this CTA
+    const int total = 2 * ntl;                    // fills of this CTA
+    if (warp == W) {
+        // ------------------------------------------------------------ producer
+        // Lanes of a row quad that hold the same activation row m (slots c of
+        // [row][m][4] they write): all four for one activation row per quad
+        // (M = 1), else c with c % MP == m (fp32, one row per lane) or the pairs
+        // of (2c) % MP (16-bit activations).
+        auto finish = [&](int tl, int rslot) {  // add the warps' sums of tile tl of this CTA, write Y
+            const int tile = blockIdx.x + tl * gridDim.x;
+            const float *r = red + (rslot >> 1) * (W * kTileRows * MP * 4);
+            for (int v = lane; v < kTileRows * MP; v += 32) {
+                const int row = v / MP, m = v - row * MP;
+                const int n = tile * kTileRows + row;
+                if (m >= p.M || n >= p.N) continue;
+                float s = 0.f;
+                for (int w = 0; w < W; ++w) {
+                    const float *q = r + (w * kTileRows * MP + v) * 4;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const bool mine = MP == 1 || (NT == 2 ? (cc % MP) == m : ((2 * cc) % MP == m || (2 * cc + 1) % MP == m));
+                        if (mine) s += q[cc];
+                    }
+                }
+                store_y_elem(p.Y, p.y_dtype, static_cast<size_t>(m) * p.N + n, s);
+            }
+        };
+        bool alive = true;
+        int slot = 0;
+        uint32_t par = 1;  // parity of the empty phase to wait for before refilling `slot`
+        for (int f = 0; f < total; ++f) {
+            if (f >= p.NST) {
+                if (!mbar_wait(&empty[slot], par, abort_flag, p.fault, FAULT_WAIT_EMPTY)) {
+                    alive = false;
+                    break;
+                }
+                __syncwarp();
+                if ((f - p.NST) & 1) finish((f - p.NST) >> 1, slot);
+                __syncwarp();
+            }
+            if (lane == 0) {
+                const int tile = blockIdx.x + (f >> 1) * gridDim.x;
+                const int row0 = tile * kTileRows + kRows * (f & 1);
+                const int valid = max(0, min(kRows, p.N - row0));
+                unsigned char *st = stages + static_cast<size_t>(slot) * p.stage_bytes;
+                const uint32_t cb = valid * p.row_bytes, pb = valid * p.nb * 2;
+                mbar_arrive_expect_tx(&full[slot], cb + pb * (ZPT ? 2 : 1));
+                if (valid) {
+                    bulk_g2s(st, p.W + static_cast<size_t>(row0) * p.row_bytes, cb, &full[slot]);
+                    bulk_g2s(st + p.par_off, p.scales + static_cast<size_t>(row0) * p.nb, pb, &full[slot]);
+                    if (ZPT) bulk_g2s(st + p.zp_off, p.zp + static_cast<size_t>(row0) * p.nb, pb, &full[slot]);
+                }
+            }
+            if (++slot == p.NST) {
+                slot = 0;
+                par ^= 1u;
+            }
+        }
+        if (alive) {  // the last tiles, once their fills come back
+            for (int f = max(0, total - p.NST); f < total; ++f) {
+                if (!(f & 1)) continue;
+                const int sj = f % p.NST;
+                if (!mbar_wait(&empty[sj], (f / p.NST) & 1, abort_flag, p.fault, FAULT_WAIT_EMPTY)) break;
+                __syncwarp();
+                finish(f >> 1, sj);
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ consumers: prologue
+    // Each warp prepares its own spans (sl, sl + W, ...) with no CTA-wide
+    // synchronisation: lane L holds the 16 activations of code word L of the
+    // span (per activation row), normalises the span by its own largest
+    // magnitude, writes the B-fragment entries of its word, and the four
+    // lanes of a block add its activation sum in a fixed order.
+    const int g = lane >> 2, c = lane & 3;
+    const int sl = warp;
+    for (int sp = sl; sp < p.spans; sp += W) build_span<MP, NT>(p, sp, lane, bfrag_w, spart, somul);
+    __syncwarp();
+
+    // ------------------------------------------------------------ consumers: tiles
+    // per-thread constants: code offsets inside a span (row g of a fill; row
+    // g + 8 is 8 rows further), the B lane slot
+    constexpr int NCO = BPG == 8 ? 2 : MNT;
+    uint32_t coff[NCO];
+#pragma unroll
+    for (int j = 0; j < NCO; ++j) {
+        const int blk = BPG == 8 ? 2 * c + j : block_of<BPG>(j, c, 0);
+        coff[j] = g * p.row_bytes + 16 * blk + (BPG == 2 ? 8 * (c & 1) : (BPG == 1 ? 4 * c : 0));
+    }
+    const int r8 = 8 * p.row_bytes;
+    const int slot_b = (g % MNT) * 4 + c;
+    const bool nz0 = (g / MNT) == beta_of<BPG>(c, 0);
+    const bool nz1 = (g / MNT) == beta_of<BPG>(c, BPG - 1);  // BPG = 8: the second block of the thread
+    const unsigned char *zero_slab = smem + p.zero_off;
+    const int m0 = NT == 2 ? c % MP : (2 * c) % MP;
+    const int m1 = NT == 2 ? m0 : (2 * c + 1) % MP;
+    const int pw = p.nb;  // parameters per row in a stage
+    const int pg = g * pw, pg8 = (g + 8) * pw;
+    int sa_ = 0, sb_ = 1 % p.NST;
+    uint32_t pa = 0, pbp = p.NST == 1 ? 1u : 0u;
+    for (int i = 0; i < ntl; ++i) {
+        const bool ok = mbar_wait(&full[sa_], pa, abort_flag, p.fault, FAULT_WAIT_FULL) &&
+                        mbar_wait(&full[sb_], pbp, abort_flag, p.fault, FAULT_WAIT_FULL);
+        float acc[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // [row g, g+8, 16+g, 24+g][column]
+        if (ok) {
+            const unsigned char *sta = stages + static_cast<size_t>(sa_) * p.stage_bytes;  // rows 0 .. 15
+            const unsigned char *stb = stages + static_cast<size_t>(sb_) * p.stage_bytes;  // rows 16 .. 31
+            const uint16_t *psa = reinterpret_cast<const uint16_t *>(sta + p.par_off);
+            const uint16_t *psb = reinterpret_cast<const uint16_t *>(stb + p.par_off);
+            const uint16_t *zsa = reinterpret_cast<const uint16_t *>(sta + p.zp_off);
+            const uint16_t *zsb = reinterpret_cast<const uint16_t *>(stb + p.zp_off);
+#pragma unroll 1
+            for (int sp = sl; sp < p.spans; sp += W) {
+                const unsigned char *ca = sta + sp * kSpanBytes, *cb = stb + sp * kSpanBytes;
+                const float *spw = spart + sp * 8 * MP;
+                const unsigned char *span_b = bfrag_w + static_cast<size_t>(sp) * 1024 * MNT + slot_b * 16;
+                const unsigned char *bb0 = nz0 ? span_b : zero_slab;
+                const unsigned char *bb1 = nz1 ? span_b : zero_slab;
+                const int pb = sp * 8;  // first block of the span
+                float accs[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+                for (int j = 0; j < MNT; ++j) {
+                    float d[2][4];  // [row tile][fragment]: the two row tiles are independent chains
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) d[t][0] = d[t][1] = d[t][2] = d[t][3] = 0.f;
+                    // this thread's BPG code words of rows g, g + 8, 16 + g, 24 + g (vector loads)
+                    uint32_t xw[4][BPG];
+#pragma unroll
+                    for (int rr = 0; rr < 4; ++rr) {
+                        const unsigned char *base = (rr < 2 ? ca : cb) + ((rr & 1) ? r8 : 0);
+                        if constexpr (BPG == 8) {
+#pragma unroll
+                            for (int hb = 0; hb < 2; ++hb) {
+                                const uint4 v = *reinterpret_cast<const uint4 *>(base + coff[hb]);
+                                xw[rr][4 * hb] = v.x; xw[rr][4 * hb + 1] = v.y; xw[rr][4 * hb + 2] = v.z; xw[rr][4 * hb + 3] = v.w;
+                            }
+                        } else if constexpr (BPG == 4) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(base + coff[j]);
+                            xw[rr][0] = v.x; xw[rr][1] = v.y; xw[rr][2] = v.z; xw[rr][3] = v.w;
+                        } else if constexpr (BPG == 2) {
+                            const uint2 v = *reinterpret_cast<const uint2 *>(base + coff[j]);
+                            xw[rr][0] = v.x; xw[rr][1] = v.y;
+                        } else {
+                            xw[rr][0] = *reinterpret_cast<const uint32_t *>(base + coff[j]);
+                        }
+                    }
+#pragma unroll
+                    for (int w = 0; w < BPG; ++w) {
+                        // B entries of (j, w, h = 0 / 1): a compile-time offset from the span base;
+                        // one load serves both row tiles
+                        const unsigned char *bb = (BPG == 8 && w >= 4) ? bb1 : bb0;
+                        const int eo = ((j * BPG + w) * 2) * 64 * MNT;
+                        const uint4 bq0 = *reinterpret_cast<const uint4 *>(bb + eo);
+                        const uint4 bq1 = *reinterpret_cast<const uint4 *>(bb + eo + 64 * MNT);
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            const uint32_t x0 = xw[2 * t][w], x1 = xw[2 * t + 1][w];
+                            const uint32_t t0 = x0 >> 8, t1 = x1 >> 8;
+                            uint32_t u0[8], u1[8];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const uint32_t mk = 0x00030003u << (2 * q);
+                                u0[q] = x0 & mk;
+                                u0[4 + q] = t0 & mk;
+                                u1[q] = x1 & mk;
+                                u1[4 + q] = t1 & mk;
+                            }
+                            mma16816(d[t], u0[0], u1[0], u0[1], u1[1], bq0.x, bq0.y);
+                            mma16816(d[t], u0[2], u1[2], u0[3], u1[3], bq0.z, bq0.w);
+                            mma16816(d[t], u0[4], u1[4], u0[5], u1[5], bq1.x, bq1.y);
+                            mma16816(d[t], u0[6], u1[6], u0[7], u1[7], bq1.z, bq1.w);
+                        }
+                    }
+                    // columns 2c, 2c+1 -> (beta, m, term); the block's scale (and zero point)
+                    // times (sum a' q - zp sum a'), both sums carrying 2^-24
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const float D0 = d[t][0], D1 = d[t][1], D2 = d[t][2], D3 = d[t][3];
+                        const uint16_t *ps = t ? psb : psa;
+                        const uint16_t *zs = t ? zsb : zsa;
+                        if constexpr (NT == 2) {
+                            const int bl = block_of_beta<BPG>(j, (2 * c) / MNT);
+                            const float sa = spw[bl * MP + m0];
+                            const float s0 = h2f(ps[pg + pb + bl]), s1 = h2f(ps[pg8 + pb + bl]);
+                            const float z0 = ZPT ? h2f(zs[pg + pb + bl]) : p.zpv;
+                            const float z1 = ZPT ? h2f(zs[pg8 + pb + bl]) : p.zpv;
+                            accs[2 * t][0] = fmaf(s0, (D0 + D1) - z0 * sa, accs[2 * t][0]);
+                            accs[2 * t + 1][0] = fmaf(s1, (D2 + D3) - z1 * sa, accs[2 * t + 1][0]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int bl = block_of_beta<BPG>(j, (2 * c + e) / MNT);
+                                const float sa = spw[bl * MP + (e ? m1 : m0)];
+                                const float s0 = h2f(ps[pg + pb + bl]), s1 = h2f(ps[pg8 + pb + bl]);
+                                const float z0 = ZPT ? h2f(zs[pg + pb + bl]) : p.zpv;
+                                const float z1 = ZPT ? h2f(zs[pg8 + pb + bl]) : p.zpv;
+                                accs[2 * t][e] = fmaf(s0, (e ? D1 : D0) - z0 * sa, accs[2 * t][e]);
+                                accs[2 * t + 1][e] = fmaf(s1, (e ? D3 : D2) - z1 * sa, accs[2 * t + 1][e]);
+                            }
+                        }
+                    }
+                }
+                // the span's own output multiplier 2^(10 + e)
+                const float om0 = somul[sp * MP + m0], om1 = somul[sp * MP + m1];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    acc[r][0] = fmaf(accs[r][0], om0, acc[r][0]);
+                    acc[r][1] = fmaf(accs[r][1], om1, acc[r][1]);
+                }
+            }
+        }
+        // this warp's span sums of the tile's 32 rows, for the producer (in the
+        // reduction slot of the tile's second fill): every lane of a row quad
+        // leaves its own partial of each (row, activation row) it holds, in slot c
+        // of [row][m][4], and the producer adds them (fixed order, no shuffles)
+        float *rw = red + (sb_ >> 1) * (W * kTileRows * MP * 4) + sl * kTileRows * MP * 4;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int row = g + 8 * r;  // rows g, g + 8, 16 + g, 24 + g
+            if (NT == 1 && MP == 1) {   // both columns are row 0: lane c's slot holds their sum
+                rw[row * 4 + c] = acc[r][0] + acc[r][1];
+            } else if (NT == 2) {       // one activation row per lane; MP x 4 slots, lanes of the same m add up
+                rw[(row * MP + m0) * 4 + c] = acc[r][0];
+            } else {                    // two activation rows per lane
+                rw[(row * MP + m0) * 4 + c] = acc[r][0];
+                rw[(row * MP + m1) * 4 + c] = acc[r][1];
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&empty[sa_]);
+            mbar_arrive(&empty[sb_]);
+        }
+        // the next tile's two fills
+        for (int step = 0; step < 2; ++step) {
+            if (++sa_ == p.NST) { sa_ = 0; pa ^= 1u; }
+            if (++sb_ == p.NST) { sb_ = 0; pbp ^= 1u; }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- host side
+struct MgCfg {
+    int MP, NT, spans, W, NST, ntiles, grid;
+    int b_off, sp_off, om_off, zero_off, stage_off, stage_bytes, par_off, zp_off, red_off, smem;
+};
+
+inline int rup(int x, int a) { return (x + a - 1) / a * a; }
+
+bool choose_mg(int M, int N, int K, int a_dtype, bool zpt, MgCfg &c) {
+    const DeviceInfo &di = device_info();
+    c.NT = a_dtype == 0 ? 2 : 1;
+    c.MP = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
+    if (c.MP * c.NT > 8) return false;
+    c.spans = K / kSpanCodes;
+    // consumer warps: the fewest that still give the smallest number of spans per warp
+    const int per = (c.spans + kMaxWarps - 1) / kMaxWarps;
+    c.W = (c.spans + per - 1) / per;
+    const int mnt = c.MP * c.NT;
+    const int nblk = c.spans * 8, nb = K / 64, row_bytes = K / 4;
+    c.b_off = kHeader;
+    c.sp_off = c.b_off + c.spans * 1024 * mnt;
+    c.om_off = c.sp_off + nblk * c.MP * 4;
+    c.zero_off = rup(c.om_off + c.spans * c.MP * 4, 16);
+    c.stage_off = rup(c.zero_off + 1024 * mnt, 1024);
+    // a stage: 16 whole weight rows, their codes then their block parameters
+    c.par_off = rup(kRows * row_bytes, 128);
+    c.zp_off = rup(c.par_off + kRows * nb * 2, 128);
+    c.stage_bytes = rup(c.zp_off + (zpt ? kRows * nb * 2 : 0), 128);
+    const int red_stage = c.W * kTileRows * c.MP * 4 * 4;
+    const int budget = di.max_smem_optin - 1024 - c.stage_off;  // 1024: alignment slack
+    // an even number of stages: a tile's second fill always lands in an odd
+    // stage, whose reduction slot (stage / 2) it owns
+    c.NST = std::min(kMaxStages, budget / (c.stage_bytes + red_stage / 2)) & ~1;
+    if (c.NST < 4) return false;  // at least two 32-row tiles in flight
+    c.red_off = c.stage_off + c.NST * c.stage_bytes;
+    c.smem = c.red_off + (c.NST / 2) * red_stage + 1024;
+    c.ntiles = (N + kTileRows - 1) / kTileRows;
+    c.grid = std::min(c.ntiles, di.sm_count);
+    return true;
+}
+
+template <int MP, int NT, bool ZPT>
+cudaError_t launch_mg(const MgArgs &a, const MgCfg &c, cudaStream_t s) {
+    auto kern = mma_gemv_kernel<MP, NT, ZPT>;
+    static std::atomic<unsigned> configured{0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const unsigned bit = 1u << (dev & 31);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, device_info().max_smem_optin);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const cudaError_t e = launch_pdl(kern, dim3(c.grid), dim3((c.W + 1) * 32), c.smem, s, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace
+
+bool mma_gemv_eligible(const GemmProblem &p) {
+    if (p.kind != WK_NBITS || p.bits != 2 || p.bs != 64 || p.K % kSpanCodes != 0) return false;
+    if (p.M < 1 || p.M > (p.a_dtype == 0 ? 4 : 8)) return false;
+    MgCfg c;
+    return choose_mg(p.M, p.N, p.K, p.a_dtype, p.zp_mode == ZP_TENSOR, c);
+}
+
+cudaError_t mma_gemv(const GemmProblem &p, cudaStream_t s) {
+    MgCfg c;
+    const bool zpt = p.zp_mode == ZP_TENSOR;
+    if (!choose_mg(p.M, p.N, p.K, p.a_dtype, zpt, c)) return cudaErrorNotSupported;
+    const int nb = p.K / p.bs;
+    MgArgs a{};
+    a.A = p.A;
+    a.a_dtype = p.a_dtype;
+    a.W = p.W;
+    a.scales = p.scales;
+    a.zp = p.zp;
+    a.row_bytes = p.K / 4;
+    a.zpv = p.uniform_zp;
+    a.Y = p.Y;
+    a.y_dtype = p.y_dtype;
+    a.M = p.M;
+    a.N = p.N;
+    a.K = p.K;
+    a.nb = nb;
+    a.spans = c.spans;
+    a.W_ = c.W;
+    a.NST = c.NST;
+    a.ntiles = c.ntiles;
+    a.b_off = c.b_off;
+    a.sp_off = c.sp_off;
+    a.om_off = c.om_off;
+    a.zero_off = c.zero_off;
+    a.stage_off = c.stage_off;
+    a.stage_bytes = c.stage_bytes;
+    a.par_off = c.par_off;
+    a.zp_off = c.zp_off;
+    a.red_off = c.red_off;
+    a.fault = fault_word();
+#define QG_MG(MP_, NT_)                                                                             \
+    if (c.MP == MP_ && c.NT == NT_)                                                                 \
+        return zpt ? launch_mg<MP_, NT_, true>(a, c, s) : launch_mg<MP_, NT_, false>(a, c, s);
+    QG_MG(1, 2)
+    QG_MG(2, 2)
+    QG_MG(4, 2)
+    QG_MG(1, 1)
+    QG_MG(2, 1)
+    QG_MG(4, 1)
+    QG_MG(8, 1)
+#undef QG_MG
+    return cudaErrorNotSupported;
+}
+
+}  // namespace qg

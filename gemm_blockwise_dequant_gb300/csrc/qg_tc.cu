@@ -813,8 +813,6 @@ TcArgs make_args(const GemmProblem &p, const TcCfg &c) {
 // activations stay on the SIMT path (rounding them to 16 bits would break the
 // 1e-4 bar), and so do shapes whose packed rows or parameter rows are not a
 // multiple of 16 bytes (the TMA row stride).
-void *tensor_map_encode_fn() { return reinterpret_cast<void *>(encode_fn()); }
-
 bool tc_eligible(int M, int K, int bits, int a_dtype, int bs, int kind) {
     if (M < 9 || a_dtype == 0) return false;
     if (bits == 3) return false;  // 3-bit codes (8 per 3 bytes) run on the SIMT path

@@ -1,0 +1,119 @@
+"""GPU parity of the 2-bit MatMulNBits GEMV / small-M GEMM that runs on warp-level
+MMAs (block 64, K a multiple of 512; M <= 4 with fp32 activations, M <= 8 with
+fp16 / bf16 ones): every column layout of the kernel (activation rows x fp16
+terms per block = 1, 2, 4 or 8), every zero-point mode and output type, K from
+one span to several ragged K chunks, N with a ragged last tile.
+
+Bars: max relative L2 1e-4 (fp32 activations and output), 5e-3 otherwise; the
+one-hot activations recover a dequantized weight column bit for bit; an
+all-zero activation row gives exact zeros; activation rows of very different
+magnitudes are normalised separately.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as WL
+from gpu_util import BF16, F16, F32, nbits_case, oracle_nbits, to64, tol_for, torch, y_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qg():
+    t = torch()
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gemm_blockwise_dequant_gb300 as qg
+    from gemm_blockwise_dequant_gb300 import build
+
+    build.build()
+    qg.lib()
+    return qg
+
+
+def _case(seed, M, N, K, ad, zp_mode):
+    g = WL.rng(seed)
+    d = dict(M=M, N=N, K=K, bits=2, block_size=64, a_dtype=ad)
+    d["W"] = WL.packed_codes(g, N, K, 2)
+    d["scales"] = WL.fp16_uniform(g, (N, K // 64), 0.01, 0.05)
+    d["zero_points"] = WL.fp16_uniform_int(g, (N, K // 64), 0, 3) if zp_mode == "tensor" else None
+    d["uniform_zp"] = 1.5 if zp_mode == "uniform" else None
+    d["A"] = WL.activations(g, M, K, ad)
+    return d
+
+
+def _run(qg, d, yd):
+    t = nbits_case(d)
+    Y = y_tensor(d["M"], d["N"], yd)
+    if d.get("uniform_zp") is not None:
+        qg.qgemm_nbits_uniform_zp(t["A"], t["W"], t["scales"], d["uniform_zp"], Y, bits=2, block_size=64)
+    else:
+        qg.qgemm_nbits(t["A"], t["W"], t["scales"], t["zero_points"], Y, bits=2, block_size=64)
+    torch().cuda.synchronize()
+    return Y
+
+
+CASES = [
+    # (M, N, K, a_dtype, zp_mode, y_dtype)
+    (1, 333, 512, F32, "uniform", F32),     # one span
+    (1, 17, 1536, F32, "tensor", F32),      # two tiles, the second with one row
+    (1, 1000, 5120, F32, "none", F32),
+    (1, 100, 17920, F32, "uniform", F32),   # 35 spans: three K chunks, the last one ragged
+    (1, 64, 8704, F32, "tensor", F32),      # 17 spans: two chunks of 9 and 8
+    (2, 301, 2048, F32, "tensor", F32),
+    (2, 96, 17920, F32, "uniform", F32),
+    (3, 150, 1536, F32, "uniform", F32),    # 3 rows in the 4-row layout
+    (4, 301, 5120, F32, "tensor", F32),
+    (4, 48, 1024, F32, "none", F16),
+    (1, 301, 5120, F16, "uniform", F32),
+    (1, 301, 17920, BF16, "tensor", BF16),
+    (2, 200, 2048, BF16, "none", F32),
+    (4, 130, 5120, F16, "tensor", F16),
+    (5, 97, 1536, BF16, "uniform", F32),    # 5 rows in the 8-row layout
+    (8, 97, 5120, F16, "uniform", F32),
+    (8, 40, 17920, BF16, "tensor", BF16),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "M%d_N%d_K%d_a%d_%s_y%d" % c)
+def test_mma_gemv_parity(qg, case):
+    M, N, K, ad, zpm, yd = case
+    d = _case(21, M, N, K, ad, zpm)
+    Y = _run(qg, d, yd)
+    err = O.max_rel_l2(to64(Y), oracle_nbits(d))
+    assert err <= tol_for(ad, yd), err
+
+
+@pytest.mark.parametrize("M", [1, 2, 4])
+def test_mma_gemv_onehot_exact(qg, M):
+    """A = e_k rows (fp32): each output is the dequantized weight w[n, k] bit for bit."""
+    N, K = 70, 1024
+    d = _case(5, M, N, K, F32, "tensor")
+    deq = O.dequant_nbits(d["W"], d["scales"], d["zero_points"], N=N, K=K, bits=2, block_size=64)
+    ks = [0, 1, 7, 8, 9, 15, 16, 63, 64, 255, 256, 511, 512, 777, 1000, 1023][: 4 * M]
+    for i in range(0, len(ks), M):
+        d["A"] = np.zeros((M, K), np.float32)
+        for m in range(M):
+            d["A"][m, ks[i + m]] = 1.0
+        Y = _run(qg, d, F32).cpu().numpy()
+        for m in range(M):
+            assert np.array_equal(Y[m], deq[:, ks[i + m]]), (M, ks[i + m])
+
+
+def test_mma_gemv_zero_row_and_separate_row_scales(qg):
+    """Row 0 all zeros (exact zero output), rows 1-3 of magnitudes 2^-60, 1 and 2^70:
+    each row is normalised by its own largest magnitude."""
+    M, N, K = 4, 200, 2048
+    d = _case(8, M, N, K, F32, "uniform")
+    A = d["A"].astype(np.float64)
+    A[0] = 0.0
+    A[1] *= 2.0 ** -60
+    A[3] *= 2.0 ** 70
+    d["A"] = A.astype(np.float32)
+    Y = _run(qg, d, F32)
+    y = Y.cpu().numpy()
+    assert np.all(y[0] == 0.0)
+    ref = oracle_nbits(d)
+    for m in (1, 2, 3):
+        assert O.max_rel_l2(to64(Y)[m:m + 1], ref[m:m + 1]) <= 1e-4, m
