@@ -212,8 +212,13 @@ __device__ __forceinline__ void build_span(const MgArgs &p, int sp, int lane, un
     }
 }
 
+// At most kMaxWarps + 1 warps of 32 threads: 416 x 152 registers fit the
+// 64 K register file (the B fragments a warp may keep take 64 of them).
+constexpr int kMaxRegs = 152;
+static_assert((kMaxWarps + 1) * 32 * kMaxRegs <= 65536, "register file");
+
 template <int MP, int NT, bool ZPT>
-__global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
+__global__ void __maxnreg__(kMaxRegs)
     mma_gemv_kernel(const MgArgs p) {
     constexpr int MNT = MP * NT;
     constexpr int BPG = 8 / MNT;
@@ -354,6 +359,26 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
     const int m1 = NT == 2 ? m0 : (2 * c + 1) % MP;
     const int pw = p.nb;  // parameters per row in a stage
     const int pg = g * pw, pg8 = (g + 8) * pw;
+    // With one or two fp16 columns per block a warp's B fragments for one span
+    // fit in 64 registers: a warp that owns a single span loads them once, here,
+    // instead of from shared memory for every tile.
+    constexpr bool BREG = MNT <= 2;
+    const bool one_span = p.spans <= W;
+    uint4 breg[BREG ? 8 : 1][2];  // [j * BPG + w][h]
+    auto load_breg = [&](int sp) {
+        const unsigned char *span_b = bfrag_w + static_cast<size_t>(sp) * 1024 * MNT + slot_b * 16;
+        const unsigned char *bb0 = nz0 ? span_b : zero_slab;
+        const unsigned char *bb1 = nz1 ? span_b : zero_slab;
+#pragma unroll
+        for (int jw = 0; jw < (BREG ? 8 : 1); ++jw) {
+            const int w = jw % BPG;
+            const unsigned char *bb = (BPG == 8 && w >= 4) ? bb1 : bb0;
+            const int eo = jw * 2 * 64 * MNT;
+            breg[jw][0] = *reinterpret_cast<const uint4 *>(bb + eo);
+            breg[jw][1] = *reinterpret_cast<const uint4 *>(bb + eo + 64 * MNT);
+        }
+    };
+    if (BREG && one_span) load_breg(sl);
     int sa_ = 0, sb_ = 1 % p.NST;
     uint32_t pa = 0, pbp = p.NST == 1 ? 1u : 0u;
     for (int i = 0; i < ntl; ++i) {
@@ -374,6 +399,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
                 const unsigned char *span_b = bfrag_w + static_cast<size_t>(sp) * 1024 * MNT + slot_b * 16;
                 const unsigned char *bb0 = nz0 ? span_b : zero_slab;
                 const unsigned char *bb1 = nz1 ? span_b : zero_slab;
+                if (BREG && !one_span) load_breg(sp);
                 const int pb = sp * 8;  // first block of the span
                 float accs[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
@@ -406,10 +432,16 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
                     for (int w = 0; w < BPG; ++w) {
                         // B entries of (j, w, h = 0 / 1): a compile-time offset from the span base;
                         // one load serves both row tiles
-                        const unsigned char *bb = (BPG == 8 && w >= 4) ? bb1 : bb0;
-                        const int eo = ((j * BPG + w) * 2) * 64 * MNT;
-                        const uint4 bq0 = *reinterpret_cast<const uint4 *>(bb + eo);
-                        const uint4 bq1 = *reinterpret_cast<const uint4 *>(bb + eo + 64 * MNT);
+                        uint4 bq0, bq1;
+                        if constexpr (BREG) {
+                            bq0 = breg[j * BPG + w][0];
+                            bq1 = breg[j * BPG + w][1];
+                        } else {
+                            const unsigned char *bb = (BPG == 8 && w >= 4) ? bb1 : bb0;
+                            const int eo = ((j * BPG + w) * 2) * 64 * MNT;
+                            bq0 = *reinterpret_cast<const uint4 *>(bb + eo);
+                            bq1 = *reinterpret_cast<const uint4 *>(bb + eo + 64 * MNT);
+                        }
 #pragma unroll
                         for (int t = 0; t < 2; ++t) {
                             const uint32_t x0 = xw[2 * t][w], x1 = xw[2 * t + 1][w];
