@@ -46,12 +46,10 @@
 namespace qg {
 namespace {
 
-constexpr int kRows = 16;          // weight rows per MMA row tile (the MMA's M) and per fill
-constexpr int kTileRows = 32;      // weight rows per tile: two MMA row tiles
 constexpr int kSpanBytes = 128;    // u2 code bytes of one row in a span: 512 codes, 8 blocks of 64
 constexpr int kSpanCodes = 512;
 constexpr int kMaxStages = 16;
-constexpr int kMaxWarps = 12;      // consumer warps (warp w owns spans w, w + W, ...)
+constexpr int kMaxWarps = 11;      // consumer warps (warp w owns spans w, w + W, ...)
 constexpr int kHeader = 512;       // barriers, abort flag, row exponents
 
 struct MgArgs {
@@ -212,16 +210,24 @@ __device__ __forceinline__ void build_span(const MgArgs &p, int sp, int lane, un
     }
 }
 
-// At most kMaxWarps + 1 warps of 32 threads: 416 x 152 registers fit the
-// 64 K register file (the B fragments a warp may keep take 64 of them).
+// At most kMaxWarps + 1 = 12 warps: three per SM sub-partition, whose 16 K
+// registers hold three warps of 152 registers (the B fragments a warp may keep
+// take 64 of them).
 constexpr int kMaxRegs = 152;
-static_assert((kMaxWarps + 1) * 32 * kMaxRegs <= 65536, "register file");
+static_assert((kMaxWarps + 1 + 3) / 4 * 32 * kMaxRegs <= 16384, "registers of one SM sub-partition");
 
-template <int MP, int NT, bool ZPT>
+// TR: MMA row tiles per tile.  TR = 2: 32-row tiles of two 16-row fills, the
+// block parameters copied into the stage with the codes.  TR = 1 (long K,
+// where the B fragments leave room for 8-row stages only): 16-row tiles of two
+// 8-row fills, the block parameters read from global memory.
+template <int MP, int NT, bool ZPT, int TR>
 __global__ void __maxnreg__(kMaxRegs)
     mma_gemv_kernel(const MgArgs p) {
     constexpr int MNT = MP * NT;
     constexpr int BPG = 8 / MNT;
+    constexpr int FR = 8 * TR;       // weight rows per fill
+    constexpr int TROWS = 16 * TR;   // weight rows per tile
+    constexpr bool PSMEM = TR == 2;  // block parameters in the stage
     static_assert(MNT >= 1 && MNT <= 8 && (8 % MNT) == 0, "columns per block");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -253,11 +259,11 @@ __global__ void __maxnreg__(kMaxRegs)
     pdl_launch_dependents();
     pdl_wait();
 
-    // A tile is 32 weight rows: two 16-row MMA row tiles.  Fill f of this CTA
-    // holds rows 16 (f % 2) .. + 15 of its tile f / 2 -- whole rows: their
-    // codes are one contiguous run of HBM, copied by ONE bulk copy, and their
-    // block parameters by one more (a copy instruction costs the TMA engine a
-    // fixed time, so few large copies keep HBM busy).
+    // A tile is TROWS weight rows (TR 16-row MMA row tiles).  Fill f of this CTA
+    // holds rows FR (f % 2) .. + FR - 1 of its tile f / 2 -- whole rows: their
+    // codes are one contiguous run of HBM, copied by ONE bulk copy, and (TR = 2)
+    // their block parameters by one more (a copy instruction costs the TMA
+    // engine a fixed time, so few large copies keep HBM busy).
     const int ntl = (p.ntiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                     static_cast<int>(gridDim.x);  // tiles of this CTA
     const int total = 2 * ntl;                    // fills of this CTA
@@ -269,14 +275,14 @@ __global__ void __maxnreg__(kMaxRegs)
         // of (2c) % MP (16-bit activations).
         auto finish = [&](int tl, int rslot) {  // add the warps' sums of tile tl of this CTA, write Y
             const int tile = blockIdx.x + tl * gridDim.x;
-            const float *r = red + (rslot >> 1) * (W * kTileRows * MP * 4);
-            for (int v = lane; v < kTileRows * MP; v += 32) {
+            const float *r = red + (rslot >> 1) * (W * TROWS * MP * 4);
+            for (int v = lane; v < TROWS * MP; v += 32) {
                 const int row = v / MP, m = v - row * MP;
-                const int n = tile * kTileRows + row;
+                const int n = tile * TROWS + row;
                 if (m >= p.M || n >= p.N) continue;
                 float s = 0.f;
                 for (int w = 0; w < W; ++w) {
-                    const float *q = r + (w * kTileRows * MP + v) * 4;
+                    const float *q = r + (w * TROWS * MP + v) * 4;
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
                         const bool mine = MP == 1 || (NT == 2 ? (cc % MP) == m : ((2 * cc) % MP == m || (2 * cc + 1) % MP == m));
@@ -301,15 +307,17 @@ __global__ void __maxnreg__(kMaxRegs)
             }
             if (lane == 0) {
                 const int tile = blockIdx.x + (f >> 1) * gridDim.x;
-                const int row0 = tile * kTileRows + kRows * (f & 1);
-                const int valid = max(0, min(kRows, p.N - row0));
+                const int row0 = tile * TROWS + FR * (f & 1);
+                const int valid = max(0, min(FR, p.N - row0));
                 unsigned char *st = stages + static_cast<size_t>(slot) * p.stage_bytes;
-                const uint32_t cb = valid * p.row_bytes, pb = valid * p.nb * 2;
+                const uint32_t cb = valid * p.row_bytes, pb = PSMEM ? valid * p.nb * 2 : 0;
                 mbar_arrive_expect_tx(&full[slot], cb + pb * (ZPT ? 2 : 1));
                 if (valid) {
                     bulk_g2s(st, p.W + static_cast<size_t>(row0) * p.row_bytes, cb, &full[slot]);
-                    bulk_g2s(st + p.par_off, p.scales + static_cast<size_t>(row0) * p.nb, pb, &full[slot]);
-                    if (ZPT) bulk_g2s(st + p.zp_off, p.zp + static_cast<size_t>(row0) * p.nb, pb, &full[slot]);
+                    if (PSMEM) {
+                        bulk_g2s(st + p.par_off, p.scales + static_cast<size_t>(row0) * p.nb, pb, &full[slot]);
+                        if (ZPT) bulk_g2s(st + p.zp_off, p.zp + static_cast<size_t>(row0) * p.nb, pb, &full[slot]);
+                    }
                 }
             }
             if (++slot == p.NST) {
@@ -358,7 +366,6 @@ __global__ void __maxnreg__(kMaxRegs)
     const int m0 = NT == 2 ? c % MP : (2 * c) % MP;
     const int m1 = NT == 2 ? m0 : (2 * c + 1) % MP;
     const int pw = p.nb;  // parameters per row in a stage
-    const int pg = g * pw, pg8 = (g + 8) * pw;
     // With one or two fp16 columns per block a warp's B fragments for one span
     // fit in 64 registers: a warp that owns a single span loads them once, here,
     // instead of from shared memory for every tile.
@@ -384,10 +391,15 @@ __global__ void __maxnreg__(kMaxRegs)
     for (int i = 0; i < ntl; ++i) {
         const bool ok = mbar_wait(&full[sa_], pa, abort_flag, p.fault, FAULT_WAIT_FULL) &&
                         mbar_wait(&full[sb_], pbp, abort_flag, p.fault, FAULT_WAIT_FULL);
-        float acc[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // [row g, g+8, 16+g, 24+g][column]
+        // the thread's rows: rr = 0 .. 2 TR - 1 is row g + 8 (rr % TR) of fill rr / TR,
+        // i.e. tile row (rr / TR) FR + g + 8 (rr % TR); MMA row tile t takes rr = 2t, 2t + 1
+        float acc[2 * TR][2];
+#pragma unroll
+        for (int r = 0; r < 2 * TR; ++r) acc[r][0] = acc[r][1] = 0.f;
+        const int tile_row0 = (blockIdx.x + i * gridDim.x) * TROWS;
         if (ok) {
-            const unsigned char *sta = stages + static_cast<size_t>(sa_) * p.stage_bytes;  // rows 0 .. 15
-            const unsigned char *stb = stages + static_cast<size_t>(sb_) * p.stage_bytes;  // rows 16 .. 31
+            const unsigned char *sta = stages + static_cast<size_t>(sa_) * p.stage_bytes;  // the tile's first fill
+            const unsigned char *stb = stages + static_cast<size_t>(sb_) * p.stage_bytes;  // its second fill
             const uint16_t *psa = reinterpret_cast<const uint16_t *>(sta + p.par_off);
             const uint16_t *psb = reinterpret_cast<const uint16_t *>(stb + p.par_off);
             const uint16_t *zsa = reinterpret_cast<const uint16_t *>(sta + p.zp_off);
@@ -401,17 +413,36 @@ __global__ void __maxnreg__(kMaxRegs)
                 const unsigned char *bb1 = nz1 ? span_b : zero_slab;
                 if (BREG && !one_span) load_breg(sp);
                 const int pb = sp * 8;  // first block of the span
-                float accs[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+                float accs[2 * TR][2];
+#pragma unroll
+                for (int r = 0; r < 2 * TR; ++r) accs[r][0] = accs[r][1] = 0.f;
+                // TR = 1: the block parameters of this span, read from global memory now so
+                // that the loads are in flight during the span's MMAs
+                float spre[PSMEM ? 1 : MNT][2][2], zpre[PSMEM ? 1 : MNT][2][2];
+                if constexpr (!PSMEM) {
+#pragma unroll
+                    for (int j = 0; j < MNT; ++j)
+#pragma unroll
+                        for (int r = 0; r < 2; ++r)
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int bl = block_of_beta<BPG>(j, (2 * c + (NT == 2 ? 0 : e)) / MNT);
+                                const int n = min(tile_row0 + r * FR + g, p.N - 1);  // rows past N: any row
+                                const size_t idx = static_cast<size_t>(n) * p.nb + pb + bl;
+                                spre[j][r][e] = h2f(__ldg(p.scales + idx));
+                                zpre[j][r][e] = ZPT ? h2f(__ldg(p.zp + idx)) : p.zpv;
+                            }
+                }
 #pragma unroll
                 for (int j = 0; j < MNT; ++j) {
-                    float d[2][4];  // [row tile][fragment]: the two row tiles are independent chains
+                    float d[TR][4];  // [row tile][fragment]: the row tiles are independent chains
 #pragma unroll
-                    for (int t = 0; t < 2; ++t) d[t][0] = d[t][1] = d[t][2] = d[t][3] = 0.f;
-                    // this thread's BPG code words of rows g, g + 8, 16 + g, 24 + g (vector loads)
-                    uint32_t xw[4][BPG];
+                    for (int t = 0; t < TR; ++t) d[t][0] = d[t][1] = d[t][2] = d[t][3] = 0.f;
+                    // this thread's BPG code words of its 2 TR rows (vector loads)
+                    uint32_t xw[2 * TR][BPG];
 #pragma unroll
-                    for (int rr = 0; rr < 4; ++rr) {
-                        const unsigned char *base = (rr < 2 ? ca : cb) + ((rr & 1) ? r8 : 0);
+                    for (int rr = 0; rr < 2 * TR; ++rr) {
+                        const unsigned char *base = (rr / TR ? cb : ca) + (rr % TR) * r8;
                         if constexpr (BPG == 8) {
 #pragma unroll
                             for (int hb = 0; hb < 2; ++hb) {
@@ -443,7 +474,7 @@ __global__ void __maxnreg__(kMaxRegs)
                             bq1 = *reinterpret_cast<const uint4 *>(bb + eo + 64 * MNT);
                         }
 #pragma unroll
-                        for (int t = 0; t < 2; ++t) {
+                        for (int t = 0; t < TR; ++t) {
                             const uint32_t x0 = xw[2 * t][w], x1 = xw[2 * t + 1][w];
                             const uint32_t t0 = x0 >> 8, t1 = x1 >> 8;
                             uint32_t u0[8], u1[8];
@@ -464,49 +495,54 @@ __global__ void __maxnreg__(kMaxRegs)
                     // columns 2c, 2c+1 -> (beta, m, term); the block's scale (and zero point)
                     // times (sum a' q - zp sum a'), both sums carrying 2^-24
 #pragma unroll
-                    for (int t = 0; t < 2; ++t) {
+                    for (int t = 0; t < TR; ++t) {
                         const float D0 = d[t][0], D1 = d[t][1], D2 = d[t][2], D3 = d[t][3];
-                        const uint16_t *ps = t ? psb : psa;
-                        const uint16_t *zs = t ? zsb : zsa;
-                        if constexpr (NT == 2) {
-                            const int bl = block_of_beta<BPG>(j, (2 * c) / MNT);
-                            const float sa = spw[bl * MP + m0];
-                            const float s0 = h2f(ps[pg + pb + bl]), s1 = h2f(ps[pg8 + pb + bl]);
-                            const float z0 = ZPT ? h2f(zs[pg + pb + bl]) : p.zpv;
-                            const float z1 = ZPT ? h2f(zs[pg8 + pb + bl]) : p.zpv;
-                            accs[2 * t][0] = fmaf(s0, (D0 + D1) - z0 * sa, accs[2 * t][0]);
-                            accs[2 * t + 1][0] = fmaf(s1, (D2 + D3) - z1 * sa, accs[2 * t + 1][0]);
-                        } else {
+                        // rows rr = 2t and 2t + 1: fill rr / TR, row g + 8 (rr % TR) of it
+                        const uint16_t *ps0 = ((2 * t) / TR ? psb : psa) + (g + 8 * ((2 * t) % TR)) * pw;
+                        const uint16_t *ps1 = ((2 * t + 1) / TR ? psb : psa) + (g + 8 * ((2 * t + 1) % TR)) * pw;
+                        const uint16_t *zs0 = ((2 * t) / TR ? zsb : zsa) + (g + 8 * ((2 * t) % TR)) * pw;
+                        const uint16_t *zs1 = ((2 * t + 1) / TR ? zsb : zsa) + (g + 8 * ((2 * t + 1) % TR)) * pw;
 #pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const int bl = block_of_beta<BPG>(j, (2 * c + e) / MNT);
-                                const float sa = spw[bl * MP + (e ? m1 : m0)];
-                                const float s0 = h2f(ps[pg + pb + bl]), s1 = h2f(ps[pg8 + pb + bl]);
-                                const float z0 = ZPT ? h2f(zs[pg + pb + bl]) : p.zpv;
-                                const float z1 = ZPT ? h2f(zs[pg8 + pb + bl]) : p.zpv;
-                                accs[2 * t][e] = fmaf(s0, (e ? D1 : D0) - z0 * sa, accs[2 * t][e]);
-                                accs[2 * t + 1][e] = fmaf(s1, (e ? D3 : D2) - z1 * sa, accs[2 * t + 1][e]);
+                        for (int e = 0; e < (NT == 2 ? 1 : 2); ++e) {
+                            const int bl = block_of_beta<BPG>(j, (2 * c + e) / MNT);
+                            const float sa = spw[bl * MP + (e ? m1 : m0)];
+                            float s0, s1, z0, z1;
+                            if constexpr (PSMEM) {
+                                s0 = h2f(ps0[pb + bl]);
+                                s1 = h2f(ps1[pb + bl]);
+                                z0 = ZPT ? h2f(zs0[pb + bl]) : p.zpv;
+                                z1 = ZPT ? h2f(zs1[pb + bl]) : p.zpv;
+                            } else {
+                                s0 = spre[PSMEM ? 0 : j][0][e];
+                                s1 = spre[PSMEM ? 0 : j][1][e];
+                                z0 = zpre[PSMEM ? 0 : j][0][e];
+                                z1 = zpre[PSMEM ? 0 : j][1][e];
                             }
+                            // NT = 2: columns 2c, 2c + 1 are the hi / lo terms of one block and row
+                            const float P0 = NT == 2 ? D0 + D1 : (e ? D1 : D0);
+                            const float P1 = NT == 2 ? D2 + D3 : (e ? D3 : D2);
+                            accs[2 * t][e] = fmaf(s0, P0 - z0 * sa, accs[2 * t][e]);
+                            accs[2 * t + 1][e] = fmaf(s1, P1 - z1 * sa, accs[2 * t + 1][e]);
                         }
                     }
                 }
                 // the span's own output multiplier 2^(10 + e)
                 const float om0 = somul[sp * MP + m0], om1 = somul[sp * MP + m1];
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
+                for (int r = 0; r < 2 * TR; ++r) {
                     acc[r][0] = fmaf(accs[r][0], om0, acc[r][0]);
                     acc[r][1] = fmaf(accs[r][1], om1, acc[r][1]);
                 }
             }
         }
-        // this warp's span sums of the tile's 32 rows, for the producer (in the
+        // this warp's span sums of the tile's rows, for the producer (in the
         // reduction slot of the tile's second fill): every lane of a row quad
         // leaves its own partial of each (row, activation row) it holds, in slot c
         // of [row][m][4], and the producer adds them (fixed order, no shuffles)
-        float *rw = red + (sb_ >> 1) * (W * kTileRows * MP * 4) + sl * kTileRows * MP * 4;
+        float *rw = red + (sb_ >> 1) * (W * TROWS * MP * 4) + sl * TROWS * MP * 4;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int row = g + 8 * r;  // rows g, g + 8, 16 + g, 24 + g
+        for (int r = 0; r < 2 * TR; ++r) {
+            const int row = (r / TR) * FR + g + 8 * (r % TR);  // tile row of the thread's row r
             if (NT == 1 && MP == 1) {   // both columns are row 0: lane c's slot holds their sum
                 rw[row * 4 + c] = acc[r][0] + acc[r][1];
             } else if (NT == 2) {       // one activation row per lane; MP x 4 slots, lanes of the same m add up
@@ -531,13 +567,14 @@ __global__ void __maxnreg__(kMaxRegs)
 
 // ---------------------------------------------------------------- host side
 struct MgCfg {
-    int MP, NT, spans, W, NST, ntiles, grid;
+    int MP, NT, TR, spans, W, NST, ntiles, grid;
     int b_off, sp_off, om_off, zero_off, stage_off, stage_bytes, par_off, zp_off, red_off, smem;
 };
 
 inline int rup(int x, int a) { return (x + a - 1) / a * a; }
 
-bool choose_mg(int M, int N, int K, int a_dtype, bool zpt, MgCfg &c) {
+bool choose_mg1(int M, int N, int K, int a_dtype, bool zpt, int tr, MgCfg &c) {
+    c.TR = tr;
     const DeviceInfo &di = device_info();
     c.NT = a_dtype == 0 ? 2 : 1;
     c.MP = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
@@ -553,11 +590,12 @@ bool choose_mg(int M, int N, int K, int a_dtype, bool zpt, MgCfg &c) {
     c.om_off = c.sp_off + nblk * c.MP * 4;
     c.zero_off = rup(c.om_off + c.spans * c.MP * 4, 16);
     c.stage_off = rup(c.zero_off + 1024 * mnt, 1024);
-    // a stage: 16 whole weight rows, their codes then their block parameters
-    c.par_off = rup(kRows * row_bytes, 128);
-    c.zp_off = rup(c.par_off + kRows * nb * 2, 128);
-    c.stage_bytes = rup(c.zp_off + (zpt ? kRows * nb * 2 : 0), 128);
-    const int red_stage = c.W * kTileRows * c.MP * 4 * 4;
+    // a stage: FR whole weight rows, their codes then (TR = 2) their block parameters
+    const int fr = 8 * c.TR;
+    c.par_off = rup(fr * row_bytes, 128);
+    c.zp_off = rup(c.par_off + (c.TR == 2 ? fr * nb * 2 : 0), 128);
+    c.stage_bytes = rup(c.zp_off + (zpt && c.TR == 2 ? fr * nb * 2 : 0), 128);
+    const int red_stage = c.W * 16 * c.TR * c.MP * 4 * 4;
     const int budget = di.max_smem_optin - 1024 - c.stage_off;  // 1024: alignment slack
     // an even number of stages: a tile's second fill always lands in an odd
     // stage, whose reduction slot (stage / 2) it owns
@@ -565,14 +603,22 @@ bool choose_mg(int M, int N, int K, int a_dtype, bool zpt, MgCfg &c) {
     if (c.NST < 4) return false;  // at least two 32-row tiles in flight
     c.red_off = c.stage_off + c.NST * c.stage_bytes;
     c.smem = c.red_off + (c.NST / 2) * red_stage + 1024;
-    c.ntiles = (N + kTileRows - 1) / kTileRows;
+    c.ntiles = (N + 16 * c.TR - 1) / (16 * c.TR);
     c.grid = std::min(c.ntiles, di.sm_count);
     return true;
 }
 
-template <int MP, int NT, bool ZPT>
+// 32-row tiles with the block parameters in the stage, or, when those stages
+// do not fit beside the B fragments (long K), 16-row tiles of 8-row fills
+// (the one-row-quad activation layouts only).
+bool choose_mg(int M, int N, int K, int a_dtype, bool zpt, MgCfg &c) {
+    if (choose_mg1(M, N, K, a_dtype, zpt, 2, c)) return true;
+    return (M <= 1) && choose_mg1(M, N, K, a_dtype, zpt, 1, c);
+}
+
+template <int MP, int NT, bool ZPT, int TR>
 cudaError_t launch_mg(const MgArgs &a, const MgCfg &c, cudaStream_t s) {
-    auto kern = mma_gemv_kernel<MP, NT, ZPT>;
+    auto kern = mma_gemv_kernel<MP, NT, ZPT, TR>;
     static std::atomic<unsigned> configured{0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -630,8 +676,12 @@ cudaError_t mma_gemv(const GemmProblem &p, cudaStream_t s) {
     a.red_off = c.red_off;
     a.fault = fault_word();
 #define QG_MG(MP_, NT_)                                                                             \
-    if (c.MP == MP_ && c.NT == NT_)                                                                 \
-        return zpt ? launch_mg<MP_, NT_, true>(a, c, s) : launch_mg<MP_, NT_, false>(a, c, s);
+    if (c.MP == MP_ && c.NT == NT_ && c.TR == 2)                                                    \
+        return zpt ? launch_mg<MP_, NT_, true, 2>(a, c, s) : launch_mg<MP_, NT_, false, 2>(a, c, s);
+    if (c.TR == 1 && c.MP == 1) {
+        if (c.NT == 2) return zpt ? launch_mg<1, 2, true, 1>(a, c, s) : launch_mg<1, 2, false, 1>(a, c, s);
+        return zpt ? launch_mg<1, 1, true, 1>(a, c, s) : launch_mg<1, 1, false, 1>(a, c, s);
+    }
     QG_MG(1, 2)
     QG_MG(2, 2)
     QG_MG(4, 2)
