@@ -39,7 +39,7 @@ METRIC = "M=1 quantized GEMV weight GB/s (% of GB300 HBM peak) and µs/call"
 SHAPES = ["qkv", "o", "gate_up", "down", "lm_head"]
 BITS, BS, ZP = 2, 64, 1.5
 L2_BYTES = 129 * 1024 * 1024
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemv_u2_m1_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "mma_gemv_u2_m1_traffic.json")
 
 
 def weight_bytes(N, K):
@@ -48,7 +48,7 @@ def weight_bytes(N, K):
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("qg_simt.cu", "qg_device.cuh"):
+    for f in ("qg_mma_gemv.cu", "qg_device.cuh"):
         with open(os.path.join(ROOT, "gemm_blockwise_dequant_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -531,7 +531,7 @@ def run_ours(args, world, rank, local):
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "gemv_kernel u2 M=1 (K=5120 launches: qkv, o, gate_up, lm_head)",
+                     "kernel": "mma_gemv_kernel u2 M=1 (K=5120 launches: qkv, o, gate_up, lm_head)",
                      "peak_kind": peak_kind},
         "e2e": {"value": round(world * per_step / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -862,6 +862,7 @@ def run_probe(name):
     gemv_k5120   3 warm-up calls, then one call, of each K=5120 phi4 u2 M=1 shape
                  (qkv, o, gate_up, lm_head): the launches of the dominant kernel
     gemv_lm_head 4 calls of the lm_head shape (100352 x 5120, u2, M=1)
+    gemv_down    4 calls of the down shape (5120 x 17920, u2, M=1)
     tc_prefill   4 calls of a prefill-sized u2 GEMM on the tensor cores
                  (M=2048, N=K=5120, fp16 activations, fp32 out)
     tc_nf4_m64   4 calls of the NF4 codebook GEMM 14336 x 4096 at M=64 (bf16, tensor cores)
@@ -895,8 +896,8 @@ def run_probe(name):
                 c()
         for c in calls:
             c()
-    elif name == "gemv_lm_head":
-        c = nbits(WL.phi4_u2("lm_head", M=1))
+    elif name in ("gemv_lm_head", "gemv_down"):
+        c = nbits(WL.phi4_u2(name[5:], M=1))
         for _ in range(4):
             c()
     elif name == "tc_prefill":
@@ -961,7 +962,7 @@ def main():
                     help="steps per CUDA graph in the timed region (each step is 5 GEMV launches)")
     ap.add_argument("--clocks-log", default=None,
                     help="file for the raw nvidia-smi samples of the timed region (%%d: GPU index); default a temp file")
-    ap.add_argument("--probe", choices=["gemv_k5120", "gemv_lm_head", "tc_prefill", "tc_nf4_m64", "qmoe",
+    ap.add_argument("--probe", choices=["gemv_k5120", "gemv_lm_head", "gemv_down", "tc_prefill", "tc_nf4_m64", "qmoe",
                                         "qmoe_dp4a", "ragged", "gather"],
                     help="run a small fixed workload for a profiler capture instead of the benchmark")
     ap.add_argument("--suite", action="store_true",

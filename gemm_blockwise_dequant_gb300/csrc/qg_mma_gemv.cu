@@ -51,6 +51,7 @@ constexpr int kSpanCodes = 512;
 constexpr int kMaxStages = 16;
 constexpr int kMaxWarps = 11;      // consumer warps (warp w owns spans w, w + W, ...)
 constexpr int kHeader = 512;       // barriers, abort flag, row exponents
+constexpr int kPqBytes = 2 * 16 * 16;  // two buffers of 16 rows x 8 fp16 block parameters
 
 struct MgArgs {
     const void *A;
@@ -65,9 +66,17 @@ struct MgArgs {
     int spans;        // K / 512
     int W_;           // consumer warps: warp w owns spans w, w + W_, ...
     int NST, ntiles;  // ring stages (16-row fills), 32-row tiles
-    int b_off, sp_off, om_off, zero_off, stage_off, stage_bytes, par_off, zp_off, red_off;
+    int b_off, sp_off, om_off, zero_off, stage_off, stage_bytes, par_off, zp_off, red_off, pq_off;
     unsigned *fault;
 };
+
+// 16-byte global -> shared copy that completes asynchronously (cp.async,
+// bypassing L1), and the wait for every such copy this thread issued
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -124,89 +133,101 @@ __device__ __forceinline__ void owner_of(int blk, int wd, int &j, int &c, int &w
 }
 
 // One warp prepares span sp: lane L owns code word L (block L / 4, word L % 4,
-// codes k = 512 sp + 16 L .. + 15).  Per activation row m: the span's largest
-// |a| gives e and a' = a * 2^(14 - e); the lane writes the B entries of its
-// word (fp16 a' * 2^-p, split into hi / lo terms for fp32 activations); the
-// block's four lanes add the sum of a' in a fixed order (2^-24 sum stored in
-// spart); lane 0 stores the span's output multiplier 2^(10 + e).
+// codes k = 512 sp + 16 L .. + 15).  Lane L's 16 activations of span sp,
+// activation row m: zeros for rows m >= M.
+__device__ __forceinline__ void load_span_act(const MgArgs &p, int sp, int m, int lane, float (&a)[16]) {
+    const size_t k0 = static_cast<size_t>(sp) * kSpanCodes + 16 * lane;
+    if (m >= p.M) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a[i] = 0.f;
+    } else if (p.a_dtype == 0) {
+        const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(p.A) + m * static_cast<size_t>(p.K) + k0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 v = __ldg(src + q);
+            a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
+        }
+    } else {
+        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.A) + m * static_cast<size_t>(p.K) + k0);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const uint4 v = __ldg(src + q);
+            const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const uint16_t lo = static_cast<uint16_t>(ww[r] & 0xFFFFu), hi = static_cast<uint16_t>(ww[r] >> 16);
+                a[8 * q + 2 * r] = p.a_dtype == 1 ? h2f(lo) : bf2f(lo);
+                a[8 * q + 2 * r + 1] = p.a_dtype == 1 ? h2f(hi) : bf2f(hi);
+            }
+        }
+    }
+}
+
+// One activation row m of span sp (its activations `a`, loaded by
+// load_span_act): the span's largest magnitude |a| gives e and
+// a' = a * 2^(14 - e); the lane writes the B entries of its word (fp16
+// a' * 2^-p, split into hi / lo terms for fp32 activations); the block's four
+// lanes add the sum of a' in a fixed order (2^-24 sum stored in spart); lane 0
+// stores the span's output multiplier 2^(10 + e).
 template <int MP, int NT>
-__device__ __forceinline__ void build_span(const MgArgs &p, int sp, int lane, unsigned char *bfrag, float *spart,
-                                           float *somul) {
+__device__ __forceinline__ void build_span_row(int sp, int m, int lane, float (&a)[16], unsigned char *bfrag,
+                                               float *spart, float *somul) {
     constexpr int MNT = MP * NT;
     constexpr int BPG = 8 / MNT;
     const int blk = lane >> 2, wd = lane & 3;
     int j, c, w;
     owner_of<BPG>(blk, wd, j, c, w);
-    const size_t k0 = static_cast<size_t>(sp) * kSpanCodes + 16 * lane;
+    float mx = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(a[i]));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    // e clamped to [-110, 117]: both 2^(14 - e) and 2^(10 + e) stay normal
+    const unsigned bits = __float_as_uint(mx);
+    const int ef = static_cast<int>((bits >> 23) & 0xFFu);
+    const int e = (bits == 0u || ef == 255) ? 0 : min(max(ef - 127, -110), 117);
+    const float asc = exp2i(14 - e);
+    float bs = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        a[i] *= asc;
+        bs += a[i];
+    }
+    bs += __shfl_xor_sync(0xffffffffu, bs, 1);
+    bs += __shfl_xor_sync(0xffffffffu, bs, 2);
+    if (wd == 0) spart[(sp * 8 + blk) * MP + m] = bs * 5.9604644775390625e-08f;  // 2^-24
+    if (lane == 0) somul[sp * MP + m] = exp2i(10 + e);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const int slot = (m * NT + t) * 4 + c;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t regs[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int i = 2 * (2 * h + (q >> 1)) + (q & 1);  // codes i and i + 8 of the word
+                const float pinv = exp2i(-2 * (i & 3));           // 2^-p
+                const float x0 = a[i] * pinv, x1 = a[i + 8] * pinv;
+                const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+                const uint16_t v0 = t == 0 ? __half_as_ushort(h0) : __half_as_ushort(__float2half_rn(x0 - __half2float(h0)));
+                const uint16_t v1 = t == 0 ? __half_as_ushort(h1) : __half_as_ushort(__float2half_rn(x1 - __half2float(h1)));
+                regs[q] = static_cast<uint32_t>(v0) | (static_cast<uint32_t>(v1) << 16);
+            }
+            *reinterpret_cast<uint4 *>(bfrag + static_cast<size_t>(b_entry<MNT>(sp, j, w, h, slot)) * 16) =
+                make_uint4(regs[0], regs[1], regs[2], regs[3]);
+        }
+    }
+}
+
+// The B fragments, block sums and output multipliers of span sp.
+template <int MP, int NT>
+__device__ __forceinline__ void build_span(const MgArgs &p, int sp, int lane, unsigned char *bfrag, float *spart,
+                                           float *somul) {
 #pragma unroll 1
     for (int m = 0; m < MP; ++m) {
         float a[16];
-        if (m < p.M) {
-            if (p.a_dtype == 0) {
-                const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(p.A) + m * static_cast<size_t>(p.K) + k0);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 v = __ldg(src + q);
-                    a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
-                }
-            } else {
-                const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.A) + m * static_cast<size_t>(p.K) + k0);
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const uint4 v = __ldg(src + q);
-                    const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const uint16_t lo = static_cast<uint16_t>(ww[r] & 0xFFFFu), hi = static_cast<uint16_t>(ww[r] >> 16);
-                        a[8 * q + 2 * r] = p.a_dtype == 1 ? h2f(lo) : bf2f(lo);
-                        a[8 * q + 2 * r + 1] = p.a_dtype == 1 ? h2f(hi) : bf2f(hi);
-                    }
-                }
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) a[i] = 0.f;
-        }
-        float mx = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(a[i]));
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        // e clamped to [-110, 117]: both 2^(14 - e) and 2^(10 + e) stay normal
-        const unsigned bits = __float_as_uint(mx);
-        const int ef = static_cast<int>((bits >> 23) & 0xFFu);
-        const int e = (bits == 0u || ef == 255) ? 0 : min(max(ef - 127, -110), 117);
-        const float asc = exp2i(14 - e);
-        float bs = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            a[i] *= asc;
-            bs += a[i];
-        }
-        bs += __shfl_xor_sync(0xffffffffu, bs, 1);
-        bs += __shfl_xor_sync(0xffffffffu, bs, 2);
-        if (wd == 0) spart[(sp * 8 + blk) * MP + m] = bs * 5.9604644775390625e-08f;  // 2^-24
-        if (lane == 0) somul[sp * MP + m] = exp2i(10 + e);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            const int slot = (m * NT + t) * 4 + c;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t regs[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int i = 2 * (2 * h + (q >> 1)) + (q & 1);  // codes i and i + 8 of the word
-                    const float pinv = exp2i(-2 * (i & 3));           // 2^-p
-                    const float x0 = a[i] * pinv, x1 = a[i + 8] * pinv;
-                    const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-                    const uint16_t v0 = t == 0 ? __half_as_ushort(h0) : __half_as_ushort(__float2half_rn(x0 - __half2float(h0)));
-                    const uint16_t v1 = t == 0 ? __half_as_ushort(h1) : __half_as_ushort(__float2half_rn(x1 - __half2float(h1)));
-                    regs[q] = static_cast<uint32_t>(v0) | (static_cast<uint32_t>(v1) << 16);
-                }
-                *reinterpret_cast<uint4 *>(bfrag + static_cast<size_t>(b_entry<MNT>(sp, j, w, h, slot)) * 16) =
-                    make_uint4(regs[0], regs[1], regs[2], regs[3]);
-            }
-        }
+        load_span_act(p, sp, m, lane, a);
+        build_span_row<MP, NT>(sp, m, lane, a, bfrag, spart, somul);
     }
 }
 
@@ -345,7 +366,19 @@ __global__ void __maxnreg__(kMaxRegs)
     // lanes of a block add its activation sum in a fixed order.
     const int g = lane >> 2, c = lane & 3;
     const int sl = warp;
-    for (int sp = sl; sp < p.spans; sp += W) build_span<MP, NT>(p, sp, lane, bfrag_w, spart, somul);
+    if constexpr (MP == 1) {  // the next span's activations load while this one is built
+        float a[16], an[16];
+        if (sl < p.spans) load_span_act(p, sl, 0, lane, a);
+#pragma unroll 1
+        for (int sp = sl; sp < p.spans; sp += W) {
+            if (sp + W < p.spans) load_span_act(p, sp + W, 0, lane, an);
+            build_span_row<MP, NT>(sp, 0, lane, a, bfrag_w, spart, somul);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) a[i] = an[i];
+        }
+    } else {
+        for (int sp = sl; sp < p.spans; sp += W) build_span<MP, NT>(p, sp, lane, bfrag_w, spart, somul);
+    }
     __syncwarp();
 
     // ------------------------------------------------------------ consumers: tiles
@@ -386,6 +419,22 @@ __global__ void __maxnreg__(kMaxRegs)
         }
     };
     if (BREG && one_span) load_breg(sl);
+    // TR = 1: the block parameters stay in global memory; the warp copies the
+    // ones of its next (tile, span) item -- 16 rows x the span's 8 blocks, a
+    // 16-byte run per row -- into one of its two buffers while it works on the
+    // current item (lanes 0-15 the scales, 16-31 the zero points)
+    unsigned char *pq = smem + p.pq_off + sl * kPqBytes * (ZPT ? 2 : 1);
+    auto fetch_params = [&](int row0, int spn, int buf) {
+        const int rr = lane & 15;
+        if (ZPT || lane < 16) {
+            const int n = min(row0 + rr, p.N - 1);  // rows past N: any row
+            const uint16_t *src = (lane < 16 ? p.scales : p.zp) + static_cast<size_t>(n) * p.nb + spn * 8;
+            cp_async16(pq + (buf * (ZPT ? 2 : 1) + (lane >> 4)) * (kPqBytes / 2) + rr * 16, src);
+        }
+        cp_async_commit();
+    };
+    int pqb = 0;
+    if (!PSMEM && ntl > 0) fetch_params(blockIdx.x * TROWS, sl, 0);
     int sa_ = 0, sb_ = 1 % p.NST;
     uint32_t pa = 0, pbp = p.NST == 1 ? 1u : 0u;
     for (int i = 0; i < ntl; ++i) {
@@ -416,22 +465,17 @@ __global__ void __maxnreg__(kMaxRegs)
                 float accs[2 * TR][2];
 #pragma unroll
                 for (int r = 0; r < 2 * TR; ++r) accs[r][0] = accs[r][1] = 0.f;
-                // TR = 1: the block parameters of this span, read from global memory now so
-                // that the loads are in flight during the span's MMAs
-                float spre[PSMEM ? 1 : MNT][2][2], zpre[PSMEM ? 1 : MNT][2][2];
+                // TR = 1: this item's parameters have landed (each lane waits for its own
+                // copies; the warp barrier shows them to every lane and ends every
+                // lane's reads of the other buffer); start the next item's copy
+                const uint16_t *pqs = reinterpret_cast<const uint16_t *>(pq + pqb * (ZPT ? 2 : 1) * (kPqBytes / 2));
                 if constexpr (!PSMEM) {
-#pragma unroll
-                    for (int j = 0; j < MNT; ++j)
-#pragma unroll
-                        for (int r = 0; r < 2; ++r)
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const int bl = block_of_beta<BPG>(j, (2 * c + (NT == 2 ? 0 : e)) / MNT);
-                                const int n = min(tile_row0 + r * FR + g, p.N - 1);  // rows past N: any row
-                                const size_t idx = static_cast<size_t>(n) * p.nb + pb + bl;
-                                spre[j][r][e] = h2f(__ldg(p.scales + idx));
-                                zpre[j][r][e] = ZPT ? h2f(__ldg(p.zp + idx)) : p.zpv;
-                            }
+                    cp_async_wait_all();
+                    __syncwarp();
+                    if (sp + W < p.spans)
+                        fetch_params(tile_row0, sp + W, pqb ^ 1);
+                    else if (i + 1 < ntl)
+                        fetch_params(tile_row0 + static_cast<int>(gridDim.x) * TROWS, sl, pqb ^ 1);
                 }
 #pragma unroll
                 for (int j = 0; j < MNT; ++j) {
@@ -513,10 +557,10 @@ __global__ void __maxnreg__(kMaxRegs)
                                 z0 = ZPT ? h2f(zs0[pb + bl]) : p.zpv;
                                 z1 = ZPT ? h2f(zs1[pb + bl]) : p.zpv;
                             } else {
-                                s0 = spre[PSMEM ? 0 : j][0][e];
-                                s1 = spre[PSMEM ? 0 : j][1][e];
-                                z0 = zpre[PSMEM ? 0 : j][0][e];
-                                z1 = zpre[PSMEM ? 0 : j][1][e];
+                                s0 = h2f(pqs[g * 8 + bl]);         // tile row g
+                                s1 = h2f(pqs[(g + 8) * 8 + bl]);   // tile row g + 8
+                                z0 = ZPT ? h2f(pqs[128 + g * 8 + bl]) : p.zpv;
+                                z1 = ZPT ? h2f(pqs[128 + (g + 8) * 8 + bl]) : p.zpv;
                             }
                             // NT = 2: columns 2c, 2c + 1 are the hi / lo terms of one block and row
                             const float P0 = NT == 2 ? D0 + D1 : (e ? D1 : D0);
@@ -533,6 +577,7 @@ __global__ void __maxnreg__(kMaxRegs)
                     acc[r][0] = fmaf(accs[r][0], om0, acc[r][0]);
                     acc[r][1] = fmaf(accs[r][1], om1, acc[r][1]);
                 }
+                pqb ^= 1;
             }
         }
         // this warp's span sums of the tile's rows, for the producer (in the
@@ -563,12 +608,13 @@ __global__ void __maxnreg__(kMaxRegs)
             if (++sb_ == p.NST) { sb_ = 0; pbp ^= 1u; }
         }
     }
+    if (!PSMEM) cp_async_wait_all();  // no copy outlives the CTA (after a give-up)
 }
 
 // ---------------------------------------------------------------- host side
 struct MgCfg {
     int MP, NT, TR, spans, W, NST, ntiles, grid;
-    int b_off, sp_off, om_off, zero_off, stage_off, stage_bytes, par_off, zp_off, red_off, smem;
+    int b_off, sp_off, om_off, zero_off, stage_off, stage_bytes, par_off, zp_off, red_off, pq_off, smem;
 };
 
 inline int rup(int x, int a) { return (x + a - 1) / a * a; }
@@ -596,13 +642,16 @@ bool choose_mg1(int M, int N, int K, int a_dtype, bool zpt, int tr, MgCfg &c) {
     c.zp_off = rup(c.par_off + (c.TR == 2 ? fr * nb * 2 : 0), 128);
     c.stage_bytes = rup(c.zp_off + (zpt && c.TR == 2 ? fr * nb * 2 : 0), 128);
     const int red_stage = c.W * 16 * c.TR * c.MP * 4 * 4;
-    const int budget = di.max_smem_optin - 1024 - c.stage_off;  // 1024: alignment slack
+    // TR = 1: each consumer warp's two buffers of one span's block parameters of a tile
+    const int pq_bytes = c.TR == 1 ? c.W * kPqBytes * (zpt ? 2 : 1) : 0;
+    const int budget = di.max_smem_optin - 1024 - c.stage_off - pq_bytes;  // 1024: alignment slack
     // an even number of stages: a tile's second fill always lands in an odd
     // stage, whose reduction slot (stage / 2) it owns
     c.NST = std::min(kMaxStages, budget / (c.stage_bytes + red_stage / 2)) & ~1;
     if (c.NST < 4) return false;  // at least two 32-row tiles in flight
     c.red_off = c.stage_off + c.NST * c.stage_bytes;
-    c.smem = c.red_off + (c.NST / 2) * red_stage + 1024;
+    c.pq_off = c.red_off + (c.NST / 2) * red_stage;
+    c.smem = c.pq_off + pq_bytes + 1024;
     c.ntiles = (N + 16 * c.TR - 1) / (16 * c.TR);
     c.grid = std::min(c.ntiles, di.sm_count);
     return true;
@@ -639,7 +688,12 @@ bool mma_gemv_eligible(const GemmProblem &p) {
     if (p.kind != WK_NBITS || p.bits != 2 || p.bs != 64 || p.K % kSpanCodes != 0) return false;
     if (p.M < 1 || p.M > (p.a_dtype == 0 ? 4 : 8)) return false;
     MgCfg c;
-    return choose_mg(p.M, p.N, p.K, p.a_dtype, p.zp_mode == ZP_TENSOR, c);
+    const bool zpt = p.zp_mode == ZP_TENSOR;
+    if (!choose_mg(p.M, p.N, p.K, p.a_dtype, zpt, c)) return false;
+    // 16-row tiles copy each row's eight block parameters of a span as one
+    // 16-byte run: the parameter tensors must start on a 16-byte boundary
+    const auto a16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    return c.TR == 2 || (a16(p.scales) && (!zpt || a16(p.zp)));
 }
 
 cudaError_t mma_gemv(const GemmProblem &p, cudaStream_t s) {
@@ -674,6 +728,7 @@ cudaError_t mma_gemv(const GemmProblem &p, cudaStream_t s) {
     a.par_off = c.par_off;
     a.zp_off = c.zp_off;
     a.red_off = c.red_off;
+    a.pq_off = c.pq_off;
     a.fault = fault_word();
 #define QG_MG(MP_, NT_)                                                                             \
     if (c.MP == MP_ && c.NT == NT_ && c.TR == 2)                                                    \
