@@ -197,37 +197,28 @@ __device__ __forceinline__ void build_span_row(int sp, int m, int lane, float (&
     bs += __shfl_xor_sync(0xffffffffu, bs, 2);
     if (wd == 0) spart[(sp * 8 + blk) * MP + m] = bs * 5.9604644775390625e-08f;  // 2^-24
     if (lane == 0) somul[sp * MP + m] = exp2i(10 + e);
+    // (codes i, i + 8) pairs: hi = fp16(x) rounded to nearest, lo = fp16(x - hi),
+    // two values per packed conversion
+    uint32_t hi[8], lo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float pinv = exp2i(-2 * (i & 3));  // 2^-p
+        const float x0 = a[i] * pinv, x1 = a[i + 8] * pinv;
+        const __half2 h = __floats2half2_rn(x0, x1);
+        hi[i] = *reinterpret_cast<const uint32_t *>(&h);
+        if (NT == 2) {
+            const __half2 l = __floats2half2_rn(x0 - __low2float(h), x1 - __high2float(h));
+            lo[i] = *reinterpret_cast<const uint32_t *>(&l);
+        }
+    }
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         const int slot = (m * NT + t) * 4 + c;
+        const uint32_t *v = t == 0 ? hi : lo;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t regs[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int i = 2 * (2 * h + (q >> 1)) + (q & 1);  // codes i and i + 8 of the word
-                const float pinv = exp2i(-2 * (i & 3));           // 2^-p
-                const float x0 = a[i] * pinv, x1 = a[i + 8] * pinv;
-                const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-                const uint16_t v0 = t == 0 ? __half_as_ushort(h0) : __half_as_ushort(__float2half_rn(x0 - __half2float(h0)));
-                const uint16_t v1 = t == 0 ? __half_as_ushort(h1) : __half_as_ushort(__float2half_rn(x1 - __half2float(h1)));
-                regs[q] = static_cast<uint32_t>(v0) | (static_cast<uint32_t>(v1) << 16);
-            }
+        for (int h = 0; h < 2; ++h)  // entry h: codes (4h, 4h+8), (4h+1, 4h+9), (4h+2, ..), (4h+3, ..)
             *reinterpret_cast<uint4 *>(bfrag + static_cast<size_t>(b_entry<MNT>(sp, j, w, h, slot)) * 16) =
-                make_uint4(regs[0], regs[1], regs[2], regs[3]);
-        }
-    }
-}
-
-// The B fragments, block sums and output multipliers of span sp.
-template <int MP, int NT>
-__device__ __forceinline__ void build_span(const MgArgs &p, int sp, int lane, unsigned char *bfrag, float *spart,
-                                           float *somul) {
-#pragma unroll 1
-    for (int m = 0; m < MP; ++m) {
-        float a[16];
-        load_span_act(p, sp, m, lane, a);
-        build_span_row<MP, NT>(sp, m, lane, a, bfrag, spart, somul);
+                make_uint4(v[4 * h], v[4 * h + 1], v[4 * h + 2], v[4 * h + 3]);
     }
 }
 
@@ -240,7 +231,7 @@ static_assert((kMaxWarps + 1 + 3) / 4 * 32 * kMaxRegs <= 16384, "registers of on
 // TR: MMA row tiles per tile.  TR = 2: 32-row tiles of two 16-row fills, the
 // block parameters copied into the stage with the codes.  TR = 1 (long K,
 // where the B fragments leave room for 8-row stages only): 16-row tiles of two
-// 8-row fills, the block parameters read from global memory.
+// 8-row fills, the block parameters copied by each warp (cp.async).
 template <int MP, int NT, bool ZPT, int TR>
 __global__ void __maxnreg__(kMaxRegs)
     mma_gemv_kernel(const MgArgs p) {
@@ -366,18 +357,22 @@ __global__ void __maxnreg__(kMaxRegs)
     // lanes of a block add its activation sum in a fixed order.
     const int g = lane >> 2, c = lane & 3;
     const int sl = warp;
-    if constexpr (MP == 1) {  // the next span's activations load while this one is built
-        float a[16], an[16];
-        if (sl < p.spans) load_span_act(p, sl, 0, lane, a);
+    // The warp's (span, activation row) items in batches of four: the loads of
+    // a batch are all in flight together (one memory latency per batch, which
+    // the weight stream started by the producer makes long).
+    {
+        const int items = (p.spans - sl + W - 1) / W * MP;
 #pragma unroll 1
-        for (int sp = sl; sp < p.spans; sp += W) {
-            if (sp + W < p.spans) load_span_act(p, sp + W, 0, lane, an);
-            build_span_row<MP, NT>(sp, 0, lane, a, bfrag_w, spart, somul);
+        for (int b = 0; b < items; b += 4) {
+            float a[4][16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) a[i] = an[i];
+            for (int q = 0; q < 4; ++q)
+                if (b + q < items) load_span_act(p, sl + (b + q) / MP * W, (b + q) % MP, lane, a[q]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (b + q < items)
+                    build_span_row<MP, NT>(sl + (b + q) / MP * W, (b + q) % MP, lane, a[q], bfrag_w, spart, somul);
         }
-    } else {
-        for (int sp = sl; sp < p.spans; sp += W) build_span<MP, NT>(p, sp, lane, bfrag_w, spart, somul);
     }
     __syncwarp();
 
