@@ -26,6 +26,7 @@ __all__ = [
     "qgemm_codebook4_nested", "qgemm_codebook4_nested_workspace_bytes", "qmoe_ragged_mm",
     "qmoe_ragged_mm_workspace_bytes", "qg_gather_block_quantized", "QG_WF_U2", "QG_WF_U4", "QG_WF_U8", "QG_WF_E4M3",
     "qgemm_nbits_packed_zp", "qgemm_nbits_packed_zp_workspace_bytes", "qg_test_bounded_wait",
+    "qg_test_gemv_plan",
 ]
 
 QG_OK, QG_ERR_INVALID_ARG, QG_ERR_UNSUPPORTED, QG_ERR_CUDA, QG_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3, 4
@@ -80,6 +81,7 @@ _SIGS = {
     "qmoe_ragged_mm_workspace_bytes": ([_I, _P, _I, _I, _I, _I, _I], _SZ),
     "qg_read_device_fault": ([_P], _I),
     "qg_test_bounded_wait": ([_I, ctypes.c_uint, _P, _P], _I),
+    "qg_test_gemv_plan": ([_I, _I, _I, _I, _I, _P], _I),
     "qg_status_string": ([_I], ctypes.c_char_p),
 }
 
@@ -363,6 +365,18 @@ def qg_test_bounded_wait(fill: bool, limit_us: int, out, stream=None, raw=False)
     gave up)."""
     s = lib().qg_test_bounded_wait(1 if fill else 0, int(limit_us), _ptr(out), _stream(stream))
     return s if raw else _check(s, "qg_test_bounded_wait")
+
+
+def qg_test_gemv_plan(M: int, N: int, K: int, a_dtype: int = QG_F32, zp_mode: int = 2):
+    """Test hook (include/qgemm_testing.h): the launch plan of the 2-bit
+    tensor-core GEMV for this shape -- a dict of rows_per_tile, warps (consumer
+    warps), ctas, stages -- or None when the shape takes another path."""
+    out = (ctypes.c_int * 4)()
+    s = lib().qg_test_gemv_plan(int(M), int(N), int(K), int(a_dtype), int(zp_mode), ctypes.cast(out, ctypes.c_void_p))
+    if s == QG_ERR_UNSUPPORTED:
+        return None
+    _check(s, "qg_test_gemv_plan")
+    return dict(zip(("rows_per_tile", "warps", "ctas", "stages"), list(out)))
 
 
 def qg_status_string(status: int) -> str:

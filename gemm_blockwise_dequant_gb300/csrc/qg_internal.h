@@ -76,6 +76,10 @@ cudaError_t simt_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStrea
 // fp32 activations, M <= 8 with 16-bit ones; block 64, K a multiple of 512).
 bool mma_gemv_eligible(const GemmProblem &p);
 cudaError_t mma_gemv(const GemmProblem &p, cudaStream_t s);
+// The plan mma_gemv takes for a 2-bit block-64 request of this shape: rows per
+// tile, consumer warps, CTAs, ring stages; false when the request does not
+// take it.
+bool mma_gemv_plan(int M, int N, int K, int a_dtype, int zp_mode, int out[4]);
 
 // Tensor-core path (M >= 9 with 16-bit activations).
 bool tc_eligible(int M, int K, int bits, int a_dtype, int bs, int kind);

@@ -691,6 +691,17 @@ bool mma_gemv_eligible(const GemmProblem &p) {
     return c.TR == 2 || (a16(p.scales) && (!zpt || a16(p.zp)));
 }
 
+bool mma_gemv_plan(int M, int N, int K, int a_dtype, int zp_mode, int out[4]) {
+    if (K % kSpanCodes != 0 || M < 1 || M > (a_dtype == 0 ? 4 : 8)) return false;
+    MgCfg c;
+    if (!choose_mg(M, N, K, a_dtype, zp_mode == ZP_TENSOR, c)) return false;
+    out[0] = 16 * c.TR;
+    out[1] = c.W;
+    out[2] = c.grid;
+    out[3] = c.NST;
+    return true;
+}
+
 cudaError_t mma_gemv(const GemmProblem &p, cudaStream_t s) {
     MgCfg c;
     const bool zpt = p.zp_mode == ZP_TENSOR;

@@ -45,3 +45,8 @@ extern "C" int qg_test_bounded_wait(int fill, unsigned int limit_us, int *out_de
         fill ? 1 : 0, 1000ull * limit_us, fault, out_dev);
     return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
+
+extern "C" int qg_test_gemv_plan(int M, int N, int K, int a_dtype, int zp_mode, int *out) {
+    if (!out || M < 1 || N < 1 || K < 1) return QG_ERR_INVALID_ARG;
+    return qg::mma_gemv_plan(M, N, K, a_dtype, zp_mode, out) ? QG_OK : QG_ERR_UNSUPPORTED;
+}

@@ -1,5 +1,5 @@
 /*
- * qgemm_testing.h -- a test hook of libqgemm.so, not part of the compute API.
+ * qgemm_testing.h -- test hooks of libqgemm.so, not part of the compute API.
  *
  * qg_test_bounded_wait -- runs the library's bounded pipeline wait on the GPU
  * in a kernel shaped like its pipelines (a producer warp and three consumer
@@ -21,6 +21,20 @@
  * QG_ERR_CUDA (launch error).  Enqueued on `stream` of the current device;
  * nothing is synchronised.
  */
+/*
+ * qg_test_gemv_plan -- the launch plan the 2-bit tensor-core GEMV takes on
+ * the current device for a 2-bit, block-64 request of this shape, so that
+ * tests can check that their shapes reach each variant.  Nothing is launched.
+ *
+ *   a_dtype, zp_mode  as in qgemm_nbits (0 fp32, 1 fp16, 2 bf16; 0 none,
+ *                     1 tensor, 2 uniform)
+ *   out               host int[4]: weight rows per tile (32: block parameters
+ *                     staged with the codes; 16: long K, block parameters
+ *                     copied per span by the consumer warps), consumer warps,
+ *                     CTAs launched, shared-memory ring stages.
+ * Returns QG_OK, QG_ERR_INVALID_ARG (null out, M, N or K not positive) or
+ * QG_ERR_UNSUPPORTED (the request does not take this GEMV: other paths serve it).
+ */
 #ifndef QGEMM_TESTING_H
 #define QGEMM_TESTING_H
 
@@ -31,6 +45,7 @@ extern "C" {
 #endif
 
 int qg_test_bounded_wait(int fill, unsigned int limit_us, int *out_dev, qg_stream_t stream);
+int qg_test_gemv_plan(int M, int N, int K, int a_dtype, int zp_mode, int *out);
 
 #ifdef __cplusplus
 }
