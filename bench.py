@@ -865,6 +865,9 @@ def run_probe(name):
     gemv_down    4 calls of the down shape (5120 x 17920, u2, M=1)
     tc_prefill   4 calls of a prefill-sized u2 GEMM on the tensor cores
                  (M=2048, N=K=5120, fp16 activations, fp32 out)
+    tc_prefill_gate_up, tc_prefill_down
+                 3 calls of the phi4-14B prefill GEMMs (M=2048; 35840 x 5120,
+                 5120 x 17920)
     tc_nf4_m64   4 calls of the NF4 codebook GEMM 14336 x 4096 at M=64 (bf16, tensor cores)
     qmoe         4 calls of the 128-expert top-8 2880/2880 block-32 QMoE decode
     qmoe_dp4a    the same with int8 activations
@@ -903,6 +906,10 @@ def run_probe(name):
     elif name == "tc_prefill":
         c = nbits(WL.prefill_u2((5120, 5120), M=2048))
         for _ in range(4):
+            c()
+    elif name in ("tc_prefill_gate_up", "tc_prefill_down"):
+        c = nbits(WL.prefill_u2(name[len("tc_prefill_"):], M=2048))
+        for _ in range(3):
             c()
     elif name in ("qmoe", "qmoe_dp4a"):
         d = WL.qmoe()
@@ -962,7 +969,8 @@ def main():
                     help="steps per CUDA graph in the timed region (each step is 5 GEMV launches)")
     ap.add_argument("--clocks-log", default=None,
                     help="file for the raw nvidia-smi samples of the timed region (%%d: GPU index); default a temp file")
-    ap.add_argument("--probe", choices=["gemv_k5120", "gemv_lm_head", "gemv_down", "tc_prefill", "tc_nf4_m64", "qmoe",
+    ap.add_argument("--probe", choices=["gemv_k5120", "gemv_lm_head", "gemv_down", "tc_prefill", "tc_prefill_gate_up",
+                                        "tc_prefill_down", "tc_nf4_m64", "qmoe",
                                         "qmoe_dp4a", "ragged", "gather"],
                     help="run a small fixed workload for a profiler capture instead of the benchmark")
     ap.add_argument("--suite", action="store_true",
