@@ -29,13 +29,12 @@
 //    accumulator back after every block, the B columns are block-diagonal:
 //    column (block, row m, term) holds the activations of that block only, so
 //    one accumulator fragment carries up to eight blocks' sums side by side.
-//  * Weights stream through an mbarrier ring of shared-memory stages filled by
-//    TMA 2-D copies (one producer warp; 128-byte swizzled boxes of 16 rows x
-//    128 bytes, which makes the consumers' code loads bank-conflict free and
-//    zero-fills rows past N).  Each consumer warp owns one 512-code span of
-//    each K chunk; the producer adds the warps' span sums of a tile in span
-//    order and writes Y.  Fixed order everywhere: repeated calls are
-//    bit-identical (hip-ep #1328, "Why").
+//  * Weights stream through an mbarrier ring of shared-memory stages, each
+//    filled by one producer warp with one 1-D bulk copy of whole weight rows
+//    (one contiguous run of HBM) and one of their block parameters.  Consumer
+//    warp w owns the 512-code spans w, w + W, ... of every row; the producer
+//    adds the warps' span sums of a tile in span order and writes Y.  Fixed
+//    order everywhere: repeated calls are bit-identical (hip-ep #1328, "Why").
 //  * Every wait is bounded (qg_device.cuh).
 #include <algorithm>
 #include <atomic>
