@@ -66,6 +66,7 @@ struct MgArgs {
     int W_;           // consumer warps: warp w owns spans w, w + W_, ...
     int NST, ntiles;  // ring stages (16-row fills), 32-row tiles
     int b_off, sp_off, om_off, zero_off, stage_off, stage_bytes, par_off, zp_off, red_off, pq_off;
+    int bov;          // first ring stage that holds the B fragments until every warp has them in registers (NST: none)
     unsigned *fault;
 };
 
@@ -245,6 +246,7 @@ __global__ void __maxnreg__(kMaxRegs)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + kMaxStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 2 * kMaxStages * 8);
+    uint64_t *bfree = reinterpret_cast<uint64_t *>(smem + 2 * kMaxStages * 8 + 8);  // every consumer holds its B
     unsigned char *bfrag_w = smem + p.b_off;                    // B-fragment entries of every span
     float *spart = reinterpret_cast<float *>(smem + p.sp_off);  // [blocks][MP]: 2^-24 sum of a' per block
     float *somul = reinterpret_cast<float *>(smem + p.om_off);  // [spans][MP]: each span's output multiplier
@@ -258,6 +260,7 @@ __global__ void __maxnreg__(kMaxRegs)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], W);
         }
+        mbar_init(bfree, W * 32);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -307,6 +310,13 @@ __global__ void __maxnreg__(kMaxRegs)
         int slot = 0;
         uint32_t par = 1;  // parity of the empty phase to wait for before refilling `slot`
         for (int f = 0; f < total; ++f) {
+            // the first fill into the stages that held the B fragments waits
+            // until every consumer thread has its fragments in registers
+            if (f == p.bov && p.bov < p.NST &&
+                !__all_sync(0xffffffffu, mbar_wait(bfree, 0, abort_flag, p.fault, FAULT_WAIT_EMPTY))) {
+                alive = false;
+                break;
+            }
             if (f >= p.NST) {
                 if (!mbar_wait(&empty[slot], par, abort_flag, p.fault, FAULT_WAIT_EMPTY)) {
                     alive = false;
@@ -393,10 +403,11 @@ __global__ void __maxnreg__(kMaxRegs)
     const int m0 = NT == 2 ? c % MP : (2 * c) % MP;
     const int m1 = NT == 2 ? m0 : (2 * c + 1) % MP;
     const int pw = p.nb;  // parameters per row in a stage
-    // With one or two fp16 columns per block a warp's B fragments for one span
-    // fit in 64 registers: a warp that owns a single span loads them once, here,
-    // instead of from shared memory for every tile.
-    constexpr bool BREG = MNT <= 2;
+    // A warp's B fragments for one span fit in 64 registers (eight 16-byte
+    // entries per lane whatever the column layout): a warp that owns a single
+    // span loads them once, here, instead of from shared memory for every tile,
+    // and the shared memory that held them becomes ring stages.
+    constexpr bool BREG = true;
     const bool one_span = p.spans <= W;
     uint4 breg[BREG ? 8 : 1][2];  // [j * BPG + w][h]
     auto load_breg = [&](int sp) {
@@ -413,6 +424,10 @@ __global__ void __maxnreg__(kMaxRegs)
         }
     };
     if (BREG && one_span) load_breg(sl);
+    if (p.bov < p.NST) {  // the B fragments' stages go back to the ring
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // this thread's B stores before the copies
+        mbar_arrive(bfree);
+    }
     // TR = 1: the block parameters stay in global memory; the warp copies the
     // ones of its next (tile, span) item -- 16 rows x the span's 8 blocks, a
     // 16-byte run per row -- into one of its two buffers while it works on the
@@ -609,11 +624,15 @@ __global__ void __maxnreg__(kMaxRegs)
 struct MgCfg {
     int MP, NT, TR, spans, W, NST, ntiles, grid;
     int b_off, sp_off, om_off, zero_off, stage_off, stage_bytes, par_off, zp_off, red_off, pq_off, smem;
+    int bov;
 };
 
 inline int rup(int x, int a) { return (x + a - 1) / a * a; }
 
-bool choose_mg1(int M, int N, int K, int a_dtype, bool zpt, int tr, MgCfg &c) {
+// Shared-memory layout and ring depth for tiles of 16 TR rows.  ov: the B
+// fragments live in the ring's last stages, which the producer fills only
+// once every consumer warp holds its (single) span's fragments in registers.
+bool layout_mg(int M, int N, int K, int a_dtype, bool zpt, int tr, bool ov, MgCfg &c) {
     c.TR = tr;
     const DeviceInfo &di = device_info();
     c.NT = a_dtype == 0 ? 2 : 1;
@@ -625,8 +644,9 @@ bool choose_mg1(int M, int N, int K, int a_dtype, bool zpt, int tr, MgCfg &c) {
     c.W = (c.spans + per - 1) / per;
     const int mnt = c.MP * c.NT;
     const int nblk = c.spans * 8, nb = K / 64, row_bytes = K / 4;
-    c.b_off = kHeader;
-    c.sp_off = c.b_off + c.spans * 1024 * mnt;
+    const int b_bytes = c.spans * 1024 * mnt;
+    if (ov && c.spans > c.W) return false;  // only single-span warps keep B in registers
+    c.sp_off = kHeader + (ov ? 0 : b_bytes);
     c.om_off = c.sp_off + nblk * c.MP * 4;
     c.zero_off = rup(c.om_off + c.spans * c.MP * 4, 16);
     c.stage_off = rup(c.zero_off + 1024 * mnt, 1024);
@@ -643,6 +663,15 @@ bool choose_mg1(int M, int N, int K, int a_dtype, bool zpt, int tr, MgCfg &c) {
     // stage, whose reduction slot (stage / 2) it owns
     c.NST = std::min(kMaxStages, budget / (c.stage_bytes + red_stage / 2)) & ~1;
     if (c.NST < 4) return false;  // at least two 32-row tiles in flight
+    if (ov) {
+        const int kb = (b_bytes + c.stage_bytes - 1) / c.stage_bytes;
+        if (kb > c.NST) return false;
+        c.bov = c.NST - kb;
+        c.b_off = c.stage_off + c.bov * c.stage_bytes;
+    } else {
+        c.bov = c.NST;
+        c.b_off = kHeader;
+    }
     c.red_off = c.stage_off + c.NST * c.stage_bytes;
     c.pq_off = c.red_off + (c.NST / 2) * red_stage;
     c.smem = c.pq_off + pq_bytes + 1024;
@@ -651,12 +680,16 @@ bool choose_mg1(int M, int N, int K, int a_dtype, bool zpt, int tr, MgCfg &c) {
     return true;
 }
 
+bool choose_mg1(int M, int N, int K, int a_dtype, bool zpt, int tr, MgCfg &c) {
+    return layout_mg(M, N, K, a_dtype, zpt, tr, true, c) || layout_mg(M, N, K, a_dtype, zpt, tr, false, c);
+}
+
 // 32-row tiles with the block parameters in the stage, or, when those stages
-// do not fit beside the B fragments (long K), 16-row tiles of 8-row fills
-// (the one-row-quad activation layouts only).
+// do not fit beside the B fragments (long K, or eight B columns per block),
+// 16-row tiles of 8-row fills.
 bool choose_mg(int M, int N, int K, int a_dtype, bool zpt, MgCfg &c) {
     if (choose_mg1(M, N, K, a_dtype, zpt, 2, c)) return true;
-    return (M <= 1) && choose_mg1(M, N, K, a_dtype, zpt, 1, c);
+    return choose_mg1(M, N, K, a_dtype, zpt, 1, c);
 }
 
 template <int MP, int NT, bool ZPT, int TR>
@@ -734,21 +767,25 @@ cudaError_t mma_gemv(const GemmProblem &p, cudaStream_t s) {
     a.zp_off = c.zp_off;
     a.red_off = c.red_off;
     a.pq_off = c.pq_off;
+    a.bov = c.bov;
     a.fault = fault_word();
-#define QG_MG(MP_, NT_)                                                                             \
-    if (c.MP == MP_ && c.NT == NT_ && c.TR == 2)                                                    \
-        return zpt ? launch_mg<MP_, NT_, true, 2>(a, c, s) : launch_mg<MP_, NT_, false, 2>(a, c, s);
-    if (c.TR == 1 && c.MP == 1) {
-        if (c.NT == 2) return zpt ? launch_mg<1, 2, true, 1>(a, c, s) : launch_mg<1, 2, false, 1>(a, c, s);
-        return zpt ? launch_mg<1, 1, true, 1>(a, c, s) : launch_mg<1, 1, false, 1>(a, c, s);
-    }
-    QG_MG(1, 2)
-    QG_MG(2, 2)
-    QG_MG(4, 2)
-    QG_MG(1, 1)
-    QG_MG(2, 1)
-    QG_MG(4, 1)
-    QG_MG(8, 1)
+#define QG_MG(MP_, NT_, TR_)                                                                        \
+    if (c.MP == MP_ && c.NT == NT_ && c.TR == TR_)                                                  \
+        return zpt ? launch_mg<MP_, NT_, true, TR_>(a, c, s) : launch_mg<MP_, NT_, false, TR_>(a, c, s);
+    QG_MG(1, 2, 2)
+    QG_MG(2, 2, 2)
+    QG_MG(4, 2, 2)
+    QG_MG(1, 1, 2)
+    QG_MG(2, 1, 2)
+    QG_MG(4, 1, 2)
+    QG_MG(8, 1, 2)
+    QG_MG(1, 2, 1)
+    QG_MG(2, 2, 1)
+    QG_MG(4, 2, 1)
+    QG_MG(1, 1, 1)
+    QG_MG(2, 1, 1)
+    QG_MG(4, 1, 1)
+    QG_MG(8, 1, 1)
 #undef QG_MG
     return cudaErrorNotSupported;
 }

@@ -73,6 +73,9 @@ CASES = [
     (5, 97, 1536, BF16, "uniform", F32),    # 5 rows in the 8-row layout
     (8, 97, 5120, F16, "uniform", F32),
     (8, 40, 17920, BF16, "tensor", BF16),
+    (2, 150, 8704, F32, "tensor", F32),     # 16-row tiles with two activation rows
+    (4, 70, 8704, F16, "uniform", F32),
+    (8, 200, 5120, BF16, "none", F32),      # eight B columns per block: B fragments in the ring's stages
 ]
 
 
@@ -133,7 +136,9 @@ def test_mma_gemv_plans_reach_both_tile_shapes(qg):
         assert 1 <= plan["ctas"] <= N and plan["stages"] >= 4, (s, plan)
     plans = [qg.qg_test_gemv_plan(c[0], c[1], c[2], c[3], zp[c[4]]) for c in CASES]
     assert {p["rows_per_tile"] for p in plans if p is not None} == {16, 32}
-    # B fragments of 35 spans x 4 or 8 columns leave no room for the ring: M > 1
-    # with K = 17920 is served by the SIMT GEMV
+    # M = 2 with fp32 activations: at K = 8704 (17 spans x 4 B columns, two spans
+    # for some warps) only 16-row tiles fit beside the B fragments; at K = 17920
+    # nothing does, and the SIMT GEMV serves it
+    assert qg.qg_test_gemv_plan(2, 150, 8704, F32, 1)["rows_per_tile"] == 16
     assert qg.qg_test_gemv_plan(2, 96, 17920, F32, 2) is None
     assert qg.qg_test_gemv_plan(1, 100, 1536 + 64, F32, 2) is None
