@@ -222,6 +222,16 @@ __device__ __forceinline__ void build_span_row(int sp, int m, int lane, float (&
     }
 }
 
+// Lanes of a row quad that leave a partial sum of the same (weight row,
+// activation row): four for one activation row (both fp16 columns of a lane
+// are that row), else the lanes c whose columns hold row m -- c % MP == m for
+// fp32 activations (one row per lane), the pairs (2c, 2c + 1) % MP for 16-bit
+// ones.  Lane c's partial goes to slot c * SL / 4 of [row][m][SL].
+template <int MP, int NT>
+__host__ __device__ constexpr int red_slots() {
+    return NT == 2 ? 4 / MP : (MP <= 2 ? 4 : 8 / MP);
+}
+
 // At most kMaxWarps + 1 = 12 warps: three per SM sub-partition, whose 16 K
 // registers hold three warps of 152 registers (the B fragments a warp may keep
 // take 64 of them).
@@ -240,6 +250,7 @@ __global__ void __maxnreg__(kMaxRegs)
     constexpr int FR = 8 * TR;       // weight rows per fill
     constexpr int TROWS = 16 * TR;   // weight rows per tile
     constexpr bool PSMEM = TR == 2;  // block parameters in the stage
+    constexpr int SL = red_slots<MP, NT>();
     static_assert(MNT >= 1 && MNT <= 8 && (8 % MNT) == 0, "columns per block");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -251,7 +262,7 @@ __global__ void __maxnreg__(kMaxRegs)
     float *spart = reinterpret_cast<float *>(smem + p.sp_off);  // [blocks][MP]: 2^-24 sum of a' per block
     float *somul = reinterpret_cast<float *>(smem + p.om_off);  // [spans][MP]: each span's output multiplier
     unsigned char *stages = smem + p.stage_off;
-    float *red = reinterpret_cast<float *>(smem + p.red_off);   // [stage / 2][warp][32 rows][MP][4 lanes]
+    float *red = reinterpret_cast<float *>(smem + p.red_off);   // [stage / 2][warp][rows][MP][SL]
 
     const int W = p.W_;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -283,25 +294,18 @@ __global__ void __maxnreg__(kMaxRegs)
     const int total = 2 * ntl;                    // fills of this CTA
     if (warp == W) {
         // ------------------------------------------------------------ producer
-        // Lanes of a row quad that hold the same activation row m (slots c of
-        // [row][m][4] they write): all four for one activation row per quad
-        // (M = 1), else c with c % MP == m (fp32, one row per lane) or the pairs
-        // of (2c) % MP (16-bit activations).
         auto finish = [&](int tl, int rslot) {  // add the warps' sums of tile tl of this CTA, write Y
             const int tile = blockIdx.x + tl * gridDim.x;
-            const float *r = red + (rslot >> 1) * (W * TROWS * MP * 4);
+            const float *r = red + (rslot >> 1) * (W * TROWS * MP * SL);
             for (int v = lane; v < TROWS * MP; v += 32) {
                 const int row = v / MP, m = v - row * MP;
                 const int n = tile * TROWS + row;
                 if (m >= p.M || n >= p.N) continue;
                 float s = 0.f;
-                for (int w = 0; w < W; ++w) {
-                    const float *q = r + (w * TROWS * MP + v) * 4;
+                for (int w = 0; w < W; ++w) {  // warp (span) order, then lane order
+                    const float *q = r + (w * TROWS * MP + v) * SL;
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const bool mine = MP == 1 || (NT == 2 ? (cc % MP) == m : ((2 * cc) % MP == m || (2 * cc + 1) % MP == m));
-                        if (mine) s += q[cc];
-                    }
+                    for (int k = 0; k < SL; ++k) s += q[k];
                 }
                 store_y_elem(p.Y, p.y_dtype, static_cast<size_t>(m) * p.N + n, s);
             }
@@ -591,19 +595,20 @@ __global__ void __maxnreg__(kMaxRegs)
         }
         // this warp's span sums of the tile's rows, for the producer (in the
         // reduction slot of the tile's second fill): every lane of a row quad
-        // leaves its own partial of each (row, activation row) it holds, in slot c
-        // of [row][m][4], and the producer adds them (fixed order, no shuffles)
-        float *rw = red + (sb_ >> 1) * (W * TROWS * MP * 4) + sl * TROWS * MP * 4;
+        // leaves its own partial of each (row, activation row) it holds, in its
+        // slot of [row][m][SL], and the producer adds them (fixed order, no shuffles)
+        float *rw = red + (sb_ >> 1) * (W * TROWS * MP * SL) + sl * TROWS * MP * SL;
+        const int ks = c * SL / 4;
 #pragma unroll
         for (int r = 0; r < 2 * TR; ++r) {
             const int row = (r / TR) * FR + g + 8 * (r % TR);  // tile row of the thread's row r
             if (NT == 1 && MP == 1) {   // both columns are row 0: lane c's slot holds their sum
-                rw[row * 4 + c] = acc[r][0] + acc[r][1];
-            } else if (NT == 2) {       // one activation row per lane; MP x 4 slots, lanes of the same m add up
-                rw[(row * MP + m0) * 4 + c] = acc[r][0];
+                rw[row * SL + ks] = acc[r][0] + acc[r][1];
+            } else if (NT == 2) {       // one activation row per lane
+                rw[(row * MP + m0) * SL + ks] = acc[r][0];
             } else {                    // two activation rows per lane
-                rw[(row * MP + m0) * 4 + c] = acc[r][0];
-                rw[(row * MP + m1) * 4 + c] = acc[r][1];
+                rw[(row * MP + m0) * SL + ks] = acc[r][0];
+                rw[(row * MP + m1) * SL + ks] = acc[r][1];
             }
         }
         __syncwarp();
@@ -655,7 +660,8 @@ bool layout_mg(int M, int N, int K, int a_dtype, bool zpt, int tr, bool ov, MgCf
     c.par_off = rup(fr * row_bytes, 128);
     c.zp_off = rup(c.par_off + (c.TR == 2 ? fr * nb * 2 : 0), 128);
     c.stage_bytes = rup(c.zp_off + (zpt && c.TR == 2 ? fr * nb * 2 : 0), 128);
-    const int red_stage = c.W * 16 * c.TR * c.MP * 4 * 4;
+    const int sl = c.NT == 2 ? 4 / c.MP : (c.MP <= 2 ? 4 : 8 / c.MP);  // red_slots<MP, NT>()
+    const int red_stage = c.W * 16 * c.TR * c.MP * sl * 4;
     // TR = 1: each consumer warp's two buffers of one span's block parameters of a tile
     const int pq_bytes = c.TR == 1 ? c.W * kPqBytes * (zpt ? 2 : 1) : 0;
     const int budget = di.max_smem_optin - 1024 - c.stage_off - pq_bytes;  // 1024: alignment slack
