@@ -554,7 +554,8 @@ def run_ours(args, world, rank, local):
 
 # ------------------------------------------------------------- config suite
 # the groups the benchmark line carries (the N sweep only runs under --suite)
-CONFIG_GROUPS = ("tiny_u4", "phi4_u2", "nf4", "qmoe", "prefill", "phi4_u8", "packed_zp", "ragged", "gather")
+CONFIG_GROUPS = ("tiny_u4", "phi4_u2", "nf4", "qmoe", "prefill", "f32_large_m", "phi4_u8", "packed_zp", "ragged",
+                 "gather")
 
 
 def run_suite(only=None, groups=None, echo=True):
@@ -564,6 +565,7 @@ def run_suite(only=None, groups=None, echo=True):
     the NF4 codebook shapes at M=1, 4, 16, 64 (bf16 activations); the QMoE
     decode (128 experts, top-8, 2880/2880, u4 block 32) with and without zero
     points, with fp16 and with int8 activations; the two M=2048 prefill GEMMs; the
+    phi4 gate_up projection with fp32 activations at M=64 and M=2048; the
     ragged expert GEMM of a 128-expert top-8 2048/768 layer over a 2048-token prompt; an N sweep
     around two decode shapes (partition-camping outliers);
     the block-quantized embedding gather
@@ -709,6 +711,20 @@ def run_suite(only=None, groups=None, echo=True):
                                                     workspace=ws, stream=st)
                 emit("u4_bs32_%s_zp_%s_m1" % ("packed" if packed else "fp16", shape), timed(call, 2 * r), nbytes=wb)
                 del Ws, Ss, Zs
+
+    # fp32 activations at prefill sizes: the phi4 gate_up projection, M = 64 and 2048
+    if want("f32_large_m"):
+        d = WL.phi4_u2("gate_up", M=2048)
+        W, S = torch.from_numpy(d["W"]).to(dev), t16(d["scales"], torch.float16)
+        for M in (64, 2048):
+            A = torch.from_numpy(np.ascontiguousarray(d["A"][:M])).to(dev)
+            Y = torch.empty(M, d["N"], device=dev)
+            ws = torch.empty(max(16, qg.qgemm_workspace_bytes(0, M, d["N"], d["K"], 2, 64)), dtype=torch.uint8,
+                             device=dev)
+            us = timed(lambda i: qg.qgemm_nbits_uniform_zp(A, W, S, ZP, Y, bits=2, block_size=64, workspace=ws,
+                                                           stream=st), 2)
+            emit("phi4_u2_gate_up_f32_m%d" % M, us, nbytes=d["W"].nbytes + d["scales"].nbytes,
+                 flops=2.0 * M * d["N"] * d["K"])
 
     # NF4 codebook, bf16 activations
     if want("nf4"):
@@ -975,8 +991,8 @@ def main():
                     help="run a small fixed workload for a profiler capture instead of the benchmark")
     ap.add_argument("--suite", action="store_true",
                     help="time every configuration (one JSON line each) instead of the benchmark")
-    ap.add_argument("--only", choices=["tiny_u4", "phi4_u2", "phi4_u8", "packed_zp", "nf4", "qmoe", "prefill", "ragged",
-                                       "gather", "nsweep"],
+    ap.add_argument("--only", choices=["tiny_u4", "phi4_u2", "phi4_u8", "packed_zp", "nf4", "qmoe", "prefill",
+                                       "f32_large_m", "ragged", "gather", "nsweep"],
                     help="with --suite: time one group of configurations only")
     args = ap.parse_args()
     if args.oracle_timing is not None:  # child of oracle_single_thread()

@@ -717,12 +717,20 @@ cudaError_t launch_mg(const MgArgs &a, const MgCfg &c, cudaStream_t s) {
 
 }  // namespace
 
+// Activation rows per launch: four with fp32 activations (hi / lo terms: eight
+// B columns per block), eight with 16-bit ones.  fp32 requests with more rows
+// run as one launch per group of four rows (each streams the weights once);
+// 16-bit requests with more rows belong to the tcgen05 path.
+int mma_rows(int a_dtype) { return a_dtype == 0 ? 4 : 8; }
+
 bool mma_gemv_eligible(const GemmProblem &p) {
     if (p.kind != WK_NBITS || p.bits != 2 || p.bs != 64 || p.K % kSpanCodes != 0) return false;
-    if (p.M < 1 || p.M > (p.a_dtype == 0 ? 4 : 8)) return false;
+    const int g = mma_rows(p.a_dtype);
+    if (p.M < 1 || (p.M > g && p.a_dtype != 0)) return false;
     MgCfg c;
     const bool zpt = p.zp_mode == ZP_TENSOR;
-    if (!choose_mg(p.M, p.N, p.K, p.a_dtype, zpt, c)) return false;
+    if (!choose_mg(std::min(p.M, g), p.N, p.K, p.a_dtype, zpt, c)) return false;
+    if (p.M > g && p.M % g != 0 && !choose_mg(p.M % g, p.N, p.K, p.a_dtype, zpt, c)) return false;
     // 16-row tiles copy each row's eight block parameters of a span as one
     // 16-byte run: the parameter tensors must start on a 16-byte boundary
     const auto a16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
@@ -730,9 +738,10 @@ bool mma_gemv_eligible(const GemmProblem &p) {
 }
 
 bool mma_gemv_plan(int M, int N, int K, int a_dtype, int zp_mode, int out[4]) {
-    if (K % kSpanCodes != 0 || M < 1 || M > (a_dtype == 0 ? 4 : 8)) return false;
+    const int g = mma_rows(a_dtype);
+    if (K % kSpanCodes != 0 || M < 1 || (M > g && a_dtype != 0)) return false;
     MgCfg c;
-    if (!choose_mg(M, N, K, a_dtype, zp_mode == ZP_TENSOR, c)) return false;
+    if (!choose_mg(std::min(M, g), N, K, a_dtype, zp_mode == ZP_TENSOR, c)) return false;
     out[0] = 16 * c.TR;
     out[1] = c.W;
     out[2] = c.grid;
@@ -740,7 +749,9 @@ bool mma_gemv_plan(int M, int N, int K, int a_dtype, int zp_mode, int out[4]) {
     return true;
 }
 
-cudaError_t mma_gemv(const GemmProblem &p, cudaStream_t s) {
+namespace {
+
+cudaError_t mma_gemv_rows(const GemmProblem &p, cudaStream_t s) {
     MgCfg c;
     const bool zpt = p.zp_mode == ZP_TENSOR;
     if (!choose_mg(p.M, p.N, p.K, p.a_dtype, zpt, c)) return cudaErrorNotSupported;
@@ -794,6 +805,23 @@ cudaError_t mma_gemv(const GemmProblem &p, cudaStream_t s) {
     QG_MG(8, 1, 1)
 #undef QG_MG
     return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+cudaError_t mma_gemv(const GemmProblem &p, cudaStream_t s) {
+    const int g = mma_rows(p.a_dtype);
+    if (p.M <= g) return mma_gemv_rows(p, s);
+    const size_t asz = p.a_dtype == 0 ? 4 : 2, ysz = p.y_dtype == 0 ? 4 : 2;
+    for (int m0 = 0; m0 < p.M; m0 += g) {
+        GemmProblem q = p;
+        q.A = static_cast<const char *>(p.A) + static_cast<size_t>(m0) * p.K * asz;
+        q.Y = static_cast<char *>(p.Y) + static_cast<size_t>(m0) * p.N * ysz;
+        q.M = std::min(g, p.M - m0);
+        const cudaError_t e = mma_gemv_rows(q, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace qg

@@ -14,7 +14,7 @@ import pytest
 
 import oracle as O
 import workloads as WL
-from gpu_util import BF16, F16, F32, nbits_case, oracle_nbits, to64, tol_for, torch, y_tensor
+from gpu_util import BF16, F16, F32, nbits_case, oracle_nbits, sample_rows, to64, tol_for, torch, y_tensor
 
 pytestmark = pytest.mark.gpu
 
@@ -142,3 +142,36 @@ def test_mma_gemv_plans_reach_both_tile_shapes(qg):
     assert qg.qg_test_gemv_plan(2, 150, 8704, F32, 1)["rows_per_tile"] == 16
     assert qg.qg_test_gemv_plan(2, 96, 17920, F32, 2) is None
     assert qg.qg_test_gemv_plan(1, 100, 1536 + 64, F32, 2) is None
+
+
+@pytest.mark.parametrize("case", [
+    (5, 130, 1536, "uniform", F32),    # one group of four rows and one of one
+    (9, 97, 5120, "tensor", F32),
+    (13, 200, 2048, "none", F16),      # a 16-bit output
+    (8, 70, 4608, "tensor", F32),      # two full groups
+])
+def test_mma_gemv_fp32_row_groups(qg, case):
+    """fp32 activations with more than four rows: one launch per group of four
+    rows, each against the oracle's fp64 result."""
+    M, N, K, zpm, yd = case
+    d = _case(23, M, N, K, F32, zpm)
+    plan = qg.qg_test_gemv_plan(M, N, K, F32, {"none": 0, "tensor": 1, "uniform": 2}[zpm])
+    assert plan is not None
+    Y = _run(qg, d, yd)
+    err = O.max_rel_l2(to64(Y), oracle_nbits(d))
+    assert err <= tol_for(F32, yd), err
+
+
+@pytest.mark.parametrize("M", [64, 2048])
+def test_mma_gemv_fp32_prefill_gate_up_sampled(qg, M):
+    """The phi4-14B gate_up projection (35840 x 5120, u2 block 64, zero point
+    1.5) with fp32 activations at M = 64 and M = 2048: every activation row,
+    on sampled weight rows (the first and last tiles included), at the fp32 bar;
+    a second call is bit-identical."""
+    d = WL.phi4_u2("gate_up", M=M)
+    Y = _run(qg, d, F32)
+    rows = np.unique(np.concatenate([sample_rows(d["N"], 40, seed=5), np.arange(d["N"] - 40, d["N"], 7)]))
+    got = to64(Y)[:, rows]
+    err = O.max_rel_l2(got, oracle_nbits(d, rows=rows))
+    assert err <= 1e-4, err
+    assert torch().equal(_run(qg, d, F32), Y)
