@@ -819,6 +819,14 @@ def run_suite(only=None, groups=None, echo=True):
                                                    stream=st), 4)
             emit("ragged_fc1_128x%dx%d_u4_bs32_tokens2048_top8" % NK, us, flops=2.0 * T * d["N"] * d["K"],
                  rows=T, experts_min_rows=int(np.diff(off).min()), experts_max_rows=int(np.diff(off).max()))
+            if NK == (1536, 2048):  # the same with the offsets in device memory (no host copy of them)
+                off_d = torch.from_numpy(np.asarray(off, np.int64)).to(dev)
+                wsd = torch.empty(qg.qmoe_ragged_mm_device_offsets_workspace_bytes(len(off) - 1), dtype=torch.uint8,
+                                  device=dev)
+                us = timed(lambda i: qg.qmoe_ragged_mm_device_offsets(X, off_d, W, S, None, Y, bits=4, block_size=32,
+                                                                      workspace=wsd, stream=st), 4)
+                emit("ragged_fc1_128x%dx%d_u4_bs32_tokens2048_top8_device_offsets" % NK, us,
+                     flops=2.0 * T * d["N"] * d["K"], rows=T)
             del X, W, S, Y
 
     # N sweep around the decode shapes (u2 M=1, K = 5120 around qkv's N and K = 17920 around down's N, steps

@@ -26,7 +26,7 @@ __all__ = [
     "qgemm_codebook4_nested", "qgemm_codebook4_nested_workspace_bytes", "qmoe_ragged_mm",
     "qmoe_ragged_mm_workspace_bytes", "qg_gather_block_quantized", "QG_WF_U2", "QG_WF_U4", "QG_WF_U8", "QG_WF_E4M3",
     "qgemm_nbits_packed_zp", "qgemm_nbits_packed_zp_workspace_bytes", "qg_test_bounded_wait",
-    "qg_test_gemv_plan",
+    "qg_test_gemv_plan", "qmoe_ragged_mm_device_offsets", "qmoe_ragged_mm_device_offsets_workspace_bytes",
 ]
 
 QG_OK, QG_ERR_INVALID_ARG, QG_ERR_UNSUPPORTED, QG_ERR_CUDA, QG_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3, 4
@@ -79,6 +79,8 @@ _SIGS = {
     "qgemm_nbits_packed_zp_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _SZ),
     "qmoe_ragged_mm": ([_P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P], _I),
     "qmoe_ragged_mm_workspace_bytes": ([_I, _P, _I, _I, _I, _I, _I], _SZ),
+    "qmoe_ragged_mm_device_offsets": ([_P, _I, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P, _P], _I),
+    "qmoe_ragged_mm_device_offsets_workspace_bytes": ([_I], _SZ),
     "qg_read_device_fault": ([_P], _I),
     "qg_test_bounded_wait": ([_I, ctypes.c_uint, _P, _P], _I),
     "qg_test_gemv_plan": ([_I, _I, _I, _I, _I, _P], _I),
@@ -335,6 +337,26 @@ def qmoe_ragged_mm(X, offsets, W, scales, zero_points, Y, *, bits, block_size, w
     s = lib().qmoe_ragged_mm(_ptr(X), _dtype_code(X), p, E, _ptr(W), _ptr(scales), _ptr(zero_points), _ptr(Y),
                              _dtype_code(Y), N, K, bits, block_size, _ptr(ws), wsb, _stream(stream))
     return s if raw else _check(s, "qmoe_ragged_mm")
+
+
+def qmoe_ragged_mm_device_offsets_workspace_bytes(num_experts: int) -> int:
+    return lib().qmoe_ragged_mm_device_offsets_workspace_bytes(int(num_experts))
+
+
+def qmoe_ragged_mm_device_offsets(X, offsets_dev, W, scales, zero_points, Y, *, bits, block_size, status=None,
+                                  workspace=None, stream=None, raw=False):
+    """qmoe_ragged_mm with the E+1 expert offsets in a device int64 tensor (no host copy).
+
+    X: [max_rows, K] float16/bfloat16 (max_rows >= offsets[E]); Y: [max_rows, N]; rows of Y at or
+    past offsets[E] are left untouched; status: a device int32 set to 1 for refused offsets, or None.
+    """
+    E, N = W.shape[0], W.shape[1]
+    max_rows, K = X.shape
+    ws, wsb = _workspace(lambda: lib().qmoe_ragged_mm_device_offsets_workspace_bytes(E), workspace, X.device)
+    s = lib().qmoe_ragged_mm_device_offsets(_ptr(X), _dtype_code(X), _ptr(offsets_dev), E, max_rows, _ptr(W),
+                                            _ptr(scales), _ptr(zero_points), _ptr(Y), _dtype_code(Y), N, K, bits,
+                                            block_size, _ptr(ws), wsb, _ptr(status), _stream(stream))
+    return s if raw else _check(s, "qmoe_ragged_mm_device_offsets")
 
 
 def qg_gather_block_quantized(indices, W, scales, zero_points, Y, *, w_format, block_size, status=None, stream=None,

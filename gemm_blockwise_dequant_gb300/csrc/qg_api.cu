@@ -665,6 +665,59 @@ int qmoe_ragged_mm(const void *X, int x_dtype, const int64_t *expert_offsets, in
     return QG_OK;
 }
 
+size_t qmoe_ragged_mm_device_offsets_workspace_bytes(int num_experts) {
+    if (num_experts < 1 || num_experts > 256) return 0;
+    return 2 * (256 + 1) * sizeof(int);
+}
+
+int qmoe_ragged_mm_device_offsets(const void *X, int x_dtype, const int64_t *expert_offsets_dev, int num_experts,
+                                  int max_rows, const uint8_t *W, const uint16_t *scales_f16,
+                                  const uint16_t *zero_points_f16, void *Y, int y_dtype, int N, int K, int bits,
+                                  int block_size, void *workspace, size_t workspace_bytes, int *status_dev,
+                                  qg_stream_t stream) {
+    (void)cudaGetLastError();
+    if (num_experts < 1 || max_rows < 0 || N < 0 || K < 0) return QG_ERR_INVALID_ARG;
+    if (!valid_dtype(x_dtype) || !valid_dtype(y_dtype)) return QG_ERR_INVALID_ARG;
+    if (x_dtype == QG_F32 || num_experts > 256) return QG_ERR_UNSUPPORTED;  // the grouped tensor-core launch only
+    if (bits != 2 && bits != 4 && bits != 8) return QG_ERR_UNSUPPORTED;
+    if (!valid_bs(block_size)) return QG_ERR_UNSUPPORTED;
+    if (K % block_size) return QG_ERR_INVALID_ARG;
+    if (max_rows > kMaxM || N > kMaxN || K > kMaxK) return QG_ERR_UNSUPPORTED;
+    if ((static_cast<long long>(N) * K * bits / 8) % 16 || (static_cast<long long>(N) * (K / block_size) * 2) % 16)
+        return QG_ERR_UNSUPPORTED;
+    if (!expert_offsets_dev || (reinterpret_cast<uintptr_t>(expert_offsets_dev) & 7u)) return QG_ERR_INVALID_ARG;
+    if (max_rows == 0 || N == 0) return QG_OK;
+    if (!Y) return QG_ERR_INVALID_ARG;
+    if (K == 0) return QG_ERR_UNSUPPORTED;  // no contraction: the rows to zero are not known on the host
+    if (!X || !W || !scales_f16) return QG_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(W) || !aligned16(scales_f16) || (zero_points_f16 && !aligned16(zero_points_f16)))
+        return QG_ERR_INVALID_ARG;
+    if (!qg::tc_eligible(kRaggedTcRows, K, bits, x_dtype, block_size, qg::WK_NBITS)) return QG_ERR_UNSUPPORTED;
+    const size_t need = qmoe_ragged_mm_device_offsets_workspace_bytes(num_experts);
+    if (!workspace || workspace_bytes < need) return QG_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(workspace)) return QG_ERR_INVALID_ARG;
+    GemmProblem p{};
+    p.A = X;
+    p.a_dtype = x_dtype;
+    p.W = W;
+    p.kind = qg::WK_NBITS;
+    p.scales = scales_f16;
+    p.zp = zero_points_f16;
+    p.zp_mode = zero_points_f16 ? qg::ZP_TENSOR : qg::ZP_NONE;
+    p.uniform_zp = static_cast<float>(1 << (bits - 1));
+    p.Y = Y;
+    p.y_dtype = y_dtype;
+    p.M = max_rows;
+    p.N = N;
+    p.K = K;
+    p.bits = bits;
+    p.bs = block_size;
+    const cudaError_t e = qg::tc_gemm_grouped_dev(p, expert_offsets_dev, num_experts, static_cast<int *>(workspace),
+                                                  status_dev, reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return QG_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
 int qg_read_device_fault(unsigned int *flags) {
     if (!flags) return QG_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return QG_ERR_CUDA;

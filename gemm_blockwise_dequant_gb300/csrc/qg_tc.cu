@@ -272,7 +272,11 @@ __device__ __forceinline__ uint4 dequant8_codebook(uint32_t codes, float am, con
 // Grouped (ragged expert) mode: expert e owns activation rows row_off[e] ..
 // row_off[e+1]-1 and weight rows e*N .. e*N+N-1 of the stacked [E*N] weight
 // tensors; its M tiles are numbered mt_prefix[e] .. mt_prefix[e+1]-1 (an
-// expert the grouped launch leaves out has none).  Passed by value.
+// expert the grouped launch leaves out has none).  Passed by value -- or,
+// when `dev` is set, read after the grid-dependency wait from that device
+// table (mt_prefix[kMaxGroups + 1] then row_off[kMaxGroups + 1]), which the
+// planning kernel wrote from device-resident offsets; M tiles at or past
+// mt_prefix[count] then have no work.
 constexpr int kMaxGroups = 256;
 template <bool G>
 struct TcGroups {
@@ -281,6 +285,7 @@ struct TcGroups {
 template <>
 struct TcGroups<true> {
     int count;
+    const int *dev;
     int mt_prefix[kMaxGroups + 1];
     int row_off[kMaxGroups + 1];
 };
@@ -378,6 +383,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if constexpr (GROUPED) {
+        if (grp.dev) {  // the tile map the planning kernel wrote (visible after pdl_wait)
+            const int *pre = grp.dev, *roff = grp.dev + kMaxGroups + 1;
+            const int mt = tile / p.nt;
+            if (mt >= __ldcg(pre + grp.count)) {
+                nks = 0;  // no work: no copies, no MMAs, no rows written
+                m0 = m_end = wrow = 0;
+            } else {
+                int lo = 0, hi = grp.count;
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (__ldcg(pre + mid) <= mt) lo = mid;
+                    else hi = mid;
+                }
+                m0 = __ldcg(roff + lo) + (mt - __ldcg(pre + lo)) * kBM;
+                m_end = __ldcg(roff + lo + 1);
+                wrow = lo * p.N;
+            }
+        }
+    }
 
     if (warp == 0 && p.par_plain) {
         // ------------------------------------------------------------ producer, parameters by cp.async
@@ -605,6 +630,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// The tile map of a grouped launch from device-resident expert offsets: expert
+// e owns rows offs[e] .. offs[e+1]-1 and ceil(rows / kBM) M tiles (none when
+// it has no row); map = mt_prefix[kMaxGroups + 1] then row_off[kMaxGroups + 1].
+// Offsets that do not start at 0, decrease, or end past max_rows give an
+// empty map (no tile has work) and set *status to 1.
+__global__ void ragged_plan_kernel(const int64_t *__restrict__ offs, int E, long long max_rows, int *__restrict__ map,
+                                   int *__restrict__ status) {
+    __shared__ int tiles[kMaxGroups];
+    __shared__ int bad;
+    pdl_wait();  // the offsets may come from the preceding kernel (a router)
+    pdl_launch_dependents();
+    if (threadIdx.x == 0) bad = (offs[0] != 0 || offs[E] > max_rows) ? 1 : 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const long long c = offs[e + 1] - offs[e];
+        if (c < 0) atomicOr(&bad, 1);
+        tiles[e] = c > 0 ? static_cast<int>((c + kBM - 1) / kBM) : 0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int acc = 0;
+        for (int e = 0; e <= E; ++e) {
+            map[e] = bad ? 0 : acc;
+            map[kMaxGroups + 1 + e] = bad ? 0 : static_cast<int>(offs[e]);
+            if (e < E && !bad) acc += tiles[e];
+        }
+        if (bad && status) *status = 1;
     }
 }
 
@@ -913,6 +968,48 @@ cudaError_t tc_gemm_grouped(const GemmProblem &p, const int64_t *offsets, int E,
     CUtensorMap am, cm, pm, zm;
     const cudaError_t me = build_maps(enc, p, c.bn, static_cast<long long>(E) * p.N, am, cm, pm, zm);
     if (me != cudaSuccess) return me;
+    TcArgs a = make_args(p, c);
+    a.w_rows = E * p.N;
+    const bool bf16 = p.a_dtype == 2;
+    const int grid = c.full_tiles;
+#define QG_TCG(B_, BF_, BN_) \
+    if (p.bits == B_ && bf16 == BF_ && c.bn == BN_) return launch_tc<WK_NBITS, B_, BF_, BN_, true>(am, cm, pm, zm, a, grid, g, s);
+    QG_TCG(4, false, 256) QG_TCG(4, false, 128) QG_TCG(4, true, 256) QG_TCG(4, true, 128)
+    QG_TCG(2, false, 256) QG_TCG(2, false, 128) QG_TCG(2, true, 256) QG_TCG(2, true, 128)
+    QG_TCG(8, false, 256) QG_TCG(8, false, 128) QG_TCG(8, true, 256) QG_TCG(8, true, 128)
+#undef QG_TCG
+    return cudaErrorNotSupported;
+}
+
+// The same grouped launch from device-resident offsets (no host copy of them):
+// a one-CTA planning kernel writes the tile map into `map_ws` (2 (kMaxGroups +
+// 1) ints), then the grid covers the most M tiles any offsets within max_rows
+// rows can need, ceil(max_rows / kBM) + E, and tiles past the map's end exit.
+// Every expert with rows takes the tensor cores.  p.M = max_rows.
+cudaError_t tc_gemm_grouped_dev(const GemmProblem &p, const int64_t *offsets_dev, int E, int *map_ws, int *status,
+                                cudaStream_t s) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc || E > kMaxGroups || p.kind != WK_NBITS) return cudaErrorNotSupported;
+    cudaError_t e = launch_pdl(ragged_plan_kernel, dim3(1), dim3(256), 0, s, offsets_dev, E,
+                               static_cast<long long>(p.M), map_ws, status);
+    if (e != cudaSuccess) return e;
+    TcGroups<true> g{};
+    g.count = E;
+    g.dev = map_ws;
+    const int tiles_m = (p.M + kBM - 1) / kBM + E;
+    TcCfg c = choose_tc(std::max(kBM, p.M / E), p.N, p.K, p.bits);
+    if (c.bn == 0) return cudaErrorNotSupported;
+    const int bn = (p.N >= 256 && smem_bytes(256, p.bits) <= device_info().max_smem_optin) ? 256 : 128;
+    c.bn = bn;
+    c.nt = (p.N + bn - 1) / bn;
+    c.mt = tiles_m;
+    c.full_tiles = tiles_m * c.nt;
+    c.tail_tiles = 0;
+    c.tail_splits = 1;
+    c.tail_kps = c.nk;
+    CUtensorMap am, cm, pm, zm;
+    e = build_maps(enc, p, c.bn, static_cast<long long>(E) * p.N, am, cm, pm, zm);
+    if (e != cudaSuccess) return e;
     TcArgs a = make_args(p, c);
     a.w_rows = E * p.N;
     const bool bf16 = p.a_dtype == 2;

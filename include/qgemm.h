@@ -351,6 +351,39 @@ size_t qmoe_ragged_mm_workspace_bytes(int x_dtype, const int64_t *expert_offsets
                                       int bits, int block_size);
 
 /*
+ * qmoe_ragged_mm_device_offsets -- the ragged expert GEMM above with the
+ * expert offsets in DEVICE memory, so that a router on the GPU needs no host
+ * round trip: the computation and the reading of the pages are those of
+ * qmoe_ragged_mm ([hip-ep #1318] kernel test table, qmoe_ragged_mm leaf;
+ * [hip-ep #1328] "Summary": the QMoE op family).
+ *
+ *   expert_offsets_dev  [num_experts + 1] int64, device, 8-byte aligned,
+ *                       read on the device after the preceding work on the
+ *                       stream: offs[0] = 0, never decreasing, offs[E] <=
+ *                       max_rows.  Offsets breaking that rule make the call
+ *                       compute nothing and set *status_dev to 1 (status_dev
+ *                       may be NULL; it is never cleared).
+ *   max_rows            rows X and Y hold (host int, >= the real T); rows of
+ *                       Y at or past offs[E] are left untouched
+ *   X                   [max_rows][K] fp16 or bf16 (fp32: QG_ERR_UNSUPPORTED)
+ *   W, scales, zero points, Y, N, K, bits, block_size as qmoe_ragged_mm
+ *   num_experts         1 .. 256
+ *   workspace           device, 16-byte aligned, at least
+ *                       qmoe_ragged_mm_device_offsets_workspace_bytes(E)
+ *                       bytes (the tile map the planning kernel writes)
+ * Every expert with rows runs in one grouped tensor-core launch (sized for the
+ * most tiles offsets within max_rows can need; tiles past the real count end
+ * at once), after a one-CTA planning kernel.  Returns QG_OK, QG_ERR_* for
+ * refused arguments (before any launch) or QG_ERR_CUDA.
+ */
+int qmoe_ragged_mm_device_offsets(const void *X, int x_dtype, const int64_t *expert_offsets_dev, int num_experts,
+                                  int max_rows, const uint8_t *W, const uint16_t *scales_f16,
+                                  const uint16_t *zero_points_f16, void *Y, int y_dtype, int N, int K, int bits,
+                                  int block_size, void *workspace, size_t workspace_bytes, int *status_dev,
+                                  qg_stream_t stream);
+size_t qmoe_ragged_mm_device_offsets_workspace_bytes(int num_experts);
+
+/*
  * qg_gather_block_quantized -- embedding lookup in a block-quantized table.
  * [hip-ep #1318] kernel test table, gather_block_quantized leaves
  * Xi64_Wu4_Yfp16, Xi64_Wu8_Yfp16 and Xi64_Wfp8_Yfp16 ("Summary", Commit 3:

@@ -145,3 +145,93 @@ def test_ragged_prompt_128_experts_top8_full_size(qg, N, K):
         got = Y[rows][:, cols].float().double().cpu().numpy()
         assert O.max_rel_l2(got, ref) <= 5e-3, e
     assert not torch().isnan(Y).any()
+
+
+def _run_dev(qg, d, Xd, y_dtype, extra_rows=0, offsets=None, status=None):
+    """The device-offset entry point; X and Y hold extra_rows rows past T (Y's NaN there must stay)."""
+    t = torch()
+    off = np.asarray(d["offsets"] if offsets is None else offsets, np.int64)
+    T = int(d["offsets"][-1])
+    if extra_rows:
+        Xd = t.cat([Xd, t.zeros((extra_rows, Xd.shape[1]), dtype=Xd.dtype, device="cuda")])
+    Y = t.full((T + extra_rows, d["N"]), float("nan"), dtype=getattr(t, DT[y_dtype]), device="cuda")
+    zp = None if d["zero_points"] is None else dev(d["zero_points"], t.float16)
+    s = qg.qmoe_ragged_mm_device_offsets(Xd, t.from_numpy(off).cuda(), dev(d["W"]), dev(d["scales"], t.float16), zp,
+                                         Y, bits=d["bits"], block_size=d["block_size"], status=status, raw=True)
+    t.cuda.synchronize()
+    return s, Y
+
+
+@pytest.mark.parametrize("bits,bs,x_dtype,y_dtype,zp", [
+    (4, 64, 1, 1, False),
+    (4, 32, 2, 0, True),
+    (2, 64, 1, 0, False),
+    (8, 128, 2, 2, True),
+])
+def test_ragged_device_offsets_match_oracle(qg, bits, bs, x_dtype, y_dtype, zp):
+    """Offsets in device memory: every expert with rows (1..8 included) runs in the grouped tensor-core
+    launch, sized for max_rows; rows of Y past offsets[E] stay untouched."""
+    t = torch()
+    d = WL.ragged(num_experts=len(COUNTS), N=200, K=512, bits=bits, block_size=bs, with_zp=zp, counts=COUNTS,
+                  seed=bits + bs + 1)
+    Xd, Xo, od = _x(d, x_dtype)
+    status = t.zeros(1, dtype=t.int32, device="cuda")
+    s, Y = _run_dev(qg, d, Xd, y_dtype, extra_rows=300, status=status)
+    assert s == qg.QG_OK
+    assert int(status.item()) == 0
+    T = int(d["offsets"][-1])
+    ref = O.qmoe_ragged_mm(Xo, d["offsets"], d["W"], d["scales"], d["zero_points"], N=d["N"], K=d["K"],
+                           bits=bits, block_size=bs, x_dtype=od)
+    got = Y[:T].float().double().cpu().numpy()
+    assert O.max_rel_l2(got, ref) <= 5e-3
+    assert t.isnan(Y[T:].float()).all()
+    # repeated calls are bit-identical
+    _, Y2 = _run_dev(qg, d, Xd, y_dtype, extra_rows=300)
+    assert t.equal(Y2[:T], Y[:T])
+
+
+def test_ragged_device_offsets_refusals(qg):
+    """Offsets the planning kernel refuses (not starting at 0, decreasing, past max_rows) compute nothing
+    and set the status word; host-side refusals come before any launch."""
+    t = torch()
+    d = WL.ragged(num_experts=4, N=96, K=256, bits=4, block_size=32, counts=[5, 20, 0, 7], seed=4)
+    Xd, _, _ = _x(d, 1)
+    for bad in ([1, 5, 25, 25, 32], [0, 5, 3, 25, 32], [0, 5, 25, 25, 40]):
+        status = t.zeros(1, dtype=t.int32, device="cuda")
+        s, Y = _run_dev(qg, d, Xd, 1, offsets=bad, status=status)
+        assert s == qg.QG_OK
+        assert int(status.item()) == 1, bad
+        assert t.isnan(Y.float()).all(), bad
+    W, S = dev(d["W"]), dev(d["scales"], t.float16)
+    off = t.from_numpy(np.asarray(d["offsets"], np.int64)).cuda()
+    Y = t.zeros((32, 96), dtype=t.float16, device="cuda")
+    x32 = t.zeros((32, 256), dtype=t.float32, device="cuda")
+    assert qg.qmoe_ragged_mm_device_offsets(x32, off, W, S, None, Y, bits=4, block_size=32, raw=True) == \
+        qg.QG_ERR_UNSUPPORTED  # fp32 activations: not on the grouped launch
+    assert qg.qmoe_ragged_mm_device_offsets(Xd, off, W, S, None, Y, bits=3, block_size=32, raw=True) == \
+        qg.QG_ERR_UNSUPPORTED
+    assert qg.qmoe_ragged_mm_device_offsets_workspace_bytes(0) == 0
+    assert qg.qmoe_ragged_mm_device_offsets_workspace_bytes(257) == 0
+    t.cuda.synchronize()
+
+
+def test_ragged_device_offsets_prompt_full_size(qg):
+    """The 128-expert top-8 2048 / 768 layer's fc1 over 2048 tokens with device offsets: sampled rows of
+    sampled experts against the oracle."""
+    d = WL.ragged(N=1536, K=2048)
+    Xd, Xo, od = _x(d, 1)
+    s, Y = _run_dev(qg, d, Xd, 1)
+    assert s == qg.QG_OK
+    off = d["offsets"]
+    g = np.random.default_rng(7)
+    cols = np.unique(np.concatenate([[0, d["N"] - 1], g.choice(d["N"], 62, replace=False)])).astype(np.int64)
+    for e in sorted(set(g.choice(d["num_experts"], 6, replace=False).tolist()) | {0, d["num_experts"] - 1}):
+        a, b = int(off[e]), int(off[e + 1])
+        if a == b:
+            continue
+        rows = sorted({a, b - 1, int(g.integers(a, b))})
+        ref = O.qgemm_nbits(Xo[rows], d["W"][e], d["scales"][e], None, M=len(rows), N=d["N"], K=d["K"], bits=4,
+                            block_size=32, a_dtype=od, rows=cols)
+        got = Y[rows][:, cols].float().double().cpu().numpy()
+        assert O.max_rel_l2(got, ref) <= 5e-3, e
+    assert not torch().isnan(Y).any()
