@@ -85,7 +85,9 @@ constexpr long long kMaxM = 1 << 20;
 // Code widths of the GEMM entry points: MatMulNBits u2 / u3 / u4 / u8 (the codebook is 4-bit).
 bool valid_bits(int bits) { return bits == 2 || bits == 3 || bits == 4 || bits == 8; }
 
-size_t gemm_workspace(int a_dtype, int M, int N, int K, int bits, int bs) {
+// The workspace a GEMM call cannot do without (the SIMT split-K partials, the
+// tensor-core tail pieces).
+size_t gemm_workspace_min(int a_dtype, int M, int N, int K, int bits, int bs) {
     if (M <= 0 || N <= 0 || K <= 0 || !valid_bits(bits) || !valid_bs(bs) || K % bs) return 0;
     // the query has no weight kind: the larger need of MatMulNBits and codebook
     // (their tensor-core eligibility differs when K / bs is not a multiple of 8)
@@ -93,6 +95,17 @@ size_t gemm_workspace(int a_dtype, int M, int N, int K, int bits, int bs) {
     for (int kind : {qg::WK_NBITS, qg::WK_CODEBOOK})
         need = std::max(need, qg::tc_eligible(M, K, bits, a_dtype, bs, kind) ? qg::tc_workspace_bytes(M, N, K, bits)
                                                                               : qg::simt_workspace_bytes(M, N, K, bits, bs));
+    return need;
+}
+
+// The workspace the query reports: the minimum, or, for fp32 activations with
+// enough rows on a tensor-core shape, room for the split-precision path (a
+// call whose workspace is smaller takes the slower path instead).
+size_t gemm_workspace(int a_dtype, int M, int N, int K, int bits, int bs) {
+    size_t need = gemm_workspace_min(a_dtype, M, N, K, bits, bs);
+    if (need == 0 && (M <= 0 || N <= 0 || K <= 0 || !valid_bits(bits) || !valid_bs(bs) || K % bs)) return 0;
+    if (a_dtype == QG_F32 && M >= qg::kSplitMinRows && qg::tc_eligible(M, K, bits, QG_F16, bs, qg::WK_NBITS))
+        need = std::max(need, qg::split_workspace_bytes(M, K));
     return need;
 }
 
@@ -113,7 +126,7 @@ int check_gemm(const void *A, int a_dtype, const uint8_t *W, const void *params,
         if (!aligned16(A) || !aligned16(W) || !aligned16(params)) return QG_ERR_INVALID_ARG;
         if (zp && !aligned16(zp)) return QG_ERR_INVALID_ARG;
     }
-    const size_t need = gemm_workspace(a_dtype, M, N, K, bits, bs);
+    const size_t need = gemm_workspace_min(a_dtype, M, N, K, bits, bs);
     if (need > 0) {
         if (!ws || ws_bytes < need) return QG_ERR_WORKSPACE_TOO_SMALL;
         if (!aligned16(ws)) return QG_ERR_INVALID_ARG;
@@ -130,7 +143,9 @@ int run_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s) {
             return QG_ERR_CUDA;
         return QG_OK;
     }
-    const cudaError_t e = qg::tc_eligible(p.M, p.K, p.bits, p.a_dtype, p.bs, p.kind) ? qg::tc_gemm(p, ws, ws_bytes, s)
+    const bool split = qg::split_eligible(p) && ws && aligned16(ws) && ws_bytes >= qg::split_workspace_bytes(p.M, p.K);
+    const cudaError_t e = split                                                             ? qg::split_gemm(p, ws, ws_bytes, s)
+                          : qg::tc_eligible(p.M, p.K, p.bits, p.a_dtype, p.bs, p.kind) ? qg::tc_gemm(p, ws, ws_bytes, s)
                           : qg::mma_gemv_eligible(p)                                   ? qg::mma_gemv(p, s)
                                                                                        : qg::simt_gemm(p, ws, ws_bytes, s);
     if (e == cudaErrorNotSupported) return QG_ERR_UNSUPPORTED;

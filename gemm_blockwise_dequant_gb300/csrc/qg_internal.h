@@ -66,6 +66,10 @@ struct GemmProblem {
     void *Y;
     int y_dtype;
     int M, N, K, bits, bs;
+    // tensor-core split-precision pass (qg_tc.cu): weight part, accumulate, row scales
+    int tc_wpart = 0;
+    int tc_acc = 0;
+    const float *tc_row_scale = nullptr;
 };
 
 // SIMT decode path (small M).
@@ -83,6 +87,13 @@ bool mma_gemv_plan(int M, int N, int K, int a_dtype, int zp_mode, int out[4]);
 
 // Tensor-core path (M >= 9 with 16-bit activations).
 bool tc_eligible(int M, int K, int bits, int a_dtype, int bs, int kind);
+// fp32 activations on the tensor cores by split precision (three fp16 passes:
+// A_hi w_hi + A_hi w_lo + A_lo w_hi, per-row power-of-two scaling), when the
+// caller's workspace holds split_workspace_bytes(M, K).
+constexpr int kSplitMinRows = 16;
+size_t split_workspace_bytes(int M, int K);
+bool split_eligible(const GemmProblem &p);
+cudaError_t split_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s);
 size_t tc_workspace_bytes(int M, int N, int K, int bits);
 cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s);
 // Ragged expert GEMM (grouped tensor-core launch over the experts with at least

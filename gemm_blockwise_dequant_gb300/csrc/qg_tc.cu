@@ -92,6 +92,12 @@ struct TcArgs {
     // bytes cannot be a tensor map: the producer warp copies them with 4-byte
     // cp.async instead (nb even); w_rows = rows of the weight tensors
     int par_plain, w_rows;
+    // Split-precision passes (fp32 activations): wpart 1 makes the fp16 weight
+    // operand the residual fp16(w - fp16(w)) of the fp32 weight w instead of
+    // fp16(w); the epilogue multiplies activation row m by row_scale[m] (when
+    // set) and, with acc, adds to the fp32 Y instead of writing it.
+    int wpart, acc;
+    const float *row_scale;
     unsigned *fault;
 };
 
@@ -187,6 +193,7 @@ __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_c
 struct UnitPar {
     __half2 zp2, s2;  // fp16 operand
     float zpf, sf;    // bf16 operand
+    bool lo;          // fp16 operand: the residual part of the weight
 };
 
 // One operand pair from two exact integer codes q (an fp16 pair).
@@ -206,7 +213,13 @@ __device__ __forceinline__ uint32_t operand_pair(__half2 q, const UnitPar &u) {
         const __nv_bfloat162 b = __floats2bfloat162_rn(w0, w1);
         return *reinterpret_cast<const uint32_t *>(&b);
     } else {
-        return h2_as_u32(__hmul2(__hsub2(q, u.zp2), u.s2));
+        if (!u.lo) return h2_as_u32(__hmul2(__hsub2(q, u.zp2), u.s2));
+        // the residual: w (exact in fp32) minus its fp16 rounding, rounded to fp16
+        const float2 qf = __half22float2(q);
+        const float zf = __low2float(u.zp2), sf = __low2float(u.s2);
+        const float w0 = __fmul_rn(__fsub_rn(qf.x, zf), sf), w1 = __fmul_rn(__fsub_rn(qf.y, zf), sf);
+        const __half2 hi = __floats2half2_rn(w0, w1);
+        return h2_as_u32(__floats2half2_rn(w0 - __low2float(hi), w1 - __high2float(hi)));
     }
 }
 
@@ -551,6 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint4 w;
                 if constexpr (WK == WK_NBITS) {
                     UnitPar u;
+                    u.lo = p.wpart != 0;
                     if constexpr (BF16) {
                         u.zpf = zt ? h2f(static_cast<uint16_t>(zv[j])) : p.zpv;
                         u.sf = h2f(static_cast<uint16_t>(pv[j]));
@@ -594,6 +608,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 8; ++j)
                     dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            } else if (p.row_scale) {  // split-precision pass: fp32 Y = (acc ? Y : 0) + sum * row scale
+                const float rs = p.row_scale[m];
+                float *y = static_cast<float *>(p.Y) + static_cast<size_t>(m) * p.N + nb0;
+                if ((p.N & 3) == 0 && nb0 + 32 <= p.N) {
+                    float4 *dst = reinterpret_cast<float4 *>(y);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float4 v = make_float4(__uint_as_float(r[4 * j]) * rs, __uint_as_float(r[4 * j + 1]) * rs,
+                                               __uint_as_float(r[4 * j + 2]) * rs, __uint_as_float(r[4 * j + 3]) * rs);
+                        if (p.acc) {
+                            const float4 o = dst[j];
+                            v = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+                        }
+                        dst[j] = v;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (nb0 + j < p.N) y[j] = (p.acc ? y[j] : 0.f) + __uint_as_float(r[j]) * rs;
+                }
             } else if (p.y_dtype == 0 && (p.N & 3) == 0 && nb0 + 32 <= p.N) {
                 float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.Y) + static_cast<size_t>(m) * p.N + nb0);
 #pragma unroll
@@ -660,6 +694,40 @@ __global__ void ragged_plan_kernel(const int64_t *__restrict__ offs, int E, long
             if (e < E && !bad) acc += tiles[e];
         }
         if (bad && status) *status = 1;
+    }
+}
+
+// fp32 activations for the split-precision passes: per row m, e = the exponent
+// of the largest |a| (clamped to [-110, 117]), a' = a * 2^(14 - e) (largest
+// magnitude in [2^14, 2^15): fp16 range), hi = fp16(a'), lo = fp16(a' - hi),
+// and the row's output multiplier 2^(e - 14).  One CTA per row.
+__global__ void split_rows_kernel(const float *__restrict__ A, int K, __half *__restrict__ hi,
+                                  __half *__restrict__ lo, float *__restrict__ row_scale) {
+    __shared__ float wmax[32];
+    pdl_wait();
+    pdl_launch_dependents();
+    const size_t base = static_cast<size_t>(blockIdx.x) * K;
+    float mx = 0.f;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) mx = fmaxf(mx, fabsf(A[base + k]));
+    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        mx = threadIdx.x < blockDim.x / 32 ? wmax[threadIdx.x] : 0.f;
+        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (threadIdx.x == 0) wmax[0] = mx;
+    }
+    __syncthreads();
+    const unsigned bits = __float_as_uint(wmax[0]);
+    const int ef = static_cast<int>((bits >> 23) & 0xFFu);
+    const int e = (bits == 0u || ef == 255) ? 0 : min(max(ef - 127, -110), 117);
+    const float up = exp2i(14 - e);
+    if (threadIdx.x == 0) row_scale[blockIdx.x] = exp2i(e - 14);
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+        const float x = A[base + k] * up;
+        const __half h = __float2half_rn(x);
+        hi[base + k] = h;
+        lo[base + k] = __float2half_rn(x - __half2float(h));
     }
 }
 
@@ -858,6 +926,9 @@ TcArgs make_args(const GemmProblem &p, const TcCfg &c) {
     a.y_vec16 = p.y_dtype != 0 && (p.N & 7) == 0 && (reinterpret_cast<uintptr_t>(p.Y) & 15u) == 0;
     a.par_plain = p.kind == WK_NBITS && (p.K / p.bs) % 8 != 0;
     a.w_rows = p.N;
+    a.wpart = p.tc_wpart;
+    a.acc = p.tc_acc;
+    a.row_scale = p.tc_row_scale;
     a.fault = fault_word();
     return a;
 }
@@ -887,8 +958,14 @@ size_t tc_workspace_bytes(int M, int N, int K, int bits) {
 cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    const TcCfg c = choose_tc(p.M, p.N, p.K, p.bits);
+    TcCfg c = choose_tc(p.M, p.N, p.K, p.bits);
     if (c.bn == 0) return cudaErrorNotSupported;
+    if (p.tc_row_scale) {  // split-precision passes write (or add to) Y directly: every tile takes the whole K
+        c.full_tiles += c.tail_tiles;
+        c.tail_tiles = 0;
+        c.tail_splits = 1;
+        c.tail_kps = c.nk;
+    }
     CUtensorMap am, cm, pm, zm;
     const cudaError_t me = build_maps(enc, p, c.bn, p.N, am, cm, pm, zm);
     if (me != cudaSuccess) return me;
@@ -1021,6 +1098,43 @@ cudaError_t tc_gemm_grouped_dev(const GemmProblem &p, const int64_t *offsets_dev
     QG_TCG(8, false, 256) QG_TCG(8, false, 128) QG_TCG(8, true, 256) QG_TCG(8, true, 128)
 #undef QG_TCG
     return cudaErrorNotSupported;
+}
+
+size_t split_workspace_bytes(int M, int K) {
+    const size_t part = (static_cast<size_t>(M) * K * 2 + 255) / 256 * 256;
+    return 2 * part + (static_cast<size_t>(M) * 4 + 255) / 256 * 256;
+}
+
+bool split_eligible(const GemmProblem &p) {
+    return p.a_dtype == 0 && p.y_dtype == 0 && p.kind == WK_NBITS && p.M >= kSplitMinRows &&
+           tc_eligible(p.M, p.K, p.bits, 1, p.bs, p.kind);
+}
+
+// Y = rs (A_hi w_hi + A_hi w_lo + A_lo w_hi): three tensor-core passes over the
+// activations split by split_rows_kernel, in that fixed order (the first
+// writes Y, the others add to it).  A_lo w_lo (below 2^-22 of each product)
+// is left out.
+cudaError_t split_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s) {
+    if (!ws || ws_bytes < split_workspace_bytes(p.M, p.K)) return cudaErrorInvalidValue;
+    const size_t part = (static_cast<size_t>(p.M) * p.K * 2 + 255) / 256 * 256;
+    __half *hi = static_cast<__half *>(ws);
+    __half *lo = reinterpret_cast<__half *>(static_cast<char *>(ws) + part);
+    float *rs = reinterpret_cast<float *>(static_cast<char *>(ws) + 2 * part);
+    cudaError_t e = launch_pdl(split_rows_kernel, dim3(p.M), dim3(256), 0, s, static_cast<const float *>(p.A), p.K, hi,
+                               lo, rs);
+    if (e != cudaSuccess) return e;
+    GemmProblem q = p;
+    q.a_dtype = 1;
+    q.tc_row_scale = rs;
+    const void *a_of[3] = {hi, hi, lo};
+    for (int pass = 0; pass < 3; ++pass) {
+        q.A = a_of[pass];
+        q.tc_wpart = pass == 1 ? 1 : 0;
+        q.tc_acc = pass > 0 ? 1 : 0;
+        e = tc_gemm(q, nullptr, 0, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace qg
