@@ -175,3 +175,33 @@ def test_mma_gemv_fp32_prefill_gate_up_sampled(qg, M):
     err = O.max_rel_l2(got, oracle_nbits(d, rows=rows))
     assert err <= 1e-4, err
     assert torch().equal(_run(qg, d, F32), Y)
+
+
+def test_fp32_split_precision_rows_and_workspace(qg):
+    """fp32 activations and output with M >= 16 on the tensor cores by split precision: rows of very
+    different magnitudes (each scaled by its own power of two), a zero row (exact zeros), a zero-point
+    tensor, at the fp32 bar per row; with a workspace too small for the split activations the call takes
+    the tensor-pipe GEMV row groups instead and agrees within the same bar."""
+    t = torch()
+    M, N, K = 40, 300, 2048
+    d = _case(29, M, N, K, F32, "tensor")
+    A = d["A"].astype(np.float64)
+    A[1] = 0.0
+    A[2] *= 2.0 ** -60
+    A[3] *= 2.0 ** 70
+    d["A"] = A.astype(np.float32)
+    tv = nbits_case(d)
+    ref = oracle_nbits(d)
+    Y = y_tensor(M, N, F32)
+    qg.qgemm_nbits(tv["A"], tv["W"], tv["scales"], tv["zero_points"], Y, bits=2, block_size=64)
+    t.cuda.synchronize()
+    y = Y.cpu().numpy()
+    assert np.all(y[1] == 0.0)
+    for m in [0] + list(range(2, M)):
+        assert O.max_rel_l2(to64(Y)[m:m + 1], ref[m:m + 1]) <= 1e-4, m
+    small = t.empty(16, dtype=t.uint8, device="cuda")
+    Y2 = y_tensor(M, N, F32)
+    qg.qgemm_nbits(tv["A"], tv["W"], tv["scales"], tv["zero_points"], Y2, bits=2, block_size=64, workspace=small)
+    t.cuda.synchronize()
+    assert O.max_rel_l2(to64(Y2), ref) <= 1e-4
+    assert qg.qgemm_workspace_bytes(F32, M, N, K, 2, 64) >= 2 * M * K * 2
