@@ -67,6 +67,7 @@ struct MgArgs {
     int NST, ntiles;  // ring stages (16-row fills), 32-row tiles
     int b_off, sp_off, om_off, zero_off, stage_off, stage_bytes, par_off, zp_off, red_off, pq_off;
     int bov;          // first ring stage that holds the B fragments until every warp has them in registers (NST: none)
+    int ast;          // first ring stage that receives the activations (one bulk copy) for the prologue, or -1
     unsigned *fault;
 };
 
@@ -135,23 +136,24 @@ __device__ __forceinline__ void owner_of(int blk, int wd, int &j, int &c, int &w
 // One warp prepares span sp: lane L owns code word L (block L / 4, word L % 4,
 // codes k = 512 sp + 16 L .. + 15).  Lane L's 16 activations of span sp,
 // activation row m: zeros for rows m >= M.
-__device__ __forceinline__ void load_span_act(const MgArgs &p, int sp, int m, int lane, float (&a)[16]) {
+// A is the activation matrix in global memory, or its copy in shared memory.
+__device__ __forceinline__ void load_span_act(const MgArgs &p, const void *A, int sp, int m, int lane, float (&a)[16]) {
     const size_t k0 = static_cast<size_t>(sp) * kSpanCodes + 16 * lane;
     if (m >= p.M) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) a[i] = 0.f;
     } else if (p.a_dtype == 0) {
-        const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(p.A) + m * static_cast<size_t>(p.K) + k0);
+        const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(A) + m * static_cast<size_t>(p.K) + k0);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float4 v = __ldg(src + q);
+            const float4 v = src[q];
             a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
         }
     } else {
-        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.A) + m * static_cast<size_t>(p.K) + k0);
+        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(A) + m * static_cast<size_t>(p.K) + k0);
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-            const uint4 v = __ldg(src + q);
+            const uint4 v = src[q];
             const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
@@ -258,6 +260,8 @@ __global__ void __maxnreg__(kMaxRegs)
     uint64_t *empty = full + kMaxStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 2 * kMaxStages * 8);
     uint64_t *bfree = reinterpret_cast<uint64_t *>(smem + 2 * kMaxStages * 8 + 8);  // every consumer holds its B
+    uint64_t *afull = bfree + 1;  // the activations' copy has landed
+    uint64_t *afree = bfree + 2;  // every consumer has read them
     unsigned char *bfrag_w = smem + p.b_off;                    // B-fragment entries of every span
     float *spart = reinterpret_cast<float *>(smem + p.sp_off);  // [blocks][MP]: 2^-24 sum of a' per block
     float *somul = reinterpret_cast<float *>(smem + p.om_off);  // [spans][MP]: each span's output multiplier
@@ -272,6 +276,8 @@ __global__ void __maxnreg__(kMaxRegs)
             mbar_init(&empty[i], W);
         }
         mbar_init(bfree, W * 32);
+        mbar_init(afull, 1);
+        mbar_init(afree, W * 32);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -310,10 +316,21 @@ __global__ void __maxnreg__(kMaxRegs)
                 store_y_elem(p.Y, p.y_dtype, static_cast<size_t>(m) * p.N + n, s);
             }
         };
+        const uint32_t a_bytes = static_cast<uint32_t>(p.M) * p.K * (p.a_dtype == 0 ? 4 : 2);
+        if (p.ast >= 0 && lane == 0) {  // the activations, for the consumers' prologue, ahead of the weights
+            mbar_arrive_expect_tx(afull, a_bytes);
+            bulk_g2s(stages + static_cast<size_t>(p.ast) * p.stage_bytes, p.A, a_bytes, afull);
+        }
         bool alive = true;
         int slot = 0;
         uint32_t par = 1;  // parity of the empty phase to wait for before refilling `slot`
         for (int f = 0; f < total; ++f) {
+            // the first fill into the stages that hold the activations waits
+            // until every consumer thread has read them
+            if (f == p.ast && !__all_sync(0xffffffffu, mbar_wait(afree, 0, abort_flag, p.fault, FAULT_WAIT_EMPTY))) {
+                alive = false;
+                break;
+            }
             // the first fill into the stages that held the B fragments waits
             // until every consumer thread has its fragments in registers
             if (f == p.bov && p.bov < p.NST &&
@@ -374,18 +391,25 @@ __global__ void __maxnreg__(kMaxRegs)
     // a batch are all in flight together (one memory latency per batch, which
     // the weight stream started by the producer makes long).
     {
+        // the activations' copy in the ring (one bulk copy by the producer), or global memory
+        const void *asrc = p.A;
+        if (p.ast >= 0) {
+            mbar_wait(afull, 0, abort_flag, p.fault, FAULT_WAIT_FULL);
+            asrc = stages + static_cast<size_t>(p.ast) * p.stage_bytes;
+        }
         const int items = (p.spans - sl + W - 1) / W * MP;
 #pragma unroll 1
         for (int b = 0; b < items; b += 4) {
             float a[4][16];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                if (b + q < items) load_span_act(p, sl + (b + q) / MP * W, (b + q) % MP, lane, a[q]);
+                if (b + q < items) load_span_act(p, asrc, sl + (b + q) / MP * W, (b + q) % MP, lane, a[q]);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 if (b + q < items)
                     build_span_row<MP, NT>(sl + (b + q) / MP * W, (b + q) % MP, lane, a[q], bfrag_w, spart, somul);
         }
+        if (p.ast >= 0) mbar_arrive(afree);  // this thread's reads of the copy are done
     }
     __syncwarp();
 
@@ -629,7 +653,7 @@ __global__ void __maxnreg__(kMaxRegs)
 struct MgCfg {
     int MP, NT, TR, spans, W, NST, ntiles, grid;
     int b_off, sp_off, om_off, zero_off, stage_off, stage_bytes, par_off, zp_off, red_off, pq_off, smem;
-    int bov;
+    int bov, ast;
 };
 
 inline int rup(int x, int a) { return (x + a - 1) / a * a; }
@@ -677,6 +701,17 @@ bool layout_mg(int M, int N, int K, int a_dtype, bool zpt, int tr, bool ov, MgCf
     } else {
         c.bov = c.NST;
         c.b_off = kHeader;
+    }
+    // Long K (several spans per warp): the activations go through the ring's
+    // stages 2, 3, ... (after the first tile's two fills, before the B
+    // fragments' stages) as one bulk copy ahead of the weights, when they fit
+    // there -- each warp's loads of four spans' activations otherwise queue
+    // behind the weight stream (down, K = 17920: 18.0 -> 17.0 us).  With one
+    // span per warp the plain loads are as fast.
+    {
+        const int a_bytes = M * K * (a_dtype == 0 ? 4 : 2);
+        const int ka = (a_bytes + c.stage_bytes - 1) / c.stage_bytes;
+        c.ast = (c.spans > c.W && 2 + ka <= c.bov) ? 2 : -1;
     }
     c.red_off = c.stage_off + c.NST * c.stage_bytes;
     c.pq_off = c.red_off + (c.NST / 2) * red_stage;
@@ -785,6 +820,7 @@ cudaError_t mma_gemv_rows(const GemmProblem &p, cudaStream_t s) {
     a.red_off = c.red_off;
     a.pq_off = c.pq_off;
     a.bov = c.bov;
+    a.ast = c.ast;
     a.fault = fault_word();
 #define QG_MG(MP_, NT_, TR_)                                                                        \
     if (c.MP == MP_ && c.NT == NT_ && c.TR == TR_)                                                  \
