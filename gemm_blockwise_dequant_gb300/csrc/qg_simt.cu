@@ -48,7 +48,7 @@ namespace {
 
 constexpr int kMaxStages = 16;
 constexpr int kLutOff = 512;  // after the 2 x kMaxStages mbarriers and the abort flag
-static_assert(2 * kMaxStages * 8 + 4 <= kLutOff, "shared-memory header overlaps the codebook table");
+static_assert(2 * kMaxStages * 8 + 16 <= kLutOff, "shared-memory header overlaps the codebook table");
 
 // Most consumer warps a CTA may have (launch bound), by activation rows held.
 __host__ __device__ constexpr int max_consumer_warps(int mt) { return mt == 1 ? 15 : 11; }
@@ -92,6 +92,7 @@ struct GemvArgs {
     int swiglu_interleaved;
     float *out_f32;           // slot outputs [slots][N] (QMoE), with bias added
     const uint16_t *bias;     // fp16 [experts][N], or nullptr
+    int bias_bulk;            // the producer stages the expert's bias row (one bulk copy), not the consumers
 };
 
 // u3: 32 codes in 3 words; bit position of code i of the group after its
@@ -533,6 +534,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + kMaxStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 2 * kMaxStages * 8);
+    uint64_t *bias_bar = reinterpret_cast<uint64_t *>(smem + 2 * kMaxStages * 8 + 8);  // the bias row landed
     float *lut = reinterpret_cast<float *>(smem + kLutOff);
     float *red = reinterpret_cast<float *>(smem + p.red_off);
     unsigned char *stages = smem + p.stage_off;
@@ -545,6 +547,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], p.S_cta);  // released by the warps of the group that consumed it
         }
+        mbar_init(bias_bar, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -592,6 +595,19 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
         const int e = p.ids ? __ldg(p.ids + cta_slot) : 0;
         const bool valid = e >= 0 && e < p.num_experts;
         const int sl = cta_slot;
+        // the expert's bias row for finish_tile, ahead of the weights (an
+        // invalid expert's outputs are zeros and read no bias)
+        const bool bias_copy = p.bias_off && p.bias_bulk && valid;
+        if (bias_copy && lane == 0) {
+            const uint32_t bb = static_cast<uint32_t>(p.N) * 2;
+            mbar_arrive_expect_tx(bias_bar, bb);
+            bulk_g2s(smem + p.bias_off, p.bias + static_cast<size_t>(e) * p.N, bb, bias_bar);
+        }
+        bool bias_ready = !bias_copy;
+        auto wait_bias = [&]() -> bool {
+            if (!bias_ready) bias_ready = mbar_wait(bias_bar, 0, abort_flag, p.fault, FAULT_WAIT_FULL);
+            return bias_ready;
+        };
         for (int tile = t_begin; tile < t_end; tile += t_stride, ++it) {
             if (!mbar_wait(&empty[slot], par, abort_flag, p.fault, FAULT_WAIT_EMPTY)) {
                 alive = false;
@@ -618,6 +634,10 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
             // finish the tile this slot held before the refill (its sums sit in
             // the reduction slot of the previous fill's parity)
             if (it >= p.NST) {
+                if (!wait_bias()) {
+                    alive = false;
+                    break;
+                }
                 finish_tile<MT, LPR, IT>(p, red + (slot * 2 + par) * (p.S_cta * RV * H), s_count,
                                      tile - p.NST * t_stride, sl, lane, bias_s, e);
             }
@@ -631,6 +651,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
             for (int j = max(0, it - p.NST); j < it; ++j) {
                 const int sj = j % p.NST;
                 if (!mbar_wait(&empty[sj], (j / p.NST) & 1, abort_flag, p.fault, FAULT_WAIT_EMPTY)) break;
+                if (!wait_bias()) break;
                 finish_tile<MT, LPR, IT>(p, red + (sj * 2 + ((j / p.NST) & 1)) * (p.S_cta * RV * H), s_count,
                                      t_begin + j * t_stride, sl, lane, bias_s, e);
             }
@@ -671,7 +692,7 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
             stage_activations<MT, KPL>(p, as, kc0, p.S_cta * LPR, threadIdx.x, NWC * 32);
         else
             stage_swiglu_activations<KPL>(p, as, cta_slot, kc0, p.S_cta * LPR, threadIdx.x, NWC * 32);
-        if (p.bias_off) {  // this CTA's expert bias row, for the producer's finish_tile
+        if (p.bias_off && !p.bias_bulk) {  // this CTA's expert bias row, for the producer's finish_tile
             uint16_t *bs = reinterpret_cast<uint16_t *>(smem + p.bias_off);
             const int be = p.ids ? __ldg(p.ids + cta_slot) : 0;
             const bool bvalid = be >= 0 && be < p.num_experts;
@@ -1135,6 +1156,8 @@ cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s) {
         a.swiglu_interleaved = q.swiglu_interleaved;
         a.out_f32 = fc1 ? g : o;
         a.bias = fc1 ? q.fc1_bias : q.fc2_bias;
+        // one bulk copy of the expert's bias row when its rows are 16-byte runs
+        a.bias_bulk = a.bias && (N * 2) % 16 == 0 && (reinterpret_cast<uintptr_t>(a.bias) & 15u) == 0;
         // each expert slot owns an equal share of the SMs (its activation row is staged once per CTA)
         a.cps = std::max(1, di.sm_count / q.k);
         c.grid_x = q.k * a.cps;
