@@ -90,7 +90,9 @@ enum { QG_F32 = 0, QG_F16 = 1, QG_BF16 = 2 };
  *
  *   w[n][k] = (q[n][k] - zp[n][k/bs]) * s[n][k/bs], computed exactly in fp32;
  *   Y[m][n] = sum_k A[m][k] * w[n][k], accumulated in fp32 (tensor-core path:
- *   the weight is rounded to A's 16-bit type before the product) and rounded
+ *   the weight is rounded to A's 16-bit type before the product; fp32
+ *   activations on the tensor cores -- M >= 16, fp32 Y -- go in split
+ *   precision: A and w each as two fp16 terms, three products) and rounded
  *   once to y_dtype.
  *
  *   A            [M][K], a_dtype (QG_F32, QG_F16 or QG_BF16)
@@ -106,7 +108,11 @@ enum { QG_F32 = 0, QG_F16 = 1, QG_BF16 = 2 };
  *   workspace    device scratch of at least
  *                qgemm_workspace_bytes(a_dtype, M, N, K, bits, block_size)
  *                bytes (NULL allowed when that is 0); its contents on entry
- *                do not matter and are garbage on return.
+ *                do not matter and are garbage on return.  For fp32
+ *                activations with M >= 16 that size includes room for the
+ *                split-precision activations (4 M K bytes); a smaller
+ *                workspace that still covers the call's other needs is
+ *                accepted and takes a slower path (fp32 row groups).
  *   Returns a QG_* status.
  */
 int qgemm_nbits(const void *A, int a_dtype, const uint8_t *W, const uint16_t *scales_f16,

@@ -222,7 +222,10 @@ def test_qgemm_codebook4_parity(qg, case):
 # each compared with the first, the output refilled with NaN before every call
 # (hip-ep #1328, "Test plan": 129 calls, a distinct shape per process).
 REPEAT_CASES = ["tiny_u4", "phi4_qkv_M1", "phi4_lm_head_M4", "split_k_M4", "nf4_simt_M1", "nf4_simt_M4",
-                "nf4_tc_M16", "nf4_tc_M64", "prefill_gate_up", "prefill_down"]
+                "nf4_tc_M16", "nf4_tc_M64", "prefill_gate_up", "prefill_down",
+                # the tensor-pipe GEMV's 16-row tiles (down, long K), eight 16-bit activation rows,
+                # and fp32 activations at M = 64 (split-precision tensor cores)
+                "phi4_down_M1", "phi4_qkv_M8_f16", "phi4_gate_up_M64_f32"]
 
 
 def _repeat_case(qg, which):
@@ -242,6 +245,13 @@ def _repeat_case(qg, which):
         d = WL.phi4_u2("lm_head", M=4)
     elif which == "split_k_M4":
         d = _rand_nbits(17, 4, 70, 8192, 2, 64, F32, "uniform")
+    elif which == "phi4_down_M1":
+        d = WL.phi4_u2("down", M=1)
+    elif which == "phi4_qkv_M8_f16":
+        N, K = WL.PHI4_SHAPES["qkv"]
+        d = _rand_nbits(19, 8, N, K, 2, 64, F16, "tensor")
+    elif which == "phi4_gate_up_M64_f32":
+        d = WL.phi4_u2("gate_up", M=64)
     else:
         d = WL.prefill_u2(which.split("_", 1)[1])
     t = nbits_case(d)
