@@ -144,7 +144,9 @@ int run_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s) {
         return QG_OK;
     }
     const bool split = qg::split_eligible(p) && ws && aligned16(ws) && ws_bytes >= qg::split_workspace_bytes(p.M, p.K);
-    const cudaError_t e = split                                                             ? qg::split_gemm(p, ws, ws_bytes, s)
+    const bool packed = p.zp_mode == qg::ZP_PACKED;  // chosen only where the SIMT kernel takes the request
+    const cudaError_t e = packed                                                            ? qg::simt_gemm(p, ws, ws_bytes, s)
+                          : split                                                           ? qg::split_gemm(p, ws, ws_bytes, s)
                           : qg::tc_eligible(p.M, p.K, p.bits, p.a_dtype, p.bs, p.kind) ? qg::tc_gemm(p, ws, ws_bytes, s)
                           : qg::mma_gemv_eligible(p)                                   ? qg::mma_gemv(p, s)
                                                                                        : qg::simt_gemm(p, ws, ws_bytes, s);
@@ -437,7 +439,6 @@ int qgemm_nbits_packed_zp(const void *A, int a_dtype, const uint8_t *W, const ui
     // everything qgemm_nbits checks, before anything is enqueued
     const int st = check_gemm(A, a_dtype, W, scales_f16, zp16, Y, y_dtype, M, N, K, bits, block_size, gws, gws_bytes);
     if (st != QG_OK) return st;
-    if (qg::launch_unpack_zero_points(zero_points_packed, bits, N, nb, zp16, s) != cudaSuccess) return QG_ERR_CUDA;
     GemmProblem p{};
     p.A = A;
     p.a_dtype = a_dtype;
@@ -453,6 +454,17 @@ int qgemm_nbits_packed_zp(const void *A, int a_dtype, const uint8_t *W, const ui
     p.K = K;
     p.bits = bits;
     p.bs = block_size;
+    // A request the SIMT kernel takes stages the packed bytes with the codes
+    // and widens each zero point where it is used; the others (tensor-pipe
+    // GEMV, tensor cores) read an fp16 copy widened into the workspace first.
+    const bool split = qg::split_eligible(p) && aligned16(gws) && gws_bytes >= qg::split_workspace_bytes(M, K);
+    const bool simt = !split && !qg::tc_eligible(M, K, bits, a_dtype, block_size, qg::WK_NBITS) && !qg::mma_gemv_eligible(p);
+    GemmProblem q = p;
+    q.zp = nullptr;
+    q.zp_packed = zero_points_packed;
+    q.zp_mode = qg::ZP_PACKED;
+    if (simt && qg::simt_packed_zp_ok(q)) return run_gemm(q, gws, gws_bytes, s);
+    if (qg::launch_unpack_zero_points(zero_points_packed, bits, N, nb, zp16, s) != cudaSuccess) return QG_ERR_CUDA;
     return run_gemm(p, gws, gws_bytes, s);
 }
 

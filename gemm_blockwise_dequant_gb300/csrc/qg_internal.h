@@ -28,7 +28,9 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-enum ZpMode { ZP_NONE = 0, ZP_TENSOR = 1, ZP_UNIFORM = 2 };
+// ZP_PACKED: bits-wide unsigned zero points packed along each row, rows padded
+// to whole bytes (the SIMT kernel reads them as staged; no other kernel does).
+enum ZpMode { ZP_NONE = 0, ZP_TENSOR = 1, ZP_UNIFORM = 2, ZP_PACKED = 3 };
 enum WeightKind { WK_NBITS = 0, WK_CODEBOOK = 1 };
 
 // The library's per-device caches (device attributes, symbol addresses) hold
@@ -59,6 +61,7 @@ struct GemmProblem {
     int kind;                 // WeightKind
     const uint16_t *scales;   // nbits
     const uint16_t *zp;       // nbits, ZP_TENSOR
+    const uint8_t *zp_packed = nullptr;  // nbits, ZP_PACKED
     int zp_mode;
     float uniform_zp;         // ZP_UNIFORM (ZP_NONE: midpoint filled in by the caller)
     const float *codebook;    // codebook
@@ -75,6 +78,8 @@ struct GemmProblem {
 // SIMT decode path (small M).
 size_t simt_workspace_bytes(int M, int N, int K, int bits, int bs);
 cudaError_t simt_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s);
+// The SIMT kernel has a stage plan for this request with packed zero points.
+bool simt_packed_zp_ok(const GemmProblem &p);
 
 // 2-bit MatMulNBits GEMV / small-M GEMM through warp-level MMAs (M <= 4 with
 // fp32 activations, M <= 8 with 16-bit ones; block 64, K a multiple of 512).

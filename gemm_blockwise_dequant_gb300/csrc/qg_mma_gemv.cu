@@ -759,7 +759,8 @@ cudaError_t launch_mg(const MgArgs &a, const MgCfg &c, cudaStream_t s) {
 int mma_rows(int a_dtype) { return a_dtype == 0 ? 4 : 8; }
 
 bool mma_gemv_eligible(const GemmProblem &p) {
-    if (p.kind != WK_NBITS || p.bits != 2 || p.bs != 64 || p.K % kSpanCodes != 0) return false;
+    if (p.kind != WK_NBITS || p.bits != 2 || p.bs != 64 || p.K % kSpanCodes != 0 || p.zp_mode == ZP_PACKED)
+        return false;
     const int g = mma_rows(p.a_dtype);
     if (p.M < 1 || (p.M > g && p.a_dtype != 0)) return false;
     MgCfg c;

@@ -66,7 +66,9 @@ struct GemvArgs {
     const uint8_t *W;
     const unsigned char *params;  // fp16 scales (nbits) or fp32 absmax (codebook), [N][nb]
     const uint16_t *zp;           // fp16 zero points [N][nb] (ZP_TENSOR)
+    const uint8_t *zpk;           // bits-wide zero points packed per row, rows padded to bytes (ZP_PACKED)
     int zp_mode;
+    int zrow;                     // staged zero-point bytes per row: nb * 2, ceil(nb * bits / 8), or 0
     float zpv;  // zero point for ZP_UNIFORM / ZP_NONE
     const float *codebook;
     void *Y;
@@ -209,16 +211,18 @@ __device__ __forceinline__ void dot_word_codebook(uint32_t x, const float (&ap)[
 
 // One tile's dot products for one lane: ITER rows (stride `row_stride` in the
 // stage) times this lane's KPL codes, scaled per block; racc[i * MT + m] gets
-// row i, activation row m.  ZPT: a zero point per block and row (else the
-// scalar zero point folded into zah).  The lane's power-of-two activation
+// row i, activation row m.  ZPM: 1 a zero point per block and row in fp16,
+// 2 the same packed as BITS-wide integers (zsh: the bit of the lane's first
+// block in the byte zpp points at), 0 the scalar zero point folded into zah.  The lane's power-of-two activation
 // scale e2 is folded into the constants: c23 = 2^23 e2c, ahat and zah are
 // pre-multiplied by e2c = min(e2, 2^104) (exact scalings, and 2^23 e2c stays
 // finite), so no multiply per row remains; in the rare case that a lane of
 // the warp has e2 > 2^104 (activations of 2^105 or more) the remaining power
 // of two `post` is applied to the row sums once per tile.
-template <bool ZPT, int BITS, int VEC, int MT, int BPL, int WK, int ITER, int KPL = kpl_of(VEC, BITS)>
+template <int ZPM, int BITS, int VEC, int MT, int BPL, int WK, int ITER, int KPL = kpl_of(VEC, BITS)>
 __device__ __forceinline__ void tile_dot(const unsigned char *wp, const unsigned char *sp, const unsigned char *zpp,
-                                         int row_stride, int prow_stride, int zrow_stride, const float (&ap)[MT][KPL],
+                                         int zsh, int row_stride, int prow_stride, int zrow_stride,
+                                         const float (&ap)[MT][KPL],
                                          const float (&c23)[MT], const float (&ahat)[MT][BPL],
                                          const float (&zah)[MT][BPL], const float *lut_lane, float (&racc)[ITER * MT],
                                          const float (&post)[MT], bool need_post) {
@@ -255,8 +259,16 @@ __device__ __forceinline__ void tile_dot(const unsigned char *wp, const unsigned
             }
             if constexpr (WK == WK_NBITS) {
                 const float s = h2f(*reinterpret_cast<const uint16_t *>(sp + b * 2));
-                if constexpr (ZPT) {
-                    const float z = h2f(*reinterpret_cast<const uint16_t *>(zpp + b * 2));
+                if constexpr (ZPM != 0) {
+                    float z;
+                    if constexpr (ZPM == 1) {
+                        z = h2f(*reinterpret_cast<const uint16_t *>(zpp + b * 2));
+                    } else {  // the block's BITS-wide field; only 3-bit fields cross a byte
+                        const int bit = zsh + b * BITS, by = bit >> 3, sh = bit & 7;
+                        uint32_t v = zpp[by];
+                        if (BITS == 3 && sh > 5) v |= static_cast<uint32_t>(zpp[by + 1]) << 8;
+                        z = static_cast<float>((v >> sh) & ((1u << BITS) - 1u));
+                    }
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
                         const float P = (acc0[m].x + acc0[m].y) + (acc1[m].x + acc1[m].y);
@@ -450,10 +462,15 @@ __device__ __forceinline__ void fill_stage_general(const GemvArgs &p, unsigned c
         copy_tail_lanes(st + p.s_off, src, rows * prow, cp, lane);
         tx += cp.bulk_bytes;
     }
-    if (p.zp_mode == ZP_TENSOR) {
-        const unsigned char *src = Zb + static_cast<size_t>(r0) * p.nb * 2;
-        const CopyPlan cp = copy_plan(st + p.z_off, src, rows * p.nb * 2);
-        copy_tail_lanes(st + p.z_off, src, rows * p.nb * 2, cp, lane);
+    if (p.zrow) {
+        const unsigned char *src = Zb + static_cast<size_t>(r0) * p.zrow;
+        const uint32_t zb = rows * p.zrow;
+        const CopyPlan cp = copy_plan(st + p.z_off, src, zb);
+        if (p.zp_mode == ZP_PACKED) {  // any byte count, any alignment: byte by byte past the bulk prefix
+            for (uint32_t i = cp.bulk_bytes + lane; i < zb; i += 32) st[p.z_off + i] = __ldg(src + i);
+        } else {
+            copy_tail_lanes(st + p.z_off, src, zb, cp, lane);
+        }
         tx += cp.bulk_bytes;
     }
     __syncwarp();
@@ -479,9 +496,9 @@ __device__ __forceinline__ void fill_stage_general(const GemvArgs &p, unsigned c
         const CopyPlan cp = copy_plan(st + p.s_off, src, rows * prow);
         if (cp.bulk_bytes) bulk_g2s(st + p.s_off, src, cp.bulk_bytes, fullb);
     }
-    if (lane == 2 && p.zp_mode == ZP_TENSOR) {
-        const unsigned char *src = Zb + static_cast<size_t>(r0) * p.nb * 2;
-        const CopyPlan cp = copy_plan(st + p.z_off, src, rows * p.nb * 2);
+    if (lane == 2 && p.zrow) {
+        const unsigned char *src = Zb + static_cast<size_t>(r0) * p.zrow;
+        const CopyPlan cp = copy_plan(st + p.z_off, src, rows * p.zrow);
         if (cp.bulk_bytes) bulk_g2s(st + p.z_off, src, cp.bulk_bytes, fullb);
     }
 }
@@ -618,15 +635,16 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
             const int es = valid ? e : 0;
             const unsigned char *Wb = p.W + es * p.w_slot_stride;
             const unsigned char *Pb = p.params + es * p.p_slot_stride;
-            const unsigned char *Zb = reinterpret_cast<const unsigned char *>(p.zp) + es * p.z_slot_stride;
+            const unsigned char *Zb =
+                (p.zp_mode == ZP_PACKED ? p.zpk : reinterpret_cast<const unsigned char *>(p.zp)) + es * p.z_slot_stride;
             unsigned char *st = stages + static_cast<size_t>(slot) * p.stage_bytes;
             if (p.fast_tx && rows == p.SR && !split) {  // warp-uniform: a whole stage, every copy 16-byte aligned
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&full[slot], p.fast_tx);
                     bulk_g2s(st, Wb + static_cast<size_t>(r0) * p.row_bytes, p.SR * p.row_bytes, &full[slot]);
                     bulk_g2s(st + p.s_off, Pb + static_cast<size_t>(r0) * prow, p.SR * prow, &full[slot]);
-                    if (p.zp_mode == ZP_TENSOR)
-                        bulk_g2s(st + p.z_off, Zb + static_cast<size_t>(r0) * p.nb * 2, p.SR * p.nb * 2, &full[slot]);
+                    if (p.zrow)
+                        bulk_g2s(st + p.z_off, Zb + static_cast<size_t>(r0) * p.zrow, p.SR * p.zrow, &full[slot]);
                 }
             } else {
                 fill_stage_general<LPR, VEC, BITS>(p, st, Wb, Pb, Zb, r0, rows, split, kb0, kb1, prow, &full[slot], lane);
@@ -671,7 +689,8 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     const float *lut_lane = lut + lane;
     const int row_stride = H * p.w_pitch;           // stage bytes between a lane's successive rows
     const int prow_stride = H * p.nb * PB;          // same for the block parameters
-    const int zrow_stride = H * p.nb * 2;
+    const int zrow_stride = H * p.zrow;
+    const int zbit0 = blk0 * BITS;  // ZP_PACKED: bit of the lane's first block in its row
     constexpr int VPW = RV * H;  // reduced values per warp and tile
     const bool writer = (gl & (LPR / RV - 1)) == 0;
     const int red_idx = sigma * VPW + half * RV + gl / (LPR / RV);
@@ -756,13 +775,18 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
         if (ok && valid) {  // warp-uniform
             const unsigned char *wp = st + half * p.w_pitch + lane_boff;  // this lane's first row is `half`
             const unsigned char *sp = st + p.s_off + (half * p.nb + blk0) * PB;
-            const unsigned char *zpp = st + p.z_off + (half * p.nb + blk0) * 2;
+            const unsigned char *zrw = st + p.z_off + half * p.zrow;  // the lane's first row of zero points
             if (WK == WK_NBITS && p.zp_mode == ZP_TENSOR)
-                tile_dot<true, BITS, VEC, MT, BPL, WK, ITER>(wp, sp, zpp, row_stride, prow_stride, zrow_stride, ap, c23,
-                                                            ahat, zah, lut_lane, racc, post, need_post);
+                tile_dot<1, BITS, VEC, MT, BPL, WK, ITER>(wp, sp, zrw + blk0 * 2, 0, row_stride, prow_stride,
+                                                         zrow_stride, ap, c23, ahat, zah, lut_lane, racc, post,
+                                                         need_post);
+            else if (WK == WK_NBITS && AM == A_ROWS && p.zp_mode == ZP_PACKED)
+                tile_dot<2, BITS, VEC, MT, BPL, WK, ITER>(wp, sp, zrw + (zbit0 >> 3), zbit0 & 7, row_stride,
+                                                         prow_stride, zrow_stride, ap, c23, ahat, zah, lut_lane, racc,
+                                                         post, need_post);
             else
-                tile_dot<false, BITS, VEC, MT, BPL, WK, ITER>(wp, sp, zpp, row_stride, prow_stride, zrow_stride, ap, c23,
-                                                             ahat, zah, lut_lane, racc, post, need_post);
+                tile_dot<0, BITS, VEC, MT, BPL, WK, ITER>(wp, sp, zrw, 0, row_stride, prow_stride, zrow_stride, ap,
+                                                         c23, ahat, zah, lut_lane, racc, post, need_post);
 #pragma unroll
             for (int v = 0; v < RV; ++v) racc[v] = lane_active ? racc[v] : 0.f;
         }
@@ -829,7 +853,8 @@ inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
 // per useful code: idle lanes of the last K-slice, the per-row bookkeeping
 // (about 12 instructions per lane and row) and, for layouts needing more
 // slices than fit in one CTA, a split-K penalty.
-bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, Cfg &c, int bias_bytes = 0) {
+// zrow: bytes of zero points staged per row (0: none).
+bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zrow, Cfg &c, int bias_bytes = 0) {
     const DeviceInfo &di = device_info();
     c.mt = M <= 1 ? 1 : (M <= 2 ? 2 : 4);
     if (bits == 3) c.mt = std::min(c.mt, 2);  // u3 groups of 32 codes: at most 2 activation rows in registers
@@ -898,7 +923,7 @@ bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zp_tensor, 
     const int budget = di.max_smem_optin - c.stage_off;
     c.s_off = round_up(c.SR * c.w_pitch, 128);
     c.z_off = c.s_off + round_up(c.SR * nb * pb, 128);
-    c.stage_bytes = c.z_off + (zp_tensor ? round_up(c.SR * nb * 2, 128) : 0);
+    c.stage_bytes = c.z_off + (zrow ? round_up(c.SR * zrow, 128) : 0);
     // each stage also has a reduction slot: S_cta slices x iter x MT x H sums
     const int red_slot = c.S_cta * c.iter * c.mt * (32 / c.lpr) * 4;
     const int nfit = std::min(kMaxStages, budget / (c.stage_bytes + 2 * red_slot));
@@ -1021,7 +1046,8 @@ int fast_stage_tx(const GemvArgs &a, const Cfg &c, int pb) {
     if (c.splits > 1) return 0;
     const long long code = static_cast<long long>(c.SR) * a.row_bytes;
     const long long par = static_cast<long long>(c.SR) * a.nb * pb;
-    const long long zp = a.zp_mode == ZP_TENSOR ? static_cast<long long>(c.SR) * a.nb * 2 : 0;
+    const long long zp = static_cast<long long>(c.SR) * a.zrow;
+    if (a.zp_mode == ZP_PACKED && (reinterpret_cast<uintptr_t>(a.zpk) & 15u)) return 0;
     if (code % 16 || par % 16 || zp % 16) return 0;
     if (a.ids && (a.w_slot_stride % 16 || a.p_slot_stride % 16 || a.z_slot_stride % 16)) return 0;
     return static_cast<int>(code + par + zp);
@@ -1051,13 +1077,26 @@ size_t simt_workspace_bytes(int M, int N, int K, int bits, int bs) {
     Cfg c;
     if (M <= 0 || N <= 0 || K <= 0) return 0;
     // the zero-point mode and the weight kind do not change the split count
-    if (!choose_cfg(M, N, K, bits, bs, WK_NBITS, 1, c)) return 0;
+    if (!choose_cfg(M, N, K, bits, bs, WK_NBITS, (K / bs) * 2, c)) return 0;
     return c.splits > 1 ? static_cast<size_t>(c.splits) * M * N * sizeof(float) : 0;
+}
+
+// Staged zero-point bytes per weight row of a request.
+static int zp_row_bytes(const GemmProblem &p) {
+    const int nb = p.K / p.bs;
+    return p.zp_mode == ZP_TENSOR ? nb * 2 : (p.zp_mode == ZP_PACKED ? (nb * p.bits + 7) / 8 : 0);
+}
+
+bool simt_packed_zp_ok(const GemmProblem &p) {
+    Cfg c;
+    return p.kind == WK_NBITS && p.zp_mode == ZP_PACKED && p.zp_packed &&
+           choose_cfg(p.M, p.N, p.K, p.bits, p.bs, p.kind, zp_row_bytes(p), c);
 }
 
 cudaError_t simt_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_t s) {
     Cfg c;
-    if (!choose_cfg(p.M, p.N, p.K, p.bits, p.bs, p.kind, p.zp_mode == ZP_TENSOR, c)) return cudaErrorNotSupported;
+    if (p.zp_mode == ZP_PACKED && (p.kind != WK_NBITS || !p.zp_packed)) return cudaErrorNotSupported;
+    if (!choose_cfg(p.M, p.N, p.K, p.bits, p.bs, p.kind, zp_row_bytes(p), c)) return cudaErrorNotSupported;
     GemvArgs a{};
     a.A = p.A;
     a.a_dtype = p.a_dtype;
@@ -1065,7 +1104,9 @@ cudaError_t simt_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStrea
     a.params = p.kind == WK_CODEBOOK ? reinterpret_cast<const unsigned char *>(p.absmax)
                                      : reinterpret_cast<const unsigned char *>(p.scales);
     a.zp = p.zp;
+    a.zpk = p.zp_packed;
     a.zp_mode = p.zp_mode;
+    a.zrow = zp_row_bytes(p);
     a.zpv = p.uniform_zp;
     a.codebook = p.codebook;
     a.Y = p.Y;
@@ -1126,7 +1167,7 @@ cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s) {
         // the expert's bias row is staged in shared memory when it is small enough
         const uint16_t *bias = fc1 ? q.fc1_bias : q.fc2_bias;
         const int bias_bytes = bias && N <= 16384 ? (N * 2 + 15) / 16 * 16 : 0;
-        if (!choose_cfg(1, N, K, q.bits, q.bs, WK_NBITS, zp != nullptr, c, bias_bytes) || c.splits != 1)
+        if (!choose_cfg(1, N, K, q.bits, q.bs, WK_NBITS, zp ? (K / q.bs) * 2 : 0, c, bias_bytes) || c.splits != 1)
             return cudaErrorNotSupported;
         GemvArgs a{};
         a.A = q.x;
@@ -1135,6 +1176,7 @@ cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s) {
         a.params = reinterpret_cast<const unsigned char *>(fc1 ? q.fc1_scales : q.fc2_scales);
         a.zp = zp;
         a.zp_mode = zp ? ZP_TENSOR : ZP_NONE;
+        a.zrow = zp ? (K / q.bs) * 2 : 0;
         a.zpv = static_cast<float>(mid);
         a.M = 1;
         a.N = N;

@@ -1106,7 +1106,7 @@ size_t split_workspace_bytes(int M, int K) {
 }
 
 bool split_eligible(const GemmProblem &p) {
-    return p.a_dtype == 0 && p.y_dtype == 0 && p.kind == WK_NBITS && p.M >= kSplitMinRows &&
+    return p.a_dtype == 0 && p.y_dtype == 0 && p.kind == WK_NBITS && p.zp_mode != ZP_PACKED && p.M >= kSplitMinRows &&
            tc_eligible(p.M, p.K, p.bits, 1, p.bs, p.kind);
 }
 

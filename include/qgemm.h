@@ -313,13 +313,15 @@ size_t qgemm_codebook4_nested_workspace_bytes(int a_dtype, int M, int N, int K, 
  *
  *   zero_points_packed  [N][ceil((K/block_size)*bits/8)] uint8 (device, any
  *                alignment; NULL: QG_ERR_INVALID_ARG)
- *   Other arguments as qgemm_nbits.  The zero points are widened to fp16
- *   [N][K/block_size] at the front of the workspace (at least
- *   qgemm_nbits_packed_zp_workspace_bytes() bytes, 16-byte aligned) by one
- *   small kernel, then the call runs exactly as qgemm_nbits with that
- *   zero-point tensor: the result is bit-identical to qgemm_nbits given the
- *   same integers as fp16.  Every check of qgemm_nbits happens before
- *   anything is enqueued.
+ *   Other arguments as qgemm_nbits; the workspace holds at least
+ *   qgemm_nbits_packed_zp_workspace_bytes() bytes, 16-byte aligned.  A request
+ *   that qgemm_nbits would serve with its SIMT GEMV kernel stages the packed
+ *   bytes beside the codes and widens each field where it is used; any other
+ *   (2-bit block-64 tensor-pipe GEMV, tensor cores) first widens the zero
+ *   points to fp16 [N][K/block_size] at the front of the workspace with one
+ *   small kernel.  Either way the result is bit-identical to qgemm_nbits
+ *   given the same integers as fp16 zero points.  Every check of qgemm_nbits
+ *   happens before anything is enqueued.
  */
 int qgemm_nbits_packed_zp(const void *A, int a_dtype, const uint8_t *W, const uint16_t *scales_f16,
                           const uint8_t *zero_points_packed, void *Y, int y_dtype, int M, int N, int K, int bits,

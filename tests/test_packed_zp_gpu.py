@@ -116,3 +116,56 @@ def test_packed_zp_refusals(qg):
     small = t.zeros(16, dtype=t.uint8, device="cuda")
     assert f(ws=small) == qg.QG_ERR_WORKSPACE_TOO_SMALL
     t.cuda.synchronize()
+
+
+@pytest.mark.parametrize("bits,bs,K", [(4, 32, 17920), (3, 32, 8960), (2, 128, 17920), (8, 64, 4096)])
+def test_packed_zp_long_rows(qg, bits, bs, K):
+    """Rows long enough that the SIMT kernel splits K across CTAs: each slice
+    reads its blocks' fields out of the whole staged row of packed bytes."""
+    d = WL.packed_zp(96, K, M=1, bits=bits, block_size=bs, a_dtype=0, seed=K + bits)
+    Y = _run(qg, d)
+    assert O.max_rel_l2(to64(Y), _oracle(d)) <= 1e-4
+
+
+@pytest.mark.parametrize("bits,bs,M,N,K,widened", [
+    (4, 32, 1, 640, 1024, False),   # SIMT kernel: packed bytes staged with the codes
+    (3, 32, 2, 333, 224, False),
+    (8, 128, 4, 256, 2048, False),
+    (2, 64, 1, 640, 1024, True),    # tensor-pipe GEMV: an fp16 copy first
+    (4, 32, 16, 256, 1024, True),   # tensor cores (16-bit activations)
+])
+def test_packed_zp_widened_copy_only_off_simt(qg, bits, bs, M, N, K, widened):
+    """The fp16 copy of the zero points (the workspace's first N * nb * 2
+    bytes) is written only for requests that another kernel than the SIMT
+    one takes; a SIMT request leaves those bytes as they were."""
+    t = torch()
+    a_dtype = 1 if M >= 16 else 0
+    d = WL.packed_zp(N, K, M=M, bits=bits, block_size=bs, a_dtype=a_dtype, seed=N + K + bits)
+    A, W, S, Z = _dev(d)
+    nbytes = qg.qgemm_nbits_packed_zp_workspace_bytes(a_dtype, M, N, K, bits, bs)
+    ws = t.full((nbytes,), 0xA5, dtype=t.uint8, device="cuda")
+    Y = y_tensor(M, N, a_dtype)
+    qg.qgemm_nbits_packed_zp(A, W, S, Z, Y, bits=bits, block_size=bs, workspace=ws)
+    t.cuda.synchronize()
+    expanded = N * (K // bs) * 2
+    untouched = bool((ws[:expanded] == 0xA5).all().item())
+    assert untouched != widened
+    tol = 1e-4 if a_dtype == 0 else 5e-3
+    assert O.max_rel_l2(to64(Y), _oracle(d)) <= tol
+
+
+@pytest.mark.parametrize("bits,nb_rows", [(4, 32), (3, 7)])
+def test_packed_zp_unaligned_pointer(qg, bits, nb_rows):
+    """Packed zero points at an odd address (any byte offset is allowed): the
+    SIMT kernel copies them byte by byte instead of with bulk copies."""
+    t = torch()
+    K = 32 * nb_rows
+    d = WL.packed_zp(203, K, M=1, bits=bits, block_size=32, a_dtype=0, seed=77 + bits)
+    A, W, S, Z = _dev(d)
+    buf = t.zeros(Z.numel() + 1, dtype=t.uint8, device="cuda")
+    buf[1:] = Z.flatten()
+    Zodd = buf[1:].view(Z.shape)
+    Y = y_tensor(1, d["N"], 0)
+    qg.qgemm_nbits_packed_zp(A, W, S, Zodd, Y, bits=bits, block_size=32)
+    t.cuda.synchronize()
+    assert O.max_rel_l2(to64(Y), _oracle(d)) <= 1e-4
