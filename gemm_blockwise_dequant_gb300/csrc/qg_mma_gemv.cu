@@ -38,6 +38,7 @@
 //  * Every wait is bounded (qg_device.cuh).
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 
 #include "qg_device.cuh"
 #include "qg_internal.h"
@@ -290,22 +291,32 @@ __global__ void __maxnreg__(kMaxRegs)
     pdl_launch_dependents();
     pdl_wait();
 
-    // A tile is TROWS weight rows (TR 16-row MMA row tiles).  Fill f of this CTA
-    // holds rows FR (f % 2) .. + FR - 1 of its tile f / 2 -- whole rows: their
-    // codes are one contiguous run of HBM, copied by ONE bulk copy, and (TR = 2)
-    // their block parameters by one more (a copy instruction costs the TMA
-    // engine a fixed time, so few large copies keep HBM busy).
-    const int ntl = (p.ntiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                    static_cast<int>(gridDim.x);  // tiles of this CTA
+    // A tile is two fills of FR weight rows (TR 16-row MMA row tiles); fill f of
+    // this CTA is fill f % 2 of its tile f / 2 -- whole rows: their codes are one
+    // contiguous run of HBM, copied by ONE bulk copy, and (TR = 2) their block
+    // parameters by one more (a copy instruction costs the TMA engine a fixed
+    // time, so few large copies keep HBM busy).  Whole rounds of 2 G fills go
+    // out by tile, round-robin (tile b + i G: rows (b + i G) TROWS ..); the
+    // fills left over (fewer than 2 G) are dealt one per CTA, then a second
+    // per CTA, so no CTA takes more than one fill beyond another.  A CTA's last
+    // tile may hold one fill: its second fill's rows lie at or past N.
+    const int G = static_cast<int>(gridDim.x), bx = static_cast<int>(blockIdx.x);
+    const int nfills = (p.N + FR - 1) / FR;
+    const int rounds = nfills / (2 * G);
+    const int rem = nfills - 2 * G * rounds;
+    const int ntl = rounds + (bx < rem ? 1 : 0);  // tiles of this CTA
     const int total = 2 * ntl;                    // fills of this CTA
+    auto fill_row0 = [&](int i, int h) -> int {   // first row of fill h of this CTA's tile i
+        return (i < rounds ? (bx + i * G) * 2 + h : 2 * G * rounds + bx + h * G) * FR;
+    };
     if (warp == W) {
         // ------------------------------------------------------------ producer
         auto finish = [&](int tl, int rslot) {  // add the warps' sums of tile tl of this CTA, write Y
-            const int tile = blockIdx.x + tl * gridDim.x;
+            const int rb0 = fill_row0(tl, 0), rb1 = fill_row0(tl, 1);
             const float *r = red + (rslot >> 1) * (W * TROWS * MP * SL);
             for (int v = lane; v < TROWS * MP; v += 32) {
                 const int row = v / MP, m = v - row * MP;
-                const int n = tile * TROWS + row;
+                const int n = (row < FR ? rb0 : rb1 - FR) + row;
                 if (m >= p.M || n >= p.N) continue;
                 float s = 0.f;
                 for (int w = 0; w < W; ++w) {  // warp (span) order, then lane order
@@ -348,8 +359,7 @@ __global__ void __maxnreg__(kMaxRegs)
                 __syncwarp();
             }
             if (lane == 0) {
-                const int tile = blockIdx.x + (f >> 1) * gridDim.x;
-                const int row0 = tile * TROWS + FR * (f & 1);
+                const int row0 = fill_row0(f >> 1, f & 1);
                 const int valid = max(0, min(FR, p.N - row0));
                 unsigned char *st = stages + static_cast<size_t>(slot) * p.stage_bytes;
                 const uint32_t cb = valid * p.row_bytes, pb = PSMEM ? valid * p.nb * 2 : 0;
@@ -461,17 +471,17 @@ __global__ void __maxnreg__(kMaxRegs)
     // 16-byte run per row -- into one of its two buffers while it works on the
     // current item (lanes 0-15 the scales, 16-31 the zero points)
     unsigned char *pq = smem + p.pq_off + sl * kPqBytes * (ZPT ? 2 : 1);
-    auto fetch_params = [&](int row0, int spn, int buf) {
+    auto fetch_params = [&](int tl, int spn, int buf) {  // tile tl's rows: FR of each fill
         const int rr = lane & 15;
         if (ZPT || lane < 16) {
-            const int n = min(row0 + rr, p.N - 1);  // rows past N: any row
+            const int n = min(fill_row0(tl, rr / FR) + rr % FR, p.N - 1);  // rows past N: any row
             const uint16_t *src = (lane < 16 ? p.scales : p.zp) + static_cast<size_t>(n) * p.nb + spn * 8;
             cp_async16(pq + (buf * (ZPT ? 2 : 1) + (lane >> 4)) * (kPqBytes / 2) + rr * 16, src);
         }
         cp_async_commit();
     };
     int pqb = 0;
-    if (!PSMEM && ntl > 0) fetch_params(blockIdx.x * TROWS, sl, 0);
+    if (!PSMEM && ntl > 0) fetch_params(0, sl, 0);
     int sa_ = 0, sb_ = 1 % p.NST;
     uint32_t pa = 0, pbp = p.NST == 1 ? 1u : 0u;
     for (int i = 0; i < ntl; ++i) {
@@ -482,10 +492,16 @@ __global__ void __maxnreg__(kMaxRegs)
         float acc[2 * TR][2];
 #pragma unroll
         for (int r = 0; r < 2 * TR; ++r) acc[r][0] = acc[r][1] = 0.f;
-        const int tile_row0 = (blockIdx.x + i * gridDim.x) * TROWS;
-        if (ok) {
+        // a tile whose second fill is empty: TR = 2 skips that fill's MMA row tile;
+        // TR = 1 (one MMA row tile over both fills) reads the first fill twice
+        const bool two = i < rounds || bx + G < rem;  // (fill_row0(i, 1) < N)
+        // the tile body, compiled twice: TWO = false is a TR = 2 tile whose second
+        // fill is empty (no loads, MMAs or epilogue for it); one straight-line body
+        // each, so no branch splits the unrolled MMA sequence
+        auto tile_body = [&](auto two_c) {
+            constexpr bool TWO = decltype(two_c)::value;
             const unsigned char *sta = stages + static_cast<size_t>(sa_) * p.stage_bytes;  // the tile's first fill
-            const unsigned char *stb = stages + static_cast<size_t>(sb_) * p.stage_bytes;  // its second fill
+            const unsigned char *stb = stages + static_cast<size_t>((TR == 1 && !two) ? sa_ : sb_) * p.stage_bytes;
             const uint16_t *psa = reinterpret_cast<const uint16_t *>(sta + p.par_off);
             const uint16_t *psb = reinterpret_cast<const uint16_t *>(stb + p.par_off);
             const uint16_t *zsa = reinterpret_cast<const uint16_t *>(sta + p.zp_off);
@@ -497,6 +513,8 @@ __global__ void __maxnreg__(kMaxRegs)
                 const unsigned char *span_b = bfrag_w + static_cast<size_t>(sp) * 1024 * MNT + slot_b * 16;
                 const unsigned char *bb0 = nz0 ? span_b : zero_slab;
                 const unsigned char *bb1 = nz1 ? span_b : zero_slab;
+                (void)bb0;
+                (void)bb1;
                 if (BREG && !one_span) load_breg(sp);
                 const int pb = sp * 8;  // first block of the span
                 float accs[2 * TR][2];
@@ -506,13 +524,14 @@ __global__ void __maxnreg__(kMaxRegs)
                 // copies; the warp barrier shows them to every lane and ends every
                 // lane's reads of the other buffer); start the next item's copy
                 const uint16_t *pqs = reinterpret_cast<const uint16_t *>(pq + pqb * (ZPT ? 2 : 1) * (kPqBytes / 2));
+                (void)pqs;
                 if constexpr (!PSMEM) {
                     cp_async_wait_all();
                     __syncwarp();
                     if (sp + W < p.spans)
-                        fetch_params(tile_row0, sp + W, pqb ^ 1);
+                        fetch_params(i, sp + W, pqb ^ 1);
                     else if (i + 1 < ntl)
-                        fetch_params(tile_row0 + static_cast<int>(gridDim.x) * TROWS, sl, pqb ^ 1);
+                        fetch_params(i + 1, sl, pqb ^ 1);
                 }
 #pragma unroll
                 for (int j = 0; j < MNT; ++j) {
@@ -523,6 +542,11 @@ __global__ void __maxnreg__(kMaxRegs)
                     uint32_t xw[2 * TR][BPG];
 #pragma unroll
                     for (int rr = 0; rr < 2 * TR; ++rr) {
+                        if (TR == 2 && rr >= 2 && !TWO) {  // the empty second fill: no loads
+#pragma unroll
+                            for (int w = 0; w < BPG; ++w) xw[rr][w] = 0u;
+                            continue;
+                        }
                         const unsigned char *base = (rr / TR ? cb : ca) + (rr % TR) * r8;
                         if constexpr (BPG == 8) {
 #pragma unroll
@@ -556,6 +580,7 @@ __global__ void __maxnreg__(kMaxRegs)
                         }
 #pragma unroll
                         for (int t = 0; t < TR; ++t) {
+                            if (TR == 2 && t == 1 && !TWO) continue;
                             const uint32_t x0 = xw[2 * t][w], x1 = xw[2 * t + 1][w];
                             const uint32_t t0 = x0 >> 8, t1 = x1 >> 8;
                             uint32_t u0[8], u1[8];
@@ -577,6 +602,7 @@ __global__ void __maxnreg__(kMaxRegs)
                     // times (sum a' q - zp sum a'), both sums carrying 2^-24
 #pragma unroll
                     for (int t = 0; t < TR; ++t) {
+                        if (TR == 2 && t == 1 && !TWO) continue;
                         const float D0 = d[t][0], D1 = d[t][1], D2 = d[t][2], D3 = d[t][3];
                         // rows rr = 2t and 2t + 1: fill rr / TR, row g + 8 (rr % TR) of it
                         const uint16_t *ps0 = ((2 * t) / TR ? psb : psa) + (g + 8 * ((2 * t) % TR)) * pw;
@@ -616,6 +642,10 @@ __global__ void __maxnreg__(kMaxRegs)
                 }
                 pqb ^= 1;
             }
+        };
+        if (ok) {
+            if (TR == 1 || two) tile_body(std::true_type{});
+            else tile_body(std::false_type{});
         }
         // this warp's span sums of the tile's rows, for the producer (in the
         // reduction slot of the tile's second fill): every lane of a row quad
