@@ -39,7 +39,7 @@ constexpr int kRCons = 16;
 constexpr int kRGroups = 4;
 constexpr int kRGWarps = kRCons / kRGroups;
 constexpr int kRRows = 8;
-static_assert(kRRows == 2 * kRGWarps, "two rows per consumer warp and stage");
+constexpr int kRPW = kRRows / kRGWarps;  // rows per consumer warp and stage
 constexpr int kRThreads = (kRCons + 1) * 32;
 constexpr int kRRegs = 96;
 static_assert((kRCons + 1 + 3) / 4 * 32 * kRRegs <= 16384, "registers of one SM sub-partition");
@@ -400,37 +400,37 @@ __global__ void __maxnreg__(kRRegs) dp4a_ring_kernel(Dp4aGemv p) {
     const int grp = warp / kRGWarps, wg = warp % kRGWarps;
     int st_i = grp;
     uint32_t par = 0;
-    float bias_l[2] = {0.f, 0.f};  // lane l: the biases of this warp's rows in its stage 32 q + l
+    float bias_l[kRPW] = {};  // lane l: the biases of this warp's rows in its stage 32 q + l
     for (int sgi = grp, q = 0; sgi < nst; sgi += kRGroups, ++q) {
         if ((q & 31) == 0 && p.bias) {  // a row load per stage would stall the warp
             const int sl = sgi + kRGroups * lane;
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                const int rb = r_lo + sl * kRRows + 2 * wg + rr;
+            for (int rr = 0; rr < kRPW; ++rr) {
+                const int rb = r_lo + sl * kRRows + kRPW * wg + rr;
                 bias_l[rr] = sl < nst && rb < r_hi ? h2f(__ldg(p.bias + static_cast<size_t>(e) * p.N + rb)) : 0.f;
             }
         }
-        float bias_r[2];
+        float bias_r[kRPW];
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) bias_r[rr] = __shfl_sync(0xffffffffu, bias_l[rr], q & 31);
+        for (int rr = 0; rr < kRPW; ++rr) bias_r[rr] = __shfl_sync(0xffffffffu, bias_l[rr], q & 31);
         const bool ok = mbar_wait(&full[st_i], par, abort_flag, p.fault, FAULT_WAIT_FULL);
-        const int r0 = r_lo + sgi * kRRows + 2 * wg;
+        const int r0 = r_lo + sgi * kRRows + kRPW * wg;
         if (ok && r0 < r_hi) {  // warp-uniform; a second row past r_hi is computed and dropped
             const unsigned char *st = stages + static_cast<size_t>(st_i) * p.stage_bytes;
-            const unsigned char *rowp = st + 2 * wg * row_bytes;
-            const uint16_t *srow = reinterpret_cast<const uint16_t *>(st + p.par_off) + 2 * wg * nb;
-            const uint16_t *zrow = reinterpret_cast<const uint16_t *>(st + p.zp_off) + 2 * wg * nb;
-            float part[2] = {0.f, 0.f};
+            const unsigned char *rowp = st + kRPW * wg * row_bytes;
+            const uint16_t *srow = reinterpret_cast<const uint16_t *>(st + p.par_off) + kRPW * wg * nb;
+            const uint16_t *zrow = reinterpret_cast<const uint16_t *>(st + p.zp_off) + kRPW * wg * nb;
+            float part[kRPW] = {};
             for (int ub = 0; ub < units; ub += 32 * UR) {
-                uint32_t cw[2][UR][WPU];
-                uint16_t sb[2][UR][SPU], zb[2][UR][SPU];
+                uint32_t cw[kRPW][UR][WPU];
+                uint16_t sb[kRPW][UR][SPU], zb[kRPW][UR][SPU];
 #pragma unroll
                 for (int i = 0; i < UR; ++i) {
                     const int u = ub + lane + 32 * i;
                     if (u >= units) continue;
                     if constexpr (UPL == 0) load_unit_consts(i, u);
 #pragma unroll
-                    for (int rr = 0; rr < 2; ++rr) {
+                    for (int rr = 0; rr < kRPW; ++rr) {
                         const uint4 t = *reinterpret_cast<const uint4 *>(rowp + rr * row_bytes + u * VEC);
                         cw[rr][i][0] = t.x;
                         cw[rr][i][1] = t.y;
@@ -447,7 +447,7 @@ __global__ void __maxnreg__(kRRegs) dp4a_ring_kernel(Dp4aGemv p) {
                 for (int i = 0; i < UR; ++i) {
                     if (ub + lane + 32 * i >= units) continue;
 #pragma unroll
-                    for (int rr = 0; rr < 2; ++rr) {
+                    for (int rr = 0; rr < kRPW; ++rr) {
 #pragma unroll
                         for (int g = 0; g < SPU; ++g) {
                             int acc = 0;
@@ -462,13 +462,13 @@ __global__ void __maxnreg__(kRRegs) dp4a_ring_kernel(Dp4aGemv p) {
                 }
             }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                part[0] += __shfl_xor_sync(0xffffffffu, part[0], off);
-                part[1] += __shfl_xor_sync(0xffffffffu, part[1], off);
-            }
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                for (int rr = 0; rr < kRPW; ++rr) part[rr] += __shfl_xor_sync(0xffffffffu, part[rr], off);
             if (lane == 0) {
-                p.out[static_cast<size_t>(slot) * p.N + r0] = p.bias ? part[0] + bias_r[0] : part[0];
-                if (r0 + 1 < r_hi) p.out[static_cast<size_t>(slot) * p.N + r0 + 1] = p.bias ? part[1] + bias_r[1] : part[1];
+#pragma unroll
+                for (int rr = 0; rr < kRPW; ++rr)
+                    if (r0 + rr < r_hi) p.out[static_cast<size_t>(slot) * p.N + r0 + rr] = p.bias ? part[rr] + bias_r[rr] : part[rr];
             }
         }
         __syncwarp();
