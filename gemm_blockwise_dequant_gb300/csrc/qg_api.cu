@@ -235,7 +235,10 @@ int qmoe_common(bool dp4a, const uint16_t *x_f16, const int32_t *expert_ids, con
     q.swiglu_interleaved = swiglu_interleaved;
     q.y = y_f16;
     q.status = status_dev;
-    const cudaError_t e = dp4a ? qg::qmoe_decode_dp4a(q, workspace, s) : qg::qmoe_decode(q, workspace, s);
+    // int8 activations: the SIMT kernel's dp4a kind where it has a plan, else the plain-load kernels
+    const cudaError_t e = !dp4a                         ? qg::qmoe_decode(q, workspace, s)
+                          : qg::qmoe_dp4a_simt_ok(q) ? qg::qmoe_decode(q, workspace, s, true)
+                                                     : qg::qmoe_decode_dp4a(q, workspace, s);
     if (e == cudaErrorNotSupported) return QG_ERR_UNSUPPORTED;
     return e == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }

@@ -31,7 +31,9 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // ZP_PACKED: bits-wide unsigned zero points packed along each row, rows padded
 // to whole bytes (the SIMT kernel reads them as staged; no other kernel does).
 enum ZpMode { ZP_NONE = 0, ZP_TENSOR = 1, ZP_UNIFORM = 2, ZP_PACKED = 3 };
-enum WeightKind { WK_NBITS = 0, WK_CODEBOOK = 1 };
+// WK_DP4A: MatMulNBits codes against int8 activations quantized per block
+// (the int8-activation QMoE decode).
+enum WeightKind { WK_NBITS = 0, WK_CODEBOOK = 1, WK_DP4A = 2 };
 
 // The library's per-device caches (device attributes, symbol addresses) hold
 // kMaxDevices entries.  device_slot() is the current device's index into them,
@@ -125,7 +127,9 @@ struct QmoeProblem {
     int *status;
 };
 size_t qmoe_workspace_bytes(int k, int hidden, int inter);
-cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s);
+cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s, bool dp4a = false);
+// The SIMT kernel serves this int8-activation decode (else qmoe_decode_dp4a).
+bool qmoe_dp4a_simt_ok(const QmoeProblem &q);
 // Same decode with int8 activations (dp4a); hidden and inter at most 65536.
 cudaError_t qmoe_decode_dp4a(const QmoeProblem &q, void *ws, cudaStream_t s);
 

@@ -209,6 +209,102 @@ __device__ __forceinline__ void dot_word_codebook(uint32_t x, const float (&ap)[
     }
 }
 
+// ---- int8 activations (WK_DP4A)
+__device__ __forceinline__ int dp4a_us(uint32_t codes, uint32_t acts, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(codes), "r"(acts), "r"(c));
+    return d;
+}
+
+// Activation word and byte that pair with lane-local code k: one AND of a u4
+// code word yields its codes 0, 2, 4, 6 (then 1, 3, 5, 7 after a 4-bit
+// shift); one of a u2 word its codes t, t + 4, t + 8, t + 12 after a 2t shift.
+template <int BITS>
+__host__ __device__ constexpr int dp4a_word(int k) {
+    return BITS == 4 ? 2 * (k / 8) + (k % 8) % 2 : 4 * (k / 16) + (k % 16) % 4;
+}
+template <int BITS>
+__host__ __device__ constexpr int dp4a_byte(int k) {
+    return BITS == 4 ? (k % 8) / 2 : (k % 16) / 4;
+}
+
+// acc += dot of the codes of word x with their int8 activations a[0 ..]
+template <int BITS>
+__device__ __forceinline__ int dot_word_dp4a(uint32_t x, const uint32_t *a, int acc) {
+    if constexpr (BITS == 4) {
+        acc = dp4a_us(x & 0x0f0f0f0fu, a[0], acc);
+        acc = dp4a_us((x >> 4) & 0x0f0f0f0fu, a[1], acc);
+    } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc = dp4a_us((x >> (2 * t)) & 0x03030303u, a[t], acc);
+    }
+    return acc;
+}
+
+// The lane's KPL activations quantized to int8 per block of bs values: step
+// sx = (largest magnitude of the block) / 127 (a block of more than KPL values
+// spans bs / KPL neighbouring lanes), q = round-to-nearest-even(v / sx)
+// clamped to +-127 (both divisions IEEE round-to-nearest), all zero for an
+// all-zero block.  Packed into the words dot_word_dp4a pairs with the codes;
+// per block part of the lane its step and the sum of its q.
+template <int BITS, int KPL, int BPL>
+__device__ __forceinline__ void prepare_dp4a(const float (&v)[KPL], int bs, uint32_t (&aq)[KPL / 4],
+                                             float (&sxb)[BPL], float (&fsq)[BPL]) {
+    constexpr int PART = KPL / BPL;
+    const int lb = bs > KPL ? bs / KPL : 1;  // lanes per block
+#pragma unroll
+    for (int w = 0; w < KPL / 4; ++w) aq[w] = 0u;
+#pragma unroll
+    for (int b = 0; b < BPL; ++b) {
+        float a = 0.f;
+#pragma unroll
+        for (int i = 0; i < PART; ++i) a = fmaxf(a, fabsf(v[b * PART + i]));
+        for (int off = 1; off < lb; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+        const float sx = a > 0.f ? __fdiv_rn(a, 127.f) : 0.f;
+        int sq = 0;
+#pragma unroll
+        for (int i = 0; i < PART; ++i) {
+            const int k = b * PART + i;
+            int q = 0;
+            if (a > 0.f) q = max(-127, min(127, __float2int_rn(__fdiv_rn(v[k], sx))));
+            sq += q;
+            aq[dp4a_word<BITS>(k)] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * dp4a_byte<BITS>(k));
+        }
+        sxb[b] = sx;
+        fsq[b] = static_cast<float>(sq);
+    }
+}
+
+// One tile's int8-activation dot products for one lane: ITER rows, each the
+// sum over the lane's blocks of s * sx * (sum q8 * q - zp * sum q8).
+template <bool ZPT, int BITS, int VEC, int BPL, int ITER, int KPL = kpl_of(VEC, BITS)>
+__device__ __forceinline__ void tile_dot_dp4a(const unsigned char *wp, const unsigned char *sp, const unsigned char *zpp,
+                                              int row_stride, int prow_stride, int zrow_stride,
+                                              const uint32_t (&aq)[KPL / 4], const float (&sxb)[BPL],
+                                              const float (&fsq)[BPL], float zdef, float (&racc)[ITER]) {
+    constexpr int WPL = VEC / 4;
+    constexpr int AW = (32 / BITS) / 4;  // activation words per code word
+#pragma unroll
+    for (int i = 0; i < ITER; ++i) {
+        uint32_t x[WPL];
+        load_words<VEC>(wp, x);
+        float rv = 0.f;
+#pragma unroll
+        for (int b = 0; b < BPL; ++b) {
+            int acc = 0;
+#pragma unroll
+            for (int j = b * (WPL / BPL); j < (b + 1) * (WPL / BPL); ++j) acc = dot_word_dp4a<BITS>(x[j], &aq[j * AW], acc);
+            const float s = h2f(*reinterpret_cast<const uint16_t *>(sp + b * 2));
+            const float z = ZPT ? h2f(*reinterpret_cast<const uint16_t *>(zpp + b * 2)) : zdef;
+            rv = fmaf(s * sxb[b], static_cast<float>(acc) - z * fsq[b], rv);
+        }
+        racc[i] = rv;
+        wp += row_stride;
+        sp += prow_stride;
+        zpp += zrow_stride;
+    }
+}
+
 // One tile's dot products for one lane: ITER rows (stride `row_stride` in the
 // stage) times this lane's KPL codes, scaled per block; racc[i * MT + m] gets
 // row i, activation row m.  ZPM: 1 a zero point per block and row in fp16,
@@ -703,6 +799,10 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
     float c23[MT];       // 2^23 e2c (see tile_dot)
     float post[MT];
     bool need_post = false;
+    // WK_DP4A: the lane's int8 activation words, per block part its step and sum of codes
+    constexpr bool DP4A = WK == WK_DP4A;
+    uint32_t aq[DP4A ? KPL / 4 : 1];
+    float sxb[BPL], fsq[BPL];
     // This CTA's activation row (the same for every tile it computes): staged
     // in shared memory with coalesced loads, then each lane takes its slice.
     {
@@ -739,21 +839,26 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
                 ap[m][4 * j + 2] = v.z;
                 ap[m][4 * j + 3] = v.w;
             }
-        prepare_activations<BITS, MT, KPL, BPL, WK>(ap, e2, ahat);
-        bool big = false;
+        if constexpr (DP4A) {
+            static_assert(!DP4A || MT == 1, "int8 activations: one activation row");
+            prepare_dp4a<BITS, KPL, BPL>(ap[0], p.bs, aq, sxb, fsq);
+        } else {
+            prepare_activations<BITS, MT, KPL, BPL, WK>(ap, e2, ahat);
+            bool big = false;
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            const float e2c = fminf(e2[m], __uint_as_float((104u + 127u) << 23));  // min(e2, 2^104)
-            post[m] = e2[m] / e2c;                                    // 1, or the power of two left over
-            big |= post[m] != 1.f;
-            c23[m] = 8388608.f * e2c;  // 2^23 e2c: exact, finite
+            for (int m = 0; m < MT; ++m) {
+                const float e2c = fminf(e2[m], __uint_as_float((104u + 127u) << 23));  // min(e2, 2^104)
+                post[m] = e2[m] / e2c;                                    // 1, or the power of two left over
+                big |= post[m] != 1.f;
+                c23[m] = 8388608.f * e2c;  // 2^23 e2c: exact, finite
 #pragma unroll
-            for (int b = 0; b < BPL; ++b) {
-                zah[m][b] = (p.zpv * ahat[m][b]) * e2c;
-                ahat[m][b] *= e2c;
+                for (int b = 0; b < BPL; ++b) {
+                    zah[m][b] = (p.zpv * ahat[m][b]) * e2c;
+                    ahat[m][b] *= e2c;
+                }
             }
+            need_post = __any_sync(0xffffffffu, big);
         }
-        need_post = __any_sync(0xffffffffu, big);
     }
     const int e = p.ids ? __ldg(p.ids + cta_slot) : 0;
     const bool valid = e >= 0 && e < p.num_experts;
@@ -776,7 +881,14 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
             const unsigned char *wp = st + half * p.w_pitch + lane_boff;  // this lane's first row is `half`
             const unsigned char *sp = st + p.s_off + (half * p.nb + blk0) * PB;
             const unsigned char *zrw = st + p.z_off + half * p.zrow;  // the lane's first row of zero points
-            if (WK == WK_NBITS && p.zp_mode == ZP_TENSOR)
+            if constexpr (DP4A) {
+                if (p.zp_mode == ZP_TENSOR)
+                    tile_dot_dp4a<true, BITS, VEC, BPL, ITER>(wp, sp, zrw + blk0 * 2, row_stride, prow_stride,
+                                                              zrow_stride, aq, sxb, fsq, p.zpv, racc);
+                else
+                    tile_dot_dp4a<false, BITS, VEC, BPL, ITER>(wp, sp, zrw, row_stride, prow_stride, zrow_stride, aq,
+                                                               sxb, fsq, p.zpv, racc);
+            } else if (WK == WK_NBITS && p.zp_mode == ZP_TENSOR)
                 tile_dot<1, BITS, VEC, MT, BPL, WK, ITER>(wp, sp, zrw + blk0 * 2, 0, row_stride, prow_stride,
                                                          zrow_stride, ap, c23, ahat, zah, lut_lane, racc, post,
                                                          need_post);
@@ -884,6 +996,7 @@ bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zrow, Cfg &
     for (int i = 0; i < ncand; ++i) {
         const int v = cands[i].vec, l = cands[i].lpr;
         if (row_bytes % v) continue;
+        if (kind == WK_DP4A && v != 16) continue;  // int8 activations: 16-byte units only
         const int kpl = v * 8 / bits;
         const int sw = l * kpl;
         const int st = (K + sw - 1) / sw;
@@ -908,8 +1021,9 @@ bool choose_cfg(int M, int N, int K, int bits, int bs, int kind, int zrow, Cfg &
     // 16 rows per lane group for MatMulNBits when a lane holds 32 activations and
     // the 16-row stage stays small (the codebook kernel is slower with them); the
     // kernels instantiated with 16 are listed in dispatch()
-    c.iter = (kind == WK_NBITS && c.lpr == 32 && c.mt == 1 && row_bytes <= 4096 &&
-              ((bits == 4 && c.vec == 16) || (bits == 2 && c.vec == 8)))
+    c.iter = (c.lpr == 32 && c.mt == 1 && row_bytes <= 4096 &&
+              ((kind == WK_NBITS && ((bits == 4 && c.vec == 16) || (bits == 2 && c.vec == 8))) ||
+               (kind == WK_DP4A && bits == 4 && c.vec == 16)))
                  ? 16
                  : 8;
     c.SR = c.iter * (32 / c.lpr);
@@ -973,6 +1087,12 @@ cudaError_t dispatch(const GemvArgs &a, const Cfg &c, int bits, int kind, cudaSt
         return launch_one<B, V, 1, BPL_, WK_NBITS, L_, A_SWIGLU>(a, c, s);
     // 16 rows per tile (see choose_cfg): full-warp lane groups holding 32 activations
     if (c.iter == 16) {
+        if (kind == WK_DP4A) {
+            if (c.mt == 1 && c.lpr == 32 && c.bpl == 1 && bits == 4 && c.vec == 16)
+                return a.a_mode == A_ROWS ? launch_one<4, 16, 1, 1, WK_DP4A, 32, A_ROWS, 16>(a, c, s)
+                                          : launch_one<4, 16, 1, 1, WK_DP4A, 32, A_SWIGLU, 16>(a, c, s);
+            return cudaErrorNotSupported;
+        }
         if (c.mt == 1 && c.lpr == 32 && c.bpl == 1) {
             if (bits == 4 && c.vec == 16 && kind == WK_NBITS)
                 return a.a_mode == A_ROWS ? launch_one<4, 16, 1, 1, WK_NBITS, 32, A_ROWS, 16>(a, c, s)
@@ -983,6 +1103,17 @@ cudaError_t dispatch(const GemvArgs &a, const Cfg &c, int bits, int kind, cudaSt
         }
         return cudaErrorNotSupported;
     }
+    // int8-activation QMoE (fc1 rows of x, fc2 SwiGLU rows)
+#define QG_CASE_D4(B, BPL_, L_)                                                                        \
+    if (kind == WK_DP4A && bits == B && c.vec == 16 && c.mt == 1 && c.bpl == BPL_ && c.lpr == L_)     \
+        return a.a_mode == A_ROWS ? launch_one<B, 16, 1, BPL_, WK_DP4A, L_, A_ROWS>(a, c, s)           \
+                                  : launch_one<B, 16, 1, BPL_, WK_DP4A, L_, A_SWIGLU>(a, c, s);
+    QG_CASE_D4(4, 1, 32)
+    QG_CASE_D4(4, 1, 16)
+    QG_CASE_D4(2, 1, 32)
+    QG_CASE_D4(2, 2, 32)
+#undef QG_CASE_D4
+    if (kind == WK_DP4A) return cudaErrorNotSupported;
     // fused QMoE fc2 (activations = SwiGLU of fc1's output)
     QG_CASE_SW(4, 16, 1, 32)
     QG_CASE_SW(4, 16, 1, 16)
@@ -1152,8 +1283,33 @@ size_t qmoe_workspace_bytes(int k, int hidden, int inter) {
     return g + o;
 }
 
-cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s) {
+// The int8-activation configurations dispatch() has a kernel for.
+static bool dp4a_dispatchable(const Cfg &c, int bits) {
+    if (c.mt != 1 || c.vec != 16) return false;
+    if (c.iter == 16) return bits == 4 && c.lpr == 32 && c.bpl == 1;
+    return (bits == 4 && c.bpl == 1 && (c.lpr == 32 || c.lpr == 16)) || (bits == 2 && c.lpr == 32 && (c.bpl == 1 || c.bpl == 2));
+}
+
+// The stage plan of one of the decode's two GEMVs (fc1 or fc2).
+static bool qmoe_cfg(const QmoeProblem &q, bool fc1, int kind, Cfg &c) {
+    const int N = fc1 ? 2 * q.inter : q.hidden;
+    const int K = fc1 ? q.hidden : q.inter;
+    const uint16_t *zp = fc1 ? q.fc1_zp : q.fc2_zp;
+    // the expert's bias row is staged in shared memory when it is small enough
+    const uint16_t *bias = fc1 ? q.fc1_bias : q.fc2_bias;
+    const int bias_bytes = bias && N <= 16384 ? (N * 2 + 15) / 16 * 16 : 0;
+    return choose_cfg(1, N, K, q.bits, q.bs, kind, zp ? (K / q.bs) * 2 : 0, c, bias_bytes) && c.splits == 1;
+}
+
+bool qmoe_dp4a_simt_ok(const QmoeProblem &q) {
+    Cfg c1, c2;
+    return qmoe_cfg(q, true, WK_DP4A, c1) && dp4a_dispatchable(c1, q.bits) && qmoe_cfg(q, false, WK_DP4A, c2) &&
+           dp4a_dispatchable(c2, q.bits);
+}
+
+cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s, bool dp4a) {
     const DeviceInfo &di = device_info();
+    const int kind = dp4a ? WK_DP4A : WK_NBITS;
     float *g = static_cast<float *>(ws);
     float *o = reinterpret_cast<float *>(static_cast<char *>(ws) +
                                          (static_cast<size_t>(q.k) * 2 * q.inter * sizeof(float) + 255) / 256 * 256);
@@ -1164,11 +1320,7 @@ cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s) {
         const int K = fc1 ? q.hidden : q.inter;
         const uint16_t *zp = fc1 ? q.fc1_zp : q.fc2_zp;
         Cfg c;
-        // the expert's bias row is staged in shared memory when it is small enough
-        const uint16_t *bias = fc1 ? q.fc1_bias : q.fc2_bias;
-        const int bias_bytes = bias && N <= 16384 ? (N * 2 + 15) / 16 * 16 : 0;
-        if (!choose_cfg(1, N, K, q.bits, q.bs, WK_NBITS, zp ? (K / q.bs) * 2 : 0, c, bias_bytes) || c.splits != 1)
-            return cudaErrorNotSupported;
+        if (!qmoe_cfg(q, fc1, kind, c)) return cudaErrorNotSupported;
         GemvArgs a{};
         a.A = q.x;
         a.a_dtype = 1;  // fp16 token
@@ -1204,7 +1356,7 @@ cudaError_t qmoe_decode(const QmoeProblem &q, void *ws, cudaStream_t s) {
         a.cps = std::max(1, di.sm_count / q.k);
         c.grid_x = q.k * a.cps;
         a.fast_tx = fast_stage_tx(a, c, 2);
-        cudaError_t e = dispatch(a, c, q.bits, WK_NBITS, s);
+        cudaError_t e = dispatch(a, c, q.bits, kind, s);
         if (e != cudaSuccess) return e;
     }
     const int threads = 256;
