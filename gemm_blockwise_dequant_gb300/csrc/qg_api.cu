@@ -236,6 +236,7 @@ int qmoe_common(bool dp4a, const uint16_t *x_f16, const int32_t *expert_ids, con
     q.y = y_f16;
     q.status = status_dev;
     // int8 activations: the SIMT kernel's dp4a kind where it has a plan, else the plain-load kernels
+    // (rows that are not a multiple of 16 bytes)
     const cudaError_t e = !dp4a                         ? qg::qmoe_decode(q, workspace, s)
                           : qg::qmoe_dp4a_simt_ok(q) ? qg::qmoe_decode(q, workspace, s, true)
                                                      : qg::qmoe_decode_dp4a(q, workspace, s);

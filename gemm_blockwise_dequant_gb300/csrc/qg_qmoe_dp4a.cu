@@ -8,18 +8,15 @@
 //     sum over blocks b of  s[r,b] * sx[b] * ( sum q8 * q  -  zp[r,b] * sum q8 )
 // with the integer sums formed by dp4a (four 8-bit products per instruction).
 //
-// Kernels: two GEMVs (fc1 with the quantization of x in its prologue, fc2
-// with SwiGLU and the quantization of h in its prologue) and a combine that
-// sums the slots in slot order.  Each GEMV CTA serves one expert slot: it
-// quantizes the slot's activation vector into shared memory and reduces its
-// share of the slot's weight rows, lane l taking units l, l + 32, ... (16 or
-// 8 bytes of codes each) of a row.  Rows of a multiple of 16 bytes stream
-// through a ring of shared-memory stages of 8 rows (codes, scales, zero
-// points), filled with bulk copies by a producer warp from the start of the
-// kernel -- while the consumer warps quantize the activations -- four groups
-// of consumer warps taking every fourth stage, two rows per warp.  Other rows
-// are read with plain vector loads, two rows per warp at a time so that their
-// loads overlap.
+// This file holds the decode for the shapes the SIMT GEMV's int8-activation
+// kind (qg_simt.cu) has no plan for -- rows that are not a multiple of 16
+// bytes, or whose stages do not fit.  Kernels: two GEMVs (fc1 with the
+// quantization of x in its prologue, fc2 with SwiGLU and the quantization of
+// h in its prologue) and a combine that sums the slots in slot order.  Each
+// GEMV CTA serves one expert slot: it quantizes the slot's activation vector
+// into shared memory, then its warps stream weight rows with coalesced vector
+// loads (lane l takes the row's units l, l + 32, ...), two rows at a time so
+// that their loads overlap.
 // The quantized activations are stored in the byte order that pairs them with
 // the codes as they come out of one AND of a code word: for u4, lanes of
 // (w & 0x0f0f0f0f) hold codes 0, 2, 4, 6 of the word and (w >> 4) & ... codes
@@ -32,20 +29,6 @@ namespace {
 
 constexpr int kDThreads = 512;
 constexpr int kDWarps = kDThreads / 32;
-// ring kernel: 16 consumer warps in four groups, group i taking 8-row stages
-// i, i + 4, ... (two rows per warp), and a producer; five warps per SM
-// sub-partition at 96 registers
-constexpr int kRCons = 16;
-constexpr int kRGroups = 4;
-constexpr int kRGWarps = kRCons / kRGroups;
-constexpr int kRRows = 8;
-constexpr int kRPW = kRRows / kRGWarps;  // rows per consumer warp and stage
-constexpr int kRThreads = (kRCons + 1) * 32;
-constexpr int kRRegs = 96;
-static_assert((kRCons + 1 + 3) / 4 * 32 * kRRegs <= 16384, "registers of one SM sub-partition");
-constexpr int kRMaxStages = 16;
-constexpr int kRHeader = 512;  // full / empty barriers, abort flag
-
 struct Dp4aGemv {
     const uint16_t *x;        // fc1: fp16 activations [K]
     const float *g;           // fc2: fc1 outputs [slots][2K] (gate/up), or null
@@ -58,9 +41,6 @@ struct Dp4aGemv {
     const uint16_t *bias;     // [E][N], or null
     int N, K, bs, cps;
     float *out;               // [slots][N]
-    // ring kernel: rows per CTA (a multiple of 8), stages, their layout
-    int rows_per, NST, stage_off, stage_bytes, par_off, zp_off;
-    unsigned *fault;
 };
 
 __device__ __forceinline__ int dp4a_us(uint32_t codes, uint32_t acts, int c) {
@@ -91,11 +71,7 @@ __device__ __forceinline__ int dot_word(uint32_t w, const uint32_t *a, int acc) 
     return acc;
 }
 
-// Quantizes the slot's activation vector (x, or silu(gate) * up of the slot's
-// fc1 output) per block of bs values into the permuted int8 layout x8, the
-// sums of 16-value granules s16 and the block scales sxs; warps `warp`,
-// `warp + nwarps`, ... take one block each.  raw: the activation values
-// already staged in shared memory, or null (read and formed here).
+// Activation k of the slot's vector: x, or silu(gate) * up of the slot's fc1 output.
 template <int BITS, bool FC2>
 __device__ __forceinline__ float act_value(const Dp4aGemv &p, int slot, int k) {
     if constexpr (FC2) {
@@ -109,9 +85,12 @@ __device__ __forceinline__ float act_value(const Dp4aGemv &p, int slot, int k) {
     }
 }
 
+// Quantizes the slot's activation vector per block of bs values into the
+// permuted int8 layout x8, the sums of 16-value granules s16 and the block
+// scales sxs; warps `warp`, `warp + nwarps`, ... take one block each.
 template <int BITS, bool FC2>
 __device__ __forceinline__ void quantize_acts(const Dp4aGemv &p, int slot, int warp, int nwarps, int lane,
-                                              unsigned char *x8, int *s16, float *sxs, const float *raw) {
+                                              unsigned char *x8, int *s16, float *sxs) {
     const int K = p.K, bs = p.bs, nb = K / bs;
     for (int b = warp; b < nb; b += nwarps) {
         float v[8];  // bs / 32 <= 8 values per lane
@@ -121,7 +100,7 @@ __device__ __forceinline__ void quantize_acts(const Dp4aGemv &p, int slot, int w
             v[j] = 0.f;
             if (j >= bs / 32) continue;
             const int k = b * bs + 32 * j + lane;
-            const float val = raw ? raw[k] : act_value<BITS, FC2>(p, slot, k);
+            const float val = act_value<BITS, FC2>(p, slot, k);
             v[j] = val;
             a = fmaxf(a, fabsf(val));
         }
@@ -162,7 +141,7 @@ __global__ void __launch_bounds__(kDThreads, 1) dp4a_gemv_kernel(Dp4aGemv p) {
     if (e < 0 || e >= p.num_experts) return;  // CTA-uniform: the slot adds nothing
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    quantize_acts<BITS, FC2>(p, slot, warp, kDWarps, lane, x8, s16, sxs, nullptr);
+    quantize_acts<BITS, FC2>(p, slot, warp, kDWarps, lane, x8, s16, sxs);
     __syncthreads();
 
     // ---- rows of this CTA's share of the slot's matrix, two per warp at a time.
@@ -275,213 +254,6 @@ __global__ void __launch_bounds__(kDThreads, 1) dp4a_gemv_kernel(Dp4aGemv p) {
     }
 }
 
-// The same GEMV for rows of a multiple of 16 bytes, with the rows streamed
-// through a ring of 8-row stages.  Warp kRCons is the producer: from the
-// start of the kernel it fills stage after stage (codes with one bulk copy,
-// then scales and zero points: 8 rows of them are a multiple of 16 bytes and
-// a CTA's stages start at multiples of 8 rows, so they are bulk copies too
-// when the expert's parameter block is 16-byte aligned; otherwise, and for a
-// ragged last stage, the producer's lanes copy what is left).  The consumer warps quantize
-// their shares of the activation blocks; then group i (kRGWarps warps) takes
-// stages i, i + kRGroups, ..., warp w of it rows 2w and 2w + 1, each reduced
-// exactly as the plain kernel reduces a row, so both give the same bits.
-// Every wait is bounded (a give-up records the fault word and ends the CTA's
-// work).
-template <int BITS, bool FC2, int UPL>
-__global__ void __maxnreg__(kRRegs) dp4a_ring_kernel(Dp4aGemv p) {
-    constexpr int VEC = 16;
-    constexpr int CPW = 32 / BITS;
-    constexpr int WPU = VEC / 4;
-    constexpr int CPU = VEC * 8 / BITS;
-    constexpr int SEGC = CPU < 32 ? CPU : 32;
-    constexpr int SPU = CPU / SEGC;
-    constexpr int WPS = SEGC / CPW;
-    constexpr int AW = CPW / 4;
-    constexpr int UR = UPL > 0 ? UPL : 1;
-    extern __shared__ __align__(1024) unsigned char rsm[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(rsm);
-    uint64_t *empty = full + kRMaxStages;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(rsm + 2 * kRMaxStages * 8);
-    const int K = p.K, bs = p.bs, nb = K / bs;
-    unsigned char *x8 = rsm + kRHeader;
-    int *s16 = reinterpret_cast<int *>(x8 + ((K + 15) / 16) * 16);
-    float *sxs = reinterpret_cast<float *>(s16 + K / 16);
-    unsigned char *stages = rsm + p.stage_off;
-    const int slot = blockIdx.x / p.cps, c = blockIdx.x % p.cps;
-    const int e = __ldg(p.ids + slot);
-    if (e < 0 || e >= p.num_experts) return;  // CTA-uniform: the slot adds nothing
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int row_bytes = K * BITS / 8;
-    const int r_lo = c * p.rows_per, r_hi = min(p.N, r_lo + p.rows_per);
-    const int nst = r_hi > r_lo ? (r_hi - r_lo + kRRows - 1) / kRRows : 0;  // stages of this CTA
-    const uint8_t *we = p.w + static_cast<size_t>(e) * p.N * row_bytes;
-    const uint16_t *se = p.scales + static_cast<size_t>(e) * p.N * nb;
-    const uint16_t *ze = p.zp ? p.zp + static_cast<size_t>(e) * p.N * nb : nullptr;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < p.NST; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kRGWarps);  // released by the warps of the group that took it
-        }
-        *abort_flag = 0;
-        mbar_fence_init();
-    }
-    __syncthreads();
-
-    if (warp == kRCons) {
-        // ------------------------------------------------------------ producer
-        int st_i = 0;
-        uint32_t par = 1;  // parity of the empty phase to wait for before refilling st_i
-        for (int sgi = 0; sgi < nst; ++sgi) {
-            if (sgi >= p.NST &&
-                !__all_sync(0xffffffffu, mbar_wait(&empty[st_i], par, abort_flag, p.fault, FAULT_WAIT_EMPTY)))
-                break;
-            const int r0 = r_lo + sgi * kRRows;
-            const int rows = min(kRRows, r_hi - r0);
-            unsigned char *st = stages + static_cast<size_t>(st_i) * p.stage_bytes;
-            const uint32_t cb = static_cast<uint32_t>(rows) * row_bytes;
-            const uint32_t pb = static_cast<uint32_t>(rows) * nb * 2;
-            const uint16_t *ps = se + static_cast<size_t>(r0) * nb;
-            const uint16_t *zs = ze ? ze + static_cast<size_t>(r0) * nb : nullptr;
-            const CopyPlan cpp = copy_plan(st + p.par_off, ps, pb);
-            copy_tail_lanes(st + p.par_off, ps, pb, cpp, lane);
-            uint32_t tx = cb + cpp.bulk_bytes;
-            CopyPlan cpz{0u};
-            if (zs) {
-                cpz = copy_plan(st + p.zp_off, zs, pb);
-                copy_tail_lanes(st + p.zp_off, zs, pb, cpz, lane);
-                tx += cpz.bulk_bytes;
-            }
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&full[st_i], tx);
-                bulk_g2s(st, we + static_cast<size_t>(r0) * row_bytes, cb, &full[st_i]);
-                if (cpp.bulk_bytes) bulk_g2s(st + p.par_off, ps, cpp.bulk_bytes, &full[st_i]);
-                if (cpz.bulk_bytes) bulk_g2s(st + p.zp_off, zs, cpz.bulk_bytes, &full[st_i]);
-            }
-            if (++st_i == p.NST) {
-                st_i = 0;
-                par ^= 1u;
-            }
-        }
-        return;
-    }
-
-    // ------------------------------------------------------------ consumers
-    quantize_acts<BITS, FC2>(p, slot, warp, kRCons, lane, x8, s16, sxs, nullptr);
-    named_bar_sync(1, kRCons * 32);
-    const int units = row_bytes / VEC;
-    int bs_log2 = 5;
-    while ((1 << bs_log2) < bs) ++bs_log2;
-    const float zdef = static_cast<float>(1 << (BITS - 1));
-    uint32_t act[UR][WPU * AW];
-    int sq[UR][SPU], blk[UR][SPU];
-    float sx[UR][SPU];
-    auto load_unit_consts = [&](int i, int u) {
-#pragma unroll
-        for (int j = 0; j < WPU * AW; ++j) act[i][j] = reinterpret_cast<const uint32_t *>(x8 + u * CPU)[j];
-#pragma unroll
-        for (int sgi = 0; sgi < SPU; ++sgi) {
-            const int ks = u * CPU + sgi * SEGC;
-            int S = 0;
-#pragma unroll
-            for (int gi = 0; gi < SEGC / 16; ++gi) S += s16[ks / 16 + gi];
-            sq[i][sgi] = S;
-            blk[i][sgi] = ks >> bs_log2;
-            sx[i][sgi] = sxs[ks >> bs_log2];
-        }
-    };
-    if constexpr (UPL > 0) {
-#pragma unroll
-        for (int i = 0; i < UPL; ++i)
-            if (lane + 32 * i < units) load_unit_consts(i, lane + 32 * i);
-    }
-    // group grp takes stages grp, grp + 2, ...; warp wg of it rows 2 wg, 2 wg + 1
-    // of each (two independent row sums in flight)
-    const int grp = warp / kRGWarps, wg = warp % kRGWarps;
-    int st_i = grp;
-    uint32_t par = 0;
-    float bias_l[kRPW] = {};  // lane l: the biases of this warp's rows in its stage 32 q + l
-    for (int sgi = grp, q = 0; sgi < nst; sgi += kRGroups, ++q) {
-        if ((q & 31) == 0 && p.bias) {  // a row load per stage would stall the warp
-            const int sl = sgi + kRGroups * lane;
-#pragma unroll
-            for (int rr = 0; rr < kRPW; ++rr) {
-                const int rb = r_lo + sl * kRRows + kRPW * wg + rr;
-                bias_l[rr] = sl < nst && rb < r_hi ? h2f(__ldg(p.bias + static_cast<size_t>(e) * p.N + rb)) : 0.f;
-            }
-        }
-        float bias_r[kRPW];
-#pragma unroll
-        for (int rr = 0; rr < kRPW; ++rr) bias_r[rr] = __shfl_sync(0xffffffffu, bias_l[rr], q & 31);
-        const bool ok = mbar_wait(&full[st_i], par, abort_flag, p.fault, FAULT_WAIT_FULL);
-        const int r0 = r_lo + sgi * kRRows + kRPW * wg;
-        if (ok && r0 < r_hi) {  // warp-uniform; a second row past r_hi is computed and dropped
-            const unsigned char *st = stages + static_cast<size_t>(st_i) * p.stage_bytes;
-            const unsigned char *rowp = st + kRPW * wg * row_bytes;
-            const uint16_t *srow = reinterpret_cast<const uint16_t *>(st + p.par_off) + kRPW * wg * nb;
-            const uint16_t *zrow = reinterpret_cast<const uint16_t *>(st + p.zp_off) + kRPW * wg * nb;
-            float part[kRPW] = {};
-            for (int ub = 0; ub < units; ub += 32 * UR) {
-                uint32_t cw[kRPW][UR][WPU];
-                uint16_t sb[kRPW][UR][SPU], zb[kRPW][UR][SPU];
-#pragma unroll
-                for (int i = 0; i < UR; ++i) {
-                    const int u = ub + lane + 32 * i;
-                    if (u >= units) continue;
-                    if constexpr (UPL == 0) load_unit_consts(i, u);
-#pragma unroll
-                    for (int rr = 0; rr < kRPW; ++rr) {
-                        const uint4 t = *reinterpret_cast<const uint4 *>(rowp + rr * row_bytes + u * VEC);
-                        cw[rr][i][0] = t.x;
-                        cw[rr][i][1] = t.y;
-                        cw[rr][i][2] = t.z;
-                        cw[rr][i][3] = t.w;
-#pragma unroll
-                        for (int g = 0; g < SPU; ++g) {
-                            sb[rr][i][g] = srow[rr * nb + blk[i][g]];
-                            zb[rr][i][g] = ze ? zrow[rr * nb + blk[i][g]] : uint16_t(0);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < UR; ++i) {
-                    if (ub + lane + 32 * i >= units) continue;
-#pragma unroll
-                    for (int rr = 0; rr < kRPW; ++rr) {
-#pragma unroll
-                        for (int g = 0; g < SPU; ++g) {
-                            int acc = 0;
-#pragma unroll
-                            for (int wi = g * WPS; wi < (g + 1) * WPS; ++wi)
-                                acc = dot_word<BITS>(cw[rr][i][wi], &act[i][wi * AW], acc);
-                            const float z = ze ? h2f(zb[rr][i][g]) : zdef;
-                            part[rr] = fmaf(h2f(sb[rr][i][g]) * sx[i][g],
-                                            static_cast<float>(acc) - z * static_cast<float>(sq[i][g]), part[rr]);
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-                for (int rr = 0; rr < kRPW; ++rr) part[rr] += __shfl_xor_sync(0xffffffffu, part[rr], off);
-            if (lane == 0) {
-#pragma unroll
-                for (int rr = 0; rr < kRPW; ++rr)
-                    if (r0 + rr < r_hi) p.out[static_cast<size_t>(slot) * p.N + r0 + rr] = p.bias ? part[rr] + bias_r[rr] : part[rr];
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st_i]);
-        if (!ok) break;
-        st_i += kRGroups;
-        if (st_i >= p.NST) {
-            st_i -= p.NST;
-            par ^= 1u;
-        }
-    }
-}
-
 // y[r] = fp16( sum_j w_j * o_j[r] ) in slot order; out-of-range ids add
 // nothing and set *status to 1.
 __global__ void dp4a_combine_kernel(const float *__restrict__ o, const int32_t *__restrict__ ids,
@@ -531,51 +303,8 @@ cudaError_t launch_upl(const Dp4aGemv &a, int slots, cudaStream_t s) {
     }
 }
 
-inline int rup(int x, int a) { return (x + a - 1) / a * a; }
-
-// Ring layout for rows of a multiple of 16 bytes: [barriers][quantized
-// activations][stages of kRRows rows: codes | scales | zero points]; false
-// when fewer than two stages fit.
-bool ring_layout(Dp4aGemv &a, int bits) {
-    const int row_bytes = a.K * bits / 8, nb = a.K / a.bs;
-    if (row_bytes % 16) return false;
-    a.stage_off = rup(kRHeader + static_cast<int>(dp4a_smem(a.K, a.bs)), 128);
-    a.par_off = rup(kRRows * row_bytes, 128);
-    a.zp_off = rup(a.par_off + kRRows * nb * 2, 128);
-    a.stage_bytes = rup(a.zp_off + (a.zp ? kRRows * nb * 2 : 0), 128);
-    // a multiple of the groups: stage slot i always serves group i % kRGroups
-    a.NST = std::min(kRMaxStages, (device_info().max_smem_optin - a.stage_off) / a.stage_bytes) / kRGroups * kRGroups;
-    a.rows_per = rup((a.N + a.cps - 1) / a.cps, 8);
-    a.fault = fault_word();
-    return a.NST >= 2;
-}
-
-template <int BITS, bool FC2, int UPL>
-cudaError_t launch_ring(const Dp4aGemv &a, int slots, cudaStream_t s) {
-    auto kern = dp4a_ring_kernel<BITS, FC2, UPL>;
-    const int smem = a.stage_off + a.NST * a.stage_bytes;
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    kern<<<slots * a.cps, kRThreads, smem, s>>>(a);
-    return cudaGetLastError();
-}
-
-template <int BITS, bool FC2>
-cudaError_t launch_ring_upl(const Dp4aGemv &a, int slots, cudaStream_t s) {
-    const int units = a.K * BITS / 8 / 16;
-    const int upl = (units + 31) / 32;
-    if (upl == 1) return launch_ring<BITS, FC2, 1>(a, slots, s);
-    if (upl == 2) return launch_ring<BITS, FC2, 2>(a, slots, s);
-    if constexpr (BITS == 4) {  // three 2-bit units (192 codes) per lane would spill
-        if (upl == 3) return launch_ring<BITS, FC2, 3>(a, slots, s);
-    }
-    return launch_ring<BITS, FC2, 0>(a, slots, s);
-}
-
 template <bool FC2>
-cudaError_t launch_bits(Dp4aGemv a, int bits, int slots, cudaStream_t s) {
-    if (ring_layout(a, bits))
-        return bits == 4 ? launch_ring_upl<4, FC2>(a, slots, s) : launch_ring_upl<2, FC2>(a, slots, s);
+cudaError_t launch_bits(const Dp4aGemv &a, int bits, int slots, cudaStream_t s) {
     const bool v16 = (a.K * bits / 8) % 16 == 0;
     if (bits == 4) return v16 ? launch_upl<4, 16, FC2>(a, slots, s) : launch_upl<4, 8, FC2>(a, slots, s);
     return v16 ? launch_upl<2, 16, FC2>(a, slots, s) : launch_upl<2, 8, FC2>(a, slots, s);

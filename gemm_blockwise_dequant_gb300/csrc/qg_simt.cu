@@ -1112,6 +1112,8 @@ cudaError_t dispatch(const GemvArgs &a, const Cfg &c, int bits, int kind, cudaSt
     QG_CASE_D4(4, 1, 16)
     QG_CASE_D4(2, 1, 32)
     QG_CASE_D4(2, 2, 32)
+    QG_CASE_D4(2, 1, 16)
+    QG_CASE_D4(2, 2, 16)
 #undef QG_CASE_D4
     if (kind == WK_DP4A) return cudaErrorNotSupported;
     // fused QMoE fc2 (activations = SwiGLU of fc1's output)
@@ -1287,7 +1289,7 @@ size_t qmoe_workspace_bytes(int k, int hidden, int inter) {
 static bool dp4a_dispatchable(const Cfg &c, int bits) {
     if (c.mt != 1 || c.vec != 16) return false;
     if (c.iter == 16) return bits == 4 && c.lpr == 32 && c.bpl == 1;
-    return (bits == 4 && c.bpl == 1 && (c.lpr == 32 || c.lpr == 16)) || (bits == 2 && c.lpr == 32 && (c.bpl == 1 || c.bpl == 2));
+    return (c.lpr == 32 || c.lpr == 16) && (bits == 4 ? c.bpl == 1 : (c.bpl == 1 || c.bpl == 2));
 }
 
 // The stage plan of one of the decode's two GEMVs (fc1 or fc2).

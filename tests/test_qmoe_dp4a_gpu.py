@@ -79,11 +79,14 @@ def test_dp4a_grid(qg, bs, with_zp, with_bias):
 
 @pytest.mark.parametrize("bs", [32, 64, 128, 256])
 @pytest.mark.parametrize("bits", [2, 4])
-@pytest.mark.parametrize("hidden,inter", [(512, 768), (288, 160)])
+@pytest.mark.parametrize("hidden,inter", [(512, 768), (288, 160), (2048, 512)])
 def test_dp4a_fc1_integer_parts_exact(qg, bs, bits, hidden, inter):
     """One slot: the fc1 output in the workspace equals the oracle's to fp32
     rounding (every int8 code of x and every integer dot identical).  The
-    (288, 160) shape has u2 rows that are not a multiple of 16 bytes."""
+    shapes reach every int8 path: the SIMT kernel with 16-lane groups (512),
+    with 32-lane groups (2048; u4 with 16-row tiles), and the plain-load
+    kernel for the u2 rows of (288, 160), which are not a multiple of 16
+    bytes."""
     if hidden % bs or inter % bs:
         pytest.skip("shape not a multiple of the block")
     t = torch()
