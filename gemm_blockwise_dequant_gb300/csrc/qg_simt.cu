@@ -432,34 +432,60 @@ __device__ __forceinline__ void stage_activations(const GemvArgs &p, float *as, 
     constexpr int PITCH = KPL + 4;  // floats per lane slot
     if (p.a_dtype == 0) {
         const int nv = nslots * (KPL / 4);  // float4 per staged row
-        for (int i = tid; i < MT * nv; i += nthr) {
-            const int m = i / nv, v = i - m * nv;
-            const int k = kc0 + 4 * v, am = p.m0 + m;
-            float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (am < p.M && k < p.K)
-                val = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(p.A) + static_cast<size_t>(am) * p.K + k));
-            *reinterpret_cast<float4 *>(as + m * p.a_rstride + (v / (KPL / 4)) * PITCH + (v % (KPL / 4)) * 4) = val;
+        // two groups per thread and pass, both loads issued first
+        for (int i0 = tid; i0 < MT * nv; i0 += 2 * nthr) {
+            float4 val[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = i0 + u * nthr;
+                const int m = i / nv, v = i - m * nv;
+                const int k = kc0 + 4 * v, am = p.m0 + m;
+                val[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (i < MT * nv && am < p.M && k < p.K)
+                    val[u] = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(p.A) +
+                                                                    static_cast<size_t>(am) * p.K + k));
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = i0 + u * nthr;
+                if (i >= MT * nv) break;
+                const int m = i / nv, v = i - m * nv;
+                *reinterpret_cast<float4 *>(as + m * p.a_rstride + (v / (KPL / 4)) * PITCH + (v % (KPL / 4)) * 4) = val[u];
+            }
         }
     } else {
         const bool f16 = p.a_dtype == 1;
         const int nv = nslots * (KPL / 8);  // 8-element groups per staged row
-        for (int i = tid; i < MT * nv; i += nthr) {
-            const int m = i / nv, v = i - m * nv;
-            const int k = kc0 + 8 * v, am = p.m0 + m;
-            uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-            if (am < p.M && k < p.K)
-                raw = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.A) + static_cast<size_t>(am) * p.K + k));
-            const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-            float f[8];
+        // two groups per thread and pass, both loads issued first
+        for (int i0 = tid; i0 < MT * nv; i0 += 2 * nthr) {
+            uint4 rw[2];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint16_t lo = static_cast<uint16_t>(w4[q] & 0xFFFFu), hi = static_cast<uint16_t>(w4[q] >> 16);
-                f[2 * q] = f16 ? h2f(lo) : bf2f(lo);
-                f[2 * q + 1] = f16 ? h2f(hi) : bf2f(hi);
+            for (int u = 0; u < 2; ++u) {
+                const int i = i0 + u * nthr;
+                const int m = i / nv, v = i - m * nv;
+                const int k = kc0 + 8 * v, am = p.m0 + m;
+                rw[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (i < MT * nv && am < p.M && k < p.K)
+                    rw[u] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.A) +
+                                                                  static_cast<size_t>(am) * p.K + k));
             }
-            float *d = as + m * p.a_rstride + (v / (KPL / 8)) * PITCH + (v % (KPL / 8)) * 8;
-            *reinterpret_cast<float4 *>(d) = make_float4(f[0], f[1], f[2], f[3]);
-            *reinterpret_cast<float4 *>(d + 4) = make_float4(f[4], f[5], f[6], f[7]);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = i0 + u * nthr;
+                if (i >= MT * nv) break;
+                const int m = i / nv, v = i - m * nv;
+                const uint32_t w4[4] = {rw[u].x, rw[u].y, rw[u].z, rw[u].w};
+                float f[8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint16_t lo = static_cast<uint16_t>(w4[q] & 0xFFFFu), hi = static_cast<uint16_t>(w4[q] >> 16);
+                    f[2 * q] = f16 ? h2f(lo) : bf2f(lo);
+                    f[2 * q + 1] = f16 ? h2f(hi) : bf2f(hi);
+                }
+                float *d = as + m * p.a_rstride + (v / (KPL / 8)) * PITCH + (v % (KPL / 8)) * 8;
+                *reinterpret_cast<float4 *>(d) = make_float4(f[0], f[1], f[2], f[3]);
+                *reinterpret_cast<float4 *>(d + 4) = make_float4(f[4], f[5], f[6], f[7]);
+            }
         }
     }
 }
