@@ -180,13 +180,17 @@ __device__ __forceinline__ void build_span_row(int sp, int m, int lane, float (&
     const int blk = lane >> 2, wd = lane & 3;
     int j, c, w;
     owner_of<BPG>(blk, wd, j, c, w);
-    float mx = 0.f;
+    // the span's largest magnitude: a lane's 16 in a tree, then one warp-wide
+    // integer max (non-negative floats order as their bit patterns)
+    float m8[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(a[i]));
+    for (int i = 0; i < 8; ++i) m8[i] = fmaxf(fabsf(a[i]), fabsf(a[i + 8]));
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) m8[i] = fmaxf(m8[i], m8[i + w]);
     // e clamped to [-110, 117]: both 2^(14 - e) and 2^(10 + e) stay normal
-    const unsigned bits = __float_as_uint(mx);
+    const unsigned bits = __reduce_max_sync(0xffffffffu, __float_as_uint(m8[0]));
     const int ef = static_cast<int>((bits >> 23) & 0xFFu);
     const int e = (bits == 0u || ef == 255) ? 0 : min(max(ef - 127, -110), 117);
     const float asc = exp2i(14 - e);
@@ -517,6 +521,7 @@ __global__ void __maxnreg__(kMaxRegs)
                 (void)bb1;
                 if (BREG && !one_span) load_breg(sp);
                 const int pb = sp * 8;  // first block of the span
+                (void)pb;
                 float accs[2 * TR][2];
 #pragma unroll
                 for (int r = 0; r < 2 * TR; ++r) accs[r][0] = accs[r][1] = 0.f;
@@ -609,6 +614,10 @@ __global__ void __maxnreg__(kMaxRegs)
                         const uint16_t *ps1 = ((2 * t + 1) / TR ? psb : psa) + (g + 8 * ((2 * t + 1) % TR)) * pw;
                         const uint16_t *zs0 = ((2 * t) / TR ? zsb : zsa) + (g + 8 * ((2 * t) % TR)) * pw;
                         const uint16_t *zs1 = ((2 * t + 1) / TR ? zsb : zsa) + (g + 8 * ((2 * t + 1) % TR)) * pw;
+                        (void)ps0;
+                        (void)ps1;
+                        (void)zs0;
+                        (void)zs1;
 #pragma unroll
                         for (int e = 0; e < (NT == 2 ? 1 : 2); ++e) {
                             const int bl = block_of_beta<BPG>(j, (2 * c + e) / MNT);
