@@ -229,14 +229,15 @@ __device__ __forceinline__ void build_span_row(int sp, int m, int lane, float (&
     }
 }
 
-// Lanes of a row quad that leave a partial sum of the same (weight row,
-// activation row): four for one activation row (both fp16 columns of a lane
-// are that row), else the lanes c whose columns hold row m -- c % MP == m for
-// fp32 activations (one row per lane), the pairs (2c, 2c + 1) % MP for 16-bit
-// ones.  Lane c's partial goes to slot c * SL / 4 of [row][m][SL].
+// Lanes of a row quad that hold partial sums of the same (weight row,
+// activation row) add them with xor shuffles over the lane bits that keep the
+// activation row (a fixed order) before the lowest of them leaves the sum in
+// the reduction slot [row][m]: all four lanes for one activation row, else
+// the lanes c with c % MP == m for fp32 activations (one row per lane), or
+// with (2c, 2c + 1) % MP holding m for 16-bit ones (two rows per lane).
 template <int MP, int NT>
-__host__ __device__ constexpr int red_slots() {
-    return NT == 2 ? 4 / MP : (MP <= 2 ? 4 : 8 / MP);
+__host__ __device__ constexpr int quad_first_offset() {
+    return NT == 2 ? MP : (MP == 1 ? 1 : MP / 2);  // the xor offsets are this one, doubled, below 4
 }
 
 // At most kMaxWarps + 1 = 12 warps: three per SM sub-partition, whose 16 K
@@ -257,7 +258,6 @@ __global__ void __maxnreg__(kMaxRegs)
     constexpr int FR = 8 * TR;       // weight rows per fill
     constexpr int TROWS = 16 * TR;   // weight rows per tile
     constexpr bool PSMEM = TR == 2;  // block parameters in the stage
-    constexpr int SL = red_slots<MP, NT>();
     static_assert(MNT >= 1 && MNT <= 8 && (8 % MNT) == 0, "columns per block");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -271,7 +271,7 @@ __global__ void __maxnreg__(kMaxRegs)
     float *spart = reinterpret_cast<float *>(smem + p.sp_off);  // [blocks][MP]: 2^-24 sum of a' per block
     float *somul = reinterpret_cast<float *>(smem + p.om_off);  // [spans][MP]: each span's output multiplier
     unsigned char *stages = smem + p.stage_off;
-    float *red = reinterpret_cast<float *>(smem + p.red_off);   // [stage / 2][warp][rows][MP][SL]
+    float *red = reinterpret_cast<float *>(smem + p.red_off);   // [stage / 2][warp][rows][MP]
 
     const int W = p.W_;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -317,16 +317,14 @@ __global__ void __maxnreg__(kMaxRegs)
         // ------------------------------------------------------------ producer
         auto finish = [&](int tl, int rslot) {  // add the warps' sums of tile tl of this CTA, write Y
             const int rb0 = fill_row0(tl, 0), rb1 = fill_row0(tl, 1);
-            const float *r = red + (rslot >> 1) * (W * TROWS * MP * SL);
+            const float *r = red + (rslot >> 1) * (W * TROWS * MP);
             for (int v = lane; v < TROWS * MP; v += 32) {
                 const int row = v / MP, m = v - row * MP;
                 const int n = (row < FR ? rb0 : rb1 - FR) + row;
                 if (m >= p.M || n >= p.N) continue;
                 float s = 0.f;
                 for (int w = 0; w < W; ++w) {  // warp (span) order, then lane order
-                    const float *q = r + (w * TROWS * MP + v) * SL;
-#pragma unroll
-                    for (int k = 0; k < SL; ++k) s += q[k];
+                    s += r[w * TROWS * MP + v];
                 }
                 store_y_elem(p.Y, p.y_dtype, static_cast<size_t>(m) * p.N + n, s);
             }
@@ -657,21 +655,31 @@ __global__ void __maxnreg__(kMaxRegs)
             else tile_body(std::false_type{});
         }
         // this warp's span sums of the tile's rows, for the producer (in the
-        // reduction slot of the tile's second fill): every lane of a row quad
-        // leaves its own partial of each (row, activation row) it holds, in its
-        // slot of [row][m][SL], and the producer adds them (fixed order, no shuffles)
-        float *rw = red + (sb_ >> 1) * (W * TROWS * MP * SL) + sl * TROWS * MP * SL;
-        const int ks = c * SL / 4;
+        // reduction slot of the tile's second fill): the lanes of a row quad
+        // that hold the same (row, activation row) add their partials (xor
+        // shuffles, a fixed order) and the first of them stores the sum in
+        // [row][m]; the producer adds the warps' sums in warp order
+        float *rw = red + (sb_ >> 1) * (W * TROWS * MP) + sl * TROWS * MP;
+        constexpr int QO = quad_first_offset<MP, NT>();
 #pragma unroll
         for (int r = 0; r < 2 * TR; ++r) {
             const int row = (r / TR) * FR + g + 8 * (r % TR);  // tile row of the thread's row r
-            if (NT == 1 && MP == 1) {   // both columns are row 0: lane c's slot holds their sum
-                rw[row * SL + ks] = acc[r][0] + acc[r][1];
-            } else if (NT == 2) {       // one activation row per lane
-                rw[(row * MP + m0) * SL + ks] = acc[r][0];
-            } else {                    // two activation rows per lane
-                rw[(row * MP + m0) * SL + ks] = acc[r][0];
-                rw[(row * MP + m1) * SL + ks] = acc[r][1];
+            float v0 = NT == 1 && MP == 1 ? acc[r][0] + acc[r][1] : acc[r][0];  // one row: both columns
+            float v1 = acc[r][1];
+#pragma unroll
+            for (int off = QO; off < 4; off <<= 1) {
+                v0 += __shfl_xor_sync(0xffffffffu, v0, off);
+                if (NT == 1 && MP > 1) v1 += __shfl_xor_sync(0xffffffffu, v1, off);
+            }
+            if (c < QO) {
+                if (NT == 1 && MP == 1) {
+                    rw[row] = v0;
+                } else if (NT == 2) {  // one activation row per lane
+                    rw[row * MP + m0] = v0;
+                } else {               // two activation rows per lane
+                    rw[row * MP + m0] = v0;
+                    rw[row * MP + m1] = v1;
+                }
             }
         }
         __syncwarp();
@@ -723,8 +731,7 @@ bool layout_mg(int M, int N, int K, int a_dtype, bool zpt, int tr, bool ov, MgCf
     c.par_off = rup(fr * row_bytes, 128);
     c.zp_off = rup(c.par_off + (c.TR == 2 ? fr * nb * 2 : 0), 128);
     c.stage_bytes = rup(c.zp_off + (zpt && c.TR == 2 ? fr * nb * 2 : 0), 128);
-    const int sl = c.NT == 2 ? 4 / c.MP : (c.MP <= 2 ? 4 : 8 / c.MP);  // red_slots<MP, NT>()
-    const int red_stage = c.W * 16 * c.TR * c.MP * sl * 4;
+    const int red_stage = c.W * 16 * c.TR * c.MP * 4;  // one fp32 sum per (warp, row, activation row)
     // TR = 1: each consumer warp's two buffers of one span's block parameters of a tile
     const int pq_bytes = c.TR == 1 ? c.W * kPqBytes * (zpt ? 2 : 1) : 0;
     const int budget = di.max_smem_optin - 1024 - c.stage_off - pq_bytes;  // 1024: alignment slack
