@@ -8,6 +8,10 @@
 //   codebook: w = C[q] * absmax     (NF4/FP4; bitsandbytes #1979, "Summary":
 //                                     codes decoded inside the GEMM, decoded
 //                                     values reused across the M rows)
+//   dp4a:     nbits codes against int8 activations quantized per block
+//             (the int8-activation QMoE decode; hip-ep #1328, "Summary")
+// Zero points: none, a scalar, an fp16 tensor, or bits-wide integers packed
+// per row (staged as bytes, each block's field widened where it is used).
 //
 // Design (GB300-first; the pages' RDNA design -- dot2, DPP, LDS centroids --
 // is prior art only):
@@ -27,6 +31,11 @@
 //    codes accumulates a * q exactly as an ordinary FMA would.  The zero
 //    point and the scale are applied once per block per row:
 //        sum_k a_k (q_k - zp) s = s * (sum_k a_k q_k - zp * sum_k a_k).
+//  * int8 activations: each lane quantizes its slice per block after
+//    staging and keeps it as packed int8 words that pair with the codes as
+//    one AND of a code word yields them; the row loop is dp4a (four 8-bit
+//    products per instruction), one flush s * sx * (sum - zp * sum q8) per
+//    block.
 //  * The row loop has no data-dependent branches: lanes past the end of K
 //    read an in-bounds clamped address and are masked once per tile.
 //  * Reductions run in a fixed order: a transposed butterfly over the lanes
