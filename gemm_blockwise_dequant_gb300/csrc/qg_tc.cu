@@ -392,25 +392,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (WK == WK_CODEBOOK) {
         for (int i = threadIdx.x; i < 16 * 32; i += kThreads) lut[i] = __ldg(p.codebook + (i >> 5));
     }
+    // a device tile map: its M-tile prefix into shared memory (the codebook
+    // table's space, which the MatMulNBits grouped launch does not use), all
+    // threads' loads in flight at once, for the search below
+    int *spre = reinterpret_cast<int *>(lut);
+    if constexpr (GROUPED) {
+        static_assert(!GROUPED || WK == WK_NBITS, "grouped launches are MatMulNBits");
+        static_assert(kMaxGroups + 1 <= 16 * 32, "the prefix fits the table's space");
+        if (grp.dev)
+            for (int i = threadIdx.x; i <= grp.count; i += kThreads) spre[i] = __ldcg(grp.dev + i);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     if constexpr (GROUPED) {
         if (grp.dev) {  // the tile map the planning kernel wrote (visible after pdl_wait)
-            const int *pre = grp.dev, *roff = grp.dev + kMaxGroups + 1;
+            const int *roff = grp.dev + kMaxGroups + 1;
             const int mt = tile / p.nt;
-            if (mt >= __ldcg(pre + grp.count)) {
+            if (mt >= spre[grp.count]) {
                 nks = 0;  // no work: no copies, no MMAs, no rows written
                 m0 = m_end = wrow = 0;
             } else {
                 int lo = 0, hi = grp.count;
                 while (hi - lo > 1) {
                     const int mid = (lo + hi) >> 1;
-                    if (__ldcg(pre + mid) <= mt) lo = mid;
+                    if (spre[mid] <= mt) lo = mid;
                     else hi = mid;
                 }
-                m0 = __ldcg(roff + lo) + (mt - __ldcg(pre + lo)) * kBM;
+                m0 = __ldcg(roff + lo) + (mt - spre[lo]) * kBM;
                 m_end = __ldcg(roff + lo + 1);
                 wrow = lo * p.N;
             }
@@ -674,27 +684,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 // empty map (no tile has work) and set *status to 1.
 __global__ void ragged_plan_kernel(const int64_t *__restrict__ offs, int E, long long max_rows, int *__restrict__ map,
                                    int *__restrict__ status) {
-    __shared__ int tiles[kMaxGroups];
+    __shared__ long long so[kMaxGroups + 1];  // the offsets, loaded by all threads at once
+    __shared__ int pre[kMaxGroups + 1];       // M-tile prefix
     __shared__ int bad;
     pdl_wait();  // the offsets may come from the preceding kernel (a router)
     pdl_launch_dependents();
-    if (threadIdx.x == 0) bad = (offs[0] != 0 || offs[E] > max_rows) ? 1 : 0;
+    if (threadIdx.x == 0) bad = 0;
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) so[e] = offs[e];
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const long long c = offs[e + 1] - offs[e];
-        if (c < 0) atomicOr(&bad, 1);
-        tiles[e] = c > 0 ? static_cast<int>((c + kBM - 1) / kBM) : 0;
-    }
-    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        if (so[e + 1] < so[e]) atomicOr(&bad, 1);
     if (threadIdx.x == 0) {
-        int acc = 0;
-        for (int e = 0; e <= E; ++e) {
-            map[e] = bad ? 0 : acc;
-            map[kMaxGroups + 1 + e] = bad ? 0 : static_cast<int>(offs[e]);
-            if (e < E && !bad) acc += tiles[e];
+        if (so[0] != 0 || so[E] > max_rows) bad = 1;
+        int acc = 0;  // serial prefix over shared memory (E <= 256)
+        for (int e = 0; e < E; ++e) {
+            pre[e] = acc;
+            const long long c = so[e + 1] - so[e];
+            acc += c > 0 ? static_cast<int>((c + kBM - 1) / kBM) : 0;
         }
-        if (bad && status) *status = 1;
+        pre[E] = acc;
     }
+    __syncthreads();
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+        map[e] = bad ? 0 : pre[e];
+        map[kMaxGroups + 1 + e] = bad ? 0 : static_cast<int>(so[e]);
+    }
+    if (threadIdx.x == 0 && bad && status) *status = 1;
 }
 
 // fp32 activations for the split-precision passes: per row m, e = the exponent
