@@ -88,6 +88,34 @@ def test_mma_gemv_parity(qg, case):
     assert err <= tol_for(ad, yd), err
 
 
+# Row counts around the dealing of fills over the 152 CTAs of a GB300: whole
+# rounds of 2 x 152 fills by tile, then one leftover fill per CTA, then a
+# second (32-row tiles of 16-row fills at short K; 16-row tiles of 8-row
+# fills at K = 17920).
+FILL_CASES = [
+    # (M, N, K, a_dtype, zp_mode)
+    (1, 4864, 512, F32, "uniform"),    # one whole round, nothing left over
+    (1, 4880, 512, F32, "tensor"),     # one leftover fill: a tile holding one fill
+    (1, 5128, 512, F32, "uniform"),    # 17 leftover fills, the last one 8 rows
+    (1, 7704, 512, F32, "none"),       # more leftover fills than CTAs, the last one partial
+    (4, 4880, 1024, F32, "tensor"),    # four activation rows
+    (8, 5128, 512, F16, "uniform"),    # eight 16-bit rows
+    (1, 2440, 17920, F32, "uniform"),  # 8-row fills: one leftover
+    (1, 5120, 17920, F32, "tensor"),   # the down shape: 32 leftover fills
+]
+
+
+@pytest.mark.parametrize("case", FILL_CASES, ids=lambda c: "M%d_N%d_K%d_a%d_%s" % c)
+def test_mma_gemv_fill_dealing(qg, case):
+    """Every output row, whichever CTA, tile and fill holds it, against the oracle."""
+    M, N, K, ad, zpm = case
+    d = _case(33, M, N, K, ad, zpm)
+    Y = _run(qg, d, F32)
+    err = O.max_rel_l2(to64(Y), oracle_nbits(d))
+    assert err <= tol_for(ad, F32), err
+    assert qg.qg_test_gemv_plan(M if M <= 4 or ad != F32 else 4, N, K, ad, {"none": 0, "tensor": 1, "uniform": 2}[zpm]) is not None
+
+
 @pytest.mark.parametrize("M", [1, 2, 4])
 def test_mma_gemv_onehot_exact(qg, M):
     """A = e_k rows (fp32): each output is the dequantized weight w[n, k] bit for bit."""
