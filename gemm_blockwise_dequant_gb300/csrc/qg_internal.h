@@ -107,10 +107,9 @@ cudaError_t tc_gemm(const GemmProblem &p, void *ws, size_t ws_bytes, cudaStream_
 // min_rows rows; offsets[0..E] host values).  At most 256 experts.
 cudaError_t tc_gemm_grouped(const GemmProblem &p, const int64_t *offsets, int E, int min_rows, cudaStream_t s);
 // The grouped launch from device-resident offsets (p.M = the row capacity):
-// a planning kernel writes the tile map into map_ws (2 * 257 ints) and sets
-// *status to 1 for offsets it refuses.
-cudaError_t tc_gemm_grouped_dev(const GemmProblem &p, const int64_t *offsets_dev, int E, int *map_ws, int *status,
-                                cudaStream_t s);
+// every CTA numbers the M tiles from the offsets; *status is set to 1 for
+// offsets it refuses.
+cudaError_t tc_gemm_grouped_dev(const GemmProblem &p, const int64_t *offsets_dev, int E, int *status, cudaStream_t s);
 
 // Fused single-token QMoE decode (fc1 -> SwiGLU -> fc2 -> weighted sum).
 struct QmoeProblem {

@@ -286,10 +286,9 @@ __device__ __forceinline__ uint4 dequant8_codebook(uint32_t codes, float am, con
 // row_off[e+1]-1 and weight rows e*N .. e*N+N-1 of the stacked [E*N] weight
 // tensors; its M tiles are numbered mt_prefix[e] .. mt_prefix[e+1]-1 (an
 // expert the grouped launch leaves out has none).  Passed by value -- or,
-// when `dev` is set, read after the grid-dependency wait from that device
-// table (mt_prefix[kMaxGroups + 1] then row_off[kMaxGroups + 1]), which the
-// planning kernel wrote from device-resident offsets; M tiles at or past
-// mt_prefix[count] then have no work.
+// when `offs` is set, built by every CTA after the grid-dependency wait from
+// those device-resident row offsets (offs[count + 1] int64); M tiles at or
+// past the last prefix then have no work.
 constexpr int kMaxGroups = 256;
 template <bool G>
 struct TcGroups {
@@ -298,7 +297,9 @@ struct TcGroups {
 template <>
 struct TcGroups<true> {
     int count;
-    const int *dev;
+    const int64_t *offs;  // device offsets, or null: the tables below
+    long long max_rows;   // offs[count] may not pass it
+    int *status;          // set to 1 when the device offsets break the rules
     int mt_prefix[kMaxGroups + 1];
     int row_off[kMaxGroups + 1];
 };
@@ -392,23 +393,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (WK == WK_CODEBOOK) {
         for (int i = threadIdx.x; i < 16 * 32; i += kThreads) lut[i] = __ldg(p.codebook + (i >> 5));
     }
-    // a device tile map: its M-tile prefix into shared memory (the codebook
-    // table's space, which the MatMulNBits grouped launch does not use), all
-    // threads' loads in flight at once, for the search below
+    // device offsets: every CTA numbers the experts' M tiles itself (thread e
+    // counts expert e's tiles, a block-wide scan adds them up) into shared
+    // memory -- the codebook table's space, which the MatMulNBits grouped
+    // launch does not use -- for the search below.  Offsets that do not start
+    // at 0, decrease, or end past max_rows leave every tile without work.
     int *spre = reinterpret_cast<int *>(lut);
     if constexpr (GROUPED) {
         static_assert(!GROUPED || WK == WK_NBITS, "grouped launches are MatMulNBits");
-        static_assert(kMaxGroups + 1 <= 16 * 32, "the prefix fits the table's space");
-        if (grp.dev)
-            for (int i = threadIdx.x; i <= grp.count; i += kThreads) spre[i] = __ldcg(grp.dev + i);
+        static_assert(kMaxGroups + 1 + kThreads / 32 <= 16 * 32, "the prefix fits the table's space");
+        static_assert(kMaxGroups <= kThreads, "one thread per expert");
+        if (grp.offs) {
+            int *wsum = spre + kMaxGroups + 1;  // the warps' tile totals
+            const int e = threadIdx.x, E = grp.count;
+            int cnt = 0, bad = 0;
+            if (e < E) {
+                const long long o0 = __ldcg(grp.offs + e), o1 = __ldcg(grp.offs + e + 1);
+                bad = o1 < o0 || (e == 0 && o0 != 0) || (e == E - 1 && o1 > grp.max_rows);
+                cnt = o1 > o0 ? static_cast<int>((o1 - o0 + kBM - 1) / kBM) : 0;
+            }
+            int inc = cnt;  // inclusive scan inside the warp
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += v;
+            }
+            if (lane == 31) wsum[warp] = inc;
+            bad = __syncthreads_or(bad);
+            int base = 0;  // the earlier warps' totals
+            for (int w = 0; w < warp; ++w) base += wsum[w];
+            if (e < E) spre[e] = bad ? 0 : base + inc - cnt;
+            if (e == E - 1) spre[E] = bad ? 0 : base + inc;
+            if (bad && blockIdx.x == 0 && e == 0 && grp.status) *grp.status = 1;
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     if constexpr (GROUPED) {
-        if (grp.dev) {  // the tile map the planning kernel wrote (visible after pdl_wait)
-            const int *roff = grp.dev + kMaxGroups + 1;
+        if (grp.offs) {  // the tile prefix built above
             const int mt = tile / p.nt;
             if (mt >= spre[grp.count]) {
                 nks = 0;  // no work: no copies, no MMAs, no rows written
@@ -420,8 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (spre[mid] <= mt) lo = mid;
                     else hi = mid;
                 }
-                m0 = __ldcg(roff + lo) + (mt - spre[lo]) * kBM;
-                m_end = __ldcg(roff + lo + 1);
+                m0 = static_cast<int>(__ldcg(grp.offs + lo)) + (mt - spre[lo]) * kBM;
+                m_end = static_cast<int>(__ldcg(grp.offs + lo + 1));
                 wrow = lo * p.N;
             }
         }
@@ -675,41 +699,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
-}
-
-// The tile map of a grouped launch from device-resident expert offsets: expert
-// e owns rows offs[e] .. offs[e+1]-1 and ceil(rows / kBM) M tiles (none when
-// it has no row); map = mt_prefix[kMaxGroups + 1] then row_off[kMaxGroups + 1].
-// Offsets that do not start at 0, decrease, or end past max_rows give an
-// empty map (no tile has work) and set *status to 1.
-__global__ void ragged_plan_kernel(const int64_t *__restrict__ offs, int E, long long max_rows, int *__restrict__ map,
-                                   int *__restrict__ status) {
-    __shared__ long long so[kMaxGroups + 1];  // the offsets, loaded by all threads at once
-    __shared__ int pre[kMaxGroups + 1];       // M-tile prefix
-    __shared__ int bad;
-    pdl_wait();  // the offsets may come from the preceding kernel (a router)
-    pdl_launch_dependents();
-    if (threadIdx.x == 0) bad = 0;
-    for (int e = threadIdx.x; e <= E; e += blockDim.x) so[e] = offs[e];
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        if (so[e + 1] < so[e]) atomicOr(&bad, 1);
-    if (threadIdx.x == 0) {
-        if (so[0] != 0 || so[E] > max_rows) bad = 1;
-        int acc = 0;  // serial prefix over shared memory (E <= 256)
-        for (int e = 0; e < E; ++e) {
-            pre[e] = acc;
-            const long long c = so[e + 1] - so[e];
-            acc += c > 0 ? static_cast<int>((c + kBM - 1) / kBM) : 0;
-        }
-        pre[E] = acc;
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-        map[e] = bad ? 0 : pre[e];
-        map[kMaxGroups + 1 + e] = bad ? 0 : static_cast<int>(so[e]);
-    }
-    if (threadIdx.x == 0 && bad && status) *status = 1;
 }
 
 // fp32 activations for the split-precision passes: per row m, e = the exponent
@@ -1074,20 +1063,18 @@ cudaError_t tc_gemm_grouped(const GemmProblem &p, const int64_t *offsets, int E,
 }
 
 // The same grouped launch from device-resident offsets (no host copy of them):
-// a one-CTA planning kernel writes the tile map into `map_ws` (2 (kMaxGroups +
-// 1) ints), then the grid covers the most M tiles any offsets within max_rows
-// rows can need, ceil(max_rows / kBM) + E, and tiles past the map's end exit.
-// Every expert with rows takes the tensor cores.  p.M = max_rows.
-cudaError_t tc_gemm_grouped_dev(const GemmProblem &p, const int64_t *offsets_dev, int E, int *map_ws, int *status,
-                                cudaStream_t s) {
+// the grid covers the most M tiles any offsets within max_rows rows can need,
+// ceil(max_rows / kBM) + E; every CTA numbers the tiles from the offsets
+// itself and tiles past the real count exit.  Every expert with rows takes
+// the tensor cores.  p.M = max_rows.
+cudaError_t tc_gemm_grouped_dev(const GemmProblem &p, const int64_t *offsets_dev, int E, int *status, cudaStream_t s) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc || E > kMaxGroups || p.kind != WK_NBITS) return cudaErrorNotSupported;
-    cudaError_t e = launch_pdl(ragged_plan_kernel, dim3(1), dim3(256), 0, s, offsets_dev, E,
-                               static_cast<long long>(p.M), map_ws, status);
-    if (e != cudaSuccess) return e;
     TcGroups<true> g{};
     g.count = E;
-    g.dev = map_ws;
+    g.offs = offsets_dev;
+    g.max_rows = p.M;
+    g.status = status;
     const int tiles_m = (p.M + kBM - 1) / kBM + E;
     TcCfg c = choose_tc(std::max(kBM, p.M / E), p.N, p.K, p.bits);
     if (c.bn == 0) return cudaErrorNotSupported;
@@ -1100,7 +1087,7 @@ cudaError_t tc_gemm_grouped_dev(const GemmProblem &p, const int64_t *offsets_dev
     c.tail_splits = 1;
     c.tail_kps = c.nk;
     CUtensorMap am, cm, pm, zm;
-    e = build_maps(enc, p, c.bn, static_cast<long long>(E) * p.N, am, cm, pm, zm);
+    const cudaError_t e = build_maps(enc, p, c.bn, static_cast<long long>(E) * p.N, am, cm, pm, zm);
     if (e != cudaSuccess) return e;
     TcArgs a = make_args(p, c);
     a.w_rows = E * p.N;

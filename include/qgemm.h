@@ -376,13 +376,14 @@ size_t qmoe_ragged_mm_workspace_bytes(int x_dtype, const int64_t *expert_offsets
  *   X                   [max_rows][K] fp16 or bf16 (fp32: QG_ERR_UNSUPPORTED)
  *   W, scales, zero points, Y, N, K, bits, block_size as qmoe_ragged_mm
  *   num_experts         1 .. 256
- *   workspace           device, 16-byte aligned, at least
+ *   workspace           not used (may be NULL);
  *                       qmoe_ragged_mm_device_offsets_workspace_bytes(E)
- *                       bytes (the tile map the planning kernel writes)
+ *                       returns 0
  * Every expert with rows runs in one grouped tensor-core launch (sized for the
- * most tiles offsets within max_rows can need; tiles past the real count end
- * at once), after a one-CTA planning kernel.  Returns QG_OK, QG_ERR_* for
- * refused arguments (before any launch) or QG_ERR_CUDA.
+ * most tiles offsets within max_rows can need; each CTA numbers the experts'
+ * tiles from the offsets itself, and tiles past the real count end at once).
+ * Returns QG_OK, QG_ERR_* for refused arguments (before any launch) or
+ * QG_ERR_CUDA.
  */
 int qmoe_ragged_mm_device_offsets(const void *X, int x_dtype, const int64_t *expert_offsets_dev, int num_experts,
                                   int max_rows, const uint8_t *W, const uint16_t *scales_f16,
