@@ -804,11 +804,24 @@ cudaError_t launch_mg(const MgArgs &a, const MgCfg &c, cudaStream_t s) {
 // 16-bit requests with more rows belong to the tcgen05 path.
 int mma_rows(int a_dtype) { return a_dtype == 0 ? 4 : 8; }
 
+// Activation rows per launch: mma_rows, or -- 16-bit activations, 3 or 4 rows
+// whose B fragments leave no room for the ring (long K) -- two launches of
+// two rows each, which read the weights twice and still beat the SIMT kernel
+// there.
+static int launch_rows(const GemmProblem &p) {
+    const bool zpt = p.zp_mode == ZP_TENSOR;
+    MgCfg c;
+    if (p.a_dtype != 0 && p.M > 2 && p.M <= 4 && !choose_mg(p.M, p.N, p.K, p.a_dtype, zpt, c) &&
+        choose_mg(2, p.N, p.K, p.a_dtype, zpt, c))
+        return 2;
+    return mma_rows(p.a_dtype);
+}
+
 bool mma_gemv_eligible(const GemmProblem &p) {
     if (p.kind != WK_NBITS || p.bits != 2 || p.bs != 64 || p.K % kSpanCodes != 0 || p.zp_mode == ZP_PACKED)
         return false;
-    const int g = mma_rows(p.a_dtype);
-    if (p.M < 1 || (p.M > g && p.a_dtype != 0)) return false;
+    if (p.M < 1 || (p.M > mma_rows(p.a_dtype) && p.a_dtype != 0)) return false;
+    const int g = launch_rows(p);
     MgCfg c;
     const bool zpt = p.zp_mode == ZP_TENSOR;
     if (!choose_mg(std::min(p.M, g), p.N, p.K, p.a_dtype, zpt, c)) return false;
@@ -820,8 +833,14 @@ bool mma_gemv_eligible(const GemmProblem &p) {
 }
 
 bool mma_gemv_plan(int M, int N, int K, int a_dtype, int zp_mode, int out[4]) {
-    const int g = mma_rows(a_dtype);
-    if (K % kSpanCodes != 0 || M < 1 || (M > g && a_dtype != 0)) return false;
+    if (K % kSpanCodes != 0 || M < 1 || (M > mma_rows(a_dtype) && a_dtype != 0)) return false;
+    GemmProblem p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.a_dtype = a_dtype;
+    p.zp_mode = zp_mode == 1 ? ZP_TENSOR : (zp_mode == 2 ? ZP_UNIFORM : ZP_NONE);
+    const int g = launch_rows(p);
     MgCfg c;
     if (!choose_mg(std::min(M, g), N, K, a_dtype, zp_mode == ZP_TENSOR, c)) return false;
     out[0] = 16 * c.TR;
@@ -893,7 +912,7 @@ cudaError_t mma_gemv_rows(const GemmProblem &p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t mma_gemv(const GemmProblem &p, cudaStream_t s) {
-    const int g = mma_rows(p.a_dtype);
+    const int g = launch_rows(p);
     if (p.M <= g) return mma_gemv_rows(p, s);
     const size_t asz = p.a_dtype == 0 ? 4 : 2, ysz = p.y_dtype == 0 ? 4 : 2;
     for (int m0 = 0; m0 < p.M; m0 += g) {

@@ -76,6 +76,8 @@ CASES = [
     (2, 150, 8704, F32, "tensor", F32),     # 16-row tiles with two activation rows
     (4, 70, 8704, F16, "uniform", F32),
     (8, 200, 5120, BF16, "none", F32),      # eight B columns per block: B fragments in the ring's stages
+    (4, 130, 17920, F16, "uniform", F16),   # long K: two launches of two activation rows
+    (3, 97, 17920, BF16, "none", F32),      # the same, the second launch with one row
 ]
 
 
@@ -170,6 +172,12 @@ def test_mma_gemv_plans_reach_both_tile_shapes(qg):
     assert qg.qg_test_gemv_plan(2, 150, 8704, F32, 1)["rows_per_tile"] == 16
     assert qg.qg_test_gemv_plan(2, 96, 17920, F32, 2) is None
     assert qg.qg_test_gemv_plan(1, 100, 1536 + 64, F32, 2) is None
+    # 16-bit activations, 3-4 rows at K = 17920: four B columns per block leave
+    # no room for the ring, two launches of two rows take 16-row tiles; with a
+    # zero-point tensor (its staging buffers) two rows miss the fourth stage too
+    assert qg.qg_test_gemv_plan(4, 5120, 17920, F16, 2)["rows_per_tile"] == 16
+    assert qg.qg_test_gemv_plan(3, 5120, 17920, BF16, 0)["rows_per_tile"] == 16
+    assert qg.qg_test_gemv_plan(4, 5120, 17920, F16, 1) is None
 
 
 @pytest.mark.parametrize("case", [
