@@ -804,16 +804,17 @@ cudaError_t launch_mg(const MgArgs &a, const MgCfg &c, cudaStream_t s) {
 // 16-bit requests with more rows belong to the tcgen05 path.
 int mma_rows(int a_dtype) { return a_dtype == 0 ? 4 : 8; }
 
-// Activation rows per launch: mma_rows, or -- 16-bit activations, 3 or 4 rows
-// whose B fragments leave no room for the ring (long K) -- two launches of
-// two rows each, which read the weights twice and still beat the SIMT kernel
-// there.
+// Activation rows per launch: mma_rows, or, where the B fragments of that
+// many rows leave no room for the ring (long K), two launches of half as many
+// rows -- 16-bit activations with 3 or 4 rows, fp32 ones with 2 -- which read
+// the weights twice and still beat the SIMT kernel there.
 static int launch_rows(const GemmProblem &p) {
     const bool zpt = p.zp_mode == ZP_TENSOR;
+    const int half = p.a_dtype == 0 ? 1 : 2;
     MgCfg c;
-    if (p.a_dtype != 0 && p.M > 2 && p.M <= 4 && !choose_mg(p.M, p.N, p.K, p.a_dtype, zpt, c) &&
-        choose_mg(2, p.N, p.K, p.a_dtype, zpt, c))
-        return 2;
+    if (p.M > half && p.M <= 2 * half && !choose_mg(p.M, p.N, p.K, p.a_dtype, zpt, c) &&
+        choose_mg(half, p.N, p.K, p.a_dtype, zpt, c))
+        return half;
     return mma_rows(p.a_dtype);
 }
 

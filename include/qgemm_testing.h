@@ -28,10 +28,10 @@
  *
  *   a_dtype, zp_mode  as in qgemm_nbits (0 fp32, 1 fp16, 2 bf16; 0 none,
  *                     1 tensor, 2 uniform)
- *   (fp32 activations with M > 4 run as one launch per group of four rows,
- *   and 3 or 4 rows of 16-bit activations whose B fragments leave no room
- *   for the ring as two launches of two rows; the plan is that of a full
- *   group)
+ *   (fp32 activations with M > 4 run as one launch per group of four rows;
+ *   where the B fragments of all rows leave no room for the ring, 3 or 4 rows
+ *   of 16-bit activations run as two launches of two rows and 2 rows of fp32
+ *   activations as two launches of one; the plan is that of a full group)
  *   out               host int[4]: weight rows per tile (32: block parameters
  *                     staged with the codes; 16: long K, block parameters
  *                     copied per span by the consumer warps), consumer warps,

@@ -168,9 +168,10 @@ def test_mma_gemv_plans_reach_both_tile_shapes(qg):
     assert {p["rows_per_tile"] for p in plans if p is not None} == {16, 32}
     # M = 2 with fp32 activations: at K = 8704 (17 spans x 4 B columns, two spans
     # for some warps) only 16-row tiles fit beside the B fragments; at K = 17920
-    # nothing does, and the SIMT GEMV serves it
+    # nothing does, and two one-row launches serve it
     assert qg.qg_test_gemv_plan(2, 150, 8704, F32, 1)["rows_per_tile"] == 16
-    assert qg.qg_test_gemv_plan(2, 96, 17920, F32, 2) is None
+    assert qg.qg_test_gemv_plan(2, 96, 17920, F32, 2)["rows_per_tile"] == 16
+    assert qg.qg_test_gemv_plan(3, 96, 17920, F32, 2) is None
     assert qg.qg_test_gemv_plan(1, 100, 1536 + 64, F32, 2) is None
     # 16-bit activations, 3-4 rows at K = 17920: four B columns per block leave
     # no room for the ring, two launches of two rows take 16-row tiles; with a
