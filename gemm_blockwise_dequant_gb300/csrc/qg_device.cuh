@@ -90,6 +90,25 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                  : "memory");
 }
 
+// The same copy with an L2 eviction policy (from l2_evict_first()).
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// An L2 policy for data read once (a weight stream larger than L2): its lines
+// are evicted first, so the stream leaves the kernels' code and the small
+// operands that every launch reads resident in L2.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    return policy;
+}
+
 // Copy `bytes` (even) from global to shared memory with the calling warp.
 // The 16-byte-aligned bulk part goes through the TMA engine (lane 0 issues
 // it; its byte count is returned so the caller can add it to the barrier's

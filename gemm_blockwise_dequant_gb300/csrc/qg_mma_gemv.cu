@@ -337,6 +337,9 @@ __global__ void __maxnreg__(kMaxRegs)
         bool alive = true;
         int slot = 0;
         uint32_t par = 1;  // parity of the empty phase to wait for before refilling `slot`
+        // the weights are read once: evicted from L2 first, they do not push
+        // out the code and operands of the launches that follow
+        const uint64_t wpol = l2_evict_first();
         for (int f = 0; f < total; ++f) {
             // the first fill into the stages that hold the activations waits
             // until every consumer thread has read them
@@ -367,10 +370,12 @@ __global__ void __maxnreg__(kMaxRegs)
                 const uint32_t cb = valid * p.row_bytes, pb = PSMEM ? valid * p.nb * 2 : 0;
                 mbar_arrive_expect_tx(&full[slot], cb + pb * (ZPT ? 2 : 1));
                 if (valid) {
-                    bulk_g2s(st, p.W + static_cast<size_t>(row0) * p.row_bytes, cb, &full[slot]);
+                    bulk_g2s_hint(st, p.W + static_cast<size_t>(row0) * p.row_bytes, cb, &full[slot], wpol);
                     if (PSMEM) {
-                        bulk_g2s(st + p.par_off, p.scales + static_cast<size_t>(row0) * p.nb, pb, &full[slot]);
-                        if (ZPT) bulk_g2s(st + p.zp_off, p.zp + static_cast<size_t>(row0) * p.nb, pb, &full[slot]);
+                        bulk_g2s_hint(st + p.par_off, p.scales + static_cast<size_t>(row0) * p.nb, pb, &full[slot],
+                                      wpol);
+                        if (ZPT)
+                            bulk_g2s_hint(st + p.zp_off, p.zp + static_cast<size_t>(row0) * p.nb, pb, &full[slot], wpol);
                     }
                 }
             }
