@@ -740,6 +740,9 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
         int it = 0, slot = 0;
         uint32_t par = 1;  // parity of the empty phase that must complete before filling (it / NST)
         bool alive = true;
+        // the weights are read once: evicted from L2 first, they do not push
+        // out the code and operands of the launches that follow
+        const uint64_t wpol = l2_evict_first();
         const int e = p.ids ? __ldg(p.ids + cta_slot) : 0;
         const bool valid = e >= 0 && e < p.num_experts;
         const int sl = cta_slot;
@@ -772,10 +775,12 @@ __global__ void __launch_bounds__((max_consumer_warps(MT) + 1) * 32, 1) gemv_ker
             if (p.fast_tx && rows == p.SR && !split) {  // warp-uniform: a whole stage, every copy 16-byte aligned
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&full[slot], p.fast_tx);
-                    bulk_g2s(st, Wb + static_cast<size_t>(r0) * p.row_bytes, p.SR * p.row_bytes, &full[slot]);
-                    bulk_g2s(st + p.s_off, Pb + static_cast<size_t>(r0) * prow, p.SR * prow, &full[slot]);
+                    bulk_g2s_hint(st, Wb + static_cast<size_t>(r0) * p.row_bytes, p.SR * p.row_bytes, &full[slot],
+                                  wpol);
+                    bulk_g2s_hint(st + p.s_off, Pb + static_cast<size_t>(r0) * prow, p.SR * prow, &full[slot], wpol);
                     if (p.zrow)
-                        bulk_g2s(st + p.z_off, Zb + static_cast<size_t>(r0) * p.zrow, p.SR * p.zrow, &full[slot]);
+                        bulk_g2s_hint(st + p.z_off, Zb + static_cast<size_t>(r0) * p.zrow, p.SR * p.zrow, &full[slot],
+                                      wpol);
                 }
             } else {
                 fill_stage_general<LPR, VEC, BITS>(p, st, Wb, Pb, Zb, r0, rows, split, kb0, kb1, prow, &full[slot], lane);
