@@ -53,6 +53,22 @@ def test_ragged_refuses_bad_offsets_widths_and_alignment(L):
     assert L.qmoe_ragged_mm_workspace_bytes(1, p, 1, 64, 64, 4, 32) == 0
 
 
+def test_ragged_device_offsets_needs_no_workspace(L):
+    """The device-offset launch numbers its tiles inside the kernel: no
+    workspace at any expert count, and a NULL workspace passes the host
+    checks (refusals here come from the other arguments)."""
+    for E in (1, 2, 128, 256, 257):
+        assert L.qmoe_ragged_mm_device_offsets_workspace_bytes(E) == 0
+    call = lambda E=4, x=1, bits=4, bs=32, K=64, off=P16: L.qmoe_ragged_mm_device_offsets(
+        P16, x, off, E, 64, P16, P16, None, P16, 1, 64, K, bits, bs, None, 0, None, None)
+    assert call(x=0) == qg.QG_ERR_UNSUPPORTED     # fp32 activations: not on the grouped launch
+    assert call(E=257) == qg.QG_ERR_UNSUPPORTED
+    assert call(bits=3) == qg.QG_ERR_UNSUPPORTED
+    assert call(K=80) == qg.QG_ERR_INVALID_ARG    # K % block_size
+    assert call(off=ctypes.c_void_p(4100)) == qg.QG_ERR_INVALID_ARG  # offsets not 8-byte aligned
+    assert call(off=None) == qg.QG_ERR_INVALID_ARG
+
+
 def test_gather_refusals(L):
     call = lambda n=4, fmt=qg.QG_WF_U4, zp=None, V=100, D=64, bs=32, y=1: L.qg_gather_block_quantized(
         P16, n, P16, fmt, P16, zp, V, D, bs, P16, y, None, None)
