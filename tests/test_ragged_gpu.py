@@ -191,7 +191,7 @@ def test_ragged_device_offsets_match_oracle(qg, bits, bs, x_dtype, y_dtype, zp):
 
 
 def test_ragged_device_offsets_refusals(qg):
-    """Offsets the planning kernel refuses (not starting at 0, decreasing, past max_rows) compute nothing
+    """Offsets the grouped launch refuses (not starting at 0, decreasing, past max_rows) compute nothing
     and set the status word; host-side refusals come before any launch."""
     t = torch()
     d = WL.ragged(num_experts=4, N=96, K=256, bits=4, block_size=32, counts=[5, 20, 0, 7], seed=4)
